@@ -1,0 +1,131 @@
+"""Float64 CPU oracle of the Mamba-3 SSM layer recurrence.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package.  It shares no code with
+the CUDA library (``state_space_sequence_04_b300``) and never imports it.
+
+Two parts:
+
+* ``m3_oracle.c`` (built to ``liboracle.so`` with gcc, float64, OpenMP over
+  independent (batch, head) sequences): the sequential recurrence in the
+  physical frame, one token at a time.  ``scan`` below wraps it; a decode step
+  is ``scan`` with T = 1 and a carried state.
+* ``forms.py`` (numpy, float64): the other evaluations of the same recurrence
+  that the tests use to pin the sequential oracle (Mamba-2 reduction, decay x
+  two-band mask matrix form, complex-diagonal state, rotating-frame form,
+  chunked evaluation with state passing), and the state-passing recurrence.
+
+Layouts are those of ``synth.py``: x [Bt,T,H,R,P], B/C [Bt,T,H,R,N],
+dt/lam [Bt,T,H], A [H], omega [Bt,T,H,N/2], y [Bt,T,H,R,P], states [Bt,H,N,P],
+delayed-write cache [Bt,H,R*N+R*P].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "m3_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``m3_oracle.c`` to ``liboracle.so`` (gcc -O2 -fopenmp, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-Wall",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        dp = ctypes.POINTER(ctypes.c_double)
+        i64 = ctypes.c_int64
+        lib.m3o_scan.argtypes = [dp] * 7 + [i64] * 6 + [dp] * 5
+        lib.m3o_scan.restype = ctypes.c_int
+        lib.m3o_num_threads.argtypes = []
+        lib.m3o_num_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle runs with."""
+    return int(_load().m3o_num_threads())
+
+
+def f64(a) -> np.ndarray:
+    """Contiguous float64 numpy copy of a numpy array or (CPU or CUDA) torch tensor."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def scan(x, B, C, dt, A, lam, omega, h0=None, prev=None):
+    """Sequential recurrence (float64) over all tokens.
+
+    Returns (y [Bt,T,H,R,P], hT [Bt,H,N,P], prevT [Bt,H,R*(N+P)]).
+    ``h0`` / ``prev`` are the carried state and delayed-write factors (zero if None).
+    """
+    x, B, C, dt, A, lam, omega = (f64(v) for v in (x, B, C, dt, A, lam, omega))
+    Bt, T, H, R, P = x.shape
+    N = B.shape[-1]
+    if B.shape != (Bt, T, H, R, N) or C.shape != B.shape:
+        raise ValueError("B, C must be [Bt,T,H,R,N]")
+    if dt.shape != (Bt, T, H) or lam.shape != (Bt, T, H) or A.shape != (H,):
+        raise ValueError("dt, lam must be [Bt,T,H]; A must be [H]")
+    if omega.shape != (Bt, T, H, N // 2):
+        raise ValueError("omega must be [Bt,T,H,N/2]")
+    h0 = None if h0 is None else f64(h0).reshape(Bt, H, N, P)
+    prev = None if prev is None else f64(prev).reshape(Bt, H, R * (N + P))
+    y = np.zeros((Bt, T, H, R, P))
+    hT = np.zeros((Bt, H, N, P))
+    prevT = np.zeros((Bt, H, R * (N + P)))
+    st = _load().m3o_scan(_ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A), _ptr(lam), _ptr(omega),
+                          Bt, T, H, P, N, R, _ptr(h0), _ptr(prev), _ptr(y), _ptr(hT), _ptr(prevT))
+    if st != 0:
+        raise ValueError(f"oracle rejected its inputs (code {st}): shapes, or a precondition "
+                         "Delta >= 0, A <= 0, lambda in [0, 1], finite values")
+    return y, hT, prevT
+
+
+def decode_step(state, x_t, B_t, prev, C_t, dt_t, A, lam_t, omega_t):
+    """One decode token: the sequential step from a carried state.
+
+    state [b,H,N,P]; x_t [b,H,R,P]; B_t, C_t [b,H,R,N]; prev [b,H,R*(N+P)];
+    dt_t, lam_t [b,H]; A [H]; omega_t [b,H,N/2].
+    Returns (y_t [b,H,R,P], new state, new prev).
+    """
+    xt = f64(x_t)[:, None]
+    y, hT, prevT = scan(xt, f64(B_t)[:, None], f64(C_t)[:, None], f64(dt_t)[:, None], A,
+                        f64(lam_t)[:, None], f64(omega_t)[:, None], h0=state, prev=prev)
+    return y[:, 0], hT, prevT
+
+
+def rel_err(got, ref) -> float:
+    """max |got - ref| / max |ref| (the parity metric)."""
+    got = f64(got)
+    ref = f64(ref)
+    den = float(np.max(np.abs(ref))) if ref.size else 0.0
+    num = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    if den == 0.0:
+        return num
+    return num / den
+
+
+from . import forms  # noqa: E402,F401
