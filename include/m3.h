@@ -1,0 +1,171 @@
+/*
+ * m3 -- Mamba-3 SSM layer recurrence on NVIDIA B300 (sm_103a).
+ *
+ * C ABI of libm3.so.  All tensor arguments are DEVICE pointers owned by the
+ * caller; the library never allocates or frees device memory and never
+ * synchronises.  Every call is validated on the host first; on any violation
+ * it returns an error code and launches nothing.  Work is enqueued on the
+ * given stream (a cudaStream_t passed as void*; NULL = the legacy default
+ * stream); a launch failure is returned as M3_ERR_CUDA, execution errors show
+ * up at the caller's next synchronisation.
+ *
+ * What is computed follows "Mamba-3: Improved Sequence Modeling using State
+ * Space Principles" (abhik.ai/papers/mamba3; thelatestinai.com/papers/2603.15569):
+ *
+ *   alpha_t = exp(dt_t A_h), beta_t = (1 - lambda_t) dt_t alpha_t, gamma_t = lambda_t dt_t
+ *                                       (Proposition 1, Eq. 6; Table 1)
+ *   h_t = R(phi_t) (alpha_t h_{t-1} + beta_t B_{t-1} X_{t-1}^T) + gamma_t B_t X_t^T
+ *   Y_t = h_t^T C_t                     (section 3.3, Eqs. 12-14: MIMO rank R)
+ *
+ * where h_t is the N x P state of one (batch, head), phi_{t,j} = dt_t omega_{t,j}
+ * rotates state pair j = rows (2j, 2j+1) counter-clockwise (Propositions 2-4,
+ * Eq. 11: the complex state realised as data-dependent rotary), and
+ * R(theta)(a, b) = (a cos theta - b sin theta, a sin theta + b cos theta).
+ * lambda_t = 1 is Mamba-2's exponential-Euler update.
+ *
+ * Layouts (row-major, contiguous, time-major):
+ *   x, y          [batch, T, H, R, P]   io dtype
+ *   B, C          [batch, T, H, R, N]   io dtype
+ *   dt, lambda    [batch, T, H]         fp32  (dt >= 0, lambda in [0,1])
+ *   A             [H]                   fp32  (A <= 0)
+ *   omega         [batch, T, H, N/2]    fp32
+ *   state         [batch, H, N, P]      fp32, physical (unrotated) frame
+ * The preconditions dt >= 0, A <= 0, 0 <= lambda <= 1 are documented, not
+ * checked per element.
+ *
+ * io dtype: M3_DTYPE_BF16 (inputs bf16, fp32 accumulation, bf16 y) or
+ * M3_DTYPE_F32 (fp32 everywhere).  Every pointer must be 16-byte aligned.
+ */
+#ifndef M3_H
+#define M3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define M3_API __attribute__((visibility("default")))
+#else
+#define M3_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    M3_OK = 0,
+    M3_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, bad size or dtype */
+    M3_ERR_UNSUPPORTED = -2,   /* valid arguments outside what the kernels implement */
+    M3_ERR_WORKSPACE = -3,     /* workspace missing or smaller than *_workspace_size */
+    M3_ERR_CUDA = -4,          /* a CUDA call or kernel launch failed */
+    M3_ERR_TIMEOUT = -5        /* a bounded device-side wait gave up */
+} m3_status;
+
+typedef enum { M3_DTYPE_BF16 = 0, M3_DTYPE_F32 = 1 } m3_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+M3_API const char* m3_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+M3_API int m3_version(void);
+
+/*
+ * Bytes of device workspace m3_scan_fwd needs for these sizes (0 if none).
+ * Returns 0 too for sizes m3_scan_fwd would reject; call it to size the
+ * buffer, then pass the buffer and this size.
+ */
+M3_API size_t m3_scan_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                                  int64_t dstate, int R, int chunk, int io_dtype);
+
+/*
+ * How m3_scan_fwd would run for these sizes, without running it.
+ *   path      out: 0 = CUDA-core kernels (fp32 arithmetic; the fp32 io mode
+ *             and the fallback), 1 = tensor-core kernels (bf16 MMA with
+ *             fp32 accumulation)
+ *   launches  out: number of kernel launches one m3_scan_fwd call makes
+ * Returns M3_OK, or the error m3_scan_fwd would return for these sizes.
+ */
+M3_API int m3_scan_fwd_plan(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+                            int R, int chunk, int io_dtype, int* path, int* launches);
+
+/*
+ * Chunked parallel prefill over T = seqlen tokens from a zero state
+ * (h_{-1} = 0 and no delayed write before the first token, as in the
+ * page's scalar scan helper, panel 1).
+ *
+ *   x, B, C, dt, A, lambda, omega : inputs, layouts above
+ *   R        MIMO rank, one of 1, 2, 4, 8
+ *   chunk    tokens per chunk Q of the chunked algorithm (section 3.3):
+ *            intra-chunk masked scores (decay x two-band mask, Eq. 7)
+ *            plus inter-chunk state passing; 16 <= chunk <= 256 and a
+ *            multiple of 16.  The result does not depend on it beyond rounding.
+ *   y        out [batch, T, H, R, P], io dtype
+ *   final_state  out (nullable) [batch, H, N, P] fp32: h_{T-1}, the state a
+ *            decode step continues from (its delayed-write cache is
+ *            B_{T-1}, X_{T-1}, taken by the caller from B and x).
+ *   Sizes: batch >= 0, seqlen >= 0 (0 writes nothing except a zero
+ *   final_state), nheads >= 1, dstate N even with 2 <= N <= 256,
+ *   headdim P a multiple of 4 with 4 <= P <= 256.
+ *   workspace / workspace_bytes: device scratch of at least
+ *   m3_scan_fwd_workspace_size(...) bytes, 256-byte aligned; contents on
+ *   entry are ignored.
+ * Returns M3_OK or an error code; launches nothing on error.
+ */
+M3_API int m3_scan_fwd(const void* x, const void* B, const void* C, const float* dt, const float* A,
+                const float* lambda, const float* omega, int R, int chunk,
+                void* y, float* final_state,
+                int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+                int io_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One decode token for every (batch, head): the recurrence above with T = 1
+ * from a carried state (the single-token mode of section 3.3 / Table 6).
+ *
+ *   state          in/out [batch, H, N, P] fp32, physical frame
+ *   x_t            [batch, H, R, P] io dtype
+ *   B_t, C_t       [batch, H, R, N] io dtype
+ *   B_prev_x_prev  in/out [batch, H, R*N + R*P] io dtype: the factors of the
+ *                  previous token's write, B_{t-1} as [R, N] then X_{t-1} as
+ *                  [R, P], unrotated; overwritten with B_t, X_t.  Zero for a
+ *                  sequence's first token; after m3_scan_fwd, B[:, T-1] and
+ *                  x[:, T-1].
+ *   dt_t, lambda_t [batch, H] fp32;  A [H] fp32;  omega_t [batch, H, N/2] fp32
+ *   y_t            out [batch, H, R, P] io dtype
+ *   Sizes as for m3_scan_fwd; batch may be 0 (nothing is launched).
+ * state and B_prev_x_prev must not overlap any other argument.
+ */
+M3_API int m3_decode_step(float* state, const void* x_t, const void* B_t, void* B_prev_x_prev,
+                   const void* C_t, const float* dt_t, const float* A, const float* lambda_t,
+                   const float* omega_t, void* y_t,
+                   int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R,
+                   int io_dtype, void* stream);
+
+/*
+ * Inter-chunk state passing of the chunked algorithm, in place:
+ *
+ *   H_c = exp(l_c) R(Theta_c) H_{c-1} + U_c,   c = 0 .. nchunks-1,
+ *
+ * with H_{-1} = init_state (zero if NULL) and R(Theta_c) rotating state rows
+ * (2j, 2j+1) by Theta_c[j].  l_c is a chunk's summed log-decay
+ * (sum of dt_t A) and Theta_c its summed rotation angle per pair.
+ *
+ *   chunk_states    in/out [batch, H, nchunks, N, P] fp32: in = U_c (a
+ *                   chunk's own contribution), out = H_{c-1} (the state
+ *                   entering chunk c)
+ *   chunk_logdecay  [batch, H, nchunks] fp32
+ *   chunk_angle     [batch, H, nchunks, N/2] fp32
+ *   init_state      nullable [batch, H, N, P] fp32
+ *   final_state     nullable out [batch, H, N, P] fp32: H_{nchunks-1}
+ *   Sizes: N even, 2 <= N <= 256; P a multiple of 4, 4 <= P <= 256;
+ *   nchunks >= 0 (0 copies init_state, or zeros, to final_state).
+ */
+M3_API int m3_state_passing(float* chunk_states, const float* chunk_logdecay, const float* chunk_angle,
+                     const float* init_state, float* final_state,
+                     int64_t batch, int64_t nheads, int64_t nchunks, int64_t dstate, int64_t headdim,
+                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M3_H */

@@ -1,0 +1,209 @@
+"""Thin ctypes binding of libm3.so (the C ABI declared in include/m3.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  Tensors are torch CUDA tensors (torch provides the
+device memory and the stream); the functions named ``m3_*`` mirror the C entry
+points one to one.  ``scan_fwd`` / ``decode_step`` / ``state_passing`` are
+conveniences that allocate outputs and workspace with torch and then call the
+same entry points.
+
+There is no fallback: if libm3.so is missing or cannot be loaded, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libm3.so")
+
+M3_OK = 0
+M3_ERR_INVALID_ARG = -1
+M3_ERR_UNSUPPORTED = -2
+M3_ERR_WORKSPACE = -3
+M3_ERR_CUDA = -4
+M3_ERR_TIMEOUT = -5
+M3_DTYPE_BF16 = 0
+M3_DTYPE_F32 = 1
+
+# Every symbol include/m3.h declares, with its ctypes signature.
+_vp, _fp = ctypes.c_void_p, ctypes.c_void_p
+_i64, _int, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "m3_status_string": ([_int], ctypes.c_char_p),
+    "m3_version": ([], _int),
+    "m3_scan_fwd_workspace_size": ([_i64, _i64, _i64, _i64, _i64, _int, _int, _int], _sz),
+    "m3_scan_fwd_plan": ([_i64, _i64, _i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(_int),
+                          ctypes.POINTER(_int)], _int),
+    "m3_scan_fwd": ([_vp, _vp, _vp, _fp, _fp, _fp, _fp, _int, _int, _vp, _fp,
+                     _i64, _i64, _i64, _i64, _i64, _int, _vp, _sz, _vp], _int),
+    "m3_decode_step": ([_fp, _vp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp,
+                        _i64, _i64, _i64, _i64, _int, _int, _vp], _int),
+    "m3_state_passing": ([_fp, _fp, _fp, _fp, _fp, _i64, _i64, _i64, _i64, _i64, _vp], _int),
+}
+
+_lib = None
+
+
+class M3Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {m3_status_string(status)} ({status})")
+
+
+def load():
+    """Load libm3.so (raises if it is missing: there is no CPU fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libm3.so not built at {LIB_PATH}; run state_space_sequence_04_b300/build.py")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (argt, rest) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = argt
+            fn.restype = rest
+        _lib = lib
+    return _lib
+
+
+def m3_status_string(status: int) -> str:
+    return load().m3_status_string(int(status)).decode()
+
+
+def m3_version() -> int:
+    return int(load().m3_version())
+
+
+def io_code(dtype: torch.dtype) -> int:
+    if dtype == torch.bfloat16:
+        return M3_DTYPE_BF16
+    if dtype == torch.float32:
+        return M3_DTYPE_F32
+    raise TypeError(f"io dtype must be bfloat16 or float32, got {dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libm3 takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libm3 takes contiguous tensors")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(st: int, where: str):
+    if st != M3_OK:
+        raise M3Error(st, where)
+
+
+# ---------------------------------------------------------------------------
+# One-to-one wrappers of the C entry points.
+def m3_scan_fwd_workspace_size(batch, seqlen, nheads, headdim, dstate, R, chunk, io) -> int:
+    return int(load().m3_scan_fwd_workspace_size(batch, seqlen, nheads, headdim, dstate, R, chunk, io))
+
+
+def m3_scan_fwd_plan(batch, seqlen, nheads, headdim, dstate, R, chunk, io):
+    """(path, launches) of m3_scan_fwd for these sizes: path 0 = CUDA cores, 1 = tensor cores."""
+    path, launches = _int(0), _int(0)
+    _check(int(load().m3_scan_fwd_plan(batch, seqlen, nheads, headdim, dstate, R, chunk, io,
+                                       ctypes.byref(path), ctypes.byref(launches))), "m3_scan_fwd_plan")
+    return path.value, launches.value
+
+
+def m3_scan_fwd(x, B, C, dt, A, lam, omega, R: int, chunk: int, y, final_state, workspace,
+                stream=None) -> int:
+    """Call m3_scan_fwd; returns the status code (does not raise)."""
+    Bt, T, H, R_, P = x.shape
+    N = B.shape[-1]
+    io = io_code(x.dtype)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return int(load().m3_scan_fwd(
+        _ptr(x, x.dtype), _ptr(B, x.dtype), _ptr(C, x.dtype), _ptr(dt, torch.float32),
+        _ptr(A, torch.float32), _ptr(lam, torch.float32), _ptr(omega, torch.float32), int(R), int(chunk),
+        _ptr(y, x.dtype), _ptr(final_state, torch.float32), Bt, T, H, P, N, io, _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def m3_decode_step(state, x_t, B_t, cache, C_t, dt_t, A, lam_t, omega_t, y_t, R: int, stream=None) -> int:
+    """Call m3_decode_step; returns the status code (does not raise)."""
+    b, H, R_, P = x_t.shape
+    N = B_t.shape[-1]
+    io = io_code(x_t.dtype)
+    return int(load().m3_decode_step(
+        _ptr(state, torch.float32), _ptr(x_t, x_t.dtype), _ptr(B_t, x_t.dtype), _ptr(cache, x_t.dtype),
+        _ptr(C_t, x_t.dtype), _ptr(dt_t, torch.float32), _ptr(A, torch.float32), _ptr(lam_t, torch.float32),
+        _ptr(omega_t, torch.float32), _ptr(y_t, x_t.dtype), b, H, P, N, int(R), io, _stream(stream)))
+
+
+def m3_state_passing(chunk_states, chunk_logdecay, chunk_angle, init_state, final_state, stream=None) -> int:
+    """Call m3_state_passing; returns the status code (does not raise)."""
+    b, H, nc, N, P = chunk_states.shape
+    return int(load().m3_state_passing(
+        _ptr(chunk_states, torch.float32), _ptr(chunk_logdecay, torch.float32), _ptr(chunk_angle, torch.float32),
+        _ptr(init_state, torch.float32), _ptr(final_state, torch.float32), b, H, nc, N, P, _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# Conveniences: allocate with torch, call the entry point, raise on error.
+def alloc_workspace(x_shape, N: int, R: int, chunk: int, dtype: torch.dtype, device) -> Optional[torch.Tensor]:
+    Bt, T, H, _, P = x_shape
+    nbytes = m3_scan_fwd_workspace_size(Bt, T, H, P, N, R, chunk, io_code(dtype))
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def scan_fwd(x, B, C, dt, A, lam, omega, R: int, chunk: int, want_final: bool = True, workspace=None,
+             stream=None):
+    """Prefill; returns (y, final_state or None)."""
+    Bt, T, H, _, P = x.shape
+    N = B.shape[-1]
+    y = torch.empty_like(x)
+    fin = torch.empty((Bt, H, N, P), dtype=torch.float32, device=x.device) if want_final else None
+    if workspace is None:
+        workspace = alloc_workspace(x.shape, N, R, chunk, x.dtype, x.device)
+    _check(m3_scan_fwd(x, B, C, dt, A, lam, omega, R, chunk, y, fin, workspace, stream), "m3_scan_fwd")
+    return y, fin
+
+
+def decode_step(state, x_t, B_t, cache, C_t, dt_t, A, lam_t, omega_t, R: int, y_t=None, stream=None):
+    """One decode token in place on ``state`` and ``cache``; returns y_t."""
+    if y_t is None:
+        y_t = torch.empty_like(x_t)
+    _check(m3_decode_step(state, x_t, B_t, cache, C_t, dt_t, A, lam_t, omega_t, y_t, R, stream), "m3_decode_step")
+    return y_t
+
+
+def state_passing(chunk_states, chunk_logdecay, chunk_angle, init_state=None, want_final: bool = True,
+                  stream=None):
+    """In-place state passing; returns final_state (or None)."""
+    b, H, nc, N, P = chunk_states.shape
+    fin = torch.empty((b, H, N, P), dtype=torch.float32, device=chunk_states.device) if want_final else None
+    _check(m3_state_passing(chunk_states, chunk_logdecay, chunk_angle, init_state, fin, stream), "m3_state_passing")
+    return fin
+
+
+def new_decode_cache(batch: int, heads: int, dstate: int, headdim: int, R: int, dtype, device) -> torch.Tensor:
+    """Zeroed delayed-write cache [b, H, R*N + R*P] (a sequence's first token)."""
+    return torch.zeros((batch, heads, R * (dstate + headdim)), dtype=dtype, device=device)
+
+
+def cache_from_prefill(B: torch.Tensor, x: torch.Tensor) -> torch.Tensor:
+    """Delayed-write cache after a prefill: B[:, T-1] then x[:, T-1], flattened per (b, h)."""
+    Bl = B[:, -1]                       # [b, H, R, N]
+    Xl = x[:, -1]                       # [b, H, R, P]
+    b, H = Bl.shape[:2]
+    return torch.cat([Bl.reshape(b, H, -1), Xl.reshape(b, H, -1)], dim=-1).contiguous()

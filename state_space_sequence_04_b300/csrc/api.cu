@@ -1,0 +1,142 @@
+// C ABI of libm3: host-side validation, then launches on the caller's stream.
+// Every entry point checks its arguments before touching the GPU and returns
+// an m3_status; nothing is launched when a check fails.
+#include <stdint.h>
+
+#include "m3_common.cuh"
+
+namespace m3 {
+
+// Prefill paths other than the CUDA-core one register here (tensor-core path).
+size_t tc_workspace_size(const ScanDims& d);
+int tc_launch_count(const ScanDims& d);
+bool tc_supported(const ScanDims& d);
+cudaError_t launch_scan_tc(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
+                           const float* A, const float* lambda, const float* omega, void* y, float* final_state,
+                           void* workspace, cudaStream_t stream);
+
+}  // namespace m3
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+bool ok_nullable(const void* p) { return p == nullptr || aligned16(p); }
+bool ok_io(int io) { return io == M3_DTYPE_BF16 || io == M3_DTYPE_F32; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? M3_OK : M3_ERR_CUDA; }
+
+// Which prefill implementation runs for these sizes: 1 = tensor cores, 0 = CUDA cores.
+int pick_path(const m3::ScanDims& d) { return (d.io == M3_DTYPE_BF16 && m3::tc_supported(d)) ? 1 : 0; }
+
+int validate_scan_sizes(const m3::ScanDims& d) {
+    if (!ok_io(d.io)) return M3_ERR_INVALID_ARG;
+    if (d.batch < 0 || d.seqlen < 0 || d.nheads < 1 || d.headdim < 1 || d.dstate < 2) return M3_ERR_INVALID_ARG;
+    if (d.dstate % 2) return M3_ERR_INVALID_ARG;
+    if (d.R < 1 || d.chunk < 1) return M3_ERR_INVALID_ARG;
+    if (d.batch * d.nheads > (int64_t)INT32_MAX || d.seqlen > (int64_t)INT32_MAX) return M3_ERR_UNSUPPORTED;
+    if (!m3::simt_supported(d) && !(d.io == M3_DTYPE_BF16 && m3::tc_supported(d))) return M3_ERR_UNSUPPORTED;
+    return M3_OK;
+}
+
+size_t scan_workspace(const m3::ScanDims& d) {
+    return pick_path(d) == 1 ? m3::tc_workspace_size(d) : m3::simt_workspace_size(d);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* m3_status_string(int status) {
+    switch (status) {
+        case M3_OK: return "M3_OK";
+        case M3_ERR_INVALID_ARG: return "M3_ERR_INVALID_ARG: null or misaligned pointer, or an invalid size or dtype";
+        case M3_ERR_UNSUPPORTED: return "M3_ERR_UNSUPPORTED: valid arguments outside the sizes the kernels implement";
+        case M3_ERR_WORKSPACE: return "M3_ERR_WORKSPACE: workspace missing or smaller than m3_scan_fwd_workspace_size";
+        case M3_ERR_CUDA: return "M3_ERR_CUDA: a CUDA call or kernel launch failed";
+        case M3_ERR_TIMEOUT: return "M3_ERR_TIMEOUT: a bounded device-side wait gave up";
+        default: return "unknown m3 status";
+    }
+}
+
+int m3_version(void) { return 100; }
+
+size_t m3_scan_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+                                  int R, int chunk, int io_dtype) {
+    const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, chunk, io_dtype};
+    if (validate_scan_sizes(d) != M3_OK) return 0;
+    return scan_workspace(d);
+}
+
+int m3_scan_fwd_plan(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate, int R,
+                     int chunk, int io_dtype, int* path, int* launches) {
+    const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, chunk, io_dtype};
+    const int st = validate_scan_sizes(d);
+    if (st != M3_OK) return st;
+    const int p = pick_path(d);
+    int n = 0;
+    if (batch > 0) n = p == 1 ? m3::tc_launch_count(d) : (batch * nheads > 0 && seqlen > 0 ? 3 : 1);
+    if (path) *path = p;
+    if (launches) *launches = n;
+    return M3_OK;
+}
+
+int m3_scan_fwd(const void* x, const void* B, const void* C, const float* dt, const float* A, const float* lambda,
+                const float* omega, int R, int chunk, void* y, float* final_state, int64_t batch, int64_t seqlen,
+                int64_t nheads, int64_t headdim, int64_t dstate, int io_dtype, void* workspace,
+                size_t workspace_bytes, void* stream) {
+    const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, chunk, io_dtype};
+    int st = validate_scan_sizes(d);
+    if (st != M3_OK) return st;
+    if (!ok_ptr(A) || !ok_nullable(final_state)) return M3_ERR_INVALID_ARG;
+    const bool any_tokens = batch > 0 && seqlen > 0;
+    if (any_tokens) {
+        if (!ok_ptr(x) || !ok_ptr(B) || !ok_ptr(C) || !ok_ptr(dt) || !ok_ptr(lambda) || !ok_ptr(omega) || !ok_ptr(y))
+            return M3_ERR_INVALID_ARG;
+    }
+    const size_t need = scan_workspace(d);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return M3_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (batch == 0) return M3_OK;
+    if (pick_path(d) == 1)
+        return cuda_status(m3::launch_scan_tc(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, s));
+    return cuda_status(m3::launch_scan_simt(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, s));
+}
+
+int m3_decode_step(float* state, const void* x_t, const void* B_t, void* B_prev_x_prev, const void* C_t,
+                   const float* dt_t, const float* A, const float* lambda_t, const float* omega_t, void* y_t,
+                   int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R, int io_dtype,
+                   void* stream) {
+    if (!ok_io(io_dtype)) return M3_ERR_INVALID_ARG;
+    if (batch < 0 || nheads < 1 || headdim < 1 || dstate < 2 || dstate % 2 || R < 1) return M3_ERR_INVALID_ARG;
+    if (!m3::decode_supported(headdim, dstate, R)) return M3_ERR_UNSUPPORTED;
+    if (batch * nheads > (int64_t)INT32_MAX) return M3_ERR_UNSUPPORTED;
+    if (!ok_ptr(A)) return M3_ERR_INVALID_ARG;
+    if (batch == 0) return M3_OK;
+    if (!ok_ptr(state) || !ok_ptr(x_t) || !ok_ptr(B_t) || !ok_ptr(B_prev_x_prev) || !ok_ptr(C_t) || !ok_ptr(dt_t) ||
+        !ok_ptr(lambda_t) || !ok_ptr(omega_t) || !ok_ptr(y_t))
+        return M3_ERR_INVALID_ARG;
+    return cuda_status(m3::launch_decode(state, x_t, B_t, B_prev_x_prev, C_t, dt_t, A, lambda_t, omega_t, y_t, batch,
+                                         nheads, headdim, dstate, R, io_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int m3_state_passing(float* chunk_states, const float* chunk_logdecay, const float* chunk_angle,
+                     const float* init_state, float* final_state, int64_t batch, int64_t nheads, int64_t nchunks,
+                     int64_t dstate, int64_t headdim, void* stream) {
+    if (batch < 0 || nheads < 1 || nchunks < 0) return M3_ERR_INVALID_ARG;
+    if (dstate < 2 || dstate % 2 || headdim < 4 || headdim % 4) return M3_ERR_INVALID_ARG;
+    if (dstate > 256 || headdim > 256) return M3_ERR_UNSUPPORTED;
+    if (batch * nheads > (int64_t)INT32_MAX || nchunks > (int64_t)INT32_MAX) return M3_ERR_UNSUPPORTED;
+    if (!ok_nullable(init_state) || !ok_nullable(final_state)) return M3_ERR_INVALID_ARG;
+    if (batch > 0 && nchunks > 0) {
+        if (!ok_ptr(chunk_states) || !ok_ptr(chunk_logdecay) || !ok_ptr(chunk_angle)) return M3_ERR_INVALID_ARG;
+    }
+    if (batch == 0) return M3_OK;
+    return cuda_status(m3::launch_state_passing(chunk_states, chunk_logdecay, chunk_angle, init_state, final_state,
+                                                batch, nheads, nchunks, dstate, headdim,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// Shared device helpers of libm3 (kernels and host launchers only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/m3.h"
+
+namespace m3 {
+
+// ---- io element access ----------------------------------------------------
+__device__ __forceinline__ float ld_io(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld_io(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ void st_io(float* p, int64_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void st_io(__nv_bfloat16* p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+
+// Rotate the pair (a, b) counter-clockwise by the angle whose cosine and sine are c, s.
+__device__ __forceinline__ void rot2(float c, float s, float a, float b, float& oa, float& ob) {
+    oa = c * a - s * b;
+    ob = s * a + c * b;
+}
+
+// Inclusive prefix sum over a warp.
+__device__ __forceinline__ float warp_inclusive_sum(float v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        float n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace m3
+
+// ---- host-side launchers shared between translation units ----------------
+namespace m3 {
+
+struct ScanDims {
+    int64_t batch, seqlen, nheads, headdim, dstate;
+    int R, chunk, io;
+    int64_t nchunks() const { return (seqlen + chunk - 1) / chunk; }
+};
+
+cudaError_t launch_decode(float* state, const void* x_t, const void* B_t, void* cache, const void* C_t,
+                          const float* dt_t, const float* A, const float* lambda_t, const float* omega_t,
+                          void* y_t, int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R,
+                          int io, cudaStream_t stream);
+bool decode_supported(int64_t headdim, int64_t dstate, int R);
+
+cudaError_t launch_state_passing(float* chunk_states, const float* chunk_logdecay, const float* chunk_angle,
+                                 const float* init_state, float* final_state, int64_t batch, int64_t nheads,
+                                 int64_t nchunks, int64_t dstate, int64_t headdim, cudaStream_t stream);
+
+// Generic CUDA-core chunked prefill (any supported size; fp32 or bf16 io).
+size_t simt_workspace_size(const ScanDims& d);
+bool simt_supported(const ScanDims& d);
+cudaError_t launch_scan_simt(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
+                             const float* A, const float* lambda, const float* omega, void* y,
+                             float* final_state, void* workspace, cudaStream_t stream);
+
+}  // namespace m3
