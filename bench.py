@@ -95,57 +95,60 @@ def decode_bytes(b: int, H: int, P: int, N: int, R: int, io: str = "bf16") -> in
 
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    """Samples SM clocks and throttle reasons through NVML while running (read only)."""
+    """Samples SM clocks and clock-event (throttle) reasons with nvidia-smi while
+    the timed work runs (read only; changes no setting)."""
 
-    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
-               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
-               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int, period_s: float = 0.01):
-        self.samples = []
-        self.period = period_s
-        self._stop = threading.Event()
-        self._thread = None
-        self.max_mhz = None
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-        except Exception as exc:  # NVML missing: report no clocks rather than guess
-            self._nv = None
-            self.error = str(exc)
-
-    def _run(self):
-        nv = self._nv
-        while not self._stop.is_set():
-            try:
-                mhz = nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)
-                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                self.samples.append((mhz, int(rs)))
-            except Exception:
-                pass
-            time.sleep(self.period)
+    def __init__(self, device_index: int, period_ms: int = 50):
+        self.idx = device_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self.error = None
 
     def __enter__(self):
-        if self._nv is not None:
-            self._thread = threading.Thread(target=self._run, daemon=True)
-            self._thread.start()
+        import subprocess
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.period)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as exc:
+            self.error = str(exc)
+        time.sleep(0.3)
         return self
 
     def __exit__(self, *a):
-        self._stop.set()
-        if self._thread is not None:
-            self._thread.join()
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
-        if self._nv is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
-        busy = [s for s in self.samples if not (s[1] & 0x1)] or self.samples
-        reasons = sorted({name for _, r in busy for bit, name in self.REASONS.items() if r & bit})
-        mhz = statistics.median([m for m, _ in busy]) if busy else None
-        return {"sm_mhz": mhz, "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(busy)}
+        if self.error or not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"no clock samples ({self.error})"]}
+        samples = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                samples.append((float(f[0]), float(f[1]), float(f[2]), int(f[3], 16), f[4:8]))
+            except Exception:
+                continue
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unparsed clock samples"]}
+        loaded = [x for x in samples if x[2] > 250.0] or samples     # under load: power above idle
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for x in loaded for n, v in zip(names, x[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(x[0] for x in loaded), "sm_max_mhz": max(x[1] for x in samples),
+                "reasons": reasons, "samples": len(samples), "samples_under_load": len(loaded),
+                "power_w_max": max(x[2] for x in samples)}
 
 
 # ---------------------------------------------------------------------------
@@ -258,6 +261,7 @@ def time_decode(binding, b, R, stream, device, steps=synth.DECODE_STEPS, ring=32
     ins = synth.make_decode_steps(b, H, P, N, R, ring, io="bf16", seed=1, device=device)
     cache = binding.new_decode_cache(b, H, N, P, R, torch.bfloat16, device)
     y_t = torch.empty((b, H, R, P), dtype=torch.bfloat16, device=device)
+    torch.cuda.synchronize()          # inputs were drawn on the default stream
     A = ins["A"]
     per = [[ins[k][i] for k in ("x", "B", "C", "dt", "lam", "omega")] for i in range(ring)]
 
@@ -278,32 +282,96 @@ def time_decode(binding, b, R, stream, device, steps=synth.DECODE_STEPS, ring=32
         call(i)
     t1.record(stream)
     torch.cuda.synchronize()
+    eager = t0.elapsed_time(t1) / 1e3
+    # the same carried steps replayed from a CUDA graph of `ring` calls (no host launch cost)
+    graph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(ring):
+                call(i)
+        torch.cuda.synchronize()
+        reps = max(1, steps // ring)
+        with torch.cuda.stream(stream):      # replay on the stream the events are recorded on
+            g.replay()
+            torch.cuda.synchronize()
+            t0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+        graph = t0.elapsed_time(t1) / 1e3 / (reps * ring) * steps
+    except Exception as exc:  # report, do not hide
+        graph = f"graph capture failed: {exc}"
     ok = bool(torch.isfinite(state).all())
-    return t0.elapsed_time(t1) / 1e3, ok
+    return eager, graph, ok
+
+
+def decode_sweep(binding, args, stream, device, pk):
+    dec = {}
+    ranks = synth.DECODE_RANKS if args.decode_rank is None else (args.decode_rank,)
+    batches = synth.DECODE_BATCHES if args.decode_batch is None else (args.decode_batch,)
+    for R in ranks:
+        for b in batches:
+            esec, gsec, ok = time_decode(binding, b, R, stream, device, steps=args.decode_steps)
+            nbytes = decode_bytes(b, 64, 64, 128, R)
+            ent = {"bytes_per_step": nbytes, "finite": ok}
+            for tag, sec in (("eager", esec), ("graph", gsec)):
+                if not isinstance(sec, float):
+                    ent[tag] = sec
+                    continue
+                per_step = sec / args.decode_steps
+                gbs = nbytes / per_step / 1e9
+                ent[tag] = {"steps_per_s": 1.0 / per_step, "us_per_step": per_step * 1e6,
+                            "tokens_per_s": b / per_step, "achieved_gbs": gbs,
+                            "frac_of_measured_hbm": gbs / pk["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0}
+            dec[f"b{b}_R{R}"] = ent
+    return {"unit": "steps/s", "steps": args.decode_steps, "heads": 64, "headdim": 64, "dstate": 128,
+            "sweep": dec}
 
 
 # ---------------------------------------------------------------------------
-def cpu_baseline_run(w, target_s: float = 12.0, max_s: float = 40.0):
+def _oracle_sample(inp, w, n):
+    """The first n (batch, head) sequences of the workload, stacked as heads of one
+    batch-1 problem (float64 numpy), in the oracle's argument order."""
+    import numpy as np
+    import oracle
+    pairs = [(b, h) for b in range(w.batch) for h in range(w.heads)][:n]
+    cols = []
+    for i, key in enumerate(KEYS):
+        if key == "A":
+            cols.append(np.array([float(inp["A"][h]) for _, h in pairs]))
+        else:
+            cols.append(np.concatenate([oracle.f64(inp[key][b:b + 1, :, h:h + 1]) for b, h in pairs], axis=2))
+    return cols
+
+
+def cpu_baseline_run(w, inp, target_s: float = 10.0, max_s: float = 30.0):
     """Time the float64 oracle on a bounded sample of the workload: whole sequences
-    (one (batch, head) of T tokens each), doubling the sample until it runs
-    >= target_s.  Returns (Mtok/s, threads, sample description, seconds)."""
+    (one (batch, head) of T tokens each), doubling the sample from one per thread
+    until one run takes >= target_s or the whole workload is covered.
+    ``inp`` are the benchmark's own inputs (on any device); the sampled sequences
+    are copied to the host.  Returns (Mtok/s, threads, sample description, seconds)."""
     import oracle
     threads = oracle.num_threads()
-    inp = synth.make_inputs(w, seed=0, batch=1)   # batch row 0 of the workload: H sequences
-    n = max(1, min(w.heads, threads))
+    total = w.batch * w.heads
+    n = max(1, min(total, threads))
     while True:
-        heads = list(range(n))
-        args = [inp["x"][:, :, heads], inp["B"][:, :, heads], inp["C"][:, :, heads], inp["dt"][:, :, heads],
-                inp["A"][heads], inp["lam"][:, :, heads], inp["omega"][:, :, heads]]
-        args = [oracle.f64(a) for a in args]
+        a = _oracle_sample(inp, w, n)
         t0 = time.perf_counter()
-        oracle.scan(*args)
+        oracle.scan(*a)
         el = time.perf_counter() - t0
-        if el >= target_s or n >= w.heads or el * 2 > max_s:
+        if el >= target_s or n >= total or el * 2 > max_s:
             break
-        n = min(w.heads, n * 2)
-    tokens = n * w.seqlen / w.heads          # token-equivalents (a token covers all heads)
-    sample = f"{n} of {w.heads * w.batch} (batch, head) sequences x {w.seqlen} tokens, float64"
+        n = min(total, n * 2)
+    runs = 1
+    while el < target_s and el * (runs + 1) / runs <= max_s:   # whole workload is quick: repeat it
+        t0 = time.perf_counter()
+        oracle.scan(*a)
+        el += time.perf_counter() - t0
+        runs += 1
+    tokens = n * w.seqlen / w.heads * runs   # token-equivalents (a token covers all heads)
+    sample = f"{n} of {total} (batch, head) sequences x {w.seqlen} tokens, float64, {runs} run(s)"
     return tokens / el / 1e6, threads, sample, el
 
 
@@ -313,14 +381,11 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    w = synth.SISO_1P5B
+    w = synth.WORKLOADS[args.workload]
     threads = oracle.num_threads()
-    inp = synth.make_inputs(w, seed=0, batch=1)
+    inp = synth.make_inputs(w, seed=0, batch=1)      # batch row 0 on the host
     n = max(1, min(w.heads, threads))
-    heads = list(range(n))
-    a = [oracle.f64(v) for v in (inp["x"][:, :, heads], inp["B"][:, :, heads], inp["C"][:, :, heads],
-                                 inp["dt"][:, :, heads], inp["A"][heads], inp["lam"][:, :, heads],
-                                 inp["omega"][:, :, heads])]
+    a = _oracle_sample(inp, w, n)
     for _ in range(args.warmup):
         oracle.scan(*a)
     t0 = time.perf_counter()
@@ -353,6 +418,11 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default=synth.SISO_1P5B.name, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--mode", choices=["all", "decode"], default="all",
+                    help="decode: only the decode sweep (restricted by --decode-batch/--decode-rank)")
+    ap.add_argument("--decode-batch", type=int, default=None)
+    ap.add_argument("--decode-rank", type=int, default=None)
+    ap.add_argument("--decode-steps", type=int, default=synth.DECODE_STEPS)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -369,15 +439,23 @@ def main():
     w = synth.WORKLOADS[args.workload]
     stream = torch.cuda.Stream(device=device)
 
+    if args.mode == "decode":
+        line = {"metric": METRIC, "mode": "decode",
+                "decode": decode_sweep(binding, args, stream, device, pk)}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return 0
+
     # every rank draws its own replica of the workload (seeded by rank)
     d = synth.make_inputs(w, seed=rank, device=device)
+    torch.cuda.synchronize()
     path, launches = binding.m3_scan_fwd_plan(w.batch, w.seqlen, w.heads, w.headdim, w.dstate, w.rank, w.chunk,
                                               binding.io_code(d["x"].dtype))
     with ClockSampler(local) as clk:
         sec, per_ms, _ = time_prefill(binding, w, d, stream, args.steps, args.warmup, dist, device)
     clocks = clk.summary()
-    tokens = w.batch * w.seqlen * ws
-    value = tokens / sec / 1e6
+    tokens = w.batch * w.seqlen * ws                  # per step, all ranks
+    value = tokens * args.steps / sec / 1e6
     avg_call_ms = sum(per_ms) / len(per_ms)
     nbytes = prefill_bytes(w)
     achieved_gbs = nbytes / (avg_call_ms * 1e-3) / 1e9
@@ -409,21 +487,10 @@ def main():
         del host
 
     if not args.no_decode and rank == 0:
-        dec = {}
-        for R in synth.DECODE_RANKS:
-            for b in synth.DECODE_BATCHES:
-                dsec, ok = time_decode(binding, b, R, stream, device)
-                per_step = dsec / synth.DECODE_STEPS
-                gbs = decode_bytes(b, 64, 64, 128, R) / per_step / 1e9
-                dec[f"b{b}_R{R}"] = {"steps_per_s": 1.0 / per_step, "us_per_step": per_step * 1e6,
-                                     "tokens_per_s": b / per_step, "achieved_gbs": gbs,
-                                     "frac_of_measured_hbm": gbs / pk["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0,
-                                     "finite": ok}
-        line["decode"] = {"unit": "steps/s", "steps": synth.DECODE_STEPS, "heads": 64, "headdim": 64,
-                          "dstate": 128, "eager": True, "sweep": dec}
+        line["decode"] = decode_sweep(binding, args, stream, device, pk)
 
     if not args.no_cpu_baseline and rank == 0 and ws == 1:
-        v, threads, sample, el = cpu_baseline_run(w)
+        v, threads, sample, el = cpu_baseline_run(w, d)
         line["cpu_baseline"] = {"value": v, "unit": "Mtok/s", "cores": threads, "kind": "oracle",
                                 "sample": sample, "seconds": el}
 

@@ -101,6 +101,35 @@ def test_scan_small(io, Bt, H, T, P, N, R, Q):
     assert_close(fin, hr, TOL[io], "final_state")
 
 
+# shapes the tensor-core path takes (bf16, N = 128, P = 64, H % 4 == 0)
+TC_CASES = [
+    # Bt, H, T, P, N, R, Q
+    (1, 4, 1, 64, 128, 1, 64),
+    (1, 4, 63, 64, 128, 1, 64),
+    (2, 4, 65, 64, 128, 1, 64),
+    (1, 8, 300, 64, 128, 1, 64),
+    (2, 4, 1000, 64, 128, 1, 128),
+    (1, 4, 200, 64, 128, 2, 64),
+    (1, 4, 129, 64, 128, 2, 64),
+]
+
+
+@pytest.mark.parametrize("Bt,H,T,P,N,R,Q", TC_CASES)
+def test_scan_tensor_core_path(Bt, H, T, P, N, R, Q):
+    path, launches = binding.m3_scan_fwd_plan(Bt, T, H, P, N, R, Q, binding.M3_DTYPE_BF16)
+    assert path == 1 and launches == 1
+    w = synth.Workload("case", Bt, H, T, P, N, R, Q, "bf16")
+    inp = synth.make_inputs(w, seed=T + R + Q)
+    d = to_dev(inp)
+    ws = binding.alloc_workspace(d["x"].shape, N, R, Q, d["x"].dtype, "cuda")
+    y, fin = binding.scan_fwd(*[d[k] for k in KEYS], R, Q, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0, "device-side wait gave up"
+    yr, hr, _ = oracle_full(inp)
+    assert_close(y, yr, TOL["bf16"], "y")
+    assert_close(fin, hr, TOL["bf16"], "final_state")
+
+
 def test_scan_chunk_independence():
     """Different chunk lengths give the same result up to rounding (section 3.3)."""
     w = synth.Workload("case", 1, 2, 300, 64, 64, 2, 64, "fp32")
