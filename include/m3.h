@@ -117,6 +117,39 @@ M3_API int m3_scan_fwd(const void* x, const void* B, const void* C, const float*
                 int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
                 int io_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of the fixed scratch array behind m3_scan_fwd_noalloc (16 MiB). */
+#define M3_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * m3_scan_fwd for callers that cannot allocate device memory.  The paper has
+ * no counterpart: this is a library convenience, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc or hand the library a workspace: an
+ * application that owns every device allocation and passes only inputs and
+ * outputs, a serving loop that forbids allocation once it runs, a plugin
+ * host with no allocator callback.  This entry point takes the arguments of
+ * m3_scan_fwd minus the workspace and computes the same result, using a fixed
+ * scratch array of M3_NOALLOC_SCRATCH_BYTES that is part of the library's
+ * device image (every GPU that loads the library keeps it reserved until the
+ * process exits).  It allocates nothing.
+ *
+ *   - Sizes whose workspace (m3_scan_fwd_workspace_size) exceeds
+ *     M3_NOALLOC_SCRATCH_BYTES return M3_ERR_WORKSPACE and launch nothing;
+ *     other errors are those of m3_scan_fwd.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents (each call clears what must start at zero).  Calls that
+ *     overlap on the GPU -- on different streams or from different host
+ *     threads -- race on it: serialise them.
+ */
+M3_API int m3_scan_fwd_noalloc(const void* x, const void* B, const void* C, const float* dt, const float* A,
+                               const float* lambda, const float* omega, int R, int chunk,
+                               void* y, float* final_state,
+                               int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+                               int io_dtype, void* stream);
+
 /*
  * One decode token for every (batch, head): the recurrence above with T = 1
  * from a carried state (the single-token mode of section 3.3 / Table 6).

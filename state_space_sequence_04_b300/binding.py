@@ -41,6 +41,8 @@ SIGNATURES = {
                           ctypes.POINTER(_int)], _int),
     "m3_scan_fwd": ([_vp, _vp, _vp, _fp, _fp, _fp, _fp, _int, _int, _vp, _fp,
                      _i64, _i64, _i64, _i64, _i64, _int, _vp, _sz, _vp], _int),
+    "m3_scan_fwd_noalloc": ([_vp, _vp, _vp, _fp, _fp, _fp, _fp, _int, _int, _vp, _fp,
+                             _i64, _i64, _i64, _i64, _i64, _int, _vp], _int),
     "m3_decode_step": ([_fp, _vp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp,
                         _i64, _i64, _i64, _i64, _int, _int, _vp], _int),
     "m3_state_passing": ([_fp, _fp, _fp, _fp, _fp, _i64, _i64, _i64, _i64, _i64, _vp], _int),
@@ -135,6 +137,18 @@ def m3_scan_fwd(x, B, C, dt, A, lam, omega, R: int, chunk: int, y, final_state, 
         _ptr(A, torch.float32), _ptr(lam, torch.float32), _ptr(omega, torch.float32), int(R), int(chunk),
         _ptr(y, x.dtype), _ptr(final_state, torch.float32), Bt, T, H, P, N, io, _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def m3_scan_fwd_noalloc(x, B, C, dt, A, lam, omega, R: int, chunk: int, y, final_state, stream=None) -> int:
+    """Call m3_scan_fwd_noalloc: m3_scan_fwd without a workspace (the library's
+    fixed scratch array instead); returns the status code (does not raise)."""
+    Bt, T, H, R_, P = x.shape
+    N = B.shape[-1]
+    io = io_code(x.dtype)
+    return int(load().m3_scan_fwd_noalloc(
+        _ptr(x, x.dtype), _ptr(B, x.dtype), _ptr(C, x.dtype), _ptr(dt, torch.float32),
+        _ptr(A, torch.float32), _ptr(lam, torch.float32), _ptr(omega, torch.float32), int(R), int(chunk),
+        _ptr(y, x.dtype), _ptr(final_state, torch.float32), Bt, T, H, P, N, io, _stream(stream)))
 
 
 def m3_decode_step(state, x_t, B_t, cache, C_t, dt_t, A, lam_t, omega_t, y_t, R: int, stream=None) -> int:

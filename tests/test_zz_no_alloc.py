@@ -1,0 +1,74 @@
+"""m3_scan_fwd_noalloc: the prefill for callers that cannot allocate device memory.
+
+Such callers (an application that owns every device allocation, a serving
+loop that forbids allocation once running, a plugin host without an allocator
+callback) cannot hand m3_scan_fwd a workspace; m3_scan_fwd_noalloc uses the
+library's fixed scratch array instead.  These tests call it through the C ABI
+several times in a row (so later calls see the scratch array as earlier calls
+left it) and check each result against m3_scan_fwd on the same inputs, with
+the parity tolerances of the other GPU tests.  The file is named to be
+collected last.
+"""
+import pytest
+import torch
+
+from state_space_sequence_04_b300 import binding, synth
+
+from parity_util import TOL, KEYS, assert_close, need_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 16 * 1024 * 1024     # M3_NOALLOC_SCRATCH_BYTES in include/m3.h
+
+# One problem per path: CUDA-core kernels (scratch holds the chunk states) and
+# the tensor-core kernel (scratch holds its status word).
+CASES = [
+    # name, Bt, H, T, P, N, R, Q, io, seed
+    ("cuda_core_fp32", 2, 4, 1000, 64, 64, 1, 64, "fp32", 1),
+    ("tensor_core_bf16", 2, 4, 700, 64, 128, 1, 64, "bf16", 2),
+    ("cuda_core_fp32_again", 1, 4, 333, 32, 128, 2, 32, "fp32", 3),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _run_both(Bt, H, T, P, N, R, Q, io, seed):
+    w = synth.Workload("noalloc", Bt, H, T, P, N, R, Q, io)
+    d = to_dev(synth.make_inputs(w, seed=seed))
+    args = [d[k] for k in KEYS]
+    need = binding.m3_scan_fwd_workspace_size(Bt, T, H, P, N, R, Q, binding.io_code(d["x"].dtype))
+    assert 0 < need <= SCRATCH_BYTES
+    y_ref, fin_ref = binding.scan_fwd(*args, R, Q)
+    y = torch.full_like(y_ref, float("nan"))
+    fin = torch.full_like(fin_ref, float("nan"))
+    st = binding.m3_scan_fwd_noalloc(*args, R, Q, y, fin)
+    assert st == binding.M3_OK, binding.m3_status_string(st)
+    torch.cuda.synchronize()
+    return y, fin, y_ref, fin_ref
+
+
+def test_noalloc_matches_scan_fwd_on_consecutive_calls():
+    for name, Bt, H, T, P, N, R, Q, io, seed in CASES:
+        y, fin, y_ref, fin_ref = _run_both(Bt, H, T, P, N, R, Q, io, seed)
+        assert torch.isfinite(y.float()).all(), name
+        assert_close(y, y_ref, TOL[io], f"{name}: y")
+        assert_close(fin, fin_ref, TOL[io], f"{name}: final_state")
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    # fp32, batch 4 x 64 heads x 4096 tokens needs ~0.5 GB of chunk states:
+    # more than the fixed scratch, so the call must fail before any launch.
+    lib = binding.load()
+    need = binding.m3_scan_fwd_workspace_size(4, 4096, 64, 64, 128, 1, 64, binding.M3_DTYPE_F32)
+    assert need > SCRATCH_BYTES
+    p = [16 * (i + 1) for i in range(9)]   # aligned placeholders; never dereferenced
+    st = lib.m3_scan_fwd_noalloc(p[0], p[1], p[2], p[3], p[4], p[5], p[6], 1, 64, p[7], p[8],
+                                 4, 4096, 64, 64, 128, binding.M3_DTYPE_F32, None)
+    assert st == binding.M3_ERR_WORKSPACE
+    # invalid sizes keep m3_scan_fwd's own answer
+    st = lib.m3_scan_fwd_noalloc(p[0], p[1], p[2], p[3], p[4], p[5], p[6], 3, 64, p[7], p[8],
+                                 1, 128, 4, 64, 128, binding.M3_DTYPE_F32, None)
+    assert st == binding.M3_ERR_UNSUPPORTED
