@@ -174,6 +174,15 @@ M3_API int m3_decode_step(float* state, const void* x_t, const void* B_t, void* 
                    int io_dtype, void* stream);
 
 /*
+ * Sticky device-side error word of m3_decode_step, which takes no workspace:
+ * M3_OK, or M3_ERR_TIMEOUT once a bounded wait inside a decode kernel gave up
+ * (the outputs of that call are then not valid).  Reading it synchronises
+ * with the current device; clear != 0 resets it to M3_OK afterwards.
+ * Returns the word, or M3_ERR_CUDA if it could not be read.
+ */
+M3_API int m3_device_status(int clear);
+
+/*
  * Inter-chunk state passing of the chunked algorithm, in place:
  *
  *   H_c = exp(l_c) R(Theta_c) H_{c-1} + U_c,   c = 0 .. nchunks-1,

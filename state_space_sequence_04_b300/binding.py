@@ -45,6 +45,7 @@ SIGNATURES = {
                              _i64, _i64, _i64, _i64, _i64, _int, _vp], _int),
     "m3_decode_step": ([_fp, _vp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp,
                         _i64, _i64, _i64, _i64, _int, _int, _vp], _int),
+    "m3_device_status": ([_int], _int),
     "m3_state_passing": ([_fp, _fp, _fp, _fp, _fp, _i64, _i64, _i64, _i64, _i64, _vp], _int),
 }
 
@@ -160,6 +161,11 @@ def m3_decode_step(state, x_t, B_t, cache, C_t, dt_t, A, lam_t, omega_t, y_t, R:
         _ptr(state, torch.float32), _ptr(x_t, x_t.dtype), _ptr(B_t, x_t.dtype), _ptr(cache, x_t.dtype),
         _ptr(C_t, x_t.dtype), _ptr(dt_t, torch.float32), _ptr(A, torch.float32), _ptr(lam_t, torch.float32),
         _ptr(omega_t, torch.float32), _ptr(y_t, x_t.dtype), b, H, P, N, int(R), io, _stream(stream)))
+
+
+def m3_device_status(clear: bool = False) -> int:
+    """Sticky device-side error word of the decode kernels (M3_OK or M3_ERR_TIMEOUT)."""
+    return int(load().m3_device_status(1 if clear else 0))
 
 
 def m3_state_passing(chunk_states, chunk_logdecay, chunk_angle, init_state, final_state, stream=None) -> int:

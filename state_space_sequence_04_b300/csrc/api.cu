@@ -122,6 +122,8 @@ int m3_decode_step(float* state, const void* x_t, const void* B_t, void* B_prev_
                                          nheads, headdim, dstate, R, io_dtype, static_cast<cudaStream_t>(stream)));
 }
 
+int m3_device_status(int clear) { return m3::decode_device_status(clear); }
+
 int m3_state_passing(float* chunk_states, const float* chunk_logdecay, const float* chunk_angle,
                      const float* init_state, float* final_state, int64_t batch, int64_t nheads, int64_t nchunks,
                      int64_t dstate, int64_t headdim, void* stream) {

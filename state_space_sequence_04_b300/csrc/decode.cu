@@ -9,37 +9,82 @@
 //   h <- R(phi_t) (alpha_t h + beta_t B_{t-1} X_{t-1}^T) + gamma_t B_t X_t^T
 //   y_t = h^T C_t
 //
-// One CTA owns one (batch, head).  Thread (g, c4) handles state pairs
-// j = g, g + G, ... (rows 2j, 2j+1) for float4 column c4; the readout's sum
-// over N is a per-thread partial followed by a shared-memory reduction over
-// the G pair groups.
+// One CTA (at most 256 threads) owns one (batch, head).  Thread (g, c4)
+// handles state pairs j = g, g + G, ... (rows 2j, 2j+1) for float4 column c4,
+// in slabs of four pairs whose loads are issued together (the first slab
+// before anything else).  B_t, B_{t-1}, C_t are staged in shared
+// memory pair-major ([j][r] float2) and X_t, X_{t-1} row-major, so that a
+// pair costs a handful of vector shared-memory loads for its 24R
+// multiply-adds.  The readout's sum over N is a warp-shuffle reduction over
+// the pair groups of a warp followed by a shared-memory sum over warps.
+//
+// Two kernels share that arithmetic:
+//   decode_stream_kernel  persistent CTAs (two per SM) walk the (batch, head)
+//                         units; each unit's state and step inputs are
+//                         brought into shared memory by bulk asynchronous
+//                         copies (cp.async.bulk, mbarrier completion) two or
+//                         three units ahead, so HBM reads overlap the
+//                         arithmetic of earlier units.  Used when every per-unit block is a
+//                         multiple of 16 bytes (N % 8 == 0 and the io rows
+//                         16-byte sized).
+//   decode_kernel         one CTA per unit, state loaded straight into
+//                         registers; any other supported shape.
 #include "m3_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace m3 {
 namespace {
 
 constexpr int kMaxUnits = 4;   // state pairs per thread
 
+__device__ __forceinline__ float4 fma4(float a, float4 x, float4 y) {
+    return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+}
+
+#ifndef M3_DECODE_OCC_R4
+#define M3_DECODE_OCC_R4 2
+#endif
+template <int R>
+struct DecodeOcc {   // resident CTAs per SM the register budget is sized for (256-thread CTAs)
+    static constexpr int value = R == 1 ? 4 : (R == 2 ? 3 : (R == 4 ? M3_DECODE_OCC_R4 : 2));
+};
+
 template <typename IO, int R>
-__global__ void __launch_bounds__(512) decode_kernel(
+__global__ void __launch_bounds__(256, DecodeOcc<R>::value) decode_kernel(
     float* __restrict__ state, const IO* __restrict__ x_t, const IO* __restrict__ B_t,
     IO* __restrict__ cache, const IO* __restrict__ C_t, const float* __restrict__ dt_t,
     const float* __restrict__ A, const float* __restrict__ lam_t, const float* __restrict__ omega_t,
     IO* __restrict__ y_t, int H, int P, int N, int G) {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const int64_t bh = blockIdx.x;
     const int h = (int)(bh % H);
     const int P4 = P >> 2, NP2 = N >> 1;
     const int tid = threadIdx.x, nt = blockDim.x;
 
-    float* sB = sm;              // [R][N]  B_t
-    float* sC = sB + R * N;      // [R][N]  C_t
-    float* sBp = sC + R * N;     // [R][N]  B_{t-1}
-    float* sX = sBp + R * N;     // [R][P]  X_t
-    float* sXp = sX + R * P;     // [R][P]  X_{t-1}
-    float* sCos = sXp + R * P;   // [N/2]
-    float* sSin = sCos + NP2;    // [N/2]
-    float* sRed = sSin + NP2;    // [nt][R*4]
+    float2* sB2 = reinterpret_cast<float2*>(sm);     // [N/2][R]  B_t pairs
+    float2* sBp2 = sB2 + NP2 * R;                    // [N/2][R]  B_{t-1} pairs
+    float2* sC2 = sBp2 + NP2 * R;                    // [N/2][R]  C_t pairs
+    float2* sCS = sC2 + NP2 * R;                     // [N/2]     (cos, sin) of phi_t
+    float* sX = reinterpret_cast<float*>(sCS + NP2); // [R][P]    X_t
+    float* sXp = sX + R * P;                         // [R][P]    X_{t-1}
+    float* sRed = sXp + R * P;                       // [rows][R*P] readout partials
+
+    // Issue the first slab of state loads before anything else: they are the
+    // bytes that matter.  Slab s covers pairs j = g + (s*kMaxUnits + k)*G.
+    const int c4 = tid % P4, g = tid / P4;
+    float4* st4 = reinterpret_cast<float4*>(state + bh * (int64_t)N * P);
+    float4 h0[kMaxUnits], h1[kMaxUnits];
+    auto load_slab = [&](int s0) {
+#pragma unroll
+        for (int k = 0; k < kMaxUnits; ++k) {
+            const int j = g + (s0 + k) * G;
+            if (j < NP2) {
+                h0[k] = st4[(2 * j) * P4 + c4];
+                h1[k] = st4[(2 * j + 1) * P4 + c4];
+            }
+        }
+    };
+    load_slab(0);
 
     const float d = dt_t[bh], l = lam_t[bh], a = A[h];
     const float alpha = expf(d * a);
@@ -51,23 +96,15 @@ __global__ void __launch_bounds__(512) decode_kernel(
     const IO* Cb = C_t + bh * R * N;
     IO* cb = cache + bh * (int64_t)R * (N + P);
 
-    // Issue the state loads first: they are the bytes that matter.
-    const int c4 = tid % P4, g = tid / P4;
-    float4* st4 = reinterpret_cast<float4*>(state + bh * (int64_t)N * P);
-    float4 h0[kMaxUnits], h1[kMaxUnits];
-#pragma unroll
-    for (int k = 0; k < kMaxUnits; ++k) {
-        const int j = g + k * G;
-        if (j < NP2) {
-            h0[k] = st4[(2 * j) * P4 + c4];
-            h1[k] = st4[(2 * j + 1) * P4 + c4];
-        }
-    }
-
+    float* sB2f = reinterpret_cast<float*>(sB2);
+    float* sBp2f = reinterpret_cast<float*>(sBp2);
+    float* sC2f = reinterpret_cast<float*>(sC2);
     for (int i = tid; i < R * N; i += nt) {
-        sB[i] = ld_io(Bb, i);
-        sC[i] = ld_io(Cb, i);
-        sBp[i] = ld_io(cb, i);
+        const int r = i / N, n = i % N;
+        const int o = ((n >> 1) * R + r) * 2 + (n & 1);
+        sB2f[o] = ld_io(Bb, i);
+        sC2f[o] = ld_io(Cb, i);
+        sBp2f[o] = ld_io(cb, i);
     }
     for (int i = tid; i < R * P; i += nt) {
         sX[i] = ld_io(xb, i);
@@ -76,69 +113,345 @@ __global__ void __launch_bounds__(512) decode_kernel(
     for (int j = tid; j < NP2; j += nt) {
         float sn, cs;
         sincosf(d * omega_t[bh * NP2 + j], &sn, &cs);
-        sCos[j] = cs;
-        sSin[j] = sn;
+        sCS[j] = make_float2(cs, sn);
     }
     __syncthreads();
     // The old cache is in shared memory now: replace it with this token's factors.
     for (int i = tid; i < R * N; i += nt) cb[i] = Bb[i];
     for (int i = tid; i < R * P; i += nt) cb[R * N + i] = xb[i];
 
-    float acc[R][4];
+    const float4* sX4 = reinterpret_cast<const float4*>(sX);
+    const float4* sXp4 = reinterpret_cast<const float4*>(sXp);
+    float4 acc[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[r][e] = 0.0f;
+    for (int r = 0; r < R; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
 
+    const int slabs = (NP2 + G * kMaxUnits - 1) / (G * kMaxUnits);
+    for (int sl = 0; sl < slabs; ++sl) {
+        if (sl > 0) load_slab(sl * kMaxUnits);
 #pragma unroll
-    for (int k = 0; k < kMaxUnits; ++k) {
-        const int j = g + k * G;
-        if (j < NP2) {
-            const float cs = sCos[j], sn = sSin[j];
-            float o0[4], o1[4];
-            const float a0v[4] = {h0[k].x, h0[k].y, h0[k].z, h0[k].w};
-            const float a1v[4] = {h1[k].x, h1[k].y, h1[k].z, h1[k].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int p = c4 * 4 + e;
-                float vp0 = 0.f, vp1 = 0.f, v0 = 0.f, v1 = 0.f;
+        for (int k = 0; k < kMaxUnits; ++k) {
+            const int j = g + (sl * kMaxUnits + k) * G;
+            if (j < NP2) {
+                const float2 cs = sCS[j];
+                // u = alpha h + beta v_{t-1}, v_{t-1} = B_{t-1} X_{t-1}^T (rows 2j, 2j+1)
+                float4 w0 = make_float4(0.f, 0.f, 0.f, 0.f), w1 = w0;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const float xp = sXp[r * P + p], xc = sX[r * P + p];
-                    vp0 = fmaf(sBp[r * N + 2 * j], xp, vp0);
-                    vp1 = fmaf(sBp[r * N + 2 * j + 1], xp, vp1);
-                    v0 = fmaf(sB[r * N + 2 * j], xc, v0);
-                    v1 = fmaf(sB[r * N + 2 * j + 1], xc, v1);
+                    const float2 bp = sBp2[j * R + r];
+                    const float4 xp = sXp4[r * P4 + c4];
+                    w0 = fma4(bp.x, xp, w0);
+                    w1 = fma4(bp.y, xp, w1);
                 }
-                const float u0 = fmaf(alpha, a0v[e], beta * vp0);
-                const float u1 = fmaf(alpha, a1v[e], beta * vp1);
-                float n0, n1;
-                rot2(cs, sn, u0, u1, n0, n1);
-                o0[e] = fmaf(gamma, v0, n0);
-                o1[e] = fmaf(gamma, v1, n1);
+                const float4 u0 = fma4(alpha, h0[k], make_float4(beta * w0.x, beta * w0.y, beta * w0.z, beta * w0.w));
+                const float4 u1 = fma4(alpha, h1[k], make_float4(beta * w1.x, beta * w1.y, beta * w1.z, beta * w1.w));
+                // h' = R(phi) u + gamma v_t, v_t = B_t X_t^T
+                float4 o0, o1;
+                rot2(cs.x, cs.y, u0.x, u1.x, o0.x, o1.x);
+                rot2(cs.x, cs.y, u0.y, u1.y, o0.y, o1.y);
+                rot2(cs.x, cs.y, u0.z, u1.z, o0.z, o1.z);
+                rot2(cs.x, cs.y, u0.w, u1.w, o0.w, o1.w);
+                float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
 #pragma unroll
-                for (int r = 0; r < R; ++r)
-                    acc[r][e] = fmaf(o0[e], sC[r * N + 2 * j], fmaf(o1[e], sC[r * N + 2 * j + 1], acc[r][e]));
+                for (int r = 0; r < R; ++r) {
+                    const float2 bc = sB2[j * R + r];
+                    const float4 xc = sX4[r * P4 + c4];
+                    v0 = fma4(bc.x, xc, v0);
+                    v1 = fma4(bc.y, xc, v1);
+                }
+                o0 = fma4(gamma, v0, o0);
+                o1 = fma4(gamma, v1, o1);
+                st4[(2 * j) * P4 + c4] = o0;
+                st4[(2 * j + 1) * P4 + c4] = o1;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float2 cc = sC2[j * R + r];
+                    acc[r] = fma4(cc.x, o0, fma4(cc.y, o1, acc[r]));
+                }
             }
-            st4[(2 * j) * P4 + c4] = make_float4(o0[0], o0[1], o0[2], o0[3]);
-            st4[(2 * j + 1) * P4 + c4] = make_float4(o1[0], o1[1], o1[2], o1[3]);
         }
     }
 
-    // Readout: sum the G pair-group partials of each (r, p).
+    // Readout: sum the G pair-group partials of each (r, p).  Pair groups that
+    // share a full warp (P4 a power of two below 32) are combined with shuffles
+    // first.
+    int gpw = 1;
+    if (P4 < 32 && (P4 & (P4 - 1)) == 0 && nt % 32 == 0) {
+        gpw = 32 / P4;
+        for (int o = P4; o < 32; o <<= 1) {
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+            for (int r = 0; r < R; ++r) {
+                acc[r].x += __shfl_xor_sync(0xffffffffu, acc[r].x, o);
+                acc[r].y += __shfl_xor_sync(0xffffffffu, acc[r].y, o);
+                acc[r].z += __shfl_xor_sync(0xffffffffu, acc[r].z, o);
+                acc[r].w += __shfl_xor_sync(0xffffffffu, acc[r].w, o);
+            }
+        }
+    }
+    const int rows = (G + gpw - 1) / gpw;
+    if (g % gpw == 0) {
+        float4* red4 = reinterpret_cast<float4*>(sRed) + (g / gpw) * (R * P4);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sRed[tid * (R * 4) + r * 4 + e] = acc[r][e];
+        for (int r = 0; r < R; ++r) red4[r * P4 + c4] = acc[r];
+    }
     __syncthreads();
     IO* yb = y_t + bh * R * P;
     for (int o = tid; o < R * P; o += nt) {
-        const int r = o / P, p = o % P;
-        const int cc = p >> 2, e = p & 3;
         float s = 0.f;
-        for (int gg = 0; gg < G; ++gg) s += sRed[(gg * P4 + cc) * (R * 4) + r * 4 + e];
+        for (int gg = 0; gg < rows; ++gg) s += sRed[gg * (R * P) + o];
         st_io(yb, o, s);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Streaming variant.  Per-unit slot in shared memory (16-byte aligned pieces):
+//   state [N*P] fp32 | B_t [R*N] | C_t [R*N] | x_t [R*P] | cache [R*(N+P)] (io) | omega [N/2] fp32
+constexpr int kMaxSlots = 3;   // units in flight per CTA (3, or 2 when 3 do not fit)
+constexpr uint64_t kStreamWaitNs = 2000000000ull;   // 2 s per wait, then give up
+
+// Sticky error word of the decode kernels (they have no workspace): set to
+// M3_ERR_TIMEOUT when a bounded wait gives up; read by m3_device_status.
+__device__ int g_decode_status = 0;
+
+__host__ __device__ inline int round16(int v) { return (v + 15) & ~15; }
+
+struct StreamLayout {
+    int st, b, c, x, ca, om, slot, tx;
+};
+
+__host__ __device__ inline StreamLayout stream_layout(int N, int P, int R, int es) {
+    StreamLayout L;
+    L.st = 0;
+    L.b = L.st + N * P * 4;
+    L.c = L.b + round16(R * N * es);
+    L.x = L.c + round16(R * N * es);
+    L.ca = L.x + round16(R * P * es);
+    L.om = L.ca + round16(R * (N + P) * es);
+    L.slot = (L.om + round16((N / 2) * 4) + 127) & ~127;
+    L.tx = N * P * 4 + 2 * R * N * es + R * P * es + R * (N + P) * es + (N / 2) * 4;
+    return L;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            tc::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
+        : "memory");
+}
+
+template <typename IO, int R>
+__global__ void __launch_bounds__(256, 2) decode_stream_kernel(
+    float* __restrict__ state, const IO* __restrict__ x_t, const IO* __restrict__ B_t,
+    IO* __restrict__ cache, const IO* __restrict__ C_t, const float* __restrict__ dt_t,
+    const float* __restrict__ A, const float* __restrict__ lam_t, const float* __restrict__ omega_t,
+    IO* __restrict__ y_t, int H, int P, int N, int G, int64_t units, int nslots) {
+    extern __shared__ __align__(128) uint8_t smraw[];
+    const int P4 = P >> 2, NP2 = N >> 1;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const StreamLayout L = stream_layout(N, P, R, (int)sizeof(IO));
+
+    uint8_t* slots = smraw;
+    float2* sB2 = reinterpret_cast<float2*>(smraw + nslots * L.slot);
+    float2* sBp2 = sB2 + NP2 * R;
+    float2* sC2 = sBp2 + NP2 * R;
+    float2* sCS = sC2 + NP2 * R;
+    float* sX = reinterpret_cast<float*>(sCS + NP2);
+    float* sXp = sX + R * P;
+    float* sRed = sXp + R * P;
+    const int gpw = (P4 < 32 && (P4 & (P4 - 1)) == 0 && nt % 32 == 0) ? 32 / P4 : 1;
+    const int rows = (G + gpw - 1) / gpw;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRed + rows * R * P + 2);   // 8-byte aligned
+    int* sFail = reinterpret_cast<int*>(bars + kMaxSlots);
+
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    auto issue = [&](int64_t u, int slot) {
+        uint8_t* sl = slots + slot * L.slot;
+        uint64_t* bar = &bars[slot];
+        tc::mbar_arrive_expect_tx(bar, (uint32_t)L.tx);
+        const int es = (int)sizeof(IO);
+        bulk_g2s(sl + L.st, state + u * (int64_t)N * P, (uint32_t)(N * P * 4), bar);
+        bulk_g2s(sl + L.b, B_t + u * R * N, (uint32_t)(R * N * es), bar);
+        bulk_g2s(sl + L.c, C_t + u * R * N, (uint32_t)(R * N * es), bar);
+        bulk_g2s(sl + L.x, x_t + u * R * P, (uint32_t)(R * P * es), bar);
+        bulk_g2s(sl + L.ca, cache + u * (int64_t)R * (N + P), (uint32_t)(R * (N + P) * es), bar);
+        bulk_g2s(sl + L.om, omega_t + u * NP2, (uint32_t)(NP2 * 4), bar);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < nslots; ++s) tc::mbar_init(&bars[s], 1);
+        *sFail = 0;
+        tc::fence_mbar_init();
+        for (int s = 0; s < nslots; ++s) {
+            const int64_t u = first + s * step;
+            if (u < units) issue(u, s);
+        }
+    }
+    __syncthreads();
+
+    const int c4 = tid % P4, g = tid / P4;
+    // scalars of the first unit; later units' are prefetched one unit ahead
+    float d_n = 0.f, l_n = 0.f, a_n = 0.f;
+    if (first < units) {
+        d_n = dt_t[first];
+        l_n = lam_t[first];
+        a_n = A[first % H];
+    }
+    int it = 0;
+    for (int64_t u = first; u < units; u += step, ++it) {
+        const int slot = it % nslots;
+        const uint32_t parity = (uint32_t)((it / nslots) & 1);
+        const float d = d_n, l = l_n, a = a_n;
+        const int64_t un = u + step;
+        if (un < units) {
+            d_n = dt_t[un];
+            l_n = lam_t[un];
+            a_n = A[un % H];
+        }
+        if (!tc::mbar_wait(&bars[slot], parity, kStreamWaitNs)) *sFail = 1;
+        __syncthreads();
+        if (*sFail) break;
+        const uint8_t* sl = slots + slot * L.slot;
+        const IO* sBt = reinterpret_cast<const IO*>(sl + L.b);
+        const IO* sCt = reinterpret_cast<const IO*>(sl + L.c);
+        const IO* sXt = reinterpret_cast<const IO*>(sl + L.x);
+        const IO* sCa = reinterpret_cast<const IO*>(sl + L.ca);
+        const float* sOm = reinterpret_cast<const float*>(sl + L.om);
+        const float4* sSt4 = reinterpret_cast<const float4*>(sl + L.st);
+
+        const float alpha = expf(d * a);
+        const float beta = (1.0f - l) * d * alpha;
+        const float gamma = l * d;
+
+        float* sB2f = reinterpret_cast<float*>(sB2);
+        float* sBp2f = reinterpret_cast<float*>(sBp2);
+        float* sC2f = reinterpret_cast<float*>(sC2);
+        for (int i = tid; i < R * N; i += nt) {
+            const int r = i / N, n = i % N;
+            const int o = ((n >> 1) * R + r) * 2 + (n & 1);
+            sB2f[o] = ld_io(sBt, i);
+            sC2f[o] = ld_io(sCt, i);
+            sBp2f[o] = ld_io(sCa, i);
+        }
+        for (int i = tid; i < R * P; i += nt) {
+            sX[i] = ld_io(sXt, i);
+            sXp[i] = ld_io(sCa, R * N + i);
+        }
+        for (int j = tid; j < NP2; j += nt) {
+            float sn, cs;
+            sincosf(d * sOm[j], &sn, &cs);
+            sCS[j] = make_float2(cs, sn);
+        }
+        __syncthreads();
+        // new delayed-write cache: this token's B_t then X_t (raw io values)
+        IO* cb = cache + u * (int64_t)R * (N + P);
+        for (int i = tid; i < R * N; i += nt) cb[i] = sBt[i];
+        for (int i = tid; i < R * P; i += nt) cb[R * N + i] = sXt[i];
+
+        const float4* sX4 = reinterpret_cast<const float4*>(sX);
+        const float4* sXp4 = reinterpret_cast<const float4*>(sXp);
+        float4* st4 = reinterpret_cast<float4*>(state + u * (int64_t)N * P);
+        float4 acc[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = g; j < NP2; j += G) {
+            const float4 h0 = sSt4[(2 * j) * P4 + c4], h1 = sSt4[(2 * j + 1) * P4 + c4];
+            const float2 cs = sCS[j];
+            float4 w0 = make_float4(0.f, 0.f, 0.f, 0.f), w1 = w0;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float2 bp = sBp2[j * R + r];
+                const float4 xp = sXp4[r * P4 + c4];
+                w0 = fma4(bp.x, xp, w0);
+                w1 = fma4(bp.y, xp, w1);
+            }
+            const float4 u0 = fma4(alpha, h0, make_float4(beta * w0.x, beta * w0.y, beta * w0.z, beta * w0.w));
+            const float4 u1 = fma4(alpha, h1, make_float4(beta * w1.x, beta * w1.y, beta * w1.z, beta * w1.w));
+            float4 o0, o1;
+            rot2(cs.x, cs.y, u0.x, u1.x, o0.x, o1.x);
+            rot2(cs.x, cs.y, u0.y, u1.y, o0.y, o1.y);
+            rot2(cs.x, cs.y, u0.z, u1.z, o0.z, o1.z);
+            rot2(cs.x, cs.y, u0.w, u1.w, o0.w, o1.w);
+            float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float2 bc = sB2[j * R + r];
+                const float4 xc = sX4[r * P4 + c4];
+                v0 = fma4(bc.x, xc, v0);
+                v1 = fma4(bc.y, xc, v1);
+            }
+            o0 = fma4(gamma, v0, o0);
+            o1 = fma4(gamma, v1, o1);
+            st4[(2 * j) * P4 + c4] = o0;
+            st4[(2 * j + 1) * P4 + c4] = o1;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float2 cc = sC2[j * R + r];
+                acc[r] = fma4(cc.x, o0, fma4(cc.y, o1, acc[r]));
+            }
+        }
+        if (gpw > 1) {
+            for (int o = P4; o < 32; o <<= 1) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    acc[r].x += __shfl_xor_sync(0xffffffffu, acc[r].x, o);
+                    acc[r].y += __shfl_xor_sync(0xffffffffu, acc[r].y, o);
+                    acc[r].z += __shfl_xor_sync(0xffffffffu, acc[r].z, o);
+                    acc[r].w += __shfl_xor_sync(0xffffffffu, acc[r].w, o);
+                }
+            }
+        }
+        if (g % gpw == 0) {
+            float4* red4 = reinterpret_cast<float4*>(sRed) + (g / gpw) * (R * P4);
+#pragma unroll
+            for (int r = 0; r < R; ++r) red4[r * P4 + c4] = acc[r];
+        }
+        __syncthreads();   // readout partials written; every read of this slot done
+        if (tid == 0) {
+            const int64_t u3 = u + (int64_t)nslots * step;
+            if (u3 < units) issue(u3, slot);
+        }
+        IO* yb = y_t + u * R * P;
+        for (int o = tid; o < R * P; o += nt) {
+            float s = 0.f;
+            for (int gg = 0; gg < rows; ++gg) s += sRed[gg * (R * P) + o];
+            st_io(yb, o, s);
+        }
+        __syncthreads();   // sRed and the staged operands are free for the next unit
+    }
+    if (*sFail && tid == 0) {
+        atomicExch(&g_decode_status, (int)M3_ERR_TIMEOUT);
+        // let the copies still in flight land before the CTA's shared memory goes away (bounded)
+        int it2 = it;
+        for (int64_t u = first + (int64_t)it * step; u < units && it2 < it + nslots; u += step, ++it2)
+            (void)tc::mbar_wait(&bars[it2 % nslots], (uint32_t)((it2 / nslots) & 1), kStreamWaitNs);
+    }
+}
+
+bool stream_ok(int64_t P, int64_t N, int R, int es) {
+    if (N % 8) return false;
+    if ((R * N * es) % 16 || (R * P * es) % 16 || (R * (N + P) * es) % 16) return false;
+    return true;
+}
+
+size_t stream_smem(int64_t P, int64_t N, int R, int es, int G, int nslots) {
+    const StreamLayout L = stream_layout((int)N, (int)P, R, es);
+    const int P4 = (int)(P / 4);
+    const int gpw = (P4 < 32 && (P4 & (P4 - 1)) == 0 && (G * P4) % 32 == 0) ? 32 / P4 : 1;
+    const int rows = (G + gpw - 1) / gpw;
+    const size_t fixed = sizeof(float) * (size_t)(3 * R * N + N + 2 * R * P + (size_t)rows * R * P + 2);
+    return (size_t)nslots * L.slot + fixed + 8 * kMaxSlots + 16;
+}
+
+int device_sms() {
+    static int sms[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+    if (sms[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        sms[dev] = v;
+    }
+    return sms[dev];
 }
 
 struct DecodeShape {
@@ -149,12 +462,14 @@ struct DecodeShape {
 DecodeShape decode_shape(int64_t P, int64_t N, int R) {
     DecodeShape s{};
     const int P4 = (int)(P / 4), NP2 = (int)(N / 2);
-    int G = (NP2 + kMaxUnits - 1) / kMaxUnits;
-    const int want = 256 / P4 > 0 ? 256 / P4 : 1;
-    if (G < want) G = want < NP2 ? want : NP2;
+    int G = 256 / P4;
+    if (G > NP2) G = NP2;
+    if (G < 1) G = 1;
     s.G = G;
     s.threads = G * P4;
-    s.smem = sizeof(float) * (size_t)(3 * R * N + 2 * R * P + N + (size_t)s.threads * R * 4);
+    const int gpw = P4 < 32 ? 32 / P4 : 1;
+    const int rows = (G + gpw - 1) / gpw;
+    s.smem = sizeof(float) * (size_t)(3 * R * N + N + 2 * R * P + (size_t)rows * R * P);
     return s;
 }
 
@@ -163,13 +478,31 @@ cudaError_t launch_t(float* state, const void* x_t, const void* B_t, void* cache
                      const float* dt_t, const float* A, const float* lambda_t, const float* omega_t, void* y_t,
                      int64_t batch, int64_t nheads, int64_t P, int64_t N, cudaStream_t stream) {
     const DecodeShape s = decode_shape(P, N, R);
+    const int64_t units = batch * nheads;
+    const int es = (int)sizeof(IO);
+    if (stream_ok(P, N, R, es)) {
+        // two CTAs per SM: at most ~110 KB of shared memory each
+        int nslots = kMaxSlots;
+        size_t smem = stream_smem(P, N, R, es, s.G, nslots);
+        if (smem > 110 * 1024) smem = stream_smem(P, N, R, es, s.G, nslots = 2);
+        if (smem <= 110 * 1024) {
+            auto kern = decode_stream_kernel<IO, R>;
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            int64_t grid = 2 * (int64_t)device_sms();
+            if (grid > units) grid = units;
+            kern<<<(unsigned)grid, s.threads, smem, stream>>>(
+                state, (const IO*)x_t, (const IO*)B_t, (IO*)cache, (const IO*)C_t, dt_t, A, lambda_t, omega_t,
+                (IO*)y_t, (int)nheads, (int)P, (int)N, s.G, units, nslots);
+            return cudaGetLastError();
+        }
+    }
     auto kern = decode_kernel<IO, R>;
     if (s.smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s.smem);
         if (e != cudaSuccess) return e;
     }
-    const int64_t blocks = batch * nheads;
-    kern<<<(unsigned)blocks, s.threads, s.smem, stream>>>(
+    kern<<<(unsigned)units, s.threads, s.smem, stream>>>(
         state, (const IO*)x_t, (const IO*)B_t, (IO*)cache, (const IO*)C_t, dt_t, A, lambda_t, omega_t, (IO*)y_t,
         (int)nheads, (int)P, (int)N, s.G);
     return cudaGetLastError();
@@ -198,8 +531,7 @@ bool decode_supported(int64_t headdim, int64_t dstate, int R) {
     if (headdim % 4 || headdim < 4 || headdim > 256) return false;
     if (dstate % 2 || dstate < 2 || dstate > 256) return false;
     const DecodeShape s = decode_shape(headdim, dstate, R);
-    if (s.threads > 512) return false;
-    if ((int64_t)s.G * kMaxUnits < dstate / 2) return false;
+    if (s.threads > 256) return false;
     return s.smem <= 200 * 1024;
 }
 
@@ -213,6 +545,16 @@ cudaError_t launch_decode(float* state, const void* x_t, const void* B_t, void* 
                                         nheads, headdim, dstate, stream);
     return launch_io<float>(R, state, x_t, B_t, cache, C_t, dt_t, A, lambda_t, omega_t, y_t, batch, nheads,
                             headdim, dstate, stream);
+}
+
+int decode_device_status(int clear) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_decode_status, sizeof(int)) != cudaSuccess) return M3_ERR_CUDA;
+    if (clear && v != 0) {
+        const int z = 0;
+        if (cudaMemcpyToSymbol(g_decode_status, &z, sizeof(int)) != cudaSuccess) return M3_ERR_CUDA;
+    }
+    return v;
 }
 
 }  // namespace m3

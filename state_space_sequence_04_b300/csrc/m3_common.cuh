@@ -54,6 +54,7 @@ cudaError_t launch_decode(float* state, const void* x_t, const void* B_t, void* 
                           void* y_t, int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R,
                           int io, cudaStream_t stream);
 bool decode_supported(int64_t headdim, int64_t dstate, int R);
+int decode_device_status(int clear);
 
 cudaError_t launch_state_passing(float* chunk_states, const float* chunk_logdecay, const float* chunk_angle,
                                  const float* init_state, float* final_state, int64_t batch, int64_t nheads,

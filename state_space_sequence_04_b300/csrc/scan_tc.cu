@@ -9,28 +9,41 @@
 // c = tokens [c0, c0+Q) (rows ordered (token, rank), QR = Q*R <= 128):
 //
 //   coefficients   l_t = dt_t A, cum_t = sum_{k<=t} l_k (chunk-local),
-//                  gamma_t = lambda_t dt_t, w_s = gamma_s + (1-lambda_{s+1}) dt_{s+1}
+//                  gamma_t = lambda_t dt_t, w_s = gamma_s + (1-lambda_{s+1}) dt_{s+1},
+//                  rho_t = gamma_t / w_t (0 when w_t = 0; w_t >= gamma_t >= 0)
 //   rotation       Psi_t = sum_{k<=t} dt_k omega_k (chunk-local),
-//                  B~ = R(-Psi) B, C~ = R(-Psi) C, in place in shared memory
-//   MMA1           S = C~ B~^T                                (TMEM, fp32)
-//   mask           SL_ts = S_ts exp(cum_t - cum_s) (t == s ? gamma_t : w_s), s <= t
-//   MMA2, MMA4     Y = SL X + (exp(cum_t) C~) H_{c-1}          (TMEM, fp32)
-//   MMA3           U = (exp(cum_end - cum_s) w_s B~)^T X        (TMEM, fp32)
-//   state          H_c = R(Theta_c) (exp(cum_end) H_{c-1} + U),  Theta_c = Psi_end
-//                  (U is in the chunk's rotating frame; the rotation commutes
-//                  with the scalar decay, so one rotation serves both terms)
+//                  C~ = R(-Psi) C,  B' = w R(-Psi) B   (in place in shared memory)
+//                  X^ = exp(cum_end - cum_s) X          (separate buffer)
+//   batch 1        S  = C~ B'^T                       (= S_ts w_s)
+//                  Yi = C~ Hb_{c-1}                    (inter-chunk readout)
+//                  H += B'^T X^                        (chunk state onto the carry)
+//   mask           SL_ts = S_ts exp(cum_t - cum_s) for s < t, S_tt rho_t, 0 for s > t
+//   batch 2        Y  = SL X
+//   state          H_c = exp(cum_end(c+1)) R(Theta_c) H,  Hb_c = bf16(R(Theta_c) H)
+//   output         y_t = Y_t + exp(cum_t) Yi_t
 //
-// H is the physical-frame state plus the pending delayed write of the
-// chunk's last token (its w uses the next token's lambda, dt; zero past the
-// end), so H after the last chunk is the true final state h_{T-1}.
+// The carry H entering batch 1 of chunk c is exp(cum_end(c)) R(Theta_{c-1}) H_{c-1}
+// (the decay of chunk c applied ahead of time by the previous state step), so
+// that the chunk-state MMA accumulates straight onto it and
+// H_c = R(Theta_c) (exp(cum_end) H_{c-1} + U_c) needs one pass over TMEM.
+// H is the physical-frame state plus the pending delayed write of the chunk's
+// last token (its w uses the next token's lambda, dt; zero past the end), so
+// H after the last chunk is the true final state h_{T-1}.
+//
+// Warp roles (256 threads): warps 0-3 "consumer" (mask, state, output; thread
+// 0 issues every MMA and TMA), warps 4-7 "rotate" (coefficients, angles,
+// rotation, X^), which run one chunk ahead of the consumer on the other
+// shared-memory stage.  Every wait is bounded: on timeout the kernel records
+// M3_ERR_TIMEOUT in the status word, drains its copies and MMAs and exits.
 //
 // MMA operand layouts (all 128-byte swizzled, bf16):
-//   C~, C~'  A, K-major  (rows (t,r), K = n)     B~  B, K-major (rows (s,r), K = n)
-//   SL       A, K-major  (rows (t,r), K = (s,r')) X   B, MN-major (K = (s,r'), N = p)
-//   Hb       B, MN-major (K = n, N = p)          B^  A, MN-major (M = n, K = (s,r'))
+//   C~   A, K-major  (rows (t,r), K = n)     B'  B, K-major (rows (s,r), K = n)
+//   SL   A, K-major  (rows (t,r), K = (s,r')) X   B, MN-major (K = (s,r'), N = p)
+//   Hb   B, MN-major (K = n, N = p)          B'^T A, MN-major (M = n, K = (s,r'))
+//   X^   B, MN-major (K = (s,r'), N = p)
 // When QR = 64 the MMAs still run with M = 128; rows 64..127 read the next
 // 8 KB of shared memory (always inside this CTA's allocation) and their
-// results are never read.
+// results are never read.  SL is written over C~ (dead once batch 1 is done).
 #include <cuda.h>
 
 #include "m3_common.cuh"
@@ -42,6 +55,7 @@ namespace {
 using namespace tc;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait, then give up with M3_ERR_TIMEOUT
+constexpr float kLog2e = 1.4426950408889634f;
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
@@ -50,41 +64,40 @@ struct Cfg {
     static constexpr int P = 64;                 // head dim (one 128-byte swizzle panel of bf16)
     static constexpr int QR = Q * R;             // rows of the chunk
     static constexpr int NPAN = NS / 64;         // 64-wide panels of B / C
-    static constexpr int kThreads = 128;
+    static constexpr int kThreads = 256;
     static_assert(QR == 64 || QR == 128, "chunk rows must be 64 or 128");
     static_assert(NS == 64 || NS == 128, "state size must be 64 or 128");
     static_assert(Q <= 128, "chunk too long");
 
     static constexpr int X_BYTES = QR * 128;
     static constexpr int BC_BYTES = NPAN * QR * 128;
-    static constexpr int SC_BYTES = 16 * (Q + 1);          // dt / lambda box {4 heads, Q+1 tokens}
-    static constexpr int OFF_C = 0;
-    static constexpr int OFF_B = OFF_C + BC_BYTES;
-    static constexpr int OFF_X = OFF_B + BC_BYTES;
-    static constexpr int OFF_DT = OFF_X + X_BYTES;
-    static constexpr int OFF_LAM = OFF_DT + align_up(SC_BYTES, 128);
-    static constexpr int STAGE = align_up(OFF_LAM + align_up(SC_BYTES, 128), 1024);
-    static constexpr int TX_BYTES = X_BYTES + 2 * BC_BYTES + 2 * SC_BYTES;
-
-    static constexpr int OFF_SL = 2 * STAGE;
-    static constexpr int SL_BYTES = (QR / 64) * QR * 128;
-    static constexpr int OFF_HB = OFF_SL + SL_BYTES;
-    static constexpr int HB_BYTES = NS * 128;
-    static constexpr int OFF_SMALL = OFF_HB + HB_BYTES;
-    // small arrays (floats): cum[Q], gam[Q], w[Q], warp sums[4], theta[NS/2]
-    static constexpr int TG = kThreads / (NS / 8);          // token groups of the rotation phase
-    static constexpr int TPG = Q / TG;                      // tokens per group
+    static constexpr int STG_TILE = 2 * BC_BYTES + X_BYTES;      // C | B | X of one stage
+    static constexpr int BOX_BYTES = 16 * (Q + 1);                // dt / lambda box {4 heads, Q+1 tokens}
+    static constexpr int BOX_STRIDE = align_up(BOX_BYTES, 128);
+    static constexpr int OFF_XHAT = 2 * STG_TILE;
+    static constexpr int OFF_HB = OFF_XHAT + X_BYTES;
+    static constexpr int OFF_BOX = OFF_HB + NS * 128;             // [stage][dt | lambda]
+    // rotate-phase mapping: pair group jg (4 pairs = 16 bytes of a row), token group tg
+    static constexpr int NG = NS / 8;
+    static constexpr int TG = 128 / NG;
+    static constexpr int TPG = Q / TG;
     static_assert(Q % TG == 0, "tokens must split evenly over token groups");
-    // the rotation phase's partial angle sums [TG][NS/2] live in the SL buffer (free at that point)
-    static_assert(TG * (NS / 2) * 4 <= SL_BYTES, "partial angle sums must fit in the SL buffer");
-    static constexpr int SMALL_FLOATS = 3 * Q + 4 + NS / 2;
-    static constexpr int OFF_BAR = align_up(OFF_SMALL + 4 * SMALL_FLOATS, 16);
-    static constexpr int SMEM = OFF_BAR + 64 + 1024;        // barriers, tmem slot, alignment slack
+    static constexpr int OFF_PART = OFF_BOX + 4 * BOX_STRIDE;     // [TG][NS/2] partial angle sums
+    static constexpr int OFF_RPRIV = OFF_PART + TG * (NS / 2) * 4;   // w[Q], f[Q], warp sums[4]
+    static constexpr int OFF_BAR = align_up(OFF_RPRIV + (2 * Q + 4) * 4, 16);
+    static constexpr int SMEM = OFF_BAR + 128 + 1024;             // barriers / flags, alignment slack
+    // two CTAs per SM when both fit (228 KB per SM, 1 KB reserved per CTA)
+    static constexpr int MIN_BLOCKS = 2 * (SMEM + 1024) <= 233472 ? 2 : 1;
+    static constexpr int TX_BYTES = X_BYTES + 2 * BC_BYTES + 2 * BOX_BYTES;
+
+    // coefficient block the consumer reads, written over the lambda box once read
+    static constexpr int CO_CUM2 = 0, CO_RHO = Q, CO_ECUM = 2 * Q, CO_THETA = 3 * Q, CO_EEND = 3 * Q + NS / 2;
+    static_assert((3 * Q + NS / 2 + 1) * 4 <= BOX_BYTES, "coefficient block must fit in the lambda box");
 
     // TMEM columns
     static constexpr int T_S = 0;
-    static constexpr int T_Y = QR;
-    static constexpr int T_U = QR + P;
+    static constexpr int T_YI = QR;
+    static constexpr int T_Y = QR + P;
     static constexpr int T_H = QR + 2 * P;
     static constexpr int TMEM_COLS = (QR + 3 * P) <= 256 ? 256 : 512;
 };
@@ -98,47 +111,101 @@ struct TcArgs {
     int T, H, nc;
 };
 
+// Shared control block (after the barriers).
+struct Ctl {
+    uint64_t full[2];        // TMA stage landed
+    uint64_t rot_done[2];    // rotate group finished the stage (count 128)
+    uint64_t coef_ready[2];  // coefficient block of the stage written (count 128)
+    uint64_t b1;             // MMA batch 1 complete
+    uint64_t b2;             // MMA batch 2 complete
+    uint32_t tmem;
+    int fail_c, fail_r;      // per-group failure flags
+    int tma_issued[2];       // loads issued per stage (consumer thread 0)
+    int tma_waited[2];       // loads waited for per stage (rotate group)
+    int b1_issued, b2_issued, b1_waited, b2_waited;
+};
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&v);
 }
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
-    return __bfloat1622float2(v);
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void group_bar(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
+// Bounded wait on an mbarrier phase.  Gives up (setting *mine) on timeout or
+// when either group has already failed.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* mine,
+                                             volatile int* other) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*mine || *other || globaltimer_ns() - t0 > kWaitLimitNs) {
+                *mine = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Rotate the 4 pairs of one 16-byte piece by (c[k], s[k]) (angle -Psi), optionally
+// scaling by wt, in place; fp32 arithmetic on packed pairs of pairs.
+__device__ __forceinline__ uint4 rotate4(uint4 v, const float2 (&c01)[2], const float2 (&s01)[2]) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float2 a = make_float2(bf_lo(w[2 * h]), bf_lo(w[2 * h + 1]));
+        const float2 b = make_float2(bf_hi(w[2 * h]), bf_hi(w[2 * h + 1]));
+        // a' = c a - s b ; b' = s a + c b
+        const float2 na = __ffma2_rn(c01[h], a, __fmul2_rn(make_float2(-s01[h].x, -s01[h].y), b));
+        const float2 nb = __ffma2_rn(s01[h], a, __fmul2_rn(c01[h], b));
+        w[2 * h] = pack_bf16(na.x, nb.x);
+        w[2 * h + 1] = pack_bf16(na.y, nb.y);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 template <int NS, int R, int Q>
-__global__ void __launch_bounds__(128, 2) scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+__global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                          const __grid_constant__ CUtensorMap tm_B,
                                                          const __grid_constant__ CUtensorMap tm_C,
                                                          const __grid_constant__ CUtensorMap tm_dt,
                                                          const __grid_constant__ CUtensorMap tm_lam, TcArgs args) {
     using K = Cfg<NS, R, Q>;
-    constexpr int P = K::P, QR = K::QR, NP2 = NS / 2, NG = NS / 8, TG = K::TG, TPG = K::TPG;
+    constexpr int P = K::P, QR = K::QR, NP2 = NS / 2, NG = K::NG, TG = K::TG, TPG = K::TPG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* sCum = reinterpret_cast<float*>(sm + K::OFF_SMALL);
-    float* sGam = sCum + Q;
-    float* sW = sGam + Q;
-    float* sWarp = sW + Q;
-    float* sTheta = sWarp + 4;           // [NS/2]
-    float* sPart = reinterpret_cast<float*>(sm + K::OFF_SL);   // [TG][NS/2], before SL is written
-    uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + K::OFF_BAR);   // [2]
-    uint64_t* bar_mma = bar_full + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
-    int* sFail = reinterpret_cast<int*>(tmem_slot + 1);
+    Ctl* ctl = reinterpret_cast<Ctl*>(sm + K::OFF_BAR);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x;
-    const int b = bh / args.H, h = bh % args.H;
+    const int b = bh / args.H, h = bh % args.H, hq = h & 3;
     const int T = args.T, nc = args.nc;
-    const float a = args.A[h];
+
+    auto tile_c = [&](int s) { return sm + s * K::STG_TILE; };
+    auto tile_b = [&](int s) { return sm + s * K::STG_TILE + K::BC_BYTES; };
+    auto tile_x = [&](int s) { return sm + s * K::STG_TILE + 2 * K::BC_BYTES; };
+    auto box_dt = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_BOX + (2 * s) * K::BOX_STRIDE); };
+    auto box_lam = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_BOX + (2 * s + 1) * K::BOX_STRIDE); };
+    uint8_t* xhat = sm + K::OFF_XHAT;
+    uint8_t* hb = sm + K::OFF_HB;
 
     if (tid == 0) {
-        mbar_init(&bar_full[0], 1);
-        mbar_init(&bar_full[1], 1);
-        mbar_init(bar_mma, 1);
-        *sFail = 0;
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->rot_done[s], 128);
+            mbar_init(&ctl->coef_ready[s], 128);
+            ctl->tma_issued[s] = 0;
+            ctl->tma_waited[s] = 0;
+        }
+        mbar_init(&ctl->b1, 1);
+        mbar_init(&ctl->b2, 1);
+        ctl->fail_c = 0;
+        ctl->fail_r = 0;
+        ctl->b1_issued = ctl->b2_issued = ctl->b1_waited = ctl->b2_waited = 0;
         fence_mbar_init();
         prefetch_tensormap(&tm_x);
         prefetch_tensormap(&tm_B);
@@ -147,340 +214,257 @@ __global__ void __launch_bounds__(128, 2) scan_tc_kernel(const __grid_constant__
         prefetch_tensormap(&tm_lam);
     }
     __syncthreads();
-    if (warp == 0) {
-        tmem_alloc(tmem_slot, K::TMEM_COLS);
-        tmem_relinquish();
-    }
 
-    auto issue_loads = [&](int c, int s) {
-        uint8_t* st = sm + s * K::STAGE;
+    auto issue_loads = [&](int c, int s) {   // consumer thread 0 only
         const int c0 = c * Q;
-        mbar_arrive_expect_tx(&bar_full[s], K::TX_BYTES);
+        mbar_arrive_expect_tx(&ctl->full[s], K::TX_BYTES);
 #pragma unroll
         for (int p = 0; p < K::NPAN; ++p) {
-            tma_load_5d(st + K::OFF_C + p * QR * 128, &tm_C, &bar_full[s], 64 * p, 0, h, c0, b);
-            tma_load_5d(st + K::OFF_B + p * QR * 128, &tm_B, &bar_full[s], 64 * p, 0, h, c0, b);
+            tma_load_5d(tile_c(s) + p * QR * 128, &tm_C, &ctl->full[s], 64 * p, 0, h, c0, b);
+            tma_load_5d(tile_b(s) + p * QR * 128, &tm_B, &ctl->full[s], 64 * p, 0, h, c0, b);
         }
-        tma_load_5d(st + K::OFF_X, &tm_x, &bar_full[s], 0, 0, h, c0, b);
-        tma_load_3d(st + K::OFF_DT, &tm_dt, &bar_full[s], h & ~3, c0, b);
-        tma_load_3d(st + K::OFF_LAM, &tm_lam, &bar_full[s], h & ~3, c0, b);
+        tma_load_5d(tile_x(s), &tm_x, &ctl->full[s], 0, 0, h, c0, b);
+        tma_load_3d(box_dt(s), &tm_dt, &ctl->full[s], h & ~3, c0, b);
+        tma_load_3d(box_lam(s), &tm_lam, &ctl->full[s], h & ~3, c0, b);
+        ctl->tma_issued[s] += 1;
     };
-    // chunk whose loads are in flight into each stage (-1: none), for the bounded drain on failure
-    int inflight[2] = {-1, -1};
+
+    if (warp == 0) {
+        tmem_alloc(&ctl->tmem, K::TMEM_COLS);
+        tmem_relinquish();
+    }
     if (tid == 0) {
-        if (nc > 0) issue_loads(0, 0);
+        issue_loads(0, 0);
         if (nc > 1) issue_loads(1, 1);
     }
-    if (nc > 0) inflight[0] = 0;
-    if (nc > 1) inflight[1] = 1;
-
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t tmem = ctl->tmem;
+    volatile int* fail_c = &ctl->fail_c;
+    volatile int* fail_r = &ctl->fail_r;
 
-    // H_{-1} = 0
-    if (tid < NS) {
-        float z[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) z[i] = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < P; cc += 16) tmem_st16(tlane + K::T_H + cc, z);
-        tmem_st_wait();
-    }
-
-    // rotation-phase mapping: pair group jg (4 pairs = 16 bytes of a row), token group tg
-    const int jg = tid % NG, tg = tid / NG;
-    const int pan = jg / 8, cib = (jg % 8) * 16;     // panel and byte-in-row of my 16-byte piece
-    const float* om_base = args.omega + ((int64_t)b * T * args.H + h) * NP2 + 4 * jg;
-    const int64_t om_tok = (int64_t)args.H * NP2;
-    float4 om[TPG];
-    auto load_omega = [&](int c) {
-#pragma unroll
-        for (int i = 0; i < TPG; ++i) {
-            const int t = c * Q + tg * TPG + i;
-            om[i] = t < T ? *reinterpret_cast<const float4*>(om_base + t * om_tok) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-    if (nc > 0) load_omega(0);
-
-    uint32_t mma_phase = 0;
-    bool failed = false;
-    for (int c = 0; c < nc; ++c) {
-        const int s = c & 1;
-        uint8_t* st = sm + s * K::STAGE;
-        const float* sDt = reinterpret_cast<const float*>(st + K::OFF_DT);
-        const float* sLam = reinterpret_cast<const float*>(st + K::OFF_LAM);
-        if (!mbar_wait(&bar_full[s], (c >> 1) & 1, kWaitLimitNs)) *sFail = 1;
-        __syncthreads();
-        if (*sFail) { failed = true; break; }
-        inflight[s] = -1;
-
-        // ---- coefficients and chunk-local log-decay prefix
-        const int hq = h & 3;
+    if (warp < 4) {
+        // =============================== consumer ===============================
+        const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+        // H_{-1} = 0 (TMEM) and Hb_{-1} = 0 (shared)
         {
-            float ell = 0.f, gam = 0.f, wv = 0.f;
-            if (tid < Q) {
-                const float d = sDt[tid * 4 + hq], l = sLam[tid * 4 + hq];
-                const float dn = sDt[(tid + 1) * 4 + hq], ln = sLam[(tid + 1) * 4 + hq];
-                ell = d * a;
-                gam = l * d;
-                wv = gam + (1.f - ln) * dn;
-            }
-            float v = warp_inclusive_sum(ell);
-            if (lane == 31) sWarp[warp] = v;
-            __syncthreads();
-            float off = 0.f;
-            for (int i = 0; i < warp; ++i) off += sWarp[i];
-            if (tid < Q) {
-                sCum[tid] = v + off;
-                sGam[tid] = gam;
-                sW[tid] = wv;
-            }
-        }
-        // ---- rotation angles: partial sums per token group
-        float dtk[TPG];
-        {
-            float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+            float z[16];
 #pragma unroll
-            for (int i = 0; i < TPG; ++i) {
-                const float d = sDt[(tg * TPG + i) * 4 + hq];
-                dtk[i] = d;
-                part.x = fmaf(d, om[i].x, part.x);
-                part.y = fmaf(d, om[i].y, part.y);
-                part.z = fmaf(d, om[i].z, part.z);
-                part.w = fmaf(d, om[i].w, part.w);
-            }
-            *reinterpret_cast<float4*>(&sPart[tg * NP2 + 4 * jg]) = part;
-        }
-        __syncthreads();
-        {
-            float4 psi = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int g = 0; g < tg; ++g) {
-                const float4 p4 = *reinterpret_cast<const float4*>(&sPart[g * NP2 + 4 * jg]);
-                psi.x += p4.x; psi.y += p4.y; psi.z += p4.z; psi.w += p4.w;
-            }
+            for (int i = 0; i < 16; ++i) z[i] = 0.f;
 #pragma unroll
-            for (int i = 0; i < TPG; ++i) {
-                const int t = tg * TPG + i;
-                psi.x = fmaf(dtk[i], om[i].x, psi.x);
-                psi.y = fmaf(dtk[i], om[i].y, psi.y);
-                psi.z = fmaf(dtk[i], om[i].z, psi.z);
-                psi.w = fmaf(dtk[i], om[i].w, psi.w);
-                float cs[4], sn[4];
-                __sincosf(-psi.x, &sn[0], &cs[0]);
-                __sincosf(-psi.y, &sn[1], &cs[1]);
-                __sincosf(-psi.z, &sn[2], &cs[2]);
-                __sincosf(-psi.w, &sn[3], &cs[3]);
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int row = t * R + r;
-                    const uint32_t off = pan * QR * 128 + sw128_offset(row, cib);
-#pragma unroll
-                    for (int m = 0; m < 2; ++m) {   // m = 0: C, m = 1: B
-                        uint4* p = reinterpret_cast<uint4*>(st + (m == 0 ? K::OFF_C : K::OFF_B) + off);
-                        uint4 v = *p;
-                        uint32_t wv4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = unpack_bf16(wv4[e]);
-                            float o0, o1;
-                            rot2(cs[e], sn[e], f.x, f.y, o0, o1);
-                            wv4[e] = pack_bf16(o0, o1);
-                        }
-                        *p = make_uint4(wv4[0], wv4[1], wv4[2], wv4[3]);
-                    }
-                }
-            }
-            if (tg == TG - 1) *reinterpret_cast<float4*>(&sTheta[4 * jg]) = psi;
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-
-        // ---- MMA1: S = C~ B~^T
-        if (tid == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, QR, false, false);
-            const uint32_t aC = smem_u32(st + K::OFF_C), aB = smem_u32(st + K::OFF_B);
-#pragma unroll
-            for (int kk = 0; kk < NS / 16; ++kk) {
-                const uint32_t koff = (kk >> 2) * QR * 128 + (kk & 3) * 32;
-                mma_bf16_ss(tmem + K::T_S, smem_desc(aC + koff, 16, 1024, kSwizzle128B),
-                            smem_desc(aB + koff, 16, 1024, kSwizzle128B), idesc, kk > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        // overlap: next chunk's omega, and H_{c-1} -> bf16 operand
-        if (c + 1 < nc) load_omega(c + 1);
-        if (tid < NS) {
-            uint8_t* hb = sm + K::OFF_HB;
-#pragma unroll
-            for (int cc = 0; cc < P; cc += 16) {
-                float v[16];
-                tmem_ld16(tlane + K::T_H + cc, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8) {
-                    uint4 pk = make_uint4(pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]), pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]),
-                                          pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
-                    *reinterpret_cast<uint4*>(hb + sw128_offset(tid, (cc + q8 * 8) * 2)) = pk;
-                }
-            }
-        }
-        if (!mbar_wait(bar_mma, mma_phase, kWaitLimitNs)) *sFail = 1;
-        mma_phase ^= 1;
-        tc_fence_after();
-
-        // ---- mask: SL = S o L (bf16, K-major rows (t,r))
-        if (tid < QR) {
-            const int t = tid / R;
-            const float ct = sCum[t], gt = sGam[t];
-            uint8_t* sl = sm + K::OFF_SL;
-#pragma unroll
-            for (int cc = 0; cc < QR; cc += 16) {
-                float v[16];
-                tmem_ld16(tlane + K::T_S + cc, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int sidx = (cc + i) / R;
-                    float m = 0.f;
-                    if (sidx < t) m = __expf(ct - sCum[sidx]) * sW[sidx];
-                    else if (sidx == t) m = gt;
-                    v[i] *= m;
-                }
-#pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8) {
-                    const int col = cc + q8 * 8;
-                    uint4 pk = make_uint4(pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]), pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]),
-                                          pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
-                    *reinterpret_cast<uint4*>(sl + (col / 64) * QR * 128 + sw128_offset(tid, (col % 64) * 2)) = pk;
-                }
-            }
-        }
-        // ---- scale in place: C~' = exp(cum_t) C~ ; B^ = exp(cum_end - cum_s) w_s B~
-        {
-            const float cend = sCum[Q - 1];
-#pragma unroll
-            for (int i = 0; i < TPG; ++i) {
-                const int t = tg * TPG + i;
-                const float fc = __expf(sCum[t]);
-                const float fb = __expf(cend - sCum[t]) * sW[t];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const uint32_t off = pan * QR * 128 + sw128_offset(t * R + r, cib);
-#pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const float f = m == 0 ? fc : fb;
-                        uint4* p = reinterpret_cast<uint4*>(st + (m == 0 ? K::OFF_C : K::OFF_B) + off);
-                        uint4 v = *p;
-                        uint32_t wv4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 g = unpack_bf16(wv4[e]);
-                            wv4[e] = pack_bf16(g.x * f, g.y * f);
-                        }
-                        *p = make_uint4(wv4[0], wv4[1], wv4[2], wv4[3]);
-                    }
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (*sFail) { failed = true; break; }
-
-        // ---- MMA2 + MMA4 -> Y ; MMA3 -> U
-        if (tid == 0) {
-            const uint32_t aSL = smem_u32(sm + K::OFF_SL), aX = smem_u32(st + K::OFF_X);
-            const uint32_t aC = smem_u32(st + K::OFF_C), aHb = smem_u32(sm + K::OFF_HB);
-            const uint32_t aB = smem_u32(st + K::OFF_B);
-            constexpr uint32_t id_y = idesc_bf16_f32(128, P, false, true);
-            constexpr uint32_t id_u = idesc_bf16_f32(128, P, true, true);
-#pragma unroll
-            for (int kk = 0; kk < QR / 16; ++kk) {   // Y = SL X
-                const uint32_t koff = (kk >> 2) * QR * 128 + (kk & 3) * 32;
-                mma_bf16_ss(tmem + K::T_Y, smem_desc(aSL + koff, 16, 1024, kSwizzle128B),
-                            smem_desc(aX + kk * 2048, 16, 1024, kSwizzle128B), id_y, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < NS / 16; ++kk) {   // Y += C~' Hb
-                const uint32_t koff = (kk >> 2) * QR * 128 + (kk & 3) * 32;
-                mma_bf16_ss(tmem + K::T_Y, smem_desc(aC + koff, 16, 1024, kSwizzle128B),
-                            smem_desc(aHb + kk * 2048, 16, 1024, kSwizzle128B), id_y, 1);
-            }
-            // U = B^^T X : A is MN-major over n (NS rows; panels QR*128 bytes apart)
-            // (NS = 64: the second panel reads the next QR*128 bytes, results unused)
-            constexpr uint32_t lbo_u = QR * 128;
-#pragma unroll
-            for (int kk = 0; kk < QR / 16; ++kk) {
-                mma_bf16_ss(tmem + K::T_U, smem_desc(aB + kk * 2048, lbo_u, 1024, kSwizzle128B),
-                            smem_desc(aX + kk * 2048, 16, 1024, kSwizzle128B), id_u, kk > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        if (!mbar_wait(bar_mma, mma_phase, kWaitLimitNs)) *sFail = 1;
-        mma_phase ^= 1;
-        tc_fence_after();
-        __syncthreads();
-        if (*sFail) { failed = true; break; }
-        // the stage is free again: prefetch chunk c+2 into it
-        if (tid == 0 && c + 2 < nc) issue_loads(c + 2, s);
-        if (c + 2 < nc) inflight[s] = c + 2;
-
-        // ---- state update H_c = R(Theta) (exp(cum_end) H_{c-1} + U)   (thread = state row n)
-        if (tid < NS) {
-            const float e = __expf(sCum[Q - 1]);
-            float sn, cs;
-            sincosf(sTheta[tid >> 1], &sn, &cs);
-            const bool odd = tid & 1;
-#pragma unroll
-            for (int cc = 0; cc < P; cc += 16) {
-                float hv[16], uv[16];
-                tmem_ld16(tlane + K::T_H + cc, hv);
-                tmem_ld16(tlane + K::T_U + cc, uv);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float pre = fmaf(e, hv[i], uv[i]);
-                    const float other = __shfl_xor_sync(0xffffffffu, pre, 1);
-                    // even row 2j: cos*v_2j - sin*v_2j+1 ; odd row 2j+1: sin*v_2j + cos*v_2j+1
-                    hv[i] = odd ? fmaf(sn, other, cs * pre) : fmaf(-sn, other, cs * pre);
-                }
-                tmem_st16(tlane + K::T_H + cc, hv);
-            }
+            for (int cc = 0; cc < P; cc += 16) tmem_st16(tlane + K::T_H + cc, z);
             tmem_st_wait();
-        }
-        // ---- outputs y rows (t, r)
-        if (tid < QR) {
-            const int t = tid / R, r = tid % R;
-            const int tok = c * Q + t;
-            __nv_bfloat16* yrow = args.y + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P;
-#pragma unroll
-            for (int cc = 0; cc < P; cc += 16) {
-                float v[16];
-                tmem_ld16(tlane + K::T_Y + cc, v);
-                tmem_ld_wait();
-                if (tok < T) {
-                    uint4 p0 = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
-                                          pack_bf16(v[6], v[7]));
-                    uint4 p1 = make_uint4(pack_bf16(v[8], v[9]), pack_bf16(v[10], v[11]), pack_bf16(v[12], v[13]),
-                                          pack_bf16(v[14], v[15]));
-                    *reinterpret_cast<uint4*>(yrow + cc) = p0;
-                    *reinterpret_cast<uint4*>(yrow + cc + 8) = p1;
-                }
-            }
+            uint4* hb4 = reinterpret_cast<uint4*>(hb);
+            for (int i = tid; i < NS * 128 / 16; i += 128) hb4[i] = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
         }
         tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    }
+        group_bar(1);
+        const bool odd = tid & 1;
+        for (int c = 0; c < nc; ++c) {
+            const int s = c & 1;
+            const float* co = box_lam(s);
+            // ---- batch 1 once the rotate group has finished this stage
+            (void)wait_bounded(&ctl->rot_done[s], (c >> 1) & 1, fail_c, fail_r);
+            tc_fence_before();
+            group_bar(1);
+            if (*fail_c) break;
+            if (tid == 0) {
+                tc_fence_after();
+                // descriptors of the operand bases; a byte offset o moves the start address field by o >> 4
+                const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
+                const uint64_t dB = smem_desc(smem_u32(tile_b(s)), 16, 1024, kSwizzle128B);
+                const uint64_t dBt = smem_desc(smem_u32(tile_b(s)), QR * 128, 1024, kSwizzle128B);
+                const uint64_t dX = smem_desc(smem_u32(xhat), 16, 1024, kSwizzle128B);
+                const uint64_t dHb = smem_desc(smem_u32(hb), 16, 1024, kSwizzle128B);
+                constexpr uint32_t id_s = idesc_bf16_f32(128, QR, false, false);
+                constexpr uint32_t id_y = idesc_bf16_f32(128, P, false, true);
+                constexpr uint32_t id_u = idesc_bf16_f32(128, P, true, true);
+#pragma unroll
+                for (int kk = 0; kk < NS / 16; ++kk) {   // S = C~ B'^T
+                    const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
+                    mma_bf16_ss(tmem + K::T_S, dC + ko, dB + ko, id_s, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < NS / 16; ++kk) {   // Yi = C~ Hb_{c-1}
+                    const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
+                    mma_bf16_ss(tmem + K::T_YI, dC + ko, dHb + kk * (2048 >> 4), id_y, kk > 0);
+                }
+                // H += B'^T X^ : A is MN-major over n (NS rows; panels QR*128 bytes apart)
+                // (NS = 64: the second panel reads the next QR*128 bytes, results unused)
+#pragma unroll
+                for (int kk = 0; kk < QR / 16; ++kk)
+                    mma_bf16_ss(tmem + K::T_H, dBt + kk * (2048 >> 4), dX + kk * (2048 >> 4), id_u, 1);
+                mma_commit(&ctl->b1);
+                ctl->b1_issued += 1;
+            }
+            (void)wait_bounded(&ctl->b1, c & 1, fail_c, fail_r);
+            tc_fence_after();
 
-    if (!failed) {
-        if (args.final_state != nullptr && tid < NS) {
+            // ---- mask: SL = S o L (bf16, K-major rows (t,r)) over the dead C~ tile.
+            // 16-column blocks strictly below the diagonal use the factorised decay
+            // 2^(cum2_t - cum2_e) 2^(cum2_e - cum2_s), e = the block's last token (both
+            // factors <= 1; the second, b_s, comes from the rotate group); blocks
+            // holding the diagonal use exp of the difference directly.
+            float ecum_t = 0.f;
+            if (warp * 32 < QR) {
+                const int row = tid, t = row / R;
+                const float* cum2 = co + K::CO_CUM2;
+                const float* bneg = box_dt(s);
+                const float ct = cum2[t], rt = co[K::CO_RHO + t];
+                ecum_t = co[K::CO_ECUM + t];
+                uint8_t* sl = tile_c(s);
+                const int tmax = (warp * 32 + 31) / R;   // last token of this warp's rows
+#pragma unroll
+                for (int c32 = 0; c32 < QR; c32 += 32) {
+                    float v[32];
+                    const bool any = c32 / R <= tmax;    // warp-uniform
+                    if (any) {
+                        tmem_ld32_sync(tlane + K::T_S + c32, v);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    }
+#pragma unroll
+                    for (int hb2 = 0; hb2 < 2; ++hb2) {
+                        const int cb = c32 + 16 * hb2;
+                        const int s_lo = cb / R, s_hi = (cb + 15) / R;
+                        if (s_lo > t) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[16 * hb2 + i] = 0.f;
+                        } else if (s_hi < t) {
+                            const float a = ex2_approx(ct - cum2[s_hi]);
+                            const float2 a2 = make_float2(a, a);
+#pragma unroll
+                            for (int i = 0; i < 16; i += 2) {
+                                const float2 bb = make_float2(bneg[(cb + i) / R], bneg[(cb + i + 1) / R]);
+                                const float2 r2 = __fmul2_rn(make_float2(v[16 * hb2 + i], v[16 * hb2 + i + 1]),
+                                                             __fmul2_rn(a2, bb));
+                                v[16 * hb2 + i] = r2.x;
+                                v[16 * hb2 + i + 1] = r2.y;
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const int sidx = (cb + i) / R;
+                                float m = 0.f;
+                                if (sidx < t) m = ex2_approx(ct - cum2[sidx]);
+                                else if (sidx == t) m = rt;
+                                v[16 * hb2 + i] *= m;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        const int col = c32 + q8 * 8;
+                        *reinterpret_cast<uint4*>(sl + (col / 64) * QR * 128 + sw128_offset(row, (col % 64) * 2)) =
+                            make_uint4(pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]), pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]),
+                                       pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
+                    }
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            group_bar(1);
+            if (tid == 0) {   // batch 2: Y = SL X
+                tc_fence_after();
+                const uint64_t dSL = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
+                const uint64_t dX = smem_desc(smem_u32(tile_x(s)), 16, 1024, kSwizzle128B);
+                constexpr uint32_t id_y = idesc_bf16_f32(128, P, false, true);
+#pragma unroll
+                for (int kk = 0; kk < QR / 16; ++kk) {
+                    const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
+                    mma_bf16_ss(tmem + K::T_Y, dSL + ko, dX + kk * (2048 >> 4), id_y, kk > 0);
+                }
+                mma_commit(&ctl->b2);
+                ctl->b2_issued += 1;
+            }
+
+            // ---- state: H <- e_{c+1} R(Theta_c) H ; Hb <- bf16(R(Theta_c) H)   (thread = state row n)
+            float e_next = 1.f;
+            if (c + 1 < nc) {
+                const int s1 = (c + 1) & 1;
+                (void)wait_bounded(&ctl->coef_ready[s1], ((c + 1) >> 1) & 1, fail_c, fail_r);
+                e_next = box_lam(s1)[K::CO_EEND];
+            }
+            if (tid < NS) {
+                float sn, cs;
+                sincosf(co[K::CO_THETA + (tid >> 1)], &sn, &cs);
+                // even row 2j: cos*v_2j - sin*v_2j+1 ; odd row 2j+1: sin*v_2j + cos*v_2j+1
+                const float2 c2 = make_float2(cs, cs);
+                const float2 s2 = odd ? make_float2(sn, sn) : make_float2(-sn, -sn);
+                const float2 e2 = make_float2(e_next, e_next);
+#pragma unroll
+                for (int cc = 0; cc < P; cc += 32) {
+                    float hv[32];
+                    tmem_ld32_sync(tlane + K::T_H + cc, hv);
+                    float nv[32];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 v = make_float2(hv[i], hv[i + 1]);
+                        const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, hv[i], 1),
+                                                     __shfl_xor_sync(0xffffffffu, hv[i + 1], 1));
+                        const float2 r = __ffma2_rn(c2, v, __fmul2_rn(s2, o));
+                        nv[i] = r.x;
+                        nv[i + 1] = r.y;
+                        const float2 sc = __fmul2_rn(e2, r);
+                        hv[i] = sc.x;
+                        hv[i + 1] = sc.y;
+                    }
+                    tmem_st32(tlane + K::T_H + cc, hv);
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        const uint4 pk = make_uint4(pack_bf16(nv[q8 * 8 + 0], nv[q8 * 8 + 1]),
+                                                    pack_bf16(nv[q8 * 8 + 2], nv[q8 * 8 + 3]),
+                                                    pack_bf16(nv[q8 * 8 + 4], nv[q8 * 8 + 5]),
+                                                    pack_bf16(nv[q8 * 8 + 6], nv[q8 * 8 + 7]));
+                        *reinterpret_cast<uint4*>(hb + sw128_offset(tid, (cc + q8 * 8) * 2)) = pk;
+                    }
+                }
+                tmem_st_wait();
+                fence_proxy_async_smem();
+            }
+
+            // ---- output rows (t, r) once batch 2 is done; the stage is then free for chunk c+2
+            (void)wait_bounded(&ctl->b2, c & 1, fail_c, fail_r);
+            tc_fence_after();
+            if (tid == 0 && c + 2 < nc && !*fail_c) issue_loads(c + 2, s);
+            if (warp * 32 < QR) {
+                const int row = tid, t = row / R, r = row % R;
+                const int tok = c * Q + t;
+                __nv_bfloat16* yrow = args.y + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P;
+                const float2 e2 = make_float2(ecum_t, ecum_t);
+#pragma unroll
+                for (int cc = 0; cc < P; cc += 32) {
+                    float yv[32], iv[32];
+                    tmem_ld32_sync(tlane + K::T_Y + cc, yv);
+                    tmem_ld32_sync(tlane + K::T_YI + cc, iv);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float2 o = __ffma2_rn(e2, make_float2(iv[2 * q], iv[2 * q + 1]),
+                                                    make_float2(yv[2 * q], yv[2 * q + 1]));
+                        pk[q] = pack_bf16(o.x, o.y);
+                    }
+                    if (tok < T) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            *reinterpret_cast<uint4*>(yrow + cc + 8 * q4) =
+                                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            group_bar(1);
+            if (tid == 0) {
+                ctl->b1_waited += 1;
+                ctl->b2_waited += 1;
+            }
+            if (*fail_c) break;
+        }
+        if (!*fail_c && !*fail_r && args.final_state != nullptr && tid < NS) {
+            tc_fence_after();
             float* fs = args.final_state + ((int64_t)bh * NS + tid) * P;
 #pragma unroll
             for (int cc = 0; cc < P; cc += 16) {
@@ -493,14 +477,166 @@ __global__ void __launch_bounds__(128, 2) scan_tc_kernel(const __grid_constant__
             }
         }
     } else {
-        if (tid == 0) {
-            atomicExch(args.status, (int)M3_ERR_TIMEOUT);
-            // drain the loads still in flight (bounded) before the shared memory goes away
-            for (int s2 = 0; s2 < 2; ++s2)
-                if (inflight[s2] >= 0) (void)mbar_wait(&bar_full[s2], (inflight[s2] >> 1) & 1, kWaitLimitNs);
+        // =============================== rotate ===============================
+        const int rt = tid - 128, rw = rt >> 5;
+        float* sPart = reinterpret_cast<float*>(sm + K::OFF_PART);
+        float* sW = reinterpret_cast<float*>(sm + K::OFF_RPRIV);
+        float* sF = sW + Q;
+        float* sWarpR = sF + Q;
+        const int jg = rt % NG, tg = rt / NG;
+        const int pan = jg / 8, cib = (jg % 8) * 16;     // panel and byte-in-row of my 16-byte piece
+        const float* om_base = args.omega + ((int64_t)b * T * args.H + h) * NP2 + 4 * jg;
+        const int64_t om_tok = (int64_t)args.H * NP2;
+        float4 om[TPG];
+        auto load_omega = [&](int c) {
+#pragma unroll
+            for (int i = 0; i < TPG; ++i) {
+                const int t = c * Q + tg * TPG + i;
+                om[i] = t < T ? *reinterpret_cast<const float4*>(om_base + t * om_tok) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        };
+        load_omega(0);
+        const float a = args.A[h];
+        for (int c = 0; c < nc; ++c) {
+            const int s = c & 1;
+            (void)wait_bounded(&ctl->full[s], (c >> 1) & 1, fail_r, fail_c);
+            group_bar(2);
+            if (*fail_r) break;
+            if (rt == 0) ctl->tma_waited[s] += 1;
+            const float* sDt = box_dt(s);
+            float* sLam = box_lam(s);
+            float* co = sLam;   // coefficient block, written once lambda is read
+
+            // ---- coefficients and chunk-local log-decay prefix
+            float ell = 0.f, gam = 0.f, wv = 0.f;
+            if (rt < Q) {
+                const float d = sDt[rt * 4 + hq], l = sLam[rt * 4 + hq];
+                const float dn = sDt[(rt + 1) * 4 + hq], ln = sLam[(rt + 1) * 4 + hq];
+                ell = d * a;
+                gam = l * d;
+                wv = gam + (1.f - ln) * dn;
+            }
+            float cum = warp_inclusive_sum(ell);
+            if (lane == 31) sWarpR[rw] = cum;
+            group_bar(2);   // also: every lambda read is done
+            float off = 0.f, cend = 0.f;
+            for (int i = 0; i < 4; ++i) {
+                const float v = sWarpR[i];
+                if (i < rw) off += v;
+                cend += v;
+            }
+            cum += off;
+            if (rt < Q) {
+                co[K::CO_CUM2 + rt] = cum * kLog2e;
+                co[K::CO_RHO + rt] = wv > 0.f ? gam / wv : 0.f;
+                co[K::CO_ECUM + rt] = __expf(cum);
+                sW[rt] = wv;
+                sF[rt] = __expf(cend - cum);
+            }
+            if (rt == 0) co[K::CO_EEND] = __expf(cend);
+
+            // ---- rotation angles: partial sums per token group
+            float dtk[TPG];
+            {
+                float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < TPG; ++i) {
+                    const float d = sDt[(tg * TPG + i) * 4 + hq];
+                    dtk[i] = d;
+                    part.x = fmaf(d, om[i].x, part.x);
+                    part.y = fmaf(d, om[i].y, part.y);
+                    part.z = fmaf(d, om[i].z, part.z);
+                    part.w = fmaf(d, om[i].w, part.w);
+                }
+                *reinterpret_cast<float4*>(&sPart[tg * NP2 + 4 * jg]) = part;
+            }
+            group_bar(2);   // every dt read is done: the dt box now takes b_s for the mask
+            if (rt < Q) {
+                const int e_tok = ((rt * R) / 16 * 16 + 15) / R;   // last token of s's 16-column block
+                box_dt(s)[rt] = ex2_approx(co[K::CO_CUM2 + e_tok] - co[K::CO_CUM2 + rt]);
+            }
+            {
+                float4 psi = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int g = 0; g < tg; ++g) {
+                    const float4 p4 = *reinterpret_cast<const float4*>(&sPart[g * NP2 + 4 * jg]);
+                    psi.x += p4.x; psi.y += p4.y; psi.z += p4.z; psi.w += p4.w;
+                }
+                uint8_t* tC = tile_c(s);
+                uint8_t* tB = tile_b(s);
+#pragma unroll
+                for (int i = 0; i < TPG; ++i) {
+                    const int t = tg * TPG + i;
+                    psi.x = fmaf(dtk[i], om[i].x, psi.x);
+                    psi.y = fmaf(dtk[i], om[i].y, psi.y);
+                    psi.z = fmaf(dtk[i], om[i].z, psi.z);
+                    psi.w = fmaf(dtk[i], om[i].w, psi.w);
+                    float cs[4], sn[4];
+                    __sincosf(-psi.x, &sn[0], &cs[0]);
+                    __sincosf(-psi.y, &sn[1], &cs[1]);
+                    __sincosf(-psi.z, &sn[2], &cs[2]);
+                    __sincosf(-psi.w, &sn[3], &cs[3]);
+                    const float wt = sW[t];
+                    const float2 c01[2] = {make_float2(cs[0], cs[1]), make_float2(cs[2], cs[3])};
+                    const float2 s01[2] = {make_float2(sn[0], sn[1]), make_float2(sn[2], sn[3])};
+                    const float2 w2 = make_float2(wt, wt);
+                    const float2 cw01[2] = {__fmul2_rn(w2, c01[0]), __fmul2_rn(w2, c01[1])};
+                    const float2 sw01[2] = {__fmul2_rn(w2, s01[0]), __fmul2_rn(w2, s01[1])};
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t off2 = pan * QR * 128 + sw128_offset(t * R + r, cib);
+                        uint4* pc = reinterpret_cast<uint4*>(tC + off2);
+                        uint4* pb = reinterpret_cast<uint4*>(tB + off2);
+                        *pc = rotate4(*pc, c01, s01);
+                        *pb = rotate4(*pb, cw01, sw01);
+                    }
+                }
+                if (tg == TG - 1) *reinterpret_cast<float4*>(&co[K::CO_THETA + 4 * jg]) = psi;
+            }
+            // the consumer may read this stage's coefficient block now
+            mbar_arrive(&ctl->coef_ready[s]);
+            if (c + 1 < nc) load_omega(c + 1);
+
+            // ---- X^ = exp(cum_end - cum_s) X into the single X^ buffer, once batch 1 of
+            //      chunk c-1 (its last reader) is done
+            if (c > 0) (void)wait_bounded(&ctl->b1, (c - 1) & 1, fail_r, fail_c);
+            {
+                const uint8_t* tX = tile_x(s);
+                // QR rows x 8 16-byte pieces; 128 threads
+                for (int pidx = rt; pidx < QR * 8; pidx += 128) {
+                    const int row = pidx >> 3, piece = pidx & 7;
+                    const float f = sF[row / R];
+                    const uint32_t off2 = sw128_offset(row, piece * 16);
+                    const uint4 v = *reinterpret_cast<const uint4*>(tX + off2);
+                    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    const float2 f2 = make_float2(f, f);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 g = __fmul2_rn(f2, make_float2(bf_lo(w[e]), bf_hi(w[e])));
+                        w[e] = pack_bf16(g.x, g.y);
+                    }
+                    *reinterpret_cast<uint4*>(xhat + off2) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&ctl->rot_done[s]);
+            group_bar(2);   // sW / sF / sPart are reused by the next chunk
+            if (*fail_r) break;
         }
     }
+
+    // ------------------------------- teardown -------------------------------
     tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && (ctl->fail_c || ctl->fail_r)) {
+        atomicExch(args.status, (int)M3_ERR_TIMEOUT);
+        // let copies and MMAs still in flight finish (bounded) before the shared
+        // memory and TMEM go away
+        for (int s = 0; s < 2; ++s)
+            for (int k = ctl->tma_waited[s]; k < ctl->tma_issued[s]; ++k)
+                (void)mbar_wait(&ctl->full[s], k & 1, kWaitLimitNs);
+        for (int k = ctl->b1_waited; k < ctl->b1_issued; ++k) (void)mbar_wait(&ctl->b1, k & 1, kWaitLimitNs);
+        for (int k = ctl->b2_waited; k < ctl->b2_issued; ++k) (void)mbar_wait(&ctl->b2, k & 1, kWaitLimitNs);
+    }
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, K::TMEM_COLS);
