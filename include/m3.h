@@ -83,6 +83,7 @@ M3_API size_t m3_scan_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t 
  *             and the fallback), 1 = tensor-core kernels (bf16 MMA with
  *             fp32 accumulation)
  *   launches  out: number of kernel launches one m3_scan_fwd call makes
+ *             (besides a 4-byte memset of the workspace's status word)
  * Returns M3_OK, or the error m3_scan_fwd would return for these sizes.
  */
 M3_API int m3_scan_fwd_plan(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
@@ -99,6 +100,12 @@ M3_API int m3_scan_fwd_plan(int64_t batch, int64_t seqlen, int64_t nheads, int64
  *            intra-chunk masked scores (decay x two-band mask, Eq. 7)
  *            plus inter-chunk state passing; 16 <= chunk <= 256 and a
  *            multiple of 16.  The result does not depend on it beyond rounding.
+ *            The tensor-core path runs chunks of more than 128 rows
+ *            (chunk * R) as sub-chunks of chunk / R tokens, the MIMO
+ *            chunk-length reduction of section 3.3, so that every score tile
+ *            stays chunk x chunk rows.  With fewer (batch, head) sequences than
+ *            the GPU has CTA slots it also cuts each sequence into segments
+ *            (a state pass, the segment scan of m3_state_passing, a full pass).
  *   y        out [batch, T, H, R, P], io dtype
  *   final_state  out (nullable) [batch, H, N, P] fp32: h_{T-1}, the state a
  *            decode step continues from (its delayed-write cache is

@@ -14,9 +14,9 @@
 //   rotation       Psi_t = sum_{k<=t} dt_k omega_k (chunk-local),
 //                  C~ = R(-Psi) C,  B' = w R(-Psi) B   (in place in shared memory)
 //                  X^ = exp(cum_end - cum_s) X          (separate buffer)
-//   batch 1        S  = C~ B'^T                       (= S_ts w_s)
-//                  Yi = C~ Hb_{c-1}                    (inter-chunk readout)
+//   batch 1        S  = C~ B'^T                       (= S_ts w_s; committed first)
 //                  H += B'^T X^                        (chunk state onto the carry)
+//                  Yi = C~ Hb_{c-1}                    (inter-chunk readout)
 //   mask           SL_ts = S_ts exp(cum_t - cum_s) for s < t, S_tt rho_t, 0 for s > t
 //   batch 2        Y  = SL X
 //   state          H_c = exp(cum_end(c+1)) R(Theta_c) H,  Hb_c = bf16(R(Theta_c) H)
@@ -41,9 +41,14 @@
 //   SL   A, K-major  (rows (t,r), K = (s,r')) X   B, MN-major (K = (s,r'), N = p)
 //   Hb   B, MN-major (K = n, N = p)          B'^T A, MN-major (M = n, K = (s,r'))
 //   X^   B, MN-major (K = (s,r'), N = p)
-// When QR = 64 the MMAs still run with M = 128; rows 64..127 read the next
-// 8 KB of shared memory (always inside this CTA's allocation) and their
-// results are never read.  SL is written over C~ (dead once batch 1 is done).
+// When QR = 64 the score, inter-readout and output MMAs run with M = 64: row r
+// of those accumulators sits in TMEM lane 32 (r / 16) + r % 16, and every
+// consumer thread takes half a row (16-lane loads, two column halves), so all
+// four consumer warps share the mask and the output.  With QR = 128 they run
+// with M = 128 (row r in lane r).  The chunk-state MMA always has M = 128
+// (state rows n); with N = 64 its rows 64..127 read the next QR*128 bytes of
+// shared memory (inside this CTA's allocation) and are never read.  SL is
+// written over C~ (dead once batch 1 is done).
 #include <cuda.h>
 
 #include "m3_common.cuh"
@@ -68,31 +73,43 @@ struct Cfg {
     static_assert(QR == 64 || QR == 128, "chunk rows must be 64 or 128");
     static_assert(NS == 64 || NS == 128, "state size must be 64 or 128");
     static_assert(Q <= 128, "chunk too long");
+    // rows of the score / inter / output accumulators: M = 64 puts row r in TMEM lane
+    // 32 (r / 16) + r % 16 (16 lanes of each warp's quadrant), M = 128 in lane r
+    static constexpr bool M64 = QR == 64;
+    static constexpr int MM = M64 ? 64 : 128;
 
     static constexpr int X_BYTES = QR * 128;
     static constexpr int BC_BYTES = NPAN * QR * 128;
+    static constexpr int SL_BYTES = QR * QR * 2;
+    static constexpr int XS_BYTES = X_BYTES > SL_BYTES ? X_BYTES : SL_BYTES;
     static constexpr int STG_TILE = 2 * BC_BYTES + X_BYTES;      // C | B | X of one stage
     static constexpr int BOX_BYTES = 16 * (Q + 1);                // dt / lambda box {4 heads, Q+1 tokens}
     static constexpr int BOX_STRIDE = align_up(BOX_BYTES, 128);
-    static constexpr int OFF_XHAT = 2 * STG_TILE;
-    static constexpr int OFF_HB = OFF_XHAT + X_BYTES;
-    static constexpr int OFF_BOX = OFF_HB + NS * 128;             // [stage][dt | lambda]
     // rotate-phase mapping: pair group jg (4 pairs = 16 bytes of a row), token group tg
     static constexpr int NG = NS / 8;
     static constexpr int TG = 128 / NG;
     static constexpr int TPG = Q / TG;
     static_assert(Q % TG == 0, "tokens must split evenly over token groups");
-    static constexpr int OFF_PART = OFF_BOX + 4 * BOX_STRIDE;     // [TG][NS/2] partial angle sums
-    static constexpr int OFF_RPRIV = OFF_PART + TG * (NS / 2) * 4;   // w[Q], f[Q], warp sums[4]
+    static constexpr int PART_BYTES = TG * (NS / 2) * 4;          // partial angle sums [TG][NS/2]
+    // the partial sums go over the stage's two boxes once their values are in registers
+    static constexpr bool PART_IN_BOX = PART_BYTES <= 2 * BOX_STRIDE;
+    // coefficient block of a stage (floats): cum*log2e[Q], rho[Q], exp(cum)[Q], b[Q], Theta[NS/2],
+    // exp(cum_end), cum_end
+    static constexpr int CO_CUM2 = 0, CO_RHO = Q, CO_ECUM = 2 * Q, CO_BNEG = 3 * Q, CO_THETA = 4 * Q,
+                         CO_EEND = 4 * Q + NS / 2, CO_CEND = 4 * Q + NS / 2 + 1;
+    static constexpr int CO_BYTES = align_up((4 * Q + NS / 2 + 2) * 4, 16);
+
+    static constexpr int OFF_XS = 2 * STG_TILE;                   // X^, then SL
+    static constexpr int OFF_HB = OFF_XS + XS_BYTES;
+    static constexpr int OFF_BOX = OFF_HB + NS * 128;             // [stage][dt | lambda]
+    static constexpr int OFF_PART = OFF_BOX + 4 * BOX_STRIDE;     // only when not in the boxes
+    static constexpr int OFF_CO = OFF_PART + (PART_IN_BOX ? 0 : align_up(PART_BYTES, 16));
+    static constexpr int OFF_RPRIV = OFF_CO + 2 * CO_BYTES;       // w[Q], f[Q], warp sums[4]
     static constexpr int OFF_BAR = align_up(OFF_RPRIV + (2 * Q + 4) * 4, 16);
-    static constexpr int SMEM = OFF_BAR + 128 + 1024;             // barriers / flags, alignment slack
+    static constexpr int SMEM = OFF_BAR + 192 + 1024;             // barriers / flags, alignment slack
     // two CTAs per SM when both fit (228 KB per SM, 1 KB reserved per CTA)
     static constexpr int MIN_BLOCKS = 2 * (SMEM + 1024) <= 233472 ? 2 : 1;
-    static constexpr int TX_BYTES = X_BYTES + 2 * BC_BYTES + 2 * BOX_BYTES;
-
-    // coefficient block the consumer reads, written over the lambda box once read
-    static constexpr int CO_CUM2 = 0, CO_RHO = Q, CO_ECUM = 2 * Q, CO_THETA = 3 * Q, CO_EEND = 3 * Q + NS / 2;
-    static_assert((3 * Q + NS / 2 + 1) * 4 <= BOX_BYTES, "coefficient block must fit in the lambda box");
+    static constexpr int TX_BOX = 2 * BOX_BYTES, TX_X = X_BYTES;
 
     // TMEM columns
     static constexpr int T_S = 0;
@@ -100,6 +117,7 @@ struct Cfg {
     static constexpr int T_Y = QR + P;
     static constexpr int T_H = QR + 2 * P;
     static constexpr int TMEM_COLS = (QR + 3 * P) <= 256 ? 256 : 512;
+    static_assert(SMEM <= 232448, "shared memory over the 227 KB per-CTA limit");
 };
 
 struct TcArgs {
@@ -109,21 +127,32 @@ struct TcArgs {
     float* final_state;
     int* status;
     int T, H, nc;
+    // sequence segments: this launch covers segments 0 .. nseg-1 of S of L chunks each
+    int L, nseg, S;
+    const float* h_in;       // [bh][S-1][N][P]: state entering segment k (k <= S-2), or null
+    const float* h_in_last;  // [bh][N][P]: state entering segment S-1, or null
+    float* seg_U;            // state pass: [bh][S-1][N][P] carry at the segment's end from a zero start
+    float* seg_ld;           // state pass: [bh][S-1] summed log-decay of the segment
+    float* seg_th;           // state pass: [bh][S-1][N/2] summed rotation angle of the segment
 };
 
-// Shared control block (after the barriers).
+// Shared control block (after the barriers).  Three TMA groups per stage, each
+// issued as soon as its previous contents are dead: the dt / lambda boxes
+// (once the rotate group has read them), C and B (after batch 1), X (after
+// batch 2).
 struct Ctl {
-    uint64_t full[2];        // TMA stage landed
+    uint64_t fbox[2], fcb[2], fx[2];   // TMA groups landed
     uint64_t rot_done[2];    // rotate group finished the stage (count 128)
     uint64_t coef_ready[2];  // coefficient block of the stage written (count 128)
-    uint64_t b1;             // MMA batch 1 complete
+    uint64_t b1a;            // MMA batch 1, scores S, complete
+    uint64_t b1b;            // MMA batch 1 complete (chunk state onto H, inter readout Yi)
     uint64_t b2;             // MMA batch 2 complete
     uint32_t tmem;
     int fail_c, fail_r;      // per-group failure flags
-    int tma_issued[2];       // loads issued per stage (consumer thread 0)
-    int tma_waited[2];       // loads waited for per stage (rotate group)
+    int box_issued[2], box_waited[2], cb_issued[2], cb_waited[2], x_issued[2], x_waited[2];
     int b1_issued, b2_issued, b1_waited, b2_waited;
 };
+static_assert(sizeof(Ctl) <= 192, "control block must fit its reserved space");
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -152,7 +181,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
 }
 
 // Rotate the 4 pairs of one 16-byte piece by (c[k], s[k]) (angle -Psi), optionally
-// scaling by wt, in place; fp32 arithmetic on packed pairs of pairs.
+// scaled, in place; fp32 arithmetic on packed pairs of pairs.
 __device__ __forceinline__ uint4 rotate4(uint4 v, const float2 (&c01)[2], const float2 (&s01)[2]) {
     uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -168,7 +197,46 @@ __device__ __forceinline__ uint4 rotate4(uint4 v, const float2 (&c01)[2], const 
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <int NS, int R, int Q>
+// Mask one 16-column block of a score row held in v[0..15]: columns cb..cb+15
+// (tokens cb/R ..), row token t.  Blocks strictly below the diagonal use the
+// factorised decay 2^(cum2_t - cum2_e) 2^(cum2_e - cum2_s), e = the block's last
+// token (both factors <= 1; the second is b_s); the diagonal block uses the
+// exponential of the difference directly; blocks above are zero.
+template <int R>
+__device__ __forceinline__ void mask_block(float* v, int cb, int t, float ct, float rt, const float* cum2,
+                                           const float* bneg) {
+    const int s_lo = cb / R, s_hi = (cb + 15) / R;
+    if (s_lo > t) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    } else if (s_hi < t) {
+        const float a = ex2_approx(ct - cum2[s_hi]);
+        const float2 a2 = make_float2(a, a);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const float2 bb = make_float2(bneg[(cb + i) / R], bneg[(cb + i + 1) / R]);
+            const float2 r2 = __fmul2_rn(make_float2(v[i], v[i + 1]), __fmul2_rn(a2, bb));
+            v[i] = r2.x;
+            v[i + 1] = r2.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int sidx = (cb + i) / R;
+            float m = 0.f;
+            if (sidx < t) m = ex2_approx(ct - cum2[sidx]);
+            else if (sidx == t) m = rt;
+            v[i] *= m;
+        }
+    }
+}
+
+// FULL = true: the whole chunked prefill of its segment (outputs y; the last
+// segment writes the final state).  FULL = false: the state pass of the
+// segmented prefill -- only the carry (rotated, scaled B, scaled X and the
+// chunk-state MMA), whose value at the segment's end from a zero start, summed
+// log-decay and summed angles go to the workspace for the segment scan.
+template <int NS, int R, int Q, bool FULL>
 __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                          const __grid_constant__ CUtensorMap tm_B,
                                                          const __grid_constant__ CUtensorMap tm_C,
@@ -176,32 +244,40 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                                                          const __grid_constant__ CUtensorMap tm_lam, TcArgs args) {
     using K = Cfg<NS, R, Q>;
     constexpr int P = K::P, QR = K::QR, NP2 = NS / 2, NG = K::NG, TG = K::TG, TPG = K::TPG;
+    constexpr int TX_CB = FULL ? 2 * K::BC_BYTES : K::BC_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctl* ctl = reinterpret_cast<Ctl*>(sm + K::OFF_BAR);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x / args.nseg, seg = blockIdx.x % args.nseg;
     const int b = bh / args.H, h = bh % args.H, hq = h & 3;
-    const int T = args.T, nc = args.nc;
+    const int T = args.T;
+    const int c_begin = seg * args.L;
+    const int nl = min(args.nc, c_begin + args.L) - c_begin;   // chunks of this segment (>= 1)
 
     auto tile_c = [&](int s) { return sm + s * K::STG_TILE; };
     auto tile_b = [&](int s) { return sm + s * K::STG_TILE + K::BC_BYTES; };
     auto tile_x = [&](int s) { return sm + s * K::STG_TILE + 2 * K::BC_BYTES; };
     auto box_dt = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_BOX + (2 * s) * K::BOX_STRIDE); };
     auto box_lam = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_BOX + (2 * s + 1) * K::BOX_STRIDE); };
-    uint8_t* xhat = sm + K::OFF_XHAT;
+    auto coef = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_CO + s * K::CO_BYTES); };
+    uint8_t* xs = sm + K::OFF_XS;   // X^ of the chunk being set up, then SL of the chunk being masked
     uint8_t* hb = sm + K::OFF_HB;
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->fbox[s], 1);
+            mbar_init(&ctl->fcb[s], 1);
+            mbar_init(&ctl->fx[s], 1);
             mbar_init(&ctl->rot_done[s], 128);
             mbar_init(&ctl->coef_ready[s], 128);
-            ctl->tma_issued[s] = 0;
-            ctl->tma_waited[s] = 0;
+            ctl->box_issued[s] = ctl->box_waited[s] = 0;
+            ctl->cb_issued[s] = ctl->cb_waited[s] = 0;
+            ctl->x_issued[s] = ctl->x_waited[s] = 0;
         }
-        mbar_init(&ctl->b1, 1);
+        mbar_init(&ctl->b1a, 1);
+        mbar_init(&ctl->b1b, 1);
         mbar_init(&ctl->b2, 1);
         ctl->fail_c = 0;
         ctl->fail_r = 0;
@@ -209,24 +285,34 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         fence_mbar_init();
         prefetch_tensormap(&tm_x);
         prefetch_tensormap(&tm_B);
-        prefetch_tensormap(&tm_C);
+        if (FULL) prefetch_tensormap(&tm_C);
         prefetch_tensormap(&tm_dt);
         prefetch_tensormap(&tm_lam);
     }
     __syncthreads();
 
-    auto issue_loads = [&](int c, int s) {   // consumer thread 0 only
-        const int c0 = c * Q;
-        mbar_arrive_expect_tx(&ctl->full[s], K::TX_BYTES);
+    // the three TMA groups of local chunk i into stage s (single issuing thread each)
+    auto load_box = [&](int i, int s) {
+        const int c0 = (c_begin + i) * Q;
+        mbar_arrive_expect_tx(&ctl->fbox[s], K::TX_BOX);
+        tma_load_3d(box_dt(s), &tm_dt, &ctl->fbox[s], h & ~3, c0, b);
+        tma_load_3d(box_lam(s), &tm_lam, &ctl->fbox[s], h & ~3, c0, b);
+        ctl->box_issued[s] += 1;
+    };
+    auto load_cb = [&](int i, int s) {
+        const int c0 = (c_begin + i) * Q;
+        mbar_arrive_expect_tx(&ctl->fcb[s], TX_CB);
 #pragma unroll
         for (int p = 0; p < K::NPAN; ++p) {
-            tma_load_5d(tile_c(s) + p * QR * 128, &tm_C, &ctl->full[s], 64 * p, 0, h, c0, b);
-            tma_load_5d(tile_b(s) + p * QR * 128, &tm_B, &ctl->full[s], 64 * p, 0, h, c0, b);
+            if (FULL) tma_load_5d(tile_c(s) + p * QR * 128, &tm_C, &ctl->fcb[s], 64 * p, 0, h, c0, b);
+            tma_load_5d(tile_b(s) + p * QR * 128, &tm_B, &ctl->fcb[s], 64 * p, 0, h, c0, b);
         }
-        tma_load_5d(tile_x(s), &tm_x, &ctl->full[s], 0, 0, h, c0, b);
-        tma_load_3d(box_dt(s), &tm_dt, &ctl->full[s], h & ~3, c0, b);
-        tma_load_3d(box_lam(s), &tm_lam, &ctl->full[s], h & ~3, c0, b);
-        ctl->tma_issued[s] += 1;
+        ctl->cb_issued[s] += 1;
+    };
+    auto load_x = [&](int i, int s) {
+        mbar_arrive_expect_tx(&ctl->fx[s], K::TX_X);
+        tma_load_5d(tile_x(s), &tm_x, &ctl->fx[s], 0, 0, h, (c_begin + i) * Q, b);
+        ctl->x_issued[s] += 1;
     };
 
     if (warp == 0) {
@@ -234,8 +320,11 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         tmem_relinquish();
     }
     if (tid == 0) {
-        issue_loads(0, 0);
-        if (nc > 1) issue_loads(1, 1);
+        for (int i = 0; i < 2 && i < nl; ++i) {
+            load_box(i, i);
+            load_cb(i, i);
+            load_x(i, i);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -247,26 +336,60 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
     if (warp < 4) {
         // =============================== consumer ===============================
         const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
-        // H_{-1} = 0 (TMEM) and Hb_{-1} = 0 (shared)
+        // the state entering the segment: zero, or from the segment scan
+        const float* hin = nullptr;
+        if (FULL && seg > 0)
+            hin = seg < args.S - 1 ? args.h_in + ((int64_t)bh * (args.S - 1) + seg) * NS * P
+                                   : args.h_in_last + (int64_t)bh * NS * P;
         {
-            float z[16];
+            // H enters batch 1 already decayed by the first chunk: exp(cum_end) H_in
+            float e0 = 0.f;
+            if (hin != nullptr) {
+                (void)wait_bounded(&ctl->coef_ready[0], 0, fail_c, fail_r);
+                e0 = coef(0)[K::CO_EEND];
+            }
+            if (tid < NS || hin == nullptr) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) z[i] = 0.f;
+                for (int cc = 0; cc < P; cc += 32) {
+                    float v[32];
+                    if (hin != nullptr && tid < NS) {
 #pragma unroll
-            for (int cc = 0; cc < P; cc += 16) tmem_st16(tlane + K::T_H + cc, z);
-            tmem_st_wait();
-            uint4* hb4 = reinterpret_cast<uint4*>(hb);
-            for (int i = tid; i < NS * 128 / 16; i += 128) hb4[i] = make_uint4(0u, 0u, 0u, 0u);
+                        for (int i4 = 0; i4 < 32; i4 += 4) {
+                            const float4 q = *reinterpret_cast<const float4*>(hin + (int64_t)tid * P + cc + i4);
+                            v[i4] = q.x; v[i4 + 1] = q.y; v[i4 + 2] = q.z; v[i4 + 3] = q.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i4 = 0; i4 < 32; ++i4) v[i4] = 0.f;
+                    }
+                    if (FULL && tid < NS) {
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8)
+                            *reinterpret_cast<uint4*>(hb + sw128_offset(tid, (cc + q8 * 8) * 2)) =
+                                make_uint4(pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]), pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]),
+                                           pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
+                    }
+#pragma unroll
+                    for (int i4 = 0; i4 < 32; ++i4) v[i4] *= e0;
+                    tmem_st32(tlane + K::T_H + cc, v);
+                }
+                tmem_st_wait();
+            }
+            if (FULL && hin == nullptr) {
+                uint4* hb4 = reinterpret_cast<uint4*>(hb);
+                for (int i = tid; i < NS * 128 / 16; i += 128) hb4[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
             fence_proxy_async_smem();
         }
         tc_fence_before();
         group_bar(1);
         const bool odd = tid & 1;
-        for (int c = 0; c < nc; ++c) {
-            const int s = c & 1;
-            const float* co = box_lam(s);
+        float ld_sum = 0.f, th_sum = 0.f;   // state pass: summed log-decay (thread 0), angle of pair tid
+        for (int i = 0; i < nl; ++i) {
+            const int c = c_begin + i, s = i & 1;
+            const float* co = coef(s);
             // ---- batch 1 once the rotate group has finished this stage
-            (void)wait_bounded(&ctl->rot_done[s], (c >> 1) & 1, fail_c, fail_r);
+            (void)wait_bounded(&ctl->rot_done[s], (i >> 1) & 1, fail_c, fail_r);
             tc_fence_before();
             group_bar(1);
             if (*fail_c) break;
@@ -276,118 +399,128 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
                 const uint64_t dB = smem_desc(smem_u32(tile_b(s)), 16, 1024, kSwizzle128B);
                 const uint64_t dBt = smem_desc(smem_u32(tile_b(s)), QR * 128, 1024, kSwizzle128B);
-                const uint64_t dX = smem_desc(smem_u32(xhat), 16, 1024, kSwizzle128B);
+                const uint64_t dX = smem_desc(smem_u32(xs), 16, 1024, kSwizzle128B);
                 const uint64_t dHb = smem_desc(smem_u32(hb), 16, 1024, kSwizzle128B);
-                constexpr uint32_t id_s = idesc_bf16_f32(128, QR, false, false);
-                constexpr uint32_t id_y = idesc_bf16_f32(128, P, false, true);
+                constexpr uint32_t id_s = idesc_bf16_f32(K::MM, QR, false, false);
+                constexpr uint32_t id_y = idesc_bf16_f32(K::MM, P, false, true);
                 constexpr uint32_t id_u = idesc_bf16_f32(128, P, true, true);
+                if (FULL) {
 #pragma unroll
-                for (int kk = 0; kk < NS / 16; ++kk) {   // S = C~ B'^T
-                    const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
-                    mma_bf16_ss(tmem + K::T_S, dC + ko, dB + ko, id_s, kk > 0);
-                }
-#pragma unroll
-                for (int kk = 0; kk < NS / 16; ++kk) {   // Yi = C~ Hb_{c-1}
-                    const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
-                    mma_bf16_ss(tmem + K::T_YI, dC + ko, dHb + kk * (2048 >> 4), id_y, kk > 0);
+                    for (int kk = 0; kk < NS / 16; ++kk) {   // S = C~ B'^T
+                        const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
+                        mma_bf16_ss(tmem + K::T_S, dC + ko, dB + ko, id_s, kk > 0);
+                    }
+                    mma_commit(&ctl->b1a);   // the mask can start on S
                 }
                 // H += B'^T X^ : A is MN-major over n (NS rows; panels QR*128 bytes apart)
                 // (NS = 64: the second panel reads the next QR*128 bytes, results unused)
 #pragma unroll
                 for (int kk = 0; kk < QR / 16; ++kk)
                     mma_bf16_ss(tmem + K::T_H, dBt + kk * (2048 >> 4), dX + kk * (2048 >> 4), id_u, 1);
-                mma_commit(&ctl->b1);
+                if (FULL) {
+#pragma unroll
+                    for (int kk = 0; kk < NS / 16; ++kk) {   // Yi = C~ Hb_{c-1}
+                        const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
+                        mma_bf16_ss(tmem + K::T_YI, dC + ko, dHb + kk * (2048 >> 4), id_y, kk > 0);
+                    }
+                }
+                mma_commit(&ctl->b1b);
                 ctl->b1_issued += 1;
             }
-            (void)wait_bounded(&ctl->b1, c & 1, fail_c, fail_r);
-            tc_fence_after();
 
-            // ---- mask: SL = S o L (bf16, K-major rows (t,r)) over the dead C~ tile.
-            // 16-column blocks strictly below the diagonal use the factorised decay
-            // 2^(cum2_t - cum2_e) 2^(cum2_e - cum2_s), e = the block's last token (both
-            // factors <= 1; the second, b_s, comes from the rotate group); blocks
-            // holding the diagonal use exp of the difference directly.
             float ecum_t = 0.f;
-            if (warp * 32 < QR) {
-                const int row = tid, t = row / R;
-                const float* cum2 = co + K::CO_CUM2;
-                const float* bneg = box_dt(s);
-                const float ct = cum2[t], rt = co[K::CO_RHO + t];
-                ecum_t = co[K::CO_ECUM + t];
-                uint8_t* sl = tile_c(s);
-                const int tmax = (warp * 32 + 31) / R;   // last token of this warp's rows
-#pragma unroll
-                for (int c32 = 0; c32 < QR; c32 += 32) {
+            if constexpr (FULL) {
+                (void)wait_bounded(&ctl->b1a, i & 1, fail_c, fail_r);
+                tc_fence_after();
+                // ---- mask: SL = S o L (bf16, K-major rows (t,r)) into the X^ / SL buffer,
+                //      once batch 1 (the last reader of X^, C~ and B') is done
+                if constexpr (K::M64) {
+                    // thread = (row, half): row 16 warp + lane % 16, columns [32 half, 32 half + 32)
+                    const int row = warp * 16 + (lane & 15), half = lane >> 4, t = row / R;
+                    const float* cum2 = co + K::CO_CUM2;
+                    const float ct = cum2[t], rt = co[K::CO_RHO + t];
+                    ecum_t = co[K::CO_ECUM + t];
                     float v[32];
-                    const bool any = c32 / R <= tmax;    // warp-uniform
-                    if (any) {
-                        tmem_ld32_sync(tlane + K::T_S + c32, v);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
-                    }
-#pragma unroll
-                    for (int hb2 = 0; hb2 < 2; ++hb2) {
-                        const int cb = c32 + 16 * hb2;
-                        const int s_lo = cb / R, s_hi = (cb + 15) / R;
-                        if (s_lo > t) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) v[16 * hb2 + i] = 0.f;
-                        } else if (s_hi < t) {
-                            const float a = ex2_approx(ct - cum2[s_hi]);
-                            const float2 a2 = make_float2(a, a);
-#pragma unroll
-                            for (int i = 0; i < 16; i += 2) {
-                                const float2 bb = make_float2(bneg[(cb + i) / R], bneg[(cb + i + 1) / R]);
-                                const float2 r2 = __fmul2_rn(make_float2(v[16 * hb2 + i], v[16 * hb2 + i + 1]),
-                                                             __fmul2_rn(a2, bb));
-                                v[16 * hb2 + i] = r2.x;
-                                v[16 * hb2 + i + 1] = r2.y;
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int sidx = (cb + i) / R;
-                                float m = 0.f;
-                                if (sidx < t) m = ex2_approx(ct - cum2[sidx]);
-                                else if (sidx == t) m = rt;
-                                v[16 * hb2 + i] *= m;
-                            }
-                        }
-                    }
+                    tmem_ld16x2_sync(tlane + K::T_S, v);
+                    mask_block<R>(v, 32 * half, t, ct, rt, cum2, co + K::CO_BNEG);
+                    mask_block<R>(v + 16, 32 * half + 16, t, ct, rt, cum2, co + K::CO_BNEG);
+                    (void)wait_bounded(&ctl->b1b, i & 1, fail_c, fail_r);
 #pragma unroll
                     for (int q8 = 0; q8 < 4; ++q8) {
-                        const int col = c32 + q8 * 8;
-                        *reinterpret_cast<uint4*>(sl + (col / 64) * QR * 128 + sw128_offset(row, (col % 64) * 2)) =
+                        const int col = 32 * half + q8 * 8;
+                        *reinterpret_cast<uint4*>(xs + sw128_offset(row, col * 2)) =
                             make_uint4(pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]), pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]),
                                        pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
                     }
-                }
-                fence_proxy_async_smem();
-            }
-            tc_fence_before();
-            group_bar(1);
-            if (tid == 0) {   // batch 2: Y = SL X
-                tc_fence_after();
-                const uint64_t dSL = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
-                const uint64_t dX = smem_desc(smem_u32(tile_x(s)), 16, 1024, kSwizzle128B);
-                constexpr uint32_t id_y = idesc_bf16_f32(128, P, false, true);
+                    fence_proxy_async_smem();
+                } else {
+                    (void)wait_bounded(&ctl->b1b, i & 1, fail_c, fail_r);
+                    if (warp * 32 < QR) {
+                        const int row = tid, t = row / R;
+                        const float* cum2 = co + K::CO_CUM2;
+                        const float ct = cum2[t], rt = co[K::CO_RHO + t];
+                        ecum_t = co[K::CO_ECUM + t];
+                        const int tmax = (warp * 32 + 31) / R;   // last token of this warp's rows
 #pragma unroll
-                for (int kk = 0; kk < QR / 16; ++kk) {
-                    const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
-                    mma_bf16_ss(tmem + K::T_Y, dSL + ko, dX + kk * (2048 >> 4), id_y, kk > 0);
+                        for (int c32 = 0; c32 < QR; c32 += 32) {
+                            float v[32];
+                            if (c32 / R <= tmax) {   // warp-uniform
+                                tmem_ld32_sync(tlane + K::T_S + c32, v);
+                            } else {
+#pragma unroll
+                                for (int i4 = 0; i4 < 32; ++i4) v[i4] = 0.f;
+                            }
+                            mask_block<R>(v, c32, t, ct, rt, cum2, co + K::CO_BNEG);
+                            mask_block<R>(v + 16, c32 + 16, t, ct, rt, cum2, co + K::CO_BNEG);
+#pragma unroll
+                            for (int q8 = 0; q8 < 4; ++q8) {
+                                const int col = c32 + q8 * 8;
+                                *reinterpret_cast<uint4*>(xs + (col / 64) * QR * 128 + sw128_offset(row, (col % 64) * 2)) =
+                                    make_uint4(pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]), pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]),
+                                               pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
+                            }
+                        }
+                        fence_proxy_async_smem();
+                    }
                 }
-                mma_commit(&ctl->b2);
-                ctl->b2_issued += 1;
+                tc_fence_before();
+                group_bar(1);
+                if (tid == 0) {
+                    tc_fence_after();
+                    // C~ and B' are dead: load C, B of local chunk i+2 into this stage
+                    if (i + 2 < nl && !*fail_c) load_cb(i + 2, s);
+                    // batch 2: Y = SL X
+                    const uint64_t dSL = smem_desc(smem_u32(xs), 16, 1024, kSwizzle128B);
+                    const uint64_t dX = smem_desc(smem_u32(tile_x(s)), 16, 1024, kSwizzle128B);
+                    constexpr uint32_t id_y = idesc_bf16_f32(K::MM, P, false, true);
+#pragma unroll
+                    for (int kk = 0; kk < QR / 16; ++kk) {
+                        const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
+                        mma_bf16_ss(tmem + K::T_Y, dSL + ko, dX + kk * (2048 >> 4), id_y, kk > 0);
+                    }
+                    mma_commit(&ctl->b2);
+                    ctl->b2_issued += 1;
+                }
+            } else {
+                (void)wait_bounded(&ctl->b1b, i & 1, fail_c, fail_r);
+                tc_fence_after();
+                // B' and X^ are consumed (X was consumed into X^): the next loads may come in
+                if (tid == 0 && i + 2 < nl && !*fail_c) {
+                    load_cb(i + 2, s);
+                    load_x(i + 2, s);
+                }
+                if (tid == 0) ld_sum += co[K::CO_CEND];
+                if (tid < NP2) th_sum += co[K::CO_THETA + tid];
             }
 
             // ---- state: H <- e_{c+1} R(Theta_c) H ; Hb <- bf16(R(Theta_c) H)   (thread = state row n)
             float e_next = 1.f;
-            if (c + 1 < nc) {
-                const int s1 = (c + 1) & 1;
-                (void)wait_bounded(&ctl->coef_ready[s1], ((c + 1) >> 1) & 1, fail_c, fail_r);
-                e_next = box_lam(s1)[K::CO_EEND];
+            if (i + 1 < nl) {
+                const int s1 = (i + 1) & 1;
+                (void)wait_bounded(&ctl->coef_ready[s1], ((i + 1) >> 1) & 1, fail_c, fail_r);
+                e_next = coef(s1)[K::CO_EEND];
             }
+            tc_fence_after();
             if (tid < NS) {
                 float sn, cs;
                 sincosf(co[K::CO_THETA + (tid >> 1)], &sn, &cs);
@@ -401,45 +534,45 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     tmem_ld32_sync(tlane + K::T_H + cc, hv);
                     float nv[32];
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float2 v = make_float2(hv[i], hv[i + 1]);
-                        const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, hv[i], 1),
-                                                     __shfl_xor_sync(0xffffffffu, hv[i + 1], 1));
+                    for (int i2 = 0; i2 < 32; i2 += 2) {
+                        const float2 v = make_float2(hv[i2], hv[i2 + 1]);
+                        const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, hv[i2], 1),
+                                                     __shfl_xor_sync(0xffffffffu, hv[i2 + 1], 1));
                         const float2 r = __ffma2_rn(c2, v, __fmul2_rn(s2, o));
-                        nv[i] = r.x;
-                        nv[i + 1] = r.y;
+                        nv[i2] = r.x;
+                        nv[i2 + 1] = r.y;
                         const float2 sc = __fmul2_rn(e2, r);
-                        hv[i] = sc.x;
-                        hv[i + 1] = sc.y;
+                        hv[i2] = sc.x;
+                        hv[i2 + 1] = sc.y;
                     }
                     tmem_st32(tlane + K::T_H + cc, hv);
+                    if (FULL) {
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        const uint4 pk = make_uint4(pack_bf16(nv[q8 * 8 + 0], nv[q8 * 8 + 1]),
-                                                    pack_bf16(nv[q8 * 8 + 2], nv[q8 * 8 + 3]),
-                                                    pack_bf16(nv[q8 * 8 + 4], nv[q8 * 8 + 5]),
-                                                    pack_bf16(nv[q8 * 8 + 6], nv[q8 * 8 + 7]));
-                        *reinterpret_cast<uint4*>(hb + sw128_offset(tid, (cc + q8 * 8) * 2)) = pk;
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            const uint4 pk = make_uint4(pack_bf16(nv[q8 * 8 + 0], nv[q8 * 8 + 1]),
+                                                        pack_bf16(nv[q8 * 8 + 2], nv[q8 * 8 + 3]),
+                                                        pack_bf16(nv[q8 * 8 + 4], nv[q8 * 8 + 5]),
+                                                        pack_bf16(nv[q8 * 8 + 6], nv[q8 * 8 + 7]));
+                            *reinterpret_cast<uint4*>(hb + sw128_offset(tid, (cc + q8 * 8) * 2)) = pk;
+                        }
                     }
                 }
                 tmem_st_wait();
-                fence_proxy_async_smem();
+                if (FULL) fence_proxy_async_smem();
             }
 
-            // ---- output rows (t, r) once batch 2 is done; the stage is then free for chunk c+2
-            (void)wait_bounded(&ctl->b2, c & 1, fail_c, fail_r);
-            tc_fence_after();
-            if (tid == 0 && c + 2 < nc && !*fail_c) issue_loads(c + 2, s);
-            if (warp * 32 < QR) {
-                const int row = tid, t = row / R, r = row % R;
-                const int tok = c * Q + t;
-                __nv_bfloat16* yrow = args.y + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P;
-                const float2 e2 = make_float2(ecum_t, ecum_t);
-#pragma unroll
-                for (int cc = 0; cc < P; cc += 32) {
+            if constexpr (FULL) {
+                // ---- output rows (t, r) once batch 2 is done; X of chunk i+2 may then come in
+                (void)wait_bounded(&ctl->b2, i & 1, fail_c, fail_r);
+                tc_fence_after();
+                if (tid == 0 && i + 2 < nl && !*fail_c) load_x(i + 2, s);
+                if constexpr (K::M64) {
+                    const int row = warp * 16 + (lane & 15), half = lane >> 4, t = row / R, r = row % R;
+                    const int tok = c * Q + t;
+                    __nv_bfloat16* yrow = args.y + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P + 32 * half;
+                    const float2 e2 = make_float2(ecum_t, ecum_t);
                     float yv[32], iv[32];
-                    tmem_ld32_sync(tlane + K::T_Y + cc, yv);
-                    tmem_ld32_sync(tlane + K::T_YI + cc, iv);
+                    tmem_ld16x2x2_sync(tlane + K::T_Y, tlane + K::T_YI, yv, iv);
                     uint32_t pk[16];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
@@ -450,8 +583,31 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     if (tok < T) {
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4)
-                            *reinterpret_cast<uint4*>(yrow + cc + 8 * q4) =
+                            *reinterpret_cast<uint4*>(yrow + 8 * q4) =
                                 make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                    }
+                } else if (warp * 32 < QR) {
+                    const int row = tid, t = row / R, r = row % R;
+                    const int tok = c * Q + t;
+                    __nv_bfloat16* yrow = args.y + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P;
+                    const float2 e2 = make_float2(ecum_t, ecum_t);
+#pragma unroll
+                    for (int cc = 0; cc < P; cc += 32) {
+                        float yv[32], iv[32];
+                        tmem_ld32x2_sync(tlane + K::T_Y + cc, tlane + K::T_YI + cc, yv, iv);
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const float2 o = __ffma2_rn(e2, make_float2(iv[2 * q], iv[2 * q + 1]),
+                                                        make_float2(yv[2 * q], yv[2 * q + 1]));
+                            pk[q] = pack_bf16(o.x, o.y);
+                        }
+                        if (tok < T) {
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                *reinterpret_cast<uint4*>(yrow + cc + 8 * q4) =
+                                    make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                        }
                     }
                 }
             }
@@ -459,27 +615,37 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             group_bar(1);
             if (tid == 0) {
                 ctl->b1_waited += 1;
-                ctl->b2_waited += 1;
+                if (FULL) ctl->b2_waited += 1;
             }
             if (*fail_c) break;
         }
-        if (!*fail_c && !*fail_r && args.final_state != nullptr && tid < NS) {
+        // the carry after the segment's last chunk (e_next = 1): the physical-frame state
+        float* dst = nullptr;
+        if (FULL) {
+            if (seg == args.nseg - 1) dst = args.final_state;
+            if (dst != nullptr) dst += (int64_t)bh * NS * P;
+        } else {
+            dst = args.seg_U + ((int64_t)bh * (args.S - 1) + seg) * NS * P;
+            if (!*fail_c && !*fail_r) {
+                if (tid == 0) args.seg_ld[(int64_t)bh * (args.S - 1) + seg] = ld_sum;
+                if (tid < NP2) args.seg_th[((int64_t)bh * (args.S - 1) + seg) * NP2 + tid] = th_sum;
+            }
+        }
+        if (!*fail_c && !*fail_r && dst != nullptr && tid < NS) {
             tc_fence_after();
-            float* fs = args.final_state + ((int64_t)bh * NS + tid) * P;
+            float* fs = dst + (int64_t)tid * P;
 #pragma unroll
-            for (int cc = 0; cc < P; cc += 16) {
-                float v[16];
-                tmem_ld16(tlane + K::T_H + cc, v);
-                tmem_ld_wait();
+            for (int cc = 0; cc < P; cc += 32) {
+                float v[32];
+                tmem_ld32_sync(tlane + K::T_H + cc, v);
 #pragma unroll
-                for (int i = 0; i < 16; i += 4)
-                    *reinterpret_cast<float4*>(fs + cc + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                for (int i4 = 0; i4 < 32; i4 += 4)
+                    *reinterpret_cast<float4*>(fs + cc + i4) = make_float4(v[i4], v[i4 + 1], v[i4 + 2], v[i4 + 3]);
             }
         }
     } else {
         // =============================== rotate ===============================
         const int rt = tid - 128, rw = rt >> 5;
-        float* sPart = reinterpret_cast<float*>(sm + K::OFF_PART);
         float* sW = reinterpret_cast<float*>(sm + K::OFF_RPRIV);
         float* sF = sW + Q;
         float* sWarpR = sF + Q;
@@ -490,86 +656,97 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         float4 om[TPG];
         auto load_omega = [&](int c) {
 #pragma unroll
-            for (int i = 0; i < TPG; ++i) {
-                const int t = c * Q + tg * TPG + i;
-                om[i] = t < T ? *reinterpret_cast<const float4*>(om_base + t * om_tok) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < TPG; ++k) {
+                const int t = c * Q + tg * TPG + k;
+                om[k] = t < T ? *reinterpret_cast<const float4*>(om_base + t * om_tok) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         };
-        load_omega(0);
+        load_omega(c_begin);
         const float a = args.A[h];
-        for (int c = 0; c < nc; ++c) {
-            const int s = c & 1;
-            (void)wait_bounded(&ctl->full[s], (c >> 1) & 1, fail_r, fail_c);
+        for (int i = 0; i < nl; ++i) {
+            const int c = c_begin + i, s = i & 1;
+            (void)wait_bounded(&ctl->fbox[s], (i >> 1) & 1, fail_r, fail_c);
             group_bar(2);
             if (*fail_r) break;
-            if (rt == 0) ctl->tma_waited[s] += 1;
+            if (rt == 0) ctl->box_waited[s] += 1;
             const float* sDt = box_dt(s);
-            float* sLam = box_lam(s);
-            float* co = sLam;   // coefficient block, written once lambda is read
+            const float* sLam = box_lam(s);
+            float* co = coef(s);
+            float* sPart = K::PART_IN_BOX ? box_dt(s) : reinterpret_cast<float*>(sm + K::OFF_PART);
 
-            // ---- coefficients and chunk-local log-decay prefix
-            float ell = 0.f, gam = 0.f, wv = 0.f;
+            // ---- every value the chunk needs from the boxes, into registers
+            float d = 0.f, l = 0.f, dn = 0.f, ln = 0.f;
             if (rt < Q) {
-                const float d = sDt[rt * 4 + hq], l = sLam[rt * 4 + hq];
-                const float dn = sDt[(rt + 1) * 4 + hq], ln = sLam[(rt + 1) * 4 + hq];
-                ell = d * a;
-                gam = l * d;
-                wv = gam + (1.f - ln) * dn;
+                d = sDt[rt * 4 + hq];
+                l = sLam[rt * 4 + hq];
+                dn = sDt[(rt + 1) * 4 + hq];
+                ln = sLam[(rt + 1) * 4 + hq];
             }
+            float dtk[TPG];
+#pragma unroll
+            for (int k = 0; k < TPG; ++k) dtk[k] = sDt[(tg * TPG + k) * 4 + hq];
+            // ---- coefficients and chunk-local log-decay prefix
+            const float ell = d * a, gam = l * d, wv = gam + (1.f - ln) * dn;
             float cum = warp_inclusive_sum(ell);
             if (lane == 31) sWarpR[rw] = cum;
-            group_bar(2);   // also: every lambda read is done
+            group_bar(2);   // every box value is read (the boxes may now hold partial sums)
             float off = 0.f, cend = 0.f;
-            for (int i = 0; i < 4; ++i) {
-                const float v = sWarpR[i];
-                if (i < rw) off += v;
+            for (int k = 0; k < 4; ++k) {
+                const float v = sWarpR[k];
+                if (k < rw) off += v;
                 cend += v;
             }
             cum += off;
             if (rt < Q) {
-                co[K::CO_CUM2 + rt] = cum * kLog2e;
-                co[K::CO_RHO + rt] = wv > 0.f ? gam / wv : 0.f;
-                co[K::CO_ECUM + rt] = __expf(cum);
+                if (FULL) {
+                    co[K::CO_CUM2 + rt] = cum * kLog2e;
+                    co[K::CO_RHO + rt] = wv > 0.f ? gam / wv : 0.f;
+                    co[K::CO_ECUM + rt] = __expf(cum);
+                }
                 sW[rt] = wv;
                 sF[rt] = __expf(cend - cum);
             }
-            if (rt == 0) co[K::CO_EEND] = __expf(cend);
-
+            if (rt == 0) {
+                co[K::CO_EEND] = __expf(cend);
+                co[K::CO_CEND] = cend;
+            }
             // ---- rotation angles: partial sums per token group
-            float dtk[TPG];
             {
                 float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int i = 0; i < TPG; ++i) {
-                    const float d = sDt[(tg * TPG + i) * 4 + hq];
-                    dtk[i] = d;
-                    part.x = fmaf(d, om[i].x, part.x);
-                    part.y = fmaf(d, om[i].y, part.y);
-                    part.z = fmaf(d, om[i].z, part.z);
-                    part.w = fmaf(d, om[i].w, part.w);
+                for (int k = 0; k < TPG; ++k) {
+                    part.x = fmaf(dtk[k], om[k].x, part.x);
+                    part.y = fmaf(dtk[k], om[k].y, part.y);
+                    part.z = fmaf(dtk[k], om[k].z, part.z);
+                    part.w = fmaf(dtk[k], om[k].w, part.w);
                 }
                 *reinterpret_cast<float4*>(&sPart[tg * NP2 + 4 * jg]) = part;
             }
-            group_bar(2);   // every dt read is done: the dt box now takes b_s for the mask
-            if (rt < Q) {
-                const int e_tok = ((rt * R) / 16 * 16 + 15) / R;   // last token of s's 16-column block
-                box_dt(s)[rt] = ex2_approx(co[K::CO_CUM2 + e_tok] - co[K::CO_CUM2 + rt]);
+            group_bar(2);   // coefficient block and partial sums written
+            if (FULL && rt < Q) {   // b_s of the mask: 2^(cum2[last token of s's 16-column block] - cum2[s])
+                const int e_tok = ((rt * R) / 16 * 16 + 15) / R;
+                co[K::CO_BNEG + rt] = ex2_approx(co[K::CO_CUM2 + e_tok] - co[K::CO_CUM2 + rt]);
             }
+            // the consumer may use exp(cum_end) of this chunk now
+            mbar_arrive(&ctl->coef_ready[s]);
+            float4 psi = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int g = 0; g < tg; ++g) {
+                const float4 p4 = *reinterpret_cast<const float4*>(&sPart[g * NP2 + 4 * jg]);
+                psi.x += p4.x; psi.y += p4.y; psi.z += p4.z; psi.w += p4.w;
+            }
+            // ---- rotate C and B in place once they have landed
+            (void)wait_bounded(&ctl->fcb[s], (i >> 1) & 1, fail_r, fail_c);
+            if (rt == 0) ctl->cb_waited[s] += 1;
             {
-                float4 psi = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int g = 0; g < tg; ++g) {
-                    const float4 p4 = *reinterpret_cast<const float4*>(&sPart[g * NP2 + 4 * jg]);
-                    psi.x += p4.x; psi.y += p4.y; psi.z += p4.z; psi.w += p4.w;
-                }
                 uint8_t* tC = tile_c(s);
                 uint8_t* tB = tile_b(s);
 #pragma unroll
-                for (int i = 0; i < TPG; ++i) {
-                    const int t = tg * TPG + i;
-                    psi.x = fmaf(dtk[i], om[i].x, psi.x);
-                    psi.y = fmaf(dtk[i], om[i].y, psi.y);
-                    psi.z = fmaf(dtk[i], om[i].z, psi.z);
-                    psi.w = fmaf(dtk[i], om[i].w, psi.w);
+                for (int k = 0; k < TPG; ++k) {
+                    const int t = tg * TPG + k;
+                    psi.x = fmaf(dtk[k], om[k].x, psi.x);
+                    psi.y = fmaf(dtk[k], om[k].y, psi.y);
+                    psi.z = fmaf(dtk[k], om[k].z, psi.z);
+                    psi.w = fmaf(dtk[k], om[k].w, psi.w);
                     float cs[4], sn[4];
                     __sincosf(-psi.x, &sn[0], &cs[0]);
                     __sincosf(-psi.y, &sn[1], &cs[1]);
@@ -584,21 +761,26 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const uint32_t off2 = pan * QR * 128 + sw128_offset(t * R + r, cib);
-                        uint4* pc = reinterpret_cast<uint4*>(tC + off2);
+                        if (FULL) {
+                            uint4* pc = reinterpret_cast<uint4*>(tC + off2);
+                            *pc = rotate4(*pc, c01, s01);
+                        }
                         uint4* pb = reinterpret_cast<uint4*>(tB + off2);
-                        *pc = rotate4(*pc, c01, s01);
                         *pb = rotate4(*pb, cw01, sw01);
                     }
                 }
                 if (tg == TG - 1) *reinterpret_cast<float4*>(&co[K::CO_THETA + 4 * jg]) = psi;
             }
-            // the consumer may read this stage's coefficient block now
-            mbar_arrive(&ctl->coef_ready[s]);
-            if (c + 1 < nc) load_omega(c + 1);
+            if (i + 1 < nl) load_omega(c + 1);
+            group_bar(2);   // partial sums read: the boxes may take chunk i+2
+            if (rt == 0 && i + 2 < nl && !*fail_r) load_box(i + 2, s);
 
-            // ---- X^ = exp(cum_end - cum_s) X into the single X^ buffer, once batch 1 of
-            //      chunk c-1 (its last reader) is done
-            if (c > 0) (void)wait_bounded(&ctl->b1, (c - 1) & 1, fail_r, fail_c);
+            // ---- X^ = exp(cum_end - cum_s) X into the X^ / SL buffer, once the previous
+            //      chunk's last reader of that buffer is done (batch 2, or batch 1 in the
+            //      state pass) and X has landed
+            if (i > 0) (void)wait_bounded(FULL ? &ctl->b2 : &ctl->b1b, (i - 1) & 1, fail_r, fail_c);
+            (void)wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_r, fail_c);
+            if (rt == 0) ctl->x_waited[s] += 1;
             {
                 const uint8_t* tX = tile_x(s);
                 // QR rows x 8 16-byte pieces; 128 threads
@@ -614,12 +796,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                         const float2 g = __fmul2_rn(f2, make_float2(bf_lo(w[e]), bf_hi(w[e])));
                         w[e] = pack_bf16(g.x, g.y);
                     }
-                    *reinterpret_cast<uint4*>(xhat + off2) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(xs + off2) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             fence_proxy_async_smem();
             mbar_arrive(&ctl->rot_done[s]);
-            group_bar(2);   // sW / sF / sPart are reused by the next chunk
+            group_bar(2);   // sW / sF are reused by the next chunk
             if (*fail_r) break;
         }
     }
@@ -631,10 +813,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         atomicExch(args.status, (int)M3_ERR_TIMEOUT);
         // let copies and MMAs still in flight finish (bounded) before the shared
         // memory and TMEM go away
-        for (int s = 0; s < 2; ++s)
-            for (int k = ctl->tma_waited[s]; k < ctl->tma_issued[s]; ++k)
-                (void)mbar_wait(&ctl->full[s], k & 1, kWaitLimitNs);
-        for (int k = ctl->b1_waited; k < ctl->b1_issued; ++k) (void)mbar_wait(&ctl->b1, k & 1, kWaitLimitNs);
+        for (int s = 0; s < 2; ++s) {
+            for (int k = ctl->box_waited[s]; k < ctl->box_issued[s]; ++k) (void)mbar_wait(&ctl->fbox[s], k & 1, kWaitLimitNs);
+            for (int k = ctl->cb_waited[s]; k < ctl->cb_issued[s]; ++k) (void)mbar_wait(&ctl->fcb[s], k & 1, kWaitLimitNs);
+            for (int k = ctl->x_waited[s]; k < ctl->x_issued[s]; ++k) (void)mbar_wait(&ctl->fx[s], k & 1, kWaitLimitNs);
+        }
+        for (int k = ctl->b1_waited; k < ctl->b1_issued; ++k) (void)mbar_wait(&ctl->b1b, k & 1, kWaitLimitNs);
         for (int k = ctl->b2_waited; k < ctl->b2_issued; ++k) (void)mbar_wait(&ctl->b2, k & 1, kWaitLimitNs);
     }
     __syncthreads();
@@ -670,6 +854,51 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Sequence segments: with fewer (batch, head) sequences than CTA slots on the
+// GPU, each sequence is cut into S segments of L chunks so that the machine
+// fills up; a state pass gives every segment's carry from a zero start, the
+// segment scan (m3_state_passing's kernel) turns those into the state entering
+// each segment, and the full pass starts each segment from it.
+constexpr int kPlanSMs = 148;   // SMs of the B300 the plan is sized for (fixed: the workspace size must not depend on the device)
+
+struct SegPlan {
+    int S, L, nc;
+};
+
+template <int NS, int R, int Q>
+SegPlan seg_plan(const ScanDims& d) {
+    using K = Cfg<NS, R, Q>;
+    SegPlan p;
+    p.nc = (int)((d.seqlen + Q - 1) / Q);
+    const int64_t seqs = d.batch * d.nheads, slots = (int64_t)kPlanSMs * K::MIN_BLOCKS;
+    int64_t S = seqs >= slots ? 1 : slots / seqs;
+    if (S > p.nc) S = p.nc;
+    if (S < 1) S = 1;
+    p.L = (int)((p.nc + S - 1) / S);
+    p.S = (p.nc + p.L - 1) / p.L;   // no empty segment
+    return p;
+}
+
+struct SegWs {
+    size_t status, U, ld, th, last, total;
+};
+
+inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+template <int NS, int R, int Q>
+SegWs seg_ws(const ScanDims& d) {
+    const SegPlan p = seg_plan<NS, R, Q>(d);
+    const size_t seqs = (size_t)(d.batch * d.nheads), P = (size_t)d.headdim, S1 = (size_t)(p.S - 1);
+    SegWs w;
+    w.status = 0;
+    w.U = 256;
+    w.ld = w.U + (p.S > 1 ? al256(S1 * seqs * NS * P * 4) : 0);
+    w.th = w.ld + (p.S > 1 ? al256(S1 * seqs * 4) : 0);
+    w.last = w.th + (p.S > 1 ? al256(S1 * seqs * (NS / 2) * 4) : 0);
+    w.total = w.last + (p.S > 1 ? al256(seqs * NS * P * 4) : 0);
+    return w;
+}
+
 template <int NS, int R, int Q>
 cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                        const float* A, const float* lambda, const float* omega, void* y, float* final_state,
@@ -702,49 +931,107 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
         if (!make_map(&mlam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, lambda, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
-    TcArgs args;
+    const SegPlan pl = seg_plan<NS, R, Q>(d);
+    const SegWs ws = seg_ws<NS, R, Q>(d);
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    const int64_t seqs = d.batch * d.nheads;
+    TcArgs args{};
     args.A = A;
     args.omega = omega;
     args.y = static_cast<__nv_bfloat16*>(y);
     args.final_state = final_state;
-    args.status = static_cast<int*>(workspace);
+    args.status = reinterpret_cast<int*>(wsb + ws.status);
     args.T = (int)d.seqlen;
     args.H = (int)d.nheads;
-    args.nc = (int)d.nchunks();
-    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int), stream);
+    args.nc = pl.nc;
+    args.L = pl.L;
+    args.S = pl.S;
+    cudaError_t e = cudaMemsetAsync(args.status, 0, sizeof(int), stream);
     if (e != cudaSuccess) return e;
-    auto kern = scan_tc_kernel<NS, R, Q>;
+    if (pl.S > 1) {
+        float* segU = reinterpret_cast<float*>(wsb + ws.U);
+        float* segLD = reinterpret_cast<float*>(wsb + ws.ld);
+        float* segTH = reinterpret_cast<float*>(wsb + ws.th);
+        float* last = reinterpret_cast<float*>(wsb + ws.last);
+        TcArgs a1 = args;
+        a1.nseg = pl.S - 1;
+        a1.seg_U = segU;
+        a1.seg_ld = segLD;
+        a1.seg_th = segTH;
+        auto k1 = scan_tc_kernel<NS, R, Q, false>;
+        e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
+        if (e != cudaSuccess) return e;
+        k1<<<(unsigned)(seqs * a1.nseg), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, a1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // segment carries -> the state entering each segment (in place), and into the last one
+        e = launch_state_passing(segU, segLD, segTH, nullptr, last, 1, seqs, pl.S - 1, NS, (int64_t)P, stream);
+        if (e != cudaSuccess) return e;
+        args.h_in = segU;
+        args.h_in_last = last;
+    }
+    args.nseg = pl.S;
+    auto kern = scan_tc_kernel<NS, R, Q, true>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(d.batch * d.nheads), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, args);
+    kern<<<(unsigned)(seqs * pl.S), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, args);
     return cudaGetLastError();
 }
 
+template <int NS, int R, int Q>
+size_t ws_cfg(const ScanDims& d) { return seg_ws<NS, R, Q>(d).total; }
+template <int NS, int R, int Q>
+int launches_cfg(const ScanDims& d) { return seg_plan<NS, R, Q>(d).S > 1 ? 3 : 1; }
+
 typedef cudaError_t (*LaunchFn)(const ScanDims&, const void*, const void*, const void*, const float*, const float*,
                                 const float*, const float*, void*, float*, void*, cudaStream_t);
+struct TcImpl {
+    LaunchFn launch;
+    size_t (*workspace)(const ScanDims&);
+    int (*launches)(const ScanDims&);
+};
 
-LaunchFn pick(const ScanDims& d) {
-    if (d.headdim != 64 || d.io != M3_DTYPE_BF16) return nullptr;
-    if (d.nheads % 4) return nullptr;
-    if (d.dstate == 128) {
-        if (d.R == 1 && d.chunk == 64) return launch_cfg<128, 1, 64>;
-        if (d.R == 1 && d.chunk == 128) return launch_cfg<128, 1, 128>;
-        if (d.R == 2 && d.chunk == 64) return launch_cfg<128, 2, 64>;
-    }
-    return nullptr;
+template <int NS, int R, int Q>
+TcImpl impl() { return TcImpl{launch_cfg<NS, R, Q>, ws_cfg<NS, R, Q>, launches_cfg<NS, R, Q>}; }
+
+// Tile configuration for (N, R, chunk).  Chunks of chunk*R <= 128 rows run as
+// given.  Wider MIMO chunks run as sub-chunks of chunk/R tokens -- the MIMO
+// chunk-length reduction of section 3.3 -- so that every score tile stays at
+// chunk x chunk rows; the state passes between sub-chunks exactly as between
+// chunks, and the result differs only in rounding.
+bool pick(const ScanDims& d, TcImpl* out) {
+    if (d.headdim != 64 || d.io != M3_DTYPE_BF16) return false;
+    if (d.nheads % 4) return false;
+    const int N = (int)d.dstate, R = d.R, Q = d.chunk;
+    TcImpl f{};
+    if (N == 128 && R == 1 && Q == 64) f = impl<128, 1, 64>();
+    else if (N == 128 && R == 1 && Q == 128) f = impl<128, 1, 128>();
+    else if (N == 128 && R == 2 && Q == 64) f = impl<128, 2, 64>();
+    else if (N == 64 && R == 1 && Q == 64) f = impl<64, 1, 64>();
+    else if (N == 64 && R == 4 && Q == 64) f = impl<64, 4, 16>();
+    else if (N == 128 && R == 4 && Q == 64) f = impl<128, 4, 16>();
+    else if (N == 128 && R == 4 && Q == 128) f = impl<128, 4, 32>();
+    else return false;
+    if (out) *out = f;
+    return true;
 }
 
 }  // namespace
 
-size_t tc_workspace_size(const ScanDims&) { return 256; }
-bool tc_supported(const ScanDims& d) { return d.seqlen > 0 && pick(d) != nullptr; }
-int tc_launch_count(const ScanDims&) { return 1; }
+size_t tc_workspace_size(const ScanDims& d) {
+    TcImpl f;
+    return pick(d, &f) ? f.workspace(d) : 0;
+}
+bool tc_supported(const ScanDims& d) { return d.seqlen > 0 && pick(d, nullptr); }
+int tc_launch_count(const ScanDims& d) {
+    TcImpl f;
+    return pick(d, &f) ? f.launches(d) : 0;
+}
 cudaError_t launch_scan_tc(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                            const float* A, const float* lambda, const float* omega, void* y, float* final_state,
                            void* workspace, cudaStream_t stream) {
-    LaunchFn f = pick(d);
-    if (!f) return cudaErrorNotSupported;
-    return f(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, stream);
+    TcImpl f;
+    if (!pick(d, &f)) return cudaErrorNotSupported;
+    return f.launch(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, stream);
 }
 
 }  // namespace m3
