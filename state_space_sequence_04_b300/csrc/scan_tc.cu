@@ -31,9 +31,11 @@
 // H after the last chunk is the true final state h_{T-1}.
 //
 // Warp roles (256 threads): warps 0-3 "consumer" (mask, state, output; thread
-// 0 issues every MMA and TMA), warps 4-7 "rotate" (coefficients, angles,
-// rotation, X^), which run one chunk ahead of the consumer on the other
-// shared-memory stage.  Every wait is bounded: on timeout the kernel records
+// 0 issues every MMA and the C/B and X loads), warps 4-7 "rotate"
+// (coefficients, angles, rotation, X^, the dt/lambda loads), which run one
+// chunk ahead of the consumer on the other shared-memory stage.  The next
+// chunk's score MMA is issued as soon as its operands are rotated, so that it
+// overlaps the current chunk's state step and output.  Every wait is bounded: on timeout the kernel records
 // M3_ERR_TIMEOUT in the status word, drains its copies and MMAs and exits.
 //
 // MMA operand layouts (all 128-byte swizzled, bf16):
@@ -93,19 +95,19 @@ struct Cfg {
     static constexpr int PART_BYTES = TG * (NS / 2) * 4;          // partial angle sums [TG][NS/2]
     // the partial sums go over the stage's two boxes once their values are in registers
     static constexpr bool PART_IN_BOX = PART_BYTES <= 2 * BOX_STRIDE;
-    // coefficient block of a stage (floats): cum*log2e[Q], rho[Q], exp(cum)[Q], b[Q], Theta[NS/2],
-    // exp(cum_end), cum_end
-    static constexpr int CO_CUM2 = 0, CO_RHO = Q, CO_ECUM = 2 * Q, CO_BNEG = 3 * Q, CO_THETA = 4 * Q,
-                         CO_EEND = 4 * Q + NS / 2, CO_CEND = 4 * Q + NS / 2 + 1;
-    static constexpr int CO_BYTES = align_up((4 * Q + NS / 2 + 2) * 4, 16);
+    // coefficient block of a stage (floats): cum*log2e[Q], rho[Q], exp(cum)[Q], b[Q],
+    // f = exp(cum_end - cum)[Q], Theta[NS/2], exp(cum_end), cum_end
+    static constexpr int CO_CUM2 = 0, CO_RHO = Q, CO_ECUM = 2 * Q, CO_BNEG = 3 * Q, CO_F = 4 * Q, CO_THETA = 5 * Q,
+                         CO_EEND = 5 * Q + NS / 2, CO_CEND = 5 * Q + NS / 2 + 1;
+    static constexpr int CO_BYTES = align_up((5 * Q + NS / 2 + 2) * 4, 16);
 
     static constexpr int OFF_XS = 2 * STG_TILE;                   // X^, then SL
     static constexpr int OFF_HB = OFF_XS + XS_BYTES;
     static constexpr int OFF_BOX = OFF_HB + NS * 128;             // [stage][dt | lambda]
     static constexpr int OFF_PART = OFF_BOX + 4 * BOX_STRIDE;     // only when not in the boxes
     static constexpr int OFF_CO = OFF_PART + (PART_IN_BOX ? 0 : align_up(PART_BYTES, 16));
-    static constexpr int OFF_RPRIV = OFF_CO + 2 * CO_BYTES;       // w[Q], f[Q], warp sums[4]
-    static constexpr int OFF_BAR = align_up(OFF_RPRIV + (2 * Q + 4) * 4, 16);
+    static constexpr int OFF_RPRIV = OFF_CO + 2 * CO_BYTES;       // w[Q], warp sums[4]
+    static constexpr int OFF_BAR = align_up(OFF_RPRIV + (Q + 4) * 4, 16);
     static constexpr int SMEM = OFF_BAR + 192 + 1024;             // barriers / flags, alignment slack
     // two CTAs per SM when both fit (228 KB per SM, 1 KB reserved per CTA)
     static constexpr int MIN_BLOCKS = 2 * (SMEM + 1024) <= 233472 ? 2 : 1;
@@ -118,6 +120,7 @@ struct Cfg {
     static constexpr int T_H = QR + 2 * P;
     static constexpr int TMEM_COLS = (QR + 3 * P) <= 256 ? 256 : 512;
     static_assert(SMEM <= 232448, "shared memory over the 227 KB per-CTA limit");
+    static_assert(!M64 || MIN_BLOCKS == 2, "64-row tiles are laid out for two CTAs per SM");
 };
 
 struct TcArgs {
@@ -144,13 +147,16 @@ struct Ctl {
     uint64_t fbox[2], fcb[2], fx[2];   // TMA groups landed
     uint64_t rot_done[2];    // rotate group finished the stage (count 128)
     uint64_t coef_ready[2];  // coefficient block of the stage written (count 128)
+    uint64_t coef_free[2];   // consumer done reading the stage's coefficient block (count 128)
     uint64_t b1a;            // MMA batch 1, scores S, complete
     uint64_t b1b;            // MMA batch 1 complete (chunk state onto H, inter readout Yi)
     uint64_t b2;             // MMA batch 2 complete
     uint32_t tmem;
     int fail_c, fail_r;      // per-group failure flags
-    int box_issued[2], box_waited[2], cb_issued[2], cb_waited[2], x_issued[2], x_waited[2];
-    int b1_issued, b2_issued, b1_waited, b2_waited;
+    // copies / MMA batches issued and waited for, modulo 2^16 (only their difference,
+    // at most 2, and their parity matter: they drive the bounded drain on failure)
+    uint16_t box_issued[2], box_waited[2], cb_issued[2], cb_waited[2], x_issued[2], x_waited[2];
+    uint16_t b1_issued, b2_issued, b1_waited, b2_waited;
 };
 static_assert(sizeof(Ctl) <= 192, "control block must fit its reserved space");
 
@@ -264,6 +270,24 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
     auto coef = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_CO + s * K::CO_BYTES); };
     uint8_t* xs = sm + K::OFF_XS;   // X^ of the chunk being set up, then SL of the chunk being masked
     uint8_t* hb = sm + K::OFF_HB;
+    // X^ = exp(cum_end - cum_s) X of the chunk in stage s, into the X^ / SL buffer (consumer threads)
+    auto make_xhat = [&](int s) {   // rotate threads
+        const uint8_t* tX = tile_x(s);
+        const float* f = coef(s) + K::CO_F;
+        for (int pidx = threadIdx.x - 128; pidx < QR * 8; pidx += 128) {   // QR rows x 8 16-byte pieces
+            const int row = pidx >> 3, piece = pidx & 7;
+            const float2 f2 = make_float2(f[row / R], f[row / R]);
+            const uint32_t off2 = sw128_offset(row, piece * 16);
+            const uint4 v = *reinterpret_cast<const uint4*>(tX + off2);
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 g = __fmul2_rn(f2, make_float2(bf_lo(w[e]), bf_hi(w[e])));
+                w[e] = pack_bf16(g.x, g.y);
+            }
+            *reinterpret_cast<uint4*>(xs + off2) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    };
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -272,6 +296,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             mbar_init(&ctl->fx[s], 1);
             mbar_init(&ctl->rot_done[s], 128);
             mbar_init(&ctl->coef_ready[s], 128);
+            mbar_init(&ctl->coef_free[s], 128);
             ctl->box_issued[s] = ctl->box_waited[s] = 0;
             ctl->cb_issued[s] = ctl->cb_waited[s] = 0;
             ctl->x_issued[s] = ctl->x_waited[s] = 0;
@@ -385,6 +410,19 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         group_bar(1);
         const bool odd = tid & 1;
         float ld_sum = 0.f, th_sum = 0.f;   // state pass: summed log-decay (thread 0), angle of pair tid
+        // S = C~ B'^T of the chunk in stage s, committed on b1a (thread 0)
+        auto issue_scores = [&](int s) {
+            const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
+            const uint64_t dB = smem_desc(smem_u32(tile_b(s)), 16, 1024, kSwizzle128B);
+            constexpr uint32_t id_s = idesc_bf16_f32(K::MM, QR, false, false);
+#pragma unroll
+            for (int kk = 0; kk < NS / 16; ++kk) {
+                const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
+                mma_bf16_ss(tmem + K::T_S, dC + ko, dB + ko, id_s, kk > 0);
+            }
+            mma_commit(&ctl->b1a);
+        };
+
         for (int i = 0; i < nl; ++i) {
             const int c = c_begin + i, s = i & 1;
             const float* co = coef(s);
@@ -397,21 +435,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 tc_fence_after();
                 // descriptors of the operand bases; a byte offset o moves the start address field by o >> 4
                 const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
-                const uint64_t dB = smem_desc(smem_u32(tile_b(s)), 16, 1024, kSwizzle128B);
                 const uint64_t dBt = smem_desc(smem_u32(tile_b(s)), QR * 128, 1024, kSwizzle128B);
                 const uint64_t dX = smem_desc(smem_u32(xs), 16, 1024, kSwizzle128B);
                 const uint64_t dHb = smem_desc(smem_u32(hb), 16, 1024, kSwizzle128B);
-                constexpr uint32_t id_s = idesc_bf16_f32(K::MM, QR, false, false);
                 constexpr uint32_t id_y = idesc_bf16_f32(K::MM, P, false, true);
                 constexpr uint32_t id_u = idesc_bf16_f32(128, P, true, true);
-                if (FULL) {
-#pragma unroll
-                    for (int kk = 0; kk < NS / 16; ++kk) {   // S = C~ B'^T
-                        const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
-                        mma_bf16_ss(tmem + K::T_S, dC + ko, dB + ko, id_s, kk > 0);
-                    }
-                    mma_commit(&ctl->b1a);   // the mask can start on S
-                }
+                if (FULL) issue_scores(s);
                 // H += B'^T X^ : A is MN-major over n (NS rows; panels QR*128 bytes apart)
                 // (NS = 64: the second panel reads the next QR*128 bytes, results unused)
 #pragma unroll
@@ -560,6 +589,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 tmem_st_wait();
                 if (FULL) fence_proxy_async_smem();
             }
+            // every read of this stage's coefficient block is done (the output keeps exp(cum_t)
+            // in a register): the rotate group may fill it for chunk i+2
+            mbar_arrive(&ctl->coef_free[s]);
 
             if constexpr (FULL) {
                 // ---- output rows (t, r) once batch 2 is done; X of chunk i+2 may then come in
@@ -647,8 +679,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         // =============================== rotate ===============================
         const int rt = tid - 128, rw = rt >> 5;
         float* sW = reinterpret_cast<float*>(sm + K::OFF_RPRIV);
-        float* sF = sW + Q;
-        float* sWarpR = sF + Q;
+        float* sWarpR = sW + Q;
         const int jg = rt % NG, tg = rt / NG;
         const int pan = jg / 8, cib = (jg % 8) * 16;     // panel and byte-in-row of my 16-byte piece
         const float* om_base = args.omega + ((int64_t)b * T * args.H + h) * NP2 + 4 * jg;
@@ -689,6 +720,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             const float ell = d * a, gam = l * d, wv = gam + (1.f - ln) * dn;
             float cum = warp_inclusive_sum(ell);
             if (lane == 31) sWarpR[rw] = cum;
+            // the consumer is done with chunk i-2's coefficients in this stage
+            if (i >= 2) (void)wait_bounded(&ctl->coef_free[s], ((i - 2) >> 1) & 1, fail_r, fail_c);
             group_bar(2);   // every box value is read (the boxes may now hold partial sums)
             float off = 0.f, cend = 0.f;
             for (int k = 0; k < 4; ++k) {
@@ -704,7 +737,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     co[K::CO_ECUM + rt] = __expf(cum);
                 }
                 sW[rt] = wv;
-                sF[rt] = __expf(cend - cum);
+                co[K::CO_F + rt] = __expf(cend - cum);
             }
             if (rt == 0) {
                 co[K::CO_EEND] = __expf(cend);
@@ -727,16 +760,19 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 const int e_tok = ((rt * R) / 16 * 16 + 15) / R;
                 co[K::CO_BNEG + rt] = ex2_approx(co[K::CO_CUM2 + e_tok] - co[K::CO_CUM2 + rt]);
             }
-            // the consumer may use exp(cum_end) of this chunk now
-            mbar_arrive(&ctl->coef_ready[s]);
             float4 psi = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int g = 0; g < tg; ++g) {
                 const float4 p4 = *reinterpret_cast<const float4*>(&sPart[g * NP2 + 4 * jg]);
                 psi.x += p4.x; psi.y += p4.y; psi.z += p4.z; psi.w += p4.w;
             }
-            // ---- rotate C and B in place once they have landed
+            // ---- rotate C and B in place once they have landed.  C and B of chunk i+2
+            //      are issued only after batch 1 of chunk i, so waiting for them here keeps
+            //      this group at most one chunk ahead of the consumer: every barrier the
+            //      consumer waits on is then at most one phase ahead.
             (void)wait_bounded(&ctl->fcb[s], (i >> 1) & 1, fail_r, fail_c);
             if (rt == 0) ctl->cb_waited[s] += 1;
+            // the consumer may use this chunk's coefficients (exp(cum_end), f) now
+            mbar_arrive(&ctl->coef_ready[s]);
             {
                 uint8_t* tC = tile_c(s);
                 uint8_t* tB = tile_b(s);
@@ -779,29 +815,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             //      chunk's last reader of that buffer is done (batch 2, or batch 1 in the
             //      state pass) and X has landed
             if (i > 0) (void)wait_bounded(FULL ? &ctl->b2 : &ctl->b1b, (i - 1) & 1, fail_r, fail_c);
-            (void)wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_r, fail_c);
+            if (wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_r, fail_c)) make_xhat(s);
             if (rt == 0) ctl->x_waited[s] += 1;
-            {
-                const uint8_t* tX = tile_x(s);
-                // QR rows x 8 16-byte pieces; 128 threads
-                for (int pidx = rt; pidx < QR * 8; pidx += 128) {
-                    const int row = pidx >> 3, piece = pidx & 7;
-                    const float f = sF[row / R];
-                    const uint32_t off2 = sw128_offset(row, piece * 16);
-                    const uint4 v = *reinterpret_cast<const uint4*>(tX + off2);
-                    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                    const float2 f2 = make_float2(f, f);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 g = __fmul2_rn(f2, make_float2(bf_lo(w[e]), bf_hi(w[e])));
-                        w[e] = pack_bf16(g.x, g.y);
-                    }
-                    *reinterpret_cast<uint4*>(xs + off2) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
+
             fence_proxy_async_smem();
             mbar_arrive(&ctl->rot_done[s]);
-            group_bar(2);   // sW / sF are reused by the next chunk
+            group_bar(2);   // sW is reused by the next chunk
             if (*fail_r) break;
         }
     }
@@ -813,13 +832,17 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         atomicExch(args.status, (int)M3_ERR_TIMEOUT);
         // let copies and MMAs still in flight finish (bounded) before the shared
         // memory and TMEM go away
+        auto drain = [&](uint64_t* bar, uint16_t waited, uint16_t issued) {
+            const uint16_t n = (uint16_t)(issued - waited);
+            for (uint16_t j = 0; j < n && j < 4; ++j) (void)mbar_wait(bar, (uint32_t)((waited + j) & 1), kWaitLimitNs);
+        };
         for (int s = 0; s < 2; ++s) {
-            for (int k = ctl->box_waited[s]; k < ctl->box_issued[s]; ++k) (void)mbar_wait(&ctl->fbox[s], k & 1, kWaitLimitNs);
-            for (int k = ctl->cb_waited[s]; k < ctl->cb_issued[s]; ++k) (void)mbar_wait(&ctl->fcb[s], k & 1, kWaitLimitNs);
-            for (int k = ctl->x_waited[s]; k < ctl->x_issued[s]; ++k) (void)mbar_wait(&ctl->fx[s], k & 1, kWaitLimitNs);
+            drain(&ctl->fbox[s], ctl->box_waited[s], ctl->box_issued[s]);
+            drain(&ctl->fcb[s], ctl->cb_waited[s], ctl->cb_issued[s]);
+            drain(&ctl->fx[s], ctl->x_waited[s], ctl->x_issued[s]);
         }
-        for (int k = ctl->b1_waited; k < ctl->b1_issued; ++k) (void)mbar_wait(&ctl->b1b, k & 1, kWaitLimitNs);
-        for (int k = ctl->b2_waited; k < ctl->b2_issued; ++k) (void)mbar_wait(&ctl->b2, k & 1, kWaitLimitNs);
+        drain(&ctl->b1b, ctl->b1_waited, ctl->b1_issued);
+        drain(&ctl->b2, ctl->b2_waited, ctl->b2_issued);
     }
     __syncthreads();
     tc_fence_after();
