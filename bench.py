@@ -93,6 +93,30 @@ def decode_bytes(b: int, H: int, P: int, N: int, R: int, io: str = "bf16") -> in
     return b * H * per + H * 4
 
 
+def profiled_traffic(kernel_source: str, profile: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) that an ncu
+    capture recorded in ``profile`` (a summary under profiles/), or None when the kernel
+    source has changed since: the summary names the source file's sha256 at capture time."""
+    import hashlib
+    try:
+        src = open(os.path.join(ROOT, kernel_source), "rb").read()
+        text = open(os.path.join(ROOT, "profiles", profile)).read()
+    except OSError:
+        return None
+    digest = hashlib.sha256(src).hexdigest()
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.lstrip("-* ").split(":", 1)[0].strip() in ("source sha256", "traffic per launch bytes"):
+            k, v = line.lstrip("-* ").split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source sha256") != digest:
+        return None
+    try:
+        return int(fields["traffic per launch bytes"])
+    except (KeyError, ValueError):
+        return None
+
+
 # ---------------------------------------------------------------------------
 class ClockSampler:
     """Samples SM clocks and clock-event (throttle) reasons with nvidia-smi while
@@ -216,37 +240,79 @@ def time_prefill(binding, w, d, stream, steps, warmup, dist, device):
     return max_over_ranks(dist, total_ms, device) / 1e3, per, (y, fin)
 
 
-def time_prefill_e2e(binding, w, host, stream, steps, warmup, dist, device):
-    """Host pinned buffers in, y and final state back to host, all inside the timed region."""
-    dev = {k: torch.empty_like(host[k], device=device) for k in KEYS}
-    y = torch.empty_like(dev["x"])
-    fin = torch.empty((w.batch, w.heads, w.dstate, w.headdim), dtype=torch.float32, device=device)
-    y_h = torch.empty_like(y, device="cpu").pin_memory()
-    fin_h = torch.empty_like(fin, device="cpu").pin_memory()
-    ws = binding.alloc_workspace(dev["x"].shape, w.dstate, w.rank, w.chunk, dev["x"].dtype, device)
+def time_prefill_e2e(binding, w, host, stream, steps, warmup, dist, device, copy_streams=4):
+    """End to end through the C ABI: every step copies its inputs from pinned host
+    buffers to the device, runs m3_scan_fwd and copies y and the final state back to
+    pinned host buffers, all inside the timed region.  Steps are pipelined over two
+    device input/output buffer sets: the inputs of step k+1 are copied (split over
+    ``copy_streams`` streams so that several copy engines share them) while step k
+    computes and its results are copied out.  The region ends when the last step's
+    results are on the host."""
+    sets = []
+    for _ in range(2):
+        dev = {k: torch.empty_like(host[k], device=device) for k in KEYS}
+        y = torch.empty_like(dev["x"])
+        fin = torch.empty((w.batch, w.heads, w.dstate, w.headdim), dtype=torch.float32, device=device)
+        sets.append((dev, y, fin))
+    y_h = [torch.empty_like(sets[0][1], device="cpu").pin_memory() for _ in range(2)]
+    fin_h = [torch.empty_like(sets[0][2], device="cpu").pin_memory() for _ in range(2)]
+    ws = binding.alloc_workspace(sets[0][0]["x"].shape, w.dstate, w.rank, w.chunk, sets[0][0]["x"].dtype, device)
     h2d = sum(host[k].numel() * host[k].element_size() for k in KEYS)
-    d2h = y.numel() * y.element_size() + fin.numel() * fin.element_size()
+    d2h = sets[0][1].numel() * sets[0][1].element_size() + sets[0][2].numel() * sets[0][2].element_size()
+    cps = [torch.cuda.Stream(device=device) for _ in range(copy_streams)]
+    outs = torch.cuda.Stream(device=device)
+    # the big tensors first, spread over the copy streams (largest remaining to the least loaded)
+    order = sorted(KEYS, key=lambda k: -host[k].numel() * host[k].element_size())
 
-    def step():
-        for k in KEYS:
-            dev[k].copy_(host[k], non_blocking=True)
+    computed = [None, None]   # per set: its last compute (its inputs are free after it)
+    copied_out = [None, None]  # per set: its last results copied to the host
+
+    def step(j):
+        dev, y, fin = sets[j & 1]
+        load = [0] * len(cps)
+        done = []
+        for k in order:
+            i = load.index(min(load))
+            cs = cps[i]
+            if computed[j & 1] is not None:
+                cs.wait_event(computed[j & 1])   # step j-2 has read this set's inputs
+            with torch.cuda.stream(cs):
+                dev[k].copy_(host[k], non_blocking=True)
+            load[i] += host[k].numel() * host[k].element_size()
+            ev = torch.cuda.Event()
+            ev.record(cs)
+            done.append(ev)
+        for ev in done:
+            stream.wait_event(ev)
+        if copied_out[j & 1] is not None:
+            stream.wait_event(copied_out[j & 1])  # step j-2's results have left this set
         st = binding.m3_scan_fwd(*[dev[k] for k in KEYS], w.rank, w.chunk, y, fin, ws, stream)
         if st != 0:
             raise binding.M3Error(st, "m3_scan_fwd")
-        y_h.copy_(y, non_blocking=True)
-        fin_h.copy_(fin, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        computed[j & 1] = ev
+        outs.wait_event(ev)
+        with torch.cuda.stream(outs):
+            y_h[j & 1].copy_(y, non_blocking=True)
+            fin_h[j & 1].copy_(fin, non_blocking=True)
+        ev2 = torch.cuda.Event()
+        ev2.record(outs)
+        copied_out[j & 1] = ev2
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            step()
-        torch.cuda.synchronize()
-        barrier(dist)
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(steps):
-            step()
-        t1.record(stream)
+    for j in range(warmup):
+        step(j)
+    torch.cuda.synchronize()
+    barrier(dist)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s_ in cps + [outs]:
+        s_.wait_stream(stream)               # nothing of the region starts before t0
+    for j in range(steps):
+        step(j)
+    stream.wait_stream(outs)
+    t1.record(stream)
     torch.cuda.synchronize()
     barrier(dist)
     sec = max_over_ranks(dist, t0.elapsed_time(t1), device) / 1e3
@@ -471,7 +537,9 @@ def main():
                    "l2": f"inputs larger than L2 ({nbytes / 1e9:.2f} GB per step), no flush"},
         "gpu_launches": launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved_gbs / pk["hbm_gbs"], "traffic": None,
+                     "frac": achieved_gbs / pk["hbm_gbs"],
+                     "traffic": (profiled_traffic("state_space_sequence_04_b300/csrc/scan_tc.cu",
+                                                  f"scan_tc_kernel_{w.name}.md") if path == 1 else None),
                      "kernel": "m3_scan_fwd (" + ("tensor-core" if path == 1 else "CUDA-core") +
                                f" path, {launches} launches per call)",
                      "algorithmic_bytes_per_call": nbytes, "peak_source": pk["source"],

@@ -148,9 +148,8 @@ struct Ctl {
     uint64_t rot_done[2];    // rotate group finished the stage (count 128)
     uint64_t coef_ready[2];  // coefficient block of the stage written (count 128)
     uint64_t coef_free[2];   // consumer done reading the stage's coefficient block (count 128)
-    uint64_t b1a;            // MMA batch 1, scores S, complete
-    uint64_t b1b;            // MMA batch 1 complete (chunk state onto H, inter readout Yi)
-    uint64_t b2;             // MMA batch 2 complete
+    uint64_t b1;             // MMA batch 1 (chunk state onto H, scores S) complete
+    uint64_t b2;             // MMA batch 2 (inter readout Yi, output Y) complete
     uint32_t tmem;
     int fail_c, fail_r;      // per-group failure flags
     // copies / MMA batches issued and waited for, modulo 2^16 (only their difference,
@@ -301,8 +300,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             ctl->cb_issued[s] = ctl->cb_waited[s] = 0;
             ctl->x_issued[s] = ctl->x_waited[s] = 0;
         }
-        mbar_init(&ctl->b1a, 1);
-        mbar_init(&ctl->b1b, 1);
+        mbar_init(&ctl->b1, 1);
         mbar_init(&ctl->b2, 1);
         ctl->fail_c = 0;
         ctl->fail_r = 0;
@@ -410,7 +408,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         group_bar(1);
         const bool odd = tid & 1;
         float ld_sum = 0.f, th_sum = 0.f;   // state pass: summed log-decay (thread 0), angle of pair tid
-        // S = C~ B'^T of the chunk in stage s, committed on b1a (thread 0)
+        // S = C~ B'^T of the chunk in stage s (thread 0)
         auto issue_scores = [&](int s) {
             const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
             const uint64_t dB = smem_desc(smem_u32(tile_b(s)), 16, 1024, kSwizzle128B);
@@ -420,13 +418,13 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
                 mma_bf16_ss(tmem + K::T_S, dC + ko, dB + ko, id_s, kk > 0);
             }
-            mma_commit(&ctl->b1a);
         };
 
         for (int i = 0; i < nl; ++i) {
             const int c = c_begin + i, s = i & 1;
             const float* co = coef(s);
-            // ---- batch 1 once the rotate group has finished this stage
+            // ---- batch 1 once the rotate group has finished this stage:
+            //      H += B'^T X^ (the chunk state onto the carry), then S = C~ B'^T
             (void)wait_bounded(&ctl->rot_done[s], (i >> 1) & 1, fail_c, fail_r);
             tc_fence_before();
             group_bar(1);
@@ -434,35 +432,24 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             if (tid == 0) {
                 tc_fence_after();
                 // descriptors of the operand bases; a byte offset o moves the start address field by o >> 4
-                const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
                 const uint64_t dBt = smem_desc(smem_u32(tile_b(s)), QR * 128, 1024, kSwizzle128B);
                 const uint64_t dX = smem_desc(smem_u32(xs), 16, 1024, kSwizzle128B);
-                const uint64_t dHb = smem_desc(smem_u32(hb), 16, 1024, kSwizzle128B);
-                constexpr uint32_t id_y = idesc_bf16_f32(K::MM, P, false, true);
                 constexpr uint32_t id_u = idesc_bf16_f32(128, P, true, true);
-                if (FULL) issue_scores(s);
-                // H += B'^T X^ : A is MN-major over n (NS rows; panels QR*128 bytes apart)
-                // (NS = 64: the second panel reads the next QR*128 bytes, results unused)
+                // A is MN-major over n (NS rows; panels QR*128 bytes apart); with NS = 64 the
+                // second panel reads the next QR*128 bytes and its results are unused
 #pragma unroll
                 for (int kk = 0; kk < QR / 16; ++kk)
                     mma_bf16_ss(tmem + K::T_H, dBt + kk * (2048 >> 4), dX + kk * (2048 >> 4), id_u, 1);
-                if (FULL) {
-#pragma unroll
-                    for (int kk = 0; kk < NS / 16; ++kk) {   // Yi = C~ Hb_{c-1}
-                        const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
-                        mma_bf16_ss(tmem + K::T_YI, dC + ko, dHb + kk * (2048 >> 4), id_y, kk > 0);
-                    }
-                }
-                mma_commit(&ctl->b1b);
+                if (FULL) issue_scores(s);
+                mma_commit(&ctl->b1);
                 ctl->b1_issued += 1;
             }
+            (void)wait_bounded(&ctl->b1, i & 1, fail_c, fail_r);
+            tc_fence_after();
 
             float ecum_t = 0.f;
             if constexpr (FULL) {
-                (void)wait_bounded(&ctl->b1a, i & 1, fail_c, fail_r);
-                tc_fence_after();
-                // ---- mask: SL = S o L (bf16, K-major rows (t,r)) into the X^ / SL buffer,
-                //      once batch 1 (the last reader of X^, C~ and B') is done
+                // ---- mask: SL = S o L (bf16, K-major rows (t,r)) over X^ (consumed by batch 1)
                 if constexpr (K::M64) {
                     // thread = (row, half): row 16 warp + lane % 16, columns [32 half, 32 half + 32)
                     const int row = warp * 16 + (lane & 15), half = lane >> 4, t = row / R;
@@ -473,7 +460,6 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     tmem_ld16x2_sync(tlane + K::T_S, v);
                     mask_block<R>(v, 32 * half, t, ct, rt, cum2, co + K::CO_BNEG);
                     mask_block<R>(v + 16, 32 * half + 16, t, ct, rt, cum2, co + K::CO_BNEG);
-                    (void)wait_bounded(&ctl->b1b, i & 1, fail_c, fail_r);
 #pragma unroll
                     for (int q8 = 0; q8 < 4; ++q8) {
                         const int col = 32 * half + q8 * 8;
@@ -482,46 +468,47 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                                        pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
                     }
                     fence_proxy_async_smem();
-                } else {
-                    (void)wait_bounded(&ctl->b1b, i & 1, fail_c, fail_r);
-                    if (warp * 32 < QR) {
-                        const int row = tid, t = row / R;
-                        const float* cum2 = co + K::CO_CUM2;
-                        const float ct = cum2[t], rt = co[K::CO_RHO + t];
-                        ecum_t = co[K::CO_ECUM + t];
-                        const int tmax = (warp * 32 + 31) / R;   // last token of this warp's rows
+                } else if (warp * 32 < QR) {
+                    const int row = tid, t = row / R;
+                    const float* cum2 = co + K::CO_CUM2;
+                    const float ct = cum2[t], rt = co[K::CO_RHO + t];
+                    ecum_t = co[K::CO_ECUM + t];
+                    const int tmax = (warp * 32 + 31) / R;   // last token of this warp's rows
 #pragma unroll
-                        for (int c32 = 0; c32 < QR; c32 += 32) {
-                            float v[32];
-                            if (c32 / R <= tmax) {   // warp-uniform
-                                tmem_ld32_sync(tlane + K::T_S + c32, v);
-                            } else {
+                    for (int c32 = 0; c32 < QR; c32 += 32) {
+                        float v[32];
+                        if (c32 / R <= tmax) {   // warp-uniform
+                            tmem_ld32_sync(tlane + K::T_S + c32, v);
+                        } else {
 #pragma unroll
-                                for (int i4 = 0; i4 < 32; ++i4) v[i4] = 0.f;
-                            }
-                            mask_block<R>(v, c32, t, ct, rt, cum2, co + K::CO_BNEG);
-                            mask_block<R>(v + 16, c32 + 16, t, ct, rt, cum2, co + K::CO_BNEG);
-#pragma unroll
-                            for (int q8 = 0; q8 < 4; ++q8) {
-                                const int col = c32 + q8 * 8;
-                                *reinterpret_cast<uint4*>(xs + (col / 64) * QR * 128 + sw128_offset(row, (col % 64) * 2)) =
-                                    make_uint4(pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]), pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]),
-                                               pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
-                            }
+                            for (int i4 = 0; i4 < 32; ++i4) v[i4] = 0.f;
                         }
-                        fence_proxy_async_smem();
+                        mask_block<R>(v, c32, t, ct, rt, cum2, co + K::CO_BNEG);
+                        mask_block<R>(v + 16, c32 + 16, t, ct, rt, cum2, co + K::CO_BNEG);
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            const int col = c32 + q8 * 8;
+                            *reinterpret_cast<uint4*>(xs + (col / 64) * QR * 128 + sw128_offset(row, (col % 64) * 2)) =
+                                make_uint4(pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]), pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]),
+                                           pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
+                        }
                     }
+                    fence_proxy_async_smem();
                 }
                 tc_fence_before();
                 group_bar(1);
-                if (tid == 0) {
+                if (tid == 0) {   // batch 2: Yi = C~ Hb_{c-1}, Y = SL X
                     tc_fence_after();
-                    // C~ and B' are dead: load C, B of local chunk i+2 into this stage
-                    if (i + 2 < nl && !*fail_c) load_cb(i + 2, s);
-                    // batch 2: Y = SL X
+                    const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
+                    const uint64_t dHb = smem_desc(smem_u32(hb), 16, 1024, kSwizzle128B);
                     const uint64_t dSL = smem_desc(smem_u32(xs), 16, 1024, kSwizzle128B);
                     const uint64_t dX = smem_desc(smem_u32(tile_x(s)), 16, 1024, kSwizzle128B);
                     constexpr uint32_t id_y = idesc_bf16_f32(K::MM, P, false, true);
+#pragma unroll
+                    for (int kk = 0; kk < NS / 16; ++kk) {
+                        const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
+                        mma_bf16_ss(tmem + K::T_YI, dC + ko, dHb + kk * (2048 >> 4), id_y, kk > 0);
+                    }
 #pragma unroll
                     for (int kk = 0; kk < QR / 16; ++kk) {
                         const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
@@ -530,9 +517,58 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     mma_commit(&ctl->b2);
                     ctl->b2_issued += 1;
                 }
-            } else {
-                (void)wait_bounded(&ctl->b1b, i & 1, fail_c, fail_r);
+                // ---- output rows (t, r) once batch 2 is done; C, B, X of chunk i+2 may then come in
+                (void)wait_bounded(&ctl->b2, i & 1, fail_c, fail_r);
                 tc_fence_after();
+                if (tid == 0 && i + 2 < nl && !*fail_c) {
+                    load_cb(i + 2, s);
+                    load_x(i + 2, s);
+                }
+                if constexpr (K::M64) {
+                    const int row = warp * 16 + (lane & 15), half = lane >> 4, t = row / R, r = row % R;
+                    const int tok = c * Q + t;
+                    __nv_bfloat16* yrow = args.y + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P + 32 * half;
+                    const float2 e2 = make_float2(ecum_t, ecum_t);
+                    float yv[32], iv[32];
+                    tmem_ld16x2x2_sync(tlane + K::T_Y, tlane + K::T_YI, yv, iv);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float2 o = __ffma2_rn(e2, make_float2(iv[2 * q], iv[2 * q + 1]),
+                                                    make_float2(yv[2 * q], yv[2 * q + 1]));
+                        pk[q] = pack_bf16(o.x, o.y);
+                    }
+                    if (tok < T) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            *reinterpret_cast<uint4*>(yrow + 8 * q4) =
+                                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                    }
+                } else if (warp * 32 < QR) {
+                    const int row = tid, t = row / R, r = row % R;
+                    const int tok = c * Q + t;
+                    __nv_bfloat16* yrow = args.y + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P;
+                    const float2 e2 = make_float2(ecum_t, ecum_t);
+#pragma unroll
+                    for (int cc = 0; cc < P; cc += 32) {
+                        float yv[32], iv[32];
+                        tmem_ld32x2_sync(tlane + K::T_Y + cc, tlane + K::T_YI + cc, yv, iv);
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const float2 o = __ffma2_rn(e2, make_float2(iv[2 * q], iv[2 * q + 1]),
+                                                        make_float2(yv[2 * q], yv[2 * q + 1]));
+                            pk[q] = pack_bf16(o.x, o.y);
+                        }
+                        if (tok < T) {
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                *reinterpret_cast<uint4*>(yrow + cc + 8 * q4) =
+                                    make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                        }
+                    }
+                }
+            } else {
                 // B' and X^ are consumed (X was consumed into X^): the next loads may come in
                 if (tid == 0 && i + 2 < nl && !*fail_c) {
                     load_cb(i + 2, s);
@@ -543,6 +579,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             }
 
             // ---- state: H <- e_{c+1} R(Theta_c) H ; Hb <- bf16(R(Theta_c) H)   (thread = state row n)
+            //      (batch 2 has read Hb_{c-1})
             float e_next = 1.f;
             if (i + 1 < nl) {
                 const int s1 = (i + 1) & 1;
@@ -589,60 +626,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 tmem_st_wait();
                 if (FULL) fence_proxy_async_smem();
             }
-            // every read of this stage's coefficient block is done (the output keeps exp(cum_t)
+            // every read of this stage's coefficient block is done (the output took exp(cum_t)
             // in a register): the rotate group may fill it for chunk i+2
             mbar_arrive(&ctl->coef_free[s]);
-
-            if constexpr (FULL) {
-                // ---- output rows (t, r) once batch 2 is done; X of chunk i+2 may then come in
-                (void)wait_bounded(&ctl->b2, i & 1, fail_c, fail_r);
-                tc_fence_after();
-                if (tid == 0 && i + 2 < nl && !*fail_c) load_x(i + 2, s);
-                if constexpr (K::M64) {
-                    const int row = warp * 16 + (lane & 15), half = lane >> 4, t = row / R, r = row % R;
-                    const int tok = c * Q + t;
-                    __nv_bfloat16* yrow = args.y + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P + 32 * half;
-                    const float2 e2 = make_float2(ecum_t, ecum_t);
-                    float yv[32], iv[32];
-                    tmem_ld16x2x2_sync(tlane + K::T_Y, tlane + K::T_YI, yv, iv);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const float2 o = __ffma2_rn(e2, make_float2(iv[2 * q], iv[2 * q + 1]),
-                                                    make_float2(yv[2 * q], yv[2 * q + 1]));
-                        pk[q] = pack_bf16(o.x, o.y);
-                    }
-                    if (tok < T) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            *reinterpret_cast<uint4*>(yrow + 8 * q4) =
-                                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-                    }
-                } else if (warp * 32 < QR) {
-                    const int row = tid, t = row / R, r = row % R;
-                    const int tok = c * Q + t;
-                    __nv_bfloat16* yrow = args.y + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P;
-                    const float2 e2 = make_float2(ecum_t, ecum_t);
-#pragma unroll
-                    for (int cc = 0; cc < P; cc += 32) {
-                        float yv[32], iv[32];
-                        tmem_ld32x2_sync(tlane + K::T_Y + cc, tlane + K::T_YI + cc, yv, iv);
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            const float2 o = __ffma2_rn(e2, make_float2(iv[2 * q], iv[2 * q + 1]),
-                                                        make_float2(yv[2 * q], yv[2 * q + 1]));
-                            pk[q] = pack_bf16(o.x, o.y);
-                        }
-                        if (tok < T) {
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4)
-                                *reinterpret_cast<uint4*>(yrow + cc + 8 * q4) =
-                                    make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-                        }
-                    }
-                }
-            }
             tc_fence_before();
             group_bar(1);
             if (tid == 0) {
@@ -814,7 +800,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             // ---- X^ = exp(cum_end - cum_s) X into the X^ / SL buffer, once the previous
             //      chunk's last reader of that buffer is done (batch 2, or batch 1 in the
             //      state pass) and X has landed
-            if (i > 0) (void)wait_bounded(FULL ? &ctl->b2 : &ctl->b1b, (i - 1) & 1, fail_r, fail_c);
+            if (i > 0) (void)wait_bounded(FULL ? &ctl->b2 : &ctl->b1, (i - 1) & 1, fail_r, fail_c);
             if (wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_r, fail_c)) make_xhat(s);
             if (rt == 0) ctl->x_waited[s] += 1;
 
@@ -841,7 +827,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             drain(&ctl->fcb[s], ctl->cb_waited[s], ctl->cb_issued[s]);
             drain(&ctl->fx[s], ctl->x_waited[s], ctl->x_issued[s]);
         }
-        drain(&ctl->b1b, ctl->b1_waited, ctl->b1_issued);
+        drain(&ctl->b1, ctl->b1_waited, ctl->b1_issued);
         drain(&ctl->b2, ctl->b2_waited, ctl->b2_issued);
     }
     __syncthreads();
