@@ -16,8 +16,13 @@ Two parts:
   chunked evaluation with state passing), and the state-passing recurrence.
 
 Layouts are those of ``synth.py``: x [Bt,T,H,R,P], B/C [Bt,T,H,R,N],
-dt/lam [Bt,T,H], A [H], omega [Bt,T,H,N/2], y [Bt,T,H,R,P], states [Bt,H,N,P],
-delayed-write cache [Bt,H,R*N+R*P].
+dt/lam [Bt,T,H], A [H] (or [Bt,T,H]: one A_t per token), omega [Bt,T,H,N/2],
+y [Bt,T,H,R,P], states [Bt,H,N,P], delayed-write cache [Bt,H,R*N+R*P].
+
+``prep`` / ``scan_prep`` / ``decode_step_prep`` take the pre-activations of
+the per-token parameters instead: Delta_t = softplus(dt_raw_t + dt_bias_h),
+lambda_t = sigmoid(u_t) (the default lambda parameterisation of the appendix
+ablation table), A_t given per token.
 """
 from __future__ import annotations
 
@@ -52,6 +57,8 @@ def _load():
         i64 = ctypes.c_int64
         lib.m3o_scan.argtypes = [dp] * 7 + [i64] * 6 + [dp] * 5
         lib.m3o_scan.restype = ctypes.c_int
+        lib.m3o_scan_tok.argtypes = [dp] * 7 + [i64] * 6 + [dp] * 5
+        lib.m3o_scan_tok.restype = ctypes.c_int
         lib.m3o_num_threads.argtypes = []
         lib.m3o_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -81,14 +88,15 @@ def scan(x, B, C, dt, A, lam, omega, h0=None, prev=None):
 
     Returns (y [Bt,T,H,R,P], hT [Bt,H,N,P], prevT [Bt,H,R*(N+P)]).
     ``h0`` / ``prev`` are the carried state and delayed-write factors (zero if None).
+    ``A`` is [H] (one decay generator per head) or [Bt,T,H] (one per token).
     """
     x, B, C, dt, A, lam, omega = (f64(v) for v in (x, B, C, dt, A, lam, omega))
     Bt, T, H, R, P = x.shape
     N = B.shape[-1]
     if B.shape != (Bt, T, H, R, N) or C.shape != B.shape:
         raise ValueError("B, C must be [Bt,T,H,R,N]")
-    if dt.shape != (Bt, T, H) or lam.shape != (Bt, T, H) or A.shape != (H,):
-        raise ValueError("dt, lam must be [Bt,T,H]; A must be [H]")
+    if dt.shape != (Bt, T, H) or lam.shape != (Bt, T, H) or A.shape not in ((H,), (Bt, T, H)):
+        raise ValueError("dt, lam must be [Bt,T,H]; A must be [H] or [Bt,T,H]")
     if omega.shape != (Bt, T, H, N // 2):
         raise ValueError("omega must be [Bt,T,H,N/2]")
     h0 = None if h0 is None else f64(h0).reshape(Bt, H, N, P)
@@ -96,8 +104,9 @@ def scan(x, B, C, dt, A, lam, omega, h0=None, prev=None):
     y = np.zeros((Bt, T, H, R, P))
     hT = np.zeros((Bt, H, N, P))
     prevT = np.zeros((Bt, H, R * (N + P)))
-    st = _load().m3o_scan(_ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A), _ptr(lam), _ptr(omega),
-                          Bt, T, H, P, N, R, _ptr(h0), _ptr(prev), _ptr(y), _ptr(hT), _ptr(prevT))
+    fn = _load().m3o_scan if A.shape == (H,) else _load().m3o_scan_tok
+    st = fn(_ptr(x), _ptr(B), _ptr(C), _ptr(dt), _ptr(A), _ptr(lam), _ptr(omega),
+            Bt, T, H, P, N, R, _ptr(h0), _ptr(prev), _ptr(y), _ptr(hT), _ptr(prevT))
     if st != 0:
         raise ValueError(f"oracle rejected its inputs (code {st}): shapes, or a precondition "
                          "Delta >= 0, A <= 0, lambda in [0, 1], finite values")
@@ -114,6 +123,42 @@ def decode_step(state, x_t, B_t, prev, C_t, dt_t, A, lam_t, omega_t):
     xt = f64(x_t)[:, None]
     y, hT, prevT = scan(xt, f64(B_t)[:, None], f64(C_t)[:, None], f64(dt_t)[:, None], A,
                         f64(lam_t)[:, None], f64(omega_t)[:, None], h0=state, prev=prev)
+    return y[:, 0], hT, prevT
+
+
+def softplus(z):
+    """log(1 + e^z) in float64 (numpy's logaddexp(0, z))."""
+    return np.logaddexp(0.0, f64(z))
+
+
+def sigmoid(u):
+    """1 / (1 + e^-u) in float64, evaluated without overflow for either sign of u."""
+    u = f64(u)
+    e = np.exp(-np.abs(u))
+    return np.where(u >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def prep(dt_raw, dt_bias, u):
+    """Per-token parameters from their pre-activations (float64):
+    Delta = softplus(dt_raw + dt_bias[h]) (dt_bias None = 0), lambda = sigmoid(u)."""
+    z = f64(dt_raw)
+    if dt_bias is not None:
+        z = z + f64(dt_bias)
+    return softplus(z), sigmoid(u)
+
+
+def scan_prep(x, B, C, dt_raw, dt_bias, A_tok, u, omega, h0=None, prev=None):
+    """``scan`` on pre-activations: Delta, lambda from ``prep``, A_tok [Bt,T,H] per token."""
+    d, lam = prep(dt_raw, dt_bias, u)
+    return scan(x, B, C, d, A_tok, lam, omega, h0=h0, prev=prev)
+
+
+def decode_step_prep(state, x_t, B_t, prev, C_t, dt_raw_t, dt_bias, A_t, u_t, omega_t):
+    """One decode token on pre-activations: dt_raw_t, A_t, u_t [b,H]; dt_bias [H] or None."""
+    d, lam = prep(dt_raw_t, dt_bias, u_t)
+    xt = f64(x_t)[:, None]
+    y, hT, prevT = scan(xt, f64(B_t)[:, None], f64(C_t)[:, None], d[:, None], f64(A_t)[:, None],
+                        lam[:, None], f64(omega_t)[:, None], h0=state, prev=prev)
     return y[:, 0], hT, prevT
 
 

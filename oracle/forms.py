@@ -44,6 +44,13 @@ def _unpack(x, B, C, dt, A, lam, omega):
     return tuple(_f64(v) for v in (x, B, C, dt, A, lam, omega))
 
 
+def a_per_token(A, dt):
+    """The decay generator of every (batch, token, head): A [H] repeats over tokens;
+    A [Bt,T,H] (the per-token A_t of Table 1) is taken as given."""
+    A, dt = _f64(A), _f64(dt)
+    return np.broadcast_to(A, dt.shape) if A.ndim == 1 else A
+
+
 def rotate_pairs(v: np.ndarray, theta: np.ndarray) -> np.ndarray:
     """Rotate consecutive pairs (2j, 2j+1) of the last axis of ``v`` by ``theta[..., j]``."""
     a = v[..., 0::2]
@@ -58,7 +65,7 @@ def rotate_pairs(v: np.ndarray, theta: np.ndarray) -> np.ndarray:
 def coefficients(dt, A, lam):
     """alpha, beta, gamma of the exponential-trapezoidal rule (Proposition 1, Eq. 6).
 
-    dt, lam [..., T, H]; A [H] broadcast over the last axis.
+    dt, lam [..., T, H]; A [H] broadcast over the last axis, or A of dt's shape.
     """
     alpha = np.exp(dt * A)
     beta = (1.0 - lam) * dt * alpha
@@ -77,10 +84,11 @@ def mamba2_euler(x, B, C, dt, A):
     Bt, T, H, R, P = x.shape
     assert R == 1
     N = B.shape[-1]
+    At = a_per_token(A, dt)
     y = np.zeros_like(x)
     h = np.zeros((Bt, H, N, P))
     for t in range(T):
-        decay = np.exp(dt[:, t] * A)                     # [Bt,H]
+        decay = np.exp(dt[:, t] * At[:, t])              # [Bt,H]
         write = B[:, t, :, 0, :, None] * x[:, t, :, 0, None, :]   # [Bt,H,N,P]
         h = decay[..., None, None] * h + dt[:, t][..., None, None] * write
         y[:, t, :, 0, :] = np.einsum("bhnp,bhn->bhp", h, C[:, t, :, 0, :])
@@ -91,7 +99,7 @@ def mamba2_euler(x, B, C, dt, A):
 def decay_matrix(dt, A):
     """D[t, s] = prod_{k=s+1..t} alpha_k for s <= t (1 on the diagonal), 0 above.
 
-    dt [T] for one head; A scalar.  Built as an explicit product, not from
+    dt [T] for one head; A scalar or [T] (per token).  Built as an explicit product, not from
     differences of cumulative sums, so it is exact for small T.
     """
     T = dt.shape[0]
@@ -142,6 +150,7 @@ def matrix_form(x, B, C, dt, A, lam, omega):
     """
     x, B, C, dt, A, lam, omega = _unpack(x, B, C, dt, A, lam, omega)
     Bt, T, H, R, P = x.shape
+    At = a_per_token(A, dt)
     y = np.zeros_like(x)
     for b in range(Bt):
         for h in range(H):
@@ -149,7 +158,7 @@ def matrix_form(x, B, C, dt, A, lam, omega):
             Phi = np.cumsum(phi, axis=0)
             Bm = rotate_pairs(B[b, :, h], -Phi[:, None, :])     # [T, R, N]
             Cm = rotate_pairs(C[b, :, h], -Phi[:, None, :])
-            L = two_band_matrix(dt[b, :, h], A[h], lam[b, :, h])  # [T, T]
+            L = two_band_matrix(dt[b, :, h], At[b, :, h], lam[b, :, h])  # [T, T]
             S = np.einsum("trn,sqn->trsq", Cm, Bm)               # [T,R,T,R]
             M = S * L[:, None, :, None]
             y[b, :, h] = np.einsum("trsq,sqp->trp", M, x[b, :, h])
@@ -239,7 +248,7 @@ def chunked(x, B, C, dt, A, lam, omega, Q: int):
     """Chunked evaluation (zero initial state) with chunk length Q tokens.
 
     Per chunk c = tokens [c0, c1):
-      l_t = Delta_t A ; cum_t = sum_{k=c0..t} l_k ; Psi_t = sum_{k=c0..t} phi_k ; Theta_c = Psi_{c1-1}
+      l_t = Delta_t A_t ; cum_t = sum_{k=c0..t} l_k ; Psi_t = sum_{k=c0..t} phi_k ; Theta_c = Psi_{c1-1}
       gamma_t = lambda_t Delta_t ; w_s = gamma_s + (1 - lambda_{s+1}) Delta_{s+1}
         (for s = c1-1 the next token's lambda, Delta; 0 past the end of the sequence)
       B~_s = R(-Psi_s) B_s ; C~_t = R(-Psi_t) C_t
@@ -254,6 +263,7 @@ def chunked(x, B, C, dt, A, lam, omega, Q: int):
     x, B, C, dt, A, lam, omega = _unpack(x, B, C, dt, A, lam, omega)
     Bt, T, H, R, P = x.shape
     N = B.shape[-1]
+    At = a_per_token(A, dt)
     nc = (T + Q - 1) // Q
     y = np.zeros_like(x)
     finals = np.zeros((Bt, H, N, P))
@@ -267,7 +277,7 @@ def chunked(x, B, C, dt, A, lam, omega, Q: int):
                 c0, c1 = c * Q, min(T, (c + 1) * Q)
                 d = dt[b, c0:c1, h]
                 lm = lam[b, c0:c1, h]
-                ell = d * A[h]
+                ell = d * At[b, c0:c1, h]
                 cum = np.cumsum(ell)
                 Psi = np.cumsum(d[:, None] * omega[b, c0:c1, h, :], axis=0)  # [q, N/2]
                 gam = lm * d

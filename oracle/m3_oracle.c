@@ -24,7 +24,8 @@
  *     v_t = B_t X_t^T (N x P, B_t is N x R and X_t is P x R) and the readout
  *     is Y_t = h_t^T C_t (P x R).
  *
- * Layouts: x [Bt,T,H,R,P], B and C [Bt,T,H,R,N], dt and lam [Bt,T,H], A [H],
+ * Layouts: x [Bt,T,H,R,P], B and C [Bt,T,H,R,N], dt and lam [Bt,T,H], A [H]
+ * (m3o_scan) or [Bt,T,H] (m3o_scan_tok: the per-token A_t of Table 1),
  * omega [Bt,T,H,N/2], y [Bt,T,H,R,P], states [Bt,H,N,P], the delayed-write
  * cache [Bt,H,R*N + R*P] = (B_{t-1} as [R,N], then X_{t-1} as [R,P]).
  *
@@ -62,9 +63,10 @@ int m3o_num_threads(void) {
 }
 
 /* One (batch, head) sequence.  h: [N*P] in/out; bprev [R*N], xprev [R*P]
- * in/out (the factors of v_{t-1}).  Scratch v, vp: [N*P]. */
+ * in/out (the factors of v_{t-1}).  Scratch v, vp: [N*P].  The decay
+ * generator of token t is a_seq[t * a_stride] (a_stride 0: one A per head). */
 static int scan_one(const double* x, const double* B, const double* C, const double* dt,
-                    double a, const double* lam, const double* omega,
+                    const double* a_seq, int64_t a_stride, const double* lam, const double* omega,
                     int64_t T, int64_t H, int64_t P, int64_t N, int64_t R,
                     double* h, double* bprev, double* xprev, double* v, double* vp,
                     double* y) {
@@ -79,6 +81,7 @@ static int scan_one(const double* x, const double* B, const double* C, const dou
         const double* wt = omega + t * tokstride_w;
         const double d = dt[t * tokstride_s];
         const double l = lam[t * tokstride_s];
+        const double a = a_seq[t * a_stride];
         if (!params_ok(d, a, l)) return M3O_BAD_PARAM;
         const double alpha = exp(d * a);
         const double beta = (1.0 - l) * d * alpha;
@@ -129,20 +132,10 @@ static int scan_one(const double* x, const double* B, const double* C, const dou
     return M3O_OK;
 }
 
-/*
- * Sequential scan over T tokens for every (batch, head).
- *   h0    nullable: initial state [Bt,H,N,P] (zero if NULL)
- *   prev  nullable: initial delayed-write factors [Bt,H,R*(N+P)] (zero if NULL)
- *   y     out [Bt,T,H,R,P]
- *   hT    nullable out: state after the last token [Bt,H,N,P]
- *   prevT nullable out: delayed-write factors after the last token
- * A decode step is this function with T = 1 and the carried h0 / prev.
- * Returns 0, or a negative code for bad shapes or violated preconditions.
- */
-int m3o_scan(const double* x, const double* B, const double* C, const double* dt,
-             const double* A, const double* lam, const double* omega,
-             int64_t Bt, int64_t T, int64_t H, int64_t P, int64_t N, int64_t R,
-             const double* h0, const double* prev, double* y, double* hT, double* prevT) {
+static int scan_all(const double* x, const double* B, const double* C, const double* dt,
+                    const double* A, int per_token, const double* lam, const double* omega,
+                    int64_t Bt, int64_t T, int64_t H, int64_t P, int64_t N, int64_t R,
+                    const double* h0, const double* prev, double* y, double* hT, double* prevT) {
     if (Bt < 0 || T < 0 || H < 1 || P < 1 || N < 2 || (N % 2) != 0 || R < 1) return M3O_BAD_SHAPE;
     const int64_t NP = N * P;
     const int64_t KV = R * (N + P);
@@ -169,8 +162,9 @@ int m3o_scan(const double* x, const double* B, const double* C, const double* dt
         const int64_t base_b = (b * T * H + hh) * R * N;
         const int64_t base_s = b * T * H + hh;
         const int64_t base_w = (b * T * H + hh) * (N / 2);
-        int st = scan_one(x + base_x, B + base_b, C + base_b, dt + base_s, A[hh], lam + base_s,
-                          omega + base_w, T, H, P, N, R, h, bprev, xprev, v, vp, y + base_x);
+        const double* a_seq = per_token ? A + base_s : A + hh;
+        int st = scan_one(x + base_x, B + base_b, C + base_b, dt + base_s, a_seq, per_token ? H : 0,
+                          lam + base_s, omega + base_w, T, H, P, N, R, h, bprev, xprev, v, vp, y + base_x);
         if (st != M3O_OK) {
 #pragma omp atomic write
             status = st;
@@ -180,4 +174,30 @@ int m3o_scan(const double* x, const double* B, const double* C, const double* dt
         free(work);
     }
     return status;
+}
+
+/*
+ * Sequential scan over T tokens for every (batch, head), one A per head.
+ *   h0    nullable: initial state [Bt,H,N,P] (zero if NULL)
+ *   prev  nullable: initial delayed-write factors [Bt,H,R*(N+P)] (zero if NULL)
+ *   y     out [Bt,T,H,R,P]
+ *   hT    nullable out: state after the last token [Bt,H,N,P]
+ *   prevT nullable out: delayed-write factors after the last token
+ * A decode step is this function with T = 1 and the carried h0 / prev.
+ * Returns 0, or a negative code for bad shapes or violated preconditions.
+ */
+int m3o_scan(const double* x, const double* B, const double* C, const double* dt,
+             const double* A, const double* lam, const double* omega,
+             int64_t Bt, int64_t T, int64_t H, int64_t P, int64_t N, int64_t R,
+             const double* h0, const double* prev, double* y, double* hT, double* prevT) {
+    return scan_all(x, B, C, dt, A, 0, lam, omega, Bt, T, H, P, N, R, h0, prev, y, hT, prevT);
+}
+
+/* The same with a decay generator per token: A_tok [Bt,T,H] (the A_t of the
+ * time-varying discretizations, Table 1). */
+int m3o_scan_tok(const double* x, const double* B, const double* C, const double* dt,
+                 const double* A_tok, const double* lam, const double* omega,
+                 int64_t Bt, int64_t T, int64_t H, int64_t P, int64_t N, int64_t R,
+                 const double* h0, const double* prev, double* y, double* hT, double* prevT) {
+    return scan_all(x, B, C, dt, A_tok, 1, lam, omega, Bt, T, H, P, N, R, h0, prev, y, hT, prevT);
 }

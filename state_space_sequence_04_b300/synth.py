@@ -116,6 +116,44 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", seqlen: Optional[int] 
     }
 
 
+def make_prep_inputs(w: Workload, seed: int = 0, device="cpu", seqlen: Optional[int] = None,
+                     batch: Optional[int] = None) -> dict:
+    """Prefill inputs in pre-activation form, for the entry points that derive
+    Delta and lambda inside the kernels and take one decay generator per token.
+
+    Draw order: x, B, C, dt_raw, dt_bias, A (per token), u, omega.
+      dt_raw [Bt,T,H] ~ N(dt_mu, dt_sd)      (Delta = softplus(dt_raw + dt_bias))
+      dt_bias [H]     ~ U(-0.5, 0.5)
+      A [Bt,T,H]      = -exp(U(0, ln 16))    (one decay generator per token)
+      u [Bt,T,H]      ~ N(0, 1), or logit(U(0,1)) for lam_uniform workloads (lambda = sigmoid(u))
+    x, B, C, omega as in ``make_inputs``.
+    """
+    Bt = w.batch if batch is None else batch
+    T = w.seqlen if seqlen is None else seqlen
+    H, P, N, R = w.heads, w.headdim, w.dstate, w.rank
+    if N % 2:
+        raise ValueError("N must be even")
+    g = _gen(seed, device)
+    io = io_torch_dtype(w.io)
+    f32 = torch.float32
+    x = torch.randn((Bt, T, H, R, P), generator=g, device=device, dtype=f32)
+    B = torch.randn((Bt, T, H, R, N), generator=g, device=device, dtype=f32) * (1.0 / math.sqrt(N))
+    C = torch.randn((Bt, T, H, R, N), generator=g, device=device, dtype=f32) * (1.0 / math.sqrt(N))
+    dt_raw = torch.randn((Bt, T, H), generator=g, device=device, dtype=f32) * w.dt_sd + w.dt_mu
+    dt_bias = torch.rand((H,), generator=g, device=device, dtype=f32) - 0.5
+    A = -torch.exp(torch.rand((Bt, T, H), generator=g, device=device, dtype=f32) * math.log(16.0))
+    if w.lam_uniform:
+        p = torch.rand((Bt, T, H), generator=g, device=device, dtype=f32).clamp(1e-6, 1 - 1e-6)
+        u = torch.log(p) - torch.log1p(-p)
+    else:
+        u = torch.randn((Bt, T, H), generator=g, device=device, dtype=f32)
+    omega = (torch.rand((Bt, T, H, N // 2), generator=g, device=device, dtype=f32) * 2.0 - 1.0) * math.pi
+    return {
+        "x": x.to(io), "B": B.to(io), "C": C.to(io), "dt_raw": dt_raw, "dt_bias": dt_bias, "A": A, "u": u,
+        "omega": omega, "R": R, "chunk": w.chunk, "io": w.io,
+    }
+
+
 def make_decode_state(batch: int, heads: int, dstate: int, headdim: int, seed: int = 0,
                       device="cpu") -> torch.Tensor:
     """fp32 state [b, H, N, P] ~ N(0, 1)."""
@@ -148,6 +186,31 @@ def make_decode_steps(batch: int, heads: int, headdim: int, dstate: int, rank: i
     omega = (torch.rand((S, b, H, N // 2), generator=g, device=device, dtype=f32) * 2.0 - 1.0) * math.pi
     return {"x": x.to(iot), "B": Bm.to(iot), "C": Cm.to(iot), "dt": dt, "A": A, "lam": lam,
             "omega": omega, "R": R, "io": io}
+
+
+def make_decode_prep_steps(batch: int, heads: int, headdim: int, dstate: int, rank: int, steps: int,
+                           io: str = "bf16", seed: int = 1, device="cpu", dt_mu: float = -3.0,
+                           dt_sd: float = 1.0) -> dict:
+    """Per-step decode inputs in pre-activation form, stacked on dim 0.
+
+    Draw order: x, B, C, dt_raw, dt_bias, A, u, omega.  x [S, b, H, R, P], B/C
+    [S, b, H, R, N] (io dtype); dt_raw ~ N(dt_mu, dt_sd), A = -exp(U(0, ln 16))
+    and u ~ N(0, 1), each [S, b, H]; dt_bias [H] ~ U(-0.5, 0.5); omega [S, b, H, N/2].
+    """
+    g = _gen(seed, device)
+    iot = io_torch_dtype(io)
+    f32 = torch.float32
+    S, b, H, P, N, R = steps, batch, heads, headdim, dstate, rank
+    x = torch.randn((S, b, H, R, P), generator=g, device=device, dtype=f32)
+    Bm = torch.randn((S, b, H, R, N), generator=g, device=device, dtype=f32) * (1.0 / math.sqrt(N))
+    Cm = torch.randn((S, b, H, R, N), generator=g, device=device, dtype=f32) * (1.0 / math.sqrt(N))
+    dt_raw = torch.randn((S, b, H), generator=g, device=device, dtype=f32) * dt_sd + dt_mu
+    dt_bias = torch.rand((H,), generator=g, device=device, dtype=f32) - 0.5
+    A = -torch.exp(torch.rand((S, b, H), generator=g, device=device, dtype=f32) * math.log(16.0))
+    u = torch.randn((S, b, H), generator=g, device=device, dtype=f32)
+    omega = (torch.rand((S, b, H, N // 2), generator=g, device=device, dtype=f32) * 2.0 - 1.0) * math.pi
+    return {"x": x.to(iot), "B": Bm.to(iot), "C": Cm.to(iot), "dt_raw": dt_raw, "dt_bias": dt_bias, "A": A,
+            "u": u, "omega": omega, "R": R, "io": io}
 
 
 def make_state_passing_inputs(batch: int, heads: int, nchunks: int, dstate: int, headdim: int,

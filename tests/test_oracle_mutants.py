@@ -15,6 +15,7 @@ import pytest
 
 import oracle
 import test_oracle_pins as pins
+import test_oracle_prep_pins as prep_pins
 
 SRC = os.path.join(os.path.dirname(os.path.abspath(oracle.__file__)), "m3_oracle.c")
 
@@ -56,6 +57,12 @@ MUTANTS = {
     "decay exponent sign flipped": [
         ("const double alpha = exp(d * a);", "const double alpha = exp(-d * a);"),
     ],
+    "per-token decay generator taken from the first token": [
+        ("const double a = a_seq[t * a_stride];", "const double a = a_seq[0];"),
+    ],
+    "per-token decay generator taken from the previous token": [
+        ("const double a = a_seq[t * a_stride];", "const double a = a_seq[(t > 0 ? t - 1 : 0) * a_stride];"),
+    ],
 }
 
 # Pins that run in well under a second each (name, callable).
@@ -73,6 +80,9 @@ PIN_SUITE = [
     ("single-token MIMO R=3", lambda: pins.test_single_token_mimo_write_and_readout(3)),
     ("lambda = 1 drops the delayed write", pins.test_lambda_one_ignores_delayed_write),
     ("chunked = sequential", lambda: pins.test_chunked_equals_sequential_T256(64)),
+    ("per-token A: Mamba-2 reduction", prep_pins.test_mamba2_reduction_per_token_A),
+    ("per-token A: chunked = sequential", lambda: prep_pins.test_chunked_per_token_A(16)),
+    ("per-token A: two steps closed form", prep_pins.test_closed_form_two_steps_per_token_A),
 ]
 
 
@@ -113,6 +123,8 @@ def test_mutant_fails_a_pin(name, monkeypatch):
         lib = ctypes.CDLL(path)
         lib.m3o_scan.argtypes = real.m3o_scan.argtypes
         lib.m3o_scan.restype = real.m3o_scan.restype
+        lib.m3o_scan_tok.argtypes = real.m3o_scan_tok.argtypes
+        lib.m3o_scan_tok.restype = real.m3o_scan_tok.restype
         lib.m3o_num_threads.argtypes = []
         lib.m3o_num_threads.restype = ctypes.c_int
         monkeypatch.setattr(oracle, "_lib", lib)
