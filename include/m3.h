@@ -181,6 +181,41 @@ M3_API int m3_decode_step(float* state, const void* x_t, const void* B_t, void* 
                    int io_dtype, void* stream);
 
 /*
+ * Per-token parameters from their pre-activations.  The time-varying
+ * discretizations of Table 1 ("Mamba-3: Improved Sequence Modeling using
+ * State Space Principles") take a decay generator per token, alpha_t =
+ * exp(Delta_t A_t), and the default parameterisation of lambda in the
+ * appendix ablation table is lambda_t = sigmoid(u_t).  These entry points take
+ *
+ *   dt_raw   [batch, T, H] fp32: Delta_t = softplus(dt_raw_t + dt_bias[h])
+ *            (softplus(z) = log(1 + e^z); the pages leave Delta's
+ *            parameterisation open, this is the Mamba family's)
+ *   dt_bias  [H] fp32, nullable (= 0)
+ *   A        [batch, T, H] fp32: A_t <= 0, one per token
+ *   u        [batch, T, H] fp32: lambda_t = sigmoid(u_t) = 1 / (1 + e^-u_t)
+ *
+ * and otherwise behave exactly as m3_scan_fwd / m3_decode_step (same
+ * layouts, sizes, errors and stream semantics).  The tensor-core prefill and
+ * the decode kernels apply softplus and sigmoid to the staged values inside
+ * the kernel; the CUDA-core prefill writes Delta and lambda of every token to
+ * the workspace first.  Workspace: m3_scan_fwd_prep_workspace_size bytes
+ * (at least m3_scan_fwd_workspace_size; larger on the CUDA-core path).
+ */
+M3_API size_t m3_scan_fwd_prep_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                                              int64_t dstate, int R, int chunk, int io_dtype);
+M3_API int m3_scan_fwd_prep(const void* x, const void* B, const void* C, const float* dt_raw,
+                            const float* dt_bias, const float* A, const float* u, const float* omega, int R,
+                            int chunk, void* y, float* final_state,
+                            int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+                            int io_dtype, void* workspace, size_t workspace_bytes, void* stream);
+/* Decode on pre-activations: dt_raw_t, A_t, u_t [batch, H] fp32; dt_bias [H] or NULL. */
+M3_API int m3_decode_step_prep(float* state, const void* x_t, const void* B_t, void* B_prev_x_prev,
+                               const void* C_t, const float* dt_raw_t, const float* dt_bias, const float* A_t,
+                               const float* u_t, const float* omega_t, void* y_t,
+                               int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R,
+                               int io_dtype, void* stream);
+
+/*
  * Sticky device-side error word of m3_decode_step, which takes no workspace:
  * M3_OK, or M3_ERR_TIMEOUT once a bounded wait inside a decode kernel gave up
  * (the outputs of that call are then not valid).  Reading it synchronises

@@ -46,6 +46,11 @@ SIGNATURES = {
     "m3_decode_step": ([_fp, _vp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp,
                         _i64, _i64, _i64, _i64, _int, _int, _vp], _int),
     "m3_device_status": ([_int], _int),
+    "m3_scan_fwd_prep_workspace_size": ([_i64, _i64, _i64, _i64, _i64, _int, _int, _int], _sz),
+    "m3_scan_fwd_prep": ([_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _int, _int, _vp, _fp,
+                          _i64, _i64, _i64, _i64, _i64, _int, _vp, _sz, _vp], _int),
+    "m3_decode_step_prep": ([_fp, _vp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp,
+                             _i64, _i64, _i64, _i64, _int, _int, _vp], _int),
     "m3_state_passing": ([_fp, _fp, _fp, _fp, _fp, _i64, _i64, _i64, _i64, _i64, _vp], _int),
 }
 
@@ -163,6 +168,37 @@ def m3_decode_step(state, x_t, B_t, cache, C_t, dt_t, A, lam_t, omega_t, y_t, R:
         _ptr(omega_t, torch.float32), _ptr(y_t, x_t.dtype), b, H, P, N, int(R), io, _stream(stream)))
 
 
+def m3_scan_fwd_prep_workspace_size(batch, seqlen, nheads, headdim, dstate, R, chunk, io) -> int:
+    return int(load().m3_scan_fwd_prep_workspace_size(batch, seqlen, nheads, headdim, dstate, R, chunk, io))
+
+
+def m3_scan_fwd_prep(x, B, C, dt_raw, dt_bias, A, u, omega, R: int, chunk: int, y, final_state, workspace,
+                     stream=None) -> int:
+    """Call m3_scan_fwd_prep (pre-activations, A per token); returns the status code."""
+    Bt, T, H, R_, P = x.shape
+    N = B.shape[-1]
+    io = io_code(x.dtype)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return int(load().m3_scan_fwd_prep(
+        _ptr(x, x.dtype), _ptr(B, x.dtype), _ptr(C, x.dtype), _ptr(dt_raw, torch.float32),
+        _ptr(dt_bias, torch.float32), _ptr(A, torch.float32), _ptr(u, torch.float32), _ptr(omega, torch.float32),
+        int(R), int(chunk), _ptr(y, x.dtype), _ptr(final_state, torch.float32), Bt, T, H, P, N, io,
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def m3_decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, dt_bias, A_t, u_t, omega_t, y_t, R: int,
+                        stream=None) -> int:
+    """Call m3_decode_step_prep (pre-activations, A per (batch, head)); returns the status code."""
+    b, H, R_, P = x_t.shape
+    N = B_t.shape[-1]
+    io = io_code(x_t.dtype)
+    return int(load().m3_decode_step_prep(
+        _ptr(state, torch.float32), _ptr(x_t, x_t.dtype), _ptr(B_t, x_t.dtype), _ptr(cache, x_t.dtype),
+        _ptr(C_t, x_t.dtype), _ptr(dt_raw_t, torch.float32), _ptr(dt_bias, torch.float32), _ptr(A_t, torch.float32),
+        _ptr(u_t, torch.float32), _ptr(omega_t, torch.float32), _ptr(y_t, x_t.dtype), b, H, P, N, int(R), io,
+        _stream(stream)))
+
+
 def m3_device_status(clear: bool = False) -> int:
     """Sticky device-side error word of the decode kernels (M3_OK or M3_ERR_TIMEOUT)."""
     return int(load().m3_device_status(1 if clear else 0))
@@ -184,6 +220,39 @@ def alloc_workspace(x_shape, N: int, R: int, chunk: int, dtype: torch.dtype, dev
     if nbytes == 0:
         return None
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def alloc_workspace_prep(x_shape, N: int, R: int, chunk: int, dtype: torch.dtype, device) -> Optional[torch.Tensor]:
+    Bt, T, H, _, P = x_shape
+    nbytes = m3_scan_fwd_prep_workspace_size(Bt, T, H, P, N, R, chunk, io_code(dtype))
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def scan_fwd_prep(x, B, C, dt_raw, dt_bias, A, u, omega, R: int, chunk: int, want_final: bool = True,
+                  workspace=None, stream=None):
+    """Prefill on pre-activations (Delta = softplus(dt_raw + dt_bias), lambda = sigmoid(u), A per
+    token); returns (y, final_state or None)."""
+    Bt, T, H, _, P = x.shape
+    N = B.shape[-1]
+    y = torch.empty_like(x)
+    fin = torch.empty((Bt, H, N, P), dtype=torch.float32, device=x.device) if want_final else None
+    if workspace is None:
+        workspace = alloc_workspace_prep(x.shape, N, R, chunk, x.dtype, x.device)
+    _check(m3_scan_fwd_prep(x, B, C, dt_raw, dt_bias, A, u, omega, R, chunk, y, fin, workspace, stream),
+           "m3_scan_fwd_prep")
+    return y, fin
+
+
+def decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, dt_bias, A_t, u_t, omega_t, R: int, y_t=None,
+                     stream=None):
+    """One decode token on pre-activations, in place on ``state`` and ``cache``; returns y_t."""
+    if y_t is None:
+        y_t = torch.empty_like(x_t)
+    _check(m3_decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, dt_bias, A_t, u_t, omega_t, y_t, R, stream),
+           "m3_decode_step_prep")
+    return y_t
 
 
 def scan_fwd(x, B, C, dt, A, lam, omega, R: int, chunk: int, want_final: bool = True, workspace=None,

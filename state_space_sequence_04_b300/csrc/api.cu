@@ -13,7 +13,7 @@ int tc_launch_count(const ScanDims& d);
 bool tc_supported(const ScanDims& d);
 cudaError_t launch_scan_tc(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                            const float* A, const float* lambda, const float* omega, void* y, float* final_state,
-                           void* workspace, cudaStream_t stream);
+                           void* workspace, const Prep& prep, cudaStream_t stream);
 
 }  // namespace m3
 
@@ -39,8 +39,53 @@ int validate_scan_sizes(const m3::ScanDims& d) {
     return M3_OK;
 }
 
-size_t scan_workspace(const m3::ScanDims& d) {
-    return pick_path(d) == 1 ? m3::tc_workspace_size(d) : m3::simt_workspace_size(d);
+size_t scan_workspace(const m3::ScanDims& d, bool prep) {
+    return pick_path(d) == 1 ? m3::tc_workspace_size(d) : m3::simt_workspace_size(d, prep);
+}
+
+int scan_impl(const void* x, const void* B, const void* C, const float* dt, const float* A, const float* lambda,
+              const float* omega, int R, int chunk, void* y, float* final_state, int64_t batch, int64_t seqlen,
+              int64_t nheads, int64_t headdim, int64_t dstate, int io_dtype, void* workspace,
+              size_t workspace_bytes, void* stream, const m3::Prep& prep) {
+    const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, chunk, io_dtype};
+    int st = validate_scan_sizes(d);
+    if (st != M3_OK) return st;
+    if (!ok_nullable(final_state) || !ok_nullable(prep.dt_bias)) return M3_ERR_INVALID_ARG;
+    if (!prep.on && !ok_ptr(A)) return M3_ERR_INVALID_ARG;
+    const bool any_tokens = batch > 0 && seqlen > 0;
+    if (any_tokens) {
+        if (!ok_ptr(x) || !ok_ptr(B) || !ok_ptr(C) || !ok_ptr(dt) || !ok_ptr(lambda) || !ok_ptr(omega) || !ok_ptr(y))
+            return M3_ERR_INVALID_ARG;
+        if (prep.on && !ok_ptr(A)) return M3_ERR_INVALID_ARG;
+    }
+    const size_t need = scan_workspace(d, prep.on);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return M3_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (batch == 0) return M3_OK;
+    if (pick_path(d) == 1)
+        return cuda_status(m3::launch_scan_tc(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, prep, s));
+    return cuda_status(m3::launch_scan_simt(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, prep, s));
+}
+
+int decode_impl(float* state, const void* x_t, const void* B_t, void* B_prev_x_prev, const void* C_t,
+                const float* dt_t, const float* A, const float* lambda_t, const float* omega_t, void* y_t,
+                int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R, int io_dtype, void* stream,
+                const m3::Prep& prep) {
+    if (!ok_io(io_dtype)) return M3_ERR_INVALID_ARG;
+    if (batch < 0 || nheads < 1 || headdim < 1 || dstate < 2 || dstate % 2 || R < 1) return M3_ERR_INVALID_ARG;
+    if (!m3::decode_supported(headdim, dstate, R)) return M3_ERR_UNSUPPORTED;
+    if (batch * nheads > (int64_t)INT32_MAX) return M3_ERR_UNSUPPORTED;
+    if (!ok_nullable(prep.dt_bias)) return M3_ERR_INVALID_ARG;
+    if (!prep.on && !ok_ptr(A)) return M3_ERR_INVALID_ARG;
+    if (batch == 0) return M3_OK;
+    if (!ok_ptr(state) || !ok_ptr(x_t) || !ok_ptr(B_t) || !ok_ptr(B_prev_x_prev) || !ok_ptr(C_t) || !ok_ptr(dt_t) ||
+        !ok_ptr(lambda_t) || !ok_ptr(omega_t) || !ok_ptr(y_t) || !ok_ptr(A))
+        return M3_ERR_INVALID_ARG;
+    return cuda_status(m3::launch_decode(state, x_t, B_t, B_prev_x_prev, C_t, dt_t, A, lambda_t, omega_t, y_t, batch,
+                                         nheads, headdim, dstate, R, io_dtype, prep,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -65,7 +110,14 @@ size_t m3_scan_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads,
                                   int R, int chunk, int io_dtype) {
     const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, chunk, io_dtype};
     if (validate_scan_sizes(d) != M3_OK) return 0;
-    return scan_workspace(d);
+    return scan_workspace(d, false);
+}
+
+size_t m3_scan_fwd_prep_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                                       int64_t dstate, int R, int chunk, int io_dtype) {
+    const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, chunk, io_dtype};
+    if (validate_scan_sizes(d) != M3_OK) return 0;
+    return scan_workspace(d, true);
 }
 
 int m3_scan_fwd_plan(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate, int R,
@@ -85,41 +137,32 @@ int m3_scan_fwd(const void* x, const void* B, const void* C, const float* dt, co
                 const float* omega, int R, int chunk, void* y, float* final_state, int64_t batch, int64_t seqlen,
                 int64_t nheads, int64_t headdim, int64_t dstate, int io_dtype, void* workspace,
                 size_t workspace_bytes, void* stream) {
-    const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, chunk, io_dtype};
-    int st = validate_scan_sizes(d);
-    if (st != M3_OK) return st;
-    if (!ok_ptr(A) || !ok_nullable(final_state)) return M3_ERR_INVALID_ARG;
-    const bool any_tokens = batch > 0 && seqlen > 0;
-    if (any_tokens) {
-        if (!ok_ptr(x) || !ok_ptr(B) || !ok_ptr(C) || !ok_ptr(dt) || !ok_ptr(lambda) || !ok_ptr(omega) || !ok_ptr(y))
-            return M3_ERR_INVALID_ARG;
-    }
-    const size_t need = scan_workspace(d);
-    if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
-                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
-        return M3_ERR_WORKSPACE;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (batch == 0) return M3_OK;
-    if (pick_path(d) == 1)
-        return cuda_status(m3::launch_scan_tc(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, s));
-    return cuda_status(m3::launch_scan_simt(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, s));
+    return scan_impl(x, B, C, dt, A, lambda, omega, R, chunk, y, final_state, batch, seqlen, nheads, headdim, dstate,
+                     io_dtype, workspace, workspace_bytes, stream, m3::Prep{false, nullptr});
+}
+
+int m3_scan_fwd_prep(const void* x, const void* B, const void* C, const float* dt_raw, const float* dt_bias,
+                     const float* A, const float* u, const float* omega, int R, int chunk, void* y,
+                     float* final_state, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                     int64_t dstate, int io_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    return scan_impl(x, B, C, dt_raw, A, u, omega, R, chunk, y, final_state, batch, seqlen, nheads, headdim, dstate,
+                     io_dtype, workspace, workspace_bytes, stream, m3::Prep{true, dt_bias});
 }
 
 int m3_decode_step(float* state, const void* x_t, const void* B_t, void* B_prev_x_prev, const void* C_t,
                    const float* dt_t, const float* A, const float* lambda_t, const float* omega_t, void* y_t,
                    int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R, int io_dtype,
                    void* stream) {
-    if (!ok_io(io_dtype)) return M3_ERR_INVALID_ARG;
-    if (batch < 0 || nheads < 1 || headdim < 1 || dstate < 2 || dstate % 2 || R < 1) return M3_ERR_INVALID_ARG;
-    if (!m3::decode_supported(headdim, dstate, R)) return M3_ERR_UNSUPPORTED;
-    if (batch * nheads > (int64_t)INT32_MAX) return M3_ERR_UNSUPPORTED;
-    if (!ok_ptr(A)) return M3_ERR_INVALID_ARG;
-    if (batch == 0) return M3_OK;
-    if (!ok_ptr(state) || !ok_ptr(x_t) || !ok_ptr(B_t) || !ok_ptr(B_prev_x_prev) || !ok_ptr(C_t) || !ok_ptr(dt_t) ||
-        !ok_ptr(lambda_t) || !ok_ptr(omega_t) || !ok_ptr(y_t))
-        return M3_ERR_INVALID_ARG;
-    return cuda_status(m3::launch_decode(state, x_t, B_t, B_prev_x_prev, C_t, dt_t, A, lambda_t, omega_t, y_t, batch,
-                                         nheads, headdim, dstate, R, io_dtype, static_cast<cudaStream_t>(stream)));
+    return decode_impl(state, x_t, B_t, B_prev_x_prev, C_t, dt_t, A, lambda_t, omega_t, y_t, batch, nheads, headdim,
+                       dstate, R, io_dtype, stream, m3::Prep{false, nullptr});
+}
+
+int m3_decode_step_prep(float* state, const void* x_t, const void* B_t, void* B_prev_x_prev, const void* C_t,
+                        const float* dt_raw_t, const float* dt_bias, const float* A_t, const float* u_t,
+                        const float* omega_t, void* y_t, int64_t batch, int64_t nheads, int64_t headdim,
+                        int64_t dstate, int R, int io_dtype, void* stream) {
+    return decode_impl(state, x_t, B_t, B_prev_x_prev, C_t, dt_raw_t, A_t, u_t, omega_t, y_t, batch, nheads, headdim,
+                       dstate, R, io_dtype, stream, m3::Prep{true, dt_bias});
 }
 
 int m3_device_status(int clear) { return m3::decode_device_status(clear); }

@@ -49,15 +49,29 @@ struct DecodeOcc {   // resident CTAs per SM the register budget is sized for (2
     static constexpr int value = R == 1 ? 4 : (R == 2 ? 3 : (R == 4 ? M3_DECODE_OCC_R4 : 2));
 };
 
+// Delta, lambda and A of unit bh = batch * H + h: as given (A per head), or from the
+// pre-activations of the *_prep entry points (A per unit).
+__device__ __forceinline__ void unit_params(const float* dt_t, const float* lam_t, const float* A, const Prep& prep,
+                                            int64_t bh, int H, float& d, float& l, float& a) {
+    if (prep.on) {
+        d = softplus_f(dt_t[bh] + (prep.dt_bias != nullptr ? prep.dt_bias[bh % H] : 0.f));
+        l = sigmoid_f(lam_t[bh]);
+        a = A[bh];
+    } else {
+        d = dt_t[bh];
+        l = lam_t[bh];
+        a = A[bh % H];
+    }
+}
+
 template <typename IO, int R>
 __global__ void __launch_bounds__(256, DecodeOcc<R>::value) decode_kernel(
     float* __restrict__ state, const IO* __restrict__ x_t, const IO* __restrict__ B_t,
     IO* __restrict__ cache, const IO* __restrict__ C_t, const float* __restrict__ dt_t,
     const float* __restrict__ A, const float* __restrict__ lam_t, const float* __restrict__ omega_t,
-    IO* __restrict__ y_t, int H, int P, int N, int G) {
+    IO* __restrict__ y_t, int H, int P, int N, int G, const Prep prep) {
     extern __shared__ __align__(16) float sm[];
     const int64_t bh = blockIdx.x;
-    const int h = (int)(bh % H);
     const int P4 = P >> 2, NP2 = N >> 1;
     const int tid = threadIdx.x, nt = blockDim.x;
 
@@ -86,7 +100,8 @@ __global__ void __launch_bounds__(256, DecodeOcc<R>::value) decode_kernel(
     };
     load_slab(0);
 
-    const float d = dt_t[bh], l = lam_t[bh], a = A[h];
+    float d, l, a;
+    unit_params(dt_t, lam_t, A, prep, bh, H, d, l, a);
     const float alpha = expf(d * a);
     const float beta = (1.0f - l) * d * alpha;
     const float gamma = l * d;
@@ -245,7 +260,7 @@ __global__ void __launch_bounds__(256, 2) decode_stream_kernel(
     float* __restrict__ state, const IO* __restrict__ x_t, const IO* __restrict__ B_t,
     IO* __restrict__ cache, const IO* __restrict__ C_t, const float* __restrict__ dt_t,
     const float* __restrict__ A, const float* __restrict__ lam_t, const float* __restrict__ omega_t,
-    IO* __restrict__ y_t, int H, int P, int N, int G, int64_t units, int nslots) {
+    IO* __restrict__ y_t, int H, int P, int N, int G, int64_t units, int nslots, const Prep prep) {
     extern __shared__ __align__(128) uint8_t smraw[];
     const int P4 = P >> 2, NP2 = N >> 1;
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -291,22 +306,14 @@ __global__ void __launch_bounds__(256, 2) decode_stream_kernel(
     const int c4 = tid % P4, g = tid / P4;
     // scalars of the first unit; later units' are prefetched one unit ahead
     float d_n = 0.f, l_n = 0.f, a_n = 0.f;
-    if (first < units) {
-        d_n = dt_t[first];
-        l_n = lam_t[first];
-        a_n = A[first % H];
-    }
+    if (first < units) unit_params(dt_t, lam_t, A, prep, first, H, d_n, l_n, a_n);
     int it = 0;
     for (int64_t u = first; u < units; u += step, ++it) {
         const int slot = it % nslots;
         const uint32_t parity = (uint32_t)((it / nslots) & 1);
         const float d = d_n, l = l_n, a = a_n;
         const int64_t un = u + step;
-        if (un < units) {
-            d_n = dt_t[un];
-            l_n = lam_t[un];
-            a_n = A[un % H];
-        }
+        if (un < units) unit_params(dt_t, lam_t, A, prep, un, H, d_n, l_n, a_n);
         if (!tc::mbar_wait(&bars[slot], parity, kStreamWaitNs)) *sFail = 1;
         __syncthreads();
         if (*sFail) break;
@@ -476,7 +483,7 @@ DecodeShape decode_shape(int64_t P, int64_t N, int R) {
 template <typename IO, int R>
 cudaError_t launch_t(float* state, const void* x_t, const void* B_t, void* cache, const void* C_t,
                      const float* dt_t, const float* A, const float* lambda_t, const float* omega_t, void* y_t,
-                     int64_t batch, int64_t nheads, int64_t P, int64_t N, cudaStream_t stream) {
+                     int64_t batch, int64_t nheads, int64_t P, int64_t N, const Prep& prep, cudaStream_t stream) {
     const DecodeShape s = decode_shape(P, N, R);
     const int64_t units = batch * nheads;
     const int es = (int)sizeof(IO);
@@ -493,7 +500,7 @@ cudaError_t launch_t(float* state, const void* x_t, const void* B_t, void* cache
             if (grid > units) grid = units;
             kern<<<(unsigned)grid, s.threads, smem, stream>>>(
                 state, (const IO*)x_t, (const IO*)B_t, (IO*)cache, (const IO*)C_t, dt_t, A, lambda_t, omega_t,
-                (IO*)y_t, (int)nheads, (int)P, (int)N, s.G, units, nslots);
+                (IO*)y_t, (int)nheads, (int)P, (int)N, s.G, units, nslots, prep);
             return cudaGetLastError();
         }
     }
@@ -504,16 +511,16 @@ cudaError_t launch_t(float* state, const void* x_t, const void* B_t, void* cache
     }
     kern<<<(unsigned)units, s.threads, s.smem, stream>>>(
         state, (const IO*)x_t, (const IO*)B_t, (IO*)cache, (const IO*)C_t, dt_t, A, lambda_t, omega_t, (IO*)y_t,
-        (int)nheads, (int)P, (int)N, s.G);
+        (int)nheads, (int)P, (int)N, s.G, prep);
     return cudaGetLastError();
 }
 
 template <typename IO>
 cudaError_t launch_io(int R, float* state, const void* x_t, const void* B_t, void* cache, const void* C_t,
                       const float* dt_t, const float* A, const float* lambda_t, const float* omega_t, void* y_t,
-                      int64_t batch, int64_t nheads, int64_t P, int64_t N, cudaStream_t stream) {
+                      int64_t batch, int64_t nheads, int64_t P, int64_t N, const Prep& prep, cudaStream_t stream) {
 #define M3_DEC_CASE(RR) \
-    case RR: return launch_t<IO, RR>(state, x_t, B_t, cache, C_t, dt_t, A, lambda_t, omega_t, y_t, batch, nheads, P, N, stream);
+    case RR: return launch_t<IO, RR>(state, x_t, B_t, cache, C_t, dt_t, A, lambda_t, omega_t, y_t, batch, nheads, P, N, prep, stream);
     switch (R) {
         M3_DEC_CASE(1)
         M3_DEC_CASE(2)
@@ -538,13 +545,13 @@ bool decode_supported(int64_t headdim, int64_t dstate, int R) {
 cudaError_t launch_decode(float* state, const void* x_t, const void* B_t, void* cache, const void* C_t,
                           const float* dt_t, const float* A, const float* lambda_t, const float* omega_t,
                           void* y_t, int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R,
-                          int io, cudaStream_t stream) {
+                          int io, const Prep& prep, cudaStream_t stream) {
     if (batch == 0) return cudaSuccess;
     if (io == M3_DTYPE_BF16)
         return launch_io<__nv_bfloat16>(R, state, x_t, B_t, cache, C_t, dt_t, A, lambda_t, omega_t, y_t, batch,
-                                        nheads, headdim, dstate, stream);
+                                        nheads, headdim, dstate, prep, stream);
     return launch_io<float>(R, state, x_t, B_t, cache, C_t, dt_t, A, lambda_t, omega_t, y_t, batch, nheads,
-                            headdim, dstate, stream);
+                            headdim, dstate, prep, stream);
 }
 
 int decode_device_status(int clear) {

@@ -32,6 +32,12 @@ __device__ __forceinline__ float warp_inclusive_sum(float v) {
     return v;
 }
 
+// Per-token parameters from their pre-activations (the *_prep entry points):
+// Delta = softplus(z) = log(1 + e^z), evaluated as max(z, 0) + log1p(e^-|z|);
+// lambda = sigmoid(u) = 1 / (1 + e^-u) (0 for very negative u, 1 for very positive u).
+__device__ __forceinline__ float softplus_f(float z) { return fmaxf(z, 0.f) + log1pf(__expf(-fabsf(z))); }
+__device__ __forceinline__ float sigmoid_f(float u) { return 1.f / (1.f + __expf(-u)); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -43,6 +49,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 // ---- host-side launchers shared between translation units ----------------
 namespace m3 {
 
+// How the per-token parameters arrive.  on = false: dt = Delta, lambda as given,
+// A one value per head [H].  on = true (the *_prep entry points): dt holds the
+// pre-activation of Delta (Delta = softplus(dt + dt_bias[h]), dt_bias nullable),
+// lambda holds u (lambda = sigmoid(u)), and A holds one value per token with
+// dt's layout.
+struct Prep {
+    bool on;
+    const float* dt_bias;
+};
+
 struct ScanDims {
     int64_t batch, seqlen, nheads, headdim, dstate;
     int R, chunk, io;
@@ -52,7 +68,7 @@ struct ScanDims {
 cudaError_t launch_decode(float* state, const void* x_t, const void* B_t, void* cache, const void* C_t,
                           const float* dt_t, const float* A, const float* lambda_t, const float* omega_t,
                           void* y_t, int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R,
-                          int io, cudaStream_t stream);
+                          int io, const Prep& prep, cudaStream_t stream);
 bool decode_supported(int64_t headdim, int64_t dstate, int R);
 int decode_device_status(int clear);
 
@@ -61,10 +77,11 @@ cudaError_t launch_state_passing(float* chunk_states, const float* chunk_logdeca
                                  int64_t nchunks, int64_t dstate, int64_t headdim, cudaStream_t stream);
 
 // Generic CUDA-core chunked prefill (any supported size; fp32 or bf16 io).
-size_t simt_workspace_size(const ScanDims& d);
+// With prep.on the workspace also holds Delta and lambda of every token.
+size_t simt_workspace_size(const ScanDims& d, bool prep);
 bool simt_supported(const ScanDims& d);
 cudaError_t launch_scan_simt(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                              const float* A, const float* lambda, const float* omega, void* y,
-                             float* final_state, void* workspace, cudaStream_t stream);
+                             float* final_state, void* workspace, const Prep& prep, cudaStream_t stream);
 
 }  // namespace m3

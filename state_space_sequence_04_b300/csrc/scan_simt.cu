@@ -21,6 +21,8 @@
 //
 // Three launches: chunk states U_c (kernel A), the state-passing scan (in
 // place, giving H_{c-1}), chunk outputs (kernel C).
+#include <algorithm>
+
 #include "m3_common.cuh"
 
 namespace m3 {
@@ -50,7 +52,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(
     const IO* __restrict__ x, const IO* __restrict__ B, const float* __restrict__ dt,
     const float* __restrict__ A, const float* __restrict__ lam, const float* __restrict__ omega,
     float* __restrict__ U, float* __restrict__ ld_out, float* __restrict__ ang_out,
-    int64_t T, int H, int P, int N, int Q, int nc) {
+    int64_t T, int H, int P, int N, int Q, int nc, int a_tok) {
     extern __shared__ float sm[];
     constexpr int KB = 32 / R > 0 ? 32 / R : 1;   // tokens per staging block
     const int64_t bh = blockIdx.x;
@@ -69,12 +71,12 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(
     float* sBr = sAng + NP2;         // [KB*R][N]
     float* sX = sBr + KB * R * N;    // [KB*R][P]
 
-    const float a = A[h];
+    const float a_head = a_tok ? 0.f : A[h];
     float ell = 0.f, gam = 0.f, wnext = 0.f;
     if (tid < q) {
         const int64_t idx = (b * T + c0 + tid) * H + h;
         const float d = dt[idx], l = lam[idx];
-        ell = d * a;
+        ell = d * (a_tok ? A[idx] : a_head);
         gam = l * d;
         if (c0 + tid + 1 < T) {
             const int64_t in = idx + H;
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     const IO* __restrict__ x, const IO* __restrict__ B, const IO* __restrict__ C,
     const float* __restrict__ dt, const float* __restrict__ A, const float* __restrict__ lam,
     const float* __restrict__ omega, const float* __restrict__ Hc, IO* __restrict__ y,
-    int64_t T, int H, int P, int N, int Q, int nc) {
+    int64_t T, int H, int P, int N, int Q, int nc, int a_tok) {
     extern __shared__ float sm[];
     constexpr int RT = kRowTile;
     constexpr int TT = RT / R;
@@ -184,12 +186,12 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     float* sX = sBt + N * LD;            // [RT][P]
     float* sS = sX + RT * P;             // [RT][RT+1]
 
-    const float a = A[h];
+    const float a_head = a_tok ? 0.f : A[h];
     float ell = 0.f, gam = 0.f, wsh = 0.f;
     if (tid < q) {
         const int64_t idx = (b * T + c0 + tid) * H + h;
         const float d = dt[idx], l = lam[idx];
-        ell = d * a;
+        ell = d * (a_tok ? A[idx] : a_head);
         gam = l * d;
         wsh = gam;
         if (tid + 1 < q) wsh += (1.f - lam[idx + H]) * dt[idx + H];
@@ -372,7 +374,7 @@ size_t smem_c(const ScanDims& d) {
 template <typename IO, int R>
 cudaError_t launch_rt(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                       const float* A, const float* lambda, const float* omega, void* y, float* final_state,
-                      void* workspace, cudaStream_t stream) {
+                      void* workspace, int a_tok, cudaStream_t stream) {
     const int64_t bh = d.batch * d.nheads;
     const int64_t nc = d.nchunks();
     const int64_t NP = d.dstate * d.headdim;
@@ -386,7 +388,7 @@ cudaError_t launch_rt(const ScanDims& d, const void* x, const void* B, const voi
         if ((e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa)) != cudaSuccess) return e;
         ka<<<dim3((unsigned)bh, (unsigned)nc), kThreads, sa, stream>>>(
             (const IO*)x, (const IO*)B, dt, A, lambda, omega, U, ld, ang, d.seqlen, (int)d.nheads, (int)d.headdim,
-            (int)d.dstate, d.chunk, (int)nc);
+            (int)d.dstate, d.chunk, (int)nc, a_tok);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if ((e = launch_state_passing(U, ld, ang, nullptr, final_state, d.batch, d.nheads, nc, d.dstate, d.headdim,
@@ -400,7 +402,7 @@ cudaError_t launch_rt(const ScanDims& d, const void* x, const void* B, const voi
         const unsigned tiles = (unsigned)((d.chunk + TT - 1) / TT);
         kc<<<dim3((unsigned)bh, (unsigned)nc, tiles), kThreads, sc, stream>>>(
             (const IO*)x, (const IO*)B, (const IO*)C, dt, A, lambda, omega, U, (IO*)y, d.seqlen, (int)d.nheads,
-            (int)d.headdim, (int)d.dstate, d.chunk, (int)nc);
+            (int)d.headdim, (int)d.dstate, d.chunk, (int)nc, a_tok);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -409,15 +411,28 @@ cudaError_t launch_rt(const ScanDims& d, const void* x, const void* B, const voi
 template <typename IO>
 cudaError_t launch_io(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                       const float* A, const float* lambda, const float* omega, void* y, float* final_state,
-                      void* workspace, cudaStream_t stream) {
+                      void* workspace, int a_tok, cudaStream_t stream) {
     switch (d.R) {
-        case 1: return launch_rt<IO, 1>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, stream);
-        case 2: return launch_rt<IO, 2>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, stream);
-        case 4: return launch_rt<IO, 4>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, stream);
-        case 8: return launch_rt<IO, 8>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, stream);
+        case 1: return launch_rt<IO, 1>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
+        case 2: return launch_rt<IO, 2>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
+        case 4: return launch_rt<IO, 4>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
+        case 8: return launch_rt<IO, 8>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
         default: return cudaErrorInvalidValue;
     }
 }
+
+// Delta = softplus(dt_raw + dt_bias[h]) and lambda = sigmoid(u) of every (batch, token, head).
+__global__ void __launch_bounds__(256) prep_kernel(const float* __restrict__ dt_raw, const float* __restrict__ dt_bias,
+                                                   const float* __restrict__ u, float* __restrict__ dt_out,
+                                                   float* __restrict__ lam_out, int64_t n, int H) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float bias = dt_bias != nullptr ? dt_bias[i % H] : 0.f;
+        dt_out[i] = softplus_f(dt_raw[i] + bias);
+        lam_out[i] = sigmoid_f(u[i]);
+    }
+}
+
+size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 
 }  // namespace
 
@@ -430,18 +445,38 @@ bool simt_supported(const ScanDims& d) {
     return smem_a(d) <= 220 * 1024 && smem_c(d) <= 220 * 1024;
 }
 
-size_t simt_workspace_size(const ScanDims& d) {
+size_t simt_workspace_size(const ScanDims& d, bool prep) {
     const int64_t bh = d.batch * d.nheads;
     const int64_t nc = d.nchunks();
-    return sizeof(float) * (size_t)(bh * nc * (d.dstate * d.headdim + 1 + d.dstate / 2));
+    const size_t base = sizeof(float) * (size_t)(bh * nc * (d.dstate * d.headdim + 1 + d.dstate / 2));
+    if (!prep) return base;
+    const size_t n = (size_t)(d.batch * d.seqlen * d.nheads);
+    return al256(base) + 2 * al256(n * sizeof(float));
 }
 
 cudaError_t launch_scan_simt(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                              const float* A, const float* lambda, const float* omega, void* y,
-                             float* final_state, void* workspace, cudaStream_t stream) {
+                             float* final_state, void* workspace, const Prep& prep, cudaStream_t stream) {
+    if (prep.on) {
+        // Delta and lambda of every token into the tail of the workspace, then the same kernels
+        // with one decay generator per token
+        const int64_t n = d.batch * d.seqlen * d.nheads;
+        uint8_t* tail = static_cast<uint8_t*>(workspace) + al256(simt_workspace_size(d, false));
+        float* dt_eff = reinterpret_cast<float*>(tail);
+        float* lam_eff = reinterpret_cast<float*>(tail + al256((size_t)n * sizeof(float)));
+        if (n > 0) {
+            const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, 148 * 16);
+            prep_kernel<<<blocks, 256, 0, stream>>>(dt, prep.dt_bias, lambda, dt_eff, lam_eff, n, (int)d.nheads);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        dt = dt_eff;
+        lambda = lam_eff;
+    }
+    const int a_tok = prep.on ? 1 : 0;
     if (d.io == M3_DTYPE_BF16)
-        return launch_io<__nv_bfloat16>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, stream);
-    return launch_io<float>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, stream);
+        return launch_io<__nv_bfloat16>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
+    return launch_io<float>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
 }
 
 }  // namespace m3

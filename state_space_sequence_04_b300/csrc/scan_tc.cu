@@ -124,7 +124,8 @@ struct Cfg {
 };
 
 struct TcArgs {
-    const float* A;
+    const float* A;          // [H], or [Bt,T,H] (one per token) in the pre-activation variant
+    const float* dt_bias;    // pre-activation variant: [H] or null
     const float* omega;
     __nv_bfloat16* y;
     float* final_state;
@@ -241,7 +242,10 @@ __device__ __forceinline__ void mask_block(float* v, int cb, int t, float ct, fl
 // segmented prefill -- only the carry (rotated, scaled B, scaled X and the
 // chunk-state MMA), whose value at the segment's end from a zero start, summed
 // log-decay and summed angles go to the workspace for the segment scan.
-template <int NS, int R, int Q, bool FULL>
+// PREP = true: the dt and lambda inputs are pre-activations (Delta =
+// softplus(dt + dt_bias[h]), lambda = sigmoid(u), applied to the staged boxes in
+// shared memory) and A holds one decay generator per token.
+template <int NS, int R, int Q, bool FULL, bool PREP>
 __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                          const __grid_constant__ CUtensorMap tm_B,
                                                          const __grid_constant__ CUtensorMap tm_C,
@@ -679,13 +683,34 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             }
         };
         load_omega(c_begin);
-        const float a = args.A[h];
+        const float a = PREP ? 0.f : args.A[h];
+        // pre-activation variant: this thread's token's decay generator, one chunk ahead
+        float a_nx = 0.f;
+        const float bias = PREP && args.dt_bias != nullptr ? args.dt_bias[h] : 0.f;
+        auto load_a = [&](int c) {
+            const int t = c * Q + rt;
+            return rt < Q && t < T ? args.A[((int64_t)b * T + t) * args.H + h] : 0.f;
+        };
+        if (PREP) a_nx = load_a(c_begin);
         for (int i = 0; i < nl; ++i) {
             const int c = c_begin + i, s = i & 1;
             (void)wait_bounded(&ctl->fbox[s], (i >> 1) & 1, fail_r, fail_c);
             group_bar(2);
             if (*fail_r) break;
             if (rt == 0) ctl->box_waited[s] += 1;
+            float a_t = a;
+            if constexpr (PREP) {
+                // Delta and lambda of this head's Q+1 staged tokens, in place (0 past the end)
+                for (int k = rt; k <= Q; k += 128) {
+                    const bool in = (int64_t)c * Q + k < T;
+                    float* pd = box_dt(s) + k * 4 + hq;
+                    float* pl = box_lam(s) + k * 4 + hq;
+                    *pd = in ? softplus_f(*pd + bias) : 0.f;
+                    *pl = in ? sigmoid_f(*pl) : 0.f;
+                }
+                a_t = a_nx;
+                group_bar(2);
+            }
             const float* sDt = box_dt(s);
             const float* sLam = box_lam(s);
             float* co = coef(s);
@@ -703,7 +728,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
 #pragma unroll
             for (int k = 0; k < TPG; ++k) dtk[k] = sDt[(tg * TPG + k) * 4 + hq];
             // ---- coefficients and chunk-local log-decay prefix
-            const float ell = d * a, gam = l * d, wv = gam + (1.f - ln) * dn;
+            const float ell = d * a_t, gam = l * d, wv = gam + (1.f - ln) * dn;
             float cum = warp_inclusive_sum(ell);
             if (lane == 31) sWarpR[rw] = cum;
             // the consumer is done with chunk i-2's coefficients in this stage
@@ -793,7 +818,10 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 }
                 if (tg == TG - 1) *reinterpret_cast<float4*>(&co[K::CO_THETA + 4 * jg]) = psi;
             }
-            if (i + 1 < nl) load_omega(c + 1);
+            if (i + 1 < nl) {
+                load_omega(c + 1);
+                if (PREP) a_nx = load_a(c + 1);
+            }
             group_bar(2);   // partial sums read: the boxes may take chunk i+2
             if (rt == 0 && i + 2 < nl && !*fail_r) load_box(i + 2, s);
 
@@ -908,10 +936,10 @@ SegWs seg_ws(const ScanDims& d) {
     return w;
 }
 
-template <int NS, int R, int Q>
+template <int NS, int R, int Q, bool PREP>
 cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                        const float* A, const float* lambda, const float* omega, void* y, float* final_state,
-                       void* workspace, cudaStream_t stream) {
+                       void* workspace, const float* dt_bias, cudaStream_t stream) {
     using K = Cfg<NS, R, Q>;
     const cuuint64_t Bt = d.batch, T = d.seqlen, H = d.nheads, P = d.headdim, N = d.dstate;
     CUtensorMap mx, mB, mC, mdt, mlam;
@@ -946,6 +974,7 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
     const int64_t seqs = d.batch * d.nheads;
     TcArgs args{};
     args.A = A;
+    args.dt_bias = dt_bias;
     args.omega = omega;
     args.y = static_cast<__nv_bfloat16*>(y);
     args.final_state = final_state;
@@ -967,7 +996,7 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
         a1.seg_U = segU;
         a1.seg_ld = segLD;
         a1.seg_th = segTH;
-        auto k1 = scan_tc_kernel<NS, R, Q, false>;
+        auto k1 = scan_tc_kernel<NS, R, Q, false, PREP>;
         e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
         if (e != cudaSuccess) return e;
         k1<<<(unsigned)(seqs * a1.nseg), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, a1);
@@ -979,7 +1008,7 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
         args.h_in_last = last;
     }
     args.nseg = pl.S;
-    auto kern = scan_tc_kernel<NS, R, Q, true>;
+    auto kern = scan_tc_kernel<NS, R, Q, true, PREP>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)(seqs * pl.S), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, args);
@@ -992,15 +1021,18 @@ template <int NS, int R, int Q>
 int launches_cfg(const ScanDims& d) { return seg_plan<NS, R, Q>(d).S > 1 ? 3 : 1; }
 
 typedef cudaError_t (*LaunchFn)(const ScanDims&, const void*, const void*, const void*, const float*, const float*,
-                                const float*, const float*, void*, float*, void*, cudaStream_t);
+                                const float*, const float*, void*, float*, void*, const float*, cudaStream_t);
 struct TcImpl {
-    LaunchFn launch;
+    LaunchFn launch;        // dt, lambda, A[H] as given
+    LaunchFn launch_prep;   // pre-activations, A per token
     size_t (*workspace)(const ScanDims&);
     int (*launches)(const ScanDims&);
 };
 
 template <int NS, int R, int Q>
-TcImpl impl() { return TcImpl{launch_cfg<NS, R, Q>, ws_cfg<NS, R, Q>, launches_cfg<NS, R, Q>}; }
+TcImpl impl() {
+    return TcImpl{launch_cfg<NS, R, Q, false>, launch_cfg<NS, R, Q, true>, ws_cfg<NS, R, Q>, launches_cfg<NS, R, Q>};
+}
 
 // Tile configuration for (N, R, chunk).  Chunks of chunk*R <= 128 rows run as
 // given.  Wider MIMO chunks run as sub-chunks of chunk/R tokens -- the MIMO
@@ -1037,10 +1069,11 @@ int tc_launch_count(const ScanDims& d) {
 }
 cudaError_t launch_scan_tc(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                            const float* A, const float* lambda, const float* omega, void* y, float* final_state,
-                           void* workspace, cudaStream_t stream) {
+                           void* workspace, const Prep& prep, cudaStream_t stream) {
     TcImpl f;
     if (!pick(d, &f)) return cudaErrorNotSupported;
-    return f.launch(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, stream);
+    return (prep.on ? f.launch_prep : f.launch)(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace,
+                                                prep.dt_bias, stream);
 }
 
 }  // namespace m3
