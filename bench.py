@@ -75,6 +75,11 @@ def prefill_bytes(w: synth.Workload) -> int:
     return per_ht * w.batch * w.seqlen * w.heads + w.batch * w.heads * N * P * 4 + w.heads * 4
 
 
+def prefill_prep_bytes(w: synth.Workload) -> int:
+    """As prefill_bytes, plus the per-token decay generator (4 B per (token, head)) and dt_bias."""
+    return prefill_bytes(w) + 4 * w.batch * w.seqlen * w.heads
+
+
 def prefill_tc_flops(w: synth.Workload) -> float:
     """Tensor-core FLOPs of the chunked form per call: causal half of the (QR)^2 score
     square times N and P, plus chunk state (N x P x QR) and inter output (QR x N x P)."""
@@ -206,18 +211,9 @@ def barrier(dist):
 
 
 # ---------------------------------------------------------------------------
-def time_prefill(binding, w, d, stream, steps, warmup, dist, device):
-    """Device-resident prefill: returns (total seconds max over ranks, per-call event ms list)."""
-    y = torch.empty_like(d["x"])
-    fin = torch.empty((w.batch, w.heads, w.dstate, w.headdim), dtype=torch.float32, device=device)
-    ws = binding.alloc_workspace(d["x"].shape, w.dstate, w.rank, w.chunk, d["x"].dtype, device)
-    args = [d[k] for k in KEYS]
-
-    def call():
-        st = binding.m3_scan_fwd(*args, w.rank, w.chunk, y, fin, ws, stream)
-        if st != 0:
-            raise binding.M3Error(st, "m3_scan_fwd")
-
+def _time_calls(call, stream, steps, warmup, dist, device):
+    """W untimed calls, then K timed calls between a barrier and a synchronize on both
+    sides: (total seconds max over ranks, per-call event ms list)."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             call()
@@ -237,7 +233,41 @@ def time_prefill(binding, w, d, stream, steps, warmup, dist, device):
     barrier(dist)
     total_ms = start.elapsed_time(end)
     per = [a.elapsed_time(b) for a, b in ev]
-    return max_over_ranks(dist, total_ms, device) / 1e3, per, (y, fin)
+    return max_over_ranks(dist, total_ms, device) / 1e3, per
+
+
+def time_prefill(binding, w, d, stream, steps, warmup, dist, device):
+    """Device-resident prefill: returns (total seconds max over ranks, per-call event ms list)."""
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((w.batch, w.heads, w.dstate, w.headdim), dtype=torch.float32, device=device)
+    ws = binding.alloc_workspace(d["x"].shape, w.dstate, w.rank, w.chunk, d["x"].dtype, device)
+    args = [d[k] for k in KEYS]
+
+    def call():
+        st = binding.m3_scan_fwd(*args, w.rank, w.chunk, y, fin, ws, stream)
+        if st != 0:
+            raise binding.M3Error(st, "m3_scan_fwd")
+
+    sec, per = _time_calls(call, stream, steps, warmup, dist, device)
+    return sec, per, (y, fin)
+
+
+PREP_KEYS = ("x", "B", "C", "dt_raw", "dt_bias", "A", "u", "omega")
+
+
+def time_prefill_prep(binding, w, dp, stream, steps, warmup, dist, device):
+    """The same over m3_scan_fwd_prep (pre-activations, one decay generator per token)."""
+    y = torch.empty_like(dp["x"])
+    fin = torch.empty((w.batch, w.heads, w.dstate, w.headdim), dtype=torch.float32, device=device)
+    ws = binding.alloc_workspace_prep(dp["x"].shape, w.dstate, w.rank, w.chunk, dp["x"].dtype, device)
+    args = [dp[k] for k in PREP_KEYS]
+
+    def call():
+        st = binding.m3_scan_fwd_prep(*args, w.rank, w.chunk, y, fin, ws, stream)
+        if st != 0:
+            raise binding.M3Error(st, "m3_scan_fwd_prep")
+
+    return _time_calls(call, stream, steps, warmup, dist, device)
 
 
 def time_prefill_e2e(binding, w, host, stream, steps, warmup, dist, device, copy_streams=4):
@@ -483,6 +513,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prep", action="store_true", help="skip the pre-activation prefill measurement")
     ap.add_argument("--workload", default=synth.SISO_1P5B.name, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--mode", choices=["all", "decode"], default="all",
                     help="decode: only the decode sweep (restricted by --decode-batch/--decode-rank)")
@@ -546,6 +577,22 @@ def main():
                      "tc_tflops": tflops, "tc_frac_of_bf16_peak": tflops / pk["bf16_tflops"]},
         "clocks": clocks,
     }
+
+    if not args.no_prep:
+        # the same workload through m3_scan_fwd_prep: Delta, lambda from pre-activations and one
+        # decay generator per token, derived inside the kernels
+        dp = {k: v for k, v in synth.make_prep_inputs(w, seed=rank, device=device).items() if k in PREP_KEYS}
+        psec, pper = time_prefill_prep(binding, w, dp, stream, args.steps, args.warmup, dist, device)
+        pms = sum(pper) / len(pper)
+        pbytes = prefill_prep_bytes(w)
+        line["prefill_prep"] = {
+            "value": tokens * args.steps / psec / 1e6, "unit": "Mtok/s", "ms_per_step": psec / args.steps * 1e3,
+            "entry": "m3_scan_fwd_prep", "algorithmic_bytes_per_call": pbytes,
+            "roofline": {"bound": "hbm", "achieved": pbytes / (pms * 1e-3) / 1e9, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": pbytes / (pms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+            # the CUDA-core path derives Delta and lambda in one extra elementwise launch
+            "gpu_launches": (launches + (1 if path == 0 else 0)) * args.steps}
+        del dp
 
     if not args.no_e2e:
         host = {k: d[k].to("cpu").pin_memory() for k in KEYS}
