@@ -22,7 +22,9 @@ y [Bt,T,H,R,P], states [Bt,H,N,P], delayed-write cache [Bt,H,R*N+R*P].
 ``prep`` / ``scan_prep`` / ``decode_step_prep`` take the pre-activations of
 the per-token parameters instead: Delta_t = softplus(dt_raw_t + dt_bias_h),
 lambda_t = sigmoid(u_t) (the default lambda parameterisation of the appendix
-ablation table), A_t given per token.
+ablation table), A_t given per token; optionally B and C are RMS-normalised
+over N, then shifted by per-head channel biases, before the rotation
+(``bc_prep``; the BC normalisation and biases of section 3.4).
 """
 from __future__ import annotations
 
@@ -147,18 +149,70 @@ def prep(dt_raw, dt_bias, u):
     return softplus(z), sigmoid(u)
 
 
-def scan_prep(x, B, C, dt_raw, dt_bias, A_tok, u, omega, h0=None, prev=None):
-    """``scan`` on pre-activations: Delta, lambda from ``prep``, A_tok [Bt,T,H] per token."""
+def bc_prep(V, norm: bool = False, eps: float = 0.0, gain=None, bias=None):
+    """B or C before the rotation (float64): every (token, rank) row v of V [..., H, R, N]
+    becomes v / sqrt(mean(v^2) + eps) * gain when ``norm`` (gain [N], None = 1), then
+    the head-specific channel bias [H, R, N] is added (None = 0)."""
+    V = f64(V)
+    if norm:
+        V = V / np.sqrt(np.mean(V * V, axis=-1, keepdims=True) + eps)
+        if gain is not None:
+            V = V * f64(gain)
+    if bias is not None:
+        V = V + f64(bias)
+    return V
+
+
+def _bc(B, C, bc):
+    bc = bc or {}
+    norm, eps = bool(bc.get("norm", False)), float(bc.get("eps", 0.0))
+    return (bc_prep(B, norm, eps, bc.get("B_gain"), bc.get("B_bias")),
+            bc_prep(C, norm, eps, bc.get("C_gain"), bc.get("C_bias")))
+
+
+def scan_prep(x, B, C, dt_raw, dt_bias, A_tok, u, omega, h0=None, prev=None, bc=None):
+    """``scan`` on pre-activations: Delta, lambda from ``prep``, A_tok [Bt,T,H] per token;
+    ``bc`` (dict: norm, eps, B_gain, C_gain, B_bias, C_bias) normalises and biases B and C
+    with ``bc_prep`` first.  ``prev`` holds the raw (unnormalised) B_{t-1}, X_{t-1}."""
     d, lam = prep(dt_raw, dt_bias, u)
-    return scan(x, B, C, d, A_tok, lam, omega, h0=h0, prev=prev)
+    Bn, Cn = _bc(B, C, bc)
+    if prev is not None and bc:
+        prev = _prev_bc(prev, f64(B).shape[-3:], f64(x).shape[-1], bc)
+    y, hT, prevT = scan(x, Bn, Cn, d, A_tok, lam, omega, h0=h0, prev=prev)
+    if bc:   # hand back the raw factors of the last token, as the kernels keep them
+        prevT = _prev_raw(f64(B)[:, -1], f64(x)[:, -1])
+    return y, hT, prevT
 
 
-def decode_step_prep(state, x_t, B_t, prev, C_t, dt_raw_t, dt_bias, A_t, u_t, omega_t):
-    """One decode token on pre-activations: dt_raw_t, A_t, u_t [b,H]; dt_bias [H] or None."""
+def _prev_bc(prev, hrn, P, bc):
+    """The delayed-write cache [b,H,R*N+R*P] with its B_{t-1} part normalised and biased."""
+    prev = f64(prev).copy()
+    H, R, N = hrn
+    b = prev.shape[0]
+    Bp = prev[:, :, :R * N].reshape(b, H, R, N)
+    Bn, _ = _bc(Bp, Bp, bc)
+    prev[:, :, :R * N] = Bn.reshape(b, H, R * N)
+    return prev
+
+
+def _prev_raw(B_last, x_last):
+    b, H = B_last.shape[:2]
+    return np.concatenate([B_last.reshape(b, H, -1), x_last.reshape(b, H, -1)], axis=-1)
+
+
+def decode_step_prep(state, x_t, B_t, prev, C_t, dt_raw_t, dt_bias, A_t, u_t, omega_t, bc=None):
+    """One decode token on pre-activations: dt_raw_t, A_t, u_t [b,H]; dt_bias [H] or None;
+    ``prev`` and the returned cache hold the raw B_{t-1}, X_{t-1}."""
     d, lam = prep(dt_raw_t, dt_bias, u_t)
+    Bt, Ct = f64(B_t), f64(C_t)
+    Bn, Cn = _bc(Bt, Ct, bc)
+    if prev is not None and bc:
+        prev = _prev_bc(prev, Bt.shape[-3:], f64(x_t).shape[-1], bc)
     xt = f64(x_t)[:, None]
-    y, hT, prevT = scan(xt, f64(B_t)[:, None], f64(C_t)[:, None], d[:, None], f64(A_t)[:, None],
+    y, hT, prevT = scan(xt, Bn[:, None], Cn[:, None], d[:, None], f64(A_t)[:, None],
                         lam[:, None], f64(omega_t)[:, None], h0=state, prev=prev)
+    if bc:
+        prevT = _prev_raw(Bt, f64(x_t))
     return y[:, 0], hT, prevT
 
 

@@ -154,6 +154,22 @@ def make_prep_inputs(w: Workload, seed: int = 0, device="cpu", seqlen: Optional[
     }
 
 
+def make_bc_params(heads: int, rank: int, dstate: int, seed: int = 7, device="cpu") -> dict:
+    """Parameters of the B / C normalisation and channel biases.
+
+    Draw order: B_gain, C_gain [N] ~ 1 + 0.1 N(0,1); B_bias, C_bias [H, R, N] ~ 0.1 N(0,1).
+    eps = 1e-5.
+    """
+    g = _gen(seed, device)
+    f32 = torch.float32
+    N = dstate
+    B_gain = 1.0 + 0.1 * torch.randn((N,), generator=g, device=device, dtype=f32)
+    C_gain = 1.0 + 0.1 * torch.randn((N,), generator=g, device=device, dtype=f32)
+    B_bias = 0.1 * torch.randn((heads, rank, N), generator=g, device=device, dtype=f32)
+    C_bias = 0.1 * torch.randn((heads, rank, N), generator=g, device=device, dtype=f32)
+    return {"norm": True, "eps": 1e-5, "B_gain": B_gain, "C_gain": C_gain, "B_bias": B_bias, "C_bias": C_bias}
+
+
 def make_decode_state(batch: int, heads: int, dstate: int, headdim: int, seed: int = 0,
                       device="cpu") -> torch.Tensor:
     """fp32 state [b, H, N, P] ~ N(0, 1)."""

@@ -6,10 +6,13 @@ State Space Principles" take a decay generator per token, exp(Delta_t A_t)
 (thelatestinai.com/papers/2603.15569, Table 1), and the default lambda
 parameterisation of the appendix ablation table is lambda_t = sigmoid(u_t);
 Delta_t = softplus(dt_raw_t + dt_bias_h) is the Mamba family's
-parameterisation (the pages leave it open).  Each test compares the oracle
-with something other than itself: the independent numpy evaluations of
-``oracle.forms`` (which take the decay generator per token), hand-derived
-closed forms, or identities of softplus and sigmoid.
+parameterisation (the pages leave it open).  B and C may also be
+RMS-normalised over N and shifted by per-head channel biases before the
+rotation (section 3.4).  Each test compares the oracle with something other
+than itself: the independent numpy evaluations of ``oracle.forms`` (which take
+the decay generator per token), hand-derived closed forms, identities of
+softplus and sigmoid, invariances of the normalisation and the linearity of the
+readout in C; planted mistakes in the normalisation fail these pins.
 """
 import math
 
@@ -180,3 +183,135 @@ def test_large_u_removes_delayed_write():
     y, _, _ = oracle.scan_prep(raw["x"], raw["B"], raw["C"], raw["dt_raw"], raw["dt_bias"], raw["A"], u, raw["omega"])
     ref = forms.complex_form(inp["x"], inp["B"], inp["C"], inp["dt"], inp["A"], np.ones_like(inp["lam"]), inp["omega"])
     assert oracle.rel_err(y, ref) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# B / C normalisation and head-specific channel biases (section 3.4), applied
+# to every (token, rank) row over the state dimension N before the rotation
+def test_bc_prep_closed_form():
+    v = np.array([3.0, 4.0]).reshape(1, 1, 1, 1, 2)        # one row, N = 2
+    out = oracle.bc_prep(v, norm=True, eps=0.0, gain=np.array([2.0, 0.5]), bias=np.array([1.0, -1.0]).reshape(1, 1, 2))
+    r = math.sqrt((9.0 + 16.0) / 2.0)
+    assert abs(out[0, 0, 0, 0, 0] - (2.0 * 3.0 / r + 1.0)) < 1e-15
+    assert abs(out[0, 0, 0, 0, 1] - (0.5 * 4.0 / r - 1.0)) < 1e-15
+    # eps enters the mean square; without the norm only the bias is added
+    out = oracle.bc_prep(v, norm=True, eps=0.5)
+    assert abs(out[0, 0, 0, 0, 0] - 3.0 / math.sqrt(12.5 + 0.5)) < 1e-15
+    out = oracle.bc_prep(v, norm=False, bias=np.array([1.0, -1.0]).reshape(1, 1, 2))
+    assert np.array_equal(out.ravel(), [4.0, 3.0])
+
+
+def test_bc_norm_rows_have_unit_rms():
+    inp = _prep_inputs(T=9, R=3, N=8, seed=2)
+    Bn = oracle.bc_prep(inp["B"], norm=True, eps=0.0)
+    assert np.max(np.abs(np.mean(Bn * Bn, axis=-1) - 1.0)) < 1e-14
+
+
+def _scan_bc(inp, B, C, bc):
+    raw = inp["raw"]
+    return oracle.scan_prep(inp["x"], B, C, raw["dt_raw"], raw["dt_bias"], raw["A"], raw["u"], raw["omega"], bc=bc)
+
+
+def test_bc_norm_scale_invariance():
+    """With the norm on (eps = 0, no bias) rescaling each row of B and C changes nothing."""
+    inp = _prep_inputs(T=21, R=2, seed=12)
+    bc = {"norm": True, "eps": 0.0}
+    y1, h1, _ = _scan_bc(inp, inp["B"], inp["C"], bc)
+    sB = np.exp(np.random.default_rng(0).standard_normal(inp["B"].shape[:-1]))[..., None]
+    y2, h2, _ = _scan_bc(inp, inp["B"] * sB, inp["C"] * 0.2, bc)
+    assert oracle.rel_err(y2, y1) < 1e-12 and oracle.rel_err(h2, h1) < 1e-12
+
+
+def test_bc_bias_enters_the_readout_linearly():
+    """y_t = h_t^T C_t is linear in C_t: a C bias b adds exactly the output of C = b."""
+    inp = _prep_inputs(T=17, R=2, seed=13)
+    Bt, T, H, R, N = inp["C"].shape
+    b = 0.3 * np.random.default_rng(1).standard_normal((H, R, N))
+    y_b, _, _ = _scan_bc(inp, inp["B"], inp["C"], {"C_bias": b})
+    y_0, _, _ = _scan_bc(inp, inp["B"], inp["C"], None)
+    y_only, _, _ = _scan_bc(inp, inp["B"], np.zeros_like(inp["C"]), {"C_bias": b})
+    assert oracle.rel_err(y_b, y_0 + y_only) < 1e-12
+
+
+def test_bc_gain_scales_the_readout():
+    inp = _prep_inputs(T=15, R=1, seed=14)
+    N = inp["C"].shape[-1]
+    y1, _, _ = _scan_bc(inp, inp["B"], inp["C"], {"norm": True, "eps": 1e-5})
+    y2, _, _ = _scan_bc(inp, inp["B"], inp["C"], {"norm": True, "eps": 1e-5, "C_gain": np.full(N, 2.5)})
+    assert oracle.rel_err(y2, 2.5 * y1) < 1e-13
+
+
+def test_continuation_with_bc():
+    """Prefill then decode with the B / C normalisation and biases; the cache holds raw B, X."""
+    inp = _prep_inputs(R=2, T=36, N=6, seed=15)
+    raw = {k: oracle.f64(v) for k, v in inp["raw"].items() if hasattr(v, "shape")}
+    bcp = synth.make_bc_params(3, 2, 6, seed=3)
+    bc = {k: (oracle.f64(v) if hasattr(v, "shape") else v) for k, v in bcp.items()}
+    yfull, hfull, _ = oracle.scan_prep(raw["x"], raw["B"], raw["C"], raw["dt_raw"], raw["dt_bias"], raw["A"],
+                                       raw["u"], raw["omega"], bc=bc)
+    T0 = 27
+    _, h, prev = oracle.scan_prep(raw["x"][:, :T0], raw["B"][:, :T0], raw["C"][:, :T0], raw["dt_raw"][:, :T0],
+                                  raw["dt_bias"], raw["A"][:, :T0], raw["u"][:, :T0], raw["omega"][:, :T0], bc=bc)
+    assert np.array_equal(prev[..., :2 * 6].reshape(raw["B"][:, T0 - 1].shape), raw["B"][:, T0 - 1])
+    for t in range(T0, 36):
+        yt, h, prev = oracle.decode_step_prep(h, raw["x"][:, t], raw["B"][:, t], prev, raw["C"][:, t],
+                                              raw["dt_raw"][:, t], raw["dt_bias"], raw["A"][:, t], raw["u"][:, t],
+                                              raw["omega"][:, t], bc=bc)
+        assert oracle.rel_err(yt, yfull[:, t]) < 1e-13
+    assert oracle.rel_err(h, hfull) < 1e-13
+
+
+BC_PINS = [test_bc_prep_closed_form, test_bc_norm_rows_have_unit_rms, test_bc_norm_scale_invariance,
+           test_bc_bias_enters_the_readout_linearly, test_bc_gain_scales_the_readout]
+
+
+def _mut_axis(V, norm=False, eps=0.0, gain=None, bias=None):
+    V = oracle.f64(V)
+    if norm:
+        V = V / np.sqrt(np.mean(V * V, axis=-2, keepdims=True) + eps)   # over the ranks, not N
+        if gain is not None:
+            V = V * oracle.f64(gain)
+    return V if bias is None else V + oracle.f64(bias)
+
+
+def _mut_bias_first(V, norm=False, eps=0.0, gain=None, bias=None):
+    V = oracle.f64(V)
+    if bias is not None:
+        V = V + oracle.f64(bias)
+    if norm:
+        V = V / np.sqrt(np.mean(V * V, axis=-1, keepdims=True) + eps)
+        if gain is not None:
+            V = V * oracle.f64(gain)
+    return V
+
+
+def _mut_gain_after_bias(V, norm=False, eps=0.0, gain=None, bias=None):
+    V = oracle.f64(V)
+    if norm:
+        V = V / np.sqrt(np.mean(V * V, axis=-1, keepdims=True) + eps)
+    if bias is not None:
+        V = V + oracle.f64(bias)
+    if norm and gain is not None:
+        V = V * oracle.f64(gain)
+    return V
+
+
+def _mut_no_eps(V, norm=False, eps=0.0, gain=None, bias=None):
+    V = oracle.f64(V)
+    if norm:
+        V = V / np.sqrt(np.mean(V * V, axis=-1, keepdims=True))
+        if gain is not None:
+            V = V * oracle.f64(gain)
+    return V if bias is None else V + oracle.f64(bias)
+
+
+@pytest.mark.parametrize("mutant", [_mut_axis, _mut_bias_first, _mut_gain_after_bias, _mut_no_eps])
+def test_bc_mutants_fail_a_pin(mutant, monkeypatch):
+    monkeypatch.setattr(oracle, "bc_prep", mutant)
+    failed = 0
+    for pin in BC_PINS:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed > 0
