@@ -252,7 +252,7 @@ def time_prefill(binding, w, d, stream, steps, warmup, dist, device):
     return sec, per, (y, fin)
 
 
-PREP_KEYS = ("x", "B", "C", "dt_raw", "dt_bias", "A", "u", "omega")
+PREP_KEYS = ("x", "B", "C", "dt_raw", "A", "u", "omega")
 
 
 def time_prefill_prep(binding, w, dp, stream, steps, warmup, dist, device):
@@ -261,9 +261,10 @@ def time_prefill_prep(binding, w, dp, stream, steps, warmup, dist, device):
     fin = torch.empty((w.batch, w.heads, w.dstate, w.headdim), dtype=torch.float32, device=device)
     ws = binding.alloc_workspace_prep(dp["x"].shape, w.dstate, w.rank, w.chunk, dp["x"].dtype, device)
     args = [dp[k] for k in PREP_KEYS]
+    params = binding.prep_params(dp["dt_bias"])
 
     def call():
-        st = binding.m3_scan_fwd_prep(*args, w.rank, w.chunk, y, fin, ws, stream)
+        st = binding.m3_scan_fwd_prep(*args, w.rank, w.chunk, y, fin, ws, params, stream)
         if st != 0:
             raise binding.M3Error(st, "m3_scan_fwd_prep")
 
@@ -581,7 +582,8 @@ def main():
     if not args.no_prep:
         # the same workload through m3_scan_fwd_prep: Delta, lambda from pre-activations and one
         # decay generator per token, derived inside the kernels
-        dp = {k: v for k, v in synth.make_prep_inputs(w, seed=rank, device=device).items() if k in PREP_KEYS}
+        dp = {k: v for k, v in synth.make_prep_inputs(w, seed=rank, device=device).items()
+              if k in PREP_KEYS or k == "dt_bias"}
         psec, pper = time_prefill_prep(binding, w, dp, stream, args.steps, args.warmup, dist, device)
         pms = sum(pper) / len(pper)
         pbytes = prefill_prep_bytes(w)

@@ -181,6 +181,30 @@ M3_API int m3_decode_step(float* state, const void* x_t, const void* B_t, void* 
                    int io_dtype, void* stream);
 
 /*
+ * Pre-SSM options of the _prep entry points.  All pointers are device
+ * pointers, nullable, 16-byte aligned; a NULL params pointer means all off.
+ *
+ *   dt_bias  [H] fp32: Delta_t = softplus(dt_raw_t + dt_bias[h]) (NULL = 0)
+ *   bc_norm  nonzero: every (token, rank) row v of B and of C is RMS-normalised
+ *            over the N channels, v / sqrt(mean(v^2) + bc_eps) * gain, before
+ *            the rotation (the BC normalisation of section 3.4)
+ *   bc_eps   >= 0, added to the mean square
+ *   B_gain, C_gain  [N] fp32 per-channel gains of the normalisation (NULL = 1;
+ *            unused without bc_norm)
+ *   B_bias, C_bias  [H, R, N] fp32 head-specific channel biases added after the
+ *            normalisation (or to the raw rows without it) (NULL = 0)
+ */
+typedef struct m3_prep_params {
+    const float* dt_bias;
+    int bc_norm;
+    float bc_eps;
+    const float* B_gain;
+    const float* C_gain;
+    const float* B_bias;
+    const float* C_bias;
+} m3_prep_params;
+
+/*
  * Per-token parameters from their pre-activations.  The time-varying
  * discretizations of Table 1 ("Mamba-3: Improved Sequence Modeling using
  * State Space Principles") take a decay generator per token, alpha_t =
@@ -190,30 +214,34 @@ M3_API int m3_decode_step(float* state, const void* x_t, const void* B_t, void* 
  *   dt_raw   [batch, T, H] fp32: Delta_t = softplus(dt_raw_t + dt_bias[h])
  *            (softplus(z) = log(1 + e^z); the pages leave Delta's
  *            parameterisation open, this is the Mamba family's)
- *   dt_bias  [H] fp32, nullable (= 0)
  *   A        [batch, T, H] fp32: A_t <= 0, one per token
  *   u        [batch, T, H] fp32: lambda_t = sigmoid(u_t) = 1 / (1 + e^-u_t)
+ *   params   the options above (dt_bias, B / C normalisation and biases)
  *
  * and otherwise behave exactly as m3_scan_fwd / m3_decode_step (same
- * layouts, sizes, errors and stream semantics).  The tensor-core prefill and
- * the decode kernels apply softplus and sigmoid to the staged values inside
- * the kernel; the CUDA-core prefill writes Delta and lambda of every token to
- * the workspace first.  Workspace: m3_scan_fwd_prep_workspace_size bytes
- * (at least m3_scan_fwd_workspace_size; larger on the CUDA-core path).
+ * layouts, sizes, errors and stream semantics).  The delayed-write cache of
+ * the decode step keeps the raw B_{t-1}, X_{t-1}; both B_t and B_{t-1} are
+ * normalised and biased inside the step.  The tensor-core prefill and the
+ * decode kernels apply softplus, sigmoid, the normalisation and the biases to
+ * the staged values inside the kernel; the CUDA-core prefill first writes
+ * Delta, lambda and the inverse RMS of every B / C row to the workspace.
+ * Workspace: m3_scan_fwd_prep_workspace_size bytes (at least
+ * m3_scan_fwd_workspace_size; larger on the CUDA-core path).  Errors: as
+ * m3_scan_fwd, and M3_ERR_INVALID_ARG for a misaligned params pointer or
+ * bc_eps < 0.
  */
 M3_API size_t m3_scan_fwd_prep_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                                               int64_t dstate, int R, int chunk, int io_dtype);
-M3_API int m3_scan_fwd_prep(const void* x, const void* B, const void* C, const float* dt_raw,
-                            const float* dt_bias, const float* A, const float* u, const float* omega, int R,
-                            int chunk, void* y, float* final_state,
+M3_API int m3_scan_fwd_prep(const void* x, const void* B, const void* C, const float* dt_raw, const float* A,
+                            const float* u, const float* omega, int R, int chunk, void* y, float* final_state,
                             int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
-                            int io_dtype, void* workspace, size_t workspace_bytes, void* stream);
-/* Decode on pre-activations: dt_raw_t, A_t, u_t [batch, H] fp32; dt_bias [H] or NULL. */
+                            int io_dtype, const m3_prep_params* params, void* workspace, size_t workspace_bytes,
+                            void* stream);
+/* Decode on pre-activations: dt_raw_t, A_t, u_t [batch, H] fp32. */
 M3_API int m3_decode_step_prep(float* state, const void* x_t, const void* B_t, void* B_prev_x_prev,
-                               const void* C_t, const float* dt_raw_t, const float* dt_bias, const float* A_t,
-                               const float* u_t, const float* omega_t, void* y_t,
-                               int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R,
-                               int io_dtype, void* stream);
+                               const void* C_t, const float* dt_raw_t, const float* A_t, const float* u_t,
+                               const float* omega_t, void* y_t, int64_t batch, int64_t nheads, int64_t headdim,
+                               int64_t dstate, int R, int io_dtype, const m3_prep_params* params, void* stream);
 
 /*
  * Sticky device-side error word of m3_decode_step, which takes no workspace:

@@ -30,6 +30,13 @@ M3_ERR_TIMEOUT = -5
 M3_DTYPE_BF16 = 0
 M3_DTYPE_F32 = 1
 
+class PrepParams(ctypes.Structure):
+    """m3_prep_params: pre-SSM options of the _prep entry points (device pointers or NULL)."""
+    _fields_ = [("dt_bias", ctypes.c_void_p), ("bc_norm", ctypes.c_int), ("bc_eps", ctypes.c_float),
+                ("B_gain", ctypes.c_void_p), ("C_gain", ctypes.c_void_p), ("B_bias", ctypes.c_void_p),
+                ("C_bias", ctypes.c_void_p)]
+
+
 # Every symbol include/m3.h declares, with its ctypes signature.
 _vp, _fp = ctypes.c_void_p, ctypes.c_void_p
 _i64, _int, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
@@ -47,10 +54,10 @@ SIGNATURES = {
                         _i64, _i64, _i64, _i64, _int, _int, _vp], _int),
     "m3_device_status": ([_int], _int),
     "m3_scan_fwd_prep_workspace_size": ([_i64, _i64, _i64, _i64, _i64, _int, _int, _int], _sz),
-    "m3_scan_fwd_prep": ([_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _int, _int, _vp, _fp,
-                          _i64, _i64, _i64, _i64, _i64, _int, _vp, _sz, _vp], _int),
-    "m3_decode_step_prep": ([_fp, _vp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp,
-                             _i64, _i64, _i64, _i64, _int, _int, _vp], _int),
+    "m3_scan_fwd_prep": ([_vp, _vp, _vp, _fp, _fp, _fp, _fp, _int, _int, _vp, _fp,
+                          _i64, _i64, _i64, _i64, _i64, _int, ctypes.POINTER(PrepParams), _vp, _sz, _vp], _int),
+    "m3_decode_step_prep": ([_fp, _vp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp,
+                             _i64, _i64, _i64, _i64, _int, _int, ctypes.POINTER(PrepParams), _vp], _int),
     "m3_state_passing": ([_fp, _fp, _fp, _fp, _fp, _i64, _i64, _i64, _i64, _i64, _vp], _int),
 }
 
@@ -172,21 +179,31 @@ def m3_scan_fwd_prep_workspace_size(batch, seqlen, nheads, headdim, dstate, R, c
     return int(load().m3_scan_fwd_prep_workspace_size(batch, seqlen, nheads, headdim, dstate, R, chunk, io))
 
 
-def m3_scan_fwd_prep(x, B, C, dt_raw, dt_bias, A, u, omega, R: int, chunk: int, y, final_state, workspace,
+def prep_params(dt_bias=None, bc=None):
+    """PrepParams from device tensors: dt_bias [H]; bc = dict(norm, eps, B_gain, C_gain,
+    B_bias, C_bias), tensors [N] / [H, R, N] or absent."""
+    bc = bc or {}
+    return PrepParams(_ptr(dt_bias, torch.float32), 1 if bc.get("norm") else 0, float(bc.get("eps", 0.0)),
+                      _ptr(bc.get("B_gain"), torch.float32), _ptr(bc.get("C_gain"), torch.float32),
+                      _ptr(bc.get("B_bias"), torch.float32), _ptr(bc.get("C_bias"), torch.float32))
+
+
+def m3_scan_fwd_prep(x, B, C, dt_raw, A, u, omega, R: int, chunk: int, y, final_state, workspace, params=None,
                      stream=None) -> int:
-    """Call m3_scan_fwd_prep (pre-activations, A per token); returns the status code."""
+    """Call m3_scan_fwd_prep (pre-activations, A per token; ``params``: PrepParams or None);
+    returns the status code."""
     Bt, T, H, R_, P = x.shape
     N = B.shape[-1]
     io = io_code(x.dtype)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return int(load().m3_scan_fwd_prep(
-        _ptr(x, x.dtype), _ptr(B, x.dtype), _ptr(C, x.dtype), _ptr(dt_raw, torch.float32),
-        _ptr(dt_bias, torch.float32), _ptr(A, torch.float32), _ptr(u, torch.float32), _ptr(omega, torch.float32),
-        int(R), int(chunk), _ptr(y, x.dtype), _ptr(final_state, torch.float32), Bt, T, H, P, N, io,
+        _ptr(x, x.dtype), _ptr(B, x.dtype), _ptr(C, x.dtype), _ptr(dt_raw, torch.float32), _ptr(A, torch.float32),
+        _ptr(u, torch.float32), _ptr(omega, torch.float32), int(R), int(chunk), _ptr(y, x.dtype),
+        _ptr(final_state, torch.float32), Bt, T, H, P, N, io, None if params is None else ctypes.byref(params),
         _ptr(workspace), ws_bytes, _stream(stream)))
 
 
-def m3_decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, dt_bias, A_t, u_t, omega_t, y_t, R: int,
+def m3_decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, A_t, u_t, omega_t, y_t, R: int, params=None,
                         stream=None) -> int:
     """Call m3_decode_step_prep (pre-activations, A per (batch, head)); returns the status code."""
     b, H, R_, P = x_t.shape
@@ -194,9 +211,9 @@ def m3_decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, dt_bias, A_t, u_t
     io = io_code(x_t.dtype)
     return int(load().m3_decode_step_prep(
         _ptr(state, torch.float32), _ptr(x_t, x_t.dtype), _ptr(B_t, x_t.dtype), _ptr(cache, x_t.dtype),
-        _ptr(C_t, x_t.dtype), _ptr(dt_raw_t, torch.float32), _ptr(dt_bias, torch.float32), _ptr(A_t, torch.float32),
-        _ptr(u_t, torch.float32), _ptr(omega_t, torch.float32), _ptr(y_t, x_t.dtype), b, H, P, N, int(R), io,
-        _stream(stream)))
+        _ptr(C_t, x_t.dtype), _ptr(dt_raw_t, torch.float32), _ptr(A_t, torch.float32), _ptr(u_t, torch.float32),
+        _ptr(omega_t, torch.float32), _ptr(y_t, x_t.dtype), b, H, P, N, int(R), io,
+        None if params is None else ctypes.byref(params), _stream(stream)))
 
 
 def m3_device_status(clear: bool = False) -> int:
@@ -230,27 +247,29 @@ def alloc_workspace_prep(x_shape, N: int, R: int, chunk: int, dtype: torch.dtype
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
-def scan_fwd_prep(x, B, C, dt_raw, dt_bias, A, u, omega, R: int, chunk: int, want_final: bool = True,
+def scan_fwd_prep(x, B, C, dt_raw, A, u, omega, R: int, chunk: int, dt_bias=None, bc=None, want_final: bool = True,
                   workspace=None, stream=None):
     """Prefill on pre-activations (Delta = softplus(dt_raw + dt_bias), lambda = sigmoid(u), A per
-    token); returns (y, final_state or None)."""
+    token; ``bc``: B / C normalisation and biases, see prep_params); returns (y, final_state or None)."""
     Bt, T, H, _, P = x.shape
     N = B.shape[-1]
     y = torch.empty_like(x)
     fin = torch.empty((Bt, H, N, P), dtype=torch.float32, device=x.device) if want_final else None
     if workspace is None:
         workspace = alloc_workspace_prep(x.shape, N, R, chunk, x.dtype, x.device)
-    _check(m3_scan_fwd_prep(x, B, C, dt_raw, dt_bias, A, u, omega, R, chunk, y, fin, workspace, stream),
+    params = prep_params(dt_bias, bc)
+    _check(m3_scan_fwd_prep(x, B, C, dt_raw, A, u, omega, R, chunk, y, fin, workspace, params, stream),
            "m3_scan_fwd_prep")
     return y, fin
 
 
-def decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, dt_bias, A_t, u_t, omega_t, R: int, y_t=None,
-                     stream=None):
-    """One decode token on pre-activations, in place on ``state`` and ``cache``; returns y_t."""
+def decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, A_t, u_t, omega_t, R: int, dt_bias=None, bc=None,
+                     y_t=None, stream=None):
+    """One decode token on pre-activations, in place on ``state`` and ``cache`` (raw B, X); returns y_t."""
     if y_t is None:
         y_t = torch.empty_like(x_t)
-    _check(m3_decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, dt_bias, A_t, u_t, omega_t, y_t, R, stream),
+    params = prep_params(dt_bias, bc)
+    _check(m3_decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, A_t, u_t, omega_t, y_t, R, params, stream),
            "m3_decode_step_prep")
     return y_t
 

@@ -43,6 +43,28 @@ size_t scan_workspace(const m3::ScanDims& d, bool prep) {
     return pick_path(d) == 1 ? m3::tc_workspace_size(d) : m3::simt_workspace_size(d, prep);
 }
 
+// The pre-SSM options of a _prep call (NULL params: all off); false for
+// misaligned pointers or a negative / non-finite bc_eps.
+bool prep_from(const m3_prep_params* p, m3::Prep* out) {
+    m3::Prep q{};
+    q.on = true;
+    if (p != nullptr) {
+        if (!ok_nullable(p->dt_bias) || !ok_nullable(p->B_gain) || !ok_nullable(p->C_gain) ||
+            !ok_nullable(p->B_bias) || !ok_nullable(p->C_bias))
+            return false;
+        if (!(p->bc_eps >= 0.f) || p->bc_eps > 3.0e38f) return false;
+        q.dt_bias = p->dt_bias;
+        q.bc_norm = p->bc_norm != 0;
+        q.bc_eps = p->bc_eps;
+        q.B_gain = p->B_gain;
+        q.C_gain = p->C_gain;
+        q.B_bias = p->B_bias;
+        q.C_bias = p->C_bias;
+    }
+    *out = q;
+    return true;
+}
+
 int scan_impl(const void* x, const void* B, const void* C, const float* dt, const float* A, const float* lambda,
               const float* omega, int R, int chunk, void* y, float* final_state, int64_t batch, int64_t seqlen,
               int64_t nheads, int64_t headdim, int64_t dstate, int io_dtype, void* workspace,
@@ -138,15 +160,17 @@ int m3_scan_fwd(const void* x, const void* B, const void* C, const float* dt, co
                 int64_t nheads, int64_t headdim, int64_t dstate, int io_dtype, void* workspace,
                 size_t workspace_bytes, void* stream) {
     return scan_impl(x, B, C, dt, A, lambda, omega, R, chunk, y, final_state, batch, seqlen, nheads, headdim, dstate,
-                     io_dtype, workspace, workspace_bytes, stream, m3::Prep{false, nullptr});
+                     io_dtype, workspace, workspace_bytes, stream, m3::Prep{});
 }
 
-int m3_scan_fwd_prep(const void* x, const void* B, const void* C, const float* dt_raw, const float* dt_bias,
-                     const float* A, const float* u, const float* omega, int R, int chunk, void* y,
-                     float* final_state, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
-                     int64_t dstate, int io_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+int m3_scan_fwd_prep(const void* x, const void* B, const void* C, const float* dt_raw, const float* A,
+                     const float* u, const float* omega, int R, int chunk, void* y, float* final_state,
+                     int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate, int io_dtype,
+                     const m3_prep_params* params, void* workspace, size_t workspace_bytes, void* stream) {
+    m3::Prep prep;
+    if (!prep_from(params, &prep)) return M3_ERR_INVALID_ARG;
     return scan_impl(x, B, C, dt_raw, A, u, omega, R, chunk, y, final_state, batch, seqlen, nheads, headdim, dstate,
-                     io_dtype, workspace, workspace_bytes, stream, m3::Prep{true, dt_bias});
+                     io_dtype, workspace, workspace_bytes, stream, prep);
 }
 
 int m3_decode_step(float* state, const void* x_t, const void* B_t, void* B_prev_x_prev, const void* C_t,
@@ -154,15 +178,17 @@ int m3_decode_step(float* state, const void* x_t, const void* B_t, void* B_prev_
                    int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R, int io_dtype,
                    void* stream) {
     return decode_impl(state, x_t, B_t, B_prev_x_prev, C_t, dt_t, A, lambda_t, omega_t, y_t, batch, nheads, headdim,
-                       dstate, R, io_dtype, stream, m3::Prep{false, nullptr});
+                       dstate, R, io_dtype, stream, m3::Prep{});
 }
 
 int m3_decode_step_prep(float* state, const void* x_t, const void* B_t, void* B_prev_x_prev, const void* C_t,
-                        const float* dt_raw_t, const float* dt_bias, const float* A_t, const float* u_t,
-                        const float* omega_t, void* y_t, int64_t batch, int64_t nheads, int64_t headdim,
-                        int64_t dstate, int R, int io_dtype, void* stream) {
+                        const float* dt_raw_t, const float* A_t, const float* u_t, const float* omega_t, void* y_t,
+                        int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int R, int io_dtype,
+                        const m3_prep_params* params, void* stream) {
+    m3::Prep prep;
+    if (!prep_from(params, &prep)) return M3_ERR_INVALID_ARG;
     return decode_impl(state, x_t, B_t, B_prev_x_prev, C_t, dt_raw_t, A_t, u_t, omega_t, y_t, batch, nheads, headdim,
-                       dstate, R, io_dtype, stream, m3::Prep{true, dt_bias});
+                       dstate, R, io_dtype, stream, prep);
 }
 
 int m3_device_status(int clear) { return m3::decode_device_status(clear); }

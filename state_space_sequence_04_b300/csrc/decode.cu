@@ -64,6 +64,68 @@ __device__ __forceinline__ void unit_params(const float* dt_t, const float* lam_
     }
 }
 
+// The B / C normalisation and channel biases of the pre-activation entry point,
+// in place on the staged rows (float pairs laid out [N/2][R]) of B_t, C_t and
+// the cached B_{t-1}: v / sqrt(mean(v^2) + eps) * gain + bias[h, r, :].
+// Block-wide; the caller synchronises before and after.
+__device__ void bc_rows(float* sB2f, float* sC2f, float* sBp2f, int R, int N, int h, const Prep& p) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int rows = 3 * R;   // B_t, C_t, B_{t-1}
+    auto row_ptrs = [&](int row, float*& base, const float*& g, const float*& bb, int& r) {
+        const int k = row / R;
+        r = row % R;
+        base = k == 0 ? sB2f : (k == 1 ? sC2f : sBp2f);
+        g = k == 1 ? p.C_gain : p.B_gain;
+        bb = k == 1 ? p.C_bias : p.B_bias;
+    };
+    auto at = [&](float* base, int r, int n) { return base + ((n >> 1) * R + r) * 2 + (n & 1); };
+    auto apply = [&](float* base, const float* g, const float* bb, int r, int n0, int step, float sc) {
+        for (int n = n0; n < N; n += step) {
+            float* q = at(base, r, n);
+            float v = *q;
+            if (p.bc_norm) v *= sc * (g != nullptr ? g[n] : 1.f);
+            if (bb != nullptr) v += bb[((int64_t)h * R + r) * N + n];
+            *q = v;
+        }
+    };
+    if ((nt & 31) == 0) {   // one warp per row
+        const int warp = tid >> 5, lane = tid & 31, nw = nt >> 5;
+        for (int row = warp; row < rows; row += nw) {
+            float* base;
+            const float *g, *bb;
+            int r;
+            row_ptrs(row, base, g, bb, r);
+            float sc = 1.f;
+            if (p.bc_norm) {
+                float ss = 0.f;
+                for (int n = lane; n < N; n += 32) {
+                    const float v = *at(base, r, n);
+                    ss = fmaf(v, v, ss);
+                }
+                sc = rsqrtf(warp_sum(ss) / N + p.bc_eps);
+            }
+            apply(base, g, bb, r, lane, 32, sc);
+        }
+    } else {                // small blocks: one thread per row
+        for (int row = tid; row < rows; row += nt) {
+            float* base;
+            const float *g, *bb;
+            int r;
+            row_ptrs(row, base, g, bb, r);
+            float sc = 1.f;
+            if (p.bc_norm) {
+                float ss = 0.f;
+                for (int n = 0; n < N; ++n) {
+                    const float v = *at(base, r, n);
+                    ss = fmaf(v, v, ss);
+                }
+                sc = rsqrtf(ss / N + p.bc_eps);
+            }
+            apply(base, g, bb, r, 0, 1, sc);
+        }
+    }
+}
+
 template <typename IO, int R>
 __global__ void __launch_bounds__(256, DecodeOcc<R>::value) decode_kernel(
     float* __restrict__ state, const IO* __restrict__ x_t, const IO* __restrict__ B_t,
@@ -131,6 +193,10 @@ __global__ void __launch_bounds__(256, DecodeOcc<R>::value) decode_kernel(
         sCS[j] = make_float2(cs, sn);
     }
     __syncthreads();
+    if (prep.bc()) {
+        bc_rows(sB2f, sC2f, sBp2f, R, N, (int)(bh % H), prep);
+        __syncthreads();
+    }
     // The old cache is in shared memory now: replace it with this token's factors.
     for (int i = tid; i < R * N; i += nt) cb[i] = Bb[i];
     for (int i = tid; i < R * P; i += nt) cb[R * N + i] = xb[i];
@@ -349,6 +415,10 @@ __global__ void __launch_bounds__(256, 2) decode_stream_kernel(
             sCS[j] = make_float2(cs, sn);
         }
         __syncthreads();
+        if (prep.bc()) {
+            bc_rows(sB2f, sC2f, sBp2f, R, N, (int)(u % H), prep);
+            __syncthreads();
+        }
         // new delayed-write cache: this token's B_t then X_t (raw io values)
         IO* cb = cache + u * (int64_t)R * (N + P);
         for (int i = tid; i < R * N; i += nt) cb[i] = sBt[i];

@@ -54,9 +54,18 @@ namespace m3 {
 // pre-activation of Delta (Delta = softplus(dt + dt_bias[h]), dt_bias nullable),
 // lambda holds u (lambda = sigmoid(u)), and A holds one value per token with
 // dt's layout.
+// With on, B and C may also be RMS-normalised per (token, rank) row over N
+// (bc_norm, bc_eps, gains [N]) and shifted by channel biases [H, R, N].
 struct Prep {
     bool on;
     const float* dt_bias;
+    bool bc_norm;
+    float bc_eps;
+    const float* B_gain;
+    const float* C_gain;
+    const float* B_bias;
+    const float* C_bias;
+    __host__ __device__ bool bc() const { return on && (bc_norm || B_bias != nullptr || C_bias != nullptr); }
 };
 
 struct ScanDims {

@@ -46,13 +46,35 @@ __device__ __forceinline__ float block_scan256(float v, float* sWarp) {
 }
 
 // ---------------------------------------------------------------------------
+// B or C of the pre-activation entry points: RMS normalisation of each
+// (token, rank) row over N (inverse RMS precomputed per row in `inv`), gain [N],
+// head-specific channel bias [H, R, N].  on = 0: the values as given.
+struct BcArgs {
+    int on, norm;
+    const float* inv;
+    const float* gain;
+    const float* bias;
+};
+
+// Element n of the row starting at `base` (= row * N); hr = h * R + r.
+template <typename IO>
+__device__ __forceinline__ float ld_bc(const IO* p, int64_t base, int n, int N, int hr, const BcArgs& a) {
+    float v = ld_io(p, base + n);
+    if (a.on) {
+        if (a.norm) v *= a.inv[base / N] * (a.gain != nullptr ? a.gain[n] : 1.f);
+        if (a.bias != nullptr) v += a.bias[(int64_t)hr * N + n];
+    }
+    return v;
+}
+
+// ---------------------------------------------------------------------------
 // Kernel A: U_c, l_c = cum_end, Theta_c for every (batch*head, chunk).
 template <typename IO, int R>
 __global__ void __launch_bounds__(kThreads) chunk_state_kernel(
     const IO* __restrict__ x, const IO* __restrict__ B, const float* __restrict__ dt,
     const float* __restrict__ A, const float* __restrict__ lam, const float* __restrict__ omega,
     float* __restrict__ U, float* __restrict__ ld_out, float* __restrict__ ang_out,
-    int64_t T, int H, int P, int N, int Q, int nc, int a_tok) {
+    int64_t T, int H, int P, int N, int Q, int nc, int a_tok, const BcArgs bcB) {
     extern __shared__ float sm[];
     constexpr int KB = 32 / R > 0 ? 32 / R : 1;   // tokens per staging block
     const int64_t bh = blockIdx.x;
@@ -114,7 +136,8 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(
                 for (int r = 0; r < R; ++r) {
                     const int64_t base = ((tok * H + h) * R + r) * N;
                     float o0, o1;
-                    rot2(cs, sn, ld_io(B, base + 2 * j), ld_io(B, base + 2 * j + 1), o0, o1);
+                    rot2(cs, sn, ld_bc(B, base, 2 * j, N, h * R + r, bcB), ld_bc(B, base, 2 * j + 1, N, h * R + r, bcB),
+                         o0, o1);
                     sBr[(sl * R + r) * N + 2 * j] = wt * o0;
                     sBr[(sl * R + r) * N + 2 * j + 1] = wt * o1;
                 }
@@ -158,7 +181,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     const IO* __restrict__ x, const IO* __restrict__ B, const IO* __restrict__ C,
     const float* __restrict__ dt, const float* __restrict__ A, const float* __restrict__ lam,
     const float* __restrict__ omega, const float* __restrict__ Hc, IO* __restrict__ y,
-    int64_t T, int H, int P, int N, int Q, int nc, int a_tok) {
+    int64_t T, int H, int P, int N, int Q, int nc, int a_tok, const BcArgs bcB, const BcArgs bcC) {
     extern __shared__ float sm[];
     constexpr int RT = kRowTile;
     constexpr int TT = RT / R;
@@ -223,7 +246,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
             const int64_t base = (((b * T + c0 + t) * H + h) * R + r) * N;
             float sn, cs;
             sincosf(-sPsi[t * NP2 + j], &sn, &cs);
-            rot2(cs, sn, ld_io(C, base + 2 * j), ld_io(C, base + 2 * j + 1), o0, o1);
+            rot2(cs, sn, ld_bc(C, base, 2 * j, N, h * R + r, bcC), ld_bc(C, base, 2 * j + 1, N, h * R + r, bcC), o0, o1);
         }
         sCt[(2 * j) * LD + row] = o0;
         sCt[(2 * j + 1) * LD + row] = o1;
@@ -289,7 +312,8 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
                 const int64_t base = (((b * T + c0 + s) * H + h) * R + r) * N;
                 float sn, cs;
                 sincosf(-sPsi[s * NP2 + j], &sn, &cs);
-                rot2(cs, sn, ld_io(B, base + 2 * j), ld_io(B, base + 2 * j + 1), o0, o1);
+                rot2(cs, sn, ld_bc(B, base, 2 * j, N, h * R + r, bcB), ld_bc(B, base, 2 * j + 1, N, h * R + r, bcB),
+                     o0, o1);
             }
             sBt[(2 * j) * LD + col] = o0;
             sBt[(2 * j + 1) * LD + col] = o1;
@@ -374,7 +398,7 @@ size_t smem_c(const ScanDims& d) {
 template <typename IO, int R>
 cudaError_t launch_rt(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                       const float* A, const float* lambda, const float* omega, void* y, float* final_state,
-                      void* workspace, int a_tok, cudaStream_t stream) {
+                      void* workspace, int a_tok, const BcArgs& bcB, const BcArgs& bcC, cudaStream_t stream) {
     const int64_t bh = d.batch * d.nheads;
     const int64_t nc = d.nchunks();
     const int64_t NP = d.dstate * d.headdim;
@@ -388,7 +412,7 @@ cudaError_t launch_rt(const ScanDims& d, const void* x, const void* B, const voi
         if ((e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa)) != cudaSuccess) return e;
         ka<<<dim3((unsigned)bh, (unsigned)nc), kThreads, sa, stream>>>(
             (const IO*)x, (const IO*)B, dt, A, lambda, omega, U, ld, ang, d.seqlen, (int)d.nheads, (int)d.headdim,
-            (int)d.dstate, d.chunk, (int)nc, a_tok);
+            (int)d.dstate, d.chunk, (int)nc, a_tok, bcB);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if ((e = launch_state_passing(U, ld, ang, nullptr, final_state, d.batch, d.nheads, nc, d.dstate, d.headdim,
@@ -402,7 +426,7 @@ cudaError_t launch_rt(const ScanDims& d, const void* x, const void* B, const voi
         const unsigned tiles = (unsigned)((d.chunk + TT - 1) / TT);
         kc<<<dim3((unsigned)bh, (unsigned)nc, tiles), kThreads, sc, stream>>>(
             (const IO*)x, (const IO*)B, (const IO*)C, dt, A, lambda, omega, U, (IO*)y, d.seqlen, (int)d.nheads,
-            (int)d.headdim, (int)d.dstate, d.chunk, (int)nc, a_tok);
+            (int)d.headdim, (int)d.dstate, d.chunk, (int)nc, a_tok, bcB, bcC);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -411,13 +435,31 @@ cudaError_t launch_rt(const ScanDims& d, const void* x, const void* B, const voi
 template <typename IO>
 cudaError_t launch_io(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                       const float* A, const float* lambda, const float* omega, void* y, float* final_state,
-                      void* workspace, int a_tok, cudaStream_t stream) {
+                      void* workspace, int a_tok, const BcArgs& bcB, const BcArgs& bcC, cudaStream_t stream) {
+#define M3_SIMT_CASE(RR) \
+    case RR: return launch_rt<IO, RR>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, bcB, bcC, stream);
     switch (d.R) {
-        case 1: return launch_rt<IO, 1>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
-        case 2: return launch_rt<IO, 2>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
-        case 4: return launch_rt<IO, 4>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
-        case 8: return launch_rt<IO, 8>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
+        M3_SIMT_CASE(1)
+        M3_SIMT_CASE(2)
+        M3_SIMT_CASE(4)
+        M3_SIMT_CASE(8)
         default: return cudaErrorInvalidValue;
+    }
+#undef M3_SIMT_CASE
+}
+
+// Inverse RMS of every (token, rank) row of V over its N channels: 1 / sqrt(mean(v^2) + eps).
+template <typename IO>
+__global__ void __launch_bounds__(256) row_inv_rms_kernel(const IO* __restrict__ V, float* __restrict__ inv,
+                                                          int64_t rows, int N, float eps) {
+    for (int64_t row = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; row < rows;
+         row += (int64_t)gridDim.x * blockDim.x) {
+        float ss = 0.f;
+        for (int n = 0; n < N; ++n) {
+            const float v = ld_io(V, row * N + n);
+            ss = fmaf(v, v, ss);
+        }
+        inv[row] = rsqrtf(ss / N + eps);
     }
 }
 
@@ -450,33 +492,55 @@ size_t simt_workspace_size(const ScanDims& d, bool prep) {
     const int64_t nc = d.nchunks();
     const size_t base = sizeof(float) * (size_t)(bh * nc * (d.dstate * d.headdim + 1 + d.dstate / 2));
     if (!prep) return base;
+    // Delta, lambda per (batch, token, head); inverse RMS of B and C per (batch, token, head, rank)
     const size_t n = (size_t)(d.batch * d.seqlen * d.nheads);
-    return al256(base) + 2 * al256(n * sizeof(float));
+    return al256(base) + 2 * al256(n * sizeof(float)) + 2 * al256(n * (size_t)d.R * sizeof(float));
 }
 
 cudaError_t launch_scan_simt(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                              const float* A, const float* lambda, const float* omega, void* y,
                              float* final_state, void* workspace, const Prep& prep, cudaStream_t stream) {
+    BcArgs bcB{}, bcC{};
     if (prep.on) {
-        // Delta and lambda of every token into the tail of the workspace, then the same kernels
-        // with one decay generator per token
-        const int64_t n = d.batch * d.seqlen * d.nheads;
+        // Delta, lambda of every token (and the inverse RMS of every B / C row) into the tail of
+        // the workspace, then the same kernels with one decay generator per token
+        const int64_t n = d.batch * d.seqlen * d.nheads, rows = n * d.R;
         uint8_t* tail = static_cast<uint8_t*>(workspace) + al256(simt_workspace_size(d, false));
         float* dt_eff = reinterpret_cast<float*>(tail);
         float* lam_eff = reinterpret_cast<float*>(tail + al256((size_t)n * sizeof(float)));
+        float* invB = reinterpret_cast<float*>(tail + 2 * al256((size_t)n * sizeof(float)));
+        float* invC = reinterpret_cast<float*>(tail + 2 * al256((size_t)n * sizeof(float)) +
+                                               al256((size_t)rows * sizeof(float)));
+        cudaError_t e;
         if (n > 0) {
             const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, 148 * 16);
             prep_kernel<<<blocks, 256, 0, stream>>>(dt, prep.dt_bias, lambda, dt_eff, lam_eff, n, (int)d.nheads);
-            cudaError_t e = cudaGetLastError();
-            if (e != cudaSuccess) return e;
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            if (prep.bc_norm) {
+                const unsigned rb = (unsigned)std::min<int64_t>((rows + 255) / 256, 148 * 16);
+                if (d.io == M3_DTYPE_BF16) {
+                    row_inv_rms_kernel<<<rb, 256, 0, stream>>>((const __nv_bfloat16*)B, invB, rows, (int)d.dstate, prep.bc_eps);
+                    row_inv_rms_kernel<<<rb, 256, 0, stream>>>((const __nv_bfloat16*)C, invC, rows, (int)d.dstate, prep.bc_eps);
+                } else {
+                    row_inv_rms_kernel<<<rb, 256, 0, stream>>>((const float*)B, invB, rows, (int)d.dstate, prep.bc_eps);
+                    row_inv_rms_kernel<<<rb, 256, 0, stream>>>((const float*)C, invC, rows, (int)d.dstate, prep.bc_eps);
+                }
+                if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            }
         }
         dt = dt_eff;
         lambda = lam_eff;
+        if (prep.bc()) {
+            const int norm = prep.bc_norm ? 1 : 0;
+            bcB = BcArgs{1, norm, invB, prep.B_gain, prep.B_bias};
+            bcC = BcArgs{1, norm, invC, prep.C_gain, prep.C_bias};
+        }
     }
     const int a_tok = prep.on ? 1 : 0;
     if (d.io == M3_DTYPE_BF16)
-        return launch_io<__nv_bfloat16>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
-    return launch_io<float>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, stream);
+        return launch_io<__nv_bfloat16>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, bcB, bcC,
+                                        stream);
+    return launch_io<float>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, bcB, bcC, stream);
 }
 
 }  // namespace m3

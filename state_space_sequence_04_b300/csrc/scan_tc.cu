@@ -126,6 +126,14 @@ struct Cfg {
 struct TcArgs {
     const float* A;          // [H], or [Bt,T,H] (one per token) in the pre-activation variant
     const float* dt_bias;    // pre-activation variant: [H] or null
+    // pre-activation variant with the B / C normalisation: per-channel gains [N] (null = 1),
+    // channel biases [H, R, N] (null = 0), RMS normalisation on / off and its eps
+    const float* B_gain;
+    const float* C_gain;
+    const float* B_bias;
+    const float* C_bias;
+    int bc_norm;
+    float bc_eps;
     const float* omega;
     __nv_bfloat16* y;
     float* final_state;
@@ -203,6 +211,61 @@ __device__ __forceinline__ uint4 rotate4(uint4 v, const float2 (&c01)[2], const 
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// The B / C normalisation of the pre-activation variant fused with the rotation:
+// the 8 channels of this 16-byte piece (4 pairs) of a row get
+// v / sqrt(mean(v^2) + eps) * g + bias (the mean over the row's N channels,
+// reduced over the NG lanes that hold the row: lanes differing in their low
+// log2(NG) bits) or, without the norm, v + bias; then the pairs are rotated as
+// in rotate4.  Warp-uniform: every lane of the warp calls it together.
+template <int NG>
+__device__ __forceinline__ uint4 bc_rotate4(uint4 v, const float2 (&c01)[2], const float2 (&s01)[2],
+                                            const float (&g)[8], const float (&bb)[8], bool norm, float eps,
+                                            float inv_n) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float e[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        e[2 * q] = bf_lo(w[q]);
+        e[2 * q + 1] = bf_hi(w[q]);
+    }
+    if (norm) {
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(e[i], e[i], ss);
+#pragma unroll
+        for (int o = 1; o < NG; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float sc = rsqrtf(fmaf(ss, inv_n, eps));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e[i] = fmaf(e[i] * sc, g[i], bb[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e[i] += bb[i];
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float2 a = make_float2(e[4 * h], e[4 * h + 2]);
+        const float2 b = make_float2(e[4 * h + 1], e[4 * h + 3]);
+        const float2 na = __ffma2_rn(c01[h], a, __fmul2_rn(make_float2(-s01[h].x, -s01[h].y), b));
+        const float2 nb = __ffma2_rn(s01[h], a, __fmul2_rn(c01[h], b));
+        w[2 * h] = pack_bf16(na.x, nb.x);
+        w[2 * h + 1] = pack_bf16(na.y, nb.y);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// 8 consecutive floats from p (16-byte aligned), or `fill` when p is null.
+__device__ __forceinline__ void load8(const float* p, float fill, float (&o)[8]) {
+    if (p == nullptr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = fill;
+        return;
+    }
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
 // Mask one 16-column block of a score row held in v[0..15]: columns cb..cb+15
 // (tokens cb/R ..), row token t.  Blocks strictly below the diagonal use the
 // factorised decay 2^(cum2_t - cum2_e) 2^(cum2_e - cum2_s), e = the block's last
@@ -242,16 +305,18 @@ __device__ __forceinline__ void mask_block(float* v, int cb, int t, float ct, fl
 // segmented prefill -- only the carry (rotated, scaled B, scaled X and the
 // chunk-state MMA), whose value at the segment's end from a zero start, summed
 // log-decay and summed angles go to the workspace for the segment scan.
-// PREP = true: the dt and lambda inputs are pre-activations (Delta =
-// softplus(dt + dt_bias[h]), lambda = sigmoid(u), applied to the staged boxes in
-// shared memory) and A holds one decay generator per token.
-template <int NS, int R, int Q, bool FULL, bool PREP>
+// PM >= 1 (pre-activation variant): the dt and lambda inputs are pre-activations
+// (Delta = softplus(dt + dt_bias[h]), lambda = sigmoid(u), applied to the staged
+// boxes in shared memory) and A holds one decay generator per token.  PM = 2
+// adds the B / C normalisation and channel biases, fused with the rotation.
+template <int NS, int R, int Q, bool FULL, int PM>
 __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                          const __grid_constant__ CUtensorMap tm_B,
                                                          const __grid_constant__ CUtensorMap tm_C,
                                                          const __grid_constant__ CUtensorMap tm_dt,
                                                          const __grid_constant__ CUtensorMap tm_lam, TcArgs args) {
     using K = Cfg<NS, R, Q>;
+    constexpr bool PREP = PM >= 1, BC = PM == 2;
     constexpr int P = K::P, QR = K::QR, NP2 = NS / 2, NG = K::NG, TG = K::TG, TPG = K::TPG;
     constexpr int TX_CB = FULL ? 2 * K::BC_BYTES : K::BC_BYTES;
     extern __shared__ uint8_t smem_raw[];
@@ -692,6 +757,15 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             return rt < Q && t < T ? args.A[((int64_t)b * T + t) * args.H + h] : 0.f;
         };
         if (PREP) a_nx = load_a(c_begin);
+        // B / C normalisation: this thread's 8 channels' gains, and with one rank its head's biases
+        float gB[8], gC[8], bB1[8], bC1[8];
+        const bool bc_norm = BC && args.bc_norm != 0;
+        if constexpr (BC) {
+            load8(args.B_gain ? args.B_gain + 8 * jg : nullptr, 1.f, gB);
+            load8(FULL && args.C_gain ? args.C_gain + 8 * jg : nullptr, 1.f, gC);
+            load8(R == 1 && args.B_bias ? args.B_bias + (int64_t)h * NS + 8 * jg : nullptr, 0.f, bB1);
+            load8(R == 1 && FULL && args.C_bias ? args.C_bias + (int64_t)h * NS + 8 * jg : nullptr, 0.f, bC1);
+        }
         for (int i = 0; i < nl; ++i) {
             const int c = c_begin + i, s = i & 1;
             (void)wait_bounded(&ctl->fbox[s], (i >> 1) & 1, fail_r, fail_c);
@@ -808,12 +882,35 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const uint32_t off2 = pan * QR * 128 + sw128_offset(t * R + r, cib);
-                        if (FULL) {
-                            uint4* pc = reinterpret_cast<uint4*>(tC + off2);
-                            *pc = rotate4(*pc, c01, s01);
+                        if constexpr (BC) {
+                            // normalise and bias the row, then rotate (B' also scaled by w)
+                            float bbB[8], bbC[8];
+                            if (R == 1) {
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    bbB[q] = bB1[q];
+                                    bbC[q] = bC1[q];
+                                }
+                            } else {
+                                load8(args.B_bias ? args.B_bias + ((int64_t)h * R + r) * NS + 8 * jg : nullptr, 0.f, bbB);
+                                if (FULL)
+                                    load8(args.C_bias ? args.C_bias + ((int64_t)h * R + r) * NS + 8 * jg : nullptr, 0.f,
+                                          bbC);
+                            }
+                            if (FULL) {
+                                uint4* pc = reinterpret_cast<uint4*>(tC + off2);
+                                *pc = bc_rotate4<NG>(*pc, c01, s01, gC, bbC, bc_norm, args.bc_eps, 1.f / NS);
+                            }
+                            uint4* pb = reinterpret_cast<uint4*>(tB + off2);
+                            *pb = bc_rotate4<NG>(*pb, cw01, sw01, gB, bbB, bc_norm, args.bc_eps, 1.f / NS);
+                        } else {
+                            if (FULL) {
+                                uint4* pc = reinterpret_cast<uint4*>(tC + off2);
+                                *pc = rotate4(*pc, c01, s01);
+                            }
+                            uint4* pb = reinterpret_cast<uint4*>(tB + off2);
+                            *pb = rotate4(*pb, cw01, sw01);
                         }
-                        uint4* pb = reinterpret_cast<uint4*>(tB + off2);
-                        *pb = rotate4(*pb, cw01, sw01);
                     }
                 }
                 if (tg == TG - 1) *reinterpret_cast<float4*>(&co[K::CO_THETA + 4 * jg]) = psi;
@@ -936,10 +1033,10 @@ SegWs seg_ws(const ScanDims& d) {
     return w;
 }
 
-template <int NS, int R, int Q, bool PREP>
+template <int NS, int R, int Q, int PM>
 cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                        const float* A, const float* lambda, const float* omega, void* y, float* final_state,
-                       void* workspace, const float* dt_bias, cudaStream_t stream) {
+                       void* workspace, const Prep& prep, cudaStream_t stream) {
     using K = Cfg<NS, R, Q>;
     const cuuint64_t Bt = d.batch, T = d.seqlen, H = d.nheads, P = d.headdim, N = d.dstate;
     CUtensorMap mx, mB, mC, mdt, mlam;
@@ -974,7 +1071,13 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
     const int64_t seqs = d.batch * d.nheads;
     TcArgs args{};
     args.A = A;
-    args.dt_bias = dt_bias;
+    args.dt_bias = prep.dt_bias;
+    args.B_gain = prep.B_gain;
+    args.C_gain = prep.C_gain;
+    args.B_bias = prep.B_bias;
+    args.C_bias = prep.C_bias;
+    args.bc_norm = prep.bc_norm ? 1 : 0;
+    args.bc_eps = prep.bc_eps;
     args.omega = omega;
     args.y = static_cast<__nv_bfloat16*>(y);
     args.final_state = final_state;
@@ -996,7 +1099,7 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
         a1.seg_U = segU;
         a1.seg_ld = segLD;
         a1.seg_th = segTH;
-        auto k1 = scan_tc_kernel<NS, R, Q, false, PREP>;
+        auto k1 = scan_tc_kernel<NS, R, Q, false, PM>;
         e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
         if (e != cudaSuccess) return e;
         k1<<<(unsigned)(seqs * a1.nseg), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, a1);
@@ -1008,7 +1111,7 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
         args.h_in_last = last;
     }
     args.nseg = pl.S;
-    auto kern = scan_tc_kernel<NS, R, Q, true, PREP>;
+    auto kern = scan_tc_kernel<NS, R, Q, true, PM>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)(seqs * pl.S), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, args);
@@ -1021,17 +1124,17 @@ template <int NS, int R, int Q>
 int launches_cfg(const ScanDims& d) { return seg_plan<NS, R, Q>(d).S > 1 ? 3 : 1; }
 
 typedef cudaError_t (*LaunchFn)(const ScanDims&, const void*, const void*, const void*, const float*, const float*,
-                                const float*, const float*, void*, float*, void*, const float*, cudaStream_t);
+                                const float*, const float*, void*, float*, void*, const Prep&, cudaStream_t);
 struct TcImpl {
-    LaunchFn launch;        // dt, lambda, A[H] as given
-    LaunchFn launch_prep;   // pre-activations, A per token
+    LaunchFn launch[3];     // dt, lambda, A[H] as given | pre-activations, A per token | the same + B / C norm
     size_t (*workspace)(const ScanDims&);
     int (*launches)(const ScanDims&);
 };
 
 template <int NS, int R, int Q>
 TcImpl impl() {
-    return TcImpl{launch_cfg<NS, R, Q, false>, launch_cfg<NS, R, Q, true>, ws_cfg<NS, R, Q>, launches_cfg<NS, R, Q>};
+    return TcImpl{{launch_cfg<NS, R, Q, 0>, launch_cfg<NS, R, Q, 1>, launch_cfg<NS, R, Q, 2>}, ws_cfg<NS, R, Q>,
+                  launches_cfg<NS, R, Q>};
 }
 
 // Tile configuration for (N, R, chunk).  Chunks of chunk*R <= 128 rows run as
@@ -1072,8 +1175,8 @@ cudaError_t launch_scan_tc(const ScanDims& d, const void* x, const void* B, cons
                            void* workspace, const Prep& prep, cudaStream_t stream) {
     TcImpl f;
     if (!pick(d, &f)) return cudaErrorNotSupported;
-    return (prep.on ? f.launch_prep : f.launch)(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace,
-                                                prep.dt_bias, stream);
+    const int mode = !prep.on ? 0 : (prep.bc() ? 2 : 1);
+    return f.launch[mode](d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, prep, stream);
 }
 
 }  // namespace m3
