@@ -255,13 +255,14 @@ def time_prefill(binding, w, d, stream, steps, warmup, dist, device):
 PREP_KEYS = ("x", "B", "C", "dt_raw", "A", "u", "omega")
 
 
-def time_prefill_prep(binding, w, dp, stream, steps, warmup, dist, device):
-    """The same over m3_scan_fwd_prep (pre-activations, one decay generator per token)."""
+def time_prefill_prep(binding, w, dp, stream, steps, warmup, dist, device, bc=None):
+    """The same over m3_scan_fwd_prep (pre-activations, one decay generator per token; ``bc``:
+    the B / C normalisation and channel biases, device tensors)."""
     y = torch.empty_like(dp["x"])
     fin = torch.empty((w.batch, w.heads, w.dstate, w.headdim), dtype=torch.float32, device=device)
     ws = binding.alloc_workspace_prep(dp["x"].shape, w.dstate, w.rank, w.chunk, dp["x"].dtype, device)
     args = [dp[k] for k in PREP_KEYS]
-    params = binding.prep_params(dp["dt_bias"])
+    params = binding.prep_params(dp["dt_bias"], bc)
 
     def call():
         st = binding.m3_scan_fwd_prep(*args, w.rank, w.chunk, y, fin, ws, params, stream)
@@ -594,7 +595,15 @@ def main():
                          "unit": "GB/s", "frac": pbytes / (pms * 1e-3) / 1e9 / pk["hbm_gbs"]},
             # the CUDA-core path derives Delta and lambda in one extra elementwise launch
             "gpu_launches": (launches + (1 if path == 0 else 0)) * args.steps}
-        del dp
+        # and with the B / C RMS normalisation, gains and head-specific channel biases
+        bc = {k: (v.to(device) if hasattr(v, "shape") else v)
+              for k, v in synth.make_bc_params(w.heads, w.rank, w.dstate).items()}
+        bsec, bper = time_prefill_prep(binding, w, dp, stream, args.steps, args.warmup, dist, device, bc=bc)
+        bms = sum(bper) / len(bper)
+        line["prefill_prep"]["with_bc_norm"] = {
+            "value": tokens * args.steps / bsec / 1e6, "unit": "Mtok/s", "ms_per_step": bsec / args.steps * 1e3,
+            "roofline_frac": pbytes / (bms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+        del dp, bc
 
     if not args.no_e2e:
         host = {k: d[k].to("cpu").pin_memory() for k in KEYS}

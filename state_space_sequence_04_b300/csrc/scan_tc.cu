@@ -126,14 +126,6 @@ struct Cfg {
 struct TcArgs {
     const float* A;          // [H], or [Bt,T,H] (one per token) in the pre-activation variant
     const float* dt_bias;    // pre-activation variant: [H] or null
-    // pre-activation variant with the B / C normalisation: per-channel gains [N] (null = 1),
-    // channel biases [H, R, N] (null = 0), RMS normalisation on / off and its eps
-    const float* B_gain;
-    const float* C_gain;
-    const float* B_bias;
-    const float* C_bias;
-    int bc_norm;
-    float bc_eps;
     const float* omega;
     __nv_bfloat16* y;
     float* final_state;
@@ -147,6 +139,21 @@ struct TcArgs {
     float* seg_ld;           // state pass: [bh][S-1] summed log-decay of the segment
     float* seg_th;           // state pass: [bh][S-1][N/2] summed rotation angle of the segment
 };
+
+// Arguments of the B / C normalisation (a separate kernel parameter, empty for the
+// other variants so that their parameter block stays as it is): per-channel gains
+// [N] (null = 1), channel biases [H, R, N] (null = 0), RMS normalisation on / off, eps.
+template <bool ON>
+struct BcArgs {
+    const float* B_gain;
+    const float* C_gain;
+    const float* B_bias;
+    const float* C_bias;
+    int bc_norm;
+    float bc_eps;
+};
+template <>
+struct BcArgs<false> {};
 
 // Shared control block (after the barriers).  Three TMA groups per stage, each
 // issued as soon as its previous contents are dead: the dt / lambda boxes
@@ -211,16 +218,25 @@ __device__ __forceinline__ uint4 rotate4(uint4 v, const float2 (&c01)[2], const 
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// The B / C normalisation of the pre-activation variant fused with the rotation:
-// the 8 channels of this 16-byte piece (4 pairs) of a row get
-// v / sqrt(mean(v^2) + eps) * g + bias (the mean over the row's N channels,
-// reduced over the NG lanes that hold the row: lanes differing in their low
-// log2(NG) bits) or, without the norm, v + bias; then the pairs are rotated as
-// in rotate4.  Warp-uniform: every lane of the warp calls it together.
-template <int NG>
+// The B / C normalisation of the pre-activation variant fused with the rotation.
+// sumsq8: the sum of squares of the 8 channels of a 16-byte piece (4 pairs) of a
+// row; the row's total comes from the NG lanes holding it (lanes differing in
+// their low log2(NG) bits).  bc_rotate4: the piece's channels become
+// v * sc * g + bias (sc = 1 / sqrt(mean(v^2) + eps)) or, without the norm,
+// v + bias, then its pairs are rotated as in rotate4.
+__device__ __forceinline__ float sumsq8(uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float ss = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        ss = fmaf(bf_lo(w[q]), bf_lo(w[q]), ss);
+        ss = fmaf(bf_hi(w[q]), bf_hi(w[q]), ss);
+    }
+    return ss;
+}
+
 __device__ __forceinline__ uint4 bc_rotate4(uint4 v, const float2 (&c01)[2], const float2 (&s01)[2],
-                                            const float (&g)[8], const float (&bb)[8], bool norm, float eps,
-                                            float inv_n) {
+                                            const float (&g)[8], const float (&bb)[8], bool norm, float sc) {
     uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float e[8];
 #pragma unroll
@@ -228,19 +244,8 @@ __device__ __forceinline__ uint4 bc_rotate4(uint4 v, const float2 (&c01)[2], con
         e[2 * q] = bf_lo(w[q]);
         e[2 * q + 1] = bf_hi(w[q]);
     }
-    if (norm) {
-        float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ss = fmaf(e[i], e[i], ss);
-#pragma unroll
-        for (int o = 1; o < NG; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float sc = rsqrtf(fmaf(ss, inv_n, eps));
-#pragma unroll
-        for (int i = 0; i < 8; ++i) e[i] = fmaf(e[i] * sc, g[i], bb[i]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) e[i] += bb[i];
-    }
+    for (int i = 0; i < 8; ++i) e[i] = norm ? fmaf(e[i] * sc, g[i], bb[i]) : e[i] + bb[i];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const float2 a = make_float2(e[4 * h], e[4 * h + 2]);
@@ -252,6 +257,15 @@ __device__ __forceinline__ uint4 bc_rotate4(uint4 v, const float2 (&c01)[2], con
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
+
+// Per-thread registers of the B / C normalisation (gains of this thread's 8
+// channels; with one rank, its head's biases); empty when the variant is off.
+template <bool ON>
+struct BcRegs {
+    float gB[8], gC[8], bB1[8], bC1[8];
+};
+template <>
+struct BcRegs<false> {};
 
 // 8 consecutive floats from p (16-byte aligned), or `fill` when p is null.
 __device__ __forceinline__ void load8(const float* p, float fill, float (&o)[8]) {
@@ -314,7 +328,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                                                          const __grid_constant__ CUtensorMap tm_B,
                                                          const __grid_constant__ CUtensorMap tm_C,
                                                          const __grid_constant__ CUtensorMap tm_dt,
-                                                         const __grid_constant__ CUtensorMap tm_lam, TcArgs args) {
+                                                         const __grid_constant__ CUtensorMap tm_lam, TcArgs args,
+                                                         const BcArgs<PM == 2> bca) {
     using K = Cfg<NS, R, Q>;
     constexpr bool PREP = PM >= 1, BC = PM == 2;
     constexpr int P = K::P, QR = K::QR, NP2 = NS / 2, NG = K::NG, TG = K::TG, TPG = K::TPG;
@@ -758,13 +773,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         };
         if (PREP) a_nx = load_a(c_begin);
         // B / C normalisation: this thread's 8 channels' gains, and with one rank its head's biases
-        float gB[8], gC[8], bB1[8], bC1[8];
-        const bool bc_norm = BC && args.bc_norm != 0;
+        BcRegs<BC> bcr;
         if constexpr (BC) {
-            load8(args.B_gain ? args.B_gain + 8 * jg : nullptr, 1.f, gB);
-            load8(FULL && args.C_gain ? args.C_gain + 8 * jg : nullptr, 1.f, gC);
-            load8(R == 1 && args.B_bias ? args.B_bias + (int64_t)h * NS + 8 * jg : nullptr, 0.f, bB1);
-            load8(R == 1 && FULL && args.C_bias ? args.C_bias + (int64_t)h * NS + 8 * jg : nullptr, 0.f, bC1);
+            load8(bca.B_gain ? bca.B_gain + 8 * jg : nullptr, 1.f, bcr.gB);
+            load8(FULL && bca.C_gain ? bca.C_gain + 8 * jg : nullptr, 1.f, bcr.gC);
+            load8(R == 1 && bca.B_bias ? bca.B_bias + (int64_t)h * NS + 8 * jg : nullptr, 0.f, bcr.bB1);
+            load8(R == 1 && FULL && bca.C_bias ? bca.C_bias + (int64_t)h * NS + 8 * jg : nullptr, 0.f, bcr.bC1);
         }
         for (int i = 0; i < nl; ++i) {
             const int c = c_begin + i, s = i & 1;
@@ -879,31 +893,58 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     const float2 w2 = make_float2(wt, wt);
                     const float2 cw01[2] = {__fmul2_rn(w2, c01[0]), __fmul2_rn(w2, c01[1])};
                     const float2 sw01[2] = {__fmul2_rn(w2, s01[0]), __fmul2_rn(w2, s01[1])};
+                    if constexpr (BC) {
+                        // every row of this token (C and B of each rank) into registers first, their
+                        // sums of squares reduced together (independent shuffle chains), then each
+                        // row normalised, biased, rotated (B' also scaled by w) and stored
+                        constexpr int NR = FULL ? 2 * R : R;
+                        uint4 vr[NR];
+                        float ss[NR];
+                        const bool bc_norm = bca.bc_norm != 0;
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint32_t off2 = pan * QR * 128 + sw128_offset(t * R + r, cib);
-                        if constexpr (BC) {
-                            // normalise and bias the row, then rotate (B' also scaled by w)
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t off2 = pan * QR * 128 + sw128_offset(t * R + r, cib);
+                            if (FULL) vr[2 * r] = *reinterpret_cast<const uint4*>(tC + off2);
+                            vr[FULL ? 2 * r + 1 : r] = *reinterpret_cast<const uint4*>(tB + off2);
+                        }
+                        if (bc_norm) {
+#pragma unroll
+                            for (int i = 0; i < NR; ++i) ss[i] = sumsq8(vr[i]);
+#pragma unroll
+                            for (int o = 1; o < NG; o <<= 1) {
+#pragma unroll
+                                for (int i = 0; i < NR; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
+                            }
+#pragma unroll
+                            for (int i = 0; i < NR; ++i) ss[i] = rsqrtf(fmaf(ss[i], 1.f / NS, bca.bc_eps));
+                        }
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t off2 = pan * QR * 128 + sw128_offset(t * R + r, cib);
                             float bbB[8], bbC[8];
                             if (R == 1) {
 #pragma unroll
                                 for (int q = 0; q < 8; ++q) {
-                                    bbB[q] = bB1[q];
-                                    bbC[q] = bC1[q];
+                                    bbB[q] = bcr.bB1[q];
+                                    bbC[q] = bcr.bC1[q];
                                 }
                             } else {
-                                load8(args.B_bias ? args.B_bias + ((int64_t)h * R + r) * NS + 8 * jg : nullptr, 0.f, bbB);
+                                load8(bca.B_bias ? bca.B_bias + ((int64_t)h * R + r) * NS + 8 * jg : nullptr, 0.f, bbB);
                                 if (FULL)
-                                    load8(args.C_bias ? args.C_bias + ((int64_t)h * R + r) * NS + 8 * jg : nullptr, 0.f,
+                                    load8(bca.C_bias ? bca.C_bias + ((int64_t)h * R + r) * NS + 8 * jg : nullptr, 0.f,
                                           bbC);
                             }
-                            if (FULL) {
-                                uint4* pc = reinterpret_cast<uint4*>(tC + off2);
-                                *pc = bc_rotate4<NG>(*pc, c01, s01, gC, bbC, bc_norm, args.bc_eps, 1.f / NS);
-                            }
-                            uint4* pb = reinterpret_cast<uint4*>(tB + off2);
-                            *pb = bc_rotate4<NG>(*pb, cw01, sw01, gB, bbB, bc_norm, args.bc_eps, 1.f / NS);
-                        } else {
+                            if (FULL)
+                                *reinterpret_cast<uint4*>(tC + off2) =
+                                    bc_rotate4(vr[2 * r], c01, s01, bcr.gC, bbC, bc_norm, bc_norm ? ss[2 * r] : 1.f);
+                            const int ib = FULL ? 2 * r + 1 : r;
+                            *reinterpret_cast<uint4*>(tB + off2) =
+                                bc_rotate4(vr[ib], cw01, sw01, bcr.gB, bbB, bc_norm, bc_norm ? ss[ib] : 1.f);
+                        }
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t off2 = pan * QR * 128 + sw128_offset(t * R + r, cib);
                             if (FULL) {
                                 uint4* pc = reinterpret_cast<uint4*>(tC + off2);
                                 *pc = rotate4(*pc, c01, s01);
@@ -1072,12 +1113,9 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
     TcArgs args{};
     args.A = A;
     args.dt_bias = prep.dt_bias;
-    args.B_gain = prep.B_gain;
-    args.C_gain = prep.C_gain;
-    args.B_bias = prep.B_bias;
-    args.C_bias = prep.C_bias;
-    args.bc_norm = prep.bc_norm ? 1 : 0;
-    args.bc_eps = prep.bc_eps;
+    BcArgs<PM == 2> bca{};
+    if constexpr (PM == 2) bca = BcArgs<true>{prep.B_gain, prep.C_gain, prep.B_bias, prep.C_bias, prep.bc_norm ? 1 : 0,
+                                              prep.bc_eps};
     args.omega = omega;
     args.y = static_cast<__nv_bfloat16*>(y);
     args.final_state = final_state;
@@ -1102,7 +1140,7 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
         auto k1 = scan_tc_kernel<NS, R, Q, false, PM>;
         e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
         if (e != cudaSuccess) return e;
-        k1<<<(unsigned)(seqs * a1.nseg), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, a1);
+        k1<<<(unsigned)(seqs * a1.nseg), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, a1, bca);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // segment carries -> the state entering each segment (in place), and into the last one
         e = launch_state_passing(segU, segLD, segTH, nullptr, last, 1, seqs, pl.S - 1, NS, (int64_t)P, stream);
@@ -1114,7 +1152,7 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
     auto kern = scan_tc_kernel<NS, R, Q, true, PM>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(seqs * pl.S), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, args);
+    kern<<<(unsigned)(seqs * pl.S), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, args, bca);
     return cudaGetLastError();
 }
 
