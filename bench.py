@@ -255,14 +255,14 @@ def time_prefill(binding, w, d, stream, steps, warmup, dist, device):
 PREP_KEYS = ("x", "B", "C", "dt_raw", "A", "u", "omega")
 
 
-def time_prefill_prep(binding, w, dp, stream, steps, warmup, dist, device, bc=None):
+def time_prefill_prep(binding, w, dp, stream, steps, warmup, dist, device, bc=None, z=None):
     """The same over m3_scan_fwd_prep (pre-activations, one decay generator per token; ``bc``:
     the B / C normalisation and channel biases, device tensors)."""
     y = torch.empty_like(dp["x"])
     fin = torch.empty((w.batch, w.heads, w.dstate, w.headdim), dtype=torch.float32, device=device)
     ws = binding.alloc_workspace_prep(dp["x"].shape, w.dstate, w.rank, w.chunk, dp["x"].dtype, device)
     args = [dp[k] for k in PREP_KEYS]
-    params = binding.prep_params(dp["dt_bias"], bc)
+    params = binding.prep_params(dp["dt_bias"], bc, z)
 
     def call():
         st = binding.m3_scan_fwd_prep(*args, w.rank, w.chunk, y, fin, ws, params, stream)
@@ -603,7 +603,15 @@ def main():
         line["prefill_prep"]["with_bc_norm"] = {
             "value": tokens * args.steps / bsec / 1e6, "unit": "Mtok/s", "ms_per_step": bsec / args.steps * 1e3,
             "roofline_frac": pbytes / (bms * 1e-3) / 1e9 / pk["hbm_gbs"]}
-        del dp, bc
+        # and with the output gate as well (the SSM + rotary + gate fusion level); z is read once
+        z = synth.make_gate(tuple(dp["x"].shape), io=w.io, seed=rank, device=device)
+        gsec, gper = time_prefill_prep(binding, w, dp, stream, args.steps, args.warmup, dist, device, bc=bc, z=z)
+        gms = sum(gper) / len(gper)
+        gbytes = pbytes + z.numel() * z.element_size()
+        line["prefill_prep"]["with_bc_norm_and_gate"] = {
+            "value": tokens * args.steps / gsec / 1e6, "unit": "Mtok/s", "ms_per_step": gsec / args.steps * 1e3,
+            "algorithmic_bytes_per_call": gbytes, "roofline_frac": gbytes / (gms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+        del dp, bc, z
 
     if not args.no_e2e:
         host = {k: d[k].to("cpu").pin_memory() for k in KEYS}

@@ -193,6 +193,11 @@ M3_API int m3_decode_step(float* state, const void* x_t, const void* B_t, void* 
  *            unused without bc_norm)
  *   B_bias, C_bias  [H, R, N] fp32 head-specific channel biases added after the
  *            normalisation (or to the raw rows without it) (NULL = 0)
+ *   z        y's layout and io dtype (prefill [batch, T, H, R, P], decode
+ *            [batch, H, R, P]), nullable: the output gate y <- y * silu(z),
+ *            silu(z) = z / (1 + e^-z), applied in the kernels' epilogues (the
+ *            SSM+Gate fusion of Tables 11-12; the pages give no gate formula,
+ *            this is the Mamba family's)
  */
 typedef struct m3_prep_params {
     const float* dt_bias;
@@ -202,6 +207,7 @@ typedef struct m3_prep_params {
     const float* C_gain;
     const float* B_bias;
     const float* C_bias;
+    const void* z;
 } m3_prep_params;
 
 /*

@@ -24,7 +24,9 @@ the per-token parameters instead: Delta_t = softplus(dt_raw_t + dt_bias_h),
 lambda_t = sigmoid(u_t) (the default lambda parameterisation of the appendix
 ablation table), A_t given per token; optionally B and C are RMS-normalised
 over N, then shifted by per-head channel biases, before the rotation
-(``bc_prep``; the BC normalisation and biases of section 3.4).
+(``bc_prep``; the BC normalisation and biases of section 3.4); and the
+output may be gated, y * silu(z) (the SSM+Gate fusion of Tables 11-12; the
+pages give no gate formula, this is the Mamba family's).
 """
 from __future__ import annotations
 
@@ -149,6 +151,12 @@ def prep(dt_raw, dt_bias, u):
     return softplus(z), sigmoid(u)
 
 
+def silu(z):
+    """z * sigmoid(z) in float64."""
+    z = f64(z)
+    return z * sigmoid(z)
+
+
 def bc_prep(V, norm: bool = False, eps: float = 0.0, gain=None, bias=None):
     """B or C before the rotation (float64): every (token, rank) row v of V [..., H, R, N]
     becomes v / sqrt(mean(v^2) + eps) * gain when ``norm`` (gain [N], None = 1), then
@@ -170,10 +178,11 @@ def _bc(B, C, bc):
             bc_prep(C, norm, eps, bc.get("C_gain"), bc.get("C_bias")))
 
 
-def scan_prep(x, B, C, dt_raw, dt_bias, A_tok, u, omega, h0=None, prev=None, bc=None):
+def scan_prep(x, B, C, dt_raw, dt_bias, A_tok, u, omega, h0=None, prev=None, bc=None, z=None):
     """``scan`` on pre-activations: Delta, lambda from ``prep``, A_tok [Bt,T,H] per token;
     ``bc`` (dict: norm, eps, B_gain, C_gain, B_bias, C_bias) normalises and biases B and C
-    with ``bc_prep`` first.  ``prev`` holds the raw (unnormalised) B_{t-1}, X_{t-1}."""
+    with ``bc_prep`` first.  ``prev`` holds the raw (unnormalised) B_{t-1}, X_{t-1}.
+    ``z`` (y's shape): the output gate, y <- y * silu(z)."""
     d, lam = prep(dt_raw, dt_bias, u)
     Bn, Cn = _bc(B, C, bc)
     if prev is not None and bc:
@@ -181,6 +190,8 @@ def scan_prep(x, B, C, dt_raw, dt_bias, A_tok, u, omega, h0=None, prev=None, bc=
     y, hT, prevT = scan(x, Bn, Cn, d, A_tok, lam, omega, h0=h0, prev=prev)
     if bc:   # hand back the raw factors of the last token, as the kernels keep them
         prevT = _prev_raw(f64(B)[:, -1], f64(x)[:, -1])
+    if z is not None:
+        y = y * silu(z)
     return y, hT, prevT
 
 
@@ -200,9 +211,10 @@ def _prev_raw(B_last, x_last):
     return np.concatenate([B_last.reshape(b, H, -1), x_last.reshape(b, H, -1)], axis=-1)
 
 
-def decode_step_prep(state, x_t, B_t, prev, C_t, dt_raw_t, dt_bias, A_t, u_t, omega_t, bc=None):
+def decode_step_prep(state, x_t, B_t, prev, C_t, dt_raw_t, dt_bias, A_t, u_t, omega_t, bc=None, z_t=None):
     """One decode token on pre-activations: dt_raw_t, A_t, u_t [b,H]; dt_bias [H] or None;
-    ``prev`` and the returned cache hold the raw B_{t-1}, X_{t-1}."""
+    ``prev`` and the returned cache hold the raw B_{t-1}, X_{t-1}; ``z_t`` [b,H,R,P]: the
+    output gate."""
     d, lam = prep(dt_raw_t, dt_bias, u_t)
     Bt, Ct = f64(B_t), f64(C_t)
     Bn, Cn = _bc(Bt, Ct, bc)
@@ -213,7 +225,8 @@ def decode_step_prep(state, x_t, B_t, prev, C_t, dt_raw_t, dt_bias, A_t, u_t, om
                         lam[:, None], f64(omega_t)[:, None], h0=state, prev=prev)
     if bc:
         prevT = _prev_raw(Bt, f64(x_t))
-    return y[:, 0], hT, prevT
+    yt = y[:, 0] if z_t is None else y[:, 0] * silu(z_t)
+    return yt, hT, prevT
 
 
 def rel_err(got, ref) -> float:

@@ -34,7 +34,7 @@ class PrepParams(ctypes.Structure):
     """m3_prep_params: pre-SSM options of the _prep entry points (device pointers or NULL)."""
     _fields_ = [("dt_bias", ctypes.c_void_p), ("bc_norm", ctypes.c_int), ("bc_eps", ctypes.c_float),
                 ("B_gain", ctypes.c_void_p), ("C_gain", ctypes.c_void_p), ("B_bias", ctypes.c_void_p),
-                ("C_bias", ctypes.c_void_p)]
+                ("C_bias", ctypes.c_void_p), ("z", ctypes.c_void_p)]
 
 
 # Every symbol include/m3.h declares, with its ctypes signature.
@@ -179,13 +179,13 @@ def m3_scan_fwd_prep_workspace_size(batch, seqlen, nheads, headdim, dstate, R, c
     return int(load().m3_scan_fwd_prep_workspace_size(batch, seqlen, nheads, headdim, dstate, R, chunk, io))
 
 
-def prep_params(dt_bias=None, bc=None):
+def prep_params(dt_bias=None, bc=None, z=None):
     """PrepParams from device tensors: dt_bias [H]; bc = dict(norm, eps, B_gain, C_gain,
-    B_bias, C_bias), tensors [N] / [H, R, N] or absent."""
+    B_bias, C_bias), tensors [N] / [H, R, N] or absent; z: the output gate's input (y's shape)."""
     bc = bc or {}
     return PrepParams(_ptr(dt_bias, torch.float32), 1 if bc.get("norm") else 0, float(bc.get("eps", 0.0)),
                       _ptr(bc.get("B_gain"), torch.float32), _ptr(bc.get("C_gain"), torch.float32),
-                      _ptr(bc.get("B_bias"), torch.float32), _ptr(bc.get("C_bias"), torch.float32))
+                      _ptr(bc.get("B_bias"), torch.float32), _ptr(bc.get("C_bias"), torch.float32), _ptr(z))
 
 
 def m3_scan_fwd_prep(x, B, C, dt_raw, A, u, omega, R: int, chunk: int, y, final_state, workspace, params=None,
@@ -247,8 +247,8 @@ def alloc_workspace_prep(x_shape, N: int, R: int, chunk: int, dtype: torch.dtype
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
-def scan_fwd_prep(x, B, C, dt_raw, A, u, omega, R: int, chunk: int, dt_bias=None, bc=None, want_final: bool = True,
-                  workspace=None, stream=None):
+def scan_fwd_prep(x, B, C, dt_raw, A, u, omega, R: int, chunk: int, dt_bias=None, bc=None, z=None,
+                  want_final: bool = True, workspace=None, stream=None):
     """Prefill on pre-activations (Delta = softplus(dt_raw + dt_bias), lambda = sigmoid(u), A per
     token; ``bc``: B / C normalisation and biases, see prep_params); returns (y, final_state or None)."""
     Bt, T, H, _, P = x.shape
@@ -257,18 +257,18 @@ def scan_fwd_prep(x, B, C, dt_raw, A, u, omega, R: int, chunk: int, dt_bias=None
     fin = torch.empty((Bt, H, N, P), dtype=torch.float32, device=x.device) if want_final else None
     if workspace is None:
         workspace = alloc_workspace_prep(x.shape, N, R, chunk, x.dtype, x.device)
-    params = prep_params(dt_bias, bc)
+    params = prep_params(dt_bias, bc, z)
     _check(m3_scan_fwd_prep(x, B, C, dt_raw, A, u, omega, R, chunk, y, fin, workspace, params, stream),
            "m3_scan_fwd_prep")
     return y, fin
 
 
 def decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, A_t, u_t, omega_t, R: int, dt_bias=None, bc=None,
-                     y_t=None, stream=None):
+                     z_t=None, y_t=None, stream=None):
     """One decode token on pre-activations, in place on ``state`` and ``cache`` (raw B, X); returns y_t."""
     if y_t is None:
         y_t = torch.empty_like(x_t)
-    params = prep_params(dt_bias, bc)
+    params = prep_params(dt_bias, bc, z_t)
     _check(m3_decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, A_t, u_t, omega_t, y_t, R, params, stream),
            "m3_decode_step_prep")
     return y_t

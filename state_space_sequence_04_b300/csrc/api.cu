@@ -50,7 +50,7 @@ bool prep_from(const m3_prep_params* p, m3::Prep* out) {
     q.on = true;
     if (p != nullptr) {
         if (!ok_nullable(p->dt_bias) || !ok_nullable(p->B_gain) || !ok_nullable(p->C_gain) ||
-            !ok_nullable(p->B_bias) || !ok_nullable(p->C_bias))
+            !ok_nullable(p->B_bias) || !ok_nullable(p->C_bias) || !ok_nullable(p->z))
             return false;
         if (!(p->bc_eps >= 0.f) || p->bc_eps > 3.0e38f) return false;
         q.dt_bias = p->dt_bias;
@@ -60,6 +60,7 @@ bool prep_from(const m3_prep_params* p, m3::Prep* out) {
         q.C_gain = p->C_gain;
         q.B_bias = p->B_bias;
         q.C_bias = p->C_bias;
+        q.z = p->z;
     }
     *out = q;
     return true;

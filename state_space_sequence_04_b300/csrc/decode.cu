@@ -277,10 +277,11 @@ __global__ void __launch_bounds__(256, DecodeOcc<R>::value) decode_kernel(
     }
     __syncthreads();
     IO* yb = y_t + bh * R * P;
+    const IO* zb = prep.z != nullptr ? static_cast<const IO*>(prep.z) + bh * R * P : nullptr;
     for (int o = tid; o < R * P; o += nt) {
         float s = 0.f;
         for (int gg = 0; gg < rows; ++gg) s += sRed[gg * (R * P) + o];
-        st_io(yb, o, s);
+        st_io(yb, o, zb != nullptr ? s * silu_f(ld_io(zb, o)) : s);   // output gate
     }
 }
 
@@ -488,10 +489,11 @@ __global__ void __launch_bounds__(256, 2) decode_stream_kernel(
             if (u3 < units) issue(u3, slot);
         }
         IO* yb = y_t + u * R * P;
+        const IO* zb = prep.z != nullptr ? static_cast<const IO*>(prep.z) + u * R * P : nullptr;
         for (int o = tid; o < R * P; o += nt) {
             float s = 0.f;
             for (int gg = 0; gg < rows; ++gg) s += sRed[gg * (R * P) + o];
-            st_io(yb, o, s);
+            st_io(yb, o, zb != nullptr ? s * silu_f(ld_io(zb, o)) : s);   // output gate
         }
         __syncthreads();   // sRed and the staged operands are free for the next unit
     }

@@ -55,7 +55,8 @@ namespace m3 {
 // lambda holds u (lambda = sigmoid(u)), and A holds one value per token with
 // dt's layout.
 // With on, B and C may also be RMS-normalised per (token, rank) row over N
-// (bc_norm, bc_eps, gains [N]) and shifted by channel biases [H, R, N].
+// (bc_norm, bc_eps, gains [N]) and shifted by channel biases [H, R, N], and the
+// output gated by z.
 struct Prep {
     bool on;
     const float* dt_bias;
@@ -65,8 +66,12 @@ struct Prep {
     const float* C_gain;
     const float* B_bias;
     const float* C_bias;
+    const void* z;   // output gate input (y's layout, io dtype): y <- y * silu(z); null = off
     __host__ __device__ bool bc() const { return on && (bc_norm || B_bias != nullptr || C_bias != nullptr); }
 };
+
+// silu(z) = z / (1 + e^-z), the output gate.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 struct ScanDims {
     int64_t batch, seqlen, nheads, headdim, dstate;

@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
     const IO* __restrict__ x, const IO* __restrict__ B, const IO* __restrict__ C,
     const float* __restrict__ dt, const float* __restrict__ A, const float* __restrict__ lam,
     const float* __restrict__ omega, const float* __restrict__ Hc, IO* __restrict__ y,
-    int64_t T, int H, int P, int N, int Q, int nc, int a_tok, const BcArgs bcB, const BcArgs bcC) {
+    int64_t T, int H, int P, int N, int Q, int nc, int a_tok, const BcArgs bcB, const BcArgs bcC,
+    const IO* __restrict__ gate) {
     extern __shared__ float sm[];
     constexpr int RT = kRowTile;
     constexpr int TT = RT / R;
@@ -378,7 +379,8 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(
             if (t < q) {
                 const int64_t base = (((b * T + c0 + t) * H + h) * R + r) * P + 4 * cg;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) st_io(y, base + e, acc[i][e]);
+                for (int e = 0; e < 4; ++e)   // output gate y * silu(z) when given
+                    st_io(y, base + e, gate != nullptr ? acc[i][e] * silu_f(ld_io(gate, base + e)) : acc[i][e]);
             }
         }
     }
@@ -398,7 +400,8 @@ size_t smem_c(const ScanDims& d) {
 template <typename IO, int R>
 cudaError_t launch_rt(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                       const float* A, const float* lambda, const float* omega, void* y, float* final_state,
-                      void* workspace, int a_tok, const BcArgs& bcB, const BcArgs& bcC, cudaStream_t stream) {
+                      void* workspace, int a_tok, const BcArgs& bcB, const BcArgs& bcC, const void* gate,
+                      cudaStream_t stream) {
     const int64_t bh = d.batch * d.nheads;
     const int64_t nc = d.nchunks();
     const int64_t NP = d.dstate * d.headdim;
@@ -426,7 +429,7 @@ cudaError_t launch_rt(const ScanDims& d, const void* x, const void* B, const voi
         const unsigned tiles = (unsigned)((d.chunk + TT - 1) / TT);
         kc<<<dim3((unsigned)bh, (unsigned)nc, tiles), kThreads, sc, stream>>>(
             (const IO*)x, (const IO*)B, (const IO*)C, dt, A, lambda, omega, U, (IO*)y, d.seqlen, (int)d.nheads,
-            (int)d.headdim, (int)d.dstate, d.chunk, (int)nc, a_tok, bcB, bcC);
+            (int)d.headdim, (int)d.dstate, d.chunk, (int)nc, a_tok, bcB, bcC, (const IO*)gate);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -435,9 +438,11 @@ cudaError_t launch_rt(const ScanDims& d, const void* x, const void* B, const voi
 template <typename IO>
 cudaError_t launch_io(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                       const float* A, const float* lambda, const float* omega, void* y, float* final_state,
-                      void* workspace, int a_tok, const BcArgs& bcB, const BcArgs& bcC, cudaStream_t stream) {
+                      void* workspace, int a_tok, const BcArgs& bcB, const BcArgs& bcC, const void* gate,
+                      cudaStream_t stream) {
 #define M3_SIMT_CASE(RR) \
-    case RR: return launch_rt<IO, RR>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, bcB, bcC, stream);
+    case RR: return launch_rt<IO, RR>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, bcB, bcC, \
+                                      gate, stream);
     switch (d.R) {
         M3_SIMT_CASE(1)
         M3_SIMT_CASE(2)
@@ -539,8 +544,9 @@ cudaError_t launch_scan_simt(const ScanDims& d, const void* x, const void* B, co
     const int a_tok = prep.on ? 1 : 0;
     if (d.io == M3_DTYPE_BF16)
         return launch_io<__nv_bfloat16>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, bcB, bcC,
-                                        stream);
-    return launch_io<float>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, bcB, bcC, stream);
+                                        prep.on ? prep.z : nullptr, stream);
+    return launch_io<float>(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, a_tok, bcB, bcC,
+                            prep.on ? prep.z : nullptr, stream);
 }
 
 }  // namespace m3

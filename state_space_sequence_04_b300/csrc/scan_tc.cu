@@ -140,20 +140,29 @@ struct TcArgs {
     float* seg_th;           // state pass: [bh][S-1][N/2] summed rotation angle of the segment
 };
 
-// Arguments of the B / C normalisation (a separate kernel parameter, empty for the
-// other variants so that their parameter block stays as it is): per-channel gains
-// [N] (null = 1), channel biases [H, R, N] (null = 0), RMS normalisation on / off, eps.
+// Arguments of the pre-activation variants' B / C normalisation and output gate
+// (a separate kernel parameter, an empty struct for the plain kernel so that its
+// parameter block stays as it is): per-channel gains [N] (null = 1), channel
+// biases [H, R, N] (null = 0), RMS normalisation on / off and its eps, the gate
+// input z (y's layout, bf16).
 template <bool ON>
-struct BcArgs {
+struct ExtArgs {
     const float* B_gain;
     const float* C_gain;
     const float* B_bias;
     const float* C_bias;
     int bc_norm;
     float bc_eps;
+    const __nv_bfloat16* z;
 };
 template <>
-struct BcArgs<false> {};
+struct ExtArgs<false> {};
+
+// Word i (two bf16) of a run of 16-byte pieces.
+__device__ __forceinline__ uint32_t word_at(const uint4* a, int i) {
+    const uint4 v = a[i >> 2];
+    return (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
+}
 
 // Shared control block (after the barriers).  Three TMA groups per stage, each
 // issued as soon as its previous contents are dead: the dt / lambda boxes
@@ -319,19 +328,20 @@ __device__ __forceinline__ void mask_block(float* v, int cb, int t, float ct, fl
 // segmented prefill -- only the carry (rotated, scaled B, scaled X and the
 // chunk-state MMA), whose value at the segment's end from a zero start, summed
 // log-decay and summed angles go to the workspace for the segment scan.
-// PM >= 1 (pre-activation variant): the dt and lambda inputs are pre-activations
-// (Delta = softplus(dt + dt_bias[h]), lambda = sigmoid(u), applied to the staged
-// boxes in shared memory) and A holds one decay generator per token.  PM = 2
-// adds the B / C normalisation and channel biases, fused with the rotation.
+// PM (bitmask) & 1, the pre-activation variant: the dt and lambda inputs are
+// pre-activations (Delta = softplus(dt + dt_bias[h]), lambda = sigmoid(u), applied
+// to the staged boxes in shared memory) and A holds one decay generator per
+// token.  PM & 2 adds the B / C normalisation and channel biases, fused with the
+// rotation; PM & 4 the output gate y * silu(z) in the epilogue.
 template <int NS, int R, int Q, bool FULL, int PM>
 __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                          const __grid_constant__ CUtensorMap tm_B,
                                                          const __grid_constant__ CUtensorMap tm_C,
                                                          const __grid_constant__ CUtensorMap tm_dt,
                                                          const __grid_constant__ CUtensorMap tm_lam, TcArgs args,
-                                                         const BcArgs<PM == 2> bca) {
+                                                         const ExtArgs<PM != 0> ext) {
     using K = Cfg<NS, R, Q>;
-    constexpr bool PREP = PM >= 1, BC = PM == 2;
+    constexpr bool PREP = (PM & 1) != 0, BC = (PM & 2) != 0, GATE = (PM & 4) != 0;
     constexpr int P = K::P, QR = K::QR, NP2 = NS / 2, NG = K::NG, TG = K::TG, TPG = K::TPG;
     constexpr int TX_CB = FULL ? 2 * K::BC_BYTES : K::BC_BYTES;
     extern __shared__ uint8_t smem_raw[];
@@ -513,6 +523,20 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             tc_fence_before();
             group_bar(1);
             if (*fail_c) break;
+            // output gate: this thread's z values of the chunk, loaded now so that their latency
+            // hides behind the MMAs and the mask (zero past the end of the sequence)
+            constexpr int NZ = GATE && FULL ? (K::M64 ? 4 : 8) : 1;
+            uint4 zg[NZ];
+            if constexpr (GATE && FULL) {
+                const bool mine = K::M64 || warp * 32 < QR;
+                const int row = K::M64 ? warp * 16 + (lane & 15) : tid, t = row / R, r = row % R;
+                const int tok = c * Q + t;
+                const __nv_bfloat16* zrow = ext.z + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P +
+                                            (K::M64 ? 32 * (lane >> 4) : 0);
+#pragma unroll
+                for (int k = 0; k < NZ; ++k)
+                    zg[k] = mine && tok < T ? __ldg(reinterpret_cast<const uint4*>(zrow) + k) : make_uint4(0u, 0u, 0u, 0u);
+            }
             if (tid == 0) {
                 tc_fence_after();
                 // descriptors of the operand bases; a byte offset o moves the start address field by o >> 4
@@ -618,8 +642,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     uint32_t pk[16];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
-                        const float2 o = __ffma2_rn(e2, make_float2(iv[2 * q], iv[2 * q + 1]),
-                                                    make_float2(yv[2 * q], yv[2 * q + 1]));
+                        float2 o = __ffma2_rn(e2, make_float2(iv[2 * q], iv[2 * q + 1]),
+                                              make_float2(yv[2 * q], yv[2 * q + 1]));
+                        if constexpr (GATE) {   // y * silu(z)
+                            const uint32_t zw = word_at(zg, q);
+                            o = make_float2(o.x * silu_f(bf_lo(zw)), o.y * silu_f(bf_hi(zw)));
+                        }
                         pk[q] = pack_bf16(o.x, o.y);
                     }
                     if (tok < T) {
@@ -640,8 +668,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                         uint32_t pk[16];
 #pragma unroll
                         for (int q = 0; q < 16; ++q) {
-                            const float2 o = __ffma2_rn(e2, make_float2(iv[2 * q], iv[2 * q + 1]),
-                                                        make_float2(yv[2 * q], yv[2 * q + 1]));
+                            float2 o = __ffma2_rn(e2, make_float2(iv[2 * q], iv[2 * q + 1]),
+                                                  make_float2(yv[2 * q], yv[2 * q + 1]));
+                            if constexpr (GATE) {   // y * silu(z)
+                                const uint32_t zw = word_at(zg, cc / 2 + q);
+                                o = make_float2(o.x * silu_f(bf_lo(zw)), o.y * silu_f(bf_hi(zw)));
+                            }
                             pk[q] = pack_bf16(o.x, o.y);
                         }
                         if (tok < T) {
@@ -775,10 +807,10 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         // B / C normalisation: this thread's 8 channels' gains, and with one rank its head's biases
         BcRegs<BC> bcr;
         if constexpr (BC) {
-            load8(bca.B_gain ? bca.B_gain + 8 * jg : nullptr, 1.f, bcr.gB);
-            load8(FULL && bca.C_gain ? bca.C_gain + 8 * jg : nullptr, 1.f, bcr.gC);
-            load8(R == 1 && bca.B_bias ? bca.B_bias + (int64_t)h * NS + 8 * jg : nullptr, 0.f, bcr.bB1);
-            load8(R == 1 && FULL && bca.C_bias ? bca.C_bias + (int64_t)h * NS + 8 * jg : nullptr, 0.f, bcr.bC1);
+            load8(ext.B_gain ? ext.B_gain + 8 * jg : nullptr, 1.f, bcr.gB);
+            load8(FULL && ext.C_gain ? ext.C_gain + 8 * jg : nullptr, 1.f, bcr.gC);
+            load8(R == 1 && ext.B_bias ? ext.B_bias + (int64_t)h * NS + 8 * jg : nullptr, 0.f, bcr.bB1);
+            load8(R == 1 && FULL && ext.C_bias ? ext.C_bias + (int64_t)h * NS + 8 * jg : nullptr, 0.f, bcr.bC1);
         }
         for (int i = 0; i < nl; ++i) {
             const int c = c_begin + i, s = i & 1;
@@ -900,7 +932,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                         constexpr int NR = FULL ? 2 * R : R;
                         uint4 vr[NR];
                         float ss[NR];
-                        const bool bc_norm = bca.bc_norm != 0;
+                        const bool bc_norm = ext.bc_norm != 0;
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const uint32_t off2 = pan * QR * 128 + sw128_offset(t * R + r, cib);
@@ -916,7 +948,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                                 for (int i = 0; i < NR; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
                             }
 #pragma unroll
-                            for (int i = 0; i < NR; ++i) ss[i] = rsqrtf(fmaf(ss[i], 1.f / NS, bca.bc_eps));
+                            for (int i = 0; i < NR; ++i) ss[i] = rsqrtf(fmaf(ss[i], 1.f / NS, ext.bc_eps));
                         }
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
@@ -929,9 +961,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                                     bbC[q] = bcr.bC1[q];
                                 }
                             } else {
-                                load8(bca.B_bias ? bca.B_bias + ((int64_t)h * R + r) * NS + 8 * jg : nullptr, 0.f, bbB);
+                                load8(ext.B_bias ? ext.B_bias + ((int64_t)h * R + r) * NS + 8 * jg : nullptr, 0.f, bbB);
                                 if (FULL)
-                                    load8(bca.C_bias ? bca.C_bias + ((int64_t)h * R + r) * NS + 8 * jg : nullptr, 0.f,
+                                    load8(ext.C_bias ? ext.C_bias + ((int64_t)h * R + r) * NS + 8 * jg : nullptr, 0.f,
                                           bbC);
                             }
                             if (FULL)
@@ -1113,9 +1145,10 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
     TcArgs args{};
     args.A = A;
     args.dt_bias = prep.dt_bias;
-    BcArgs<PM == 2> bca{};
-    if constexpr (PM == 2) bca = BcArgs<true>{prep.B_gain, prep.C_gain, prep.B_bias, prep.C_bias, prep.bc_norm ? 1 : 0,
-                                              prep.bc_eps};
+    ExtArgs<PM != 0> ext{};
+    if constexpr (PM != 0)
+        ext = ExtArgs<true>{prep.B_gain, prep.C_gain, prep.B_bias, prep.C_bias, prep.bc_norm ? 1 : 0, prep.bc_eps,
+                            static_cast<const __nv_bfloat16*>(prep.z)};
     args.omega = omega;
     args.y = static_cast<__nv_bfloat16*>(y);
     args.final_state = final_state;
@@ -1140,7 +1173,7 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
         auto k1 = scan_tc_kernel<NS, R, Q, false, PM>;
         e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
         if (e != cudaSuccess) return e;
-        k1<<<(unsigned)(seqs * a1.nseg), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, a1, bca);
+        k1<<<(unsigned)(seqs * a1.nseg), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, a1, ext);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // segment carries -> the state entering each segment (in place), and into the last one
         e = launch_state_passing(segU, segLD, segTH, nullptr, last, 1, seqs, pl.S - 1, NS, (int64_t)P, stream);
@@ -1152,7 +1185,7 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
     auto kern = scan_tc_kernel<NS, R, Q, true, PM>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(seqs * pl.S), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, args, bca);
+    kern<<<(unsigned)(seqs * pl.S), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, args, ext);
     return cudaGetLastError();
 }
 
@@ -1164,15 +1197,18 @@ int launches_cfg(const ScanDims& d) { return seg_plan<NS, R, Q>(d).S > 1 ? 3 : 1
 typedef cudaError_t (*LaunchFn)(const ScanDims&, const void*, const void*, const void*, const float*, const float*,
                                 const float*, const float*, void*, float*, void*, const Prep&, cudaStream_t);
 struct TcImpl {
-    LaunchFn launch[3];     // dt, lambda, A[H] as given | pre-activations, A per token | the same + B / C norm
+    // by kernel mode: 0 = dt, lambda, A[H] as given; bit 0 = pre-activations, A per token;
+    // bit 1 = B / C normalisation; bit 2 = output gate (modes 0, 1, 3, 5, 7)
+    LaunchFn launch[8];
     size_t (*workspace)(const ScanDims&);
     int (*launches)(const ScanDims&);
 };
 
 template <int NS, int R, int Q>
 TcImpl impl() {
-    return TcImpl{{launch_cfg<NS, R, Q, 0>, launch_cfg<NS, R, Q, 1>, launch_cfg<NS, R, Q, 2>}, ws_cfg<NS, R, Q>,
-                  launches_cfg<NS, R, Q>};
+    return TcImpl{{launch_cfg<NS, R, Q, 0>, launch_cfg<NS, R, Q, 1>, nullptr, launch_cfg<NS, R, Q, 3>, nullptr,
+                   launch_cfg<NS, R, Q, 5>, nullptr, launch_cfg<NS, R, Q, 7>},
+                  ws_cfg<NS, R, Q>, launches_cfg<NS, R, Q>};
 }
 
 // Tile configuration for (N, R, chunk).  Chunks of chunk*R <= 128 rows run as
@@ -1213,7 +1249,7 @@ cudaError_t launch_scan_tc(const ScanDims& d, const void* x, const void* B, cons
                            void* workspace, const Prep& prep, cudaStream_t stream) {
     TcImpl f;
     if (!pick(d, &f)) return cudaErrorNotSupported;
-    const int mode = !prep.on ? 0 : (prep.bc() ? 2 : 1);
+    const int mode = !prep.on ? 0 : 1 | (prep.bc() ? 2 : 0) | (prep.z != nullptr ? 4 : 0);
     return f.launch[mode](d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, prep, stream);
 }
 

@@ -170,6 +170,12 @@ def make_bc_params(heads: int, rank: int, dstate: int, seed: int = 7, device="cp
     return {"norm": True, "eps": 1e-5, "B_gain": B_gain, "C_gain": C_gain, "B_bias": B_bias, "C_bias": C_bias}
 
 
+def make_gate(shape, io: str = "bf16", seed: int = 9, device="cpu") -> torch.Tensor:
+    """The output gate's input z (y's shape) ~ N(0, 1.5^2), in the io dtype."""
+    g = _gen(seed, device)
+    return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * 1.5).to(io_torch_dtype(io))
+
+
 def make_decode_state(batch: int, heads: int, dstate: int, headdim: int, seed: int = 0,
                       device="cpu") -> torch.Tensor:
     """fp32 state [b, H, N, P] ~ N(0, 1)."""

@@ -36,9 +36,9 @@ def _bc_dev(bc):
     return None if bc is None else {k: (v.cuda().contiguous() if hasattr(v, "shape") else v) for k, v in bc.items()}
 
 
-def _oracle(inp, bias=True, bc=None):
+def _oracle(inp, bias=True, bc=None, z=None):
     return oracle.scan_prep(inp["x"], inp["B"], inp["C"], inp["dt_raw"], inp["dt_bias"] if bias else None, inp["A"],
-                            inp["u"], inp["omega"], bc=_bc_f64(bc))
+                            inp["u"], inp["omega"], bc=_bc_f64(bc), z=None if z is None else oracle.f64(z))
 
 
 def _oracle_sampled(inp, samples, bc=None):
@@ -60,13 +60,14 @@ def _oracle_sampled(inp, samples, bc=None):
     return {s: (y[:, :, i:i + 1], hT[:, i:i + 1]) for i, s in enumerate(samples)}
 
 
-def _run(inp, R, Q, bias=True, bc=None):
+def _run(inp, R, Q, bias=True, bc=None, z=None):
     d = _dev(inp)
     Bt, T, H, _, P = d["x"].shape
     N = d["B"].shape[-1]
     ws = binding.alloc_workspace_prep(d["x"].shape, N, R, Q, d["x"].dtype, "cuda")
     y, fin = binding.scan_fwd_prep(d["x"], d["B"], d["C"], d["dt_raw"], d["A"], d["u"], d["omega"], R, Q,
-                                   dt_bias=d["dt_bias"] if bias else None, bc=_bc_dev(bc), workspace=ws)
+                                   dt_bias=d["dt_bias"] if bias else None, bc=_bc_dev(bc),
+                                   z=None if z is None else z.cuda().contiguous(), workspace=ws)
     torch.cuda.synchronize()
     return y, fin, ws
 
@@ -122,6 +123,28 @@ def test_scan_prep_tensor_core_bias_only(Bt, H, T, P, N, R, Q):
     yr, hr, _ = _oracle(inp, bc=bc)
     assert_close(y, yr, TOL["bf16"], "y")
     assert_close(fin, hr, TOL["bf16"], "final_state")
+
+
+# output gate y * silu(z): 64-row tiles (SISO, MIMO sub-chunks) and 128-row tiles, with and
+# without the B / C normalisation, on both prefill paths
+@pytest.mark.parametrize("with_bc", [False, True])
+@pytest.mark.parametrize("io,Bt,H,T,P,N,R,Q", [
+    ("bf16", 1, 8, 300, 64, 128, 1, 64),
+    ("bf16", 1, 4, 200, 64, 64, 4, 64),
+    ("bf16", 2, 4, 333, 64, 128, 1, 128),
+    ("bf16", 1, 4, 129, 64, 128, 2, 64),
+    ("fp32", 1, 2, 256, 16, 16, 1, 64),
+    ("fp32", 2, 3, 77, 32, 64, 2, 64),
+])
+def test_scan_prep_gate(io, Bt, H, T, P, N, R, Q, with_bc):
+    w = synth.Workload("case", Bt, H, T, P, N, R, Q, io)
+    inp = synth.make_prep_inputs(w, seed=T + N)
+    z = synth.make_gate(tuple(inp["x"].shape), io=io, seed=T)
+    bc = _bc_case("norm", H, R, N) if with_bc else None
+    y, fin, _ = _run(inp, R, Q, bc=bc, z=z)
+    yr, hr, _ = _oracle(inp, bc=bc, z=z)
+    assert_close(y, yr, TOL[io], "gated y")
+    assert_close(fin, hr, TOL[io], "final_state (the gate leaves the state alone)")
 
 
 # ---------------------------------------------------------------------------
@@ -193,7 +216,7 @@ def test_scan_prep_full_workload_sampled(wl, samples, bc_kind):
 
 # ---------------------------------------------------------------------------
 # m3_decode_step_prep
-@pytest.mark.parametrize("bc_kind", [None, "norm"])
+@pytest.mark.parametrize("bc_kind", [None, "norm", "norm+gate"])
 @pytest.mark.parametrize("io", ["fp32", "bf16"])
 @pytest.mark.parametrize("b,H,P,N,R", [(3, 2, 16, 16, 1), (2, 3, 64, 128, 1), (2, 2, 64, 128, 4), (2, 1, 16, 32, 8),
                                        (64, 4, 64, 128, 1), (2, 1, 4, 2, 1)])
@@ -201,8 +224,10 @@ def test_decode_prep_steps(io, b, H, P, N, R, bc_kind):
     steps = 10
     st = synth.make_decode_state(b, H, N, P, seed=1)
     ins = synth.make_decode_prep_steps(b, H, P, N, R, steps, io=io, seed=2)
-    bc = _bc_case(bc_kind, H, R, N)
+    gate = bc_kind == "norm+gate"
+    bc = _bc_case("norm" if gate else bc_kind, H, R, N)
     bcd, bcf = _bc_dev(bc), _bc_f64(bc)
+    zs = synth.make_gate((steps, b, H, R, P), io=io, seed=5) if gate else None
     state = st.cuda()
     cache = binding.new_decode_cache(b, H, N, P, R, synth.io_torch_dtype(io), "cuda")
     cache.copy_(torch.randn(cache.shape, generator=torch.Generator().manual_seed(3)).to(cache.dtype))
@@ -211,10 +236,13 @@ def test_decode_prep_steps(io, b, H, P, N, R, bc_kind):
     for t in range(steps):
         x_t, B_t, C_t, dr_t, A_t, u_t, om_t = [ins[k][t].cuda().contiguous()
                                                for k in ("x", "B", "C", "dt_raw", "A", "u", "omega")]
-        y = binding.decode_step_prep(state, x_t, B_t, cache, C_t, dr_t, A_t, u_t, om_t, R, dt_bias=bias, bc=bcd)
+        z_t = None if zs is None else zs[t].cuda().contiguous()
+        y = binding.decode_step_prep(state, x_t, B_t, cache, C_t, dr_t, A_t, u_t, om_t, R, dt_bias=bias, bc=bcd,
+                                     z_t=z_t)
         yr, h_ref, prev_ref = oracle.decode_step_prep(h_ref, ins["x"][t], ins["B"][t], prev_ref, ins["C"][t],
                                                       ins["dt_raw"][t], ins["dt_bias"], ins["A"][t], ins["u"][t],
-                                                      ins["omega"][t], bc=bcf)
+                                                      ins["omega"][t], bc=bcf,
+                                                      z_t=None if zs is None else oracle.f64(zs[t]))
         torch.cuda.synchronize()
         assert_close(y, yr, TOL[io], f"y step {t}")
     assert_close(state, h_ref, TOL[io], "state")

@@ -315,3 +315,30 @@ def test_bc_mutants_fail_a_pin(mutant, monkeypatch):
         except AssertionError:
             failed += 1
     assert failed > 0
+
+
+# ---------------------------------------------------------------------------
+# output gate y * silu(z)
+def test_silu_closed_forms():
+    z = np.linspace(-20.0, 20.0, 81)
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-16
+    assert np.max(np.abs(oracle.silu(z) - oracle.silu(-z) - z)) < 1e-13      # silu(z) - silu(-z) = z
+    assert np.max(np.abs(oracle.silu(z) - z * oracle.sigmoid(z))) == 0.0
+    assert abs(oracle.silu(-800.0)) == 0.0 and oracle.silu(800.0) == 800.0
+
+
+def test_gate_multiplies_each_output_element():
+    """The gate acts elementwise on y and leaves the state alone: with z = 0 the output
+    vanishes, with a positive constant z = c it is y * silu(c)."""
+    inp = _prep_inputs(T=13, R=2, seed=16)
+    raw = inp["raw"]
+    args = [raw[k] for k in ("x", "B", "C", "dt_raw", "dt_bias", "A", "u", "omega")]
+    y, h, _ = oracle.scan_prep(*args)
+    y0, h0, _ = oracle.scan_prep(*args, z=np.zeros(y.shape))
+    assert np.max(np.abs(y0)) == 0.0 and np.array_equal(h0, h)
+    yc, _, _ = oracle.scan_prep(*args, z=np.full(y.shape, 0.7))
+    assert oracle.rel_err(yc, y * (0.7 / (1.0 + math.exp(-0.7)))) < 1e-14
+    zz = np.random.default_rng(2).standard_normal(y.shape)
+    yz, _, _ = oracle.scan_prep(*args, z=zz)
+    assert oracle.rel_err(yz, y * zz / (1.0 + np.exp(-zz))) < 1e-14
