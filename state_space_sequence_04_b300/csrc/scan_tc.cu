@@ -14,13 +14,14 @@
 //   rotation       Psi_t = sum_{k<=t} dt_k omega_k (chunk-local),
 //                  C~ = R(-Psi) C,  B' = w R(-Psi) B   (in place in shared memory)
 //                  X^ = exp(cum_end - cum_s) X          (separate buffer)
-//   batch 1        S  = C~ B'^T                       (= S_ts w_s; committed first)
-//                  H += B'^T X^                        (chunk state onto the carry)
-//                  Yi = C~ Hb_{c-1}                    (inter-chunk readout)
+//   batch 1        H += B'^T X^                        (chunk state onto the carry)
+//                  S  = C~ B'^T                       (= S_ts w_s)
 //   mask           SL_ts = S_ts exp(cum_t - cum_s) for s < t, S_tt rho_t, 0 for s > t
-//   batch 2        Y  = SL X
-//   state          H_c = exp(cum_end(c+1)) R(Theta_c) H,  Hb_c = bf16(R(Theta_c) H)
+//                  (bf16, written over X^, which batch 1 has consumed)
+//   batch 2        Yi = C~ Hb_{c-1}                    (inter-chunk readout)
+//                  Y  = SL X
 //   output         y_t = Y_t + exp(cum_t) Yi_t
+//   state          H_c = exp(cum_end(c+1)) R(Theta_c) H,  Hb_c = bf16(R(Theta_c) H)
 //
 // The carry H entering batch 1 of chunk c is exp(cum_end(c)) R(Theta_{c-1}) H_{c-1}
 // (the decay of chunk c applied ahead of time by the previous state step), so
@@ -33,10 +34,14 @@
 // Warp roles (256 threads): warps 0-3 "consumer" (mask, state, output; thread
 // 0 issues every MMA and the C/B and X loads), warps 4-7 "rotate"
 // (coefficients, angles, rotation, X^, the dt/lambda loads), which run one
-// chunk ahead of the consumer on the other shared-memory stage.  The next
-// chunk's score MMA is issued as soon as its operands are rotated, so that it
-// overlaps the current chunk's state step and output.  Every wait is bounded: on timeout the kernel records
-// M3_ERR_TIMEOUT in the status word, drains its copies and MMAs and exits.
+// chunk ahead of the consumer on the other shared-memory stage.  Every wait is
+// bounded: on timeout the kernel records M3_ERR_TIMEOUT in the status word,
+// drains its copies and MMAs and exits.
+//
+// Kernel modes (template bitmask PM) for the pre-activation entry point: bit 0
+// takes Delta and lambda as pre-activations and one decay generator per token,
+// bit 1 RMS-normalises and biases B and C in the rotation, bit 2 gates the
+// output; mode 0 is the plain kernel.
 //
 // MMA operand layouts (all 128-byte swizzled, bf16):
 //   C~   A, K-major  (rows (t,r), K = n)     B'  B, K-major (rows (s,r), K = n)
@@ -50,7 +55,7 @@
 // with M = 128 (row r in lane r).  The chunk-state MMA always has M = 128
 // (state rows n); with N = 64 its rows 64..127 read the next QR*128 bytes of
 // shared memory (inside this CTA's allocation) and are never read.  SL is
-// written over C~ (dead once batch 1 is done).
+// written over X^ (dead once batch 1 is done; C~ is still read by batch 2).
 #include <cuda.h>
 
 #include "m3_common.cuh"
