@@ -49,12 +49,24 @@ struct DecodeOcc {   // resident CTAs per SM the register budget is sized for (2
     static constexpr int value = R == 1 ? 4 : (R == 2 ? 3 : (R == 4 ? M3_DECODE_OCC_R4 : 2));
 };
 
+// The pre-activation options as a kernel parameter: the Prep descriptor for the
+// *_prep entry point, an empty struct for the plain kernels (whose parameter
+// block, and so their code, then stays as it is).
+template <bool ON>
+struct DecodeExt {
+    Prep p;
+};
+template <>
+struct DecodeExt<false> {};
+
 // Delta, lambda and A of unit bh = batch * H + h: as given (A per head), or from the
 // pre-activations of the *_prep entry points (A per unit).
-__device__ __forceinline__ void unit_params(const float* dt_t, const float* lam_t, const float* A, const Prep& prep,
-                                            int64_t bh, int H, float& d, float& l, float& a) {
-    if (prep.on) {
-        d = softplus_f(dt_t[bh] + (prep.dt_bias != nullptr ? prep.dt_bias[bh % H] : 0.f));
+template <bool PREP>
+__device__ __forceinline__ void unit_params(const float* dt_t, const float* lam_t, const float* A,
+                                            const DecodeExt<PREP>& ext, int64_t bh, int H, float& d, float& l,
+                                            float& a) {
+    if constexpr (PREP) {
+        d = softplus_f(dt_t[bh] + (ext.p.dt_bias != nullptr ? ext.p.dt_bias[bh % H] : 0.f));
         l = sigmoid_f(lam_t[bh]);
         a = A[bh];
     } else {
@@ -126,12 +138,12 @@ __device__ void bc_rows(float* sB2f, float* sC2f, float* sBp2f, int R, int N, in
     }
 }
 
-template <typename IO, int R>
+template <typename IO, int R, bool PREP>
 __global__ void __launch_bounds__(256, DecodeOcc<R>::value) decode_kernel(
     float* __restrict__ state, const IO* __restrict__ x_t, const IO* __restrict__ B_t,
     IO* __restrict__ cache, const IO* __restrict__ C_t, const float* __restrict__ dt_t,
     const float* __restrict__ A, const float* __restrict__ lam_t, const float* __restrict__ omega_t,
-    IO* __restrict__ y_t, int H, int P, int N, int G, const Prep prep) {
+    IO* __restrict__ y_t, int H, int P, int N, int G, const DecodeExt<PREP> ext) {
     extern __shared__ __align__(16) float sm[];
     const int64_t bh = blockIdx.x;
     const int P4 = P >> 2, NP2 = N >> 1;
@@ -163,7 +175,7 @@ __global__ void __launch_bounds__(256, DecodeOcc<R>::value) decode_kernel(
     load_slab(0);
 
     float d, l, a;
-    unit_params(dt_t, lam_t, A, prep, bh, H, d, l, a);
+    unit_params<PREP>(dt_t, lam_t, A, ext, bh, H, d, l, a);
     const float alpha = expf(d * a);
     const float beta = (1.0f - l) * d * alpha;
     const float gamma = l * d;
@@ -193,9 +205,11 @@ __global__ void __launch_bounds__(256, DecodeOcc<R>::value) decode_kernel(
         sCS[j] = make_float2(cs, sn);
     }
     __syncthreads();
-    if (prep.bc()) {
-        bc_rows(sB2f, sC2f, sBp2f, R, N, (int)(bh % H), prep);
-        __syncthreads();
+    if constexpr (PREP) {
+        if (ext.p.bc()) {
+            bc_rows(sB2f, sC2f, sBp2f, R, N, (int)(bh % H), ext.p);
+            __syncthreads();
+        }
     }
     // The old cache is in shared memory now: replace it with this token's factors.
     for (int i = tid; i < R * N; i += nt) cb[i] = Bb[i];
@@ -277,7 +291,8 @@ __global__ void __launch_bounds__(256, DecodeOcc<R>::value) decode_kernel(
     }
     __syncthreads();
     IO* yb = y_t + bh * R * P;
-    const IO* zb = prep.z != nullptr ? static_cast<const IO*>(prep.z) + bh * R * P : nullptr;
+    const IO* zb = nullptr;
+    if constexpr (PREP) zb = ext.p.z != nullptr ? static_cast<const IO*>(ext.p.z) + bh * R * P : nullptr;
     for (int o = tid; o < R * P; o += nt) {
         float s = 0.f;
         for (int gg = 0; gg < rows; ++gg) s += sRed[gg * (R * P) + o];
@@ -322,12 +337,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-template <typename IO, int R>
+template <typename IO, int R, bool PREP>
 __global__ void __launch_bounds__(256, 2) decode_stream_kernel(
     float* __restrict__ state, const IO* __restrict__ x_t, const IO* __restrict__ B_t,
     IO* __restrict__ cache, const IO* __restrict__ C_t, const float* __restrict__ dt_t,
     const float* __restrict__ A, const float* __restrict__ lam_t, const float* __restrict__ omega_t,
-    IO* __restrict__ y_t, int H, int P, int N, int G, int64_t units, int nslots, const Prep prep) {
+    IO* __restrict__ y_t, int H, int P, int N, int G, int64_t units, int nslots, const DecodeExt<PREP> ext) {
     extern __shared__ __align__(128) uint8_t smraw[];
     const int P4 = P >> 2, NP2 = N >> 1;
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -373,14 +388,14 @@ __global__ void __launch_bounds__(256, 2) decode_stream_kernel(
     const int c4 = tid % P4, g = tid / P4;
     // scalars of the first unit; later units' are prefetched one unit ahead
     float d_n = 0.f, l_n = 0.f, a_n = 0.f;
-    if (first < units) unit_params(dt_t, lam_t, A, prep, first, H, d_n, l_n, a_n);
+    if (first < units) unit_params<PREP>(dt_t, lam_t, A, ext, first, H, d_n, l_n, a_n);
     int it = 0;
     for (int64_t u = first; u < units; u += step, ++it) {
         const int slot = it % nslots;
         const uint32_t parity = (uint32_t)((it / nslots) & 1);
         const float d = d_n, l = l_n, a = a_n;
         const int64_t un = u + step;
-        if (un < units) unit_params(dt_t, lam_t, A, prep, un, H, d_n, l_n, a_n);
+        if (un < units) unit_params<PREP>(dt_t, lam_t, A, ext, un, H, d_n, l_n, a_n);
         if (!tc::mbar_wait(&bars[slot], parity, kStreamWaitNs)) *sFail = 1;
         __syncthreads();
         if (*sFail) break;
@@ -416,9 +431,11 @@ __global__ void __launch_bounds__(256, 2) decode_stream_kernel(
             sCS[j] = make_float2(cs, sn);
         }
         __syncthreads();
-        if (prep.bc()) {
-            bc_rows(sB2f, sC2f, sBp2f, R, N, (int)(u % H), prep);
-            __syncthreads();
+        if constexpr (PREP) {
+            if (ext.p.bc()) {
+                bc_rows(sB2f, sC2f, sBp2f, R, N, (int)(u % H), ext.p);
+                __syncthreads();
+            }
         }
         // new delayed-write cache: this token's B_t then X_t (raw io values)
         IO* cb = cache + u * (int64_t)R * (N + P);
@@ -489,7 +506,8 @@ __global__ void __launch_bounds__(256, 2) decode_stream_kernel(
             if (u3 < units) issue(u3, slot);
         }
         IO* yb = y_t + u * R * P;
-        const IO* zb = prep.z != nullptr ? static_cast<const IO*>(prep.z) + u * R * P : nullptr;
+        const IO* zb = nullptr;
+        if constexpr (PREP) zb = ext.p.z != nullptr ? static_cast<const IO*>(ext.p.z) + u * R * P : nullptr;
         for (int o = tid; o < R * P; o += nt) {
             float s = 0.f;
             for (int gg = 0; gg < rows; ++gg) s += sRed[gg * (R * P) + o];
@@ -552,10 +570,11 @@ DecodeShape decode_shape(int64_t P, int64_t N, int R) {
     return s;
 }
 
-template <typename IO, int R>
-cudaError_t launch_t(float* state, const void* x_t, const void* B_t, void* cache, const void* C_t,
+template <typename IO, int R, bool PREP>
+cudaError_t launch_p(float* state, const void* x_t, const void* B_t, void* cache, const void* C_t,
                      const float* dt_t, const float* A, const float* lambda_t, const float* omega_t, void* y_t,
-                     int64_t batch, int64_t nheads, int64_t P, int64_t N, const Prep& prep, cudaStream_t stream) {
+                     int64_t batch, int64_t nheads, int64_t P, int64_t N, const DecodeExt<PREP>& ext,
+                     cudaStream_t stream) {
     const DecodeShape s = decode_shape(P, N, R);
     const int64_t units = batch * nheads;
     const int es = (int)sizeof(IO);
@@ -565,26 +584,37 @@ cudaError_t launch_t(float* state, const void* x_t, const void* B_t, void* cache
         size_t smem = stream_smem(P, N, R, es, s.G, nslots);
         if (smem > 110 * 1024) smem = stream_smem(P, N, R, es, s.G, nslots = 2);
         if (smem <= 110 * 1024) {
-            auto kern = decode_stream_kernel<IO, R>;
+            auto kern = decode_stream_kernel<IO, R, PREP>;
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
             int64_t grid = 2 * (int64_t)device_sms();
             if (grid > units) grid = units;
             kern<<<(unsigned)grid, s.threads, smem, stream>>>(
                 state, (const IO*)x_t, (const IO*)B_t, (IO*)cache, (const IO*)C_t, dt_t, A, lambda_t, omega_t,
-                (IO*)y_t, (int)nheads, (int)P, (int)N, s.G, units, nslots, prep);
+                (IO*)y_t, (int)nheads, (int)P, (int)N, s.G, units, nslots, ext);
             return cudaGetLastError();
         }
     }
-    auto kern = decode_kernel<IO, R>;
+    auto kern = decode_kernel<IO, R, PREP>;
     if (s.smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s.smem);
         if (e != cudaSuccess) return e;
     }
     kern<<<(unsigned)units, s.threads, s.smem, stream>>>(
         state, (const IO*)x_t, (const IO*)B_t, (IO*)cache, (const IO*)C_t, dt_t, A, lambda_t, omega_t, (IO*)y_t,
-        (int)nheads, (int)P, (int)N, s.G, prep);
+        (int)nheads, (int)P, (int)N, s.G, ext);
     return cudaGetLastError();
+}
+
+template <typename IO, int R>
+cudaError_t launch_t(float* state, const void* x_t, const void* B_t, void* cache, const void* C_t,
+                     const float* dt_t, const float* A, const float* lambda_t, const float* omega_t, void* y_t,
+                     int64_t batch, int64_t nheads, int64_t P, int64_t N, const Prep& prep, cudaStream_t stream) {
+    if (prep.on)
+        return launch_p<IO, R, true>(state, x_t, B_t, cache, C_t, dt_t, A, lambda_t, omega_t, y_t, batch, nheads, P,
+                                     N, DecodeExt<true>{prep}, stream);
+    return launch_p<IO, R, false>(state, x_t, B_t, cache, C_t, dt_t, A, lambda_t, omega_t, y_t, batch, nheads, P, N,
+                                  DecodeExt<false>{}, stream);
 }
 
 template <typename IO>
