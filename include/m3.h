@@ -250,6 +250,35 @@ M3_API int m3_decode_step_prep(float* state, const void* x_t, const void* B_t, v
                                int64_t dstate, int R, int io_dtype, const m3_prep_params* params, void* stream);
 
 /*
+ * Backward pass of m3_scan_fwd (training): the gradients of a loss L with
+ * respect to every input, given dy = dL/dy and d_final = dL/d final_state.
+ * The adjoint of the recurrence runs backwards in time (dL/dh_t =
+ * C_t dy_t^T + alpha_{t+1} R(phi_{t+1})^T dL/dh_{t+1}), with the chain rule
+ * through Eq. 6's alpha, beta, gamma and the angle phi = Delta omega; the
+ * chunked algorithm's backward is the use of section 3.3 for training.
+ *
+ *   x, B, C, dt, A, lambda, omega, R, sizes, io_dtype: as m3_scan_fwd
+ *   dy        [batch, T, H, R, P] io dtype
+ *   d_final   [batch, H, N, P] fp32, nullable (= 0)
+ *   dx        out [batch, T, H, R, P] fp32;  dB, dC  out [batch, T, H, R, N] fp32
+ *   ddt, dlambda  out [batch, T, H] fp32;  domega  out [batch, T, H, N/2] fp32
+ *   dA        out [H] fp32 (summed over batch and tokens)
+ *   workspace: m3_scan_bwd_workspace_size bytes (every forward state,
+ *            batch * H * T * N * P fp32), 256-byte aligned.
+ * One CTA per (batch, head) on CUDA cores: a forward pass stores every state,
+ * then the adjoint runs from the last token to the first.  Sizes: R in
+ * {1, 2, 4, 8}; P in {4, 8, 16, 32, 64, 128}; N even, <= 256, with at most 8
+ * state pairs per thread; otherwise M3_ERR_UNSUPPORTED.  Errors as m3_scan_fwd.
+ */
+M3_API size_t m3_scan_bwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                                         int64_t dstate, int R, int io_dtype);
+M3_API int m3_scan_bwd(const void* x, const void* B, const void* C, const float* dt, const float* A,
+                       const float* lambda, const float* omega, int R, const void* dy, const float* d_final,
+                       float* dx, float* dB, float* dC, float* ddt, float* dA, float* dlambda, float* domega,
+                       int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+                       int io_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Sticky device-side error word of m3_decode_step, which takes no workspace:
  * M3_OK, or M3_ERR_TIMEOUT once a bounded wait inside a decode kernel gave up
  * (the outputs of that call are then not valid).  Reading it synchronises

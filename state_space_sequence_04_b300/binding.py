@@ -53,6 +53,9 @@ SIGNATURES = {
     "m3_decode_step": ([_fp, _vp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp,
                         _i64, _i64, _i64, _i64, _int, _int, _vp], _int),
     "m3_device_status": ([_int], _int),
+    "m3_scan_bwd_workspace_size": ([_i64, _i64, _i64, _i64, _i64, _int, _int], _sz),
+    "m3_scan_bwd": ([_vp, _vp, _vp, _fp, _fp, _fp, _fp, _int, _vp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp,
+                     _i64, _i64, _i64, _i64, _i64, _int, _vp, _sz, _vp], _int),
     "m3_scan_fwd_prep_workspace_size": ([_i64, _i64, _i64, _i64, _i64, _int, _int, _int], _sz),
     "m3_scan_fwd_prep": ([_vp, _vp, _vp, _fp, _fp, _fp, _fp, _int, _int, _vp, _fp,
                           _i64, _i64, _i64, _i64, _i64, _int, ctypes.POINTER(PrepParams), _vp, _sz, _vp], _int),
@@ -214,6 +217,40 @@ def m3_decode_step_prep(state, x_t, B_t, cache, C_t, dt_raw_t, A_t, u_t, omega_t
         _ptr(C_t, x_t.dtype), _ptr(dt_raw_t, torch.float32), _ptr(A_t, torch.float32), _ptr(u_t, torch.float32),
         _ptr(omega_t, torch.float32), _ptr(y_t, x_t.dtype), b, H, P, N, int(R), io,
         None if params is None else ctypes.byref(params), _stream(stream)))
+
+
+def m3_scan_bwd_workspace_size(batch, seqlen, nheads, headdim, dstate, R, io) -> int:
+    return int(load().m3_scan_bwd_workspace_size(batch, seqlen, nheads, headdim, dstate, R, io))
+
+
+def m3_scan_bwd(x, B, C, dt, A, lam, omega, R: int, dy, d_final, grads: dict, workspace, stream=None) -> int:
+    """Call m3_scan_bwd; ``grads`` holds the fp32 outputs dx, dB, dC, ddt, dA, dlam, domega.
+    Returns the status code."""
+    Bt, T, H, R_, P = x.shape
+    N = B.shape[-1]
+    io = io_code(x.dtype)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    f = torch.float32
+    return int(load().m3_scan_bwd(
+        _ptr(x, x.dtype), _ptr(B, x.dtype), _ptr(C, x.dtype), _ptr(dt, f), _ptr(A, f), _ptr(lam, f), _ptr(omega, f),
+        int(R), _ptr(dy, x.dtype), _ptr(d_final, f), _ptr(grads["dx"], f), _ptr(grads["dB"], f), _ptr(grads["dC"], f),
+        _ptr(grads["ddt"], f), _ptr(grads["dA"], f), _ptr(grads["dlam"], f), _ptr(grads["domega"], f),
+        Bt, T, H, P, N, io, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def scan_bwd(x, B, C, dt, A, lam, omega, R: int, dy, d_final=None, workspace=None, stream=None) -> dict:
+    """Backward pass of scan_fwd: fp32 gradients dx, dB, dC, ddt, dA, dlam, domega."""
+    Bt, T, H, _, P = x.shape
+    N = B.shape[-1]
+    f = dict(dtype=torch.float32, device=x.device)
+    grads = {"dx": torch.empty(x.shape, **f), "dB": torch.empty(B.shape, **f), "dC": torch.empty(C.shape, **f),
+             "ddt": torch.empty(dt.shape, **f), "dA": torch.empty(A.shape, **f), "dlam": torch.empty(lam.shape, **f),
+             "domega": torch.empty(omega.shape, **f)}
+    if workspace is None:
+        nbytes = m3_scan_bwd_workspace_size(Bt, T, H, P, N, R, io_code(x.dtype))
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device)
+    _check(m3_scan_bwd(x, B, C, dt, A, lam, omega, R, dy, d_final, grads, workspace, stream), "m3_scan_bwd")
+    return grads
 
 
 def m3_device_status(clear: bool = False) -> int:

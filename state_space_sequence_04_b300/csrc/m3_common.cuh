@@ -98,4 +98,12 @@ cudaError_t launch_scan_simt(const ScanDims& d, const void* x, const void* B, co
                              const float* A, const float* lambda, const float* omega, void* y,
                              float* final_state, void* workspace, const Prep& prep, cudaStream_t stream);
 
+// Backward pass (CUDA cores, fp32): workspace holds every forward state.
+bool bwd_supported(const ScanDims& d);
+size_t bwd_workspace_size(const ScanDims& d);
+cudaError_t launch_scan_bwd(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
+                            const float* A, const float* lambda, const float* omega, const void* dy,
+                            const float* d_final, float* dx, float* dB, float* dC, float* ddt, float* dA,
+                            float* dlambda, float* domega, void* workspace, cudaStream_t stream);
+
 }  // namespace m3

@@ -1,0 +1,118 @@
+"""GPU-vs-oracle parity of the backward pass (m3_scan_bwd).
+
+Small problems: every gradient element against central differences of the
+float64 oracle (``oracle.grad.grad_fd``).  Larger problems: the loss is linear
+in x, in B and in C, so along a random step d the loss changes by exactly
+<grad, d> (two oracle evaluations); along dt, lambda, omega and A the
+directional derivative by central differences.  Tolerances: the kernel
+computes in fp32 (and reads bf16 inputs as given), the references are
+float64; errors are measured relative to the largest reference value.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import grad
+from state_space_sequence_04_b300 import binding, synth
+
+from parity_util import KEYS, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+TOL_BWD = {"fp32": 2e-4, "bf16": 2e-3}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _run(inp, R, dy, dfin=None):
+    d = {k: inp[k].cuda().contiguous() for k in KEYS}
+    g = binding.scan_bwd(*[d[k] for k in KEYS], R, dy.cuda().contiguous(),
+                         None if dfin is None else dfin.cuda().contiguous())
+    torch.cuda.synchronize()
+    return {k: v.cpu().double().numpy() for k, v in g.items()}
+
+
+def _ref_inputs(inp):
+    return {"x": oracle.f64(inp["x"]), "B": oracle.f64(inp["B"]), "C": oracle.f64(inp["C"]), "dt": oracle.f64(inp["dt"]),
+            "A": oracle.f64(inp["A"]), "lam": oracle.f64(inp["lam"]), "omega": oracle.f64(inp["omega"])}
+
+
+NAMES = {"x": "dx", "B": "dB", "C": "dC", "dt": "ddt", "A": "dA", "lam": "dlam", "omega": "domega"}
+
+
+@pytest.mark.parametrize("io,Bt,H,T,P,N,R", [
+    ("fp32", 1, 2, 9, 4, 4, 1),
+    ("fp32", 2, 1, 7, 8, 6, 2),
+    ("fp32", 1, 2, 6, 4, 8, 4),
+    ("bf16", 1, 2, 8, 4, 4, 2),
+])
+@pytest.mark.parametrize("with_final", [False, True])
+def test_bwd_small_every_element(io, Bt, H, T, P, N, R, with_final):
+    w = synth.Workload("case", Bt, H, T, P, N, R, 64, io)
+    inp = synth.make_inputs(w, seed=T + N + R)
+    gen = torch.Generator().manual_seed(3)
+    dy = torch.randn(inp["x"].shape, generator=gen).to(inp["x"].dtype)
+    dfin = torch.randn((Bt, H, N, P), generator=gen) if with_final else None
+    got = _run(inp, R, dy, dfin)
+    ref = grad.grad_fd(_ref_inputs(inp), oracle.f64(dy), None if dfin is None else oracle.f64(dfin))
+    for k, name in NAMES.items():
+        err = oracle.rel_err(got[name], ref[k])
+        assert err < TOL_BWD[io], f"{name}: {err:.2e}"
+
+
+@pytest.mark.parametrize("io,Bt,H,T,P,N,R", [
+    ("fp32", 1, 2, 150, 64, 128, 1),
+    ("bf16", 2, 2, 200, 64, 64, 4),
+    ("fp32", 1, 4, 96, 32, 64, 2),
+])
+def test_bwd_larger_directional(io, Bt, H, T, P, N, R):
+    w = synth.Workload("case", Bt, H, T, P, N, R, 64, io)
+    inp = synth.make_inputs(w, seed=7)
+    gen = torch.Generator().manual_seed(5)
+    dy = torch.randn(inp["x"].shape, generator=gen).to(inp["x"].dtype)
+    dfin = torch.randn((Bt, H, N, P), generator=gen)
+    got = _run(inp, R, dy, dfin)
+    ref = _ref_inputs(inp)
+    dy64, df64 = oracle.f64(dy), oracle.f64(dfin)
+    rng = np.random.default_rng(9)
+    l0 = grad.loss(ref, dy64, df64)
+    for k in ("x", "B", "C"):   # exact: the loss is linear in each of them
+        d = rng.standard_normal(ref[k].shape)
+        moved = dict(ref)
+        moved[k] = ref[k] + d
+        exact = grad.loss(moved, dy64, df64) - l0
+        kern = float(np.sum(got[NAMES[k]] * d))
+        assert abs(kern - exact) <= TOL_BWD[io] * max(1.0, abs(exact)), (k, kern, exact)
+    for k in ("dt", "lam", "omega", "A"):
+        d = rng.standard_normal(ref[k].shape)
+        if k == "lam":   # stay inside [0, 1]
+            d = d * np.minimum(ref[k], 1.0 - ref[k])
+        if k == "dt":
+            d = d * ref[k]
+        num = grad.directional(ref, k, d, dy64, df64, eps=1e-6)
+        kern = float(np.sum(got[NAMES[k]] * d))
+        assert abs(kern - num) <= TOL_BWD[io] * max(1.0, abs(num)), (k, kern, num)
+
+
+def test_bwd_rejects_unsupported_and_bad_arguments():
+    assert binding.m3_scan_bwd_workspace_size(1, 8, 2, 12, 16, 1, 1) == 0          # P = 12: not a power of two / 4
+    w = synth.Workload("case", 1, 2, 8, 4, 4, 1, 64, "fp32")
+    d = {k: v.cuda() for k, v in synth.make_inputs(w, seed=1).items() if k in KEYS}
+    dy = torch.zeros_like(d["x"])
+    f = dict(dtype=torch.float32, device="cuda")
+    grads = {"dx": torch.empty(d["x"].shape, **f), "dB": torch.empty(d["B"].shape, **f),
+             "dC": torch.empty(d["C"].shape, **f), "ddt": torch.empty(d["dt"].shape, **f),
+             "dA": torch.empty(d["A"].shape, **f), "dlam": torch.empty(d["lam"].shape, **f),
+             "domega": torch.empty(d["omega"].shape, **f)}
+    ws = torch.empty(binding.m3_scan_bwd_workspace_size(1, 8, 2, 4, 4, 1, 1), dtype=torch.uint8, device="cuda")
+    args = [d[k] for k in KEYS]
+    assert binding.m3_scan_bwd(*args, 1, dy, None, grads, ws) == binding.M3_OK
+    assert binding.m3_scan_bwd(*args, 1, dy, None, grads, ws[:64]) == binding.M3_ERR_WORKSPACE
+    grads2 = dict(grads)
+    grads2["dB"] = None
+    assert binding.m3_scan_bwd(*args, 1, dy, None, grads2, ws) == binding.M3_ERR_INVALID_ARG
+    torch.cuda.synchronize()

@@ -1,0 +1,116 @@
+"""Pins of the finite-difference gradients of the oracle (backward-pass reference).
+
+The finite differences are pinned against exact results that do not come from
+differencing: the output is linear in x, in B and in C (for fixed other
+inputs), so along those inputs the loss changes exactly by the inner product
+of the gradient with the step; along C the gradient has the closed form
+dL/dC_t[r, n] = sum_p h_t[n, p] dy_t[r, p] (the readout Y_t = h_t^T C_t of
+section 3.3); along x it is M^T dy for the linear map M that the independent
+masked-score evaluation of ``forms.matrix_form`` materialises; and along the
+scalar parameters of one real pair over two steps it is the derivative of a
+hand-written closed form of the exponential-trapezoidal step (Eq. 6).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import forms, grad
+from state_space_sequence_04_b300 import synth
+
+
+def _inp(Bt=1, H=2, T=9, P=3, N=4, R=2, seed=0):
+    w = synth.Workload("g", Bt, H, T, P, N, R, 8, "fp32")
+    d = synth.make_inputs(w, seed=seed)
+    return {k: oracle.f64(d[k]) for k in grad.INPUTS}
+
+
+def _dy(inp, seed=1):
+    return np.random.default_rng(seed).standard_normal(inp["x"].shape)
+
+
+def test_grad_x_equals_transposed_matrix_form():
+    inp = _inp(T=7, seed=3)
+    dy = _dy(inp)
+    g = grad.grad_fd(inp, dy, keys=("x",))["x"]
+    # M x via the independent masked-score form: column i = M e_i
+    x = inp["x"]
+    M = np.zeros((dy.size, x.size))
+    args = [inp[k] for k in grad.INPUTS]
+    for i in range(x.size):
+        e = np.zeros(x.size)
+        e[i] = 1.0
+        args[0] = e.reshape(x.shape)
+        M[:, i] = forms.matrix_form(*args).reshape(-1)
+    ref = (M.T @ dy.reshape(-1)).reshape(x.shape)
+    assert np.max(np.abs(g - ref)) < 1e-8 * max(1.0, np.max(np.abs(ref)))
+
+
+def test_grad_C_closed_form():
+    inp = _inp(T=6, seed=4)
+    dy = _dy(inp, seed=2)
+    g = grad.grad_fd(inp, dy, keys=("C",))["C"]
+    Bt, T, H, R, P = inp["x"].shape
+    ref = np.zeros_like(inp["C"])
+    for t in range(T):
+        pre = [a[:, :t + 1] if a.ndim >= 3 else a for a in (inp[k] for k in grad.INPUTS)]
+        _, h_t, _ = oracle.scan(*pre)                      # [Bt,H,N,P]
+        ref[:, t] = np.einsum("bhnp,bhrp->bhrn", h_t, dy[:, t])
+    assert np.max(np.abs(g - ref)) < 1e-8
+
+
+@pytest.mark.parametrize("key", ["x", "B", "C"])
+def test_linear_inputs_exact_inner_product(key):
+    """L is linear in x, in B and in C: L(v + d) - L(v) = <dL/dv, d> exactly (and with
+    a final-state seed as well)."""
+    inp = _inp(T=8, seed=5)
+    dy = _dy(inp, seed=6)
+    dfin = np.random.default_rng(7).standard_normal((1, 2, 4, 3))
+    g = grad.grad_fd(inp, dy, dfin, keys=(key,))[key]
+    d = np.random.default_rng(8).standard_normal(inp[key].shape)
+    l0 = grad.loss(inp, dy, dfin)
+    moved = dict(inp)
+    moved[key] = inp[key] + d
+    assert abs(grad.loss(moved, dy, dfin) - l0 - float(np.sum(g * d))) < 1e-7
+
+
+def test_two_steps_scalar_parameters_closed_form():
+    """One real pair, rank 1, B = (1, 0), C = (0, 1), x0 then x1, only dy_1 = 1:
+    y_1 = sin(phi_1) (alpha_1 gamma_0 + beta_1) x_0 with alpha_1 = exp(d1 a),
+    beta_1 = (1 - l1) d1 alpha_1, gamma_0 = l0 d0, phi_1 = d1 w1."""
+    d0, d1, a, l0, l1, w0, w1, x0, x1 = 0.4, 0.7, -0.9, 0.35, 0.6, 0.75, 1.6, 1.7, -0.6
+    inp = {"x": np.array([x0, x1]).reshape(1, 2, 1, 1, 1),
+           "B": np.tile(np.array([1.0, 0.0]), (1, 2, 1, 1, 1)),
+           "C": np.tile(np.array([0.0, 1.0]), (1, 2, 1, 1, 1)),
+           "dt": np.array([d0, d1]).reshape(1, 2, 1), "A": np.array([a]),
+           "lam": np.array([l0, l1]).reshape(1, 2, 1), "omega": np.array([w0, w1]).reshape(1, 2, 1, 1)}
+    dy = np.zeros((1, 2, 1, 1, 1))
+    dy[0, 1] = 1.0
+    g = grad.grad_fd(inp, dy, keys=("dt", "A", "lam", "omega"))
+    al1 = math.exp(d1 * a)
+    be1 = (1 - l1) * d1 * al1
+    g0 = l0 * d0
+    amp = al1 * g0 + be1
+    s1, c1 = math.sin(d1 * w1), math.cos(d1 * w1)
+    # derivatives of y_1 = sin(d1 w1) (al1 l0 d0 + (1 - l1) d1 al1) x0
+    d_d1 = c1 * w1 * amp * x0 + s1 * (a * al1 * g0 + (1 - l1) * (al1 + d1 * a * al1)) * x0
+    d_d0 = s1 * al1 * l0 * x0
+    d_a = s1 * (d1 * al1 * g0 + (1 - l1) * d1 * d1 * al1) * x0
+    d_l1 = s1 * (-d1 * al1) * x0
+    d_l0 = s1 * al1 * d0 * x0
+    d_w1 = c1 * d1 * amp * x0
+    assert abs(g["dt"][0, 1, 0] - d_d1) < 1e-8 and abs(g["dt"][0, 0, 0] - d_d0) < 1e-8
+    assert abs(g["A"][0] - d_a) < 1e-8
+    assert abs(g["lam"][0, 1, 0] - d_l1) < 1e-8 and abs(g["lam"][0, 0, 0] - d_l0) < 1e-8
+    assert abs(g["omega"][0, 1, 0, 0] - d_w1) < 1e-8 and abs(g["omega"][0, 0, 0, 0]) < 1e-8
+
+
+def test_directional_matches_full_gradient():
+    inp = _inp(T=7, seed=9)
+    dy = _dy(inp, seed=10)
+    g = grad.grad_fd(inp, dy, keys=("dt", "lam", "omega"))
+    rng = np.random.default_rng(11)
+    for k in ("dt", "lam", "omega"):
+        v = rng.standard_normal(inp[k].shape)
+        assert abs(grad.directional(inp, k, v, dy) - float(np.sum(g[k] * v))) < 1e-7
