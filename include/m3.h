@@ -263,12 +263,19 @@ M3_API int m3_decode_step_prep(float* state, const void* x_t, const void* B_t, v
  *   dx        out [batch, T, H, R, P] fp32;  dB, dC  out [batch, T, H, R, N] fp32
  *   ddt, dlambda  out [batch, T, H] fp32;  domega  out [batch, T, H, N/2] fp32
  *   dA        out [H] fp32 (summed over batch and tokens)
- *   workspace: m3_scan_bwd_workspace_size bytes (every forward state,
- *            batch * H * T * N * P fp32), 256-byte aligned.
- * One CTA per (batch, head) on CUDA cores: a forward pass stores every state,
- * then the adjoint runs from the last token to the first.  Sizes: R in
- * {1, 2, 4, 8}; P in {4, 8, 16, 32, 64, 128}; N even, <= 256, with at most 8
- * state pairs per thread; otherwise M3_ERR_UNSUPPORTED.  Errors as m3_scan_fwd.
+ *   workspace: m3_scan_bwd_workspace_size bytes, 256-byte aligned: the
+ *            state entering every chunk of Q tokens (Q = 16 for R <= 2,
+ *            8 for R = 4, 4 for R = 8; batch * H * ceil(T/Q) * N * P fp32)
+ *            and per-pair-block partial sums of dx and of four per-token
+ *            scalars (fp32).
+ * CUDA cores, one CTA per (batch, head, block of state pairs): a forward
+ * sweep stores the chunk checkpoints; the reverse sweep recomputes each
+ * chunk's states from its checkpoint and runs the adjoint from the last token
+ * to the first; a finishing kernel adds the pair blocks' partial sums and
+ * applies the chain rule for dt, lambda and A.  dA is accumulated with
+ * atomics, so its last bits may differ between runs; every other output is
+ * deterministic.  Sizes: R in {1, 2, 4, 8}; P in {4, 8, 16, 32, 64, 128};
+ * N even, <= 256; otherwise M3_ERR_UNSUPPORTED.  Errors as m3_scan_fwd.
  */
 M3_API size_t m3_scan_bwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                                          int64_t dstate, int R, int io_dtype);

@@ -16,12 +16,18 @@
 //   dphi_{t,j} = sum_p (gbar[2j+1] r[2j] - gbar[2j] r[2j+1]),  r = h_t - gamma_t v_t = R(phi_t) u_t,
 // and the chain rule through alpha, beta, gamma, phi to Delta, lambda, A, omega.
 //
-// One CTA per (batch, head) sequence, CUDA cores, fp32 arithmetic: a forward
-// pass stores every state h_t to the workspace, then the adjoint runs from
-// the last token to the first, reading h_t and h_{t-1} back.  Thread layout
-// of the decode kernel: thread (g, c4) holds state rows (2j, 2j+1) of pairs
-// j = g, g + G, ... and columns 4 c4 .. 4 c4 + 3; sums over p combine the P/4
-// lanes of a pair group with shuffles, sums over n go through shared memory.
+// Work split: CTA (batch*head, pair block) owns the state rows (2j, 2j+1) of
+// PB consecutive pairs j and every column p; thread (pair, c4) holds columns
+// 4 c4 .. 4 c4 + 3 of one pair.  Pairs evolve independently (the rotation acts
+// within a pair, the decay is a scalar), so only the sums over n (dX and the
+// per-token scalars dalpha, dbeta, dgamma, sum_j omega_j dphi_j) cross CTAs:
+// each pair block writes partial sums per token, and a finishing kernel adds
+// them and applies the chain rule for Delta, lambda and A.
+//
+// Checkpointing: a forward sweep stores the state entering every chunk of Q
+// tokens; the reverse sweep then, chunk by chunk from the last, stages the
+// chunk's inputs in shared memory, recomputes its Q states from the
+// checkpoint into shared memory, and runs the adjoint over the chunk.
 #include <cuda_bf16.h>
 
 #include "m3_common.cuh"
@@ -29,7 +35,85 @@
 namespace m3 {
 namespace {
 
-constexpr int kBwdMaxK = 8;   // state pairs per thread
+constexpr int kBwdThreads = 128;
+constexpr int kStageBatch = 8;   // loads in flight per thread while staging
+
+struct Staged {
+    float v;
+    int dst;
+};
+
+template <int R>
+struct kLg {
+    static constexpr int v = R == 1 ? 0 : (R == 2 ? 1 : (R == 4 ? 2 : 3));
+};
+
+// tokens per chunk: the staged inputs and dX partials grow with R
+template <int R>
+struct BwdChunk {
+    static constexpr int Q = R <= 2 ? 8 : 4;
+};
+
+__host__ __device__ constexpr int round4(int v) { return (v + 3) & ~3; }
+
+// Shared-memory sections (offsets in floats, each on a 16-byte boundary):
+//   sB   [Q+1][PB][R] float2   B rows (2j, 2j+1), slot q <-> token t0 - 1 + q
+//   sX   [Q+1][R][P]           X, same slots
+//   sC   [Q][PB][R] float2     C rows, slot q <-> token t0 + q
+//   sDy  [Q][R][P]             dy
+//   sCS  [Q][PB] float2        (cos, sin) of phi_{t,j}
+//   sW   [Q][PB]               omega_{t,j}
+//   sABG [Q] float4            (alpha, beta, gamma, Delta)
+//   sDt, sL [Q]                Delta_t, lambda_t as loaded
+//   sDx  [Q][warps][R][P]      dX partial sums of each warp
+//   sScal[Q][PB][4]            per-pair (dalpha, dbeta, dgamma, omega dphi) partials
+//   sS   [Q][2][threads] float4 the chunk's recomputed states
+struct BwdLayout {
+    int PB, lgPB, lgP, threads, nPB;
+    int oB, oX, oC, oDy, oCS, oW, oABG, oDt, oL, oDx, oScal, oS, total;
+};
+
+BwdLayout bwd_layout(int P, int N, int R, int Q) {
+    BwdLayout L{};
+    const int P4 = P / 4, NP2 = N / 2;
+    int PB = kBwdThreads / P4;   // a power of two, the smallest one >= N/2 if that is smaller
+    if (PB < 1) PB = 1;
+    while (PB > 1 && PB / 2 >= NP2) PB /= 2;
+    L.PB = PB;
+    L.lgPB = 0;
+    while ((1 << L.lgPB) < PB) ++L.lgPB;
+    L.lgP = 0;
+    while ((1 << L.lgP) < P) ++L.lgP;
+    L.threads = (PB * P4 + 31) / 32 * 32;   // whole warps; threads past PB * P4 idle
+    L.nPB = (NP2 + PB - 1) / PB;
+    int o = 0;
+    L.oB = o;
+    o += round4((Q + 1) * PB * R * 2);
+    L.oX = o;
+    o += round4((Q + 1) * R * P);
+    L.oC = o;
+    o += round4(Q * PB * R * 2);
+    L.oDy = o;
+    o += round4(Q * R * P);
+    L.oCS = o;
+    o += round4(Q * PB * 2);
+    L.oW = o;
+    o += round4(Q * PB);
+    L.oABG = o;
+    o += Q * 4;
+    L.oDt = o;
+    o += round4(Q);
+    L.oL = o;
+    o += round4(Q);
+    L.oDx = o;
+    o += Q * (L.threads / 32) * R * P;
+    L.oScal = o;
+    o += Q * PB * 4;
+    L.oS = o;
+    o += Q * 2 * L.threads * 4;
+    L.total = o;
+    return L;
+}
 
 __device__ __forceinline__ float4 fma4b(float a, float4 x, float4 y) {
     return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
@@ -38,285 +122,367 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(
 __device__ __forceinline__ float4 sub4(float4 a, float4 b) { return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
 __device__ __forceinline__ float4 mul4(float a, float4 x) { return make_float4(a * x.x, a * x.y, a * x.z, a * x.w); }
 __device__ __forceinline__ float dot4(float4 a, float4 b) { return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w; }
-
-struct BwdShape {
-    int G, threads;
-    size_t smem;
-};
-
-__host__ __device__ constexpr int round4(int v) { return (v + 3) & ~3; }
-
-// Shared-memory sections, each starting on a 16-byte boundary (floats):
-// B/X ping-pong [2][RN + R*P], C pairs [RN], dy [R*P], (cos, sin) [N/2] pairs,
-// dX partials [warps][R*P], block partials [warps][4]; RN = R*N rounded up to 4.
-BwdShape bwd_shape(int64_t P, int64_t N, int R) {
-    BwdShape s{};
-    const int P4 = (int)(P / 4), NP2 = (int)(N / 2);
-    int G = 256 / P4;
-    if (G > NP2) G = NP2;
-    if (G < 1) G = 1;
-    s.G = G;
-    s.threads = (G * P4 + 31) / 32 * 32;   // whole warps; threads past G * P4 idle
-    const int nw = s.threads / 32, RN = round4(R * (int)N), RP = R * (int)P;
-    s.smem = sizeof(float) * (size_t)(2 * (RN + RP) + RN + RP + round4((int)N) + nw * RP + nw * 4);
-    return s;
-}
+__device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
 template <typename IO, int R>
-__global__ void __launch_bounds__(256, 1) scan_bwd_kernel(
+__global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(
     const IO* __restrict__ x, const IO* __restrict__ B, const IO* __restrict__ C, const float* __restrict__ dt,
     const float* __restrict__ A, const float* __restrict__ lam, const float* __restrict__ omega,
-    const IO* __restrict__ dy, const float* __restrict__ dfin, float* __restrict__ dx, float* __restrict__ dB,
-    float* __restrict__ dC, float* __restrict__ ddt, float* __restrict__ dA, float* __restrict__ dlam,
-    float* __restrict__ domega, float* __restrict__ S, int64_t T, int H, int P, int N, int G) {
+    const IO* __restrict__ dy, const float* __restrict__ dfin, float* __restrict__ dB, float* __restrict__ dC,
+    float* __restrict__ domega, float* __restrict__ ckpt, float* __restrict__ part_dx, float* __restrict__ part_s,
+    int64_t T, int H, int P, int N, const BwdLayout L) {
+    constexpr int Q = BwdChunk<R>::Q;
     extern __shared__ __align__(16) float sm[];
     const int64_t bh = blockIdx.x;
+    const int pb = blockIdx.y;
     const int64_t b = bh / H;
     const int h = (int)(bh % H);
-    const int P4 = P >> 2, NP2 = N >> 1;
-    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = (nt + 31) >> 5;
-    const int c4 = tid % P4, g = tid / P4;
-    const bool gv = g < G;   // holds state pairs (threads past G * P4 only join reductions)
-    const int RN = round4(R * N);
+    const int P4 = P >> 2, NP2 = N >> 1, PB = L.PB, nt = blockDim.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+    const int c4 = tid % P4, gl = tid / P4;
+    const int j = pb * PB + gl;
+    const bool on = gl < PB && j < NP2;
+    const int gc = gl < PB ? gl : 0;   // shared-memory slot of this thread's pair (idle threads read slot 0)
+    const int64_t nC = (T + Q - 1) / Q;
+    const int64_t BTH = (int64_t)gridDim.x / H * T * H;
 
-    float* sBX[2] = {sm, sm + (RN + R * P)};   // B rows as pairs [N/2][R] float2, then X [R*P] at RN
-    float* sCp = sm + 2 * (RN + R * P);        // C pairs [N/2][R]
-    float* sDy = sCp + RN;                     // [R*P]
-    float2* sCS = reinterpret_cast<float2*>(sDy + R * P);   // [N/2] (cos, sin) of phi_t
-    float* sRed = reinterpret_cast<float*>(sCS) + round4(N);  // [warps][R*P]
-    float* sBlk = sRed + nw * R * P;                        // [warps][4]
+    float* sB = sm + L.oB;
+    float* sX = sm + L.oX;
+    float* sC = sm + L.oC;
+    float* sDy = sm + L.oDy;
+    float* sCS = sm + L.oCS;
+    float* sW = sm + L.oW;
+    float* sABG = sm + L.oABG;
+    float* sDx = sm + L.oDx;
+    float* sScal = sm + L.oScal;
+    float4* sS4 = reinterpret_cast<float4*>(sm + L.oS);
+    const float2* sB2 = reinterpret_cast<const float2*>(sB);
+    const float4* sX4 = reinterpret_cast<const float4*>(sX);
+    const float2* sC2 = reinterpret_cast<const float2*>(sC);
+    const float4* sDy4 = reinterpret_cast<const float4*>(sDy);
+    const float2* sCS2 = reinterpret_cast<const float2*>(sCS);
+    const float4* sABG4 = reinterpret_cast<const float4*>(sABG);
 
     const float a_h = A[h];
     auto tok = [&](int64_t t) { return (b * T + t) * H + h; };   // (batch, token, head) index
-    auto stage_bx = [&](int64_t t, float* dst) {   // B_t (pairs) and X_t of this head; zeros for t < 0
-        for (int i = tid; i < R * N; i += nt) {
-            const int r = i / N, n = i % N;
-            dst[((n >> 1) * R + r) * 2 + (n & 1)] = t >= 0 ? ld_io(B, tok(t) * R * N + i) : 0.f;
+
+    // The inputs of tokens t0 - 1 .. t0 + Q - 1 (zeros outside [0, T) and for pairs past N/2), then the
+    // angles and decays derived from them.  One flat index space over the raw sections; each thread
+    // issues kStageBatch independent loads before storing them, so their latencies overlap.
+    const int lgPB = L.lgPB, lgRP = L.lgP + kLg<R>::v;
+    const int n1 = (Q + 1) * PB * R * 2, n2 = (Q + 1) * R * P, n3 = Q * PB * R * 2, n4 = Q * R * P, n5 = Q * PB;
+    const int ntot = n1 + n2 + n3 + n4 + n5 + 2 * Q;
+    // returns (value, destination offset in shared memory)
+    auto fetch = [&](int i, int64_t t0) -> Staged {
+        int dst;
+        if (i < n1 + n3) {   // B pairs (slot q <-> token t0 - 1 + q), then C pairs (slot q <-> token t0 + q)
+            const bool isB = i < n1;
+            const int k = isB ? i : i - n1;
+            const int e = k & 1, r = (k >> 1) & (R - 1), pl = (k >> (1 + kLg<R>::v)) & (PB - 1);
+            const int q = k >> (1 + kLg<R>::v + lgPB);
+            const int64_t t = isB ? t0 - 1 + q : t0 + q;
+            const int jp = pb * PB + pl;
+            dst = (isB ? L.oB : L.oC) + k;
+            return {(t >= 0 && t < T && jp < NP2) ? ld_io(isB ? B : C, (tok(t) * R + r) * N + 2 * jp + e) : 0.f, dst};
         }
-        for (int i = tid; i < R * P; i += nt) dst[RN + i] = t >= 0 ? ld_io(x, tok(t) * R * P + i) : 0.f;
+        int k = i - n1 - n3;
+        if (k < n2 + n4) {   // X (slots from token t0 - 1), then dy (from token t0)
+            const bool isX = k < n2;
+            if (!isX) k -= n2;
+            const int q = k >> lgRP, rp = k & ((R * P) - 1);
+            const int64_t t = isX ? t0 - 1 + q : t0 + q;
+            dst = (isX ? L.oX : L.oDy) + k;
+            return {(t >= 0 && t < T) ? ld_io(isX ? x : dy, tok(t) * R * P + rp) : 0.f, dst};
+        }
+        k -= n2 + n4;
+        if (k < n5) {
+            const int q = k >> lgPB, jp = pb * PB + (k & (PB - 1));
+            const int64_t t = t0 + q;
+            dst = L.oW + k;
+            return {(t < T && jp < NP2) ? omega[tok(t) * NP2 + jp] : 0.f, dst};
+        }
+        k -= n5;
+        const bool isD = k < Q;
+        const int q = isD ? k : k - Q;
+        dst = (isD ? L.oDt : L.oL) + q;
+        return {t0 + q < T ? (isD ? dt : lam)[tok(t0 + q)] : 0.f, dst};
     };
-    // v[rows 2j, 2j+1][cols of c4] = sum_r B[r, 2j / 2j+1] X[r, cols] from a staged buffer
-    auto outer = [&](const float* buf, int j, float4& v0, float4& v1) {
-        const float2* b2 = reinterpret_cast<const float2*>(buf);
-        const float4* x4 = reinterpret_cast<const float4*>(buf + RN);
-        v0 = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto stage = [&](int64_t t0) {
+        for (int base = 0; base < ntot; base += kStageBatch * nt) {
+            Staged v[kStageBatch];
+#pragma unroll
+            for (int u = 0; u < kStageBatch; ++u) {
+                const int i = base + u * nt + tid;
+                v[u] = i < ntot ? fetch(i, t0) : Staged{0.f, -1};
+            }
+#pragma unroll
+            for (int u = 0; u < kStageBatch; ++u)
+                if (v[u].dst >= 0) sm[v[u].dst] = v[u].v;
+        }
+        __syncthreads();
+        const float* sDt = sm + L.oDt;
+        const float* sL = sm + L.oL;
+        for (int i = tid; i < Q * PB; i += nt) {
+            float sn, cs;
+            sincosf(sDt[i >> lgPB] * sW[i], &sn, &cs);
+            sCS[2 * i] = cs;
+            sCS[2 * i + 1] = sn;
+        }
+        for (int q = tid; q < Q; q += nt) {
+            const float d = sDt[q], l = sL[q];
+            const float al = expf(d * a_h);
+            sABG[4 * q] = al;
+            sABG[4 * q + 1] = (1.f - l) * d * al;
+            sABG[4 * q + 2] = l * d;
+            sABG[4 * q + 3] = d;
+        }
+    };
+    // v[rows 2j, 2j+1][cols of c4] of slot s of the B/X buffers: sum_r B[r, 2j / 2j+1] X[r, cols]
+    auto outer = [&](int s, float4& v0, float4& v1) {
+        v0 = zero4();
         v1 = v0;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const float2 bb = b2[j * R + r];
-            const float4 xx = x4[r * P4 + c4];
+            const float2 bb = sB2[(s * PB + gc) * R + r];
+            const float4 xx = sX4[(s * R + r) * P4 + c4];
             v0 = fma4b(bb.x, xx, v0);
             v1 = fma4b(bb.y, xx, v1);
         }
     };
-    float4* S4 = reinterpret_cast<float4*>(S + bh * T * (int64_t)N * P);
-    auto srow = [&](int64_t t, int n) { return S4 + (t * N + n) * P4 + c4; };
+    // one step of the recurrence for token slot q of the staged chunk; (vp0, vp1) = v of slot q on entry,
+    // of slot q + 1 on return
+    auto step = [&](int q, float4& s0, float4& s1, float4& vp0, float4& vp1) {
+        float4 v0, v1;
+        outer(q + 1, v0, v1);
+        const float4 abg = sABG4[q];
+        const float4 u0 = fma4b(abg.x, s0, mul4(abg.y, vp0));
+        const float4 u1 = fma4b(abg.x, s1, mul4(abg.y, vp1));
+        const float2 cs = sCS2[q * PB + gc];
+        float4 o0, o1;
+        rot2(cs.x, cs.y, u0.x, u1.x, o0.x, o1.x);
+        rot2(cs.x, cs.y, u0.y, u1.y, o0.y, o1.y);
+        rot2(cs.x, cs.y, u0.z, u1.z, o0.z, o1.z);
+        rot2(cs.x, cs.y, u0.w, u1.w, o0.w, o1.w);
+        s0 = fma4b(abg.z, v0, o0);
+        s1 = fma4b(abg.z, v1, o1);
+        vp0 = v0;
+        vp1 = v1;
+    };
+    float4* ck4 = reinterpret_cast<float4*>(ckpt) + bh * nC * (int64_t)N * P4;
+    auto ckrow = [&](int64_t c, int n) { return ck4 + (c * N + n) * P4 + c4; };
 
-    // ------------------------------ forward: every h_t ------------------------------
-    float4 h0[kBwdMaxK], h1[kBwdMaxK];
+    // ---------------- forward sweep: the state entering chunks 1 .. nC-1 ----------------
+    {
+        float4 h0 = zero4(), h1 = zero4();
+        for (int64_t c = 0; c + 1 < nC; ++c) {
+            stage(c * Q);
+            __syncthreads();
+            float4 vp0, vp1;
+            outer(0, vp0, vp1);
 #pragma unroll
-    for (int k = 0; k < kBwdMaxK; ++k) h0[k] = h1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    stage_bx(-1, sBX[1]);
-    for (int64_t t = 0; t < T; ++t) {
-        float* cur = sBX[t & 1];
-        const float* prv = sBX[(t + 1) & 1];
-        stage_bx(t, cur);
-        const float d = dt[tok(t)], l = lam[tok(t)];
-        for (int j = tid; j < NP2; j += nt) {
-            float sn, cs;
-            sincosf(d * omega[tok(t) * NP2 + j], &sn, &cs);
-            sCS[j] = make_float2(cs, sn);
-        }
-        __syncthreads();
-        const float alpha = expf(d * a_h), beta = (1.f - l) * d * alpha, gamma = l * d;
-#pragma unroll
-        for (int k = 0; k < kBwdMaxK; ++k) {
-            const int j = g + k * G;
-            if (gv && j < NP2) {
-                float4 vp0, vp1, v0, v1;
-                outer(prv, j, vp0, vp1);
-                outer(cur, j, v0, v1);
-                const float4 u0 = fma4b(alpha, h0[k], mul4(beta, vp0));
-                const float4 u1 = fma4b(alpha, h1[k], mul4(beta, vp1));
-                const float2 cs = sCS[j];
-                float4 o0, o1;
-                rot2(cs.x, cs.y, u0.x, u1.x, o0.x, o1.x);
-                rot2(cs.x, cs.y, u0.y, u1.y, o0.y, o1.y);
-                rot2(cs.x, cs.y, u0.z, u1.z, o0.z, o1.z);
-                rot2(cs.x, cs.y, u0.w, u1.w, o0.w, o1.w);
-                h0[k] = fma4b(gamma, v0, o0);
-                h1[k] = fma4b(gamma, v1, o1);
-                *srow(t, 2 * j) = h0[k];
-                *srow(t, 2 * j + 1) = h1[k];
+            for (int q = 0; q < Q; ++q) step(q, h0, h1, vp0, vp1);
+            if (on) {
+                *ckrow(c + 1, 2 * j) = h0;
+                *ckrow(c + 1, 2 * j + 1) = h1;
             }
+            __syncthreads();   // the staged inputs are replaced next
         }
-        __syncthreads();   // the buffers and (cos, sin) are restaged next
     }
 
-    // ------------------------------ backward: the adjoint ------------------------------
-    float4 ub0[kBwdMaxK], ub1[kBwdMaxK];   // ubar_{t+1}
-#pragma unroll
-    for (int k = 0; k < kBwdMaxK; ++k) ub0[k] = ub1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // ---------------- reverse sweep: the adjoint, chunk by chunk ----------------
+    float4 ub0 = zero4(), ub1 = zero4();   // ubar_{t+1}
     float alpha_n = 0.f, beta_n = 0.f;     // alpha_{t+1}, beta_{t+1}
-    float dA_acc = 0.f;
-    // the buffers: B_t, X_t in sBX[t & 1] and B_{t-1}, X_{t-1} in the other one
-    stage_bx(T - 1, sBX[(T - 1) & 1]);
-    for (int64_t t = T - 1; t >= 0; --t) {
-        float* cur = sBX[t & 1];
-        float* prv = sBX[(t + 1) & 1];
-        stage_bx(t - 1, prv);
-        for (int i = tid; i < R * N; i += nt) {
-            const int r = i / N, n = i % N;
-            sCp[((n >> 1) * R + r) * 2 + (n & 1)] = ld_io(C, tok(t) * R * N + i);
-        }
-        for (int i = tid; i < R * P; i += nt) sDy[i] = ld_io(dy, tok(t) * R * P + i);
-        const float d = dt[tok(t)], l = lam[tok(t)];
-        for (int j = tid; j < NP2; j += nt) {
-            float sn, cs;
-            sincosf(d * omega[tok(t) * NP2 + j], &sn, &cs);
-            sCS[j] = make_float2(cs, sn);
+    for (int64_t c = nC - 1; c >= 0; --c) {
+        const int64_t t0 = c * Q;
+        const int qn = (int)((T - t0) < Q ? (T - t0) : Q);
+        stage(t0);
+        float4 hc0 = zero4(), hc1 = zero4();   // h_{t0-1}
+        if (c > 0 && on) {
+            hc0 = *ckrow(c, 2 * j);
+            hc1 = *ckrow(c, 2 * j + 1);
         }
         __syncthreads();
-        const float alpha = expf(d * a_h), beta = (1.f - l) * d * alpha, gamma = l * d;
-        const float2* c2 = reinterpret_cast<const float2*>(sCp);
-        const float2* b2 = reinterpret_cast<const float2*>(cur);
-        const float4* x4 = reinterpret_cast<const float4*>(cur + RN);
-        const float4* dy4 = reinterpret_cast<const float4*>(sDy);
-        float p_alpha = 0.f, p_beta = 0.f, p_gamma = 0.f, p_omega = 0.f;
-        float4 dXp[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) dXp[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < kBwdMaxK; ++k) {
-            if (k * G >= NP2) break;   // uniform over the block
-            const int j = g + k * G;
-            const bool on = gv && j < NP2;
-            const int jj = on ? j : 0;
-            float4 ht0 = make_float4(0.f, 0.f, 0.f, 0.f), ht1 = ht0, hp0 = ht0, hp1 = ht0;
-            if (on) {
-                ht0 = *srow(t, 2 * j);
-                ht1 = *srow(t, 2 * j + 1);
-                if (t > 0) {
-                    hp0 = *srow(t - 1, 2 * j);
-                    hp1 = *srow(t - 1, 2 * j + 1);
-                }
+        {
+            float4 s0 = hc0, s1 = hc1, vp0, vp1;
+            outer(0, vp0, vp1);
+            for (int q = 0; q < qn; ++q) {   // each thread reads back only its own slots
+                step(q, s0, s1, vp0, vp1);
+                sS4[(2 * q) * nt + tid] = s0;
+                sS4[(2 * q + 1) * nt + tid] = s1;
             }
-            float4 v0, v1, vp0, vp1;
-            outer(cur, jj, v0, v1);
-            outer(prv, jj, vp0, vp1);
+        }
+        float4 v0, v1;   // v of token t0 + q, carried down from the step after
+        outer(qn, v0, v1);
+#pragma unroll 2
+        for (int q = qn - 1; q >= 0; --q) {
+            const int64_t t = t0 + q;
+            const float4 ht0 = sS4[(2 * q) * nt + tid], ht1 = sS4[(2 * q + 1) * nt + tid];
+            const float4 hp0 = q > 0 ? sS4[(2 * q - 2) * nt + tid] : hc0;
+            const float4 hp1 = q > 0 ? sS4[(2 * q - 1) * nt + tid] : hc1;
+            float4 vp0, vp1;
+            outer(q, vp0, vp1);
+            const float4 abg = sABG4[q];
+            const float gamma = abg.z, d = abg.w;
             // gbar_t = C_t dy_t^T + alpha_{t+1} ubar_{t+1} (+ the final-state seed)
-            float4 g0 = mul4(alpha_n, ub0[k]), g1 = mul4(alpha_n, ub1[k]);
+            float4 g0 = mul4(alpha_n, ub0), g1 = mul4(alpha_n, ub1);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float2 cc = c2[jj * R + r];
-                g0 = fma4b(cc.x, dy4[r * P4 + c4], g0);
-                g1 = fma4b(cc.y, dy4[r * P4 + c4], g1);
+                const float2 cc = sC2[(q * PB + gc) * R + r];
+                const float4 dyr = sDy4[(q * R + r) * P4 + c4];
+                g0 = fma4b(cc.x, dyr, g0);
+                g1 = fma4b(cc.y, dyr, g1);
             }
             if (t == T - 1 && dfin != nullptr && on) {
                 const float4* df4 = reinterpret_cast<const float4*>(dfin + bh * (int64_t)N * P);
                 g0 = add4(g0, df4[(2 * j) * P4 + c4]);
                 g1 = add4(g1, df4[(2 * j + 1) * P4 + c4]);
             }
-            if (!on) g0 = g1 = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 dv0 = fma4b(gamma, g0, mul4(beta_n, ub0[k]));
-            const float4 dv1 = fma4b(gamma, g1, mul4(beta_n, ub1[k]));
-            const float4 r0 = sub4(ht0, mul4(gamma, v0)), r1 = sub4(ht1, mul4(gamma, v1));
-            // dphi_j partial over this thread's columns, then over the pair group's lanes
-            float dphi = dot4(g1, r0) - dot4(g0, r1);
-            const float2 cs = sCS[jj];
-            // ubar_t = R(phi)^T gbar_t
+            if (!on) g0 = g1 = zero4();
+            const float4 dv0 = fma4b(gamma, g0, mul4(beta_n, ub0));
+            const float4 dv1 = fma4b(gamma, g1, mul4(beta_n, ub1));
+            const float4 r0 = sub4(ht0, mul4(gamma, v0)), r1 = sub4(ht1, mul4(gamma, v1));   // R(phi_t) u_t
+            const float2 cs = sCS2[q * PB + gc];
+            // ubar_t = R(phi_t)^T gbar_t
             const float4 un0 = add4(mul4(cs.x, g0), mul4(cs.y, g1));
             const float4 un1 = sub4(mul4(cs.x, g1), mul4(cs.y, g0));
-            p_alpha += dot4(un0, hp0) + dot4(un1, hp1);
-            p_beta += dot4(un0, vp0) + dot4(un1, vp1);
-            p_gamma += dot4(g0, v0) + dot4(g1, v1);
-            ub0[k] = un0;
-            ub1[k] = un1;
-            // dC_t[r, n] = sum_p h_t[n, p] dy_t[r, p];  dB_t[r, n] = sum_p dv_t[n, p] X_t[r, p]
-            float pc[2 * R], pb[2 * R];
+            // sums over this pair's columns: dphi, dalpha, dbeta, dgamma, then dC_t and dB_t per rank
+            float red[4 + 4 * R];
+            red[0] = dot4(g1, r0) - dot4(g0, r1);
+            red[1] = dot4(un0, hp0) + dot4(un1, hp1);
+            red[2] = dot4(un0, vp0) + dot4(un1, vp1);
+            red[3] = dot4(g0, v0) + dot4(g1, v1);
+            float4 dXp[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float4 dyr = dy4[r * P4 + c4], xr = x4[r * P4 + c4];
-                pc[2 * r] = dot4(ht0, dyr);
-                pc[2 * r + 1] = dot4(ht1, dyr);
-                pb[2 * r] = dot4(dv0, xr);
-                pb[2 * r + 1] = dot4(dv1, xr);
-                // dX_t[r, p] = sum_n dv_t[n, p] B_t[r, n]
-                const float2 bb = b2[jj * R + r];
-                dXp[r] = fma4b(bb.x, dv0, fma4b(bb.y, dv1, dXp[r]));
+                const float4 dyr = sDy4[(q * R + r) * P4 + c4];
+                const float4 xr = sX4[((q + 1) * R + r) * P4 + c4];
+                red[4 + 4 * r] = dot4(ht0, dyr);   // dC_t[r, n] = sum_p h_t[n, p] dy_t[r, p]
+                red[5 + 4 * r] = dot4(ht1, dyr);
+                red[6 + 4 * r] = dot4(dv0, xr);    // dB_t[r, n] = sum_p dv_t[n, p] X_t[r, p]
+                red[7 + 4 * r] = dot4(dv1, xr);
+                const float2 bb = sB2[((q + 1) * PB + gc) * R + r];
+                dXp[r] = fma4b(bb.x, dv0, mul4(bb.y, dv1));   // dX_t[r, p] partial over this pair
             }
+            ub0 = un0;
+            ub1 = un1;
+            alpha_n = abg.x;
+            beta_n = abg.y;
             for (int o = 1; o < P4; o <<= 1) {
-                dphi += __shfl_xor_sync(0xffffffffu, dphi, o);
 #pragma unroll
-                for (int i = 0; i < 2 * R; ++i) {
-                    pc[i] += __shfl_xor_sync(0xffffffffu, pc[i], o);
-                    pb[i] += __shfl_xor_sync(0xffffffffu, pb[i], o);
-                }
+                for (int i = 0; i < 4 + 4 * R; ++i) red[i] += __shfl_xor_sync(0xffffffffu, red[i], o);
             }
             if (on && c4 == 0) {
                 const int64_t tb = tok(t);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    dC[(tb * R + r) * N + 2 * j] = pc[2 * r];
-                    dC[(tb * R + r) * N + 2 * j + 1] = pc[2 * r + 1];
-                    dB[(tb * R + r) * N + 2 * j] = pb[2 * r];
-                    dB[(tb * R + r) * N + 2 * j + 1] = pb[2 * r + 1];
+                    *reinterpret_cast<float2*>(dC + (tb * R + r) * N + 2 * j) = make_float2(red[4 + 4 * r], red[5 + 4 * r]);
+                    *reinterpret_cast<float2*>(dB + (tb * R + r) * N + 2 * j) = make_float2(red[6 + 4 * r], red[7 + 4 * r]);
                 }
-                const float w = omega[tb * NP2 + j];
-                domega[tb * NP2 + j] = d * dphi;
-                p_omega += w * dphi;
+                domega[tb * NP2 + j] = d * red[0];
+                float* sc = sScal + (q * PB + gl) * 4;
+                sc[0] = red[1];
+                sc[1] = red[2];
+                sc[2] = red[3];
+                sc[3] = sW[q * PB + gl] * red[0];
             }
-        }
-        // dX over the pair groups: lanes of one warp first, then the warps through shared memory
-        for (int o = P4; o < 32; o <<= 1) {
+            // dX over the pairs of this warp; the warps' partials are summed at the end of the chunk
+            for (int o = P4; o < 32; o <<= 1) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                dXp[r].x += __shfl_xor_sync(0xffffffffu, dXp[r].x, o);
-                dXp[r].y += __shfl_xor_sync(0xffffffffu, dXp[r].y, o);
-                dXp[r].z += __shfl_xor_sync(0xffffffffu, dXp[r].z, o);
-                dXp[r].w += __shfl_xor_sync(0xffffffffu, dXp[r].w, o);
+                for (int r = 0; r < R; ++r) {
+                    dXp[r].x += __shfl_xor_sync(0xffffffffu, dXp[r].x, o);
+                    dXp[r].y += __shfl_xor_sync(0xffffffffu, dXp[r].y, o);
+                    dXp[r].z += __shfl_xor_sync(0xffffffffu, dXp[r].z, o);
+                    dXp[r].w += __shfl_xor_sync(0xffffffffu, dXp[r].w, o);
+                }
             }
-        }
-        if (lane < P4) {
-            float4* red4 = reinterpret_cast<float4*>(sRed) + warp * (R * P4);
+            if (lane < P4) {
+                float4* dst = reinterpret_cast<float4*>(sDx) + ((q * nw + warp) * R) * P4 + c4;
 #pragma unroll
-            for (int r = 0; r < R; ++r) red4[r * P4 + c4] = dXp[r];
-        }
-        p_alpha = warp_sum(p_alpha);
-        p_beta = warp_sum(p_beta);
-        p_gamma = warp_sum(p_gamma);
-        p_omega = warp_sum(p_omega);
-        if (lane == 0) {
-            sBlk[warp * 4 + 0] = p_alpha;
-            sBlk[warp * 4 + 1] = p_beta;
-            sBlk[warp * 4 + 2] = p_gamma;
-            sBlk[warp * 4 + 3] = p_omega;
+                for (int r = 0; r < R; ++r) dst[r * P4] = dXp[r];
+            }
+            v0 = vp0;
+            v1 = vp1;
         }
         __syncthreads();
-        for (int i = tid; i < R * P; i += nt) {
+        // this pair block's partial sums of the chunk's tokens
+        for (int i = tid; i < qn * R * P; i += nt) {
+            const int q = i >> lgRP, rp = i & (R * P - 1);
+            float sx = 0.f;
+            for (int w = 0; w < nw; ++w) sx += sDx[(q * nw + w) * R * P + rp];
+            part_dx[((int64_t)pb * BTH + tok(t0 + q)) * R * P + rp] = sx;
+        }
+        const int pbn = (NP2 - pb * PB) < PB ? (NP2 - pb * PB) : PB;   // pairs of this block
+        for (int i = tid; i < qn * 4; i += nt) {
+            const int q = i >> 2, k = i & 3;
             float s = 0.f;
-            for (int w = 0; w < nw; ++w) s += sRed[w * R * P + i];
-            dx[tok(t) * R * P + i] = s;
+            for (int pl = 0; pl < pbn; ++pl) s += sScal[(q * PB + pl) * 4 + k];
+            part_s[((int64_t)pb * BTH + tok(t0 + q)) * 4 + k] = s;
         }
-        if (tid == 0) {
-            float da = 0.f, db = 0.f, dg = 0.f, dw = 0.f;
-            for (int w = 0; w < nw; ++w) {
-                da += sBlk[w * 4 + 0];
-                db += sBlk[w * 4 + 1];
-                dg += sBlk[w * 4 + 2];
-                dw += sBlk[w * 4 + 3];
-            }
-            // alpha = e^{d a}, beta = (1 - l) d alpha, gamma = l d, phi = d omega
-            const float dalpha = da + db * (1.f - l) * d;          // through alpha and beta's alpha
-            ddt[tok(t)] = dalpha * a_h * alpha + db * (1.f - l) * alpha + dg * l + dw;
-            dlam[tok(t)] = -d * alpha * db + d * dg;
-            dA_acc += dalpha * d * alpha;
-        }
-        alpha_n = alpha;
-        beta_n = beta;
-        __syncthreads();   // every buffer is restaged next
+        // the next stage() writes none of sDx, sScal, sS; the barrier after it orders the reads above
     }
-    if (tid == 0) atomicAdd(&dA[h], dA_acc);
+}
+
+// dX = the sum of the pair blocks' partials
+__global__ void bwd_finish_dx(const float4* __restrict__ part, float4* __restrict__ dx, int64_t n4, int nPB) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        float4 s = part[i];
+        for (int k = 1; k < nPB; ++k) s = add4(s, part[k * n4 + i]);
+        dx[i] = s;
+    }
+}
+
+// per token: (dalpha, dbeta, dgamma, sum_j omega_j dphi_j) summed over the pair blocks, then the chain
+// rule through alpha = exp(Delta A), beta = (1 - lambda) Delta alpha, gamma = lambda Delta, phi = Delta omega
+__global__ void bwd_finish_scalars(const float4* __restrict__ part_s, const float* __restrict__ dt,
+                                   const float* __restrict__ lam, const float* __restrict__ A,
+                                   float* __restrict__ ddt, float* __restrict__ dlam, float* __restrict__ dA,
+                                   int64_t batch, int64_t T, int H, int nPB) {
+    __shared__ float red[32];
+    const int h = blockIdx.x;
+    const float a = A[h];
+    const int64_t BTH = batch * T * H;
+    float acc = 0.f;
+    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
+        for (int64_t t = threadIdx.x; t < T; t += blockDim.x) {
+            const int64_t tk = (b * T + t) * H + h;
+            float4 s = part_s[tk];
+            for (int k = 1; k < nPB; ++k) s = add4(s, part_s[k * BTH + tk]);
+            const float d = dt[tk], l = lam[tk], al = expf(d * a);
+            const float dalpha = s.x + s.y * (1.f - l) * d;   // through alpha and through beta's alpha
+            ddt[tk] = dalpha * a * al + s.y * (1.f - l) * al + s.z * l + s.w;
+            dlam[tk] = -d * al * s.y + d * s.z;
+            acc += dalpha * d * al;
+        }
+    }
+    acc = warp_sum(acc);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
+        atomicAdd(&dA[h], s);
+    }
+}
+
+int bwd_chunk(int R) { return R <= 2 ? 8 : 4; }
+
+struct BwdWs {
+    size_t ckpt, part_dx, part_s, total;   // byte offsets of the sections, and the whole size
+};
+
+size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+BwdWs bwd_ws(const ScanDims& d) {
+    const int Q = bwd_chunk(d.R);
+    const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, Q);
+    const size_t bh = (size_t)(d.batch * d.nheads), BTH = bh * (size_t)d.seqlen;
+    const size_t nC = (size_t)((d.seqlen + Q - 1) / Q);
+    BwdWs w{};
+    w.ckpt = 0;
+    w.part_dx = round256(sizeof(float) * bh * nC * (size_t)(d.dstate * d.headdim));
+    w.part_s = w.part_dx + round256(sizeof(float) * (size_t)L.nPB * BTH * (size_t)(d.R * d.headdim));
+    w.total = w.part_s + round256(sizeof(float) * (size_t)L.nPB * BTH * 4);
+    return w;
 }
 
 template <typename IO>
@@ -324,21 +490,28 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
                           const float* A, const float* lambda, const float* omega, const void* dy,
                           const float* d_final, float* dx, float* dB, float* dC, float* ddt, float* dA,
                           float* dlambda, float* domega, void* workspace, cudaStream_t stream) {
-    const BwdShape s = bwd_shape(d.headdim, d.dstate, d.R);
+    const int Q = bwd_chunk(d.R);
+    const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, Q);
     const int64_t bh = d.batch * d.nheads;
     cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * (size_t)d.nheads, stream);
     if (e != cudaSuccess || bh == 0 || d.seqlen == 0) return e;
-#define M3_BWD_CASE(RR)                                                                                            \
-    case RR: {                                                                                                     \
-        auto k = scan_bwd_kernel<IO, RR>;                                                                          \
-        if (s.smem > 48 * 1024 &&                                                                                  \
-            (e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s.smem)) != cudaSuccess) \
-            return e;                                                                                              \
-        k<<<(unsigned)bh, s.threads, s.smem, stream>>>((const IO*)x, (const IO*)B, (const IO*)C, dt, A, lambda,    \
-                                                      omega, (const IO*)dy, d_final, dx, dB, dC, ddt, dA, dlambda, \
-                                                      domega, static_cast<float*>(workspace), d.seqlen,           \
-                                                      (int)d.nheads, (int)d.headdim, (int)d.dstate, s.G);          \
-        return cudaGetLastError();                                                                                 \
+    const BwdWs w = bwd_ws(d);
+    char* ws = static_cast<char*>(workspace);
+    float* ckpt = reinterpret_cast<float*>(ws + w.ckpt);
+    float* part_dx = reinterpret_cast<float*>(ws + w.part_dx);
+    float* part_s = reinterpret_cast<float*>(ws + w.part_s);
+    const size_t smem = sizeof(float) * (size_t)L.total;
+    const dim3 grid((unsigned)bh, (unsigned)L.nPB);
+#define M3_BWD_CASE(RR)                                                                                           \
+    case RR: {                                                                                                    \
+        auto k = scan_bwd_kernel<IO, RR>;                                                                         \
+        if (smem > 48 * 1024 &&                                                                                   \
+            (e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) \
+            return e;                                                                                             \
+        k<<<grid, L.threads, smem, stream>>>((const IO*)x, (const IO*)B, (const IO*)C, dt, A, lambda, omega,      \
+                                             (const IO*)dy, d_final, dB, dC, domega, ckpt, part_dx, part_s,       \
+                                             d.seqlen, (int)d.nheads, (int)d.headdim, (int)d.dstate, L);          \
+        break;                                                                                                    \
     }
     switch (d.R) {
         M3_BWD_CASE(1)
@@ -348,6 +521,18 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
         default: return cudaErrorInvalidValue;
     }
 #undef M3_BWD_CASE
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t n4 = bh * d.seqlen * d.R * d.headdim / 4;
+    int64_t nb = (n4 + 255) / 256;
+    if (nb > 148 * 16) nb = 148 * 16;
+    bwd_finish_dx<<<(unsigned)nb, 256, 0, stream>>>(reinterpret_cast<const float4*>(part_dx),
+                                                    reinterpret_cast<float4*>(dx), n4, L.nPB);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const unsigned gy = (unsigned)(d.batch < 65535 ? d.batch : 65535);
+    bwd_finish_scalars<<<dim3((unsigned)d.nheads, gy), 256, 0, stream>>>(
+        reinterpret_cast<const float4*>(part_s), dt, lambda, A, ddt, dlambda, dA, d.batch, d.seqlen,
+        (int)d.nheads, L.nPB);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -356,16 +541,13 @@ bool bwd_supported(const ScanDims& d) {
     if (!(d.R == 1 || d.R == 2 || d.R == 4 || d.R == 8)) return false;
     if (d.headdim < 4 || d.headdim % 4 || d.headdim > 128) return false;
     const int P4 = (int)(d.headdim / 4);
-    if (P4 & (P4 - 1)) return false;                       // the pair-group lanes are a power of two
+    if (P4 & (P4 - 1)) return false;   // a pair's column lanes are an aligned power-of-two group
     if (d.dstate < 2 || d.dstate % 2 || d.dstate > 256) return false;
-    const BwdShape s = bwd_shape(d.headdim, d.dstate, d.R);
-    if ((d.dstate / 2 + s.G - 1) / s.G > kBwdMaxK) return false;
-    return s.smem <= 200 * 1024;
+    const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, bwd_chunk(d.R));
+    return sizeof(float) * (size_t)L.total <= 200 * 1024;
 }
 
-size_t bwd_workspace_size(const ScanDims& d) {
-    return sizeof(float) * (size_t)(d.batch * d.nheads) * (size_t)d.seqlen * (size_t)(d.dstate * d.headdim);
-}
+size_t bwd_workspace_size(const ScanDims& d) { return bwd_ws(d).total; }
 
 cudaError_t launch_scan_bwd(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                             const float* A, const float* lambda, const float* omega, const void* dy,

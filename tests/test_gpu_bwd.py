@@ -16,7 +16,7 @@ import oracle
 from oracle import grad
 from state_space_sequence_04_b300 import binding, synth
 
-from parity_util import KEYS, need_gpu
+from parity_util import KEYS, need_gpu, slice_bh
 
 pytestmark = pytest.mark.gpu
 
@@ -44,11 +44,16 @@ def _ref_inputs(inp):
 NAMES = {"x": "dx", "B": "dB", "C": "dC", "dt": "ddt", "A": "dA", "lam": "dlam", "omega": "domega"}
 
 
+# chunks of Q = 16 (R <= 2), 8 (R = 4), 4 (R = 8) tokens; pair blocks of 128 / (P / 4) pairs
 @pytest.mark.parametrize("io,Bt,H,T,P,N,R", [
-    ("fp32", 1, 2, 9, 4, 4, 1),
+    ("fp32", 1, 2, 9, 4, 4, 1),      # one ragged chunk
     ("fp32", 2, 1, 7, 8, 6, 2),
     ("fp32", 1, 2, 6, 4, 8, 4),
     ("bf16", 1, 2, 8, 4, 4, 2),
+    ("fp32", 1, 2, 37, 4, 4, 1),     # three chunks, ragged tail
+    ("fp32", 1, 1, 19, 8, 6, 4),     # three chunks of 8
+    ("fp32", 1, 1, 11, 4, 4, 8),     # three chunks of 4
+    ("fp32", 1, 1, 20, 32, 40, 1),   # two pair blocks (16 + 4 pairs), two chunks
 ])
 @pytest.mark.parametrize("with_final", [False, True])
 def test_bwd_small_every_element(io, Bt, H, T, P, N, R, with_final):
@@ -96,6 +101,42 @@ def test_bwd_larger_directional(io, Bt, H, T, P, N, R):
         num = grad.directional(ref, k, d, dy64, df64, eps=1e-6)
         kern = float(np.sum(got[NAMES[k]] * d))
         assert abs(kern - num) <= TOL_BWD[io] * max(1.0, abs(num)), (k, kern, num)
+
+
+def _directional_checks(got, ref, dy64, df64, tol, rng):
+    l0 = grad.loss(ref, dy64, df64)
+    for k in ("x", "B", "C"):   # exact: the loss is linear in each of them
+        d = rng.standard_normal(ref[k].shape)
+        moved = dict(ref)
+        moved[k] = ref[k] + d
+        exact = grad.loss(moved, dy64, df64) - l0
+        kern = float(np.sum(got[NAMES[k]] * d))
+        assert abs(kern - exact) <= tol * max(1.0, abs(exact)), (k, kern, exact)
+    for k in ("dt", "lam", "omega"):
+        d = rng.standard_normal(ref[k].shape) * (ref[k] if k == "dt" else 1.0)
+        num = grad.directional(ref, k, d, dy64, df64, eps=1e-6)
+        kern = float(np.sum(got[NAMES[k]] * d))
+        assert abs(kern - num) <= tol * max(1.0, abs(num)), (k, kern, num)
+
+
+def test_bwd_full_size_sampled():
+    """Batch 4, 4096 tokens, 64 heads, P = 64, N = 128, SISO, bf16 (the prefill workload's size):
+    each (batch, head) is an independent problem, so the gradients of two sampled ones are
+    checked against the oracle run on that slice alone (dA, summed over the batch, excepted)."""
+    Bt, T, H, P, N, R = 4, 4096, 64, 64, 128, 1
+    w = synth.Workload("case", Bt, H, T, P, N, R, 64, "bf16")
+    inp = synth.make_inputs(w, seed=11)
+    gen = torch.Generator().manual_seed(12)
+    dy = torch.randn(inp["x"].shape, generator=gen).to(torch.bfloat16)
+    dfin = torch.randn((Bt, H, N, P), generator=gen)
+    got = _run(inp, R, dy, dfin)
+    rng = np.random.default_rng(13)
+    for b, h in ((0, 5), (3, 62)):
+        ref = dict(zip(grad.INPUTS, slice_bh(inp, b, h)))
+        sl = {NAMES[k]: (got[NAMES[k]][b:b + 1, :, h:h + 1] if k != "A" else got["dA"][h:h + 1])
+              for k in grad.INPUTS}
+        _directional_checks(sl, ref, oracle.f64(dy[b:b + 1, :, h:h + 1]), oracle.f64(dfin[b:b + 1, h:h + 1]),
+                            TOL_BWD["bf16"], rng)
 
 
 def test_bwd_rejects_unsupported_and_bad_arguments():
