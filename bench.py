@@ -91,6 +91,28 @@ def prefill_tc_flops(w: synth.Workload) -> float:
     return per_chunk * nchunk_tok
 
 
+# fp32 CUDA-core peak: 148 SMs x 128 FP32 lanes x 2 FLOPs per FMA x the maximum SM clock
+FP32_ALU_TFLOPS = 148 * 128 * 2 * 2032e6 / 1e12
+
+
+def bwd_flops(w: synth.Workload) -> float:
+    """FLOPs of one evaluation of the recurrence plus its adjoint, per state element and token:
+    forward v_t (2R), alpha h + beta v_{t-1} (3), rotation (3), + gamma v_t (2); adjoint gbar (2R + 2),
+    dv (3), r (2), dphi (2), ubar (3), dalpha / dbeta / dgamma dots (6), dC, dB, dX (6R).
+    The checkpoint recomputation the kernels add is not counted."""
+    R = w.rank
+    per_elem = (8 + 2 * R) + (18 + 8 * R)
+    return float(per_elem) * w.dstate * w.headdim * w.batch * w.seqlen * w.heads
+
+
+def bwd_bytes(w: synth.Workload) -> int:
+    """x, B, C, dy, dt, lambda, omega read once; dx, dB, dC, ddt, dlambda, domega written once (fp32)."""
+    e = io_bytes(w.io)
+    R, P, N = w.rank, w.headdim, w.dstate
+    per_ht = (2 * R * P + 2 * R * N) * e + 8 + (N // 2) * 4 + (R * P + 2 * R * N) * 4 + 8 + (N // 2) * 4
+    return per_ht * w.batch * w.seqlen * w.heads + 8 * w.heads
+
+
 def decode_bytes(b: int, H: int, P: int, N: int, R: int, io: str = "bf16") -> int:
     """State read + write (fp32), inputs and cache read, cache and y written."""
     e = io_bytes(io)
@@ -270,6 +292,30 @@ def time_prefill_prep(binding, w, dp, stream, steps, warmup, dist, device, bc=No
             raise binding.M3Error(st, "m3_scan_fwd_prep")
 
     return _time_calls(call, stream, steps, warmup, dist, device)
+
+
+def time_backward(binding, w, d, stream, steps, warmup, dist, device, seed=0):
+    """m3_scan_bwd on the prefill workload's inputs with a random dy (io dtype); device resident."""
+    gen = torch.Generator(device=device).manual_seed(1000 + seed)
+    dy = torch.randn(d["x"].shape, generator=gen, device=device).to(d["x"].dtype)
+    f = dict(dtype=torch.float32, device=device)
+    grads = {"dx": torch.empty(d["x"].shape, **f), "dB": torch.empty(d["B"].shape, **f),
+             "dC": torch.empty(d["C"].shape, **f), "ddt": torch.empty(d["dt"].shape, **f),
+             "dA": torch.empty(d["A"].shape, **f), "dlam": torch.empty(d["lam"].shape, **f),
+             "domega": torch.empty(d["omega"].shape, **f)}
+    nbytes = binding.m3_scan_bwd_workspace_size(w.batch, w.seqlen, w.heads, w.headdim, w.dstate, w.rank,
+                                                binding.io_code(d["x"].dtype))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    args = [d[k] for k in KEYS]
+
+    def call():
+        st = binding.m3_scan_bwd(*args, w.rank, dy, None, grads, ws, stream)
+        if st != 0:
+            raise binding.M3Error(st, "m3_scan_bwd")
+
+    sec, per = _time_calls(call, stream, steps, warmup, dist, device)
+    del grads, ws, dy
+    return sec, per
 
 
 def time_prefill_e2e(binding, w, host, stream, steps, warmup, dist, device, copy_streams=4):
@@ -516,6 +562,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prep", action="store_true", help="skip the pre-activation prefill measurement")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward-pass measurement")
     ap.add_argument("--workload", default=synth.SISO_1P5B.name, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--mode", choices=["all", "decode"], default="all",
                     help="decode: only the decode sweep (restricted by --decode-batch/--decode-rank)")
@@ -612,6 +659,24 @@ def main():
             "value": tokens * args.steps / gsec / 1e6, "unit": "Mtok/s", "ms_per_step": gsec / args.steps * 1e3,
             "algorithmic_bytes_per_call": gbytes, "roofline_frac": gbytes / (gms * 1e-3) / 1e9 / pk["hbm_gbs"]}
         del dp, bc, z
+
+    if not args.no_bwd:
+        # the backward pass (training) on the same inputs: three launches per call (the adjoint kernel
+        # over (batch*head, pair block), the dX and the per-token scalar finishing kernels)
+        bsteps = max(3, args.steps // 4)
+        with ClockSampler(local) as bclk:
+            bsec, bper = time_backward(binding, w, d, stream, bsteps, args.warmup, dist, device, seed=rank)
+        bms = sum(bper) / len(bper)
+        fl, by = bwd_flops(w), bwd_bytes(w)
+        line["backward"] = {
+            "value": tokens * bsteps / bsec / 1e6, "unit": "Mtok/s", "steps": bsteps,
+            "ms_per_step": bsec / bsteps * 1e3, "entry": "m3_scan_bwd", "gpu_launches": 3 * bsteps,
+            "roofline": {"bound": "alu", "achieved": fl / (bms * 1e-3) / 1e12, "peak": FP32_ALU_TFLOPS,
+                         "unit": "TFLOP/s", "frac": fl / (bms * 1e-3) / 1e12 / FP32_ALU_TFLOPS,
+                         "peak_source": "148 SMs x 128 FP32 lanes x 2 x 2032 MHz",
+                         "flops_per_call": fl},
+            "algorithmic_bytes_per_call": by, "hbm_frac": by / (bms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "clocks": bclk.summary()}
 
     if not args.no_e2e:
         host = {k: d[k].to("cpu").pin_memory() for k in KEYS}

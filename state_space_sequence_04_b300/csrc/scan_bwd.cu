@@ -36,12 +36,6 @@ namespace m3 {
 namespace {
 
 constexpr int kBwdThreads = 128;
-constexpr int kStageBatch = 8;   // loads in flight per thread while staging
-
-struct Staged {
-    float v;
-    int dst;
-};
 
 template <int R>
 struct kLg {
@@ -64,16 +58,22 @@ __host__ __device__ constexpr int round4(int v) { return (v + 3) & ~3; }
 //   sCS  [Q][PB] float2        (cos, sin) of phi_{t,j}
 //   sW   [Q][PB]               omega_{t,j}
 //   sABG [Q] float4            (alpha, beta, gamma, Delta)
-//   sDt, sL [Q]                Delta_t, lambda_t as loaded
 //   sDx  [Q][warps][R][P]      dX partial sums of each warp
 //   sScal[Q][PB][4]            per-pair (dalpha, dbeta, dgamma, omega dphi) partials
 //   sS   [Q][2][threads] float4 the chunk's recomputed states
+//   raw  [2] copy buffers: the loaded inputs of a chunk as stored in global memory (io dtype for B, X,
+//        C, dy; fp32 for omega, Delta, lambda), element for element in the order of sB .. sL; the next
+//        chunk's copies land in one while the current chunk is converted from the other
 struct BwdLayout {
     int PB, lgPB, lgP, threads, nPB;
-    int oB, oX, oC, oDy, oCS, oW, oABG, oDt, oL, oDx, oScal, oS, total;
+    int oB, oX, oC, oDy, oCS, oW, oABG, oDx, oScal, oS, oRaw, total;
+    int rX, rC, rDy, rW, rDt, rL, rawBytes;   // byte offsets within a copy buffer, and its size
+    int unitXY;                               // bytes per copy of an X / dy row (16 or 4)
 };
 
-BwdLayout bwd_layout(int P, int N, int R, int Q) {
+__host__ __device__ constexpr int round16(int v) { return (v + 15) & ~15; }
+
+BwdLayout bwd_layout(int P, int N, int R, int Q, int e) {
     BwdLayout L{};
     const int P4 = P / 4, NP2 = N / 2;
     int PB = kBwdThreads / P4;   // a power of two, the smallest one >= N/2 if that is smaller
@@ -101,19 +101,50 @@ BwdLayout bwd_layout(int P, int N, int R, int Q) {
     o += round4(Q * PB);
     L.oABG = o;
     o += Q * 4;
-    L.oDt = o;
-    o += round4(Q);
-    L.oL = o;
-    o += round4(Q);
     L.oDx = o;
     o += Q * (L.threads / 32) * R * P;
     L.oScal = o;
     o += Q * PB * 4;
     L.oS = o;
     o += Q * 2 * L.threads * 4;
+    int rb = round16((Q + 1) * PB * R * 2 * e);
+    L.rX = rb;
+    rb += round16((Q + 1) * R * P * e);
+    L.rC = rb;
+    rb += round16(Q * PB * R * 2 * e);
+    L.rDy = rb;
+    rb += round16(Q * R * P * e);
+    L.rW = rb;
+    rb += round16(Q * PB * 4);
+    L.rDt = rb;
+    rb += round16(Q * 4);
+    L.rL = rb;
+    rb += round16(Q * 4);
+    L.rawBytes = rb;
+    L.unitXY = (R * P * e) % 16 == 0 ? 16 : 4;
+    L.oRaw = o;
+    o += 2 * (rb / 4);
     L.total = o;
     return L;
 }
+
+__device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+// asynchronous global -> shared copies of 4, 8 or 16 bytes; ok == false writes zeros and reads nothing
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool ok) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src, bool ok) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 8 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool ok) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int NPEND>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(NPEND) : "memory"); }
 
 __device__ __forceinline__ float4 fma4b(float a, float4 x, float4 y) {
     return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
@@ -125,7 +156,7 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) { return a.x * b.x + a
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
 template <typename IO, int R>
-__global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(
+__global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     const IO* __restrict__ x, const IO* __restrict__ B, const IO* __restrict__ C, const float* __restrict__ dt,
     const float* __restrict__ A, const float* __restrict__ lam, const float* __restrict__ omega,
     const IO* __restrict__ dy, const float* __restrict__ dfin, float* __restrict__ dB, float* __restrict__ dC,
@@ -166,70 +197,88 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(
     const float a_h = A[h];
     auto tok = [&](int64_t t) { return (b * T + t) * H + h; };   // (batch, token, head) index
 
-    // The inputs of tokens t0 - 1 .. t0 + Q - 1 (zeros outside [0, T) and for pairs past N/2), then the
-    // angles and decays derived from them.  One flat index space over the raw sections; each thread
-    // issues kStageBatch independent loads before storing them, so their latencies overlap.
+    // Copies of the inputs of tokens t0 - 1 .. t0 + Q - 1 into copy buffer `buf` (zeros outside [0, T)
+    // and for pairs past N/2), asynchronous, as one commit group.
     const int lgPB = L.lgPB, lgRP = L.lgP + kLg<R>::v;
-    const int n1 = (Q + 1) * PB * R * 2, n2 = (Q + 1) * R * P, n3 = Q * PB * R * 2, n4 = Q * R * P, n5 = Q * PB;
-    const int ntot = n1 + n2 + n3 + n4 + n5 + 2 * Q;
-    // returns (value, destination offset in shared memory)
-    auto fetch = [&](int i, int64_t t0) -> Staged {
-        int dst;
-        if (i < n1 + n3) {   // B pairs (slot q <-> token t0 - 1 + q), then C pairs (slot q <-> token t0 + q)
-            const bool isB = i < n1;
-            const int k = isB ? i : i - n1;
-            const int e = k & 1, r = (k >> 1) & (R - 1), pl = (k >> (1 + kLg<R>::v)) & (PB - 1);
-            const int q = k >> (1 + kLg<R>::v + lgPB);
+    const int n1 = (Q + 1) * PB * R * 2, n2 = (Q + 1) * R * P, n3 = Q * PB * R * 2, n4 = Q * R * P;
+    char* const raw = reinterpret_cast<char*>(sm + L.oRaw);
+    constexpr int E = (int)sizeof(IO);
+    const int unit = L.unitXY, upr = R * P * E / unit;   // copies per X / dy row (a power of two)
+    int lgUpr = 0;
+    while ((1 << lgUpr) < upr) ++lgUpr;
+    auto issue = [&](int64_t t0, int buf) {
+        char* rb = raw + buf * L.rawBytes;
+        const int npB = (Q + 1) * PB * R, npC = Q * PB * R;   // (row pair, rank) copies of B, then of C
+        for (int i = tid; i < npB + npC; i += nt) {
+            const bool isB = i < npB;
+            const int k = isB ? i : i - npB;
+            const int r = k & (R - 1), pl = (k >> kLg<R>::v) & (PB - 1), q = k >> (kLg<R>::v + lgPB);
             const int64_t t = isB ? t0 - 1 + q : t0 + q;
             const int jp = pb * PB + pl;
-            dst = (isB ? L.oB : L.oC) + k;
-            return {(t >= 0 && t < T && jp < NP2) ? ld_io(isB ? B : C, (tok(t) * R + r) * N + 2 * jp + e) : 0.f, dst};
+            const bool ok = t >= 0 && t < T && jp < NP2;
+            const IO* src = (isB ? B : C) + (ok ? (tok(t) * R + r) * N + 2 * jp : 0);
+            char* dst = rb + (isB ? 0 : L.rC) + k * 2 * E;
+            if (E == 2)
+                cp_async4(dst, src, ok);
+            else
+                cp_async8(dst, src, ok);
         }
-        int k = i - n1 - n3;
-        if (k < n2 + n4) {   // X (slots from token t0 - 1), then dy (from token t0)
-            const bool isX = k < n2;
-            if (!isX) k -= n2;
-            const int q = k >> lgRP, rp = k & ((R * P) - 1);
+        for (int i = tid; i < (2 * Q + 1) * upr; i += nt) {   // X rows (slots from t0 - 1), then dy rows
+            const int row = i >> lgUpr, u = i & (upr - 1);
+            const bool isX = row <= Q;
+            const int q = isX ? row : row - (Q + 1);
             const int64_t t = isX ? t0 - 1 + q : t0 + q;
-            dst = (isX ? L.oX : L.oDy) + k;
-            return {(t >= 0 && t < T) ? ld_io(isX ? x : dy, tok(t) * R * P + rp) : 0.f, dst};
+            const bool ok = t >= 0 && t < T;
+            const char* src = reinterpret_cast<const char*>(isX ? x : dy) + (ok ? tok(t) * R * P * E + u * unit : 0);
+            char* dst = rb + (isX ? L.rX : L.rDy) + q * R * P * E + u * unit;
+            if (unit == 16)
+                cp_async16(dst, src, ok);
+            else
+                cp_async4(dst, src, ok);
         }
-        k -= n2 + n4;
-        if (k < n5) {
-            const int q = k >> lgPB, jp = pb * PB + (k & (PB - 1));
-            const int64_t t = t0 + q;
-            dst = L.oW + k;
-            return {(t < T && jp < NP2) ? omega[tok(t) * NP2 + jp] : 0.f, dst};
-        }
-        k -= n5;
-        const bool isD = k < Q;
-        const int q = isD ? k : k - Q;
-        dst = (isD ? L.oDt : L.oL) + q;
-        return {t0 + q < T ? (isD ? dt : lam)[tok(t0 + q)] : 0.f, dst};
-    };
-    auto stage = [&](int64_t t0) {
-        for (int base = 0; base < ntot; base += kStageBatch * nt) {
-            Staged v[kStageBatch];
-#pragma unroll
-            for (int u = 0; u < kStageBatch; ++u) {
-                const int i = base + u * nt + tid;
-                v[u] = i < ntot ? fetch(i, t0) : Staged{0.f, -1};
+        for (int i = tid; i < Q * PB + 2 * Q; i += nt) {   // omega, then Delta and lambda
+            const float* src;
+            char* dst;
+            bool ok;
+            if (i < Q * PB) {
+                const int q = i >> lgPB, jp = pb * PB + (i & (PB - 1));
+                ok = t0 + q < T && jp < NP2;
+                src = omega + (ok ? tok(t0 + q) * NP2 + jp : 0);
+                dst = rb + L.rW + 4 * i;
+            } else {
+                const int k = i - Q * PB, q = k < Q ? k : k - Q;
+                ok = t0 + q < T;
+                src = (k < Q ? dt : lam) + (ok ? tok(t0 + q) : 0);
+                dst = rb + (k < Q ? L.rDt : L.rL) + 4 * q;
             }
-#pragma unroll
-            for (int u = 0; u < kStageBatch; ++u)
-                if (v[u].dst >= 0) sm[v[u].dst] = v[u].v;
+            cp_async4(dst, src, ok);
         }
-        __syncthreads();
-        const float* sDt = sm + L.oDt;
-        const float* sL = sm + L.oL;
+        cp_async_commit();
+    };
+    // The copied inputs of buffer `buf` in fp32 working form, with the angles and decays they give.
+    auto convert = [&](int buf) {
+        const char* rb = raw + buf * L.rawBytes;
+        const IO* rB = reinterpret_cast<const IO*>(rb);
+        const IO* rX = reinterpret_cast<const IO*>(rb + L.rX);
+        const IO* rC = reinterpret_cast<const IO*>(rb + L.rC);
+        const IO* rDy = reinterpret_cast<const IO*>(rb + L.rDy);
+        const float* rW = reinterpret_cast<const float*>(rb + L.rW);
+        const float* rDt = reinterpret_cast<const float*>(rb + L.rDt);
+        const float* rL = reinterpret_cast<const float*>(rb + L.rL);
+        for (int i = tid; i < n1; i += nt) sB[i] = ld_io(rB, i);
+        for (int i = tid; i < n2; i += nt) sX[i] = ld_io(rX, i);
+        for (int i = tid; i < n3; i += nt) sC[i] = ld_io(rC, i);
+        for (int i = tid; i < n4; i += nt) sDy[i] = ld_io(rDy, i);
         for (int i = tid; i < Q * PB; i += nt) {
+            const float w = rW[i];
             float sn, cs;
-            sincosf(sDt[i >> lgPB] * sW[i], &sn, &cs);
+            sincosf(rDt[i >> lgPB] * w, &sn, &cs);
+            sW[i] = w;
             sCS[2 * i] = cs;
             sCS[2 * i + 1] = sn;
         }
         for (int q = tid; q < Q; q += nt) {
-            const float d = sDt[q], l = sL[q];
+            const float d = rDt[q], l = rL[q];
             const float al = expf(d * a_h);
             sABG[4 * q] = al;
             sABG[4 * q + 1] = (1.f - l) * d * al;
@@ -274,9 +323,18 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(
     // ---------------- forward sweep: the state entering chunks 1 .. nC-1 ----------------
     {
         float4 h0 = zero4(), h1 = zero4();
+        int buf = 0;
+        if (nC > 1) issue(0, 0);
         for (int64_t c = 0; c + 1 < nC; ++c) {
-            stage(c * Q);
+            if (c + 2 < nC)
+                issue((c + 1) * Q, buf ^ 1);   // the next chunk's copies overlap this chunk's work
+            else
+                cp_async_commit();
+            cp_async_wait<1>();
+            __syncthreads();   // every thread's copies of this chunk have landed
+            convert(buf);
             __syncthreads();
+            buf ^= 1;
             float4 vp0, vp1;
             outer(0, vp0, vp1);
 #pragma unroll
@@ -285,23 +343,33 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(
                 *ckrow(c + 1, 2 * j) = h0;
                 *ckrow(c + 1, 2 * j + 1) = h1;
             }
-            __syncthreads();   // the staged inputs are replaced next
+            __syncthreads();   // the working inputs are replaced next
         }
+        cp_async_wait<0>();
     }
 
     // ---------------- reverse sweep: the adjoint, chunk by chunk ----------------
     float4 ub0 = zero4(), ub1 = zero4();   // ubar_{t+1}
     float alpha_n = 0.f, beta_n = 0.f;     // alpha_{t+1}, beta_{t+1}
+    int buf = 0;
+    issue((nC - 1) * Q, 0);
     for (int64_t c = nC - 1; c >= 0; --c) {
         const int64_t t0 = c * Q;
         const int qn = (int)((T - t0) < Q ? (T - t0) : Q);
-        stage(t0);
+        if (c > 0)
+            issue((c - 1) * Q, buf ^ 1);
+        else
+            cp_async_commit();
         float4 hc0 = zero4(), hc1 = zero4();   // h_{t0-1}
         if (c > 0 && on) {
             hc0 = *ckrow(c, 2 * j);
             hc1 = *ckrow(c, 2 * j + 1);
         }
+        cp_async_wait<1>();
         __syncthreads();
+        convert(buf);
+        __syncthreads();
+        buf ^= 1;
         {
             float4 s0 = hc0, s1 = hc1, vp0, vp1;
             outer(0, vp0, vp1);
@@ -418,7 +486,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(
             for (int pl = 0; pl < pbn; ++pl) s += sScal[(q * PB + pl) * 4 + k];
             part_s[((int64_t)pb * BTH + tok(t0 + q)) * 4 + k] = s;
         }
-        // the next stage() writes none of sDx, sScal, sS; the barrier after it orders the reads above
+        // the next chunk's convert() writes none of sDx, sScal, sS; the barriers before it order the reads above
     }
 }
 
@@ -474,7 +542,7 @@ size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 BwdWs bwd_ws(const ScanDims& d) {
     const int Q = bwd_chunk(d.R);
-    const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, Q);
+    const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, Q, d.io == M3_DTYPE_BF16 ? 2 : 4);
     const size_t bh = (size_t)(d.batch * d.nheads), BTH = bh * (size_t)d.seqlen;
     const size_t nC = (size_t)((d.seqlen + Q - 1) / Q);
     BwdWs w{};
@@ -491,7 +559,7 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
                           const float* d_final, float* dx, float* dB, float* dC, float* ddt, float* dA,
                           float* dlambda, float* domega, void* workspace, cudaStream_t stream) {
     const int Q = bwd_chunk(d.R);
-    const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, Q);
+    const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, Q, (int)sizeof(IO));
     const int64_t bh = d.batch * d.nheads;
     cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * (size_t)d.nheads, stream);
     if (e != cudaSuccess || bh == 0 || d.seqlen == 0) return e;
@@ -543,7 +611,8 @@ bool bwd_supported(const ScanDims& d) {
     const int P4 = (int)(d.headdim / 4);
     if (P4 & (P4 - 1)) return false;   // a pair's column lanes are an aligned power-of-two group
     if (d.dstate < 2 || d.dstate % 2 || d.dstate > 256) return false;
-    const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, bwd_chunk(d.R));
+    const BwdLayout L =
+        bwd_layout((int)d.headdim, (int)d.dstate, d.R, bwd_chunk(d.R), d.io == M3_DTYPE_BF16 ? 2 : 4);
     return sizeof(float) * (size_t)L.total <= 200 * 1024;
 }
 
