@@ -146,13 +146,47 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int NPEND>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(NPEND) : "memory"); }
 
-__device__ __forceinline__ float4 fma4b(float a, float4 x, float4 y) {
-    return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+// Two-wide fp32 arithmetic (fma / mul / add / sub .f32x2): one instruction for two lanes, each lane
+// rounded exactly as the scalar instruction would round it.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
 }
-__device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
-__device__ __forceinline__ float4 sub4(float4 a, float4 b) { return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
-__device__ __forceinline__ float4 mul4(float a, float4 x) { return make_float4(a * x.x, a * x.y, a * x.z, a * x.w); }
-__device__ __forceinline__ float dot4(float4 a, float4 b) { return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w; }
+#define M3_BWD_OP2(name, op)                                                                                    \
+    __device__ __forceinline__ float2 name(float2 a, float2 b) {                                               \
+        float2 d;                                                                                              \
+        asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n " op                  \
+            " rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"                                                          \
+            : "=f"(d.x), "=f"(d.y)                                                                             \
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                                         \
+        return d;                                                                                              \
+    }
+M3_BWD_OP2(fmul2, "mul.rn.f32x2")
+M3_BWD_OP2(fadd2, "add.rn.f32x2")
+M3_BWD_OP2(fsub2, "sub.rn.f32x2")
+#undef M3_BWD_OP2
+
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+__device__ __forceinline__ float4 join4(float2 l, float2 h) { return make_float4(l.x, l.y, h.x, h.y); }
+
+__device__ __forceinline__ float4 fma4b(float a, float4 x, float4 y) {   // a x + y
+    const float2 aa = make_float2(a, a);
+    return join4(ffma2(aa, lo2(x), lo2(y)), ffma2(aa, hi2(x), hi2(y)));
+}
+__device__ __forceinline__ float4 add4(float4 a, float4 b) { return join4(fadd2(lo2(a), lo2(b)), fadd2(hi2(a), hi2(b))); }
+__device__ __forceinline__ float4 mul4(float a, float4 x) {
+    const float2 aa = make_float2(a, a);
+    return join4(fmul2(aa, lo2(x)), fmul2(aa, hi2(x)));
+}
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+    const float2 p = ffma2(hi2(a), hi2(b), fmul2(lo2(a), lo2(b)));
+    return p.x + p.y;
+}
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
 template <typename IO, int R>
@@ -307,13 +341,9 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
         const float4 u0 = fma4b(abg.x, s0, mul4(abg.y, vp0));
         const float4 u1 = fma4b(abg.x, s1, mul4(abg.y, vp1));
         const float2 cs = sCS2[q * PB + gc];
-        float4 o0, o1;
-        rot2(cs.x, cs.y, u0.x, u1.x, o0.x, o1.x);
-        rot2(cs.x, cs.y, u0.y, u1.y, o0.y, o1.y);
-        rot2(cs.x, cs.y, u0.z, u1.z, o0.z, o1.z);
-        rot2(cs.x, cs.y, u0.w, u1.w, o0.w, o1.w);
-        s0 = fma4b(abg.z, v0, o0);
-        s1 = fma4b(abg.z, v1, o1);
+        // R(phi) u: rows (c u0 - s u1, s u0 + c u1), then + gamma v
+        s0 = fma4b(abg.z, v0, fma4b(-cs.y, u1, mul4(cs.x, u0)));
+        s1 = fma4b(abg.z, v1, fma4b(cs.y, u0, mul4(cs.x, u1)));
         vp0 = v0;
         vp1 = v1;
     };
@@ -408,11 +438,11 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
             if (!on) g0 = g1 = zero4();
             const float4 dv0 = fma4b(gamma, g0, mul4(beta_n, ub0));
             const float4 dv1 = fma4b(gamma, g1, mul4(beta_n, ub1));
-            const float4 r0 = sub4(ht0, mul4(gamma, v0)), r1 = sub4(ht1, mul4(gamma, v1));   // R(phi_t) u_t
+            const float4 r0 = fma4b(-gamma, v0, ht0), r1 = fma4b(-gamma, v1, ht1);   // R(phi_t) u_t
             const float2 cs = sCS2[q * PB + gc];
             // ubar_t = R(phi_t)^T gbar_t
-            const float4 un0 = add4(mul4(cs.x, g0), mul4(cs.y, g1));
-            const float4 un1 = sub4(mul4(cs.x, g1), mul4(cs.y, g0));
+            const float4 un0 = fma4b(cs.y, g1, mul4(cs.x, g0));
+            const float4 un1 = fma4b(-cs.y, g0, mul4(cs.x, g1));
             // sums over this pair's columns: dphi, dalpha, dbeta, dgamma, then dC_t and dB_t per rank
             float red[4 + 4 * R];
             red[0] = dot4(g1, r0) - dot4(g0, r1);
