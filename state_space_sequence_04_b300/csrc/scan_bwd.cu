@@ -37,6 +37,15 @@ namespace {
 
 constexpr int kBwdThreads = 128;
 
+template <int V>
+struct Log2 {
+    static constexpr int v = V <= 1 ? 0 : 1 + Log2<V / 2>::v;
+};
+template <>
+struct Log2<1> {
+    static constexpr int v = 0;
+};
+
 template <int R>
 struct kLg {
     static constexpr int v = R == 1 ? 0 : (R == 2 ? 1 : (R == 4 ? 2 : 3));
@@ -189,7 +198,9 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
 }
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
-template <typename IO, int R>
+// P4T: P / 4 as a compile-time constant (with PB = kBwdThreads / P4T pairs per block and kBwdThreads
+// threads), or 0 for shapes taken at run time
+template <typename IO, int R, int P4T>
 __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     const IO* __restrict__ x, const IO* __restrict__ B, const IO* __restrict__ C, const float* __restrict__ dt,
     const float* __restrict__ A, const float* __restrict__ lam, const float* __restrict__ omega,
@@ -202,7 +213,8 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     const int pb = blockIdx.y;
     const int64_t b = bh / H;
     const int h = (int)(bh % H);
-    const int P4 = P >> 2, NP2 = N >> 1, PB = L.PB, nt = blockDim.x;
+    const int P4 = P4T ? P4T : P >> 2, NP2 = N >> 1, PP = 4 * P4;   // PP = P
+    const int PB = P4T ? kBwdThreads / P4T : L.PB, nt = P4T ? kBwdThreads : (int)blockDim.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
     const int c4 = tid % P4, gl = tid / P4;
     const int j = pb * PB + gl;
@@ -233,11 +245,13 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
 
     // Copies of the inputs of tokens t0 - 1 .. t0 + Q - 1 into copy buffer `buf` (zeros outside [0, T)
     // and for pairs past N/2), asynchronous, as one commit group.
-    const int lgPB = L.lgPB, lgRP = L.lgP + kLg<R>::v;
-    const int n1 = (Q + 1) * PB * R * 2, n2 = (Q + 1) * R * P, n3 = Q * PB * R * 2, n4 = Q * R * P;
+    const int lgPB = P4T ? Log2<kBwdThreads / (P4T ? P4T : 1)>::v : L.lgPB;
+    const int lgRP = (P4T ? Log2<4 * P4T>::v : L.lgP) + kLg<R>::v;
+    const int n1 = (Q + 1) * PB * R * 2, n2 = (Q + 1) * R * PP, n3 = Q * PB * R * 2, n4 = Q * R * PP;
     char* const raw = reinterpret_cast<char*>(sm + L.oRaw);
     constexpr int E = (int)sizeof(IO);
-    const int unit = L.unitXY, upr = R * P * E / unit;   // copies per X / dy row (a power of two)
+    const int unit = P4T ? ((R * 4 * P4T * E) % 16 == 0 ? 16 : 4) : L.unitXY;
+    const int upr = R * P4 * 4 * E / unit;   // copies per X / dy row (a power of two)
     int lgUpr = 0;
     while ((1 << lgUpr) < upr) ++lgUpr;
     auto issue = [&](int64_t t0, int buf) {
@@ -263,8 +277,8 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
             const int q = isX ? row : row - (Q + 1);
             const int64_t t = isX ? t0 - 1 + q : t0 + q;
             const bool ok = t >= 0 && t < T;
-            const char* src = reinterpret_cast<const char*>(isX ? x : dy) + (ok ? tok(t) * R * P * E + u * unit : 0);
-            char* dst = rb + (isX ? L.rX : L.rDy) + q * R * P * E + u * unit;
+            const char* src = reinterpret_cast<const char*>(isX ? x : dy) + (ok ? tok(t) * R * PP * E + u * unit : 0);
+            char* dst = rb + (isX ? L.rX : L.rDy) + q * R * PP * E + u * unit;
             if (unit == 16)
                 cp_async16(dst, src, ok);
             else
@@ -409,6 +423,10 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
                 sS4[(2 * q + 1) * nt + tid] = s1;
             }
         }
+        // this chunk's outputs of pair j: token t0 + q at q H R N (dC, dB) and q H N/2 (domega)
+        float* const dCc = dC + tok(t0) * R * N + 2 * j;
+        float* const dBc = dB + tok(t0) * R * N + 2 * j;
+        float* const domc = domega + tok(t0) * NP2 + j;
         float4 v0, v1;   // v of token t0 + q, carried down from the step after
         outer(qn, v0, v1);
 #pragma unroll 2
@@ -431,7 +449,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
                 g1 = fma4b(cc.y, dyr, g1);
             }
             if (t == T - 1 && dfin != nullptr && on) {
-                const float4* df4 = reinterpret_cast<const float4*>(dfin + bh * (int64_t)N * P);
+                const float4* df4 = reinterpret_cast<const float4*>(dfin + bh * (int64_t)N * PP);
                 g0 = add4(g0, df4[(2 * j) * P4 + c4]);
                 g1 = add4(g1, df4[(2 * j + 1) * P4 + c4]);
             }
@@ -470,13 +488,13 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
                 for (int i = 0; i < 4 + 4 * R; ++i) red[i] += __shfl_xor_sync(0xffffffffu, red[i], o);
             }
             if (on && c4 == 0) {
-                const int64_t tb = tok(t);
+                const int oq = q * H * R * N;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    *reinterpret_cast<float2*>(dC + (tb * R + r) * N + 2 * j) = make_float2(red[4 + 4 * r], red[5 + 4 * r]);
-                    *reinterpret_cast<float2*>(dB + (tb * R + r) * N + 2 * j) = make_float2(red[6 + 4 * r], red[7 + 4 * r]);
+                    *reinterpret_cast<float2*>(dCc + oq + r * N) = make_float2(red[4 + 4 * r], red[5 + 4 * r]);
+                    *reinterpret_cast<float2*>(dBc + oq + r * N) = make_float2(red[6 + 4 * r], red[7 + 4 * r]);
                 }
-                domega[tb * NP2 + j] = d * red[0];
+                domc[q * H * NP2] = d * red[0];
                 float* sc = sScal + (q * PB + gl) * 4;
                 sc[0] = red[1];
                 sc[1] = red[2];
@@ -503,18 +521,19 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
         }
         __syncthreads();
         // this pair block's partial sums of the chunk's tokens
-        for (int i = tid; i < qn * R * P; i += nt) {
-            const int q = i >> lgRP, rp = i & (R * P - 1);
+        float* pdx = part_dx + ((int64_t)pb * BTH + tok(t0)) * R * PP;   // token t0 + q at q H R P
+        for (int i = tid; i < qn * R * PP; i += nt) {
+            const int q = i >> lgRP, rp = i & (R * PP - 1);
             float sx = 0.f;
-            for (int w = 0; w < nw; ++w) sx += sDx[(q * nw + w) * R * P + rp];
-            part_dx[((int64_t)pb * BTH + tok(t0 + q)) * R * P + rp] = sx;
+            for (int w = 0; w < nw; ++w) sx += sDx[(q * nw + w) * R * PP + rp];
+            pdx[q * H * R * PP + rp] = sx;
         }
         const int pbn = (NP2 - pb * PB) < PB ? (NP2 - pb * PB) : PB;   // pairs of this block
         for (int i = tid; i < qn * 4; i += nt) {
             const int q = i >> 2, k = i & 3;
             float s = 0.f;
             for (int pl = 0; pl < pbn; ++pl) s += sScal[(q * PB + pl) * 4 + k];
-            part_s[((int64_t)pb * BTH + tok(t0 + q)) * 4 + k] = s;
+            part_s[((int64_t)pb * BTH + tok(t0) + q * H) * 4 + k] = s;
         }
         // the next chunk's convert() writes none of sDx, sScal, sS; the barriers before it order the reads above
     }
@@ -600,9 +619,10 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
     float* part_s = reinterpret_cast<float*>(ws + w.part_s);
     const size_t smem = sizeof(float) * (size_t)L.total;
     const dim3 grid((unsigned)bh, (unsigned)L.nPB);
+    const bool p64 = d.headdim == 64 && L.PB == kBwdThreads / 16;   // the compile-time P = 64 kernels
 #define M3_BWD_CASE(RR)                                                                                           \
     case RR: {                                                                                                    \
-        auto k = scan_bwd_kernel<IO, RR>;                                                                         \
+        auto k = p64 ? scan_bwd_kernel<IO, RR, 16> : scan_bwd_kernel<IO, RR, 0>;                                 \
         if (smem > 48 * 1024 &&                                                                                   \
             (e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) \
             return e;                                                                                             \

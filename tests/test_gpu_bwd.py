@@ -54,6 +54,7 @@ NAMES = {"x": "dx", "B": "dB", "C": "dC", "dt": "ddt", "A": "dA", "lam": "dlam",
     ("fp32", 1, 1, 19, 8, 6, 4),     # three chunks of 8
     ("fp32", 1, 1, 11, 4, 4, 8),     # three chunks of 4
     ("fp32", 1, 1, 20, 32, 40, 1),   # two pair blocks (16 + 4 pairs), two chunks
+    ("fp32", 1, 1, 12, 128, 8, 1),   # 32 column lanes per pair
 ])
 @pytest.mark.parametrize("with_final", [False, True])
 def test_bwd_small_every_element(io, Bt, H, T, P, N, R, with_final):
@@ -73,6 +74,8 @@ def test_bwd_small_every_element(io, Bt, H, T, P, N, R, with_final):
     ("fp32", 1, 2, 150, 64, 128, 1),
     ("bf16", 2, 2, 200, 64, 64, 4),
     ("fp32", 1, 4, 96, 32, 64, 2),
+    ("fp32", 1, 2, 64, 64, 32, 2),    # P = 64 with eight pairs per block: the compile-time-shape kernels
+    ("bf16", 1, 1, 40, 64, 16, 8),
 ])
 def test_bwd_larger_directional(io, Bt, H, T, P, N, R):
     w = synth.Workload("case", Bt, H, T, P, N, R, 64, io)
