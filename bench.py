@@ -26,6 +26,7 @@ independent: no collective on the data path), timing max-reduced over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -551,6 +552,27 @@ def run_reference(args):
     return 0
 
 
+def backward_leg(binding, w, d, args, stream, dist, device, local, ws, rank):
+    """The backward pass (training) on the prefill inputs: three launches per call (the adjoint
+    kernel over (batch*head, pair block), the dX and the per-token scalar finishing kernels)."""
+    bsteps = max(3, args.steps // 4)
+    with ClockSampler(local) as bclk:
+        bsec, bper = time_backward(binding, w, d, stream, bsteps, args.warmup, dist, device, seed=rank)
+    bms = sum(bper) / len(bper)
+    fl, by = bwd_flops(w), bwd_bytes(w)
+    pk = peaks()
+    return {
+        "value": w.batch * w.seqlen * ws * bsteps / bsec / 1e6, "unit": "Mtok/s", "steps": bsteps,
+        "ms_per_step": bsec / bsteps * 1e3, "entry": "m3_scan_bwd", "gpu_launches": 3 * bsteps,
+        "config": {"batch": w.batch, "seqlen": w.seqlen, "heads": w.heads, "headdim": w.headdim,
+                   "dstate": w.dstate, "rank": w.rank, "io": w.io},
+        "roofline": {"bound": "alu", "achieved": fl / (bms * 1e-3) / 1e12, "peak": FP32_ALU_TFLOPS,
+                     "unit": "TFLOP/s", "frac": fl / (bms * 1e-3) / 1e12 / FP32_ALU_TFLOPS,
+                     "peak_source": "148 SMs x 128 FP32 lanes x 2 x 2032 MHz", "flops_per_call": fl},
+        "algorithmic_bytes_per_call": by, "hbm_frac": by / (bms * 1e-3) / 1e9 / pk["hbm_gbs"],
+        "clocks": bclk.summary()}
+
+
 # ---------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
@@ -564,8 +586,11 @@ def main():
     ap.add_argument("--no-prep", action="store_true", help="skip the pre-activation prefill measurement")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward-pass measurement")
     ap.add_argument("--workload", default=synth.SISO_1P5B.name, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--mode", choices=["all", "decode"], default="all",
-                    help="decode: only the decode sweep (restricted by --decode-batch/--decode-rank)")
+    ap.add_argument("--mode", choices=["all", "decode", "bwd"], default="all",
+                    help="decode: only the decode sweep (restricted by --decode-batch/--decode-rank); "
+                         "bwd: only the backward pass (sizes overridable by --bwd-batch/--bwd-seqlen)")
+    ap.add_argument("--bwd-batch", type=int, default=None)
+    ap.add_argument("--bwd-seqlen", type=int, default=None)
     ap.add_argument("--decode-batch", type=int, default=None)
     ap.add_argument("--decode-rank", type=int, default=None)
     ap.add_argument("--decode-steps", type=int, default=synth.DECODE_STEPS)
@@ -588,6 +613,15 @@ def main():
     if args.mode == "decode":
         line = {"metric": METRIC, "mode": "decode",
                 "decode": decode_sweep(binding, args, stream, device, pk)}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    if args.mode == "bwd":
+        wb = dataclasses.replace(w, batch=args.bwd_batch or w.batch, seqlen=args.bwd_seqlen or w.seqlen)
+        db = synth.make_inputs(wb, seed=rank, device=device)
+        line = {"metric": METRIC, "mode": "bwd", "workload": w.name,
+                "backward": backward_leg(binding, wb, db, args, stream, dist, device, local, ws, rank)}
         if rank == 0:
             print(json.dumps(line), flush=True)
         return 0
@@ -661,22 +695,7 @@ def main():
         del dp, bc, z
 
     if not args.no_bwd:
-        # the backward pass (training) on the same inputs: three launches per call (the adjoint kernel
-        # over (batch*head, pair block), the dX and the per-token scalar finishing kernels)
-        bsteps = max(3, args.steps // 4)
-        with ClockSampler(local) as bclk:
-            bsec, bper = time_backward(binding, w, d, stream, bsteps, args.warmup, dist, device, seed=rank)
-        bms = sum(bper) / len(bper)
-        fl, by = bwd_flops(w), bwd_bytes(w)
-        line["backward"] = {
-            "value": tokens * bsteps / bsec / 1e6, "unit": "Mtok/s", "steps": bsteps,
-            "ms_per_step": bsec / bsteps * 1e3, "entry": "m3_scan_bwd", "gpu_launches": 3 * bsteps,
-            "roofline": {"bound": "alu", "achieved": fl / (bms * 1e-3) / 1e12, "peak": FP32_ALU_TFLOPS,
-                         "unit": "TFLOP/s", "frac": fl / (bms * 1e-3) / 1e12 / FP32_ALU_TFLOPS,
-                         "peak_source": "148 SMs x 128 FP32 lanes x 2 x 2032 MHz",
-                         "flops_per_call": fl},
-            "algorithmic_bytes_per_call": by, "hbm_frac": by / (bms * 1e-3) / 1e9 / pk["hbm_gbs"],
-            "clocks": bclk.summary()}
+        line["backward"] = backward_leg(binding, w, d, args, stream, dist, device, local, ws, rank)
 
     if not args.no_e2e:
         host = {k: d[k].to("cpu").pin_memory() for k in KEYS}
