@@ -209,8 +209,10 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     int64_t T, int H, int P, int N, const BwdLayout L) {
     constexpr int Q = BwdChunk<R>::Q;
     extern __shared__ __align__(16) float sm[];
-    const int64_t bh = blockIdx.x;
-    const int pb = blockIdx.y;
+    // the pair blocks of one (batch, head) are neighbours in launch order, so they run together and
+    // share their X, dy, Delta, lambda reads in L2
+    const int64_t bh = blockIdx.x / L.nPB;
+    const int pb = (int)(blockIdx.x % L.nPB);
     const int64_t b = bh / H;
     const int h = (int)(bh % H);
     const int P4 = P4T ? P4T : P >> 2, NP2 = N >> 1, PP = 4 * P4;   // PP = P
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     const bool on = gl < PB && j < NP2;
     const int gc = gl < PB ? gl : 0;   // shared-memory slot of this thread's pair (idle threads read slot 0)
     const int64_t nC = (T + Q - 1) / Q;
-    const int64_t BTH = (int64_t)gridDim.x / H * T * H;
+    const int64_t BTH = (int64_t)gridDim.x / L.nPB * T;   // batch * T * H
 
     float* sB = sm + L.oB;
     float* sX = sm + L.oX;
@@ -254,9 +256,10 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     const int upr = R * P4 * 4 * E / unit;   // copies per X / dy row (a power of two)
     int lgUpr = 0;
     while ((1 << lgUpr) < upr) ++lgUpr;
-    auto issue = [&](int64_t t0, int buf) {
+    // fwd: the forward sweep's copies only (no C, no dy)
+    auto issue = [&](int64_t t0, int buf, bool fwd) {
         char* rb = raw + buf * L.rawBytes;
-        const int npB = (Q + 1) * PB * R, npC = Q * PB * R;   // (row pair, rank) copies of B, then of C
+        const int npB = (Q + 1) * PB * R, npC = fwd ? 0 : Q * PB * R;   // (row pair, rank) copies of B, then C
         for (int i = tid; i < npB + npC; i += nt) {
             const bool isB = i < npB;
             const int k = isB ? i : i - npB;
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
             else
                 cp_async8(dst, src, ok);
         }
-        for (int i = tid; i < (2 * Q + 1) * upr; i += nt) {   // X rows (slots from t0 - 1), then dy rows
+        for (int i = tid; i < (fwd ? Q + 1 : 2 * Q + 1) * upr; i += nt) {   // X rows (from t0 - 1), then dy rows
             const int row = i >> lgUpr, u = i & (upr - 1);
             const bool isX = row <= Q;
             const int q = isX ? row : row - (Q + 1);
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
         cp_async_commit();
     };
     // The copied inputs of buffer `buf` in fp32 working form, with the angles and decays they give.
-    auto convert = [&](int buf) {
+    auto convert = [&](int buf, bool fwd) {
         const char* rb = raw + buf * L.rawBytes;
         const IO* rB = reinterpret_cast<const IO*>(rb);
         const IO* rX = reinterpret_cast<const IO*>(rb + L.rX);
@@ -315,8 +318,10 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
         const float* rL = reinterpret_cast<const float*>(rb + L.rL);
         for (int i = tid; i < n1; i += nt) sB[i] = ld_io(rB, i);
         for (int i = tid; i < n2; i += nt) sX[i] = ld_io(rX, i);
-        for (int i = tid; i < n3; i += nt) sC[i] = ld_io(rC, i);
-        for (int i = tid; i < n4; i += nt) sDy[i] = ld_io(rDy, i);
+        if (!fwd) {
+            for (int i = tid; i < n3; i += nt) sC[i] = ld_io(rC, i);
+            for (int i = tid; i < n4; i += nt) sDy[i] = ld_io(rDy, i);
+        }
         for (int i = tid; i < Q * PB; i += nt) {
             const float w = rW[i];
             float sn, cs;
@@ -368,15 +373,15 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     {
         float4 h0 = zero4(), h1 = zero4();
         int buf = 0;
-        if (nC > 1) issue(0, 0);
+        if (nC > 1) issue(0, 0, true);
         for (int64_t c = 0; c + 1 < nC; ++c) {
             if (c + 2 < nC)
-                issue((c + 1) * Q, buf ^ 1);   // the next chunk's copies overlap this chunk's work
+                issue((c + 1) * Q, buf ^ 1, true);   // the next chunk's copies overlap this chunk's work
             else
                 cp_async_commit();
             cp_async_wait<1>();
             __syncthreads();   // every thread's copies of this chunk have landed
-            convert(buf);
+            convert(buf, true);
             __syncthreads();
             buf ^= 1;
             float4 vp0, vp1;
@@ -396,12 +401,12 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     float4 ub0 = zero4(), ub1 = zero4();   // ubar_{t+1}
     float alpha_n = 0.f, beta_n = 0.f;     // alpha_{t+1}, beta_{t+1}
     int buf = 0;
-    issue((nC - 1) * Q, 0);
+    issue((nC - 1) * Q, 0, false);
     for (int64_t c = nC - 1; c >= 0; --c) {
         const int64_t t0 = c * Q;
         const int qn = (int)((T - t0) < Q ? (T - t0) : Q);
         if (c > 0)
-            issue((c - 1) * Q, buf ^ 1);
+            issue((c - 1) * Q, buf ^ 1, false);
         else
             cp_async_commit();
         float4 hc0 = zero4(), hc1 = zero4();   // h_{t0-1}
@@ -411,7 +416,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
         }
         cp_async_wait<1>();
         __syncthreads();
-        convert(buf);
+        convert(buf, false);
         __syncthreads();
         buf ^= 1;
         {
@@ -618,7 +623,7 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
     float* part_dx = reinterpret_cast<float*>(ws + w.part_dx);
     float* part_s = reinterpret_cast<float*>(ws + w.part_s);
     const size_t smem = sizeof(float) * (size_t)L.total;
-    const dim3 grid((unsigned)bh, (unsigned)L.nPB);
+    const unsigned grid = (unsigned)(bh * L.nPB);   // (batch*head, pair block), pair block fastest
     const bool p64 = d.headdim == 64 && L.PB == kBwdThreads / 16;   // the compile-time P = 64 kernels
 #define M3_BWD_CASE(RR)                                                                                           \
     case RR: {                                                                                                    \
@@ -663,6 +668,7 @@ bool bwd_supported(const ScanDims& d) {
     if (d.dstate < 2 || d.dstate % 2 || d.dstate > 256) return false;
     const BwdLayout L =
         bwd_layout((int)d.headdim, (int)d.dstate, d.R, bwd_chunk(d.R), d.io == M3_DTYPE_BF16 ? 2 : 4);
+    if ((int64_t)L.nPB * d.batch * d.nheads > (int64_t)INT32_MAX) return false;   // one-dimensional grid
     return sizeof(float) * (size_t)L.total <= 200 * 1024;
 }
 
