@@ -264,8 +264,8 @@ M3_API int m3_decode_step_prep(float* state, const void* x_t, const void* B_t, v
  *   ddt, dlambda  out [batch, T, H] fp32;  domega  out [batch, T, H, N/2] fp32
  *   dA        out [H] fp32 (summed over batch and tokens)
  *   workspace: m3_scan_bwd_workspace_size bytes, 256-byte aligned: the
- *            state entering every chunk of Q tokens (Q = 16 for R <= 2,
- *            8 for R = 4, 4 for R = 8; batch * H * ceil(T/Q) * N * P fp32)
+ *            state entering every chunk of Q tokens (Q = 8 for R <= 2,
+ *            4 for R >= 4; batch * H * ceil(T/Q) * N * P fp32)
  *            and per-pair-block partial sums of dx and of four per-token
  *            scalars (fp32).
  * CUDA cores, one CTA per (batch, head, block of state pairs): a forward

@@ -25,9 +25,12 @@
 // them and applies the chain rule for Delta, lambda and A.
 //
 // Checkpointing: a forward sweep stores the state entering every chunk of Q
-// tokens; the reverse sweep then, chunk by chunk from the last, stages the
-// chunk's inputs in shared memory, recomputes its Q states from the
-// checkpoint into shared memory, and runs the adjoint over the chunk.
+// tokens; the reverse sweep then, chunk by chunk from the last, recomputes the
+// chunk's Q states from its checkpoint into shared memory and runs the adjoint
+// over the chunk.  Both sweeps receive a chunk's inputs by cp.async into one
+// half of a double buffer while the previous chunk is processed, and convert
+// them to fp32 working copies.  Arithmetic is fp32, two lanes per instruction
+// (f32x2), each lane rounded as the scalar instruction rounds it.
 #include <cuda_bf16.h>
 
 #include "m3_common.cuh"
