@@ -286,6 +286,36 @@ M3_API int m3_scan_bwd(const void* x, const void* B, const void* C, const float*
                        int io_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward pass of m3_scan_fwd_prep without its B/C normalisation and gate:
+ * the gradients with respect to the pre-activations of Delta_t =
+ * softplus(dt_raw_t + dt_bias_h) and lambda_t = sigmoid(u_t), and to the
+ * per-token decay generators A_t (Table 1's time-varying discretisations).
+ *
+ *   x, B, C, omega, R, sizes, io_dtype, dy, d_final: as m3_scan_bwd
+ *   dt_raw, A, u   [batch, T, H] fp32 (A one value per token, as in
+ *                  m3_scan_fwd_prep)
+ *   params         nullable; only dt_bias may be set (bc_norm, the gains, the
+ *                  biases and z must be 0 / NULL, else M3_ERR_UNSUPPORTED)
+ *   dx, dB, dC, domega  out, as m3_scan_bwd
+ *   ddt_raw, dA, du     out [batch, T, H] fp32
+ *   ddt_bias       nullable out [H] fp32: sum over batch and tokens of ddt_raw
+ *                  (accumulated with atomics)
+ *   workspace: m3_scan_bwd_prep_workspace_size bytes (m3_scan_bwd's, plus
+ *            Delta and lambda: 2 * batch * T * H fp32), 256-byte aligned.
+ * Delta and lambda are derived with the forward entry's own functions; the
+ * derivative of softplus is sigmoid, that of sigmoid is lambda (1 - lambda).
+ * Sizes and errors as m3_scan_bwd.
+ */
+M3_API size_t m3_scan_bwd_prep_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                                              int64_t dstate, int R, int io_dtype);
+M3_API int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const float* dt_raw, const float* A,
+                            const float* u, const float* omega, int R, const void* dy, const float* d_final,
+                            float* dx, float* dB, float* dC, float* ddt_raw, float* dA, float* du, float* domega,
+                            float* ddt_bias, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                            int64_t dstate, int io_dtype, const m3_prep_params* params, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * Sticky device-side error word of m3_decode_step, which takes no workspace:
  * M3_OK, or M3_ERR_TIMEOUT once a bounded wait inside a decode kernel gave up
  * (the outputs of that call are then not valid).  Reading it synchronises

@@ -12,28 +12,37 @@ Propositions 2-4); its backward pass for training is the last of the chunked
 algorithm's uses listed in section 3.3.
 
 ``grad_fd`` perturbs every element (small problems only); ``directional`` gives
-the derivative of L along one direction per input, for larger problems.
+the derivative of L along one direction per input, for larger problems.  With
+``prep=True`` the loss runs ``oracle.scan_prep`` on pre-activations instead
+(Delta = softplus(dt_raw + dt_bias), lambda = sigmoid(u), A per token; the
+time-varying discretisations of the page's Table 1), over PREP_INPUTS.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import f64, scan
+from . import f64, scan, scan_prep
 
 INPUTS = ("x", "B", "C", "dt", "A", "lam", "omega")
+PREP_INPUTS = ("x", "B", "C", "dt_raw", "dt_bias", "A", "u", "omega")
 
 
-def loss(inp: dict, dy, d_final=None) -> float:
-    y, hT, _ = scan(*[inp[k] for k in INPUTS])
+def loss(inp: dict, dy, d_final=None, prep: bool = False) -> float:
+    if prep:
+        y, hT, _ = scan_prep(*[inp[k] for k in PREP_INPUTS])
+    else:
+        y, hT, _ = scan(*[inp[k] for k in INPUTS])
     val = float(np.sum(y * f64(dy)))
     if d_final is not None:
         val += float(np.sum(hT * f64(d_final)))
     return val
 
 
-def grad_fd(inp: dict, dy, d_final=None, eps: float = 1e-6, keys=INPUTS) -> dict:
+def grad_fd(inp: dict, dy, d_final=None, eps: float = 1e-6, keys=None, prep: bool = False) -> dict:
     """dL/d(input) for every element of the listed inputs, central differences with step eps."""
-    base = {k: f64(inp[k]).copy() for k in INPUTS}
+    names = PREP_INPUTS if prep else INPUTS
+    keys = names if keys is None else keys
+    base = {k: f64(inp[k]).copy() for k in names}
     out = {}
     for k in keys:
         g = np.zeros_like(base[k])
@@ -42,22 +51,22 @@ def grad_fd(inp: dict, dy, d_final=None, eps: float = 1e-6, keys=INPUTS) -> dict
         for i in range(flat.size):
             keep = flat[i]
             flat[i] = keep + eps
-            lp = loss(base, dy, d_final)
+            lp = loss(base, dy, d_final, prep)
             flat[i] = keep - eps
-            lm = loss(base, dy, d_final)
+            lm = loss(base, dy, d_final, prep)
             flat[i] = keep
             gf[i] = (lp - lm) / (2.0 * eps)
         out[k] = g
     return out
 
 
-def directional(inp: dict, key: str, v, dy, d_final=None, eps: float = 1e-6) -> float:
+def directional(inp: dict, key: str, v, dy, d_final=None, eps: float = 1e-6, prep: bool = False) -> float:
     """d/ds L(input[key] + s v) at s = 0, central differences with step eps."""
-    base = {k: f64(inp[k]).copy() for k in INPUTS}
+    base = {k: f64(inp[k]).copy() for k in (PREP_INPUTS if prep else INPUTS)}
     v = f64(v)
     keep = base[key].copy()
     base[key] = keep + eps * v
-    lp = loss(base, dy, d_final)
+    lp = loss(base, dy, d_final, prep)
     base[key] = keep - eps * v
-    lm = loss(base, dy, d_final)
+    lm = loss(base, dy, d_final, prep)
     return (lp - lm) / (2.0 * eps)

@@ -225,6 +225,43 @@ int m3_scan_bwd(const void* x, const void* B, const void* C, const float* dt, co
                                            dlambda, domega, workspace, static_cast<cudaStream_t>(stream)));
 }
 
+size_t m3_scan_bwd_prep_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                                       int64_t dstate, int R, int io_dtype) {
+    const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, 64, io_dtype};
+    if (!ok_io(io_dtype) || batch < 0 || seqlen < 0 || nheads < 1 || !m3::bwd_supported(d)) return 0;
+    return m3::bwd_prep_workspace_size(d);
+}
+
+int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const float* dt_raw, const float* A,
+                     const float* u, const float* omega, int R, const void* dy, const float* d_final, float* dx,
+                     float* dB, float* dC, float* ddt_raw, float* dA, float* du, float* domega, float* ddt_bias,
+                     int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate, int io_dtype,
+                     const m3_prep_params* params, void* workspace, size_t workspace_bytes, void* stream) {
+    const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, 64, io_dtype};
+    if (!ok_io(io_dtype)) return M3_ERR_INVALID_ARG;
+    if (batch < 0 || seqlen < 0 || nheads < 1 || headdim < 1 || dstate < 2 || dstate % 2 || R < 1)
+        return M3_ERR_INVALID_ARG;
+    if (params != nullptr && !aligned16(params)) return M3_ERR_INVALID_ARG;
+    const float* dt_bias = params != nullptr ? params->dt_bias : nullptr;
+    if (!ok_nullable(dt_bias) || !ok_nullable(ddt_bias) || !ok_nullable(d_final)) return M3_ERR_INVALID_ARG;
+    if (params != nullptr && (params->bc_norm || params->B_gain || params->C_gain || params->B_bias ||
+                              params->C_bias || params->z))
+        return M3_ERR_UNSUPPORTED;   // no backward through the B/C normalisation or the gate
+    if (batch * nheads > (int64_t)INT32_MAX || seqlen > (int64_t)INT32_MAX) return M3_ERR_UNSUPPORTED;
+    if (!m3::bwd_supported(d)) return M3_ERR_UNSUPPORTED;
+    if (batch > 0 && seqlen > 0) {
+        const void* ptrs[] = {x, B, C, dt_raw, A, u, omega, dy, dx, dB, dC, ddt_raw, dA, du, domega};
+        for (const void* q : ptrs)
+            if (!ok_ptr(q)) return M3_ERR_INVALID_ARG;
+        const size_t need = m3::bwd_prep_workspace_size(d);
+        if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return M3_ERR_WORKSPACE;
+    }
+    return cuda_status(m3::launch_scan_bwd_prep(d, x, B, C, dt_raw, dt_bias, A, u, omega, dy, d_final, dx, dB, dC,
+                                                ddt_raw, dA, du, domega, ddt_bias, workspace,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 int m3_state_passing(float* chunk_states, const float* chunk_logdecay, const float* chunk_angle,
                      const float* init_state, float* final_state, int64_t batch, int64_t nheads, int64_t nchunks,
                      int64_t dstate, int64_t headdim, void* stream) {

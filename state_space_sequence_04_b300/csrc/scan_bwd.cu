@@ -79,7 +79,7 @@ __host__ __device__ constexpr int round4(int v) { return (v + 3) & ~3; }
 struct BwdLayout {
     int PB, lgPB, lgP, threads, nPB;
     int oB, oX, oC, oDy, oCS, oW, oABG, oDx, oScal, oS, oRaw, total;
-    int rX, rC, rDy, rW, rDt, rL, rawBytes;   // byte offsets within a copy buffer, and its size
+    int rX, rC, rDy, rW, rDt, rL, rA, rawBytes;   // byte offsets within a copy buffer, and its size
     int unitXY;                               // bytes per copy of an X / dy row (16 or 4)
 };
 
@@ -132,6 +132,8 @@ BwdLayout bwd_layout(int P, int N, int R, int Q, int e) {
     rb += round16(Q * 4);
     L.rL = rb;
     rb += round16(Q * 4);
+    L.rA = rb;
+    rb += round16(Q * 4);
     L.rawBytes = rb;
     L.unitXY = (R * P * e) % 16 == 0 ? 16 : 4;
     L.oRaw = o;
@@ -158,7 +160,7 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int NPEND>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(NPEND) : "memory"); }
 
-// Two-wide fp32 arithmetic (fma / mul / add / sub .f32x2): one instruction for two lanes, each lane
+// Two-wide fp32 arithmetic (fma / mul / add .f32x2): one instruction for two lanes, each lane
 // rounded exactly as the scalar instruction would round it.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     float2 d;
@@ -179,7 +181,6 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     }
 M3_BWD_OP2(fmul2, "mul.rn.f32x2")
 M3_BWD_OP2(fadd2, "add.rn.f32x2")
-M3_BWD_OP2(fsub2, "sub.rn.f32x2")
 #undef M3_BWD_OP2
 
 __device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
@@ -201,15 +202,24 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
 }
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
+// The per-token decay generators of the pre-activation entry; an empty parameter for the plain entry, so
+// that the plain kernels' parameter block and code are those of a kernel without the option.
+template <bool ON>
+struct TokA {
+    const float* __restrict__ p;
+};
+template <>
+struct TokA<false> {};
+
 // P4T: P / 4 as a compile-time constant (with PB = kBwdThreads / P4T pairs per block and kBwdThreads
-// threads), or 0 for shapes taken at run time
-template <typename IO, int R, int P4T>
+// threads), or 0 for shapes taken at run time; TOKA: A per token (TokA<true>) or per head
+template <typename IO, int R, int P4T, bool TOKA>
 __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     const IO* __restrict__ x, const IO* __restrict__ B, const IO* __restrict__ C, const float* __restrict__ dt,
     const float* __restrict__ A, const float* __restrict__ lam, const float* __restrict__ omega,
     const IO* __restrict__ dy, const float* __restrict__ dfin, float* __restrict__ dB, float* __restrict__ dC,
     float* __restrict__ domega, float* __restrict__ ckpt, float* __restrict__ part_dx, float* __restrict__ part_s,
-    int64_t T, int H, int P, int N, const BwdLayout L) {
+    int64_t T, int H, int P, int N, const BwdLayout L, const TokA<TOKA> atok) {
     constexpr int Q = BwdChunk<R>::Q;
     extern __shared__ __align__(16) float sm[];
     // the pair blocks of one (batch, head) are neighbours in launch order, so they run together and
@@ -245,7 +255,8 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     const float2* sCS2 = reinterpret_cast<const float2*>(sCS);
     const float4* sABG4 = reinterpret_cast<const float4*>(sABG);
 
-    const float a_h = A[h];
+    float a_h = 0.f;   // one decay generator per head, or A_t per token (staged with the chunk)
+    if constexpr (!TOKA) a_h = A[h];
     auto tok = [&](int64_t t) { return (b * T + t) * H + h; };   // (batch, token, head) index
 
     // Copies of the inputs of tokens t0 - 1 .. t0 + Q - 1 into copy buffer `buf` (zeros outside [0, T)
@@ -290,7 +301,8 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
             else
                 cp_async4(dst, src, ok);
         }
-        for (int i = tid; i < Q * PB + 2 * Q; i += nt) {   // omega, then Delta and lambda
+        constexpr int nscal = TOKA ? 3 * Q : 2 * Q;
+        for (int i = tid; i < Q * PB + nscal; i += nt) {   // omega, then Delta, lambda (and A_t)
             const float* src;
             char* dst;
             bool ok;
@@ -300,10 +312,12 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
                 src = omega + (ok ? tok(t0 + q) * NP2 + jp : 0);
                 dst = rb + L.rW + 4 * i;
             } else {
-                const int k = i - Q * PB, q = k < Q ? k : k - Q;
+                const int k = i - Q * PB, sec = k / Q, q = k - sec * Q;
                 ok = t0 + q < T;
-                src = (k < Q ? dt : lam) + (ok ? tok(t0 + q) : 0);
-                dst = rb + (k < Q ? L.rDt : L.rL) + 4 * q;
+                const float* base = sec == 0 ? dt : lam;
+                if constexpr (TOKA) base = sec == 2 ? atok.p : base;
+                src = base + (ok ? tok(t0 + q) : 0);
+                dst = rb + (sec == 0 ? L.rDt : sec == 1 ? L.rL : L.rA) + 4 * q;
             }
             cp_async4(dst, src, ok);
         }
@@ -319,6 +333,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
         const float* rW = reinterpret_cast<const float*>(rb + L.rW);
         const float* rDt = reinterpret_cast<const float*>(rb + L.rDt);
         const float* rL = reinterpret_cast<const float*>(rb + L.rL);
+        const float* rA = reinterpret_cast<const float*>(rb + L.rA);
         for (int i = tid; i < n1; i += nt) sB[i] = ld_io(rB, i);
         for (int i = tid; i < n2; i += nt) sX[i] = ld_io(rX, i);
         if (!fwd) {
@@ -335,7 +350,9 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
         }
         for (int q = tid; q < Q; q += nt) {
             const float d = rDt[q], l = rL[q];
-            const float al = expf(d * a_h);
+            float a = a_h;
+            if constexpr (TOKA) a = rA[q];
+            const float al = expf(d * a);
             sABG[4 * q] = al;
             sABG[4 * q + 1] = (1.f - l) * d * al;
             sABG[4 * q + 2] = l * d;
@@ -589,10 +606,57 @@ __global__ void bwd_finish_scalars(const float4* __restrict__ part_s, const floa
     }
 }
 
+// The same on pre-activations: Delta = softplus(z), z = dt_raw + dt_bias[h], lambda = sigmoid(u), and A_t
+// per token; then dz = dDelta sigmoid(z) (softplus' = sigmoid) gives ddt_raw and, summed over batch and
+// tokens, ddt_bias; du = dlambda lambda (1 - lambda); dA_t per token.
+__global__ void bwd_finish_scalars_prep(const float4* __restrict__ part_s, const float* __restrict__ dt_eff,
+                                        const float* __restrict__ lam_eff, const float* __restrict__ A_tok,
+                                        const float* __restrict__ dt_raw, const float* __restrict__ dt_bias,
+                                        float* __restrict__ ddt_raw, float* __restrict__ du, float* __restrict__ dA_tok,
+                                        float* __restrict__ ddt_bias, int64_t batch, int64_t T, int H, int nPB) {
+    __shared__ float red[32];
+    const int h = blockIdx.x;
+    const float bias = dt_bias != nullptr ? dt_bias[h] : 0.f;
+    const int64_t BTH = batch * T * H;
+    float acc = 0.f;
+    for (int64_t b = blockIdx.y; b < batch; b += gridDim.y) {
+        for (int64_t t = threadIdx.x; t < T; t += blockDim.x) {
+            const int64_t tk = (b * T + t) * H + h;
+            float4 s = part_s[tk];
+            for (int k = 1; k < nPB; ++k) s = add4(s, part_s[k * BTH + tk]);
+            const float d = dt_eff[tk], l = lam_eff[tk], a = A_tok[tk], al = expf(d * a);
+            const float dalpha = s.x + s.y * (1.f - l) * d;
+            const float ddelta = dalpha * a * al + s.y * (1.f - l) * al + s.z * l + s.w;
+            const float dl = -d * al * s.y + d * s.z;
+            const float dz = ddelta * sigmoid_f(dt_raw[tk] + bias);
+            ddt_raw[tk] = dz;
+            du[tk] = dl * l * (1.f - l);
+            dA_tok[tk] = dalpha * d * al;
+            acc += dz;
+        }
+    }
+    if (ddt_bias == nullptr) return;
+    acc = warp_sum(acc);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
+        atomicAdd(&ddt_bias[h], s);
+    }
+}
+
+// pre-activation inputs of m3_scan_bwd_prep (on == false: the plain entry)
+struct BwdPrep {
+    bool on;
+    const float *dt_raw, *dt_bias, *u, *A_tok;
+    float* ddt_bias;
+};
+
 int bwd_chunk(int R) { return R <= 2 ? 8 : 4; }
 
 struct BwdWs {
-    size_t ckpt, part_dx, part_s, total;   // byte offsets of the sections, and the whole size
+    size_t ckpt, part_dx, part_s, dt_eff, lam_eff, total;   // byte offsets of the sections; the whole size
 };
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
@@ -606,39 +670,74 @@ BwdWs bwd_ws(const ScanDims& d) {
     w.ckpt = 0;
     w.part_dx = round256(sizeof(float) * bh * nC * (size_t)(d.dstate * d.headdim));
     w.part_s = w.part_dx + round256(sizeof(float) * (size_t)L.nPB * BTH * (size_t)(d.R * d.headdim));
-    w.total = w.part_s + round256(sizeof(float) * (size_t)L.nPB * BTH * 4);
+    w.dt_eff = w.part_s + round256(sizeof(float) * (size_t)L.nPB * BTH * 4);
+    w.lam_eff = w.dt_eff + round256(sizeof(float) * BTH);   // Delta and lambda of the pre-activation entry
+    w.total = w.dt_eff;
     return w;
+}
+
+size_t bwd_ws_prep_total(const ScanDims& d) {
+    const BwdWs w = bwd_ws(d);
+    return w.lam_eff + round256(sizeof(float) * (size_t)(d.batch * d.nheads) * (size_t)d.seqlen);
 }
 
 template <typename IO>
 cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                           const float* A, const float* lambda, const float* omega, const void* dy,
                           const float* d_final, float* dx, float* dB, float* dC, float* ddt, float* dA,
-                          float* dlambda, float* domega, void* workspace, cudaStream_t stream) {
+                          float* dlambda, float* domega, void* workspace, cudaStream_t stream, const BwdPrep& pp) {
     const int Q = bwd_chunk(d.R);
     const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, Q, (int)sizeof(IO));
     const int64_t bh = d.batch * d.nheads;
-    cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * (size_t)d.nheads, stream);
+    cudaError_t e = cudaSuccess;
+    if (!pp.on)
+        e = cudaMemsetAsync(dA, 0, sizeof(float) * (size_t)d.nheads, stream);
+    else if (pp.ddt_bias != nullptr)
+        e = cudaMemsetAsync(pp.ddt_bias, 0, sizeof(float) * (size_t)d.nheads, stream);
     if (e != cudaSuccess || bh == 0 || d.seqlen == 0) return e;
     const BwdWs w = bwd_ws(d);
     char* ws = static_cast<char*>(workspace);
+    if (pp.on) {   // Delta and lambda from their pre-activations, as the forward entry derives them
+        float* dt_eff = reinterpret_cast<float*>(ws + w.dt_eff);
+        float* lam_eff = reinterpret_cast<float*>(ws + w.lam_eff);
+        if ((e = launch_prep_params(pp.dt_raw, pp.dt_bias, pp.u, dt_eff, lam_eff, bh * d.seqlen, (int)d.nheads,
+                                    stream)) != cudaSuccess)
+            return e;
+        dt = dt_eff;
+        lambda = lam_eff;
+    }
     float* ckpt = reinterpret_cast<float*>(ws + w.ckpt);
     float* part_dx = reinterpret_cast<float*>(ws + w.part_dx);
     float* part_s = reinterpret_cast<float*>(ws + w.part_s);
     const size_t smem = sizeof(float) * (size_t)L.total;
     const unsigned grid = (unsigned)(bh * L.nPB);   // (batch*head, pair block), pair block fastest
     const bool p64 = d.headdim == 64 && L.PB == kBwdThreads / 16;   // the compile-time P = 64 kernels
-#define M3_BWD_CASE(RR)                                                                                           \
-    case RR: {                                                                                                    \
-        auto k = p64 ? scan_bwd_kernel<IO, RR, 16> : scan_bwd_kernel<IO, RR, 0>;                                 \
+#define M3_BWD_LAUNCH(RR, P4C, TA, ATOK)                                                                        \
+    {                                                                                                             \
+        auto k = scan_bwd_kernel<IO, RR, P4C, TA>;                                                                \
         if (smem > 48 * 1024 &&                                                                                   \
             (e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) \
             return e;                                                                                             \
         k<<<grid, L.threads, smem, stream>>>((const IO*)x, (const IO*)B, (const IO*)C, dt, A, lambda, omega,      \
                                              (const IO*)dy, d_final, dB, dC, domega, ckpt, part_dx, part_s,       \
-                                             d.seqlen, (int)d.nheads, (int)d.headdim, (int)d.dstate, L);          \
-        break;                                                                                                    \
+                                             d.seqlen, (int)d.nheads, (int)d.headdim, (int)d.dstate, L, ATOK);    \
     }
+#define M3_BWD_CASE(RR)                                                                                           \
+    case RR:                                                                                                      \
+        if (pp.on) {                                                                                              \
+            const TokA<true> at{pp.A_tok};                                                                        \
+            if (p64)                                                                                              \
+                M3_BWD_LAUNCH(RR, 16, true, at)                                                                   \
+            else                                                                                                  \
+                M3_BWD_LAUNCH(RR, 0, true, at)                                                                    \
+        } else {                                                                                                  \
+            const TokA<false> at{};                                                                               \
+            if (p64)                                                                                              \
+                M3_BWD_LAUNCH(RR, 16, false, at)                                                                  \
+            else                                                                                                  \
+                M3_BWD_LAUNCH(RR, 0, false, at)                                                                   \
+        }                                                                                                         \
+        break;
     switch (d.R) {
         M3_BWD_CASE(1)
         M3_BWD_CASE(2)
@@ -647,6 +746,7 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
         default: return cudaErrorInvalidValue;
     }
 #undef M3_BWD_CASE
+#undef M3_BWD_LAUNCH
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t n4 = bh * d.seqlen * d.R * d.headdim / 4;
     int64_t nb = (n4 + 255) / 256;
@@ -655,9 +755,14 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
                                                     reinterpret_cast<float4*>(dx), n4, L.nPB);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const unsigned gy = (unsigned)(d.batch < 65535 ? d.batch : 65535);
-    bwd_finish_scalars<<<dim3((unsigned)d.nheads, gy), 256, 0, stream>>>(
-        reinterpret_cast<const float4*>(part_s), dt, lambda, A, ddt, dlambda, dA, d.batch, d.seqlen,
-        (int)d.nheads, L.nPB);
+    if (pp.on)
+        bwd_finish_scalars_prep<<<dim3((unsigned)d.nheads, gy), 256, 0, stream>>>(
+            reinterpret_cast<const float4*>(part_s), dt, lambda, pp.A_tok, pp.dt_raw, pp.dt_bias, ddt, dlambda, dA,
+            pp.ddt_bias, d.batch, d.seqlen, (int)d.nheads, L.nPB);
+    else
+        bwd_finish_scalars<<<dim3((unsigned)d.nheads, gy), 256, 0, stream>>>(
+            reinterpret_cast<const float4*>(part_s), dt, lambda, A, ddt, dlambda, dA, d.batch, d.seqlen,
+            (int)d.nheads, L.nPB);
     return cudaGetLastError();
 }
 
@@ -677,15 +782,31 @@ bool bwd_supported(const ScanDims& d) {
 
 size_t bwd_workspace_size(const ScanDims& d) { return bwd_ws(d).total; }
 
+size_t bwd_prep_workspace_size(const ScanDims& d) { return bwd_ws_prep_total(d); }
+
 cudaError_t launch_scan_bwd(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                             const float* A, const float* lambda, const float* omega, const void* dy,
                             const float* d_final, float* dx, float* dB, float* dC, float* ddt, float* dA,
                             float* dlambda, float* domega, void* workspace, cudaStream_t stream) {
+    const BwdPrep pp{false, nullptr, nullptr, nullptr, nullptr, nullptr};
     if (d.io == M3_DTYPE_BF16)
         return launch_bwd_io<__nv_bfloat16>(d, x, B, C, dt, A, lambda, omega, dy, d_final, dx, dB, dC, ddt, dA,
-                                            dlambda, domega, workspace, stream);
+                                            dlambda, domega, workspace, stream, pp);
     return launch_bwd_io<float>(d, x, B, C, dt, A, lambda, omega, dy, d_final, dx, dB, dC, ddt, dA, dlambda,
-                                domega, workspace, stream);
+                                domega, workspace, stream, pp);
+}
+
+cudaError_t launch_scan_bwd_prep(const ScanDims& d, const void* x, const void* B, const void* C,
+                                 const float* dt_raw, const float* dt_bias, const float* A_tok, const float* u,
+                                 const float* omega, const void* dy, const float* d_final, float* dx, float* dB,
+                                 float* dC, float* ddt_raw, float* dA_tok, float* du, float* domega,
+                                 float* ddt_bias, void* workspace, cudaStream_t stream) {
+    const BwdPrep pp{true, dt_raw, dt_bias, u, A_tok, ddt_bias};
+    if (d.io == M3_DTYPE_BF16)
+        return launch_bwd_io<__nv_bfloat16>(d, x, B, C, nullptr, nullptr, nullptr, omega, dy, d_final, dx, dB, dC,
+                                            ddt_raw, dA_tok, du, domega, workspace, stream, pp);
+    return launch_bwd_io<float>(d, x, B, C, nullptr, nullptr, nullptr, omega, dy, d_final, dx, dB, dC, ddt_raw,
+                                dA_tok, du, domega, workspace, stream, pp);
 }
 
 }  // namespace m3

@@ -483,6 +483,14 @@ size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 
 }  // namespace
 
+cudaError_t launch_prep_params(const float* dt_raw, const float* dt_bias, const float* u, float* dt_out,
+                               float* lam_out, int64_t n, int H, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, 148 * 16);
+    prep_kernel<<<blocks, 256, 0, stream>>>(dt_raw, dt_bias, u, dt_out, lam_out, n, H);
+    return cudaGetLastError();
+}
+
 bool simt_supported(const ScanDims& d) {
     if (!(d.R == 1 || d.R == 2 || d.R == 4 || d.R == 8)) return false;
     if (!(d.headdim == 16 || d.headdim == 32 || d.headdim == 64 || d.headdim == 128)) return false;

@@ -160,3 +160,79 @@ def test_bwd_rejects_unsupported_and_bad_arguments():
     grads2["dB"] = None
     assert binding.m3_scan_bwd(*args, 1, dy, None, grads2, ws) == binding.M3_ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+# ---- m3_scan_bwd_prep: pre-activations (Delta = softplus(dt_raw + dt_bias), lambda = sigmoid(u), A per token)
+PREP_NAMES = {"x": "dx", "B": "dB", "C": "dC", "dt_raw": "ddt_raw", "dt_bias": "ddt_bias", "A": "dA",
+              "u": "du", "omega": "domega"}
+PREP_DEV = ("x", "B", "C", "dt_raw", "dt_bias", "A", "u", "omega")
+
+
+def _run_prep(inp, R, dy, dfin=None):
+    d = {k: inp[k].cuda().contiguous() for k in PREP_DEV}
+    g = binding.scan_bwd_prep(d["x"], d["B"], d["C"], d["dt_raw"], d["A"], d["u"], d["omega"], R,
+                              dy.cuda().contiguous(), None if dfin is None else dfin.cuda().contiguous(),
+                              dt_bias=d["dt_bias"])
+    torch.cuda.synchronize()
+    return {k: v.cpu().double().numpy() for k, v in g.items()}
+
+
+@pytest.mark.parametrize("io,Bt,H,T,P,N,R", [
+    ("fp32", 1, 2, 21, 4, 4, 1),    # three chunks of 8, ragged tail
+    ("fp32", 2, 1, 13, 8, 6, 4),    # chunks of 4
+    ("bf16", 1, 2, 18, 4, 4, 2),
+])
+def test_bwd_prep_small_every_element(io, Bt, H, T, P, N, R):
+    w = synth.Workload("case", Bt, H, T, P, N, R, 64, io)
+    inp = synth.make_prep_inputs(w, seed=T + R)
+    gen = torch.Generator().manual_seed(31)
+    dy = torch.randn(inp["x"].shape, generator=gen).to(inp["x"].dtype)
+    dfin = torch.randn((Bt, H, N, P), generator=gen)
+    got = _run_prep(inp, R, dy, dfin)
+    ref = grad.grad_fd({k: oracle.f64(inp[k]) for k in grad.PREP_INPUTS}, oracle.f64(dy), oracle.f64(dfin),
+                       prep=True)
+    for k, name in PREP_NAMES.items():
+        err = oracle.rel_err(got[name], ref[k])
+        assert err < TOL_BWD[io], f"{name}: {err:.2e}"
+
+
+@pytest.mark.parametrize("io,Bt,H,T,P,N,R", [
+    ("fp32", 1, 2, 150, 64, 128, 1),
+    ("bf16", 2, 2, 100, 64, 64, 4),
+])
+def test_bwd_prep_larger_directional(io, Bt, H, T, P, N, R):
+    w = synth.Workload("case", Bt, H, T, P, N, R, 64, io)
+    inp = synth.make_prep_inputs(w, seed=41)
+    gen = torch.Generator().manual_seed(42)
+    dy = torch.randn(inp["x"].shape, generator=gen).to(inp["x"].dtype)
+    dfin = torch.randn((Bt, H, N, P), generator=gen)
+    got = _run_prep(inp, R, dy, dfin)
+    ref = {k: oracle.f64(inp[k]) for k in grad.PREP_INPUTS}
+    dy64, df64 = oracle.f64(dy), oracle.f64(dfin)
+    rng = np.random.default_rng(43)
+    for k in grad.PREP_INPUTS:
+        d = rng.standard_normal(ref[k].shape)
+        num = grad.directional(ref, k, d, dy64, df64, eps=1e-6, prep=True)
+        kern = float(np.sum(got[PREP_NAMES[k]] * d))
+        assert abs(kern - num) <= TOL_BWD[io] * max(1.0, abs(num)), (k, kern, num)
+
+
+def test_bwd_prep_rejects_bc_norm_and_gate():
+    w = synth.Workload("case", 1, 2, 8, 4, 4, 1, 64, "fp32")
+    d = {k: v.cuda() for k, v in synth.make_prep_inputs(w, seed=1).items() if k in PREP_DEV}
+    dy = torch.zeros_like(d["x"])
+    f = dict(dtype=torch.float32, device="cuda")
+    grads = {"dx": torch.empty(d["x"].shape, **f), "dB": torch.empty(d["B"].shape, **f),
+             "dC": torch.empty(d["C"].shape, **f), "ddt_raw": torch.empty(d["dt_raw"].shape, **f),
+             "dA": torch.empty(d["A"].shape, **f), "du": torch.empty(d["u"].shape, **f),
+             "domega": torch.empty(d["omega"].shape, **f), "ddt_bias": torch.empty((2,), **f)}
+    ws = torch.empty(binding.m3_scan_bwd_prep_workspace_size(1, 8, 2, 4, 4, 1, 1), dtype=torch.uint8, device="cuda")
+    args = [d[k] for k in ("x", "B", "C", "dt_raw", "A", "u", "omega")]
+    ok = binding.prep_params(d["dt_bias"], None, None)
+    assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws, ok) == binding.M3_OK
+    bc = binding.prep_params(d["dt_bias"], {"norm": True, "eps": 1e-5}, None)
+    assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws, bc) == binding.M3_ERR_UNSUPPORTED
+    gate = binding.prep_params(d["dt_bias"], None, torch.zeros_like(d["x"]))
+    assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws, gate) == binding.M3_ERR_UNSUPPORTED
+    assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws[:64], ok) == binding.M3_ERR_WORKSPACE
+    torch.cuda.synchronize()

@@ -114,3 +114,45 @@ def test_directional_matches_full_gradient():
     for k in ("dt", "lam", "omega"):
         v = rng.standard_normal(inp[k].shape)
         assert abs(grad.directional(inp, k, v, dy) - float(np.sum(g[k] * v))) < 1e-7
+
+
+# ---- pre-activation inputs (Delta = softplus(dt_raw + dt_bias), lambda = sigmoid(u), A per token)
+def _prep_inp(T=7, seed=21):
+    w = synth.Workload("gp", 1, 2, T, 3, 4, 2, 8, "fp32")
+    d = synth.make_prep_inputs(w, seed=seed)
+    return {k: oracle.f64(d[k]) for k in grad.PREP_INPUTS}
+
+
+def _plain_of(pi):
+    """The plain inputs the pre-activations stand for (Delta, lambda evaluated, A per token)."""
+    d, lam = oracle.prep(pi["dt_raw"], pi["dt_bias"], pi["u"])
+    return {"x": pi["x"], "B": pi["B"], "C": pi["C"], "dt": d, "A": pi["A"], "lam": lam, "omega": pi["omega"]}
+
+
+def test_prep_chain_rule_through_softplus_and_sigmoid():
+    """dL/d dt_raw = dL/dDelta * sigmoid(z) (softplus' = sigmoid) and dL/du = dL/dlambda * lambda (1 - lambda),
+    with dL/dDelta, dL/dlambda the (separately pinned) gradients of the plain recurrence at the same point;
+    dL/d dt_bias[h] sums dL/d dt_raw over batch and tokens; the per-token dA equals the plain one."""
+    pi = _prep_inp()
+    dy = _dy(pi, seed=22)
+    gp = grad.grad_fd(pi, dy, keys=("dt_raw", "dt_bias", "A", "u"), prep=True)
+    pl = _plain_of(pi)
+    g = grad.grad_fd(pl, dy, keys=("dt", "lam", "A"))
+    z = pi["dt_raw"] + pi["dt_bias"]
+    assert np.max(np.abs(gp["dt_raw"] - g["dt"] * oracle.sigmoid(z))) < 1e-7
+    lam = pl["lam"]
+    assert np.max(np.abs(gp["u"] - g["lam"] * lam * (1.0 - lam))) < 1e-7
+    assert np.max(np.abs(gp["dt_bias"] - gp["dt_raw"].sum(axis=(0, 1)))) < 1e-7
+    assert np.max(np.abs(gp["A"] - g["A"])) < 1e-7
+
+
+def test_per_token_A_gradient_sums_to_the_per_head_one():
+    """With A_t = A_h for every token, the per-token gradients summed over batch and tokens are the
+    gradient with respect to the per-head generator."""
+    inp = _inp(T=8, seed=23)
+    dy = _dy(inp, seed=24)
+    g_head = grad.grad_fd(inp, dy, keys=("A",))["A"]
+    tok = dict(inp)
+    tok["A"] = np.broadcast_to(inp["A"], inp["dt"].shape).copy()
+    g_tok = grad.grad_fd(tok, dy, keys=("A",))["A"]
+    assert np.max(np.abs(g_tok.sum(axis=(0, 1)) - g_head)) < 1e-7
