@@ -319,6 +319,32 @@ def time_backward(binding, w, d, stream, steps, warmup, dist, device, seed=0):
     return sec, per
 
 
+def time_backward_prep(binding, w, stream, steps, warmup, dist, device, seed=0):
+    """m3_scan_bwd_prep on the workload's pre-activation inputs (dt_bias set) with a random dy."""
+    dp = synth.make_prep_inputs(w, seed=seed, device=device)
+    gen = torch.Generator(device=device).manual_seed(2000 + seed)
+    dy = torch.randn(dp["x"].shape, generator=gen, device=device).to(dp["x"].dtype)
+    f = dict(dtype=torch.float32, device=device)
+    grads = {"dx": torch.empty(dp["x"].shape, **f), "dB": torch.empty(dp["B"].shape, **f),
+             "dC": torch.empty(dp["C"].shape, **f), "ddt_raw": torch.empty(dp["dt_raw"].shape, **f),
+             "dA": torch.empty(dp["A"].shape, **f), "du": torch.empty(dp["u"].shape, **f),
+             "domega": torch.empty(dp["omega"].shape, **f), "ddt_bias": torch.empty((w.heads,), **f)}
+    nbytes = binding.m3_scan_bwd_prep_workspace_size(w.batch, w.seqlen, w.heads, w.headdim, w.dstate, w.rank,
+                                                     binding.io_code(dp["x"].dtype))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    params = binding.prep_params(dp["dt_bias"], None, None)
+    args = [dp[k] for k in ("x", "B", "C", "dt_raw", "A", "u", "omega")]
+
+    def call():
+        st = binding.m3_scan_bwd_prep(*args, w.rank, dy, None, grads, ws, params, stream)
+        if st != 0:
+            raise binding.M3Error(st, "m3_scan_bwd_prep")
+
+    sec, per = _time_calls(call, stream, steps, warmup, dist, device)
+    del grads, ws, dy, dp
+    return sec, per
+
+
 def time_prefill_e2e(binding, w, host, stream, steps, warmup, dist, device, copy_streams=4):
     """End to end through the C ABI: every step copies its inputs from pinned host
     buffers to the device, runs m3_scan_fwd and copies y and the final state back to
@@ -561,7 +587,7 @@ def backward_leg(binding, w, d, args, stream, dist, device, local, ws, rank):
     bms = sum(bper) / len(bper)
     fl, by = bwd_flops(w), bwd_bytes(w)
     pk = peaks()
-    return {
+    out = {
         "value": w.batch * w.seqlen * ws * bsteps / bsec / 1e6, "unit": "Mtok/s", "steps": bsteps,
         "ms_per_step": bsec / bsteps * 1e3, "entry": "m3_scan_bwd", "gpu_launches": 3 * bsteps,
         "config": {"batch": w.batch, "seqlen": w.seqlen, "heads": w.heads, "headdim": w.headdim,
@@ -571,6 +597,14 @@ def backward_leg(binding, w, d, args, stream, dist, device, local, ws, rank):
                      "peak_source": "148 SMs x 128 FP32 lanes x 2 x 2032 MHz", "flops_per_call": fl},
         "algorithmic_bytes_per_call": by, "hbm_frac": by / (bms * 1e-3) / 1e9 / pk["hbm_gbs"],
         "clocks": bclk.summary()}
+    # the same through m3_scan_bwd_prep (pre-activations with dt_bias, A per token): one more launch
+    # (Delta, lambda) and the chain rule through softplus / sigmoid in the scalar finishing kernel
+    psec, pper = time_backward_prep(binding, w, stream, bsteps, args.warmup, dist, device, seed=rank)
+    pms = sum(pper) / len(pper)
+    out["prep"] = {"value": w.batch * w.seqlen * ws * bsteps / psec / 1e6, "unit": "Mtok/s",
+                   "ms_per_step": psec / bsteps * 1e3, "entry": "m3_scan_bwd_prep", "gpu_launches": 4 * bsteps,
+                   "roofline_frac": fl / (pms * 1e-3) / 1e12 / FP32_ALU_TFLOPS}
+    return out
 
 
 # ---------------------------------------------------------------------------
