@@ -236,3 +236,19 @@ def test_bwd_prep_rejects_bc_norm_and_gate():
     assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws, gate) == binding.M3_ERR_UNSUPPORTED
     assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws[:64], ok) == binding.M3_ERR_WORKSPACE
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("Bt,T", [(1, 0), (0, 5)])
+def test_bwd_empty_inputs(Bt, T):
+    """No tokens or no sequences: both entries succeed, dA (summed over nothing) and ddt_bias are 0,
+    and the final-state seed alone has nothing to flow into."""
+    w = synth.Workload("case", Bt, 2, T, 8, 8, 1, 64, "fp32")
+    inp = synth.make_inputs(w, seed=0)
+    g = binding.scan_bwd(*[inp[k].cuda() for k in KEYS], 1, torch.zeros(inp["x"].shape, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(g["dA"]).item() == 0 and g["dx"].numel() == 0
+    pi = {k: v.cuda() for k, v in synth.make_prep_inputs(w, seed=0).items() if k in PREP_DEV}
+    gp = binding.scan_bwd_prep(pi["x"], pi["B"], pi["C"], pi["dt_raw"], pi["A"], pi["u"], pi["omega"], 1,
+                               torch.zeros(pi["x"].shape, device="cuda"), dt_bias=pi["dt_bias"])
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(gp["ddt_bias"]).item() == 0 and gp["dA"].numel() == 0
