@@ -286,7 +286,7 @@ M3_API int m3_scan_bwd(const void* x, const void* B, const void* C, const float*
                        int io_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Backward pass of m3_scan_fwd_prep without its B/C normalisation and gate:
+ * Backward pass of m3_scan_fwd_prep without its B/C normalisation:
  * the gradients with respect to the pre-activations of Delta_t =
  * softplus(dt_raw_t + dt_bias_h) and lambda_t = sigmoid(u_t), and to the
  * per-token decay generators A_t (Table 1's time-varying discretisations).
@@ -294,24 +294,31 @@ M3_API int m3_scan_bwd(const void* x, const void* B, const void* C, const float*
  *   x, B, C, omega, R, sizes, io_dtype, dy, d_final: as m3_scan_bwd
  *   dt_raw, A, u   [batch, T, H] fp32 (A one value per token, as in
  *                  m3_scan_fwd_prep)
- *   params         nullable; only dt_bias may be set (bc_norm, the gains, the
- *                  biases and z must be 0 / NULL, else M3_ERR_UNSUPPORTED)
+ *   params         nullable; dt_bias and z may be set (bc_norm, the gains and
+ *                  the biases must be 0 / NULL, else M3_ERR_UNSUPPORTED)
  *   dx, dB, dC, domega  out, as m3_scan_bwd
  *   ddt_raw, dA, du     out [batch, T, H] fp32
  *   ddt_bias       nullable out [H] fp32: sum over batch and tokens of ddt_raw
  *                  (accumulated with atomics)
- *   workspace: m3_scan_bwd_prep_workspace_size bytes (m3_scan_bwd's, plus
- *            Delta and lambda: 2 * batch * T * H fp32), 256-byte aligned.
+ *   dz             out [batch, T, H, R, P] fp32 when params->z is set (the
+ *                  output gate y = y_pre * SiLU(z)), else unused
+ *   workspace: m3_scan_bwd_prep_workspace_size bytes, 256-byte aligned:
+ *            m3_scan_bwd's, Delta and lambda (2 * batch * T * H fp32) and,
+ *            where the forward entry supports the shape, the ungated output
+ *            y_pre (io dtype, y's layout) and m3_scan_fwd_prep's workspace.
  * Delta and lambda are derived with the forward entry's own functions; the
  * derivative of softplus is sigmoid, that of sigmoid is lambda (1 - lambda).
- * Sizes and errors as m3_scan_bwd.
+ * With the gate, the seed of the recurrence is dy * SiLU(z) (fp32, inside the
+ * kernel) and dz = dy * y_pre * SiLU'(z), y_pre written by m3_scan_fwd_prep
+ * without the gate (chunk 64) in the io dtype; shapes that entry does not
+ * take give M3_ERR_UNSUPPORTED.  Sizes and errors as m3_scan_bwd.
  */
 M3_API size_t m3_scan_bwd_prep_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                                               int64_t dstate, int R, int io_dtype);
 M3_API int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const float* dt_raw, const float* A,
                             const float* u, const float* omega, int R, const void* dy, const float* d_final,
                             float* dx, float* dB, float* dC, float* ddt_raw, float* dA, float* du, float* domega,
-                            float* ddt_bias, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                            float* ddt_bias, float* dz, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                             int64_t dstate, int io_dtype, const m3_prep_params* params, void* workspace,
                             size_t workspace_bytes, void* stream);
 

@@ -15,7 +15,8 @@ algorithm's uses listed in section 3.3.
 the derivative of L along one direction per input, for larger problems.  With
 ``prep=True`` the loss runs ``oracle.scan_prep`` on pre-activations instead
 (Delta = softplus(dt_raw + dt_bias), lambda = sigmoid(u), A per token; the
-time-varying discretisations of the page's Table 1), over PREP_INPUTS.
+time-varying discretisations of the page's Table 1), over PREP_INPUTS, and
+with a "z" entry in the inputs through the output gate y * silu(z) as well.
 """
 from __future__ import annotations
 
@@ -27,9 +28,15 @@ INPUTS = ("x", "B", "C", "dt", "A", "lam", "omega")
 PREP_INPUTS = ("x", "B", "C", "dt_raw", "dt_bias", "A", "u", "omega")
 
 
+def _names(inp: dict, prep: bool):
+    if not prep:
+        return INPUTS
+    return PREP_INPUTS + (("z",) if inp.get("z") is not None else ())
+
+
 def loss(inp: dict, dy, d_final=None, prep: bool = False) -> float:
     if prep:
-        y, hT, _ = scan_prep(*[inp[k] for k in PREP_INPUTS])
+        y, hT, _ = scan_prep(*[inp[k] for k in PREP_INPUTS], z=inp.get("z"))
     else:
         y, hT, _ = scan(*[inp[k] for k in INPUTS])
     val = float(np.sum(y * f64(dy)))
@@ -40,7 +47,7 @@ def loss(inp: dict, dy, d_final=None, prep: bool = False) -> float:
 
 def grad_fd(inp: dict, dy, d_final=None, eps: float = 1e-6, keys=None, prep: bool = False) -> dict:
     """dL/d(input) for every element of the listed inputs, central differences with step eps."""
-    names = PREP_INPUTS if prep else INPUTS
+    names = _names(inp, prep)
     keys = names if keys is None else keys
     base = {k: f64(inp[k]).copy() for k in names}
     out = {}
@@ -62,7 +69,7 @@ def grad_fd(inp: dict, dy, d_final=None, eps: float = 1e-6, keys=None, prep: boo
 
 def directional(inp: dict, key: str, v, dy, d_final=None, eps: float = 1e-6, prep: bool = False) -> float:
     """d/ds L(input[key] + s v) at s = 0, central differences with step eps."""
-    base = {k: f64(inp[k]).copy() for k in (PREP_INPUTS if prep else INPUTS)}
+    base = {k: f64(inp[k]).copy() for k in _names(inp, prep)}
     v = f64(v)
     keep = base[key].copy()
     base[key] = keep + eps * v

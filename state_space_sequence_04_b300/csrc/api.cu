@@ -111,6 +111,29 @@ int decode_impl(float* state, const void* x_t, const void* B_t, void* B_prev_x_p
                                          static_cast<cudaStream_t>(stream)));
 }
 
+// The backward on pre-activations: m3_scan_bwd's sections, Delta and lambda; then, for the output gate,
+// the ungated forward output y_pre (io dtype) and the forward entry's own workspace (chunk 64).
+struct BwdPrepWs {
+    size_t y_pre, fwd, total;
+    bool gate;   // the forward supports the shape, so the gate's backward can run
+};
+
+size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+BwdPrepWs bwd_prep_ws(const m3::ScanDims& d) {
+    BwdPrepWs w{};
+    w.y_pre = al256(m3::bwd_prep_workspace_size(d));
+    w.total = w.y_pre;
+    const m3::ScanDims f{d.batch, d.seqlen, d.nheads, d.headdim, d.dstate, d.R, 64, d.io};
+    w.gate = validate_scan_sizes(f) == M3_OK && m3::bwd_gate_supported(d);
+    if (w.gate) {
+        const size_t e = d.io == M3_DTYPE_BF16 ? 2 : 4;
+        w.fwd = w.y_pre + al256(e * (size_t)(d.batch * d.seqlen * d.nheads) * (size_t)(d.R * d.headdim));
+        w.total = w.fwd + al256(scan_workspace(f, true));
+    }
+    return w;
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,36 +252,52 @@ size_t m3_scan_bwd_prep_workspace_size(int64_t batch, int64_t seqlen, int64_t nh
                                        int64_t dstate, int R, int io_dtype) {
     const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, 64, io_dtype};
     if (!ok_io(io_dtype) || batch < 0 || seqlen < 0 || nheads < 1 || !m3::bwd_supported(d)) return 0;
-    return m3::bwd_prep_workspace_size(d);
+    return bwd_prep_ws(d).total;
 }
 
 int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const float* dt_raw, const float* A,
                      const float* u, const float* omega, int R, const void* dy, const float* d_final, float* dx,
                      float* dB, float* dC, float* ddt_raw, float* dA, float* du, float* domega, float* ddt_bias,
-                     int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate, int io_dtype,
-                     const m3_prep_params* params, void* workspace, size_t workspace_bytes, void* stream) {
+                     float* dz, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+                     int io_dtype, const m3_prep_params* params, void* workspace, size_t workspace_bytes,
+                     void* stream) {
     const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, 64, io_dtype};
     if (!ok_io(io_dtype)) return M3_ERR_INVALID_ARG;
     if (batch < 0 || seqlen < 0 || nheads < 1 || headdim < 1 || dstate < 2 || dstate % 2 || R < 1)
         return M3_ERR_INVALID_ARG;
     if (params != nullptr && !aligned16(params)) return M3_ERR_INVALID_ARG;
     const float* dt_bias = params != nullptr ? params->dt_bias : nullptr;
-    if (!ok_nullable(dt_bias) || !ok_nullable(ddt_bias) || !ok_nullable(d_final)) return M3_ERR_INVALID_ARG;
-    if (params != nullptr && (params->bc_norm || params->B_gain || params->C_gain || params->B_bias ||
-                              params->C_bias || params->z))
-        return M3_ERR_UNSUPPORTED;   // no backward through the B/C normalisation or the gate
+    const void* z = params != nullptr ? params->z : nullptr;
+    if (!ok_nullable(dt_bias) || !ok_nullable(ddt_bias) || !ok_nullable(d_final) || !ok_nullable(z))
+        return M3_ERR_INVALID_ARG;
+    if (params != nullptr && (params->bc_norm || params->B_gain || params->C_gain || params->B_bias || params->C_bias))
+        return M3_ERR_UNSUPPORTED;   // no backward through the B/C normalisation
     if (batch * nheads > (int64_t)INT32_MAX || seqlen > (int64_t)INT32_MAX) return M3_ERR_UNSUPPORTED;
     if (!m3::bwd_supported(d)) return M3_ERR_UNSUPPORTED;
-    if (batch > 0 && seqlen > 0) {
+    const BwdPrepWs w = bwd_prep_ws(d);
+    if (z != nullptr && !w.gate) return M3_ERR_UNSUPPORTED;
+    const bool any_tokens = batch > 0 && seqlen > 0;
+    if (any_tokens) {
         const void* ptrs[] = {x, B, C, dt_raw, A, u, omega, dy, dx, dB, dC, ddt_raw, dA, du, domega};
         for (const void* q : ptrs)
             if (!ok_ptr(q)) return M3_ERR_INVALID_ARG;
-        const size_t need = m3::bwd_prep_workspace_size(d);
-        if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        if (z != nullptr && !ok_ptr(dz)) return M3_ERR_INVALID_ARG;
+        if (workspace == nullptr || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return M3_ERR_WORKSPACE;
     }
+    char* ws = static_cast<char*>(workspace);
+    void* y_pre = nullptr;
+    if (z != nullptr && any_tokens) {   // the ungated forward output, by the forward entry itself
+        m3::Prep fp{};
+        if (!prep_from(params, &fp)) return M3_ERR_INVALID_ARG;
+        fp.z = nullptr;
+        y_pre = ws + w.y_pre;
+        const int st = scan_impl(x, B, C, dt_raw, A, u, omega, R, 64, y_pre, nullptr, batch, seqlen, nheads, headdim,
+                                 dstate, io_dtype, ws + w.fwd, w.total - w.fwd, stream, fp);
+        if (st != M3_OK) return st;
+    }
     return cuda_status(m3::launch_scan_bwd_prep(d, x, B, C, dt_raw, dt_bias, A, u, omega, dy, d_final, dx, dB, dC,
-                                                ddt_raw, dA, du, domega, ddt_bias, workspace,
+                                                ddt_raw, dA, du, domega, ddt_bias, z, y_pre, dz, workspace,
                                                 static_cast<cudaStream_t>(stream)));
 }
 

@@ -85,7 +85,7 @@ struct BwdLayout {
 
 __host__ __device__ constexpr int round16(int v) { return (v + 15) & ~15; }
 
-BwdLayout bwd_layout(int P, int N, int R, int Q, int e) {
+BwdLayout bwd_layout(int P, int N, int R, int Q, int e, bool gate = false) {
     BwdLayout L{};
     const int P4 = P / 4, NP2 = N / 2;
     int PB = kBwdThreads / P4;   // a power of two, the smallest one >= N/2 if that is smaller
@@ -134,6 +134,7 @@ BwdLayout bwd_layout(int P, int N, int R, int Q, int e) {
     rb += round16(Q * 4);
     L.rA = rb;
     rb += round16(Q * 4);
+    if (gate) rb += round16(Q * R * P * e);   // the output gate's z rows, at rA + round16(4 Q)
     L.rawBytes = rb;
     L.unitXY = (R * P * e) % 16 == 0 ? 16 : 4;
     L.oRaw = o;
@@ -202,25 +203,32 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
 }
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
-// The per-token decay generators of the pre-activation entry; an empty parameter for the plain entry, so
-// that the plain kernels' parameter block and code are those of a kernel without the option.
-template <bool ON>
-struct TokA {
-    const float* __restrict__ p;
+// Options of the pre-activation entry: EXT = 1, the per-token decay generators A_t; EXT = 3, A_t and the
+// output gate's input z (io dtype, y's layout).  The plain entry (EXT = 0) takes an empty parameter, so
+// that the plain kernels' parameter block and code are those of a kernel without the options.
+template <int EXT>
+struct BwdExt {};
+template <>
+struct BwdExt<1> {
+    const float* __restrict__ a;
 };
 template <>
-struct TokA<false> {};
+struct BwdExt<3> {
+    const float* __restrict__ a;
+    const void* __restrict__ z;
+};
 
 // P4T: P / 4 as a compile-time constant (with PB = kBwdThreads / P4T pairs per block and kBwdThreads
-// threads), or 0 for shapes taken at run time; TOKA: A per token (TokA<true>) or per head
-template <typename IO, int R, int P4T, bool TOKA>
+// threads), or 0 for shapes taken at run time; EXT: the options of BwdExt
+template <typename IO, int R, int P4T, int EXT>
 __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     const IO* __restrict__ x, const IO* __restrict__ B, const IO* __restrict__ C, const float* __restrict__ dt,
     const float* __restrict__ A, const float* __restrict__ lam, const float* __restrict__ omega,
     const IO* __restrict__ dy, const float* __restrict__ dfin, float* __restrict__ dB, float* __restrict__ dC,
     float* __restrict__ domega, float* __restrict__ ckpt, float* __restrict__ part_dx, float* __restrict__ part_s,
-    int64_t T, int H, int P, int N, const BwdLayout L, const TokA<TOKA> atok) {
+    int64_t T, int H, int P, int N, const BwdLayout L, const BwdExt<EXT> ext) {
     constexpr int Q = BwdChunk<R>::Q;
+    constexpr bool TOKA = (EXT & 1) != 0, GATE = (EXT & 2) != 0;
     extern __shared__ __align__(16) float sm[];
     // the pair blocks of one (batch, head) are neighbours in launch order, so they run together and
     // share their X, dy, Delta, lambda reads in L2
@@ -267,6 +275,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
     char* const raw = reinterpret_cast<char*>(sm + L.oRaw);
     constexpr int E = (int)sizeof(IO);
     const int unit = P4T ? ((R * 4 * P4T * E) % 16 == 0 ? 16 : 4) : L.unitXY;
+    const int rZoff = L.rA + round16(Q * 4);   // the gate's z rows in a copy buffer
     const int upr = R * P4 * 4 * E / unit;   // copies per X / dy row (a power of two)
     int lgUpr = 0;
     while ((1 << lgUpr) < upr) ++lgUpr;
@@ -288,18 +297,37 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
             else
                 cp_async8(dst, src, ok);
         }
-        for (int i = tid; i < (fwd ? Q + 1 : 2 * Q + 1) * upr; i += nt) {   // X rows (from t0 - 1), then dy rows
-            const int row = i >> lgUpr, u = i & (upr - 1);
-            const bool isX = row <= Q;
-            const int q = isX ? row : row - (Q + 1);
-            const int64_t t = isX ? t0 - 1 + q : t0 + q;
-            const bool ok = t >= 0 && t < T;
-            const char* src = reinterpret_cast<const char*>(isX ? x : dy) + (ok ? tok(t) * R * PP * E + u * unit : 0);
-            char* dst = rb + (isX ? L.rX : L.rDy) + q * R * PP * E + u * unit;
-            if (unit == 16)
-                cp_async16(dst, src, ok);
-            else
-                cp_async4(dst, src, ok);
+        if constexpr (GATE) {   // X rows (from t0 - 1), then dy rows, then z rows
+            const int nrows = fwd ? Q + 1 : 3 * Q + 1;
+            for (int i = tid; i < nrows * upr; i += nt) {
+                const int row = i >> lgUpr, u = i & (upr - 1);
+                const int sec = row <= Q ? 0 : (row <= 2 * Q ? 1 : 2);
+                const int q = sec == 0 ? row : (sec == 1 ? row - (Q + 1) : row - (2 * Q + 1));
+                const int64_t t = sec == 0 ? t0 - 1 + q : t0 + q;
+                const bool ok = t >= 0 && t < T;
+                const void* base = sec == 0 ? (const void*)x : sec == 1 ? (const void*)dy : ext.z;
+                const char* src = reinterpret_cast<const char*>(base) + (ok ? tok(t) * R * PP * E + u * unit : 0);
+                char* dst = rb + (sec == 0 ? L.rX : sec == 1 ? L.rDy : rZoff) + q * R * PP * E + u * unit;
+                if (unit == 16)
+                    cp_async16(dst, src, ok);
+                else
+                    cp_async4(dst, src, ok);
+            }
+        } else {   // X rows (from t0 - 1), then dy rows
+            for (int i = tid; i < (fwd ? Q + 1 : 2 * Q + 1) * upr; i += nt) {
+                const int row = i >> lgUpr, u = i & (upr - 1);
+                const bool isX = row <= Q;
+                const int q = isX ? row : row - (Q + 1);
+                const int64_t t = isX ? t0 - 1 + q : t0 + q;
+                const bool ok = t >= 0 && t < T;
+                const char* src =
+                    reinterpret_cast<const char*>(isX ? x : dy) + (ok ? tok(t) * R * PP * E + u * unit : 0);
+                char* dst = rb + (isX ? L.rX : L.rDy) + q * R * PP * E + u * unit;
+                if (unit == 16)
+                    cp_async16(dst, src, ok);
+                else
+                    cp_async4(dst, src, ok);
+            }
         }
         constexpr int nscal = TOKA ? 3 * Q : 2 * Q;
         for (int i = tid; i < Q * PB + nscal; i += nt) {   // omega, then Delta, lambda (and A_t)
@@ -315,7 +343,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
                 const int k = i - Q * PB, sec = k / Q, q = k - sec * Q;
                 ok = t0 + q < T;
                 const float* base = sec == 0 ? dt : lam;
-                if constexpr (TOKA) base = sec == 2 ? atok.p : base;
+                if constexpr (TOKA) base = sec == 2 ? ext.a : base;
                 src = base + (ok ? tok(t0 + q) : 0);
                 dst = rb + (sec == 0 ? L.rDt : sec == 1 ? L.rL : L.rA) + 4 * q;
             }
@@ -338,7 +366,12 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_kernel(
         for (int i = tid; i < n2; i += nt) sX[i] = ld_io(rX, i);
         if (!fwd) {
             for (int i = tid; i < n3; i += nt) sC[i] = ld_io(rC, i);
-            for (int i = tid; i < n4; i += nt) sDy[i] = ld_io(rDy, i);
+            if constexpr (GATE) {   // the gated output's seed reaches the recurrence as dy silu(z)
+                const IO* rZ = reinterpret_cast<const IO*>(rb + rZoff);
+                for (int i = tid; i < n4; i += nt) sDy[i] = ld_io(rDy, i) * silu_f(ld_io(rZ, i));
+            } else {
+                for (int i = tid; i < n4; i += nt) sDy[i] = ld_io(rDy, i);
+            }
         }
         for (int i = tid; i < Q * PB; i += nt) {
             const float w = rW[i];
@@ -646,11 +679,24 @@ __global__ void bwd_finish_scalars_prep(const float4* __restrict__ part_s, const
     }
 }
 
-// pre-activation inputs of m3_scan_bwd_prep (on == false: the plain entry)
+// dz = dy y_pre silu'(z), silu'(z) = sigmoid(z) (1 + z (1 - sigmoid(z))), for the gated output
+// y = y_pre silu(z); y_pre is the ungated forward output
+template <typename IO>
+__global__ void bwd_gate_dz(const IO* __restrict__ dy, const IO* __restrict__ z, const IO* __restrict__ y_pre,
+                            float* __restrict__ dz, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float zz = ld_io(z, i), sg = sigmoid_f(zz);
+        dz[i] = ld_io(dy, i) * ld_io(y_pre, i) * sg * (1.f + zz * (1.f - sg));
+    }
+}
+
+// pre-activation inputs of m3_scan_bwd_prep (on == false: the plain entry); z != nullptr: the output gate
 struct BwdPrep {
     bool on;
     const float *dt_raw, *dt_bias, *u, *A_tok;
     float* ddt_bias;
+    const void *z, *y_pre;
+    float* dz;
 };
 
 int bwd_chunk(int R) { return R <= 2 ? 8 : 4; }
@@ -687,7 +733,8 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
                           const float* d_final, float* dx, float* dB, float* dC, float* ddt, float* dA,
                           float* dlambda, float* domega, void* workspace, cudaStream_t stream, const BwdPrep& pp) {
     const int Q = bwd_chunk(d.R);
-    const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, Q, (int)sizeof(IO));
+    const bool gate = pp.on && pp.z != nullptr;
+    const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, Q, (int)sizeof(IO), gate);
     const int64_t bh = d.batch * d.nheads;
     cudaError_t e = cudaSuccess;
     if (!pp.on)
@@ -712,30 +759,36 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
     const size_t smem = sizeof(float) * (size_t)L.total;
     const unsigned grid = (unsigned)(bh * L.nPB);   // (batch*head, pair block), pair block fastest
     const bool p64 = d.headdim == 64 && L.PB == kBwdThreads / 16;   // the compile-time P = 64 kernels
-#define M3_BWD_LAUNCH(RR, P4C, TA, ATOK)                                                                        \
+#define M3_BWD_LAUNCH(RR, P4C, EX, EXTV)                                                                        \
     {                                                                                                             \
-        auto k = scan_bwd_kernel<IO, RR, P4C, TA>;                                                                \
+        auto k = scan_bwd_kernel<IO, RR, P4C, EX>;                                                                \
         if (smem > 48 * 1024 &&                                                                                   \
             (e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) \
             return e;                                                                                             \
         k<<<grid, L.threads, smem, stream>>>((const IO*)x, (const IO*)B, (const IO*)C, dt, A, lambda, omega,      \
                                              (const IO*)dy, d_final, dB, dC, domega, ckpt, part_dx, part_s,       \
-                                             d.seqlen, (int)d.nheads, (int)d.headdim, (int)d.dstate, L, ATOK);    \
+                                             d.seqlen, (int)d.nheads, (int)d.headdim, (int)d.dstate, L, EXTV);    \
     }
 #define M3_BWD_CASE(RR)                                                                                           \
     case RR:                                                                                                      \
-        if (pp.on) {                                                                                              \
-            const TokA<true> at{pp.A_tok};                                                                        \
+        if (gate) {                                                                                               \
+            const BwdExt<3> ex{pp.A_tok, pp.z};                                                                   \
             if (p64)                                                                                              \
-                M3_BWD_LAUNCH(RR, 16, true, at)                                                                   \
+                M3_BWD_LAUNCH(RR, 16, 3, ex)                                                                      \
             else                                                                                                  \
-                M3_BWD_LAUNCH(RR, 0, true, at)                                                                    \
+                M3_BWD_LAUNCH(RR, 0, 3, ex)                                                                       \
+        } else if (pp.on) {                                                                                       \
+            const BwdExt<1> ex{pp.A_tok};                                                                         \
+            if (p64)                                                                                              \
+                M3_BWD_LAUNCH(RR, 16, 1, ex)                                                                      \
+            else                                                                                                  \
+                M3_BWD_LAUNCH(RR, 0, 1, ex)                                                                       \
         } else {                                                                                                  \
-            const TokA<false> at{};                                                                               \
+            const BwdExt<0> ex{};                                                                                 \
             if (p64)                                                                                              \
-                M3_BWD_LAUNCH(RR, 16, false, at)                                                                  \
+                M3_BWD_LAUNCH(RR, 16, 0, ex)                                                                      \
             else                                                                                                  \
-                M3_BWD_LAUNCH(RR, 0, false, at)                                                                   \
+                M3_BWD_LAUNCH(RR, 0, 0, ex)                                                                       \
         }                                                                                                         \
         break;
     switch (d.R) {
@@ -748,6 +801,12 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
 #undef M3_BWD_CASE
 #undef M3_BWD_LAUNCH
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (gate) {
+        const int64_t n = bh * d.seqlen * d.R * d.headdim;
+        const unsigned gb = (unsigned)((n + 255) / 256 < 148 * 16 ? (n + 255) / 256 : 148 * 16);
+        bwd_gate_dz<IO><<<gb, 256, 0, stream>>>((const IO*)dy, (const IO*)pp.z, (const IO*)pp.y_pre, pp.dz, n);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     const int64_t n4 = bh * d.seqlen * d.R * d.headdim / 4;
     int64_t nb = (n4 + 255) / 256;
     if (nb > 148 * 16) nb = 148 * 16;
@@ -784,11 +843,18 @@ size_t bwd_workspace_size(const ScanDims& d) { return bwd_ws(d).total; }
 
 size_t bwd_prep_workspace_size(const ScanDims& d) { return bwd_ws_prep_total(d); }
 
+bool bwd_gate_supported(const ScanDims& d) {
+    if (!bwd_supported(d)) return false;
+    const BwdLayout L =
+        bwd_layout((int)d.headdim, (int)d.dstate, d.R, bwd_chunk(d.R), d.io == M3_DTYPE_BF16 ? 2 : 4, true);
+    return sizeof(float) * (size_t)L.total <= 200 * 1024;
+}
+
 cudaError_t launch_scan_bwd(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                             const float* A, const float* lambda, const float* omega, const void* dy,
                             const float* d_final, float* dx, float* dB, float* dC, float* ddt, float* dA,
                             float* dlambda, float* domega, void* workspace, cudaStream_t stream) {
-    const BwdPrep pp{false, nullptr, nullptr, nullptr, nullptr, nullptr};
+    const BwdPrep pp{false, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     if (d.io == M3_DTYPE_BF16)
         return launch_bwd_io<__nv_bfloat16>(d, x, B, C, dt, A, lambda, omega, dy, d_final, dx, dB, dC, ddt, dA,
                                             dlambda, domega, workspace, stream, pp);
@@ -800,8 +866,9 @@ cudaError_t launch_scan_bwd_prep(const ScanDims& d, const void* x, const void* B
                                  const float* dt_raw, const float* dt_bias, const float* A_tok, const float* u,
                                  const float* omega, const void* dy, const float* d_final, float* dx, float* dB,
                                  float* dC, float* ddt_raw, float* dA_tok, float* du, float* domega,
-                                 float* ddt_bias, void* workspace, cudaStream_t stream) {
-    const BwdPrep pp{true, dt_raw, dt_bias, u, A_tok, ddt_bias};
+                                 float* ddt_bias, const void* z, const void* y_pre, float* dz, void* workspace,
+                                 cudaStream_t stream) {
+    const BwdPrep pp{true, dt_raw, dt_bias, u, A_tok, ddt_bias, z, y_pre, dz};
     if (d.io == M3_DTYPE_BF16)
         return launch_bwd_io<__nv_bfloat16>(d, x, B, C, nullptr, nullptr, nullptr, omega, dy, d_final, dx, dB, dC,
                                             ddt_raw, dA_tok, du, domega, workspace, stream, pp);

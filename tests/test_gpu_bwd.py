@@ -174,7 +174,7 @@ def _run_prep(inp, R, dy, dfin=None):
                               dy.cuda().contiguous(), None if dfin is None else dfin.cuda().contiguous(),
                               dt_bias=d["dt_bias"])
     torch.cuda.synchronize()
-    return {k: v.cpu().double().numpy() for k, v in g.items()}
+    return {k: v.cpu().double().numpy() for k, v in g.items() if v is not None}
 
 
 @pytest.mark.parametrize("io,Bt,H,T,P,N,R", [
@@ -217,7 +217,8 @@ def test_bwd_prep_larger_directional(io, Bt, H, T, P, N, R):
         assert abs(kern - num) <= TOL_BWD[io] * max(1.0, abs(num)), (k, kern, num)
 
 
-def test_bwd_prep_rejects_bc_norm_and_gate():
+def test_bwd_prep_rejects_bc_norm_and_gate_outside_forward_shapes():
+    """The B/C normalisation has no backward; the gate's needs the forward entry, which takes no P = 4."""
     w = synth.Workload("case", 1, 2, 8, 4, 4, 1, 64, "fp32")
     d = {k: v.cuda() for k, v in synth.make_prep_inputs(w, seed=1).items() if k in PREP_DEV}
     dy = torch.zeros_like(d["x"])
@@ -233,6 +234,7 @@ def test_bwd_prep_rejects_bc_norm_and_gate():
     bc = binding.prep_params(d["dt_bias"], {"norm": True, "eps": 1e-5}, None)
     assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws, bc) == binding.M3_ERR_UNSUPPORTED
     gate = binding.prep_params(d["dt_bias"], None, torch.zeros_like(d["x"]))
+    grads["dz"] = torch.empty(d["x"].shape, **f)
     assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws, gate) == binding.M3_ERR_UNSUPPORTED
     assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws[:64], ok) == binding.M3_ERR_WORKSPACE
     torch.cuda.synchronize()
@@ -252,3 +254,57 @@ def test_bwd_empty_inputs(Bt, T):
                                torch.zeros(pi["x"].shape, device="cuda"), dt_bias=pi["dt_bias"])
     torch.cuda.synchronize()
     assert torch.count_nonzero(gp["ddt_bias"]).item() == 0 and gp["dA"].numel() == 0
+
+
+# ---- through the output gate y = y_pre silu(z) (dz from the forward entry's ungated output)
+TOL_DZ = {"fp32": 2e-4, "bf16": 1e-2}   # bf16: y_pre as the forward writes it, rounded to bf16
+
+
+def _run_gate(inp, z, R, dy, dfin):
+    d = {k: inp[k].cuda().contiguous() for k in PREP_DEV}
+    g = binding.scan_bwd_prep(d["x"], d["B"], d["C"], d["dt_raw"], d["A"], d["u"], d["omega"], R,
+                              dy.cuda().contiguous(), dfin.cuda().contiguous(), dt_bias=d["dt_bias"],
+                              z=z.cuda().contiguous())
+    torch.cuda.synchronize()
+    return {k: v.cpu().double().numpy() for k, v in g.items()}
+
+
+def test_bwd_gate_small_every_element():
+    """fp32, P = 16 (the forward's CUDA-core path), three chunks: every gradient, dz included."""
+    w = synth.Workload("case", 1, 2, 21, 16, 8, 1, 64, "fp32")
+    inp = synth.make_prep_inputs(w, seed=51)
+    z = synth.make_gate(tuple(inp["x"].shape), io="fp32", seed=52)
+    gen = torch.Generator().manual_seed(53)
+    dy = torch.randn(inp["x"].shape, generator=gen)
+    dfin = torch.randn((1, 2, 8, 16), generator=gen)
+    got = _run_gate(inp, z, 1, dy, dfin)
+    ref_in = {k: oracle.f64(inp[k]) for k in grad.PREP_INPUTS}
+    ref_in["z"] = oracle.f64(z)
+    ref = grad.grad_fd(ref_in, oracle.f64(dy), oracle.f64(dfin), prep=True)
+    for k, name in list(PREP_NAMES.items()) + [("z", "dz")]:
+        err = oracle.rel_err(got[name], ref[k])
+        assert err < TOL_BWD["fp32"], f"{name}: {err:.2e}"
+
+
+@pytest.mark.parametrize("io,Bt,H,T,P,N,R", [
+    ("bf16", 1, 2, 130, 64, 64, 1),    # the forward's tensor-core path
+    ("fp32", 2, 1, 70, 32, 32, 2),
+])
+def test_bwd_gate_larger_directional(io, Bt, H, T, P, N, R):
+    w = synth.Workload("case", Bt, H, T, P, N, R, 64, io)
+    inp = synth.make_prep_inputs(w, seed=61)
+    z = synth.make_gate(tuple(inp["x"].shape), io=io, seed=62)
+    gen = torch.Generator().manual_seed(63)
+    dy = torch.randn(inp["x"].shape, generator=gen).to(inp["x"].dtype)
+    dfin = torch.randn((Bt, H, N, P), generator=gen)
+    got = _run_gate(inp, z, R, dy, dfin)
+    ref = {k: oracle.f64(inp[k]) for k in grad.PREP_INPUTS}
+    ref["z"] = oracle.f64(z)
+    dy64, df64 = oracle.f64(dy), oracle.f64(dfin)
+    rng = np.random.default_rng(64)
+    for k in grad.PREP_INPUTS + ("z",):
+        d = rng.standard_normal(ref[k].shape)
+        num = grad.directional(ref, k, d, dy64, df64, eps=1e-6, prep=True)
+        kern = float(np.sum(got[PREP_NAMES.get(k, "dz")] * d))
+        tol = TOL_DZ[io] if k == "z" else TOL_BWD[io]
+        assert abs(kern - num) <= tol * max(1.0, abs(num)), (k, kern, num)

@@ -156,3 +156,22 @@ def test_per_token_A_gradient_sums_to_the_per_head_one():
     tok["A"] = np.broadcast_to(inp["A"], inp["dt"].shape).copy()
     g_tok = grad.grad_fd(tok, dy, keys=("A",))["A"]
     assert np.max(np.abs(g_tok.sum(axis=(0, 1)) - g_head)) < 1e-7
+
+
+def test_gate_gradients_closed_form_and_reduction():
+    """Output gate y = y_pre * silu(z): dL/dz = dy * y_pre * silu'(z) with y_pre the ungated output and
+    silu'(z) = sigmoid(z) (1 + z (1 - sigmoid(z))); every other gradient equals the ungated one for the
+    seed dy * silu(z) (the loss is linear in dy)."""
+    pi = _prep_inp(T=6, seed=25)
+    rng = np.random.default_rng(26)
+    z = rng.standard_normal(pi["x"].shape)
+    dy = _dy(pi, seed=27)
+    gated = dict(pi)
+    gated["z"] = z
+    g = grad.grad_fd(gated, dy, prep=True)
+    y_pre, _, _ = oracle.scan_prep(*[pi[k] for k in grad.PREP_INPUTS])
+    s = oracle.sigmoid(z)
+    assert np.max(np.abs(g["z"] - dy * y_pre * s * (1.0 + z * (1.0 - s)))) < 1e-7
+    g0 = grad.grad_fd(pi, dy * oracle.silu(z), prep=True)
+    for k in grad.PREP_INPUTS:
+        assert np.max(np.abs(g[k] - g0[k])) < 1e-7, k
