@@ -319,20 +319,23 @@ def time_backward(binding, w, d, stream, steps, warmup, dist, device, seed=0):
     return sec, per
 
 
-def time_backward_prep(binding, w, stream, steps, warmup, dist, device, seed=0):
-    """m3_scan_bwd_prep on the workload's pre-activation inputs (dt_bias set) with a random dy."""
+def time_backward_prep(binding, w, stream, steps, warmup, dist, device, seed=0, gate=False):
+    """m3_scan_bwd_prep on the workload's pre-activation inputs (dt_bias set) with a random dy; ``gate``:
+    through the output gate as well (its z drawn like the forward leg's)."""
     dp = synth.make_prep_inputs(w, seed=seed, device=device)
+    z = synth.make_gate(tuple(dp["x"].shape), io=w.io, seed=seed, device=device) if gate else None
     gen = torch.Generator(device=device).manual_seed(2000 + seed)
     dy = torch.randn(dp["x"].shape, generator=gen, device=device).to(dp["x"].dtype)
     f = dict(dtype=torch.float32, device=device)
     grads = {"dx": torch.empty(dp["x"].shape, **f), "dB": torch.empty(dp["B"].shape, **f),
              "dC": torch.empty(dp["C"].shape, **f), "ddt_raw": torch.empty(dp["dt_raw"].shape, **f),
              "dA": torch.empty(dp["A"].shape, **f), "du": torch.empty(dp["u"].shape, **f),
-             "domega": torch.empty(dp["omega"].shape, **f), "ddt_bias": torch.empty((w.heads,), **f)}
+             "domega": torch.empty(dp["omega"].shape, **f), "ddt_bias": torch.empty((w.heads,), **f),
+             "dz": torch.empty(dp["x"].shape, **f) if gate else None}
     nbytes = binding.m3_scan_bwd_prep_workspace_size(w.batch, w.seqlen, w.heads, w.headdim, w.dstate, w.rank,
                                                      binding.io_code(dp["x"].dtype))
     ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
-    params = binding.prep_params(dp["dt_bias"], None, None)
+    params = binding.prep_params(dp["dt_bias"], None, z)
     args = [dp[k] for k in ("x", "B", "C", "dt_raw", "A", "u", "omega")]
 
     def call():
@@ -341,7 +344,7 @@ def time_backward_prep(binding, w, stream, steps, warmup, dist, device, seed=0):
             raise binding.M3Error(st, "m3_scan_bwd_prep")
 
     sec, per = _time_calls(call, stream, steps, warmup, dist, device)
-    del grads, ws, dy, dp
+    del grads, ws, dy, dp, z
     return sec, per
 
 
@@ -604,6 +607,10 @@ def backward_leg(binding, w, d, args, stream, dist, device, local, ws, rank):
     out["prep"] = {"value": w.batch * w.seqlen * ws * bsteps / psec / 1e6, "unit": "Mtok/s",
                    "ms_per_step": psec / bsteps * 1e3, "entry": "m3_scan_bwd_prep", "gpu_launches": 4 * bsteps,
                    "roofline_frac": fl / (pms * 1e-3) / 1e12 / FP32_ALU_TFLOPS}
+    # and through the output gate: one ungated forward launch for y_pre, z staged with dy, one dz launch
+    gsec, gper = time_backward_prep(binding, w, stream, bsteps, args.warmup, dist, device, seed=rank, gate=True)
+    out["prep"]["with_gate"] = {"value": w.batch * w.seqlen * ws * bsteps / gsec / 1e6, "unit": "Mtok/s",
+                                "ms_per_step": gsec / bsteps * 1e3}
     return out
 
 
