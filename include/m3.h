@@ -286,7 +286,7 @@ M3_API int m3_scan_bwd(const void* x, const void* B, const void* C, const float*
                        int io_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Backward pass of m3_scan_fwd_prep without its B/C normalisation:
+ * Backward pass of m3_scan_fwd_prep:
  * the gradients with respect to the pre-activations of Delta_t =
  * softplus(dt_raw_t + dt_bias_h) and lambda_t = sigmoid(u_t), and to the
  * per-token decay generators A_t (Table 1's time-varying discretisations).
@@ -294,16 +294,24 @@ M3_API int m3_scan_bwd(const void* x, const void* B, const void* C, const float*
  *   x, B, C, omega, R, sizes, io_dtype, dy, d_final: as m3_scan_bwd
  *   dt_raw, A, u   [batch, T, H] fp32 (A one value per token, as in
  *                  m3_scan_fwd_prep)
- *   params         nullable; dt_bias and z may be set (bc_norm, the gains and
- *                  the biases must be 0 / NULL, else M3_ERR_UNSUPPORTED)
+ *   params         nullable; as m3_scan_fwd_prep (dt_bias, the B/C
+ *                  normalisation with its gains and biases, the gate's z)
  *   dx, dB, dC, domega  out, as m3_scan_bwd
  *   ddt_raw, dA, du     out [batch, T, H] fp32
  *   ddt_bias       nullable out [H] fp32: sum over batch and tokens of ddt_raw
  *                  (accumulated with atomics)
  *   dz             out [batch, T, H, R, P] fp32 when params->z is set (the
  *                  output gate y = y_pre * SiLU(z)), else unused
+ *   dB_gain, dC_gain  nullable out [N] fp32; dB_bias, dC_bias  nullable out
+ *                  [H, R, N] fp32: the B/C normalisation's parameters (sums
+ *                  over rows by atomics); dB, dC are then the raw rows'
+ *                  gradients (through v -> v r gain + bias, r = rsqrt(mean(v^2)
+ *                  + eps)).  The B/C normalisation's backward takes fp32 io
+ *                  and no gate (else M3_ERR_UNSUPPORTED): the normalised rows
+ *                  reach the adjoint kernel in the io dtype
  *   workspace: m3_scan_bwd_prep_workspace_size bytes, 256-byte aligned:
- *            m3_scan_bwd's, Delta and lambda (2 * batch * T * H fp32) and,
+ *            m3_scan_bwd's, Delta and lambda (2 * batch * T * H fp32), the
+ *            normalised B and C rows (io dtype) and their inverse RMS, and,
  *            where the forward entry supports the shape, the ungated output
  *            y_pre (io dtype, y's layout) and m3_scan_fwd_prep's workspace.
  * Delta and lambda are derived with the forward entry's own functions; the
@@ -318,7 +326,8 @@ M3_API size_t m3_scan_bwd_prep_workspace_size(int64_t batch, int64_t seqlen, int
 M3_API int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const float* dt_raw, const float* A,
                             const float* u, const float* omega, int R, const void* dy, const float* d_final,
                             float* dx, float* dB, float* dC, float* ddt_raw, float* dA, float* du, float* domega,
-                            float* ddt_bias, float* dz, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                            float* ddt_bias, float* dz, float* dB_gain, float* dC_gain, float* dB_bias,
+                            float* dC_bias, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                             int64_t dstate, int io_dtype, const m3_prep_params* params, void* workspace,
                             size_t workspace_bytes, void* stream);
 

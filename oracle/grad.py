@@ -15,8 +15,11 @@ algorithm's uses listed in section 3.3.
 the derivative of L along one direction per input, for larger problems.  With
 ``prep=True`` the loss runs ``oracle.scan_prep`` on pre-activations instead
 (Delta = softplus(dt_raw + dt_bias), lambda = sigmoid(u), A per token; the
-time-varying discretisations of the page's Table 1), over PREP_INPUTS, and
-with a "z" entry in the inputs through the output gate y * silu(z) as well.
+time-varying discretisations of the page's Table 1), over PREP_INPUTS, with a
+"z" entry in the inputs through the output gate y * silu(z) as well, and with
+"bc_norm" / "bc_eps" entries through the B / C normalisation of ``bc_prep``
+(section 3.4), whose present "B_gain", "C_gain", "B_bias", "C_bias" entries are
+then inputs too.
 """
 from __future__ import annotations
 
@@ -28,15 +31,29 @@ INPUTS = ("x", "B", "C", "dt", "A", "lam", "omega")
 PREP_INPUTS = ("x", "B", "C", "dt_raw", "dt_bias", "A", "u", "omega")
 
 
+BC_INPUTS = ("B_gain", "C_gain", "B_bias", "C_bias")
+
+
 def _names(inp: dict, prep: bool):
     if not prep:
         return INPUTS
-    return PREP_INPUTS + (("z",) if inp.get("z") is not None else ())
+    extra = ("z",) if inp.get("z") is not None else ()
+    if "bc_norm" in inp:
+        extra += tuple(k for k in BC_INPUTS if inp.get(k) is not None)
+    return PREP_INPUTS + extra
+
+
+def _bc_of(inp: dict):
+    if "bc_norm" not in inp:
+        return None
+    bc = {"norm": bool(inp["bc_norm"]), "eps": float(inp.get("bc_eps", 0.0))}
+    bc.update({k: inp.get(k) for k in BC_INPUTS})
+    return bc
 
 
 def loss(inp: dict, dy, d_final=None, prep: bool = False) -> float:
     if prep:
-        y, hT, _ = scan_prep(*[inp[k] for k in PREP_INPUTS], z=inp.get("z"))
+        y, hT, _ = scan_prep(*[inp[k] for k in PREP_INPUTS], bc=_bc_of(inp), z=inp.get("z"))
     else:
         y, hT, _ = scan(*[inp[k] for k in INPUTS])
     val = float(np.sum(y * f64(dy)))
@@ -49,7 +66,8 @@ def grad_fd(inp: dict, dy, d_final=None, eps: float = 1e-6, keys=None, prep: boo
     """dL/d(input) for every element of the listed inputs, central differences with step eps."""
     names = _names(inp, prep)
     keys = names if keys is None else keys
-    base = {k: f64(inp[k]).copy() for k in names}
+    base = dict(inp)   # settings (bc_norm, bc_eps) as given, inputs as float64 copies
+    base.update({k: f64(inp[k]).copy() for k in names})
     out = {}
     for k in keys:
         g = np.zeros_like(base[k])
@@ -69,7 +87,8 @@ def grad_fd(inp: dict, dy, d_final=None, eps: float = 1e-6, keys=None, prep: boo
 
 def directional(inp: dict, key: str, v, dy, d_final=None, eps: float = 1e-6, prep: bool = False) -> float:
     """d/ds L(input[key] + s v) at s = 0, central differences with step eps."""
-    base = {k: f64(inp[k]).copy() for k in _names(inp, prep)}
+    base = dict(inp)
+    base.update({k: f64(inp[k]).copy() for k in _names(inp, prep)})
     v = f64(v)
     keep = base[key].copy()
     base[key] = keep + eps * v

@@ -64,7 +64,8 @@ SIGNATURES = {
     "m3_state_passing": ([_fp, _fp, _fp, _fp, _fp, _i64, _i64, _i64, _i64, _i64, _vp], _int),
     "m3_scan_bwd_prep_workspace_size": ([_i64, _i64, _i64, _i64, _i64, _int, _int], _sz),
     "m3_scan_bwd_prep": ([_vp, _vp, _vp, _fp, _fp, _fp, _fp, _int, _vp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp,
-                          _fp, _i64, _i64, _i64, _i64, _i64, _int, ctypes.POINTER(PrepParams), _vp, _sz, _vp], _int),
+                          _fp, _fp, _fp, _fp, _fp, _i64, _i64, _i64, _i64, _i64, _int, ctypes.POINTER(PrepParams),
+                          _vp, _sz, _vp], _int),
 }
 
 _lib = None
@@ -263,7 +264,7 @@ def m3_scan_bwd_prep_workspace_size(batch, seqlen, nheads, headdim, dstate, R, i
 def m3_scan_bwd_prep(x, B, C, dt_raw, A, u, omega, R: int, dy, d_final, grads: dict, workspace, params=None,
                      stream=None) -> int:
     """Call m3_scan_bwd_prep; ``grads`` holds the fp32 outputs dx, dB, dC, ddt_raw, dA, du, domega and
-    (optional, may be None) ddt_bias and dz.  Returns the status code."""
+    (optional, may be None) ddt_bias, dz, dB_gain, dC_gain, dB_bias, dC_bias.  Returns the status code."""
     Bt, T, H, R_, P = x.shape
     N = B.shape[-1]
     io = io_code(x.dtype)
@@ -273,15 +274,17 @@ def m3_scan_bwd_prep(x, B, C, dt_raw, A, u, omega, R: int, dy, d_final, grads: d
         _ptr(x, x.dtype), _ptr(B, x.dtype), _ptr(C, x.dtype), _ptr(dt_raw, f), _ptr(A, f), _ptr(u, f), _ptr(omega, f),
         int(R), _ptr(dy, x.dtype), _ptr(d_final, f), _ptr(grads["dx"], f), _ptr(grads["dB"], f), _ptr(grads["dC"], f),
         _ptr(grads["ddt_raw"], f), _ptr(grads["dA"], f), _ptr(grads["du"], f), _ptr(grads["domega"], f),
-        _ptr(grads.get("ddt_bias"), f), _ptr(grads.get("dz"), f), Bt, T, H, P, N, io,
+        _ptr(grads.get("ddt_bias"), f), _ptr(grads.get("dz"), f), _ptr(grads.get("dB_gain"), f),
+        _ptr(grads.get("dC_gain"), f), _ptr(grads.get("dB_bias"), f), _ptr(grads.get("dC_bias"), f), Bt, T, H, P, N, io,
         None if params is None else ctypes.byref(params),
         _ptr(workspace), ws_bytes, _stream(stream)))
 
 
-def scan_bwd_prep(x, B, C, dt_raw, A, u, omega, R: int, dy, d_final=None, dt_bias=None, z=None, workspace=None,
-                  stream=None) -> dict:
-    """Backward pass of scan_fwd_prep (no B/C normalisation): fp32 gradients dx, dB, dC, ddt_raw, dA (per
-    token), du, domega, with ``dt_bias`` ddt_bias, and with the output gate's ``z`` dz."""
+def scan_bwd_prep(x, B, C, dt_raw, A, u, omega, R: int, dy, d_final=None, dt_bias=None, z=None, bc=None,
+                  workspace=None, stream=None) -> dict:
+    """Backward pass of scan_fwd_prep: fp32 gradients dx, dB, dC, ddt_raw, dA (per token), du, domega, with
+    ``dt_bias`` ddt_bias, with the output gate's ``z`` dz, and with ``bc`` (as scan_fwd_prep's) the gradients
+    of its present gains and biases (dB_gain, dC_gain, dB_bias, dC_bias)."""
     Bt, T, H, _, P = x.shape
     N = B.shape[-1]
     f = dict(dtype=torch.float32, device=x.device)
@@ -290,10 +293,13 @@ def scan_bwd_prep(x, B, C, dt_raw, A, u, omega, R: int, dy, d_final=None, dt_bia
              "du": torch.empty(u.shape, **f), "domega": torch.empty(omega.shape, **f),
              "ddt_bias": None if dt_bias is None else torch.empty((H,), **f),
              "dz": None if z is None else torch.empty(x.shape, **f)}
+    for k in ("B_gain", "C_gain", "B_bias", "C_bias"):
+        if bc is not None and bc.get(k) is not None:
+            grads["d" + k] = torch.empty(bc[k].shape, **f)
     if workspace is None:
         nbytes = m3_scan_bwd_prep_workspace_size(Bt, T, H, P, N, R, io_code(x.dtype))
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device)
-    params = None if dt_bias is None and z is None else prep_params(dt_bias, None, z)
+    params = None if dt_bias is None and z is None and bc is None else prep_params(dt_bias, bc, z)
     _check(m3_scan_bwd_prep(x, B, C, dt_raw, A, u, omega, R, dy, d_final, grads, workspace, params, stream),
            "m3_scan_bwd_prep")
     return grads

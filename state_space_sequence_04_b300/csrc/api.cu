@@ -258,9 +258,9 @@ size_t m3_scan_bwd_prep_workspace_size(int64_t batch, int64_t seqlen, int64_t nh
 int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const float* dt_raw, const float* A,
                      const float* u, const float* omega, int R, const void* dy, const float* d_final, float* dx,
                      float* dB, float* dC, float* ddt_raw, float* dA, float* du, float* domega, float* ddt_bias,
-                     float* dz, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
-                     int io_dtype, const m3_prep_params* params, void* workspace, size_t workspace_bytes,
-                     void* stream) {
+                     float* dz, float* dB_gain, float* dC_gain, float* dB_bias, float* dC_bias, int64_t batch,
+                     int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate, int io_dtype,
+                     const m3_prep_params* params, void* workspace, size_t workspace_bytes, void* stream) {
     const m3::ScanDims d{batch, seqlen, nheads, headdim, dstate, R, 64, io_dtype};
     if (!ok_io(io_dtype)) return M3_ERR_INVALID_ARG;
     if (batch < 0 || seqlen < 0 || nheads < 1 || headdim < 1 || dstate < 2 || dstate % 2 || R < 1)
@@ -270,8 +270,16 @@ int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const float* d
     const void* z = params != nullptr ? params->z : nullptr;
     if (!ok_nullable(dt_bias) || !ok_nullable(ddt_bias) || !ok_nullable(d_final) || !ok_nullable(z))
         return M3_ERR_INVALID_ARG;
-    if (params != nullptr && (params->bc_norm || params->B_gain || params->C_gain || params->B_bias || params->C_bias))
-        return M3_ERR_UNSUPPORTED;   // no backward through the B/C normalisation
+    m3::Prep fp{};
+    if (params != nullptr && !prep_from(params, &fp)) return M3_ERR_INVALID_ARG;
+    const float* gouts[] = {dB_gain, dC_gain, dB_bias, dC_bias};
+    for (const float* q : gouts)
+        if (!ok_nullable(q)) return M3_ERR_INVALID_ARG;
+    const m3::BwdBcArgs bca{params != nullptr && fp.bc(), fp.bc_norm ? 1 : 0, fp.bc_eps, fp.B_gain, fp.C_gain,
+                            fp.B_bias, fp.C_bias, dB_gain, dC_gain, dB_bias, dC_bias};
+    // the normalised rows feed the adjoint kernel in the io dtype: bf16 rows lose too much for gradients,
+    // so the B / C normalisation's backward takes fp32 io, and not together with the gate
+    if (bca.on && (io_dtype != M3_DTYPE_F32 || params->z != nullptr)) return M3_ERR_UNSUPPORTED;
     if (batch * nheads > (int64_t)INT32_MAX || seqlen > (int64_t)INT32_MAX) return M3_ERR_UNSUPPORTED;
     if (!m3::bwd_supported(d)) return M3_ERR_UNSUPPORTED;
     const BwdPrepWs w = bwd_prep_ws(d);
@@ -288,16 +296,15 @@ int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const float* d
     char* ws = static_cast<char*>(workspace);
     void* y_pre = nullptr;
     if (z != nullptr && any_tokens) {   // the ungated forward output, by the forward entry itself
-        m3::Prep fp{};
-        if (!prep_from(params, &fp)) return M3_ERR_INVALID_ARG;
-        fp.z = nullptr;
+        m3::Prep ug = fp;
+        ug.z = nullptr;
         y_pre = ws + w.y_pre;
         const int st = scan_impl(x, B, C, dt_raw, A, u, omega, R, 64, y_pre, nullptr, batch, seqlen, nheads, headdim,
-                                 dstate, io_dtype, ws + w.fwd, w.total - w.fwd, stream, fp);
+                                 dstate, io_dtype, ws + w.fwd, w.total - w.fwd, stream, ug);
         if (st != M3_OK) return st;
     }
     return cuda_status(m3::launch_scan_bwd_prep(d, x, B, C, dt_raw, dt_bias, A, u, omega, dy, d_final, dx, dB, dC,
-                                                ddt_raw, dA, du, domega, ddt_bias, z, y_pre, dz, workspace,
+                                                ddt_raw, dA, du, domega, ddt_bias, z, y_pre, dz, bca, workspace,
                                                 static_cast<cudaStream_t>(stream)));
 }
 

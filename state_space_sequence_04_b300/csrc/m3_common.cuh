@@ -106,14 +106,23 @@ cudaError_t launch_scan_bwd(const ScanDims& d, const void* x, const void* B, con
                             const float* d_final, float* dx, float* dB, float* dC, float* ddt, float* dA,
                             float* dlambda, float* domega, void* workspace, cudaStream_t stream);
 size_t bwd_prep_workspace_size(const ScanDims& d);
+// the B / C normalisation of m3_scan_bwd_prep: settings, parameters and their gradients (nullable)
+struct BwdBcArgs {
+    bool on;
+    int norm;
+    float eps;
+    const float *B_gain, *C_gain, *B_bias, *C_bias;
+    float *dB_gain, *dC_gain, *dB_bias, *dC_bias;
+};
 // m3_scan_bwd on pre-activations (Delta = softplus(dt_raw + dt_bias), lambda = sigmoid(u), A_t per token);
-// z != nullptr: through the output gate y = y_pre silu(z), y_pre the ungated output (io dtype), dz out
+// z != nullptr: through the output gate y = y_pre silu(z), y_pre the ungated output (io dtype), dz out;
+// bc.on: through the B / C normalisation
 cudaError_t launch_scan_bwd_prep(const ScanDims& d, const void* x, const void* B, const void* C,
                                  const float* dt_raw, const float* dt_bias, const float* A_tok, const float* u,
                                  const float* omega, const void* dy, const float* d_final, float* dx, float* dB,
                                  float* dC, float* ddt_raw, float* dA_tok, float* du, float* domega,
-                                 float* ddt_bias, const void* z, const void* y_pre, float* dz, void* workspace,
-                                 cudaStream_t stream);
+                                 float* ddt_bias, const void* z, const void* y_pre, float* dz, const BwdBcArgs& bc,
+                                 void* workspace, cudaStream_t stream);
 // the backward through the output gate (z) fits the shared-memory budget
 bool bwd_gate_supported(const ScanDims& d);
 // Delta = softplus(dt_raw + dt_bias[h]) and lambda = sigmoid(u) of n (batch, token, head) entries

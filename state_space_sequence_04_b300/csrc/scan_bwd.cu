@@ -690,6 +690,104 @@ __global__ void bwd_gate_dz(const IO* __restrict__ dy, const IO* __restrict__ z,
     }
 }
 
+// B / C normalisation of every (token, rank) row ("Mamba-3", section 3.4): Vn = V r gain + bias with
+// r = rsqrt(mean(V^2) + eps) (the forward entry's formula; r = 1 and no gain without the norm), r kept for
+// the rows' backward.  One warp per row; rows are (batch, token, head, rank) major, HR = H * R.
+template <typename IO>
+__global__ void __launch_bounds__(256) bc_rows_forward(const IO* __restrict__ V, const float* __restrict__ gain,
+                                                       const float* __restrict__ bias, int norm, float eps,
+                                                       IO* __restrict__ Vn, float* __restrict__ rinv, int64_t rows,
+                                                       int HR, int N) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; row < rows; row += nwarps) {
+        float ss = 0.f;
+        for (int n = lane; n < N; n += 32) {
+            const float a = ld_io(V, row * N + n);
+            ss = fmaf(a, a, ss);
+        }
+        ss = warp_sum(ss);
+        const float r = norm ? rsqrtf(ss / N + eps) : 1.f;
+        const float* bb = bias != nullptr ? bias + (row % HR) * N : nullptr;
+        for (int n = lane; n < N; n += 32) {
+            float a = ld_io(V, row * N + n);
+            if (norm) {
+                a *= r;
+                if (gain != nullptr) a *= gain[n];
+            }
+            if (bb != nullptr) a += bb[n];
+            st_io(Vn, row * N + n, a);
+        }
+        if (lane == 0) rinv[row] = r;
+    }
+}
+
+// The rows' backward: dV holds dL/dVn on entry and dL/dV on return,
+//   dV = r (gain dVn) - V r^3 / N sum_n(gain dVn V)   (with the norm; dV = dVn without it);
+// dgain [N] += sum over every row of dVn V r, dbias [H, R, N] += sum over (batch, token) of dVn.
+// Block (h*R + rank, token block): 8 warps, one row at a time each; per-lane partial sums, then shared-memory
+// and one global atomic add per channel and block.
+template <typename IO>
+__global__ void __launch_bounds__(256) bc_rows_backward(const IO* __restrict__ V, const float* __restrict__ gain,
+                                                        const float* __restrict__ rinv, int norm,
+                                                        float* __restrict__ dV, float* __restrict__ dgain,
+                                                        float* __restrict__ dbias, int64_t BT, int HR, int N) {
+    __shared__ float sg[256], sb[256];
+    const int hr = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int n = threadIdx.x; n < N; n += blockDim.x) sg[n] = sb[n] = 0.f;
+    __syncthreads();
+    float ag[8], ab[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ag[k] = ab[k] = 0.f;
+    for (int64_t bt = (int64_t)blockIdx.y * 8 + warp; bt < BT; bt += (int64_t)gridDim.y * 8) {
+        const int64_t row = bt * HR + hr;
+        const float r = rinv[row];
+        float gd[8], vv[8], s = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int n = lane + 32 * k;
+            gd[k] = vv[k] = 0.f;
+            if (n < N) {
+                const float dn = dV[row * N + n], v = ld_io(V, row * N + n);
+                gd[k] = (norm && gain != nullptr ? gain[n] : 1.f) * dn;   // the gain acts only with the norm
+                vv[k] = v;
+                s = fmaf(gd[k], v, s);
+                ab[k] += dn;
+                ag[k] = fmaf(dn * v, r, ag[k]);
+            }
+        }
+        s = warp_sum(s);
+        const float c = r * r * r * s / N;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int n = lane + 32 * k;
+            if (n < N) dV[row * N + n] = norm ? fmaf(r, gd[k], -vv[k] * c) : gd[k];
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int n = lane + 32 * k;
+        if (n < N) {
+            atomicAdd(&sg[n], ag[k]);
+            atomicAdd(&sb[n], ab[k]);
+        }
+    }
+    __syncthreads();
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+        if (dgain != nullptr && norm) atomicAdd(&dgain[n], sg[n]);
+        if (dbias != nullptr) atomicAdd(&dbias[hr * N + n], sb[n]);
+    }
+}
+
+// B / C normalisation arguments of m3_scan_bwd_prep (on == false: none)
+struct BwdBc {
+    bool on;
+    int norm;
+    float eps;
+    const float *B_gain, *C_gain, *B_bias, *C_bias;
+    float *dB_gain, *dC_gain, *dB_bias, *dC_bias;
+};
+
 // pre-activation inputs of m3_scan_bwd_prep (on == false: the plain entry); z != nullptr: the output gate
 struct BwdPrep {
     bool on;
@@ -697,12 +795,13 @@ struct BwdPrep {
     float* ddt_bias;
     const void *z, *y_pre;
     float* dz;
+    BwdBc bc;
 };
 
 int bwd_chunk(int R) { return R <= 2 ? 8 : 4; }
 
 struct BwdWs {
-    size_t ckpt, part_dx, part_s, dt_eff, lam_eff, total;   // byte offsets of the sections; the whole size
+    size_t ckpt, part_dx, part_s, dt_eff, lam_eff, bn, cn, rb, rc, total;   // byte offsets; the whole size
 };
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
@@ -722,10 +821,21 @@ BwdWs bwd_ws(const ScanDims& d) {
     return w;
 }
 
-size_t bwd_ws_prep_total(const ScanDims& d) {
-    const BwdWs w = bwd_ws(d);
-    return w.lam_eff + round256(sizeof(float) * (size_t)(d.batch * d.nheads) * (size_t)d.seqlen);
+// the pre-activation entry's sections: Delta, lambda, then the normalised B and C rows (io dtype) and
+// their inverse RMS (fp32) for the B / C normalisation
+BwdWs bwd_ws_prep(const ScanDims& d) {
+    BwdWs w = bwd_ws(d);
+    const size_t bth = (size_t)(d.batch * d.nheads) * (size_t)d.seqlen, rows = bth * (size_t)d.R;
+    const size_t e = d.io == M3_DTYPE_BF16 ? 2 : 4;
+    w.bn = w.lam_eff + round256(sizeof(float) * bth);
+    w.cn = w.bn + round256(e * rows * (size_t)d.dstate);
+    w.rb = w.cn + round256(e * rows * (size_t)d.dstate);
+    w.rc = w.rb + round256(sizeof(float) * rows);
+    w.total = w.rc + round256(sizeof(float) * rows);
+    return w;
 }
+
+size_t bwd_ws_prep_total(const ScanDims& d) { return bwd_ws_prep(d).total; }
 
 template <typename IO>
 cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
@@ -741,9 +851,35 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
         e = cudaMemsetAsync(dA, 0, sizeof(float) * (size_t)d.nheads, stream);
     else if (pp.ddt_bias != nullptr)
         e = cudaMemsetAsync(pp.ddt_bias, 0, sizeof(float) * (size_t)d.nheads, stream);
+    if (e == cudaSuccess && pp.bc.on) {
+        float* zs[] = {pp.bc.dB_gain, pp.bc.dC_gain};
+        for (float* q : zs)
+            if (q != nullptr && e == cudaSuccess) e = cudaMemsetAsync(q, 0, sizeof(float) * (size_t)d.dstate, stream);
+        float* zb[] = {pp.bc.dB_bias, pp.bc.dC_bias};
+        for (float* q : zb)
+            if (q != nullptr && e == cudaSuccess)
+                e = cudaMemsetAsync(q, 0, sizeof(float) * (size_t)(d.nheads * d.R * d.dstate), stream);
+    }
     if (e != cudaSuccess || bh == 0 || d.seqlen == 0) return e;
-    const BwdWs w = bwd_ws(d);
+    const BwdWs w = pp.on ? bwd_ws_prep(d) : bwd_ws(d);
     char* ws = static_cast<char*>(workspace);
+    const void *B_raw = B, *C_raw = C;
+    const int64_t rows = bh * d.seqlen * d.R;
+    const int HR = (int)(d.nheads * d.R);
+    if (pp.bc.on) {   // the normalised rows the recurrence sees
+        void* Bn = ws + w.bn;
+        void* Cn = ws + w.cn;
+        const unsigned rbk = (unsigned)((rows + 7) / 8 < 148 * 16 ? (rows + 7) / 8 : 148 * 16);
+        bc_rows_forward<IO><<<rbk, 256, 0, stream>>>((const IO*)B, pp.bc.B_gain, pp.bc.B_bias, pp.bc.norm, pp.bc.eps,
+                                                     (IO*)Bn, reinterpret_cast<float*>(ws + w.rb), rows, HR,
+                                                     (int)d.dstate);
+        bc_rows_forward<IO><<<rbk, 256, 0, stream>>>((const IO*)C, pp.bc.C_gain, pp.bc.C_bias, pp.bc.norm, pp.bc.eps,
+                                                     (IO*)Cn, reinterpret_cast<float*>(ws + w.rc), rows, HR,
+                                                     (int)d.dstate);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        B = Bn;
+        C = Cn;
+    }
     if (pp.on) {   // Delta and lambda from their pre-activations, as the forward entry derives them
         float* dt_eff = reinterpret_cast<float*>(ws + w.dt_eff);
         float* lam_eff = reinterpret_cast<float*>(ws + w.lam_eff);
@@ -822,7 +958,19 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
         bwd_finish_scalars<<<dim3((unsigned)d.nheads, gy), 256, 0, stream>>>(
             reinterpret_cast<const float4*>(part_s), dt, lambda, A, ddt, dlambda, dA, d.batch, d.seqlen,
             (int)d.nheads, L.nPB);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (pp.bc.on) {   // from the normalised rows' gradients to the raw rows', the gains' and the biases'
+        const int64_t BT = d.batch * d.seqlen;
+        const dim3 g2((unsigned)HR, (unsigned)((BT + 7) / 8 < 1024 ? (BT + 7) / 8 : 1024));
+        bc_rows_backward<IO><<<g2, 256, 0, stream>>>((const IO*)B_raw, pp.bc.B_gain,
+                                                     reinterpret_cast<const float*>(ws + w.rb), pp.bc.norm, dB,
+                                                     pp.bc.dB_gain, pp.bc.dB_bias, BT, HR, (int)d.dstate);
+        bc_rows_backward<IO><<<g2, 256, 0, stream>>>((const IO*)C_raw, pp.bc.C_gain,
+                                                     reinterpret_cast<const float*>(ws + w.rc), pp.bc.norm, dC,
+                                                     pp.bc.dC_gain, pp.bc.dC_bias, BT, HR, (int)d.dstate);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 }  // namespace
@@ -854,7 +1002,7 @@ cudaError_t launch_scan_bwd(const ScanDims& d, const void* x, const void* B, con
                             const float* A, const float* lambda, const float* omega, const void* dy,
                             const float* d_final, float* dx, float* dB, float* dC, float* ddt, float* dA,
                             float* dlambda, float* domega, void* workspace, cudaStream_t stream) {
-    const BwdPrep pp{false, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    const BwdPrep pp{false, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, BwdBc{}};
     if (d.io == M3_DTYPE_BF16)
         return launch_bwd_io<__nv_bfloat16>(d, x, B, C, dt, A, lambda, omega, dy, d_final, dx, dB, dC, ddt, dA,
                                             dlambda, domega, workspace, stream, pp);
@@ -866,9 +1014,11 @@ cudaError_t launch_scan_bwd_prep(const ScanDims& d, const void* x, const void* B
                                  const float* dt_raw, const float* dt_bias, const float* A_tok, const float* u,
                                  const float* omega, const void* dy, const float* d_final, float* dx, float* dB,
                                  float* dC, float* ddt_raw, float* dA_tok, float* du, float* domega,
-                                 float* ddt_bias, const void* z, const void* y_pre, float* dz, void* workspace,
-                                 cudaStream_t stream) {
-    const BwdPrep pp{true, dt_raw, dt_bias, u, A_tok, ddt_bias, z, y_pre, dz};
+                                 float* ddt_bias, const void* z, const void* y_pre, float* dz, const BwdBcArgs& bca,
+                                 void* workspace, cudaStream_t stream) {
+    const BwdBc bc{bca.on, bca.norm, bca.eps, bca.B_gain, bca.C_gain, bca.B_bias, bca.C_bias,
+                   bca.dB_gain, bca.dC_gain, bca.dB_bias, bca.dC_bias};
+    const BwdPrep pp{true, dt_raw, dt_bias, u, A_tok, ddt_bias, z, y_pre, dz, bc};
     if (d.io == M3_DTYPE_BF16)
         return launch_bwd_io<__nv_bfloat16>(d, x, B, C, nullptr, nullptr, nullptr, omega, dy, d_final, dx, dB, dC,
                                             ddt_raw, dA_tok, du, domega, workspace, stream, pp);

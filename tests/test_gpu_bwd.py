@@ -217,8 +217,9 @@ def test_bwd_prep_larger_directional(io, Bt, H, T, P, N, R):
         assert abs(kern - num) <= TOL_BWD[io] * max(1.0, abs(num)), (k, kern, num)
 
 
-def test_bwd_prep_rejects_bc_norm_and_gate_outside_forward_shapes():
-    """The B/C normalisation has no backward; the gate's needs the forward entry, which takes no P = 4."""
+def test_bwd_prep_gate_outside_forward_shapes_and_bad_arguments():
+    """The gate's backward needs the forward entry, which takes no P = 4; the B/C normalisation needs no
+    forward and runs."""
     w = synth.Workload("case", 1, 2, 8, 4, 4, 1, 64, "fp32")
     d = {k: v.cuda() for k, v in synth.make_prep_inputs(w, seed=1).items() if k in PREP_DEV}
     dy = torch.zeros_like(d["x"])
@@ -232,7 +233,7 @@ def test_bwd_prep_rejects_bc_norm_and_gate_outside_forward_shapes():
     ok = binding.prep_params(d["dt_bias"], None, None)
     assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws, ok) == binding.M3_OK
     bc = binding.prep_params(d["dt_bias"], {"norm": True, "eps": 1e-5}, None)
-    assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws, bc) == binding.M3_ERR_UNSUPPORTED
+    assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws, bc) == binding.M3_OK
     gate = binding.prep_params(d["dt_bias"], None, torch.zeros_like(d["x"]))
     grads["dz"] = torch.empty(d["x"].shape, **f)
     assert binding.m3_scan_bwd_prep(*args, 1, dy, None, grads, ws, gate) == binding.M3_ERR_UNSUPPORTED
@@ -308,3 +309,70 @@ def test_bwd_gate_larger_directional(io, Bt, H, T, P, N, R):
         kern = float(np.sum(got[PREP_NAMES.get(k, "dz")] * d))
         tol = TOL_DZ[io] if k == "z" else TOL_BWD[io]
         assert abs(kern - num) <= tol * max(1.0, abs(num)), (k, kern, num)
+
+
+# ---- through the B / C normalisation (rows v -> v r gain + bias), alone and with the gate
+BC_KEYS = ("B_gain", "C_gain", "B_bias", "C_bias")
+
+
+def _bc_case(w, seed):
+    inp = synth.make_prep_inputs(w, seed=seed)
+    bc = synth.make_bc_params(w.heads, w.rank, w.dstate, seed=seed + 1)
+    return inp, bc
+
+
+def _run_bc(inp, bc, R, dy, dfin, z=None):
+    d = {k: inp[k].cuda().contiguous() for k in PREP_DEV}
+    bcd = {k: (v.cuda() if hasattr(v, "cuda") else v) for k, v in bc.items()}
+    g = binding.scan_bwd_prep(d["x"], d["B"], d["C"], d["dt_raw"], d["A"], d["u"], d["omega"], R,
+                              dy.cuda().contiguous(), dfin.cuda().contiguous(), dt_bias=d["dt_bias"], bc=bcd,
+                              z=None if z is None else z.cuda().contiguous())
+    torch.cuda.synchronize()
+    return {k: v.cpu().double().numpy() for k, v in g.items() if v is not None}
+
+
+def _bc_ref(inp, bc, z=None):
+    ref = {k: oracle.f64(inp[k]) for k in grad.PREP_INPUTS}
+    ref.update({k: oracle.f64(bc[k]) for k in BC_KEYS})
+    ref["bc_norm"], ref["bc_eps"] = bool(bc["norm"]), float(bc["eps"])
+    if z is not None:
+        ref["z"] = oracle.f64(z)
+    return ref
+
+
+def test_bwd_bc_small_every_element():
+    """fp32, three chunks, R = 2: every gradient, the gains' and the biases' included."""
+    w = synth.Workload("case", 1, 2, 19, 4, 8, 2, 64, "fp32")
+    inp, bc = _bc_case(w, 71)
+    gen = torch.Generator().manual_seed(72)
+    dy = torch.randn(inp["x"].shape, generator=gen)
+    dfin = torch.randn((1, 2, 8, 4), generator=gen)
+    got = _run_bc(inp, bc, 2, dy, dfin)
+    ref = grad.grad_fd(_bc_ref(inp, bc), oracle.f64(dy), oracle.f64(dfin), prep=True)
+    names = dict(PREP_NAMES, **{k: "d" + k for k in BC_KEYS})
+    for k, name in names.items():
+        err = oracle.rel_err(got[name], ref[k])
+        assert err < TOL_BWD["fp32"], f"{name}: {err:.2e}"
+
+
+def test_bwd_bc_unsupported_forms():
+    """The B / C normalisation's backward takes fp32 io and no gate: bf16 rows of the normalised B and C
+    would feed the adjoint kernel rounded (host-side checks, no launch)."""
+    for io, gate in (("bf16", False), ("fp32", True)):
+        w = synth.Workload("case", 1, 2, 8, 16, 8, 1, 64, io)
+        inp, bc = _bc_case(w, 91)
+        d = {k: inp[k].cuda().contiguous() for k in PREP_DEV}
+        bcd = {k: (v.cuda() if hasattr(v, "cuda") else v) for k, v in bc.items()}
+        z = torch.zeros_like(d["x"]) if gate else None
+        f = dict(dtype=torch.float32, device="cuda")
+        grads = {"dx": torch.empty(d["x"].shape, **f), "dB": torch.empty(d["B"].shape, **f),
+                 "dC": torch.empty(d["C"].shape, **f), "ddt_raw": torch.empty(d["dt_raw"].shape, **f),
+                 "dA": torch.empty(d["A"].shape, **f), "du": torch.empty(d["u"].shape, **f),
+                 "domega": torch.empty(d["omega"].shape, **f), "dz": torch.empty(d["x"].shape, **f)}
+        nbytes = binding.m3_scan_bwd_prep_workspace_size(1, 8, 2, 16, 8, 1, binding.io_code(d["x"].dtype))
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+        args = [d[k] for k in ("x", "B", "C", "dt_raw", "A", "u", "omega")]
+        params = binding.prep_params(d["dt_bias"], bcd, z)
+        assert binding.m3_scan_bwd_prep(*args, 1, torch.zeros_like(d["x"]), None, grads, ws,
+                                        params) == binding.M3_ERR_UNSUPPORTED
+    torch.cuda.synchronize()

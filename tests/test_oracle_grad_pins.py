@@ -175,3 +175,44 @@ def test_gate_gradients_closed_form_and_reduction():
     g0 = grad.grad_fd(pi, dy * oracle.silu(z), prep=True)
     for k in grad.PREP_INPUTS:
         assert np.max(np.abs(g[k] - g0[k])) < 1e-7, k
+
+
+# ---- through the B / C normalisation (section 3.4): rows v -> v r gain + bias, r = (mean(v^2) + eps)^(-1/2)
+def _bc_inp(T=6, seed=29, eps=1e-5):
+    pi = _prep_inp(T=T, seed=seed)
+    bc = synth.make_bc_params(2, 2, 4, seed=seed + 1)
+    pi.update({k: oracle.f64(bc[k]) for k in grad.BC_INPUTS})
+    pi["bc_norm"], pi["bc_eps"] = True, eps
+    return pi
+
+
+def test_bc_gradients_against_the_normalised_rows():
+    """With dn = dL/d(normalised B) from the plain recurrence run on the normalised rows: dB_bias sums dn
+    over batch and tokens, dB_gain sums dn v r over every row, and dB = r (gain dn) - v r^3 / N
+    sum(gain dn v) (the Jacobian of v -> v r gain, written out); the same for C."""
+    pi = _bc_inp()
+    dy = _dy(pi, seed=30)
+    g = grad.grad_fd(pi, dy, prep=True)
+    d, lam = oracle.prep(pi["dt_raw"], pi["dt_bias"], pi["u"])
+    Bn = oracle.bc_prep(pi["B"], True, pi["bc_eps"], pi["B_gain"], pi["B_bias"])
+    Cn = oracle.bc_prep(pi["C"], True, pi["bc_eps"], pi["C_gain"], pi["C_bias"])
+    plain = {"x": pi["x"], "B": Bn, "C": Cn, "dt": d, "A": pi["A"], "lam": lam, "omega": pi["omega"]}
+    gp = grad.grad_fd(plain, dy, keys=("B", "C"))
+    N = pi["B"].shape[-1]
+    for V, key in (("B", "B"), ("C", "C")):
+        v, dn, gain = pi[V], gp[key], pi[V + "_gain"]
+        r = 1.0 / np.sqrt(np.mean(v * v, axis=-1, keepdims=True) + pi["bc_eps"])
+        assert np.max(np.abs(g[V + "_bias"] - dn.sum(axis=(0, 1)))) < 1e-6
+        assert np.max(np.abs(g[V + "_gain"] - (dn * v * r).sum(axis=(0, 1, 2, 3)))) < 1e-6
+        gd = gain * dn
+        dv = r * gd - v * r ** 3 / N * np.sum(gd * v, axis=-1, keepdims=True)
+        assert np.max(np.abs(g[V] - dv)) < 1e-6
+
+
+def test_bc_normalisation_is_scale_invariant():
+    """With eps = 0 the normalised rows do not change when a row is scaled, so every raw row's gradient is
+    orthogonal to the row."""
+    pi = _bc_inp(eps=0.0)
+    g = grad.grad_fd(pi, _dy(pi, seed=31), prep=True, keys=("B", "C"))
+    for V in ("B", "C"):
+        assert np.max(np.abs(np.sum(g[V] * pi[V], axis=-1))) < 1e-7
