@@ -609,8 +609,12 @@ def backward_leg(binding, w, d, args, stream, dist, device, local, ws, rank):
                    "roofline_frac": fl / (pms * 1e-3) / 1e12 / FP32_ALU_TFLOPS}
     # and through the output gate: one ungated forward launch for y_pre, z staged with dy, one dz launch
     gsec, gper = time_backward_prep(binding, w, stream, bsteps, args.warmup, dist, device, seed=rank, gate=True)
+    path, flaunch = binding.m3_scan_fwd_plan(w.batch, w.seqlen, w.heads, w.headdim, w.dstate, w.rank, 64,
+                                             binding.io_code(d["x"].dtype))
     out["prep"]["with_gate"] = {"value": w.batch * w.seqlen * ws * bsteps / gsec / 1e6, "unit": "Mtok/s",
-                                "ms_per_step": gsec / bsteps * 1e3}
+                                "ms_per_step": gsec / bsteps * 1e3,
+                                # Delta/lambda, the ungated forward, the adjoint, dz, the two finishing kernels
+                                "gpu_launches": (5 + flaunch) * bsteps}
     return out
 
 
