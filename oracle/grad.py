@@ -96,3 +96,64 @@ def directional(inp: dict, key: str, v, dy, d_final=None, eps: float = 1e-6, pre
     base[key] = keep - eps * v
     lm = loss(base, dy, d_final, prep)
     return (lp - lm) / (2.0 * eps)
+
+
+def adjoint(inp: dict, dy, d_final=None) -> dict:
+    """The same gradients as ``grad_fd`` for the plain inputs, from the adjoint of the recurrence
+    written out step by step (float64, no finite differences).  With u_t = alpha_t h_{t-1} +
+    beta_t v_{t-1}, h_t = R(phi_t) u_t + gamma_t v_t, v_t = B_t^T X_t and y_t = h_t^T C_t, going
+    backwards from gbar_{T-1} = d_final:
+      gbar_t = C_t dy_t^T + alpha_{t+1} ubar_{t+1},  ubar_t = R(phi_t)^T gbar_t,
+      dv_t = gamma_t gbar_t + beta_{t+1} ubar_{t+1},
+    and dalpha_t = <ubar_t, h_{t-1}>, dbeta_t = <ubar_t, v_{t-1}>, dgamma_t = <gbar_t, v_t>,
+    dphi_t = sum_p (gbar[2j+1] r[2j] - gbar[2j] r[2j+1]) with r = R(phi_t) u_t; then the chain rule
+    through alpha = exp(Delta A), beta = (1 - lambda) Delta alpha, gamma = lambda Delta, phi = Delta omega."""
+    x, B, C, dt, A, lam, om = (f64(inp[k]) for k in INPUTS)
+    dy = f64(dy)
+    Bt, T, H, R, P = x.shape
+    N = B.shape[-1]
+    out = {k: np.zeros_like(f64(inp[k])) for k in INPUTS}
+
+    def rot(phi, u, sign=1.0):
+        c, s = np.cos(phi)[:, None], sign * np.sin(phi)[:, None]
+        o = np.empty_like(u)
+        o[0::2] = c * u[0::2] - s * u[1::2]
+        o[1::2] = s * u[0::2] + c * u[1::2]
+        return o
+
+    for b in range(Bt):
+        for h in range(H):
+            V = [B[b, t, h].T @ x[b, t, h] for t in range(T)]       # v_t, N x P
+            hs, st = [], np.zeros((N, P))
+            for t in range(T):                                      # the forward states
+                al = np.exp(dt[b, t, h] * A[h])
+                be = (1.0 - lam[b, t, h]) * dt[b, t, h] * al
+                u = al * st + (be * V[t - 1] if t > 0 else 0.0)
+                st = rot(dt[b, t, h] * om[b, t, h], u) + lam[b, t, h] * dt[b, t, h] * V[t]
+                hs.append(st)
+            ub = np.zeros((N, P))
+            al_n = be_n = 0.0
+            for t in range(T - 1, -1, -1):
+                d, l = dt[b, t, h], lam[b, t, h]
+                al = np.exp(d * A[h])
+                be, ga, phi = (1.0 - l) * d * al, l * d, d * om[b, t, h]
+                g = C[b, t, h].T @ dy[b, t, h] + al_n * ub
+                if t == T - 1 and d_final is not None:
+                    g = g + f64(d_final)[b, h]
+                dv = ga * g + be_n * ub
+                r = hs[t] - ga * V[t]
+                dphi = (g[1::2] * r[0::2] - g[0::2] * r[1::2]).sum(axis=1)
+                un = rot(phi, g, sign=-1.0)
+                hp = hs[t - 1] if t > 0 else np.zeros((N, P))
+                vp = V[t - 1] if t > 0 else np.zeros((N, P))
+                da, db, dg = float(np.sum(un * hp)), float(np.sum(un * vp)), float(np.sum(g * V[t]))
+                out["C"][b, t, h] = (hs[t] @ dy[b, t, h].T).T
+                out["B"][b, t, h] = (dv @ x[b, t, h].T).T
+                out["x"][b, t, h] = B[b, t, h] @ dv
+                out["omega"][b, t, h] = d * dphi
+                dal = da + db * (1.0 - l) * d
+                out["dt"][b, t, h] = dal * A[h] * al + db * (1.0 - l) * al + dg * l + float(np.sum(om[b, t, h] * dphi))
+                out["lam"][b, t, h] = -d * al * db + d * dg
+                out["A"][h] += dal * d * al
+                ub, al_n, be_n = un, al, be
+    return out

@@ -216,3 +216,18 @@ def test_bc_normalisation_is_scale_invariant():
     g = grad.grad_fd(pi, _dy(pi, seed=31), prep=True, keys=("B", "C"))
     for V in ("B", "C"):
         assert np.max(np.abs(np.sum(g[V] * pi[V], axis=-1))) < 1e-7
+
+
+@pytest.mark.parametrize("T,P,N,R,seed", [(9, 3, 4, 2, 41), (7, 4, 6, 1, 42), (5, 2, 8, 3, 43)])
+@pytest.mark.parametrize("with_final", [False, True])
+def test_adjoint_equals_finite_differences(T, P, N, R, seed, with_final):
+    """The step-by-step adjoint and the central differences of the recurrence agree to rounding."""
+    w = synth.Workload("g", 1, 2, T, P, N, R, 8, "fp32")
+    d = synth.make_inputs(w, seed=seed)
+    inp = {k: oracle.f64(d[k]) for k in grad.INPUTS}
+    dy = _dy(inp, seed=seed + 1)
+    dfin = np.random.default_rng(seed + 2).standard_normal((1, 2, N, P)) if with_final else None
+    a = grad.adjoint(inp, dy, dfin)
+    g = grad.grad_fd(inp, dy, dfin)
+    for k in grad.INPUTS:
+        assert np.max(np.abs(a[k] - g[k])) < 1e-6 * max(1.0, np.max(np.abs(g[k]))), k
