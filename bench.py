@@ -14,9 +14,16 @@ e2e         the same through the C ABI with pinned HOST buffers: host-to-device
 roofline    algorithmic bytes of one m3_scan_fwd call / its event-timed
             duration, against the measured HBM copy bandwidth.
 decode      the decode sweep (batch 1/8/64/256 x R 1/4, H=64, P=64, N=128):
-            1024 carried m3_decode_step calls each, steps/s and HBM roofline.
+            1024 carried m3_decode_step calls each, steps/s and HBM roofline,
+            and the float64 oracle's decode steps on the host cores.
 cpu_baseline  the float64 oracle on a bounded sample of the same workload,
             on this host's cores.
+workloads   the other prefill workloads, each with the same keys (value,
+            roofline with ncu traffic, cpu_baseline): the tiny fp32 check
+            (batch 1, 2 heads, T=256, P=N=16), MIMO prefill (batch 2, 32 heads,
+            T=8192, P=N=64, R=4) and long-context MIMO prefill (batch 1, 64
+            heads, T=65536, P=64, N=128, R=4, chunk 128) followed by 256 decode
+            steps from its final state.
 
 Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference];
 for N > 1 under torch.distributed.run, one rank per GPU, each rank an
@@ -39,6 +46,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from state_space_sequence_04_b300 import synth  # noqa: E402
@@ -257,6 +265,47 @@ def _time_calls(call, stream, steps, warmup, dist, device):
     total_ms = start.elapsed_time(end)
     per = [a.elapsed_time(b) for a, b in ev]
     return max_over_ranks(dist, total_ms, device) / 1e3, per
+
+
+def prefill_leg(binding, w, d, args, stream, dist, device, local, pk, ws, rank, steps=None, cpu=True):
+    """One prefill workload, device resident: Mtok/s, the roofline of the call (algorithmic bytes over
+    its event-timed duration; DRAM traffic per launch of the dominant kernel from the committed ncu
+    summary while the kernel source is unchanged), launches, clocks and the oracle on the host cores.
+    Returns (entry, (y, final_state))."""
+    steps = steps or args.steps
+    path, launches = binding.m3_scan_fwd_plan(w.batch, w.seqlen, w.heads, w.headdim, w.dstate, w.rank, w.chunk,
+                                              binding.io_code(d["x"].dtype))
+    with ClockSampler(local) as clk:
+        sec, per_ms, out = time_prefill(binding, w, d, stream, steps, args.warmup, dist, device)
+    tokens = w.batch * w.seqlen * ws
+    avg_call_ms = sum(per_ms) / len(per_ms)
+    nbytes = prefill_bytes(w)
+    achieved = nbytes / (avg_call_ms * 1e-3) / 1e9
+    tflops = prefill_tc_flops(w) / (avg_call_ms * 1e-3) / 1e12
+    src = "state_space_sequence_04_b300/csrc/" + ("scan_tc.cu" if path == 1 else "scan_simt.cu")
+    ent = {
+        "value": tokens * steps / sec / 1e6, "unit": "Mtok/s", "steps": steps,
+        "ms_per_step": sec / steps * 1e3,
+        "dtype": "bf16" if path == 1 else "f32",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "heads": w.heads,
+                   "headdim": w.headdim, "dstate": w.dstate, "rank": w.rank, "chunk": w.chunk, "io": w.io,
+                   "l2": (f"inputs larger than L2 ({nbytes / 1e9:.2f} GB per step), no flush" if nbytes > 126e6
+                          else f"inputs ({nbytes / 1e6:.2f} MB) fit in L2: a tiny check, not a bandwidth figure")},
+        "gpu_launches": launches * steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"],
+                     "traffic": profiled_traffic(src, f"{src.rsplit('/', 1)[1][:-3]}_{w.name}.md"),
+                     "kernel": "m3_scan_fwd (" + ("tensor-core" if path == 1 else "CUDA-core") +
+                               f" path, {launches} launches per call)",
+                     "algorithmic_bytes_per_call": nbytes, "peak_source": pk["source"],
+                     "tc_tflops": tflops, "tc_frac_of_bf16_peak": tflops / pk["bf16_tflops"]},
+    }
+    ent["clocks"] = clk.summary()
+    if cpu and rank == 0 and ws == 1:
+        v, threads, sample, el = cpu_baseline_run(w, d)
+        ent["cpu_baseline"] = {"value": v, "unit": "Mtok/s", "cores": threads, "kind": "oracle",
+                               "sample": sample, "seconds": el}
+    return ent, out
 
 
 def time_prefill(binding, w, d, stream, steps, warmup, dist, device):
@@ -481,6 +530,73 @@ def time_decode(binding, b, R, stream, device, steps=synth.DECODE_STEPS, ring=32
     return eager, graph, ok
 
 
+def decode_after_prefill(binding, w, d, y_fin, stream, device, pk, steps=256):
+    """``steps`` carried decode calls continuing the prefill (its final state and delayed-write cache),
+    per-step inputs of the workload's distributions; steps/s and the HBM roofline of a step."""
+    _, fin = y_fin
+    H, P, N, R = w.heads, w.headdim, w.dstate, w.rank
+    state = fin.clone()
+    cache = binding.cache_from_prefill(d["B"], d["x"])
+    ins = synth.make_decode_steps(w.batch, H, P, N, R, steps, io=w.io, seed=7, device=device, dt_mu=w.dt_mu,
+                                  dt_sd=w.dt_sd, lam_uniform=w.lam_uniform, A=d["A"])
+    y_t = torch.empty((w.batch, H, R, P), dtype=d["x"].dtype, device=device)
+    per = [[ins[k][i] for k in ("x", "B", "C", "dt", "lam", "omega")] for i in range(steps)]
+    torch.cuda.synchronize()
+
+    def run(lo, hi):
+        for i in range(lo, hi):
+            a = per[i]
+            st = binding.m3_decode_step(state, a[0], a[1], cache, a[2], a[3], d["A"], a[4], a[5], y_t, R, stream)
+            if st != 0:
+                raise binding.M3Error(st, "m3_decode_step")
+
+    # the 256 carried steps are captured once in a CUDA graph (as a serving loop would replay them) from a
+    # copy of the starting state and cache, then replayed from the prefill's own state and cache
+    state0, cache0 = state.clone(), cache.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run(0, steps)
+    torch.cuda.synchronize()
+    state.copy_(state0)
+    cache.copy_(cache0)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    sec = t0.elapsed_time(t1) / 1e3
+    nbytes = decode_bytes(w.batch, H, P, N, R, w.io)
+    per_step = sec / steps
+    return {"steps": steps, "unit": "steps/s", "steps_per_s": 1.0 / per_step, "us_per_step": per_step * 1e6,
+            "bytes_per_step": nbytes, "achieved_gbs": nbytes / per_step / 1e9, "launch": "CUDA graph of the steps",
+            "note": "batch 1: the 2.1 MB state stays in L2 between steps; launch-bound, not an HBM figure",
+            "finite": bool(torch.isfinite(state).all()), "gpu_launches": steps}
+
+
+def decode_cpu_baseline(b=64, R=1, target_s=10.0, max_steps=1024):
+    """The float64 oracle's decode step (OpenMP over (batch, head)) at batch b, rank R, H=64, P=64, N=128
+    on this host's cores: carried steps until ``target_s`` seconds or ``max_steps`` steps."""
+    import oracle
+    H, P, N = 64, 64, 128
+    state = synth.make_decode_state(b, H, N, P, seed=0)
+    ins = synth.make_decode_steps(b, H, P, N, R, 4, io="bf16", seed=1)
+    h = oracle.f64(state)
+    prev = np.zeros((b, H, R * (N + P)))
+    el, n = 0.0, 0
+    while el < target_s and n < max_steps:
+        i = n % 4
+        t0 = time.perf_counter()
+        _, h, prev = oracle.decode_step(h, ins["x"][i], ins["B"][i], prev, ins["C"][i], ins["dt"][i], ins["A"],
+                                        ins["lam"][i], ins["omega"][i])
+        el += time.perf_counter() - t0
+        n += 1
+    return {"value": n / el, "unit": "steps/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} carried steps at batch {b}, R={R}, 64 heads, P=64, N=128, float64", "seconds": el}
+
+
 def decode_sweep(binding, args, stream, device, pk):
     dec = {}
     ranks = synth.DECODE_RANKS if args.decode_rank is None else (args.decode_rank,)
@@ -630,6 +746,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prep", action="store_true", help="skip the pre-activation prefill measurement")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward-pass measurement")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the tiny, MIMO and long-context prefill workloads")
     ap.add_argument("--workload", default=synth.SISO_1P5B.name, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--mode", choices=["all", "decode", "bwd"], default="all",
                     help="decode: only the decode sweep (restricted by --decode-batch/--decode-rank); "
@@ -674,37 +792,21 @@ def main():
     # every rank draws its own replica of the workload (seeded by rank)
     d = synth.make_inputs(w, seed=rank, device=device)
     torch.cuda.synchronize()
+    head, _ = prefill_leg(binding, w, d, args, stream, dist, device, local, pk, ws, rank,
+                          cpu=not args.no_cpu_baseline)
+    tokens = w.batch * w.seqlen * ws                  # per step, all ranks
     path, launches = binding.m3_scan_fwd_plan(w.batch, w.seqlen, w.heads, w.headdim, w.dstate, w.rank, w.chunk,
                                               binding.io_code(d["x"].dtype))
-    with ClockSampler(local) as clk:
-        sec, per_ms, _ = time_prefill(binding, w, d, stream, args.steps, args.warmup, dist, device)
-    clocks = clk.summary()
-    tokens = w.batch * w.seqlen * ws                  # per step, all ranks
-    value = tokens * args.steps / sec / 1e6
-    avg_call_ms = sum(per_ms) / len(per_ms)
-    nbytes = prefill_bytes(w)
-    achieved_gbs = nbytes / (avg_call_ms * 1e-3) / 1e9
-    tflops = prefill_tc_flops(w) / (avg_call_ms * 1e-3) / 1e12
     line = {
-        "metric": METRIC, "value": value, "unit": "Mtok/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if path == 1 else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "heads": w.heads,
-                   "headdim": w.headdim, "dstate": w.dstate, "rank": w.rank, "chunk": w.chunk, "io": w.io,
-                   "parallelism": f"replicas x{ws} (independent (batch, head) sequences, no collective)",
-                   "l2": f"inputs larger than L2 ({nbytes / 1e9:.2f} GB per step), no flush"},
-        "gpu_launches": launches * args.steps,
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved_gbs / pk["hbm_gbs"],
-                     "traffic": (profiled_traffic("state_space_sequence_04_b300/csrc/scan_tc.cu",
-                                                  f"scan_tc_kernel_{w.name}.md") if path == 1 else None),
-                     "kernel": "m3_scan_fwd (" + ("tensor-core" if path == 1 else "CUDA-core") +
-                               f" path, {launches} launches per call)",
-                     "algorithmic_bytes_per_call": nbytes, "peak_source": pk["source"],
-                     "tc_tflops": tflops, "tc_frac_of_bf16_peak": tflops / pk["bf16_tflops"]},
-        "clocks": clocks,
+        "metric": METRIC, "value": head["value"], "unit": "Mtok/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
+        "config": dict(head["config"], parallelism=f"replicas x{ws} (independent (batch, head) sequences, "
+                                                   "no collective)"),
+        "gpu_launches": head["gpu_launches"], "roofline": head["roofline"], "clocks": head["clocks"],
     }
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
 
     if not args.no_prep:
         # the same workload through m3_scan_fwd_prep: Delta, lambda from pre-activations and one
@@ -751,11 +853,26 @@ def main():
 
     if not args.no_decode and rank == 0:
         line["decode"] = decode_sweep(binding, args, stream, device, pk)
+        if not args.no_cpu_baseline and ws == 1:
+            line["decode"]["cpu_baseline"] = decode_cpu_baseline()
 
-    if not args.no_cpu_baseline and rank == 0 and ws == 1:
-        v, threads, sample, el = cpu_baseline_run(w, d)
-        line["cpu_baseline"] = {"value": v, "unit": "Mtok/s", "cores": threads, "kind": "oracle",
-                                "sample": sample, "seconds": el}
+    if not args.no_workloads:
+        # the other prefill workloads, each a complete leg (every rank its own replica)
+        del d
+        torch.cuda.empty_cache()
+        line["workloads"] = {}
+        for wn in (synth.TINY, synth.MIMO_R4, synth.LONG_MIMO):
+            if wn.name == w.name:
+                continue
+            dn = synth.make_inputs(wn, seed=rank, device=device)
+            torch.cuda.synchronize()
+            ent, out = prefill_leg(binding, wn, dn, args, stream, dist, device, local, pk, ws, rank,
+                                   cpu=not args.no_cpu_baseline)
+            if wn is synth.LONG_MIMO and rank == 0:
+                ent["decode_after"] = decode_after_prefill(binding, wn, dn, out, stream, device, pk)
+            line["workloads"][wn.name] = ent
+            del dn, out
+            torch.cuda.empty_cache()
 
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -115,7 +115,10 @@ M3_API int m3_scan_fwd_plan(int64_t batch, int64_t seqlen, int64_t nheads, int64
  *   headdim P a multiple of 4 with 4 <= P <= 256.
  *   workspace / workspace_bytes: device scratch of at least
  *   m3_scan_fwd_workspace_size(...) bytes, 256-byte aligned; contents on
- *   entry are ignored.
+ *   entry are ignored.  On the tensor-core path (m3_scan_fwd_plan path 1)
+ *   the first int of the workspace is the call's device status once the
+ *   stream's work is done: M3_OK, or M3_ERR_TIMEOUT when a bounded wait in
+ *   the kernel gave up (y and final_state are then not valid).
  * Returns M3_OK or an error code; launches nothing on error.
  */
 M3_API int m3_scan_fwd(const void* x, const void* B, const void* C, const float* dt, const float* A,
@@ -150,6 +153,12 @@ M3_API int m3_scan_fwd(const void* x, const void* B, const void* C, const float*
  *     contents (each call clears what must start at zero).  Calls that
  *     overlap on the GPU -- on different streams or from different host
  *     threads -- race on it: serialise them.
+ *   - The tensor-core kernels record a timeout of their bounded waits in the
+ *     array's first word, which the caller cannot reach: m3_device_status
+ *     reports it (for the most recent call on the current device).
+ *   - The address is cached per device with the unique id of the context it
+ *     was looked up in, so a call after cudaDeviceReset (a new primary
+ *     context) looks it up again.
  */
 M3_API int m3_scan_fwd_noalloc(const void* x, const void* B, const void* C, const float* dt, const float* A,
                                const float* lambda, const float* omega, int R, int chunk,
@@ -233,8 +242,9 @@ typedef struct m3_prep_params {
  * Delta, lambda and the inverse RMS of every B / C row to the workspace.
  * Workspace: m3_scan_fwd_prep_workspace_size bytes (at least
  * m3_scan_fwd_workspace_size; larger on the CUDA-core path).  Errors: as
- * m3_scan_fwd, and M3_ERR_INVALID_ARG for a misaligned params pointer or
- * bc_eps < 0.
+ * m3_scan_fwd, and M3_ERR_INVALID_ARG for a misaligned pointer inside params or
+ * bc_eps < 0.  The params struct itself is read on the host: it needs only
+ * its natural alignment; the device pointers inside it must be 16-byte aligned.
  */
 M3_API size_t m3_scan_fwd_prep_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                                               int64_t dstate, int R, int chunk, int io_dtype);
@@ -332,16 +342,50 @@ M3_API int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const f
                             size_t workspace_bytes, void* stream);
 
 /*
- * Sticky device-side error word of m3_decode_step, which takes no workspace:
- * M3_OK, or M3_ERR_TIMEOUT once a bounded wait inside a decode kernel gave up
- * (the outputs of that call are then not valid).  Reading it synchronises
- * with the current device; clear != 0 resets it to M3_OK afterwards.
- * Returns the word, or M3_ERR_CUDA if it could not be read.
+ * Device-side error words of the calls that take no workspace, on the
+ * current device: M3_OK, or M3_ERR_TIMEOUT once a bounded wait inside a
+ * decode kernel (sticky across calls) or inside the most recent
+ * m3_scan_fwd_noalloc call's tensor-core kernels gave up (the outputs of that
+ * call are then not valid).  It first synchronises the current device
+ * (cudaDeviceSynchronize), so every stream's work is finished when the words
+ * are read; clear != 0 resets them to M3_OK afterwards.  Returns M3_OK,
+ * M3_ERR_TIMEOUT, or M3_ERR_CUDA if the device could not be synchronised or
+ * read.  m3_scan_fwd callers read the first int of their workspace instead.
  */
 M3_API int m3_device_status(int clear);
 
 /*
- * Inter-chunk state passing of the chunked algorithm, in place:
+ * Failure injection for tests.  The paper has no counterpart: this exercises
+ * the library's own error paths without faulting or hanging a GPU.
+ *
+ *   what = M3_TEST_LAUNCH_FAILURE: the next `count` calls of entry points
+ *          that would launch work return M3_ERR_CUDA after their argument
+ *          checks and launch nothing (a launch failure made on the host).
+ *          Calls rejected by their checks, or with nothing to launch, do not
+ *          use one up.  Returns how many were still armed before this call.
+ *   what = M3_TEST_PREFILL_TIMEOUT: the next plain m3_scan_fwd (or
+ *          m3_scan_fwd_noalloc) call that takes the tensor-core path with
+ *          N = 128, R = 1, chunk 64 runs a test instantiation of its kernel in
+ *          which every CTA's consumer warps, at their local chunk `count`, wait
+ *          with a 50 us limit on an mbarrier that nothing completes.  The
+ *          bounded-wait failure path then runs for real: both warp groups give
+ *          up, the copies and MMAs in flight are drained (each with the
+ *          normal 2 s limit), TMEM is freed and M3_ERR_TIMEOUT is written to the
+ *          status word (the workspace's first int; m3_device_status for the
+ *          noalloc entry).  That call's y and final_state are not valid; the
+ *          next call is normal.  Returns the chunk previously armed, or -1.
+ *   what = 0: disarm both; returns 0.
+ * Returns M3_ERR_INVALID_ARG for another `what` or a negative count.
+ */
+#define M3_TEST_LAUNCH_FAILURE 1
+#define M3_TEST_PREFILL_TIMEOUT 2
+M3_API int m3_test_inject(int what, int count);
+
+/*
+ * Inter-chunk state passing of the chunked algorithm (the chunked parallel
+ * form of "Mamba-3: Improved Sequence Modeling using State Space Principles",
+ * section 3.3, applied to the recurrence of Proposition 1 / Eq. 6 with the
+ * rotary form of Propositions 3-4), in place:
  *
  *   H_c = exp(l_c) R(Theta_c) H_{c-1} + U_c,   c = 0 .. nchunks-1,
  *

@@ -29,6 +29,8 @@ M3_ERR_CUDA = -4
 M3_ERR_TIMEOUT = -5
 M3_DTYPE_BF16 = 0
 M3_DTYPE_F32 = 1
+M3_TEST_LAUNCH_FAILURE = 1
+M3_TEST_PREFILL_TIMEOUT = 2
 
 class PrepParams(ctypes.Structure):
     """m3_prep_params: pre-SSM options of the _prep entry points (device pointers or NULL)."""
@@ -53,6 +55,7 @@ SIGNATURES = {
     "m3_decode_step": ([_fp, _vp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp,
                         _i64, _i64, _i64, _i64, _int, _int, _vp], _int),
     "m3_device_status": ([_int], _int),
+    "m3_test_inject": ([_int, _int], _int),
     "m3_scan_bwd_workspace_size": ([_i64, _i64, _i64, _i64, _i64, _int, _int], _sz),
     "m3_scan_bwd": ([_vp, _vp, _vp, _fp, _fp, _fp, _fp, _int, _vp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp,
                      _i64, _i64, _i64, _i64, _i64, _int, _vp, _sz, _vp], _int),
@@ -306,8 +309,14 @@ def scan_bwd_prep(x, B, C, dt_raw, A, u, omega, R: int, dy, d_final=None, dt_bia
 
 
 def m3_device_status(clear: bool = False) -> int:
-    """Sticky device-side error word of the decode kernels (M3_OK or M3_ERR_TIMEOUT)."""
+    """Device-side error words of the calls without a workspace (the decode kernels, sticky; the most
+    recent m3_scan_fwd_noalloc call): M3_OK or M3_ERR_TIMEOUT.  Synchronises the current device."""
     return int(load().m3_device_status(1 if clear else 0))
+
+
+def m3_test_inject(what: int, count: int) -> int:
+    """Arm a test failure (M3_TEST_LAUNCH_FAILURE, M3_TEST_PREFILL_TIMEOUT; 0 disarms)."""
+    return int(load().m3_test_inject(int(what), int(count)))
 
 
 def m3_state_passing(chunk_states, chunk_logdecay, chunk_angle, init_state, final_state, stream=None) -> int:

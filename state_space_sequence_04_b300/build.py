@@ -1,6 +1,7 @@
 """Build libm3.so (the CUDA library behind include/m3.h) in-tree for sm_103a."""
 from __future__ import annotations
 
+import concurrent.futures
 import glob
 import os
 import subprocess
@@ -34,15 +35,20 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     objdir = os.path.join(PKG, "_build")
     os.makedirs(objdir, exist_ok=True)
-    objs = []
+    cmds, objs = [], []
     for src in sources():
         obj = os.path.join(objdir, os.path.basename(src) + ".o")
         cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
             print(" ".join(cmd), file=sys.stderr)
-        subprocess.check_call(cmd)
+        cmds.append(cmd)
         objs.append(obj)
+    # translation units compile independently: one nvcc per source, in parallel
+    jobs = max(1, min(len(cmds), os.cpu_count() or 1))
+    with concurrent.futures.ThreadPoolExecutor(jobs) as ex:
+        for f in [ex.submit(subprocess.check_call, c) for c in cmds]:
+            f.result()
     tmp = LIB + f".tmp{os.getpid()}"
     subprocess.check_call([NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"])
     os.replace(tmp, LIB)

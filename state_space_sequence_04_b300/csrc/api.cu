@@ -3,6 +3,8 @@
 // an m3_status; nothing is launched when a check fails.
 #include <stdint.h>
 
+#include <atomic>
+
 #include "m3_common.cuh"
 
 namespace m3 {
@@ -25,6 +27,19 @@ bool ok_nullable(const void* p) { return p == nullptr || aligned16(p); }
 bool ok_io(int io) { return io == M3_DTYPE_BF16 || io == M3_DTYPE_F32; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? M3_OK : M3_ERR_CUDA; }
+
+// Failure injection of m3_test_inject: launch failures made on the host (the next n launching calls
+// return M3_ERR_CUDA after their checks), and the tensor-core prefill's simulated timeout.
+std::atomic<int> g_inject_launch{0};
+std::atomic<int> g_inject_timeout{0};   // k + 1: give up at local chunk k; 0 = off
+
+// True (and one armed failure used up) when this launching call is to fail.
+bool injected_launch_failure() {
+    int v = g_inject_launch.load();
+    while (v > 0)
+        if (g_inject_launch.compare_exchange_weak(v, v - 1)) return true;
+    return false;
+}
 
 // Which prefill implementation runs for these sizes: 1 = tensor cores, 0 = CUDA cores.
 int pick_path(const m3::ScanDims& d) { return (d.io == M3_DTYPE_BF16 && m3::tc_supported(d)) ? 1 : 0; }
@@ -87,8 +102,12 @@ int scan_impl(const void* x, const void* B, const void* C, const float* dt, cons
         return M3_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (batch == 0) return M3_OK;
-    if (pick_path(d) == 1)
-        return cuda_status(m3::launch_scan_tc(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, prep, s));
+    if (injected_launch_failure()) return M3_ERR_CUDA;
+    if (pick_path(d) == 1) {
+        m3::Prep p = prep;
+        if (!prep.on && d.dstate == 128 && d.R == 1 && d.chunk == 64) p.test_timeout_at = g_inject_timeout.exchange(0);
+        return cuda_status(m3::launch_scan_tc(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, p, s));
+    }
     return cuda_status(m3::launch_scan_simt(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, prep, s));
 }
 
@@ -106,6 +125,7 @@ int decode_impl(float* state, const void* x_t, const void* B_t, void* B_prev_x_p
     if (!ok_ptr(state) || !ok_ptr(x_t) || !ok_ptr(B_t) || !ok_ptr(B_prev_x_prev) || !ok_ptr(C_t) || !ok_ptr(dt_t) ||
         !ok_ptr(lambda_t) || !ok_ptr(omega_t) || !ok_ptr(y_t) || !ok_ptr(A))
         return M3_ERR_INVALID_ARG;
+    if (injected_launch_failure()) return M3_ERR_CUDA;
     return cuda_status(m3::launch_decode(state, x_t, B_t, B_prev_x_prev, C_t, dt_t, A, lambda_t, omega_t, y_t, batch,
                                          nheads, headdim, dstate, R, io_dtype, prep,
                                          static_cast<cudaStream_t>(stream)));
@@ -151,6 +171,19 @@ const char* m3_status_string(int status) {
 }
 
 int m3_version(void) { return 100; }
+
+int m3_test_inject(int what, int count) {
+    if (count < 0) return M3_ERR_INVALID_ARG;
+    switch (what) {
+        case 0: g_inject_launch.store(0); g_inject_timeout.store(0); return 0;
+        case M3_TEST_LAUNCH_FAILURE: return g_inject_launch.exchange(count);
+        case M3_TEST_PREFILL_TIMEOUT: {
+            const int prev = g_inject_timeout.exchange(count + 1);
+            return prev > 0 ? prev - 1 : -1;
+        }
+        default: return M3_ERR_INVALID_ARG;
+    }
+}
 
 size_t m3_scan_fwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
                                   int R, int chunk, int io_dtype) {
@@ -215,7 +248,15 @@ int m3_decode_step_prep(float* state, const void* x_t, const void* B_t, void* B_
                        dstate, R, io_dtype, stream, prep);
 }
 
-int m3_device_status(int clear) { return m3::decode_device_status(clear); }
+int m3_device_status(int clear) {
+    // the words are written by kernels on the caller's streams, which may be non-blocking
+    if (cudaDeviceSynchronize() != cudaSuccess) return M3_ERR_CUDA;
+    const int dec = m3::decode_device_status(clear);
+    if (dec == M3_ERR_CUDA) return dec;
+    const int na = m3::noalloc_device_status(clear);
+    if (na == M3_ERR_CUDA || na == M3_ERR_UNSUPPORTED) return na;
+    return dec != M3_OK ? dec : na;
+}
 
 size_t m3_scan_bwd_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
                                   int R, int io_dtype) {
@@ -244,6 +285,7 @@ int m3_scan_bwd(const void* x, const void* B, const void* C, const float* dt, co
         if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return M3_ERR_WORKSPACE;
     }
+    if (batch > 0 && injected_launch_failure()) return M3_ERR_CUDA;
     return cuda_status(m3::launch_scan_bwd(d, x, B, C, dt, A, lambda, omega, dy, d_final, dx, dB, dC, ddt, dA,
                                            dlambda, domega, workspace, static_cast<cudaStream_t>(stream)));
 }
@@ -265,7 +307,6 @@ int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const float* d
     if (!ok_io(io_dtype)) return M3_ERR_INVALID_ARG;
     if (batch < 0 || seqlen < 0 || nheads < 1 || headdim < 1 || dstate < 2 || dstate % 2 || R < 1)
         return M3_ERR_INVALID_ARG;
-    if (params != nullptr && !aligned16(params)) return M3_ERR_INVALID_ARG;
     const float* dt_bias = params != nullptr ? params->dt_bias : nullptr;
     const void* z = params != nullptr ? params->z : nullptr;
     if (!ok_nullable(dt_bias) || !ok_nullable(ddt_bias) || !ok_nullable(d_final) || !ok_nullable(z))
@@ -293,6 +334,7 @@ int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const float* d
         if (workspace == nullptr || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return M3_ERR_WORKSPACE;
     }
+    if (batch > 0 && injected_launch_failure()) return M3_ERR_CUDA;
     char* ws = static_cast<char*>(workspace);
     void* y_pre = nullptr;
     if (z != nullptr && any_tokens) {   // the ungated forward output, by the forward entry itself
@@ -320,6 +362,7 @@ int m3_state_passing(float* chunk_states, const float* chunk_logdecay, const flo
         if (!ok_ptr(chunk_states) || !ok_ptr(chunk_logdecay) || !ok_ptr(chunk_angle)) return M3_ERR_INVALID_ARG;
     }
     if (batch == 0) return M3_OK;
+    if (injected_launch_failure()) return M3_ERR_CUDA;
     return cuda_status(m3::launch_state_passing(chunk_states, chunk_logdecay, chunk_angle, init_state, final_state,
                                                 batch, nheads, nchunks, dstate, headdim,
                                                 static_cast<cudaStream_t>(stream)));

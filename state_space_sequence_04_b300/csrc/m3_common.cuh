@@ -67,6 +67,9 @@ struct Prep {
     const float* B_bias;
     const float* C_bias;
     const void* z;   // output gate input (y's layout, io dtype): y <- y * silu(z); null = off
+    // failure-path test (m3_test_inject): k + 1 makes the tensor-core prefill's consumer groups give up at
+    // their local chunk k (plain mode, the one shape that has the test kernel); 0 = off
+    int test_timeout_at;
     __host__ __device__ bool bc() const { return on && (bc_norm || B_bias != nullptr || C_bias != nullptr); }
 };
 
@@ -85,6 +88,8 @@ cudaError_t launch_decode(float* state, const void* x_t, const void* B_t, void* 
                           int io, const Prep& prep, cudaStream_t stream);
 bool decode_supported(int64_t headdim, int64_t dstate, int R);
 int decode_device_status(int clear);
+// the status word of the last m3_scan_fwd_noalloc call on the current device (M3_OK when it has none)
+int noalloc_device_status(int clear);
 
 cudaError_t launch_state_passing(float* chunk_states, const float* chunk_logdecay, const float* chunk_angle,
                                  const float* init_state, float* final_state, int64_t batch, int64_t nheads,

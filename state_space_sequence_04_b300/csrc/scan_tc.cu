@@ -150,7 +150,7 @@ struct TcArgs {
 // parameter block stays as it is): per-channel gains [N] (null = 1), channel
 // biases [H, R, N] (null = 0), RMS normalisation on / off and its eps, the gate
 // input z (y's layout, bf16).
-template <bool ON>
+template <int PM>
 struct ExtArgs {
     const float* B_gain;
     const float* C_gain;
@@ -161,7 +161,14 @@ struct ExtArgs {
     const __nv_bfloat16* z;
 };
 template <>
-struct ExtArgs<false> {};
+struct ExtArgs<0> {};
+// The failure-path test mode (kTestHook): every CTA's consumer group gives up at its local chunk
+// fail_chunk by waiting, with a short limit, on a barrier that nothing completes.
+constexpr int kTestHook = 8;
+template <>
+struct ExtArgs<kTestHook> {
+    int fail_chunk;
+};
 
 // Word i (two bf16) of a run of 16-byte pieces.
 __device__ __forceinline__ uint32_t word_at(const uint4* a, int i) {
@@ -180,6 +187,7 @@ struct Ctl {
     uint64_t coef_free[2];   // consumer done reading the stage's coefficient block (count 128)
     uint64_t b1;             // MMA batch 1 (chunk state onto H, scores S) complete
     uint64_t b2;             // MMA batch 2 (inter readout Yi, output Y) complete
+    uint64_t never;          // completed by nothing: the failure-path test mode waits on it
     uint32_t tmem;
     int fail_c, fail_r;      // per-group failure flags
     // copies / MMA batches issued and waited for, modulo 2^16 (only their difference,
@@ -201,13 +209,13 @@ __device__ __forceinline__ void group_bar(int id) { asm volatile("bar.sync %0, 1
 // Bounded wait on an mbarrier phase.  Gives up (setting *mine) on timeout or
 // when either group has already failed.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* mine,
-                                             volatile int* other) {
+                                             volatile int* other, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
-            if (*mine || *other || globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (*mine || *other || globaltimer_ns() - t0 > limit_ns) {
                 *mine = 1;
                 return false;
             }
@@ -337,16 +345,18 @@ __device__ __forceinline__ void mask_block(float* v, int cb, int t, float ct, fl
 // pre-activations (Delta = softplus(dt + dt_bias[h]), lambda = sigmoid(u), applied
 // to the staged boxes in shared memory) and A holds one decay generator per
 // token.  PM & 2 adds the B / C normalisation and channel biases, fused with the
-// rotation; PM & 4 the output gate y * silu(z) in the epilogue.
+// rotation; PM & 4 the output gate y * silu(z) in the epilogue.  PM == kTestHook
+// is the plain kernel with a simulated timeout (the failure-path test).
 template <int NS, int R, int Q, bool FULL, int PM>
 __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                          const __grid_constant__ CUtensorMap tm_B,
                                                          const __grid_constant__ CUtensorMap tm_C,
                                                          const __grid_constant__ CUtensorMap tm_dt,
                                                          const __grid_constant__ CUtensorMap tm_lam, TcArgs args,
-                                                         const ExtArgs<PM != 0> ext) {
+                                                         const ExtArgs<PM> ext) {
     using K = Cfg<NS, R, Q>;
-    constexpr bool PREP = (PM & 1) != 0, BC = (PM & 2) != 0, GATE = (PM & 4) != 0;
+    constexpr bool HOOK = PM == kTestHook;
+    constexpr bool PREP = !HOOK && (PM & 1) != 0, BC = !HOOK && (PM & 2) != 0, GATE = !HOOK && (PM & 4) != 0;
     constexpr int P = K::P, QR = K::QR, NP2 = NS / 2, NG = K::NG, TG = K::TG, TPG = K::TPG;
     constexpr int TX_CB = FULL ? 2 * K::BC_BYTES : K::BC_BYTES;
     extern __shared__ uint8_t smem_raw[];
@@ -401,6 +411,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         }
         mbar_init(&ctl->b1, 1);
         mbar_init(&ctl->b2, 1);
+        mbar_init(&ctl->never, 1);
         ctl->fail_c = 0;
         ctl->fail_r = 0;
         ctl->b1_issued = ctl->b2_issued = ctl->b1_waited = ctl->b2_waited = 0;
@@ -525,6 +536,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             // ---- batch 1 once the rotate group has finished this stage:
             //      H += B'^T X^ (the chunk state onto the carry), then S = C~ B'^T
             (void)wait_bounded(&ctl->rot_done[s], (i >> 1) & 1, fail_c, fail_r);
+            if constexpr (HOOK) {
+                if (FULL && i == ext.fail_chunk) (void)wait_bounded(&ctl->never, 0, fail_c, fail_r, 50000ull);
+            }
             tc_fence_before();
             group_bar(1);
             if (*fail_c) break;
@@ -557,7 +571,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 mma_commit(&ctl->b1);
                 ctl->b1_issued += 1;
             }
-            (void)wait_bounded(&ctl->b1, i & 1, fail_c, fail_r);
+            // a completed wait is counted (for the drain on failure) only by the thread that counts
+            const bool done_b1 = wait_bounded(&ctl->b1, i & 1, fail_c, fail_r);
+            bool done_b2 = false;
             tc_fence_after();
 
             float ecum_t = 0.f;
@@ -631,7 +647,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     ctl->b2_issued += 1;
                 }
                 // ---- output rows (t, r) once batch 2 is done; C, B, X of chunk i+2 may then come in
-                (void)wait_bounded(&ctl->b2, i & 1, fail_c, fail_r);
+                done_b2 = wait_bounded(&ctl->b2, i & 1, fail_c, fail_r);
                 tc_fence_after();
                 if (tid == 0 && i + 2 < nl && !*fail_c) {
                     load_cb(i + 2, s);
@@ -753,8 +769,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             tc_fence_before();
             group_bar(1);
             if (tid == 0) {
-                ctl->b1_waited += 1;
-                if (FULL) ctl->b2_waited += 1;
+                if (done_b1) ctl->b1_waited += 1;
+                if (FULL && done_b2) ctl->b2_waited += 1;
             }
             if (*fail_c) break;
         }
@@ -819,10 +835,10 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         }
         for (int i = 0; i < nl; ++i) {
             const int c = c_begin + i, s = i & 1;
-            (void)wait_bounded(&ctl->fbox[s], (i >> 1) & 1, fail_r, fail_c);
+            const bool got_box = wait_bounded(&ctl->fbox[s], (i >> 1) & 1, fail_r, fail_c);
             group_bar(2);
+            if (rt == 0 && got_box) ctl->box_waited[s] += 1;
             if (*fail_r) break;
-            if (rt == 0) ctl->box_waited[s] += 1;
             float a_t = a;
             if constexpr (PREP) {
                 // Delta and lambda of this head's Q+1 staged tokens, in place (0 past the end)
@@ -905,8 +921,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             //      are issued only after batch 1 of chunk i, so waiting for them here keeps
             //      this group at most one chunk ahead of the consumer: every barrier the
             //      consumer waits on is then at most one phase ahead.
-            (void)wait_bounded(&ctl->fcb[s], (i >> 1) & 1, fail_r, fail_c);
-            if (rt == 0) ctl->cb_waited[s] += 1;
+            const bool got_cb = wait_bounded(&ctl->fcb[s], (i >> 1) & 1, fail_r, fail_c);
+            if (rt == 0 && got_cb) ctl->cb_waited[s] += 1;
             // the consumer may use this chunk's coefficients (exp(cum_end), f) now
             mbar_arrive(&ctl->coef_ready[s]);
             {
@@ -1004,8 +1020,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             //      chunk's last reader of that buffer is done (batch 2, or batch 1 in the
             //      state pass) and X has landed
             if (i > 0) (void)wait_bounded(FULL ? &ctl->b2 : &ctl->b1, (i - 1) & 1, fail_r, fail_c);
-            if (wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_r, fail_c)) make_xhat(s);
-            if (rt == 0) ctl->x_waited[s] += 1;
+            const bool got_x = wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_r, fail_c);
+            if (got_x) make_xhat(s);
+            if (rt == 0 && got_x) ctl->x_waited[s] += 1;
 
             fence_proxy_async_smem();
             mbar_arrive(&ctl->rot_done[s]);
@@ -1150,10 +1167,12 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
     TcArgs args{};
     args.A = A;
     args.dt_bias = prep.dt_bias;
-    ExtArgs<PM != 0> ext{};
-    if constexpr (PM != 0)
-        ext = ExtArgs<true>{prep.B_gain, prep.C_gain, prep.B_bias, prep.C_bias, prep.bc_norm ? 1 : 0, prep.bc_eps,
-                            static_cast<const __nv_bfloat16*>(prep.z)};
+    ExtArgs<PM> ext{};
+    if constexpr (PM == kTestHook)
+        ext.fail_chunk = prep.test_timeout_at - 1;
+    else if constexpr (PM != 0)
+        ext = ExtArgs<PM>{prep.B_gain, prep.C_gain, prep.B_bias, prep.C_bias, prep.bc_norm ? 1 : 0, prep.bc_eps,
+                          static_cast<const __nv_bfloat16*>(prep.z)};
     args.omega = omega;
     args.y = static_cast<__nv_bfloat16*>(y);
     args.final_state = final_state;
@@ -1207,13 +1226,14 @@ struct TcImpl {
     LaunchFn launch[8];
     size_t (*workspace)(const ScanDims&);
     int (*launches)(const ScanDims&);
+    LaunchFn hook;   // the plain kernel with the failure-path test's simulated timeout (one shape only)
 };
 
 template <int NS, int R, int Q>
 TcImpl impl() {
     return TcImpl{{launch_cfg<NS, R, Q, 0>, launch_cfg<NS, R, Q, 1>, nullptr, launch_cfg<NS, R, Q, 3>, nullptr,
                    launch_cfg<NS, R, Q, 5>, nullptr, launch_cfg<NS, R, Q, 7>},
-                  ws_cfg<NS, R, Q>, launches_cfg<NS, R, Q>};
+                  ws_cfg<NS, R, Q>, launches_cfg<NS, R, Q>, nullptr};
 }
 
 // Tile configuration for (N, R, chunk).  Chunks of chunk*R <= 128 rows run as
@@ -1226,7 +1246,10 @@ bool pick(const ScanDims& d, TcImpl* out) {
     if (d.nheads % 4) return false;
     const int N = (int)d.dstate, R = d.R, Q = d.chunk;
     TcImpl f{};
-    if (N == 128 && R == 1 && Q == 64) f = impl<128, 1, 64>();
+    if (N == 128 && R == 1 && Q == 64) {
+        f = impl<128, 1, 64>();
+        f.hook = launch_cfg<128, 1, 64, kTestHook>;
+    }
     else if (N == 128 && R == 1 && Q == 128) f = impl<128, 1, 128>();
     else if (N == 128 && R == 2 && Q == 64) f = impl<128, 2, 64>();
     else if (N == 64 && R == 1 && Q == 64) f = impl<64, 1, 64>();
@@ -1255,6 +1278,8 @@ cudaError_t launch_scan_tc(const ScanDims& d, const void* x, const void* B, cons
     TcImpl f;
     if (!pick(d, &f)) return cudaErrorNotSupported;
     const int mode = !prep.on ? 0 : 1 | (prep.bc() ? 2 : 0) | (prep.z != nullptr ? 4 : 0);
+    if (mode == 0 && prep.test_timeout_at > 0 && f.hook != nullptr)
+        return f.hook(d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, prep, stream);
     return f.launch[mode](d, x, B, C, dt, A, lambda, omega, y, final_state, workspace, prep, stream);
 }
 

@@ -56,7 +56,13 @@ def oracle_full(inp):
     return oracle.scan(*[inp[k] for k in KEYS])
 
 
+# Every comparison's achieved error, for the margin report at the end of the run (conftest.py).
+MARGINS = []
+
+
 def assert_close(got, ref, tol, what):
     err = oracle.rel_err(got, ref)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    MARGINS.append((test, what, float(err), float(tol)))
     assert err <= tol, f"{what}: max|err|/max|ref| = {err:.3e} > {tol:.0e}"
     return err
