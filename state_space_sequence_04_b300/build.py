@@ -11,6 +11,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libm3.so")
+LIB_TRACE = os.path.join(PKG, "libm3_trace.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -21,24 +22,28 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str = None) -> bool:
+    lib = lib or LIB
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every csrc/*.cu for sm_103a and link libm3.so (skipped when up to date)."""
-    if not force and not _stale():
-        return LIB
-    objdir = os.path.join(PKG, "_build")
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Compile every csrc/*.cu for sm_103a and link libm3.so (skipped when up to date).
+    trace=True builds the diagnostic libm3_trace.so instead: the same sources with -DM3_TRACE
+    (the prefill kernel records a phase trace; see trace.py)."""
+    lib = LIB_TRACE if trace else LIB
+    if not force and not _stale(lib):
+        return lib
+    objdir = os.path.join(PKG, "_build_trace" if trace else "_build")
     os.makedirs(objdir, exist_ok=True)
     cmds, objs = [], []
     for src in sources():
         obj = os.path.join(objdir, os.path.basename(src) + ".o")
-        cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        cmd = [NVCC, *ARCH, *FLAGS, *(["-DM3_TRACE"] if trace else []), "-c", src, "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
             print(" ".join(cmd), file=sys.stderr)
@@ -49,12 +54,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with concurrent.futures.ThreadPoolExecutor(jobs) as ex:
         for f in [ex.submit(subprocess.check_call, c) for c in cmds]:
             f.result()
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.check_call([NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, trace="--trace" in sys.argv))

@@ -69,6 +69,28 @@ using namespace tc;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait, then give up with M3_ERR_TIMEOUT
 constexpr float kLog2e = 1.4426950408889634f;
 
+#ifdef M3_TRACE
+// Phase trace of a diagnostic build (compiled with -DM3_TRACE; the product build has none of it):
+// clock64 at the phase boundaries of the first kTraceChunks chunks of the first kTraceCtas CTAs.
+// Per (CTA, chunk): slots 0-15 the consumer group (thread 0; slots 11-12 thread 32), 16-31 the
+// rotate group (thread 128).  g_m3_trace_clk holds (globaltimer, clock64) at the start and the end
+// of each traced CTA, to turn cycles into time.
+constexpr int kTraceCtas = 4, kTraceChunks = 64, kTraceSlots = 32;
+__device__ long long g_m3_trace[kTraceCtas * kTraceChunks * kTraceSlots];
+__device__ long long g_m3_trace_clk[kTraceCtas * 4];
+#define M3_TRACE_BY(thread, i, slot)                                                                    \
+    do {                                                                                                \
+        if (blockIdx.x < kTraceCtas && (i) < kTraceChunks && threadIdx.x == (thread))                   \
+            g_m3_trace[((int)blockIdx.x * kTraceChunks + (i)) * kTraceSlots + (slot)] = clock64();     \
+    } while (0)
+#else
+#define M3_TRACE_BY(thread, i, slot) \
+    do {                             \
+    } while (0)
+#endif
+#define M3_TRACE_C(i, slot) M3_TRACE_BY(0, i, slot)
+#define M3_TRACE_R(i, slot) M3_TRACE_BY(128, i, 16 + (slot))
+
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 template <int NS, int R, int Q>
@@ -88,7 +110,8 @@ struct Cfg {
     static constexpr int X_BYTES = QR * 128;
     static constexpr int BC_BYTES = NPAN * QR * 128;
     static constexpr int SL_BYTES = QR * QR * 2;
-    static constexpr int XS_BYTES = X_BYTES > SL_BYTES ? X_BYTES : SL_BYTES;
+    static_assert(SL_BYTES <= BC_BYTES, "the masked scores are written over the chunk's B tile");
+    static constexpr int XS_BYTES = X_BYTES;
     static constexpr int STG_TILE = 2 * BC_BYTES + X_BYTES;      // C | B | X of one stage
     static constexpr int BOX_BYTES = 16 * (Q + 1);                // dt / lambda box {4 heads, Q+1 tokens}
     static constexpr int BOX_STRIDE = align_up(BOX_BYTES, 128);
@@ -101,12 +124,13 @@ struct Cfg {
     // the partial sums go over the stage's two boxes once their values are in registers
     static constexpr bool PART_IN_BOX = PART_BYTES <= 2 * BOX_STRIDE;
     // coefficient block of a stage (floats): cum*log2e[Q], rho[Q], exp(cum)[Q], b[Q],
-    // f = exp(cum_end - cum)[Q], Theta[NS/2], exp(cum_end), cum_end
+    // f = exp(cum_end - cum)[Q], Theta[NS/2] (the phase of each pair at the chunk's last token since
+    // the segment start, mod 2 pi), exp(cum_end), cum_end
     static constexpr int CO_CUM2 = 0, CO_RHO = Q, CO_ECUM = 2 * Q, CO_BNEG = 3 * Q, CO_F = 4 * Q, CO_THETA = 5 * Q,
                          CO_EEND = 5 * Q + NS / 2, CO_CEND = 5 * Q + NS / 2 + 1;
     static constexpr int CO_BYTES = align_up((5 * Q + NS / 2 + 2) * 4, 16);
 
-    static constexpr int OFF_XS = 2 * STG_TILE;                   // X^, then SL
+    static constexpr int OFF_XS = 2 * STG_TILE;                   // X^
     static constexpr int OFF_HB = OFF_XS + XS_BYTES;
     static constexpr int OFF_BOX = OFF_HB + NS * 128;             // [stage][dt | lambda]
     static constexpr int OFF_PART = OFF_BOX + 4 * BOX_STRIDE;     // only when not in the boxes
@@ -182,18 +206,20 @@ __device__ __forceinline__ uint32_t word_at(const uint4* a, int i) {
 // batch 2).
 struct Ctl {
     uint64_t fbox[2], fcb[2], fx[2];   // TMA groups landed
-    uint64_t rot_done[2];    // rotate group finished the stage (count 128)
+    uint64_t bc_done[2];     // rotate group rotated the stage's C and B (count 128)
+    uint64_t rot_done[2];    // rotate group finished the stage, X^ included (count 128)
     uint64_t coef_ready[2];  // coefficient block of the stage written (count 128)
     uint64_t coef_free[2];   // consumer done reading the stage's coefficient block (count 128)
-    uint64_t b1;             // MMA batch 1 (chunk state onto H, scores S) complete
-    uint64_t b2;             // MMA batch 2 (inter readout Yi, output Y) complete
+    uint64_t bS;             // scores S of a chunk complete (one commit per chunk, in chunk order)
+    uint64_t bH;             // chunk state onto the carry H complete (one per chunk)
+    uint64_t bY;             // output Y (and the inter readout Yi issued before it) complete (one per chunk)
     uint64_t never;          // completed by nothing: the failure-path test mode waits on it
+    uint64_t drain;          // on failure: one commit covering every MMA issued, waited before TMEM is freed
     uint32_t tmem;
     int fail_c, fail_r;      // per-group failure flags
-    // copies / MMA batches issued and waited for, modulo 2^16 (only their difference,
-    // at most 2, and their parity matter: they drive the bounded drain on failure)
+    // copies issued and waited for, modulo 2^16 (only their difference, at most 2, and
+    // their parity matter: they drive the bounded drain on failure)
     uint16_t box_issued[2], box_waited[2], cb_issued[2], cb_waited[2], x_issued[2], x_waited[2];
-    uint16_t b1_issued, b2_issued, b1_waited, b2_waited;
 };
 static_assert(sizeof(Ctl) <= 192, "control block must fit its reserved space");
 
@@ -221,6 +247,17 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
             }
         }
     }
+}
+
+// An angle reduced modulo 2 pi to [-pi, pi]: x - k 2pi with k = rint(x / 2pi), the product k 2pi
+// taken in two parts (2pi = 6.28125 + 1.9353071795864769e-3; the first part has few enough bits
+// that k times it is exact for |k| < 2^15), after Cody and Waite's argument reduction.
+__device__ __forceinline__ float reduce_2pi(float x) {
+    const float k = rintf(x * 0.15915494309189535f);
+    return fmaf(-k, 1.9353071795864769e-3f, fmaf(-k, 6.28125f, x));
+}
+__device__ __forceinline__ float4 reduce_2pi(float4 v) {
+    return make_float4(reduce_2pi(v.x), reduce_2pi(v.y), reduce_2pi(v.z), reduce_2pi(v.w));
 }
 
 // Rotate the 4 pairs of one 16-byte piece by (c[k], s[k]) (angle -Psi), optionally
@@ -364,6 +401,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
     Ctl* ctl = reinterpret_cast<Ctl*>(sm + K::OFF_BAR);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+#ifdef M3_TRACE
+    if (tid == 0 && blockIdx.x < kTraceCtas) {
+        g_m3_trace_clk[blockIdx.x * 4 + 0] = (long long)globaltimer_ns();
+        g_m3_trace_clk[blockIdx.x * 4 + 1] = clock64();
+    }
+#endif
     const int bh = blockIdx.x / args.nseg, seg = blockIdx.x % args.nseg;
     const int b = bh / args.H, h = bh % args.H, hq = h & 3;
     const int T = args.T;
@@ -380,20 +423,31 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
     uint8_t* hb = sm + K::OFF_HB;
     // X^ = exp(cum_end - cum_s) X of the chunk in stage s, into the X^ / SL buffer (consumer threads)
     auto make_xhat = [&](int s) {   // rotate threads
+        // QR rows x 8 16-byte pieces, NPC per thread.  Every load goes first: the compiler cannot
+        // tell a store to X^ from a later load of X, and would otherwise serialise them
+        constexpr int NPC = QR * 8 / 128;
         const uint8_t* tX = tile_x(s);
         const float* f = coef(s) + K::CO_F;
-        for (int pidx = threadIdx.x - 128; pidx < QR * 8; pidx += 128) {   // QR rows x 8 16-byte pieces
-            const int row = pidx >> 3, piece = pidx & 7;
-            const float2 f2 = make_float2(f[row / R], f[row / R]);
-            const uint32_t off2 = sw128_offset(row, piece * 16);
-            const uint4 v = *reinterpret_cast<const uint4*>(tX + off2);
-            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const int p0 = threadIdx.x - 128;
+        uint4 v[NPC];
+        float fr[NPC];
+#pragma unroll
+        for (int k = 0; k < NPC; ++k) {
+            const int pidx = p0 + 128 * k, row = pidx >> 3;
+            v[k] = *reinterpret_cast<const uint4*>(tX + sw128_offset(row, (pidx & 7) * 16));
+            fr[k] = f[row / R];
+        }
+#pragma unroll
+        for (int k = 0; k < NPC; ++k) {
+            const int pidx = p0 + 128 * k;
+            const float2 f2 = make_float2(fr[k], fr[k]);
+            uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 g = __fmul2_rn(f2, make_float2(bf_lo(w[e]), bf_hi(w[e])));
                 w[e] = pack_bf16(g.x, g.y);
             }
-            *reinterpret_cast<uint4*>(xs + off2) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(xs + sw128_offset(pidx >> 3, (pidx & 7) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     };
 
@@ -402,6 +456,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             mbar_init(&ctl->fbox[s], 1);
             mbar_init(&ctl->fcb[s], 1);
             mbar_init(&ctl->fx[s], 1);
+            mbar_init(&ctl->bc_done[s], 128);
             mbar_init(&ctl->rot_done[s], 128);
             mbar_init(&ctl->coef_ready[s], 128);
             mbar_init(&ctl->coef_free[s], 128);
@@ -409,12 +464,13 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             ctl->cb_issued[s] = ctl->cb_waited[s] = 0;
             ctl->x_issued[s] = ctl->x_waited[s] = 0;
         }
-        mbar_init(&ctl->b1, 1);
-        mbar_init(&ctl->b2, 1);
+        mbar_init(&ctl->bS, 1);
+        mbar_init(&ctl->bH, 1);
+        mbar_init(&ctl->bY, 1);
         mbar_init(&ctl->never, 1);
+        mbar_init(&ctl->drain, 1);
         ctl->fail_c = 0;
         ctl->fail_r = 0;
-        ctl->b1_issued = ctl->b2_issued = ctl->b1_waited = ctl->b2_waited = 0;
         fence_mbar_init();
         prefetch_tensormap(&tm_x);
         prefetch_tensormap(&tm_B);
@@ -517,8 +573,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         tc_fence_before();
         group_bar(1);
         const bool odd = tid & 1;
-        float ld_sum = 0.f, th_sum = 0.f;   // state pass: summed log-decay (thread 0), angle of pair tid
-        // S = C~ B'^T of the chunk in stage s (thread 0)
+        float ld_sum = 0.f;   // state pass: summed log-decay (thread 0)
+        // S = C~ B'^T of the chunk in stage s, committed to bS (thread 0)
         auto issue_scores = [&](int s) {
             const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
             const uint64_t dB = smem_desc(smem_u32(tile_b(s)), 16, 1024, kSwizzle128B);
@@ -528,13 +584,23 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
                 mma_bf16_ss(tmem + K::T_S, dC + ko, dB + ko, id_s, kk > 0);
             }
+            mma_commit(&ctl->bS);
         };
+        // the scores of local chunk s_next are the next ones to issue (thread 0): each chunk's go
+        // out as soon as its rotation is done and the previous chunk's mask has read the S columns
+        int s_next = 0;
+        if (FULL && tid == 0 && wait_bounded(&ctl->bc_done[0], 0, fail_c, fail_r)) {
+            tc_fence_after();
+            issue_scores(0);
+            s_next = 1;
+        }
 
         for (int i = 0; i < nl; ++i) {
             const int c = c_begin + i, s = i & 1;
             const float* co = coef(s);
-            // ---- batch 1 once the rotate group has finished this stage:
-            //      H += B'^T X^ (the chunk state onto the carry), then S = C~ B'^T
+            M3_TRACE_C(i, 0);
+            // ---- once the rotate group has finished this stage (X^ included):
+            //      H += B'^T X^ (the chunk state onto the carry), then Yi = C~ Hb_{c-1}
             (void)wait_bounded(&ctl->rot_done[s], (i >> 1) & 1, fail_c, fail_r);
             if constexpr (HOOK) {
                 if (FULL && i == ext.fail_chunk) (void)wait_bounded(&ctl->never, 0, fail_c, fail_r, 50000ull);
@@ -542,6 +608,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             tc_fence_before();
             group_bar(1);
             if (*fail_c) break;
+            M3_TRACE_C(i, 1);
             // output gate: this thread's z values of the chunk, loaded now so that their latency
             // hides behind the MMAs and the mask (zero past the end of the sequence)
             constexpr int NZ = GATE && FULL ? (K::M64 ? 4 : 8) : 1;
@@ -558,6 +625,10 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             }
             if (tid == 0) {
                 tc_fence_after();
+                if (FULL && s_next == i) {   // not issued early: the rotation was not done in time
+                    issue_scores(s);
+                    s_next = i + 1;
+                }
                 // descriptors of the operand bases; a byte offset o moves the start address field by o >> 4
                 const uint64_t dBt = smem_desc(smem_u32(tile_b(s)), QR * 128, 1024, kSwizzle128B);
                 const uint64_t dX = smem_desc(smem_u32(xs), 16, 1024, kSwizzle128B);
@@ -567,18 +638,30 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
 #pragma unroll
                 for (int kk = 0; kk < QR / 16; ++kk)
                     mma_bf16_ss(tmem + K::T_H, dBt + kk * (2048 >> 4), dX + kk * (2048 >> 4), id_u, 1);
-                if (FULL) issue_scores(s);
-                mma_commit(&ctl->b1);
-                ctl->b1_issued += 1;
+                mma_commit(&ctl->bH);
+                if (FULL) {   // Yi = C~ Hb_{c-1}: tracked by the output's commit
+                    const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
+                    const uint64_t dHb = smem_desc(smem_u32(hb), 16, 1024, kSwizzle128B);
+                    constexpr uint32_t id_y = idesc_bf16_f32(K::MM, P, false, true);
+#pragma unroll
+                    for (int kk = 0; kk < NS / 16; ++kk) {
+                        const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
+                        mma_bf16_ss(tmem + K::T_YI, dC + ko, dHb + kk * (2048 >> 4), id_y, kk > 0);
+                    }
+                }
+                M3_TRACE_C(i, 2);
             }
-            // a completed wait is counted (for the drain on failure) only by the thread that counts
-            const bool done_b1 = wait_bounded(&ctl->b1, i & 1, fail_c, fail_r);
-            bool done_b2 = false;
+            if (FULL) (void)wait_bounded(&ctl->bS, i & 1, fail_c, fail_r);
+            (void)wait_bounded(&ctl->bH, i & 1, fail_c, fail_r);
+            M3_TRACE_BY(32, i, 12);
+            M3_TRACE_C(i, 3);
             tc_fence_after();
 
             float ecum_t = 0.f;
             if constexpr (FULL) {
-                // ---- mask: SL = S o L (bf16, K-major rows (t,r)) over X^ (consumed by batch 1)
+                uint8_t* sl = tile_b(s);
+                // ---- mask: SL = S o L (bf16, K-major rows (t,r)) over the chunk's B' tile, which
+                //      the scores and the chunk-state MMA have consumed
                 if constexpr (K::M64) {
                     // thread = (row, half): row 16 warp + lane % 16, columns [32 half, 32 half + 32)
                     const int row = warp * 16 + (lane & 15), half = lane >> 4, t = row / R;
@@ -592,7 +675,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
 #pragma unroll
                     for (int q8 = 0; q8 < 4; ++q8) {
                         const int col = 32 * half + q8 * 8;
-                        *reinterpret_cast<uint4*>(xs + sw128_offset(row, col * 2)) =
+                        *reinterpret_cast<uint4*>(sl + sw128_offset(row, col * 2)) =
                             make_uint4(pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]), pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]),
                                        pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
                     }
@@ -617,7 +700,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
 #pragma unroll
                         for (int q8 = 0; q8 < 4; ++q8) {
                             const int col = c32 + q8 * 8;
-                            *reinterpret_cast<uint4*>(xs + (col / 64) * QR * 128 + sw128_offset(row, (col % 64) * 2)) =
+                            *reinterpret_cast<uint4*>(sl + (col / 64) * QR * 128 + sw128_offset(row, (col % 64) * 2)) =
                                 make_uint4(pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]), pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]),
                                            pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
                         }
@@ -626,28 +709,33 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 }
                 tc_fence_before();
                 group_bar(1);
-                if (tid == 0) {   // batch 2: Yi = C~ Hb_{c-1}, Y = SL X
+                M3_TRACE_C(i, 4);
+                if (tid == 0) {   // Y = SL X, then the next chunk's scores if its rotation is done
                     tc_fence_after();
-                    const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
-                    const uint64_t dHb = smem_desc(smem_u32(hb), 16, 1024, kSwizzle128B);
-                    const uint64_t dSL = smem_desc(smem_u32(xs), 16, 1024, kSwizzle128B);
+                    const uint64_t dSL = smem_desc(smem_u32(sl), 16, 1024, kSwizzle128B);
                     const uint64_t dX = smem_desc(smem_u32(tile_x(s)), 16, 1024, kSwizzle128B);
                     constexpr uint32_t id_y = idesc_bf16_f32(K::MM, P, false, true);
-#pragma unroll
-                    for (int kk = 0; kk < NS / 16; ++kk) {
-                        const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
-                        mma_bf16_ss(tmem + K::T_YI, dC + ko, dHb + kk * (2048 >> 4), id_y, kk > 0);
-                    }
 #pragma unroll
                     for (int kk = 0; kk < QR / 16; ++kk) {
                         const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
                         mma_bf16_ss(tmem + K::T_Y, dSL + ko, dX + kk * (2048 >> 4), id_y, kk > 0);
                     }
-                    mma_commit(&ctl->b2);
-                    ctl->b2_issued += 1;
+                    mma_commit(&ctl->bY);
+                    if (i + 1 < nl && !*fail_c && mbar_test_wait(&ctl->bc_done[s ^ 1], ((i + 1) >> 1) & 1)) {
+                        tc_fence_after();
+                        issue_scores(s ^ 1);
+                        s_next = i + 2;
+                    }
+                    M3_TRACE_C(i, 5);
+#ifdef M3_TRACE
+                    if (blockIdx.x < kTraceCtas && i < kTraceChunks)
+                        g_m3_trace[((int)blockIdx.x * kTraceChunks + i) * kTraceSlots + 10] = s_next == i + 2;
+#endif
                 }
-                // ---- output rows (t, r) once batch 2 is done; C, B, X of chunk i+2 may then come in
-                done_b2 = wait_bounded(&ctl->b2, i & 1, fail_c, fail_r);
+                // ---- output rows (t, r) once Yi and Y are done; C, B, X of chunk i+2 may then come in
+                (void)wait_bounded(&ctl->bY, i & 1, fail_c, fail_r);
+                M3_TRACE_BY(32, i, 11);
+                M3_TRACE_C(i, 6);
                 tc_fence_after();
                 if (tid == 0 && i + 2 < nl && !*fail_c) {
                     load_cb(i + 2, s);
@@ -705,6 +793,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                         }
                     }
                 }
+                M3_TRACE_C(i, 7);
             } else {
                 // B' and X^ are consumed (X was consumed into X^): the next loads may come in
                 if (tid == 0 && i + 2 < nl && !*fail_c) {
@@ -712,53 +801,43 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     load_x(i + 2, s);
                 }
                 if (tid == 0) ld_sum += co[K::CO_CEND];
-                if (tid < NP2) th_sum += co[K::CO_THETA + tid];
             }
 
-            // ---- state: H <- e_{c+1} R(Theta_c) H ; Hb <- bf16(R(Theta_c) H)   (thread = state row n)
-            //      (batch 2 has read Hb_{c-1})
+            // ---- state: Hb <- bf16(H), H <- e_{c+1} H   (thread = state row n).  The carry lives in
+            //      the segment's rotating frame (B and C are rotated by the phase since the segment
+            //      start), where the transition is the scalar decay alone (Propositions 3-4); Yi has
+            //      read Hb_{c-1}
             float e_next = 1.f;
             if (i + 1 < nl) {
                 const int s1 = (i + 1) & 1;
                 (void)wait_bounded(&ctl->coef_ready[s1], ((i + 1) >> 1) & 1, fail_c, fail_r);
                 e_next = coef(s1)[K::CO_EEND];
             }
+            M3_TRACE_C(i, 8);
             tc_fence_after();
             if (tid < NS) {
-                float sn, cs;
-                sincosf(co[K::CO_THETA + (tid >> 1)], &sn, &cs);
-                // even row 2j: cos*v_2j - sin*v_2j+1 ; odd row 2j+1: sin*v_2j + cos*v_2j+1
-                const float2 c2 = make_float2(cs, cs);
-                const float2 s2 = odd ? make_float2(sn, sn) : make_float2(-sn, -sn);
                 const float2 e2 = make_float2(e_next, e_next);
 #pragma unroll
                 for (int cc = 0; cc < P; cc += 32) {
                     float hv[32];
                     tmem_ld32_sync(tlane + K::T_H + cc, hv);
-                    float nv[32];
+                    if (FULL) {
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            const uint4 pk = make_uint4(pack_bf16(hv[q8 * 8 + 0], hv[q8 * 8 + 1]),
+                                                        pack_bf16(hv[q8 * 8 + 2], hv[q8 * 8 + 3]),
+                                                        pack_bf16(hv[q8 * 8 + 4], hv[q8 * 8 + 5]),
+                                                        pack_bf16(hv[q8 * 8 + 6], hv[q8 * 8 + 7]));
+                            *reinterpret_cast<uint4*>(hb + sw128_offset(tid, (cc + q8 * 8) * 2)) = pk;
+                        }
+                    }
 #pragma unroll
                     for (int i2 = 0; i2 < 32; i2 += 2) {
-                        const float2 v = make_float2(hv[i2], hv[i2 + 1]);
-                        const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, hv[i2], 1),
-                                                     __shfl_xor_sync(0xffffffffu, hv[i2 + 1], 1));
-                        const float2 r = __ffma2_rn(c2, v, __fmul2_rn(s2, o));
-                        nv[i2] = r.x;
-                        nv[i2 + 1] = r.y;
-                        const float2 sc = __fmul2_rn(e2, r);
+                        const float2 sc = __fmul2_rn(e2, make_float2(hv[i2], hv[i2 + 1]));
                         hv[i2] = sc.x;
                         hv[i2 + 1] = sc.y;
                     }
                     tmem_st32(tlane + K::T_H + cc, hv);
-                    if (FULL) {
-#pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) {
-                            const uint4 pk = make_uint4(pack_bf16(nv[q8 * 8 + 0], nv[q8 * 8 + 1]),
-                                                        pack_bf16(nv[q8 * 8 + 2], nv[q8 * 8 + 3]),
-                                                        pack_bf16(nv[q8 * 8 + 4], nv[q8 * 8 + 5]),
-                                                        pack_bf16(nv[q8 * 8 + 6], nv[q8 * 8 + 7]));
-                            *reinterpret_cast<uint4*>(hb + sw128_offset(tid, (cc + q8 * 8) * 2)) = pk;
-                        }
-                    }
                 }
                 tmem_st_wait();
                 if (FULL) fence_proxy_async_smem();
@@ -768,13 +847,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             mbar_arrive(&ctl->coef_free[s]);
             tc_fence_before();
             group_bar(1);
-            if (tid == 0) {
-                if (done_b1) ctl->b1_waited += 1;
-                if (FULL && done_b2) ctl->b2_waited += 1;
-            }
+            M3_TRACE_C(i, 9);
             if (*fail_c) break;
         }
-        // the carry after the segment's last chunk (e_next = 1): the physical-frame state
+        // the carry after the segment's last chunk (e_next = 1), rotated from the segment's frame
+        // to the physical frame by the segment's phase Theta (the last chunk's phase, mod 2 pi)
+        const float* co_last = coef((nl - 1) & 1);
         float* dst = nullptr;
         if (FULL) {
             if (seg == args.nseg - 1) dst = args.final_state;
@@ -783,16 +861,29 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             dst = args.seg_U + ((int64_t)bh * (args.S - 1) + seg) * NS * P;
             if (!*fail_c && !*fail_r) {
                 if (tid == 0) args.seg_ld[(int64_t)bh * (args.S - 1) + seg] = ld_sum;
-                if (tid < NP2) args.seg_th[((int64_t)bh * (args.S - 1) + seg) * NP2 + tid] = th_sum;
+                if (tid < NP2) args.seg_th[((int64_t)bh * (args.S - 1) + seg) * NP2 + tid] = co_last[K::CO_THETA + tid];
             }
         }
         if (!*fail_c && !*fail_r && dst != nullptr && tid < NS) {
             tc_fence_after();
+            float sn, cs;
+            sincosf(co_last[K::CO_THETA + (tid >> 1)], &sn, &cs);
+            // even row 2j: cos*v_2j - sin*v_2j+1 ; odd row 2j+1: sin*v_2j + cos*v_2j+1
+            const float2 c2 = make_float2(cs, cs);
+            const float2 s2 = odd ? make_float2(sn, sn) : make_float2(-sn, -sn);
             float* fs = dst + (int64_t)tid * P;
 #pragma unroll
             for (int cc = 0; cc < P; cc += 32) {
                 float v[32];
                 tmem_ld32_sync(tlane + K::T_H + cc, v);
+#pragma unroll
+                for (int i2 = 0; i2 < 32; i2 += 2) {
+                    const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[i2], 1),
+                                                 __shfl_xor_sync(0xffffffffu, v[i2 + 1], 1));
+                    const float2 r = __ffma2_rn(c2, make_float2(v[i2], v[i2 + 1]), __fmul2_rn(s2, o));
+                    v[i2] = r.x;
+                    v[i2 + 1] = r.y;
+                }
 #pragma unroll
                 for (int i4 = 0; i4 < 32; i4 += 4)
                     *reinterpret_cast<float4*>(fs + cc + i4) = make_float4(v[i4], v[i4 + 1], v[i4 + 2], v[i4 + 3]);
@@ -816,6 +907,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             }
         };
         load_omega(c_begin);
+        // phase of this thread's 4 pairs at the end of the previous chunk, since the segment start (mod 2 pi)
+        float4 phi0 = make_float4(0.f, 0.f, 0.f, 0.f);
         const float a = PREP ? 0.f : args.A[h];
         // pre-activation variant: this thread's token's decay generator, one chunk ahead
         float a_nx = 0.f;
@@ -835,6 +928,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         }
         for (int i = 0; i < nl; ++i) {
             const int c = c_begin + i, s = i & 1;
+            M3_TRACE_R(i, 0);
             const bool got_box = wait_bounded(&ctl->fbox[s], (i >> 1) & 1, fail_r, fail_c);
             group_bar(2);
             if (rt == 0 && got_box) ctl->box_waited[s] += 1;
@@ -852,6 +946,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 a_t = a_nx;
                 group_bar(2);
             }
+            M3_TRACE_R(i, 1);
             const float* sDt = box_dt(s);
             const float* sLam = box_lam(s);
             float* co = coef(s);
@@ -912,7 +1007,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 const int e_tok = ((rt * R) / 16 * 16 + 15) / R;
                 co[K::CO_BNEG + rt] = ex2_approx(co[K::CO_CUM2 + e_tok] - co[K::CO_CUM2 + rt]);
             }
-            float4 psi = make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 psi = phi0;
             for (int g = 0; g < tg; ++g) {
                 const float4 p4 = *reinterpret_cast<const float4*>(&sPart[g * NP2 + 4 * jg]);
                 psi.x += p4.x; psi.y += p4.y; psi.z += p4.z; psi.w += p4.w;
@@ -921,15 +1016,40 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             //      are issued only after batch 1 of chunk i, so waiting for them here keeps
             //      this group at most one chunk ahead of the consumer: every barrier the
             //      consumer waits on is then at most one phase ahead.
+            M3_TRACE_R(i, 2);
             const bool got_cb = wait_bounded(&ctl->fcb[s], (i >> 1) & 1, fail_r, fail_c);
+            M3_TRACE_R(i, 3);
             if (rt == 0 && got_cb) ctl->cb_waited[s] += 1;
             // the consumer may use this chunk's coefficients (exp(cum_end), f) now
             mbar_arrive(&ctl->coef_ready[s]);
             {
                 uint8_t* tC = tile_c(s);
                 uint8_t* tB = tile_b(s);
+                // tokens per batch of the plain rotation: the loads of a batch's 8 row pieces go out
+                // together, ahead of their stores (the compiler cannot tell the in-place stores from
+                // the next pieces' loads)
+                constexpr int TB = BC || R >= 2 ? 1 : 2;
+                static_assert(TPG % TB == 0, "token batches must divide the token group");
 #pragma unroll
-                for (int k = 0; k < TPG; ++k) {
+                for (int k0 = 0; k0 < TPG; k0 += TB) {
+                uint4 vc[TB * R], vb[TB * R];
+                float wb[TB];
+                if constexpr (!BC) {
+#pragma unroll
+                    for (int kb = 0; kb < TB; ++kb) {
+                        const int t = tg * TPG + k0 + kb;
+                        wb[kb] = sW[t];
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t off2 = pan * QR * 128 + sw128_offset(t * R + r, cib);
+                            if (FULL) vc[kb * R + r] = *reinterpret_cast<const uint4*>(tC + off2);
+                            vb[kb * R + r] = *reinterpret_cast<const uint4*>(tB + off2);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int kb = 0; kb < TB; ++kb) {
+                    const int k = k0 + kb;
                     const int t = tg * TPG + k;
                     psi.x = fmaf(dtk[k], om[k].x, psi.x);
                     psi.y = fmaf(dtk[k], om[k].y, psi.y);
@@ -940,7 +1060,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     __sincosf(-psi.y, &sn[1], &cs[1]);
                     __sincosf(-psi.z, &sn[2], &cs[2]);
                     __sincosf(-psi.w, &sn[3], &cs[3]);
-                    const float wt = sW[t];
+                    const float wt = BC ? sW[t] : wb[kb];
                     const float2 c01[2] = {make_float2(cs[0], cs[1]), make_float2(cs[2], cs[3])};
                     const float2 s01[2] = {make_float2(sn[0], sn[1]), make_float2(sn[2], sn[3])};
                     const float2 w2 = make_float2(wt, wt);
@@ -998,35 +1118,41 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const uint32_t off2 = pan * QR * 128 + sw128_offset(t * R + r, cib);
-                            if (FULL) {
-                                uint4* pc = reinterpret_cast<uint4*>(tC + off2);
-                                *pc = rotate4(*pc, c01, s01);
-                            }
-                            uint4* pb = reinterpret_cast<uint4*>(tB + off2);
-                            *pb = rotate4(*pb, cw01, sw01);
+                            if (FULL) *reinterpret_cast<uint4*>(tC + off2) = rotate4(vc[kb * R + r], c01, s01);
+                            *reinterpret_cast<uint4*>(tB + off2) = rotate4(vb[kb * R + r], cw01, sw01);
                         }
                     }
                 }
-                if (tg == TG - 1) *reinterpret_cast<float4*>(&co[K::CO_THETA + 4 * jg]) = psi;
+                }
+                // the phase at the chunk's last token: the next chunk starts from it
+                if (tg == TG - 1) *reinterpret_cast<float4*>(&co[K::CO_THETA + 4 * jg]) = reduce_2pi(psi);
             }
+            // C~ and B' are in place: the consumer may issue this chunk's scores
+            fence_proxy_async_smem();
+            mbar_arrive(&ctl->bc_done[s]);
+            M3_TRACE_R(i, 4);
             if (i + 1 < nl) {
                 load_omega(c + 1);
                 if (PREP) a_nx = load_a(c + 1);
             }
             group_bar(2);   // partial sums read: the boxes may take chunk i+2
+            phi0 = *reinterpret_cast<const float4*>(&co[K::CO_THETA + 4 * jg]);
             if (rt == 0 && i + 2 < nl && !*fail_r) load_box(i + 2, s);
 
-            // ---- X^ = exp(cum_end - cum_s) X into the X^ / SL buffer, once the previous
-            //      chunk's last reader of that buffer is done (batch 2, or batch 1 in the
-            //      state pass) and X has landed
-            if (i > 0) (void)wait_bounded(FULL ? &ctl->b2 : &ctl->b1, (i - 1) & 1, fail_r, fail_c);
+            // ---- X^ = exp(cum_end - cum_s) X into the X^ buffer, once the previous chunk's
+            //      chunk-state MMA has read it and X has landed
+            M3_TRACE_R(i, 5);
+            if (i > 0) (void)wait_bounded(&ctl->bH, (i - 1) & 1, fail_r, fail_c);
+            M3_TRACE_R(i, 6);
             const bool got_x = wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_r, fail_c);
             if (got_x) make_xhat(s);
             if (rt == 0 && got_x) ctl->x_waited[s] += 1;
 
+            M3_TRACE_R(i, 7);
             fence_proxy_async_smem();
             mbar_arrive(&ctl->rot_done[s]);
             group_bar(2);   // sW is reused by the next chunk
+            M3_TRACE_R(i, 8);
             if (*fail_r) break;
         }
     }
@@ -1047,12 +1173,19 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             drain(&ctl->fcb[s], ctl->cb_waited[s], ctl->cb_issued[s]);
             drain(&ctl->fx[s], ctl->x_waited[s], ctl->x_issued[s]);
         }
-        drain(&ctl->b1, ctl->b1_waited, ctl->b1_issued);
-        drain(&ctl->b2, ctl->b2_waited, ctl->b2_issued);
+        // thread 0 issued every MMA: a commit arrives once all of them are complete
+        mma_commit(&ctl->drain);
+        (void)mbar_wait(&ctl->drain, 0, kWaitLimitNs);
     }
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, K::TMEM_COLS);
+#ifdef M3_TRACE
+    if (tid == 0 && blockIdx.x < kTraceCtas) {
+        g_m3_trace_clk[blockIdx.x * 4 + 2] = (long long)globaltimer_ns();
+        g_m3_trace_clk[blockIdx.x * 4 + 3] = clock64();
+    }
+#endif
 }
 
 // ---------------------------------------------------------------------------
@@ -1236,26 +1369,24 @@ TcImpl impl() {
                   ws_cfg<NS, R, Q>, launches_cfg<NS, R, Q>, nullptr};
 }
 
-// Tile configuration for (N, R, chunk).  Chunks of chunk*R <= 128 rows run as
-// given.  Wider MIMO chunks run as sub-chunks of chunk/R tokens -- the MIMO
-// chunk-length reduction of section 3.3 -- so that every score tile stays at
-// chunk x chunk rows; the state passes between sub-chunks exactly as between
-// chunks, and the result differs only in rounding.
+// Tile configuration for (N, R, chunk).  Every chunk runs as sub-chunks of 64 / R tokens -- 64-row
+// tiles, the MIMO chunk-length reduction of section 3.3 taken to one tile shape -- so that two CTAs
+// fit on an SM (measured faster than 128-row tiles at one CTA per SM for every workload here); the
+// state passes between sub-chunks exactly as between chunks, and the result differs only in rounding.
 bool pick(const ScanDims& d, TcImpl* out) {
     if (d.headdim != 64 || d.io != M3_DTYPE_BF16) return false;
     if (d.nheads % 4) return false;
-    const int N = (int)d.dstate, R = d.R, Q = d.chunk;
+    if (d.chunk != 64 && d.chunk != 128) return false;
+    const int N = (int)d.dstate, R = d.R;
     TcImpl f{};
-    if (N == 128 && R == 1 && Q == 64) {
+    if (N == 128 && R == 1) {
         f = impl<128, 1, 64>();
         f.hook = launch_cfg<128, 1, 64, kTestHook>;
-    }
-    else if (N == 128 && R == 1 && Q == 128) f = impl<128, 1, 128>();
-    else if (N == 128 && R == 2 && Q == 64) f = impl<128, 2, 64>();
-    else if (N == 64 && R == 1 && Q == 64) f = impl<64, 1, 64>();
-    else if (N == 64 && R == 4 && Q == 64) f = impl<64, 4, 16>();
-    else if (N == 128 && R == 4 && Q == 64) f = impl<128, 4, 16>();
-    else if (N == 128 && R == 4 && Q == 128) f = impl<128, 4, 32>();
+    } else if (N == 128 && R == 2) f = impl<128, 2, 32>();
+    else if (N == 128 && R == 4) f = impl<128, 4, 16>();
+    else if (N == 64 && R == 1) f = impl<64, 1, 64>();
+    else if (N == 64 && R == 2) f = impl<64, 2, 32>();
+    else if (N == 64 && R == 4) f = impl<64, 4, 16>();
     else return false;
     if (out) *out = f;
     return true;
@@ -1284,3 +1415,22 @@ cudaError_t launch_scan_tc(const ScanDims& d, const void* x, const void* B, cons
 }
 
 }  // namespace m3
+
+#ifdef M3_TRACE
+// Diagnostic build only: copy out (or clear, dst = NULL) the phase trace; n = number of int64 entries of
+// the trace (kTraceCtas * kTraceChunks * kTraceSlots) followed by the clock pairs (kTraceCtas * 4).
+extern "C" __attribute__((visibility("default"))) int m3_trace_read(long long* dst, int n) {
+    using namespace m3;
+    constexpr int nt = kTraceCtas * kTraceChunks * kTraceSlots, nc = kTraceCtas * 4;
+    if (n != nt + nc) return M3_ERR_INVALID_ARG;
+    if (dst == nullptr) {
+        static long long zeros[nt + nc] = {};
+        if (cudaMemcpyToSymbol(g_m3_trace, zeros, sizeof(long long) * nt) != cudaSuccess) return M3_ERR_CUDA;
+        if (cudaMemcpyToSymbol(g_m3_trace_clk, zeros, sizeof(long long) * nc) != cudaSuccess) return M3_ERR_CUDA;
+        return M3_OK;
+    }
+    if (cudaMemcpyFromSymbol(dst, g_m3_trace, sizeof(long long) * nt) != cudaSuccess) return M3_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(dst + nt, g_m3_trace_clk, sizeof(long long) * nc) != cudaSuccess) return M3_ERR_CUDA;
+    return M3_OK;
+}
+#endif

@@ -1,0 +1,142 @@
+"""Phase trace of the tensor-core prefill kernel (a diagnostic, not part of the product path).
+
+Builds libm3_trace.so -- the library compiled with -DM3_TRACE, in which the
+prefill kernel records clock64 at the phase boundaries of the first chunks of
+its first CTAs -- runs one m3_scan_fwd call on a workload after warm-up calls,
+and prints, per warp group, the median cycles each phase takes and the chunk
+period, plus the tensor-pipe rate inside two of the chunk's MMA batches
+measured in place: the chunk-state GEMM H += B'^T X^ (issue by thread 0 right
+after the group barrier, completion seen by a consumer thread spinning on its
+commit barrier) and the intra-chunk output GEMM Y = SL X (likewise).  A
+batch's rate is its executed FLOPs over its issue-to-completion cycles,
+against the SM's share of the measured dense bf16 peak at the traced clock.
+
+    python -m state_space_sequence_04_b300.trace [--workload NAME] [--json PATH]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from state_space_sequence_04_b300 import binding, build, synth  # noqa: E402
+
+CTAS, CHUNKS, SLOTS = 4, 64, 32          # kTraceCtas, kTraceChunks, kTraceSlots of the kernel
+SMS = 148
+KEYS = ("x", "B", "C", "dt", "A", "lam", "omega")
+# slot names: consumer thread 0 (0-9), observers (11, 12), rotate thread 128 (16-24)
+CONSUMER = ["top", "stage ready (rot_done + barrier)", "H+= and Yi issued", "S and H+= waited",
+            "mask + barrier", "Y issued (+ next S)", "Y waited", "output stored", "next coefficients",
+            "state step + barrier"]
+ROTATE = ["top", "dt/lambda boxes", "coefficients + angle partial sums", "C/B landed", "rotation (C~, B')",
+          "barrier + next boxes issued", "previous H+= waited", "X^ written", "barrier"]
+
+
+def peak_bf16_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1800.0, "fallback"
+
+
+def run(wname: str):
+    lib_path = build.build(trace=True)
+    binding.LIB_PATH = lib_path
+    lib = binding.load()
+    lib.m3_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.m3_trace_read.restype = ctypes.c_int
+    n = CTAS * CHUNKS * SLOTS + CTAS * 4
+    w = synth.WORKLOADS[wname]
+    d = synth.make_inputs(w, seed=0, device="cuda")
+    args = [d[k] for k in KEYS]
+    path, launches = binding.m3_scan_fwd_plan(w.batch, w.seqlen, w.heads, w.headdim, w.dstate, w.rank, w.chunk,
+                                              binding.io_code(d["x"].dtype))
+    if path != 1:
+        raise SystemExit(f"{wname} does not take the tensor-core path")
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((w.batch, w.heads, w.dstate, w.headdim), dtype=torch.float32, device="cuda")
+    ws = binding.alloc_workspace(d["x"].shape, w.dstate, w.rank, w.chunk, d["x"].dtype, "cuda")
+    for _ in range(3):
+        binding._check(binding.m3_scan_fwd(*args, w.rank, w.chunk, y, fin, ws), "m3_scan_fwd")
+    torch.cuda.synchronize()
+    binding._check(lib.m3_trace_read(None, n), "m3_trace_read")
+    binding._check(binding.m3_scan_fwd(*args, w.rank, w.chunk, y, fin, ws), "m3_scan_fwd")
+    torch.cuda.synchronize()
+    buf = (ctypes.c_longlong * n)()
+    binding._check(lib.m3_trace_read(ctypes.addressof(buf), n), "m3_trace_read")
+    tr = list(buf)
+    clk = tr[CTAS * CHUNKS * SLOTS:]
+    # cycles per ns from the traced CTAs' (globaltimer, clock64) pairs
+    rates = [(clk[4 * c + 3] - clk[4 * c + 1]) / (clk[4 * c + 2] - clk[4 * c + 0])
+             for c in range(CTAS) if clk[4 * c + 2] > clk[4 * c + 0]]
+    ghz = statistics.median(rates)
+
+    def at(cta, i, slot):
+        return tr[(cta * CHUNKS + i) * SLOTS + slot]
+
+    # the last launch of the call (the full pass) is the one traced last: its values overwrite the state pass's
+    QR, P, N = w.chunk * w.rank if w.chunk * w.rank <= 128 else w.chunk, w.headdim, w.dstate
+    QR = min(QR, 128)
+    MM = 64 if QR == 64 else 128
+    out = {"workload": wname, "launches_per_call": launches, "sm_ghz_traced": ghz, "consumer": {}, "rotate": {}}
+    nchunk = []
+    for cta in range(CTAS):
+        k = 0
+        while k < CHUNKS and at(cta, k, 0) != 0 and at(cta, k, 9) != 0:
+            k += 1
+        nchunk.append(k)
+    use = [(cta, i) for cta in range(CTAS) for i in range(1, nchunk[cta] - 1)]
+    if not use:
+        raise SystemExit("no traced chunks")
+    for j in range(1, len(CONSUMER)):
+        dts = [at(c, i, j) - at(c, i, j - 1) for c, i in use if at(c, i, j) and at(c, i, j - 1)]
+        out["consumer"][CONSUMER[j]] = statistics.median(dts) if dts else None
+    for j in range(1, len(ROTATE)):
+        dts = [at(c, i, 16 + j) - at(c, i, 16 + j - 1) for c, i in use]
+        out["rotate"][ROTATE[j]] = statistics.median(dts)
+    out["chunk_period_cycles"] = statistics.median(at(c, i + 1, 0) - at(c, i, 0) for c, i in use)
+    out["chunk_period_us"] = out["chunk_period_cycles"] / ghz / 1e3
+    out["rotate_busy_cycles"] = statistics.median(at(c, i, 24) - at(c, i, 16) for c, i in use)
+    out["scores_issued_early"] = sum(at(c, i, 10) for c, i in use) / len(use)
+    pk, src = peak_bf16_tflops()
+    per_cycle = pk * 1e12 / SMS / (ghz * 1e9)          # FLOP per cycle of one SM at the traced clock
+    # chunks whose scores went out early: thread 0 issued only H+= (and Yi) after the barrier
+    hplus = [at(c, i, 12) - at(c, i, 1) for c, i in use if at(c, i - 1, 10) == 1 and at(c, i, 12)]
+    yb = [at(c, i, 11) - at(c, i, 4) for c, i in use if at(c, i, 11)]
+    f_h = 2.0 * 128 * P * QR                            # executed: M = 128 state rows, N = P, K = QR
+    f_y = 2.0 * MM * P * QR                             # executed: M = MM rows, N = P, K = QR
+    out["gemm_phase"] = {
+        "peak_bf16_tflops": pk, "peak_source": src, "sm_flop_per_cycle": per_cycle,
+        "chunk_state": {"shape_MxNxK": [128, P, QR], "cycles": statistics.median(hplus) if hplus else None,
+                        "frac_of_sm_peak": f_h / statistics.median(hplus) / per_cycle if hplus else None},
+        "output_SLX": {"shape_MxNxK": [MM, P, QR], "cycles": statistics.median(yb) if yb else None,
+                       "frac_of_sm_peak": f_y / statistics.median(yb) / per_cycle if yb else None},
+        "note": "issue-to-completion in place, the SM's tensor pipe shared by its CTAs",
+    }
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default=synth.SISO_1P5B.name, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--json", default=None)
+    a = ap.parse_args()
+    out = run(a.workload)
+    print(json.dumps(out, indent=1))
+    if a.json:
+        with open(a.json, "w") as f:
+            json.dump(out, f, indent=1)
+
+
+if __name__ == "__main__":
+    main()
