@@ -111,7 +111,6 @@ struct Cfg {
     static constexpr int BC_BYTES = NPAN * QR * 128;
     static constexpr int SL_BYTES = QR * QR * 2;
     static_assert(SL_BYTES <= BC_BYTES, "the masked scores are written over the chunk's B tile");
-    static constexpr int XS_BYTES = X_BYTES;
     static constexpr int STG_TILE = 2 * BC_BYTES + X_BYTES;      // C | B | X of one stage
     static constexpr int BOX_BYTES = 16 * (Q + 1);                // dt / lambda box {4 heads, Q+1 tokens}
     static constexpr int BOX_STRIDE = align_up(BOX_BYTES, 128);
@@ -126,12 +125,11 @@ struct Cfg {
     // coefficient block of a stage (floats): cum*log2e[Q], rho[Q], exp(cum)[Q], b[Q],
     // f = exp(cum_end - cum)[Q], Theta[NS/2] (the phase of each pair at the chunk's last token since
     // the segment start, mod 2 pi), exp(cum_end), cum_end
-    static constexpr int CO_CUM2 = 0, CO_RHO = Q, CO_ECUM = 2 * Q, CO_BNEG = 3 * Q, CO_F = 4 * Q, CO_THETA = 5 * Q,
+    static constexpr int CO_CUM2 = 0, CO_RHO = Q, CO_ECUM = 2 * Q, CO_BNEG = 3 * Q, CO_CG = 4 * Q, CO_THETA = 5 * Q,
                          CO_EEND = 5 * Q + NS / 2, CO_CEND = 5 * Q + NS / 2 + 1;
     static constexpr int CO_BYTES = align_up((5 * Q + NS / 2 + 2) * 4, 16);
 
-    static constexpr int OFF_XS = 2 * STG_TILE;                   // X^
-    static constexpr int OFF_HB = OFF_XS + XS_BYTES;
+    static constexpr int OFF_HB = 2 * STG_TILE;
     static constexpr int OFF_BOX = OFF_HB + NS * 128;             // [stage][dt | lambda]
     static constexpr int OFF_PART = OFF_BOX + 4 * BOX_STRIDE;     // only when not in the boxes
     static constexpr int OFF_CO = OFF_PART + (PART_IN_BOX ? 0 : align_up(PART_BYTES, 16));
@@ -207,7 +205,7 @@ __device__ __forceinline__ uint32_t word_at(const uint4* a, int i) {
 struct Ctl {
     uint64_t fbox[2], fcb[2], fx[2];   // TMA groups landed
     uint64_t bc_done[2];     // rotate group rotated the stage's C and B (count 128)
-    uint64_t rot_done[2];    // rotate group finished the stage, X^ included (count 128)
+    uint64_t rot_done[2];    // rotate group finished the stage (count 128)
     uint64_t coef_ready[2];  // coefficient block of the stage written (count 128)
     uint64_t coef_free[2];   // consumer done reading the stage's coefficient block (count 128)
     uint64_t bS;             // scores S of a chunk complete (one commit per chunk, in chunk order)
@@ -340,13 +338,16 @@ __device__ __forceinline__ void load8(const float* p, float fill, float (&o)[8])
 }
 
 // Mask one 16-column block of a score row held in v[0..15]: columns cb..cb+15
-// (tokens cb/R ..), row token t.  Blocks strictly below the diagonal use the
-// factorised decay 2^(cum2_t - cum2_e) 2^(cum2_e - cum2_s), e = the block's last
-// token (both factors <= 1; the second is b_s); the diagonal block uses the
-// exponential of the difference directly; blocks above are zero.
+// (tokens cb/R ..), row token t.  The scores were taken with B'' = f' B' (f'_s =
+// 2^g_s, the decay from token s to the chunk's end, clamped at 2^-100), so the
+// mask also divides by f'_s.  Blocks strictly below the diagonal use the
+// factorised factor 2^(cum2_t - cum2_e) 2^(cum2_e - cum2_s - g_s), e = the
+// block's last token (the first factor <= 1, the second, b_s, <= 2^100); the
+// diagonal block uses 2^(cum2_t - (cum2_s + g_s)) directly (cg = cum2 + g) and
+// rho_t 2^-g_t on the diagonal; blocks above are zero.
 template <int R>
 __device__ __forceinline__ void mask_block(float* v, int cb, int t, float ct, float rt, const float* cum2,
-                                           const float* bneg) {
+                                           const float* bneg, const float* cg) {
     const int s_lo = cb / R, s_hi = (cb + 15) / R;
     if (s_lo > t) {
 #pragma unroll
@@ -366,7 +367,7 @@ __device__ __forceinline__ void mask_block(float* v, int cb, int t, float ct, fl
         for (int i = 0; i < 16; ++i) {
             const int sidx = (cb + i) / R;
             float m = 0.f;
-            if (sidx < t) m = ex2_approx(ct - cum2[sidx]);
+            if (sidx < t) m = ex2_approx(ct - cg[sidx]);
             else if (sidx == t) m = rt;
             v[i] *= m;
         }
@@ -419,37 +420,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
     auto box_dt = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_BOX + (2 * s) * K::BOX_STRIDE); };
     auto box_lam = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_BOX + (2 * s + 1) * K::BOX_STRIDE); };
     auto coef = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_CO + s * K::CO_BYTES); };
-    uint8_t* xs = sm + K::OFF_XS;   // X^ of the chunk being set up, then SL of the chunk being masked
     uint8_t* hb = sm + K::OFF_HB;
-    // X^ = exp(cum_end - cum_s) X of the chunk in stage s, into the X^ / SL buffer (consumer threads)
-    auto make_xhat = [&](int s) {   // rotate threads
-        // QR rows x 8 16-byte pieces, NPC per thread.  Every load goes first: the compiler cannot
-        // tell a store to X^ from a later load of X, and would otherwise serialise them
-        constexpr int NPC = QR * 8 / 128;
-        const uint8_t* tX = tile_x(s);
-        const float* f = coef(s) + K::CO_F;
-        const int p0 = threadIdx.x - 128;
-        uint4 v[NPC];
-        float fr[NPC];
-#pragma unroll
-        for (int k = 0; k < NPC; ++k) {
-            const int pidx = p0 + 128 * k, row = pidx >> 3;
-            v[k] = *reinterpret_cast<const uint4*>(tX + sw128_offset(row, (pidx & 7) * 16));
-            fr[k] = f[row / R];
-        }
-#pragma unroll
-        for (int k = 0; k < NPC; ++k) {
-            const int pidx = p0 + 128 * k;
-            const float2 f2 = make_float2(fr[k], fr[k]);
-            uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 g = __fmul2_rn(f2, make_float2(bf_lo(w[e]), bf_hi(w[e])));
-                w[e] = pack_bf16(g.x, g.y);
-            }
-            *reinterpret_cast<uint4*>(xs + sw128_offset(pidx >> 3, (pidx & 7) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    };
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -574,7 +545,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
         group_bar(1);
         const bool odd = tid & 1;
         float ld_sum = 0.f;   // state pass: summed log-decay (thread 0)
-        // S = C~ B'^T of the chunk in stage s, committed to bS (thread 0)
+        // S = C~ B''^T of the chunk in stage s, committed to bS (thread 0, which issues every MMA)
         auto issue_scores = [&](int s) {
             const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
             const uint64_t dB = smem_desc(smem_u32(tile_b(s)), 16, 1024, kSwizzle128B);
@@ -599,8 +570,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             const int c = c_begin + i, s = i & 1;
             const float* co = coef(s);
             M3_TRACE_C(i, 0);
-            // ---- once the rotate group has finished this stage (X^ included):
-            //      H += B'^T X^ (the chunk state onto the carry), then Yi = C~ Hb_{c-1}
+            // ---- once the rotate group has finished this stage:
+            //      H += B''^T X (the chunk state onto the carry), then Yi = C~ Hb_{c-1}
             (void)wait_bounded(&ctl->rot_done[s], (i >> 1) & 1, fail_c, fail_r);
             if constexpr (HOOK) {
                 if (FULL && i == ext.fail_chunk) (void)wait_bounded(&ctl->never, 0, fail_c, fail_r, 50000ull);
@@ -629,9 +600,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     issue_scores(s);
                     s_next = i + 1;
                 }
+                // the chunk's X (read by the chunk state here and by the output later)
+                if (wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_c, fail_r)) ctl->x_waited[s] += 1;
+                tc_fence_after();
                 // descriptors of the operand bases; a byte offset o moves the start address field by o >> 4
                 const uint64_t dBt = smem_desc(smem_u32(tile_b(s)), QR * 128, 1024, kSwizzle128B);
-                const uint64_t dX = smem_desc(smem_u32(xs), 16, 1024, kSwizzle128B);
+                const uint64_t dX = smem_desc(smem_u32(tile_x(s)), 16, 1024, kSwizzle128B);
                 constexpr uint32_t id_u = idesc_bf16_f32(128, P, true, true);
                 // A is MN-major over n (NS rows; panels QR*128 bytes apart); with NS = 64 the
                 // second panel reads the next QR*128 bytes and its results are unused
@@ -670,8 +644,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                     ecum_t = co[K::CO_ECUM + t];
                     float v[32];
                     tmem_ld16x2_sync(tlane + K::T_S, v);
-                    mask_block<R>(v, 32 * half, t, ct, rt, cum2, co + K::CO_BNEG);
-                    mask_block<R>(v + 16, 32 * half + 16, t, ct, rt, cum2, co + K::CO_BNEG);
+                    mask_block<R>(v, 32 * half, t, ct, rt, cum2, co + K::CO_BNEG, co + K::CO_CG);
+                    mask_block<R>(v + 16, 32 * half + 16, t, ct, rt, cum2, co + K::CO_BNEG, co + K::CO_CG);
 #pragma unroll
                     for (int q8 = 0; q8 < 4; ++q8) {
                         const int col = 32 * half + q8 * 8;
@@ -695,8 +669,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
 #pragma unroll
                             for (int i4 = 0; i4 < 32; ++i4) v[i4] = 0.f;
                         }
-                        mask_block<R>(v, c32, t, ct, rt, cum2, co + K::CO_BNEG);
-                        mask_block<R>(v + 16, c32 + 16, t, ct, rt, cum2, co + K::CO_BNEG);
+                        mask_block<R>(v, c32, t, ct, rt, cum2, co + K::CO_BNEG, co + K::CO_CG);
+                        mask_block<R>(v + 16, c32 + 16, t, ct, rt, cum2, co + K::CO_BNEG, co + K::CO_CG);
 #pragma unroll
                         for (int q8 = 0; q8 < 4; ++q8) {
                             const int col = c32 + q8 * 8;
@@ -795,7 +769,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 }
                 M3_TRACE_C(i, 7);
             } else {
-                // B' and X^ are consumed (X was consumed into X^): the next loads may come in
+                // B'' and X are consumed: the next loads may come in
                 if (tid == 0 && i + 2 < nl && !*fail_c) {
                     load_cb(i + 2, s);
                     load_x(i + 2, s);
@@ -966,10 +940,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             // ---- coefficients and chunk-local log-decay prefix
             const float ell = d * a_t, gam = l * d, wv = gam + (1.f - ln) * dn;
             float cum = warp_inclusive_sum(ell);
+            M3_TRACE_R(i, 9);
             if (lane == 31) sWarpR[rw] = cum;
             // the consumer is done with chunk i-2's coefficients in this stage
             if (i >= 2) (void)wait_bounded(&ctl->coef_free[s], ((i - 2) >> 1) & 1, fail_r, fail_c);
             group_bar(2);   // every box value is read (the boxes may now hold partial sums)
+            M3_TRACE_R(i, 10);
             float off = 0.f, cend = 0.f;
             for (int k = 0; k < 4; ++k) {
                 const float v = sWarpR[k];
@@ -978,18 +954,23 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             }
             cum += off;
             if (rt < Q) {
+                // g = log2 of the decay from this token to the chunk's end, clamped at -100: B is
+                // scaled by it here (B'' = 2^g w R(-Psi) B, the chunk state's weight), and the mask
+                // divides the scores by it again (every mask factor stays <= 2^100)
+                const float g = fmaxf((cend - cum) * kLog2e, -100.f);
                 if (FULL) {
                     co[K::CO_CUM2 + rt] = cum * kLog2e;
-                    co[K::CO_RHO + rt] = wv > 0.f ? gam / wv : 0.f;
+                    co[K::CO_CG + rt] = fmaf(cum, kLog2e, g);
+                    co[K::CO_RHO + rt] = (wv > 0.f ? __fdividef(gam, wv) : 0.f) * ex2_approx(-g);
                     co[K::CO_ECUM + rt] = __expf(cum);
                 }
-                sW[rt] = wv;
-                co[K::CO_F + rt] = __expf(cend - cum);
+                sW[rt] = wv * ex2_approx(g);
             }
             if (rt == 0) {
                 co[K::CO_EEND] = __expf(cend);
                 co[K::CO_CEND] = cend;
             }
+            M3_TRACE_R(i, 11);
             // ---- rotation angles: partial sums per token group
             {
                 float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1002,15 +983,25 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
                 }
                 *reinterpret_cast<float4*>(&sPart[tg * NP2 + 4 * jg]) = part;
             }
+            M3_TRACE_R(i, 12);
             group_bar(2);   // coefficient block and partial sums written
+            M3_TRACE_R(i, 13);
             if (FULL && rt < Q) {   // b_s of the mask: 2^(cum2[last token of s's 16-column block] - cum2[s])
                 const int e_tok = ((rt * R) / 16 * 16 + 15) / R;
-                co[K::CO_BNEG + rt] = ex2_approx(co[K::CO_CUM2 + e_tok] - co[K::CO_CUM2 + rt]);
+                co[K::CO_BNEG + rt] = ex2_approx(co[K::CO_CUM2 + e_tok] - co[K::CO_CG + rt]);
             }
+            // exclusive prefix of the token groups' partial sums: every load issued together
             float4 psi = phi0;
-            for (int g = 0; g < tg; ++g) {
-                const float4 p4 = *reinterpret_cast<const float4*>(&sPart[g * NP2 + 4 * jg]);
-                psi.x += p4.x; psi.y += p4.y; psi.z += p4.z; psi.w += p4.w;
+            {
+                float4 p4[TG - 1];
+#pragma unroll
+                for (int g = 0; g < TG - 1; ++g)
+                    p4[g] = g < tg ? *reinterpret_cast<const float4*>(&sPart[g * NP2 + 4 * jg])
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int g = 0; g < TG - 1; ++g) {
+                    psi.x += p4[g].x; psi.y += p4[g].y; psi.z += p4[g].z; psi.w += p4[g].w;
+                }
             }
             // ---- rotate C and B in place once they have landed.  C and B of chunk i+2
             //      are issued only after batch 1 of chunk i, so waiting for them here keeps
@@ -1139,17 +1130,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
             phi0 = *reinterpret_cast<const float4*>(&co[K::CO_THETA + 4 * jg]);
             if (rt == 0 && i + 2 < nl && !*fail_r) load_box(i + 2, s);
 
-            // ---- X^ = exp(cum_end - cum_s) X into the X^ buffer, once the previous chunk's
-            //      chunk-state MMA has read it and X has landed
             M3_TRACE_R(i, 5);
-            if (i > 0) (void)wait_bounded(&ctl->bH, (i - 1) & 1, fail_r, fail_c);
             M3_TRACE_R(i, 6);
-            const bool got_x = wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_r, fail_c);
-            if (got_x) make_xhat(s);
-            if (rt == 0 && got_x) ctl->x_waited[s] += 1;
-
             M3_TRACE_R(i, 7);
-            fence_proxy_async_smem();
             mbar_arrive(&ctl->rot_done[s]);
             group_bar(2);   // sW is reused by the next chunk
             M3_TRACE_R(i, 8);

@@ -37,8 +37,8 @@ KEYS = ("x", "B", "C", "dt", "A", "lam", "omega")
 CONSUMER = ["top", "stage ready (rot_done + barrier)", "H+= and Yi issued", "S and H+= waited",
             "mask + barrier", "Y issued (+ next S)", "Y waited", "output stored", "next coefficients",
             "state step + barrier"]
-ROTATE = ["top", "dt/lambda boxes", "coefficients + angle partial sums", "C/B landed", "rotation (C~, B')",
-          "barrier + next boxes issued", "previous H+= waited", "X^ written", "barrier"]
+ROTATE = ["top", "dt/lambda boxes", "coefficients + angle partial sums", "C/B landed", "rotation (C~, B'')",
+          "barrier + next boxes issued", "-", "-", "barrier"]
 
 
 def peak_bf16_tflops():
@@ -104,6 +104,12 @@ def run(wname: str):
     for j in range(1, len(ROTATE)):
         dts = [at(c, i, 16 + j) - at(c, i, 16 + j - 1) for c, i in use]
         out["rotate"][ROTATE[j]] = statistics.median(dts)
+    # inside the rotate group's coefficient phase (slots 16+1 -> 16+9 .. 16+13 -> 16+2)
+    sub = [(1, 9, "box values read + log-decay warp scan"), (9, 10, "coefficient-block release + barrier"),
+           (10, 11, "coefficients written"), (11, 12, "angle partial sums written"), (12, 13, "barrier"),
+           (13, 2, "mask factors + angle prefix")]
+    out["rotate_coefficient_phase"] = {name: statistics.median(at(c, i, 16 + b) - at(c, i, 16 + a) for c, i in use)
+                                       for a, b, name in sub}
     out["chunk_period_cycles"] = statistics.median(at(c, i + 1, 0) - at(c, i, 0) for c, i in use)
     out["chunk_period_us"] = out["chunk_period_cycles"] / ghz / 1e3
     out["rotate_busy_cycles"] = statistics.median(at(c, i, 24) - at(c, i, 16) for c, i in use)
