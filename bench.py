@@ -294,7 +294,9 @@ def prefill_leg(binding, w, d, args, stream, dist, device, local, pk, ws, rank, 
         "gpu_launches": launches * steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"],
-                     "traffic": profiled_traffic(src, f"{src.rsplit('/', 1)[1][:-3]}_{w.name}.md"),
+                     # the committed ncu summary of this workload's dominant kernel (only for the named sizes)
+                     "traffic": (profiled_traffic(src, f"{src.rsplit('/', 1)[1][:-3]}_{w.name}.md")
+                                 if synth.WORKLOADS.get(w.name) == w else None),
                      "kernel": "m3_scan_fwd (" + ("tensor-core" if path == 1 else "CUDA-core") +
                                f" path, {launches} launches per call)",
                      "algorithmic_bytes_per_call": nbytes, "peak_source": pk["source"],
@@ -752,6 +754,9 @@ def main():
     ap.add_argument("--mode", choices=["all", "decode", "bwd"], default="all",
                     help="decode: only the decode sweep (restricted by --decode-batch/--decode-rank); "
                          "bwd: only the backward pass (sizes overridable by --bwd-batch/--bwd-seqlen)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (a smaller case of the same shape, e.g. for a profiler)")
+    ap.add_argument("--seqlen", type=int, default=None, help="override the workload's sequence length")
     ap.add_argument("--bwd-batch", type=int, default=None)
     ap.add_argument("--bwd-seqlen", type=int, default=None)
     ap.add_argument("--decode-batch", type=int, default=None)
@@ -771,6 +776,8 @@ def main():
     binding.load()
     pk = peaks()
     w = synth.WORKLOADS[args.workload]
+    if args.batch or args.seqlen:
+        w = dataclasses.replace(w, batch=args.batch or w.batch, seqlen=args.seqlen or w.seqlen)
     stream = torch.cuda.Stream(device=device)
 
     if args.mode == "decode":

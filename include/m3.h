@@ -100,10 +100,9 @@ M3_API int m3_scan_fwd_plan(int64_t batch, int64_t seqlen, int64_t nheads, int64
  *            intra-chunk masked scores (decay x two-band mask, Eq. 7)
  *            plus inter-chunk state passing; 16 <= chunk <= 256 and a
  *            multiple of 16.  The result does not depend on it beyond rounding.
- *            The tensor-core path runs chunks of more than 128 rows
- *            (chunk * R) as sub-chunks of chunk / R tokens, the MIMO
- *            chunk-length reduction of section 3.3, so that every score tile
- *            stays chunk x chunk rows.  With fewer (batch, head) sequences than
+ *            The tensor-core path runs every chunk as sub-chunks of 64 / R
+ *            tokens (64-row score tiles), the MIMO chunk-length reduction of
+ *            section 3.3 taken to one tile shape.  With fewer (batch, head) sequences than
  *            the GPU has CTA slots it also cuts each sequence into segments
  *            (a state pass, the segment scan of m3_state_passing, a full pass).
  *   y        out [batch, T, H, R, P], io dtype
@@ -316,14 +315,18 @@ M3_API int m3_scan_bwd(const void* x, const void* B, const void* C, const float*
  *                  [H, R, N] fp32: the B/C normalisation's parameters (sums
  *                  over rows by atomics); dB, dC are then the raw rows'
  *                  gradients (through v -> v r gain + bias, r = rsqrt(mean(v^2)
- *                  + eps)).  The B/C normalisation's backward takes fp32 io
- *                  and no gate (else M3_ERR_UNSUPPORTED): the normalised rows
- *                  reach the adjoint kernel in the io dtype
- *   workspace: m3_scan_bwd_prep_workspace_size bytes, 256-byte aligned:
- *            m3_scan_bwd's, Delta and lambda (2 * batch * T * H fp32), the
- *            normalised B and C rows (io dtype) and their inverse RMS, and,
- *            where the forward entry supports the shape, the ungated output
- *            y_pre (io dtype, y's layout) and m3_scan_fwd_prep's workspace.
+ *                  + eps)).  With bf16 io, or together with the gate, the
+ *                  adjoint runs in fp32 on fp32 copies of x, of the seed
+ *                  dy * SiLU(z) and of the normalised rows, so that nothing it
+ *                  reads is rounded to bf16 beyond the inputs themselves
+ *   workspace: m3_scan_bwd_prep_workspace_size bytes, 256-byte aligned, an
+ *            upper bound over the options params may select: m3_scan_bwd's
+ *            (fp32 layout where the B/C normalisation's fp32 copies need it),
+ *            Delta and lambda (2 * batch * T * H fp32), the normalised B and C
+ *            rows and their inverse RMS, the fp32 copies of x and of the seed,
+ *            and, where the forward entry supports the shape, the ungated
+ *            output y_pre (io dtype, y's layout) and m3_scan_fwd_prep's
+ *            workspace.
  * Delta and lambda are derived with the forward entry's own functions; the
  * derivative of softplus is sigmoid, that of sigmoid is lambda (1 - lambda).
  * With the gate, the seed of the recurrence is dy * SiLU(z) (fp32, inside the

@@ -318,11 +318,9 @@ int m3_scan_bwd_prep(const void* x, const void* B, const void* C, const float* d
         if (!ok_nullable(q)) return M3_ERR_INVALID_ARG;
     const m3::BwdBcArgs bca{params != nullptr && fp.bc(), fp.bc_norm ? 1 : 0, fp.bc_eps, fp.B_gain, fp.C_gain,
                             fp.B_bias, fp.C_bias, dB_gain, dC_gain, dB_bias, dC_bias};
-    // the normalised rows feed the adjoint kernel in the io dtype: bf16 rows lose too much for gradients,
-    // so the B / C normalisation's backward takes fp32 io, and not together with the gate
-    if (bca.on && (io_dtype != M3_DTYPE_F32 || params->z != nullptr)) return M3_ERR_UNSUPPORTED;
     if (batch * nheads > (int64_t)INT32_MAX || seqlen > (int64_t)INT32_MAX) return M3_ERR_UNSUPPORTED;
     if (!m3::bwd_supported(d)) return M3_ERR_UNSUPPORTED;
+    if (bca.on && !m3::bwd_bc_supported(d)) return M3_ERR_UNSUPPORTED;
     const BwdPrepWs w = bwd_prep_ws(d);
     if (z != nullptr && !w.gate) return M3_ERR_UNSUPPORTED;
     const bool any_tokens = batch > 0 && seqlen > 0;

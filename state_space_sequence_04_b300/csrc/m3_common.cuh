@@ -130,6 +130,8 @@ cudaError_t launch_scan_bwd_prep(const ScanDims& d, const void* x, const void* B
                                  void* workspace, cudaStream_t stream);
 // the backward through the output gate (z) fits the shared-memory budget
 bool bwd_gate_supported(const ScanDims& d);
+// the B / C normalisation's backward (its fp32 adjoint run) fits it
+bool bwd_bc_supported(const ScanDims& d);
 // Delta = softplus(dt_raw + dt_bias[h]) and lambda = sigmoid(u) of n (batch, token, head) entries
 cudaError_t launch_prep_params(const float* dt_raw, const float* dt_bias, const float* u, float* dt_out,
                                float* lam_out, int64_t n, int H, cudaStream_t stream);

@@ -692,11 +692,12 @@ __global__ void bwd_gate_dz(const IO* __restrict__ dy, const IO* __restrict__ z,
 
 // B / C normalisation of every (token, rank) row ("Mamba-3", section 3.4): Vn = V r gain + bias with
 // r = rsqrt(mean(V^2) + eps) (the forward entry's formula; r = 1 and no gain without the norm), r kept for
-// the rows' backward.  One warp per row; rows are (batch, token, head, rank) major, HR = H * R.
-template <typename IO>
+// the rows' backward.  One warp per row; rows are (batch, token, head, rank) major, HR = H * R.  The rows
+// are written in OT (fp32 where the adjoint runs on fp32 copies of bf16 inputs).
+template <typename IO, typename OT>
 __global__ void __launch_bounds__(256) bc_rows_forward(const IO* __restrict__ V, const float* __restrict__ gain,
                                                        const float* __restrict__ bias, int norm, float eps,
-                                                       IO* __restrict__ Vn, float* __restrict__ rinv, int64_t rows,
+                                                       OT* __restrict__ Vn, float* __restrict__ rinv, int64_t rows,
                                                        int HR, int N) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -779,6 +780,19 @@ __global__ void __launch_bounds__(256) bc_rows_backward(const IO* __restrict__ V
     }
 }
 
+// fp32 copies for the adjoint of the promoted path: dst = src, and the seed dst = dy silu(z) (z null: dy)
+template <typename IO>
+__global__ void to_f32(const IO* __restrict__ src, float* __restrict__ dst, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = ld_io(src, i);
+}
+template <typename IO>
+__global__ void gate_seed_f32(const IO* __restrict__ dy, const IO* __restrict__ z, float* __restrict__ dst,
+                              int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = z != nullptr ? ld_io(dy, i) * silu_f(ld_io(z, i)) : ld_io(dy, i);
+}
+
 // B / C normalisation arguments of m3_scan_bwd_prep (on == false: none)
 struct BwdBc {
     bool on;
@@ -835,13 +849,112 @@ BwdWs bwd_ws_prep(const ScanDims& d) {
     return w;
 }
 
-size_t bwd_ws_prep_total(const ScanDims& d) { return bwd_ws_prep(d).total; }
+// The promoted path of the B / C normalisation's backward (bf16 io, or together with the output gate):
+// the adjoint's fp32 run uses the fp32 layout up to its Delta / lambda sections (inner), then come the
+// normalised B and C rows in fp32 and their inverse RMS, fp32 copies of x and of the seed dy silu(z).
+struct BwdWsUp {
+    size_t inner, bn, cn, rb, rc, xf, dyf, total;
+};
+
+BwdWsUp bwd_ws_promoted(const ScanDims& d) {
+    ScanDims f = d;
+    f.io = M3_DTYPE_F32;
+    const BwdWs wi = bwd_ws_prep(f);
+    const size_t rows = (size_t)(d.batch * d.nheads) * (size_t)d.seqlen * (size_t)d.R;
+    BwdWsUp w{};
+    w.inner = wi.bn;
+    w.bn = wi.bn;
+    w.cn = w.bn + round256(sizeof(float) * rows * (size_t)d.dstate);
+    w.rb = w.cn + round256(sizeof(float) * rows * (size_t)d.dstate);
+    w.rc = w.rb + round256(sizeof(float) * rows);
+    w.xf = w.rc + round256(sizeof(float) * rows);
+    w.dyf = w.xf + round256(sizeof(float) * rows * (size_t)d.headdim);
+    w.total = w.dyf + round256(sizeof(float) * rows * (size_t)d.headdim);
+    return w;
+}
+
+size_t bwd_ws_prep_total(const ScanDims& d) {
+    const size_t a = bwd_ws_prep(d).total, b = bwd_ws_promoted(d).total;
+    return a > b ? a : b;
+}
+
+template <typename IO>
+cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
+                          const float* A, const float* lambda, const float* omega, const void* dy,
+                          const float* d_final, float* dx, float* dB, float* dC, float* ddt, float* dA,
+                          float* dlambda, float* domega, void* workspace, cudaStream_t stream, const BwdPrep& pp);
+
+// The B / C normalisation's backward for bf16 io or with the output gate: the adjoint runs in its fp32
+// instantiation on fp32 copies -- x, the seed dy silu(z), and the normalised rows written in fp32 -- so
+// that nothing the recurrence sees is rounded to bf16 beyond the inputs themselves; then the gate's dz
+// from the ungated output and the rows' backward on the raw rows, as in the direct path.
+template <typename IO>
+cudaError_t launch_bwd_promoted(const ScanDims& d, const void* x, const void* B, const void* C, const float* omega,
+                                const void* dy, const float* d_final, float* dx, float* dB, float* dC, float* ddt,
+                                float* dA, float* dlambda, float* domega, void* workspace, cudaStream_t stream,
+                                const BwdPrep& pp) {
+    cudaError_t e = cudaSuccess;
+    float* zs[] = {pp.bc.dB_gain, pp.bc.dC_gain};
+    for (float* q : zs)
+        if (q != nullptr && e == cudaSuccess) e = cudaMemsetAsync(q, 0, sizeof(float) * (size_t)d.dstate, stream);
+    float* zb[] = {pp.bc.dB_bias, pp.bc.dC_bias};
+    for (float* q : zb)
+        if (q != nullptr && e == cudaSuccess)
+            e = cudaMemsetAsync(q, 0, sizeof(float) * (size_t)(d.nheads * d.R * d.dstate), stream);
+    if (e != cudaSuccess) return e;
+    const BwdWsUp w = bwd_ws_promoted(d);
+    char* ws = static_cast<char*>(workspace);
+    const int64_t bh = d.batch * d.nheads, rows = bh * d.seqlen * d.R, nx = rows * d.headdim;
+    const int HR = (int)(d.nheads * d.R);
+    float* Bn = reinterpret_cast<float*>(ws + w.bn);
+    float* Cn = reinterpret_cast<float*>(ws + w.cn);
+    float* rb = reinterpret_cast<float*>(ws + w.rb);
+    float* rc = reinterpret_cast<float*>(ws + w.rc);
+    float* xf = reinterpret_cast<float*>(ws + w.xf);
+    float* dyf = reinterpret_cast<float*>(ws + w.dyf);
+    if (bh > 0 && d.seqlen > 0) {
+        const unsigned rbk = (unsigned)((rows + 7) / 8 < 148 * 16 ? (rows + 7) / 8 : 148 * 16);
+        bc_rows_forward<IO, float><<<rbk, 256, 0, stream>>>((const IO*)B, pp.bc.B_gain, pp.bc.B_bias, pp.bc.norm,
+                                                            pp.bc.eps, Bn, rb, rows, HR, (int)d.dstate);
+        bc_rows_forward<IO, float><<<rbk, 256, 0, stream>>>((const IO*)C, pp.bc.C_gain, pp.bc.C_bias, pp.bc.norm,
+                                                            pp.bc.eps, Cn, rc, rows, HR, (int)d.dstate);
+        const unsigned eb = (unsigned)((nx + 255) / 256 < 148 * 16 ? (nx + 255) / 256 : 148 * 16);
+        to_f32<IO><<<eb, 256, 0, stream>>>((const IO*)x, xf, nx);
+        gate_seed_f32<IO><<<eb, 256, 0, stream>>>((const IO*)dy, (const IO*)pp.z, dyf, nx);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    ScanDims f = d;
+    f.io = M3_DTYPE_F32;
+    BwdPrep p2 = pp;
+    p2.z = nullptr;
+    p2.y_pre = nullptr;
+    p2.dz = nullptr;
+    p2.bc.on = false;
+    e = launch_bwd_io<float>(f, xf, Bn, Cn, nullptr, nullptr, nullptr, omega, dyf, d_final, dx, dB, dC, ddt, dA,
+                             dlambda, domega, workspace, stream, p2);
+    if (e != cudaSuccess || bh == 0 || d.seqlen == 0) return e;
+    if (pp.z != nullptr) {
+        const unsigned gb = (unsigned)((nx + 255) / 256 < 148 * 16 ? (nx + 255) / 256 : 148 * 16);
+        bwd_gate_dz<IO><<<gb, 256, 0, stream>>>((const IO*)dy, (const IO*)pp.z, (const IO*)pp.y_pre, pp.dz, nx);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const int64_t BT = d.batch * d.seqlen;
+    const dim3 g2((unsigned)HR, (unsigned)((BT + 7) / 8 < 1024 ? (BT + 7) / 8 : 1024));
+    bc_rows_backward<IO><<<g2, 256, 0, stream>>>((const IO*)B, pp.bc.B_gain, rb, pp.bc.norm, dB, pp.bc.dB_gain,
+                                                 pp.bc.dB_bias, BT, HR, (int)d.dstate);
+    bc_rows_backward<IO><<<g2, 256, 0, stream>>>((const IO*)C, pp.bc.C_gain, rc, pp.bc.norm, dC, pp.bc.dC_gain,
+                                                 pp.bc.dC_bias, BT, HR, (int)d.dstate);
+    return cudaGetLastError();
+}
 
 template <typename IO>
 cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                           const float* A, const float* lambda, const float* omega, const void* dy,
                           const float* d_final, float* dx, float* dB, float* dC, float* ddt, float* dA,
                           float* dlambda, float* domega, void* workspace, cudaStream_t stream, const BwdPrep& pp) {
+    if (pp.on && pp.bc.on && (sizeof(IO) == 2 || pp.z != nullptr))
+        return launch_bwd_promoted<IO>(d, x, B, C, omega, dy, d_final, dx, dB, dC, ddt, dA, dlambda, domega,
+                                       workspace, stream, pp);
     const int Q = bwd_chunk(d.R);
     const bool gate = pp.on && pp.z != nullptr;
     const BwdLayout L = bwd_layout((int)d.headdim, (int)d.dstate, d.R, Q, (int)sizeof(IO), gate);
@@ -870,12 +983,12 @@ cudaError_t launch_bwd_io(const ScanDims& d, const void* x, const void* B, const
         void* Bn = ws + w.bn;
         void* Cn = ws + w.cn;
         const unsigned rbk = (unsigned)((rows + 7) / 8 < 148 * 16 ? (rows + 7) / 8 : 148 * 16);
-        bc_rows_forward<IO><<<rbk, 256, 0, stream>>>((const IO*)B, pp.bc.B_gain, pp.bc.B_bias, pp.bc.norm, pp.bc.eps,
-                                                     (IO*)Bn, reinterpret_cast<float*>(ws + w.rb), rows, HR,
-                                                     (int)d.dstate);
-        bc_rows_forward<IO><<<rbk, 256, 0, stream>>>((const IO*)C, pp.bc.C_gain, pp.bc.C_bias, pp.bc.norm, pp.bc.eps,
-                                                     (IO*)Cn, reinterpret_cast<float*>(ws + w.rc), rows, HR,
-                                                     (int)d.dstate);
+        bc_rows_forward<IO, IO><<<rbk, 256, 0, stream>>>((const IO*)B, pp.bc.B_gain, pp.bc.B_bias, pp.bc.norm,
+                                                         pp.bc.eps, (IO*)Bn, reinterpret_cast<float*>(ws + w.rb),
+                                                         rows, HR, (int)d.dstate);
+        bc_rows_forward<IO, IO><<<rbk, 256, 0, stream>>>((const IO*)C, pp.bc.C_gain, pp.bc.C_bias, pp.bc.norm,
+                                                         pp.bc.eps, (IO*)Cn, reinterpret_cast<float*>(ws + w.rc),
+                                                         rows, HR, (int)d.dstate);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         B = Bn;
         C = Cn;
@@ -990,6 +1103,12 @@ bool bwd_supported(const ScanDims& d) {
 size_t bwd_workspace_size(const ScanDims& d) { return bwd_ws(d).total; }
 
 size_t bwd_prep_workspace_size(const ScanDims& d) { return bwd_ws_prep_total(d); }
+
+bool bwd_bc_supported(const ScanDims& d) {
+    ScanDims f = d;
+    f.io = M3_DTYPE_F32;   // the promoted path runs the fp32 adjoint
+    return bwd_supported(d) && bwd_supported(f);
+}
 
 bool bwd_gate_supported(const ScanDims& d) {
     if (!bwd_supported(d)) return false;

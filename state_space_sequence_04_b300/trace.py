@@ -85,9 +85,8 @@ def run(wname: str):
         return tr[(cta * CHUNKS + i) * SLOTS + slot]
 
     # the last launch of the call (the full pass) is the one traced last: its values overwrite the state pass's
-    QR, P, N = w.chunk * w.rank if w.chunk * w.rank <= 128 else w.chunk, w.headdim, w.dstate
-    QR = min(QR, 128)
-    MM = 64 if QR == 64 else 128
+    QR, P, N = 64, w.headdim, w.dstate   # every chunk runs as 64-row sub-chunks (64 / R tokens)
+    MM = 64
     out = {"workload": wname, "launches_per_call": launches, "sm_ghz_traced": ghz, "consumer": {}, "rotate": {}}
     nchunk = []
     for cta in range(CTAS):

@@ -73,17 +73,28 @@ def test_plain_entry_rejects_before_any_launch(lib):
     assert f(*args, 1, 8, 2, 64, 128, 7, p, 1 << 30, None) == binding.M3_ERR_INVALID_ARG   # io dtype
 
 
-def test_prep_entry_rejects_bf16_normalisation_and_normalisation_with_gate(lib):
+def test_prep_entry_takes_bf16_normalisation_and_normalisation_with_gate(lib):
+    """The B / C normalisation's backward accepts bf16 io and the gate: the calls pass every argument
+    check and reach the launch, which an armed host-made launch failure turns into M3_ERR_CUDA before
+    any CUDA call."""
     keep, p = _fake()
     params = binding.PrepParams(p, 1, 1e-5, None, None, None, None, None)
     gated = binding.PrepParams(p, 1, 1e-5, None, None, None, None, p)
     f = lib.m3_scan_bwd_prep
     args = [p] * 7 + [1] + [p] * 2 + [p] * 13
 
-    def call(io, prm):
-        return f(*args, 1, 8, 2, 64, 128, io, ctypes.byref(prm), p, 1 << 30, None)
+    ws = (p + 255) & ~255   # a 256-byte-aligned stand-in for the workspace (never dereferenced here)
 
-    assert call(BF16, params) == binding.M3_ERR_UNSUPPORTED
-    assert call(F32, gated) == binding.M3_ERR_UNSUPPORTED
+    def call(io, prm):
+        return f(*args, 1, 8, 2, 64, 128, io, ctypes.byref(prm), ws, 1 << 30, None)
+
+    try:
+        assert lib.m3_test_inject(binding.M3_TEST_LAUNCH_FAILURE, 3) == 0
+        assert call(BF16, params) == binding.M3_ERR_CUDA
+        assert call(F32, gated) == binding.M3_ERR_CUDA
+        assert call(BF16, gated) == binding.M3_ERR_CUDA
+        assert lib.m3_test_inject(binding.M3_TEST_LAUNCH_FAILURE, 0) == 0
+    finally:
+        lib.m3_test_inject(0, 0)
     bad_eps = binding.PrepParams(p, 1, -1.0, None, None, None, None, None)
     assert call(F32, bad_eps) == binding.M3_ERR_INVALID_ARG

@@ -355,24 +355,46 @@ def test_bwd_bc_small_every_element():
         assert err < TOL_BWD["fp32"], f"{name}: {err:.2e}"
 
 
-def test_bwd_bc_unsupported_forms():
-    """The B / C normalisation's backward takes fp32 io and no gate: bf16 rows of the normalised B and C
-    would feed the adjoint kernel rounded (host-side checks, no launch)."""
-    for io, gate in (("bf16", False), ("fp32", True)):
-        w = synth.Workload("case", 1, 2, 8, 16, 8, 1, 64, io)
-        inp, bc = _bc_case(w, 91)
-        d = {k: inp[k].cuda().contiguous() for k in PREP_DEV}
-        bcd = {k: (v.cuda() if hasattr(v, "cuda") else v) for k, v in bc.items()}
-        z = torch.zeros_like(d["x"]) if gate else None
-        f = dict(dtype=torch.float32, device="cuda")
-        grads = {"dx": torch.empty(d["x"].shape, **f), "dB": torch.empty(d["B"].shape, **f),
-                 "dC": torch.empty(d["C"].shape, **f), "ddt_raw": torch.empty(d["dt_raw"].shape, **f),
-                 "dA": torch.empty(d["A"].shape, **f), "du": torch.empty(d["u"].shape, **f),
-                 "domega": torch.empty(d["omega"].shape, **f), "dz": torch.empty(d["x"].shape, **f)}
-        nbytes = binding.m3_scan_bwd_prep_workspace_size(1, 8, 2, 16, 8, 1, binding.io_code(d["x"].dtype))
-        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
-        args = [d[k] for k in ("x", "B", "C", "dt_raw", "A", "u", "omega")]
-        params = binding.prep_params(d["dt_bias"], bcd, z)
-        assert binding.m3_scan_bwd_prep(*args, 1, torch.zeros_like(d["x"]), None, grads, ws,
-                                        params) == binding.M3_ERR_UNSUPPORTED
-    torch.cuda.synchronize()
+@pytest.mark.parametrize("io,gate", [("bf16", False), ("fp32", True), ("bf16", True)])
+def test_bwd_bc_bf16_and_gate_every_element(io, gate):
+    """The B / C normalisation's backward with bf16 io and together with the output gate (the adjoint in
+    fp32 on fp32 copies): every gradient against the oracle's, dz and the gains' and biases' included."""
+    w = synth.Workload("case", 1, 2, 19, 4, 8, 2, 64, io)
+    inp, bc = _bc_case(w, 91)
+    z = synth.make_gate(tuple(inp["x"].shape), io=io, seed=92) if gate else None
+    gen = torch.Generator().manual_seed(93)
+    dy = torch.randn(inp["x"].shape, generator=gen).to(inp["x"].dtype)
+    dfin = torch.randn((1, 2, 8, 4), generator=gen)
+    got = _run_bc(inp, bc, 2, dy, dfin, z=z)
+    ref = grad.grad_fd(_bc_ref(inp, bc, z), oracle.f64(dy), oracle.f64(dfin), prep=True)
+    names = dict(PREP_NAMES, **{k: "d" + k for k in BC_KEYS})
+    if gate:
+        names["z"] = "dz"
+    for k, name in names.items():
+        tol = TOL_DZ[io] if k == "z" else TOL_BWD[io]
+        err = oracle.rel_err(got[name], ref[k])
+        assert err < tol, f"{name}: {err:.2e}"
+
+
+@pytest.mark.parametrize("io,gate", [("bf16", False), ("bf16", True)])
+def test_bwd_bc_bf16_larger_directional(io, gate):
+    """bf16, the forward's tensor-core shape (P = 64, N = 128), B / C normalisation alone and with the gate:
+    inner products of the gradients with random directions against the oracle's derivatives."""
+    Bt, H, T, P, N, R = 1, 4, 90, 64, 128, 1
+    w = synth.Workload("case", Bt, H, T, P, N, R, 64, io)
+    inp, bc = _bc_case(w, 95)
+    z = synth.make_gate(tuple(inp["x"].shape), io=io, seed=96) if gate else None
+    gen = torch.Generator().manual_seed(97)
+    dy = torch.randn(inp["x"].shape, generator=gen).to(inp["x"].dtype)
+    dfin = torch.randn((Bt, H, N, P), generator=gen)
+    got = _run_bc(inp, bc, R, dy, dfin, z=z)
+    ref = _bc_ref(inp, bc, z)
+    dy64, df64 = oracle.f64(dy), oracle.f64(dfin)
+    rng = np.random.default_rng(98)
+    keys = grad.PREP_INPUTS + BC_KEYS + (("z",) if gate else ())
+    for k in keys:
+        d = rng.standard_normal(ref[k].shape)
+        num = grad.directional(ref, k, d, dy64, df64, eps=1e-6, prep=True)
+        kern = float(np.sum(got[PREP_NAMES.get(k, "dz" if k == "z" else "d" + k)] * d))
+        tol = TOL_DZ[io] if k == "z" else TOL_BWD[io]
+        assert abs(kern - num) <= tol * max(1.0, abs(num)), (k, kern, num)

@@ -103,8 +103,8 @@ def test_scan_small(io, Bt, H, T, P, N, R, Q):
 
 # shapes the tensor-core path takes (bf16, P = 64, H % 4 == 0).  Few (batch, head)
 # sequences against many chunks make it cut each sequence into segments (state
-# pass, segment scan, full pass: 3 launches); MIMO chunks wider than 128 rows run
-# as sub-chunks of chunk/R tokens.
+# pass, segment scan, full pass: 3 launches); every chunk runs as sub-chunks of
+# 64/R tokens (64-row tiles).
 TC_CASES = [
     # Bt, H, T, P, N, R, Q
     (1, 4, 1, 64, 128, 1, 64),
@@ -117,8 +117,9 @@ TC_CASES = [
     (1, 4, 6400, 64, 128, 1, 64),     # segments of two chunks
     (1, 4, 150, 64, 64, 1, 64),
     (1, 4, 200, 64, 64, 4, 64),       # MIMO, N = 64: sub-chunks of 16 tokens
-    (2, 4, 333, 64, 128, 4, 128),     # MIMO, N = 128: sub-chunks of 32 tokens
+    (2, 4, 333, 64, 128, 4, 128),     # MIMO, N = 128: sub-chunks of 16 tokens
     (1, 4, 100, 64, 128, 4, 64),
+    (1, 4, 257, 64, 64, 2, 128),      # R = 2, N = 64: sub-chunks of 32 tokens
 ]
 
 
@@ -133,6 +134,27 @@ def test_scan_tensor_core_path(Bt, H, T, P, N, R, Q):
     y, fin = binding.scan_fwd(*[d[k] for k in KEYS], R, Q, workspace=ws)
     torch.cuda.synchronize()
     assert int(ws[:4].view(torch.int32).item()) == 0, "device-side wait gave up"
+    yr, hr, _ = oracle_full(inp)
+    assert_close(y, yr, TOL["bf16"], "y")
+    assert_close(fin, hr, TOL["bf16"], "final_state")
+
+
+@pytest.mark.parametrize("Bt,H,T,P,N,R,Q", [(1, 4, 300, 64, 128, 1, 64), (1, 4, 200, 64, 64, 4, 64),
+                                            (1, 4, 150, 64, 128, 4, 128), (1, 4, 180, 64, 128, 2, 64)])
+def test_scan_tensor_core_extreme_decay(Bt, H, T, P, N, R, Q):
+    """Decays far beyond fp32's range inside one chunk: every 7th token has Delta = 8 and head 0
+    has A = -16 (a log-decay of -128 for one token), so the tensor-core kernel's decay-to-chunk-end
+    factor of earlier tokens hits its 2^-100 clamp and the mask's factors reach 2^100."""
+    w = synth.Workload("case", Bt, H, T, P, N, R, Q, "bf16")
+    inp = synth.make_inputs(w, seed=T + 5 * R)
+    inp["dt"][:, ::7] = 8.0
+    inp["A"][0] = -16.0
+    d = to_dev(inp)
+    path, _ = binding.m3_scan_fwd_plan(Bt, T, H, P, N, R, Q, binding.M3_DTYPE_BF16)
+    assert path == 1
+    y, fin = binding.scan_fwd(*[d[k] for k in KEYS], R, Q)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y.float()).all() and torch.isfinite(fin).all()
     yr, hr, _ = oracle_full(inp)
     assert_close(y, yr, TOL["bf16"], "y")
     assert_close(fin, hr, TOL["bf16"], "final_state")
