@@ -359,12 +359,13 @@ def test_bwd_bc_small_every_element():
 def test_bwd_bc_bf16_and_gate_every_element(io, gate):
     """The B / C normalisation's backward with bf16 io and together with the output gate (the adjoint in
     fp32 on fp32 copies): every gradient against the oracle's, dz and the gains' and biases' included."""
-    w = synth.Workload("case", 1, 2, 19, 4, 8, 2, 64, io)
+    # P = 16: the gate's y_pre comes from the forward entry, whose CUDA-core path takes P >= 16
+    w = synth.Workload("case", 1, 2, 19, 16, 8, 2, 64, io)
     inp, bc = _bc_case(w, 91)
     z = synth.make_gate(tuple(inp["x"].shape), io=io, seed=92) if gate else None
     gen = torch.Generator().manual_seed(93)
     dy = torch.randn(inp["x"].shape, generator=gen).to(inp["x"].dtype)
-    dfin = torch.randn((1, 2, 8, 4), generator=gen)
+    dfin = torch.randn((1, 2, 8, 16), generator=gen)
     got = _run_bc(inp, bc, 2, dy, dfin, z=z)
     ref = grad.grad_fd(_bc_ref(inp, bc, z), oracle.f64(dy), oracle.f64(dfin), prep=True)
     names = dict(PREP_NAMES, **{k: "d" + k for k in BC_KEYS})
