@@ -93,7 +93,8 @@ __device__ long long g_m3_trace_clk[kTraceCtas * 4];
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-template <int NS, int R, int Q>
+// FULL = false is the state pass's layout: no C tile, no bf16 copy of the carry, only the carry in TMEM.
+template <int NS, int R, int Q, bool FULL = true>
 struct Cfg {
     static constexpr int P = 64;                 // head dim (one 128-byte swizzle panel of bf16)
     static constexpr int QR = Q * R;             // rows of the chunk
@@ -110,8 +111,11 @@ struct Cfg {
     static constexpr int X_BYTES = QR * 128;
     static constexpr int BC_BYTES = NPAN * QR * 128;
     static constexpr int SL_BYTES = QR * QR * 2;
-    static_assert(SL_BYTES <= BC_BYTES, "the masked scores are written over the chunk's B tile");
-    static constexpr int STG_TILE = 2 * BC_BYTES + X_BYTES;      // C | B | X of one stage
+    static_assert(!FULL || SL_BYTES <= BC_BYTES, "the masked scores are written over the chunk's B tile");
+    // one stage: C | B | X, or B | X in the state pass (B is followed by X either way: with NS = 64
+    // the carry MMA's second 64-row half reads X's bytes and its results go unused)
+    static constexpr int STG_B = FULL ? BC_BYTES : 0, STG_X = STG_B + BC_BYTES;
+    static constexpr int STG_TILE = STG_X + X_BYTES;
     static constexpr int BOX_BYTES = 16 * (Q + 1);                // dt / lambda box {4 heads, Q+1 tokens}
     static constexpr int BOX_STRIDE = align_up(BOX_BYTES, 128);
     // rotate-phase mapping: pair group jg (4 pairs = 16 bytes of a row), token group tg
@@ -130,7 +134,7 @@ struct Cfg {
     static constexpr int CO_BYTES = align_up((5 * Q + NS / 2 + 2) * 4, 16);
 
     static constexpr int OFF_HB = 2 * STG_TILE;
-    static constexpr int OFF_BOX = OFF_HB + NS * 128;             // [stage][dt | lambda]
+    static constexpr int OFF_BOX = OFF_HB + (FULL ? NS * 128 : 0);   // [stage][dt | lambda]
     static constexpr int OFF_PART = OFF_BOX + 4 * BOX_STRIDE;     // only when not in the boxes
     static constexpr int OFF_CO = OFF_PART + (PART_IN_BOX ? 0 : align_up(PART_BYTES, 16));
     static constexpr int OFF_RPRIV = OFF_CO + 2 * CO_BYTES;       // w[Q], warp sums[4]
@@ -140,14 +144,14 @@ struct Cfg {
     static constexpr int MIN_BLOCKS = 2 * (SMEM + 1024) <= 233472 ? 2 : 1;
     static constexpr int TX_BOX = 2 * BOX_BYTES, TX_X = X_BYTES;
 
-    // TMEM columns
+    // TMEM columns (the state pass holds the carry alone)
     static constexpr int T_S = 0;
     static constexpr int T_YI = QR;
     static constexpr int T_Y = QR + P;
-    static constexpr int T_H = QR + 2 * P;
-    static constexpr int TMEM_COLS = (QR + 3 * P) <= 256 ? 256 : 512;
+    static constexpr int T_H = FULL ? QR + 2 * P : 0;
+    static constexpr int TMEM_COLS = !FULL ? P : (QR + 3 * P) <= 256 ? 256 : 512;
     static_assert(SMEM <= 232448, "shared memory over the 227 KB per-CTA limit");
-    static_assert(!M64 || MIN_BLOCKS == 2, "64-row tiles are laid out for two CTAs per SM");
+    static_assert(FULL ? !M64 || MIN_BLOCKS == 2 : MIN_BLOCKS == 2, "64-row tiles and the state pass are laid out for two CTAs per SM");
 };
 
 struct TcArgs {
@@ -386,13 +390,13 @@ __device__ __forceinline__ void mask_block(float* v, int cb, int t, float ct, fl
 // rotation; PM & 4 the output gate y * silu(z) in the epilogue.  PM == kTestHook
 // is the plain kernel with a simulated timeout (the failure-path test).
 template <int NS, int R, int Q, bool FULL, int PM>
-__global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+__global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                          const __grid_constant__ CUtensorMap tm_B,
                                                          const __grid_constant__ CUtensorMap tm_C,
                                                          const __grid_constant__ CUtensorMap tm_dt,
                                                          const __grid_constant__ CUtensorMap tm_lam, TcArgs args,
                                                          const ExtArgs<PM> ext) {
-    using K = Cfg<NS, R, Q>;
+    using K = Cfg<NS, R, Q, FULL>;
     constexpr bool HOOK = PM == kTestHook;
     constexpr bool PREP = !HOOK && (PM & 1) != 0, BC = !HOOK && (PM & 2) != 0, GATE = !HOOK && (PM & 4) != 0;
     constexpr int P = K::P, QR = K::QR, NP2 = NS / 2, NG = K::NG, TG = K::TG, TPG = K::TPG;
@@ -414,9 +418,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q>::MIN_BLOCKS)) scan_tc_kern
     const int c_begin = seg * args.L;
     const int nl = min(args.nc, c_begin + args.L) - c_begin;   // chunks of this segment (>= 1)
 
-    auto tile_c = [&](int s) { return sm + s * K::STG_TILE; };
-    auto tile_b = [&](int s) { return sm + s * K::STG_TILE + K::BC_BYTES; };
-    auto tile_x = [&](int s) { return sm + s * K::STG_TILE + 2 * K::BC_BYTES; };
+    auto tile_c = [&](int s) { return sm + s * K::STG_TILE; };   // full pass only
+    auto tile_b = [&](int s) { return sm + s * K::STG_TILE + K::STG_B; };
+    auto tile_x = [&](int s) { return sm + s * K::STG_TILE + K::STG_X; };
     auto box_dt = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_BOX + (2 * s) * K::BOX_STRIDE); };
     auto box_lam = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_BOX + (2 * s + 1) * K::BOX_STRIDE); };
     auto coef = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_CO + s * K::CO_BYTES); };
@@ -1203,8 +1207,14 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr,
 // GPU, each sequence is cut into S segments of L chunks so that the machine
 // fills up; a state pass gives every segment's carry from a zero start, the
 // segment scan (m3_state_passing's kernel) turns those into the state entering
-// each segment, and the full pass starts each segment from it.
+// each segment, and the full pass starts each segment from it.  The state pass
+// has no scores or outputs, so its tiles can be longer at two CTAs per SM: with
+// R >= 2 it takes chunks of 128 / R tokens (128 rows), twice the full pass's,
+// and segments hold an even number of the full pass's chunks.
 constexpr int kPlanSMs = 148;   // SMs of the B300 the plan is sized for (fixed: the workspace size must not depend on the device)
+
+template <int R, int Q>
+constexpr int state_pass_q() { return R >= 2 && 2 * Q * R <= 128 ? 2 * Q : Q; }
 
 struct SegPlan {
     int S, L, nc;
@@ -1213,6 +1223,7 @@ struct SegPlan {
 template <int NS, int R, int Q>
 SegPlan seg_plan(const ScanDims& d) {
     using K = Cfg<NS, R, Q>;
+    constexpr int F = state_pass_q<R, Q>() / Q;
     SegPlan p;
     p.nc = (int)((d.seqlen + Q - 1) / Q);
     const int64_t seqs = d.batch * d.nheads, slots = (int64_t)kPlanSMs * K::MIN_BLOCKS;
@@ -1220,6 +1231,7 @@ SegPlan seg_plan(const ScanDims& d) {
     if (S > p.nc) S = p.nc;
     if (S < 1) S = 1;
     p.L = (int)((p.nc + S - 1) / S);
+    if (S > 1) p.L = (p.L + F - 1) / F * F;   // whole state-pass chunks per segment
     p.S = (p.nc + p.L - 1) / p.L;   // no empty segment
     return p;
 }
@@ -1244,38 +1256,54 @@ SegWs seg_ws(const ScanDims& d) {
     return w;
 }
 
+// The five tensor maps of chunks of QT tokens: x, B, C (boxes of QT tokens x R ranks x 64
+// channels, 128-byte swizzle) and dt, lambda (boxes of 4 heads x QT+1 tokens).
+struct Maps {
+    CUtensorMap x, B, C, dt, lam;
+};
+
+template <int R>
+bool make_maps(Maps& m, const ScanDims& d, int QT, const void* x, const void* B, const void* C, const float* dt,
+               const float* lambda) {
+    const cuuint64_t Bt = d.batch, T = d.seqlen, H = d.nheads, P = d.headdim, N = d.dstate;
+    {
+        cuuint64_t dims[5] = {P, (cuuint64_t)R, H, T, Bt};
+        cuuint64_t str[4] = {P * 2, R * P * 2, H * R * P * 2, T * H * R * P * 2};
+        cuuint32_t box[5] = {64, (cuuint32_t)R, 1, (cuuint32_t)QT, 1};
+        if (!make_map(&m.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, x, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+    }
+    {
+        cuuint64_t dims[5] = {N, (cuuint64_t)R, H, T, Bt};
+        cuuint64_t str[4] = {N * 2, R * N * 2, H * R * N * 2, T * H * R * N * 2};
+        cuuint32_t box[5] = {64, (cuuint32_t)R, 1, (cuuint32_t)QT, 1};
+        if (!make_map(&m.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+        if (!make_map(&m.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, C, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+    }
+    {
+        cuuint64_t dims[3] = {H, T, Bt};
+        cuuint64_t str[2] = {H * 4, T * H * 4};
+        cuuint32_t box[3] = {4, (cuuint32_t)(QT + 1), 1};
+        if (!make_map(&m.dt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dt, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
+        if (!make_map(&m.lam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, lambda, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
+    }
+    return true;
+}
+
 template <int NS, int R, int Q, int PM>
 cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const void* C, const float* dt,
                        const float* A, const float* lambda, const float* omega, void* y, float* final_state,
                        void* workspace, const Prep& prep, cudaStream_t stream) {
     using K = Cfg<NS, R, Q>;
-    const cuuint64_t Bt = d.batch, T = d.seqlen, H = d.nheads, P = d.headdim, N = d.dstate;
-    CUtensorMap mx, mB, mC, mdt, mlam;
-    {
-        cuuint64_t dims[5] = {P, (cuuint64_t)R, H, T, Bt};
-        cuuint64_t str[4] = {P * 2, R * P * 2, H * R * P * 2, T * H * R * P * 2};
-        cuuint32_t box[5] = {64, (cuuint32_t)R, 1, (cuuint32_t)Q, 1};
-        if (!make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, x, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorInvalidValue;
-    }
-    {
-        cuuint64_t dims[5] = {N, (cuuint64_t)R, H, T, Bt};
-        cuuint64_t str[4] = {N * 2, R * N * 2, H * R * N * 2, T * H * R * N * 2};
-        cuuint32_t box[5] = {64, (cuuint32_t)R, 1, (cuuint32_t)Q, 1};
-        if (!make_map(&mB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorInvalidValue;
-        if (!make_map(&mC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, C, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorInvalidValue;
-    }
-    {
-        cuuint64_t dims[3] = {H, T, Bt};
-        cuuint64_t str[2] = {H * 4, T * H * 4};
-        cuuint32_t box[3] = {4, (cuuint32_t)(Q + 1), 1};
-        if (!make_map(&mdt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dt, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
-        if (!make_map(&mlam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, lambda, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
-    }
+    constexpr int QS = state_pass_q<R, Q>();
+    using KS = Cfg<NS, R, QS, false>;
+    const cuuint64_t P = d.headdim;
+    Maps mf;
+    if (!make_maps<R>(mf, d, Q, x, B, C, dt, lambda)) return cudaErrorInvalidValue;
     const SegPlan pl = seg_plan<NS, R, Q>(d);
     const SegWs ws = seg_ws<NS, R, Q>(d);
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
@@ -1305,15 +1333,21 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
         float* segLD = reinterpret_cast<float*>(wsb + ws.ld);
         float* segTH = reinterpret_cast<float*>(wsb + ws.th);
         float* last = reinterpret_cast<float*>(wsb + ws.last);
+        Maps ms;
+        if (QS == Q) ms = mf;
+        else if (!make_maps<R>(ms, d, QS, x, B, C, dt, lambda)) return cudaErrorInvalidValue;
         TcArgs a1 = args;
+        // the same segments in the state pass's chunks (segments 0 .. S-2 hold L whole chunks of Q tokens)
+        a1.nc = (int)((d.seqlen + QS - 1) / QS);
+        a1.L = pl.L * Q / QS;
         a1.nseg = pl.S - 1;
         a1.seg_U = segU;
         a1.seg_ld = segLD;
         a1.seg_th = segTH;
-        auto k1 = scan_tc_kernel<NS, R, Q, false, PM>;
-        e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
+        auto k1 = scan_tc_kernel<NS, R, QS, false, PM>;
+        e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, KS::SMEM);
         if (e != cudaSuccess) return e;
-        k1<<<(unsigned)(seqs * a1.nseg), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, a1, ext);
+        k1<<<(unsigned)(seqs * a1.nseg), KS::kThreads, KS::SMEM, stream>>>(ms.x, ms.B, ms.C, ms.dt, ms.lam, a1, ext);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // segment carries -> the state entering each segment (in place), and into the last one
         e = launch_state_passing(segU, segLD, segTH, nullptr, last, 1, seqs, pl.S - 1, NS, (int64_t)P, stream);
@@ -1325,7 +1359,7 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
     auto kern = scan_tc_kernel<NS, R, Q, true, PM>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(seqs * pl.S), K::kThreads, K::SMEM, stream>>>(mx, mB, mC, mdt, mlam, args, ext);
+    kern<<<(unsigned)(seqs * pl.S), K::kThreads, K::SMEM, stream>>>(mf.x, mf.B, mf.C, mf.dt, mf.lam, args, ext);
     return cudaGetLastError();
 }
 

@@ -104,7 +104,8 @@ def test_scan_small(io, Bt, H, T, P, N, R, Q):
 # shapes the tensor-core path takes (bf16, P = 64, H % 4 == 0).  Few (batch, head)
 # sequences against many chunks make it cut each sequence into segments (state
 # pass, segment scan, full pass: 3 launches); every chunk runs as sub-chunks of
-# 64/R tokens (64-row tiles).
+# 64/R tokens (64-row tiles), and with R >= 2 the state pass takes chunks of
+# 128/R tokens (segments of an even number of sub-chunks).
 TC_CASES = [
     # Bt, H, T, P, N, R, Q
     (1, 4, 1, 64, 128, 1, 64),
@@ -120,6 +121,8 @@ TC_CASES = [
     (2, 4, 333, 64, 128, 4, 128),     # MIMO, N = 128: sub-chunks of 16 tokens
     (1, 4, 100, 64, 128, 4, 64),
     (1, 4, 257, 64, 64, 2, 128),      # R = 2, N = 64: sub-chunks of 32 tokens
+    (1, 4, 9001, 64, 128, 4, 64),     # segments of 8 sub-chunks (4 state-pass chunks), ragged end
+    (1, 4, 5000, 64, 64, 2, 64),      # R = 2: segments of 4 sub-chunks (2 state-pass chunks)
 ]
 
 
