@@ -73,11 +73,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Phase trace of a diagnostic build (compiled with -DM3_TRACE; the product build has none of it):
 // clock64 at the phase boundaries of the first kTraceChunks chunks of the first kTraceCtas CTAs.
 // Per (CTA, chunk): slots 0-15 the consumer group (thread 0; slots 11-12 thread 32), 16-31 the
-// rotate group (thread 128).  g_m3_trace_clk holds (globaltimer, clock64) at the start and the end
-// of each traced CTA, to turn cycles into time.
-constexpr int kTraceCtas = 4, kTraceChunks = 64, kTraceSlots = 32;
+// rotate group (thread 128).  g_m3_trace_clk holds, for each of the first kClkCtas CTAs of a launch,
+// (globaltimer, clock64) at its start and its end and its SM's id: cycles into time, and the spread
+// of CTA durations by SM.
+constexpr int kTraceCtas = 4, kTraceChunks = 64, kTraceSlots = 32, kClkCtas = 4096, kClkSlots = 6;
 __device__ long long g_m3_trace[kTraceCtas * kTraceChunks * kTraceSlots];
-__device__ long long g_m3_trace_clk[kTraceCtas * 4];
+__device__ long long g_m3_trace_clk[kClkCtas * kClkSlots];
 #define M3_TRACE_BY(thread, i, slot)                                                                    \
     do {                                                                                                \
         if (blockIdx.x < kTraceCtas && (i) < kTraceChunks && threadIdx.x == (thread))                   \
@@ -407,9 +408,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 #ifdef M3_TRACE
-    if (tid == 0 && blockIdx.x < kTraceCtas) {
-        g_m3_trace_clk[blockIdx.x * 4 + 0] = (long long)globaltimer_ns();
-        g_m3_trace_clk[blockIdx.x * 4 + 1] = clock64();
+    if (tid == 0 && blockIdx.x < kClkCtas) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        g_m3_trace_clk[blockIdx.x * kClkSlots + 0] = (long long)globaltimer_ns();
+        g_m3_trace_clk[blockIdx.x * kClkSlots + 1] = clock64();
+        g_m3_trace_clk[blockIdx.x * kClkSlots + 4] = smid;
     }
 #endif
     const int bh = blockIdx.x / args.nseg, seg = blockIdx.x % args.nseg;
@@ -1168,9 +1172,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, K::TMEM_COLS);
 #ifdef M3_TRACE
-    if (tid == 0 && blockIdx.x < kTraceCtas) {
-        g_m3_trace_clk[blockIdx.x * 4 + 2] = (long long)globaltimer_ns();
-        g_m3_trace_clk[blockIdx.x * 4 + 3] = clock64();
+    if (tid == 0 && blockIdx.x < kClkCtas) {
+        g_m3_trace_clk[blockIdx.x * kClkSlots + 2] = (long long)globaltimer_ns();
+        g_m3_trace_clk[blockIdx.x * kClkSlots + 3] = clock64();
     }
 #endif
 }
@@ -1435,10 +1439,10 @@ cudaError_t launch_scan_tc(const ScanDims& d, const void* x, const void* B, cons
 
 #ifdef M3_TRACE
 // Diagnostic build only: copy out (or clear, dst = NULL) the phase trace; n = number of int64 entries of
-// the trace (kTraceCtas * kTraceChunks * kTraceSlots) followed by the clock pairs (kTraceCtas * 4).
+// the trace (kTraceCtas * kTraceChunks * kTraceSlots) followed by the per-CTA clocks (kClkCtas * kClkSlots).
 extern "C" __attribute__((visibility("default"))) int m3_trace_read(long long* dst, int n) {
     using namespace m3;
-    constexpr int nt = kTraceCtas * kTraceChunks * kTraceSlots, nc = kTraceCtas * 4;
+    constexpr int nt = kTraceCtas * kTraceChunks * kTraceSlots, nc = kClkCtas * kClkSlots;
     if (n != nt + nc) return M3_ERR_INVALID_ARG;
     if (dst == nullptr) {
         static long long zeros[nt + nc] = {};

@@ -31,12 +31,13 @@ import torch  # noqa: E402
 from state_space_sequence_04_b300 import binding, build, synth  # noqa: E402
 
 CTAS, CHUNKS, SLOTS = 4, 64, 32          # kTraceCtas, kTraceChunks, kTraceSlots of the kernel
+CLK_CTAS, CLK_SLOTS = 4096, 6            # kClkCtas, kClkSlots: per CTA (t0 ns, clk0, t1 ns, clk1, SM id, -)
 SMS = 148
 KEYS = ("x", "B", "C", "dt", "A", "lam", "omega")
-# slot names: consumer thread 0 (0-9), observers (11, 12), rotate thread 128 (16-24)
-CONSUMER = ["top", "stage ready (rot_done + barrier)", "H+= and Yi issued", "S and H+= waited",
-            "mask + barrier", "Y issued (+ next S)", "Y waited", "output stored", "next coefficients",
-            "state step + barrier"]
+# slot names: consumer thread 0 (0-9, in the time order below), observers (11, 12), rotate thread 128 (16-24)
+CONSUMER = [(0, "top"), (1, "stage ready (rot_done + barrier)"), (2, "H+= and Yi issued"), (3, "S and H+= waited"),
+            (4, "mask + barrier"), (5, "Y issued (+ next S)"), (6, "Y waited"), (7, "output stored"),
+            (8, "next coefficients"), (9, "state step + barrier")]
 ROTATE = ["top", "dt/lambda boxes", "coefficients + angle partial sums", "C/B landed", "rotation (C~, B'')",
           "barrier + next boxes issued", "-", "-", "barrier"]
 
@@ -55,7 +56,7 @@ def run(wname: str):
     lib = binding.load()
     lib.m3_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int]
     lib.m3_trace_read.restype = ctypes.c_int
-    n = CTAS * CHUNKS * SLOTS + CTAS * 4
+    n = CTAS * CHUNKS * SLOTS + CLK_CTAS * CLK_SLOTS
     w = synth.WORKLOADS[wname]
     d = synth.make_inputs(w, seed=0, device="cuda")
     args = [d[k] for k in KEYS]
@@ -76,10 +77,23 @@ def run(wname: str):
     binding._check(lib.m3_trace_read(ctypes.addressof(buf), n), "m3_trace_read")
     tr = list(buf)
     clk = tr[CTAS * CHUNKS * SLOTS:]
-    # cycles per ns from the traced CTAs' (globaltimer, clock64) pairs
-    rates = [(clk[4 * c + 3] - clk[4 * c + 1]) / (clk[4 * c + 2] - clk[4 * c + 0])
-             for c in range(CTAS) if clk[4 * c + 2] > clk[4 * c + 0]]
-    ghz = statistics.median(rates)
+    cta = [clk[k * CLK_SLOTS:(k + 1) * CLK_SLOTS] for k in range(CLK_CTAS)]
+    ran = [c for c in cta if c[2] > c[0] > 0]
+    # cycles per ns from the CTAs' (globaltimer, clock64) pairs
+    ghz = statistics.median((c[3] - c[1]) / (c[2] - c[0]) for c in ran[:CTAS])
+    # CTA durations of the last launch of the call, by how many of its CTAs shared the SM
+    t0 = min(c[0] for c in ran)
+    per_sm = {}
+    for c in ran:
+        per_sm.setdefault(c[4], []).append(c)
+    spread = {}
+    for k in sorted({len(v) for v in per_sm.values()}):
+        d = [(c[2] - c[0]) / 1e3 for v in per_sm.values() if len(v) == k for c in v]
+        e = [(c[2] - t0) / 1e3 for v in per_sm.values() if len(v) == k for c in v]
+        spread[f"{k}_per_sm"] = {"sms": sum(1 for v in per_sm.values() if len(v) == k), "ctas": len(d),
+                                 "duration_us_min_med_max": [min(d), statistics.median(d), max(d)],
+                                 "end_us_max": max(e)}
+    pair_gap = [abs((v[0][2] - v[0][0]) - (v[1][2] - v[1][0])) / 1e3 for v in per_sm.values() if len(v) == 2]
 
     def at(cta, i, slot):
         return tr[(cta * CHUNKS + i) * SLOTS + slot]
@@ -87,7 +101,9 @@ def run(wname: str):
     # the last launch of the call (the full pass) is the one traced last: its values overwrite the state pass's
     QR, P, N = 64, w.headdim, w.dstate   # every chunk runs as 64-row sub-chunks (64 / R tokens)
     MM = 64
-    out = {"workload": wname, "launches_per_call": launches, "sm_ghz_traced": ghz, "consumer": {}, "rotate": {}}
+    out = {"workload": wname, "launches_per_call": launches, "sm_ghz_traced": ghz, "consumer": {}, "rotate": {},
+           "ctas": {"count": len(ran), "span_us": (max(c[2] for c in ran) - t0) / 1e3, "by_sm_load": spread,
+                    "pair_duration_gap_us_median": statistics.median(pair_gap) if pair_gap else None}}
     nchunk = []
     for cta in range(CTAS):
         k = 0
@@ -98,8 +114,9 @@ def run(wname: str):
     if not use:
         raise SystemExit("no traced chunks")
     for j in range(1, len(CONSUMER)):
-        dts = [at(c, i, j) - at(c, i, j - 1) for c, i in use if at(c, i, j) and at(c, i, j - 1)]
-        out["consumer"][CONSUMER[j]] = statistics.median(dts) if dts else None
+        (a, _), (b, name) = CONSUMER[j - 1], CONSUMER[j]
+        dts = [at(c, i, b) - at(c, i, a) for c, i in use if at(c, i, b) and at(c, i, a)]
+        out["consumer"][name] = statistics.median(dts) if dts else None
     for j in range(1, len(ROTATE)):
         dts = [at(c, i, 16 + j) - at(c, i, 16 + j - 1) for c, i in use]
         out["rotate"][ROTATE[j]] = statistics.median(dts)
