@@ -130,9 +130,10 @@ def decode_bytes(b: int, H: int, P: int, N: int, R: int, io: str = "bf16") -> in
 
 
 def profiled_traffic(kernel_source: str, profile: str):
-    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) that an ncu
-    capture recorded in ``profile`` (a summary under profiles/), or None when the kernel
-    source has changed since: the summary names the source file's sha256 at capture time."""
+    """DRAM bytes per call (dram__bytes_read.sum + dram__bytes_write.sum summed over the call's
+    launches of the kernel; one launch when the call has one) that an ncu capture recorded in
+    ``profile`` (a summary under profiles/), or None when the kernel source has changed since:
+    the summary names the source file's sha256 at capture time."""
     import hashlib
     try:
         src = open(os.path.join(ROOT, kernel_source), "rb").read()
@@ -142,13 +143,13 @@ def profiled_traffic(kernel_source: str, profile: str):
     digest = hashlib.sha256(src).hexdigest()
     fields = {}
     for line in text.splitlines():
-        if ":" in line and line.lstrip("-* ").split(":", 1)[0].strip() in ("source sha256", "traffic per launch bytes"):
+        if ":" in line and line.lstrip("-* ").split(":", 1)[0].strip() in ("source sha256", "traffic per call bytes"):
             k, v = line.lstrip("-* ").split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
     if fields.get("source sha256") != digest:
         return None
     try:
-        return int(fields["traffic per launch bytes"])
+        return int(fields["traffic per call bytes"])
     except (KeyError, ValueError):
         return None
 
@@ -297,6 +298,7 @@ def prefill_leg(binding, w, d, args, stream, dist, device, local, pk, ws, rank, 
                      # the committed ncu summary of this workload's dominant kernel (only for the named sizes)
                      "traffic": (profiled_traffic(src, f"{src.rsplit('/', 1)[1][:-3]}_{w.name}.md")
                                  if synth.WORKLOADS.get(w.name) == w else None),
+                     "traffic_scope": "ncu DRAM read + write bytes per call, over all its launches",
                      "kernel": "m3_scan_fwd (" + ("tensor-core" if path == 1 else "CUDA-core") +
                                f" path, {launches} launches per call)",
                      "algorithmic_bytes_per_call": nbytes, "peak_source": pk["source"],

@@ -4,58 +4,58 @@
 // The chunked algorithm of "Mamba-3: Improved Sequence Modeling using State
 // Space Principles" (section 3.3; decay x two-band mask of section 3.1.3 /
 // Eq. 7; rotary form of Propositions 3-4), fused into one kernel: one CTA owns
-// one (batch, head) sequence and walks its chunks in order, carrying the
-// fp32 N x P state in TMEM, so no chunk state ever goes to HBM.  Per chunk
-// c = tokens [c0, c0+Q) (rows ordered (token, rank), QR = Q*R <= 128):
+// one (batch, head) sequence, or one segment of it, and walks its chunks in
+// order, carrying the fp32 N x P state in TMEM, so no chunk state ever goes to
+// HBM.  Per chunk c = tokens [c0, c0+Q) (rows ordered (token, rank), QR = Q*R):
 //
 //   coefficients   l_t = dt_t A, cum_t = sum_{k<=t} l_k (chunk-local),
 //                  gamma_t = lambda_t dt_t, w_s = gamma_s + (1-lambda_{s+1}) dt_{s+1},
-//                  rho_t = gamma_t / w_t (0 when w_t = 0; w_t >= gamma_t >= 0)
-//   rotation       Psi_t = sum_{k<=t} dt_k omega_k (chunk-local),
-//                  C~ = R(-Psi) C,  B' = w R(-Psi) B   (in place in shared memory)
-//                  X^ = exp(cum_end - cum_s) X          (separate buffer)
-//   batch 1        H += B'^T X^                        (chunk state onto the carry)
-//                  S  = C~ B'^T                       (= S_ts w_s)
-//   mask           SL_ts = S_ts exp(cum_t - cum_s) for s < t, S_tt rho_t, 0 for s > t
-//                  (bf16, written over X^, which batch 1 has consumed)
-//   batch 2        Yi = C~ Hb_{c-1}                    (inter-chunk readout)
-//                  Y  = SL X
+//                  rho_t = gamma_t / w_t (0 when w_t = 0; w_t >= gamma_t >= 0),
+//                  g_s = log2 of exp(cum_end - cum_s), clamped at -100
+//   rotation       Phi_t = the angle sum_k dt_k omega_k since the segment start (mod 2 pi),
+//                  C~ = R(-Phi) C,  B'' = 2^g w R(-Phi) B   (in place in shared memory)
+//   batch 1        H += B''^T X                       (chunk state onto the carry)
+//                  Yi = C~ Hb_{c-1}                   (inter-chunk readout)
+//   scores         S  = C~ B''^T
+//   mask           SL_ts = S_ts 2^(cum2_t - cum2_s - g_s) for s < t, S_tt rho_t 2^-g_t, 0 for s > t
+//                  (cum2 = cum log2 e; bf16, written over the B'' tile, which the MMAs have consumed)
+//   batch 2        Y  = SL X
 //   output         y_t = Y_t + exp(cum_t) Yi_t
-//   state          H_c = exp(cum_end(c+1)) R(Theta_c) H,  Hb_c = bf16(R(Theta_c) H)
+//   state          Hb_c = bf16(H),  H <- exp(cum_end(c+1)) H
 //
-// The carry H entering batch 1 of chunk c is exp(cum_end(c)) R(Theta_{c-1}) H_{c-1}
-// (the decay of chunk c applied ahead of time by the previous state step), so
-// that the chunk-state MMA accumulates straight onto it and
-// H_c = R(Theta_c) (exp(cum_end) H_{c-1} + U_c) needs one pass over TMEM.
-// H is the physical-frame state plus the pending delayed write of the chunk's
-// last token (its w uses the next token's lambda, dt; zero past the end), so
-// H after the last chunk is the true final state h_{T-1}.
+// The carry stays in the segment's rotating frame (B and C carry the phase since
+// the segment start), where the transition between chunks is the scalar decay
+// alone; the segment's final state is rotated back by R(Phi_end).  The decay
+// to the chunk end rides on B'' (2^g), so the chunk-state MMA reads the raw X
+// tile, and the mask divides it out again (every mask factor <= 2^100).  w_s
+// takes the next token's lambda and dt (zero past the end), so the carry after
+// a chunk already holds the delayed half of its last token's trapezoid, and
+// after the last chunk it is the final state h_{T-1}.
 //
 // Warp roles (256 threads): warps 0-3 "consumer" (mask, state, output; thread
-// 0 issues every MMA and the C/B and X loads), warps 4-7 "rotate"
-// (coefficients, angles, rotation, X^, the dt/lambda loads), which run one
-// chunk ahead of the consumer on the other shared-memory stage.  Every wait is
-// bounded: on timeout the kernel records M3_ERR_TIMEOUT in the status word,
-// drains its copies and MMAs and exits.
+// 0 issues every MMA and the C/B and X loads), warps 4-7 "rotate" (coefficients,
+// angles, rotation, the dt/lambda loads), which run one chunk ahead of the
+// consumer on the other shared-memory stage.
+// Every wait is bounded: on timeout the kernel records M3_ERR_TIMEOUT in the
+// status word, drains its copies and MMAs and exits.
 //
 // Kernel modes (template bitmask PM) for the pre-activation entry point: bit 0
 // takes Delta and lambda as pre-activations and one decay generator per token,
 // bit 1 RMS-normalises and biases B and C in the rotation, bit 2 gates the
-// output; mode 0 is the plain kernel.
+// output; mode 0 is the plain kernel.  FULL = false is the state pass of a
+// segmented call: the rotated, scaled B and the chunk-state MMA only.
 //
 // MMA operand layouts (all 128-byte swizzled, bf16):
-//   C~   A, K-major  (rows (t,r), K = n)     B'  B, K-major (rows (s,r), K = n)
+//   C~   A, K-major  (rows (t,r), K = n)     B''  B, K-major (rows (s,r), K = n)
 //   SL   A, K-major  (rows (t,r), K = (s,r')) X   B, MN-major (K = (s,r'), N = p)
-//   Hb   B, MN-major (K = n, N = p)          B'^T A, MN-major (M = n, K = (s,r'))
-//   X^   B, MN-major (K = (s,r'), N = p)
+//   Hb   B, MN-major (K = n, N = p)          B''^T A, MN-major (M = n, K = (s,r'))
 // When QR = 64 the score, inter-readout and output MMAs run with M = 64: row r
 // of those accumulators sits in TMEM lane 32 (r / 16) + r % 16, and every
 // consumer thread takes half a row (16-lane loads, two column halves), so all
 // four consumer warps share the mask and the output.  With QR = 128 they run
 // with M = 128 (row r in lane r).  The chunk-state MMA always has M = 128
 // (state rows n); with N = 64 its rows 64..127 read the next QR*128 bytes of
-// shared memory (inside this CTA's allocation) and are never read.  SL is
-// written over X^ (dead once batch 1 is done; C~ is still read by batch 2).
+// shared memory (X, inside this CTA's allocation) and are never read.
 #include <cuda.h>
 
 #include "m3_common.cuh"
@@ -71,12 +71,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 #ifdef M3_TRACE
 // Phase trace of a diagnostic build (compiled with -DM3_TRACE; the product build has none of it):
-// clock64 at the phase boundaries of the first kTraceChunks chunks of the first kTraceCtas CTAs.
+// clock64 at the phase boundaries of the first kTraceChunks chunks of each of the first kTraceCtas CTAs.
 // Per (CTA, chunk): slots 0-15 the consumer group (thread 0; slots 11-12 thread 32), 16-31 the
 // rotate group (thread 128).  g_m3_trace_clk holds, for each of the first kClkCtas CTAs of a launch,
 // (globaltimer, clock64) at its start and its end and its SM's id: cycles into time, and the spread
 // of CTA durations by SM.
-constexpr int kTraceCtas = 4, kTraceChunks = 64, kTraceSlots = 32, kClkCtas = 4096, kClkSlots = 6;
+constexpr int kTraceCtas = 512, kTraceChunks = 32, kTraceSlots = 32, kClkCtas = 4096, kClkSlots = 6;
 __device__ long long g_m3_trace[kTraceCtas * kTraceChunks * kTraceSlots];
 __device__ long long g_m3_trace_clk[kClkCtas * kClkSlots];
 #define M3_TRACE_BY(thread, i, slot)                                                                    \
@@ -1445,10 +1445,12 @@ extern "C" __attribute__((visibility("default"))) int m3_trace_read(long long* d
     constexpr int nt = kTraceCtas * kTraceChunks * kTraceSlots, nc = kClkCtas * kClkSlots;
     if (n != nt + nc) return M3_ERR_INVALID_ARG;
     if (dst == nullptr) {
-        static long long zeros[nt + nc] = {};
-        if (cudaMemcpyToSymbol(g_m3_trace, zeros, sizeof(long long) * nt) != cudaSuccess) return M3_ERR_CUDA;
-        if (cudaMemcpyToSymbol(g_m3_trace_clk, zeros, sizeof(long long) * nc) != cudaSuccess) return M3_ERR_CUDA;
-        return M3_OK;
+        void *pt = nullptr, *pc = nullptr;
+        if (cudaGetSymbolAddress(&pt, g_m3_trace) != cudaSuccess) return M3_ERR_CUDA;
+        if (cudaGetSymbolAddress(&pc, g_m3_trace_clk) != cudaSuccess) return M3_ERR_CUDA;
+        if (cudaMemset(pt, 0, sizeof(long long) * nt) != cudaSuccess) return M3_ERR_CUDA;
+        if (cudaMemset(pc, 0, sizeof(long long) * nc) != cudaSuccess) return M3_ERR_CUDA;
+        return cudaDeviceSynchronize() == cudaSuccess ? M3_OK : M3_ERR_CUDA;
     }
     if (cudaMemcpyFromSymbol(dst, g_m3_trace, sizeof(long long) * nt) != cudaSuccess) return M3_ERR_CUDA;
     if (cudaMemcpyFromSymbol(dst + nt, g_m3_trace_clk, sizeof(long long) * nc) != cudaSuccess) return M3_ERR_CUDA;

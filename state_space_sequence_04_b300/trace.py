@@ -2,14 +2,17 @@
 
 Builds libm3_trace.so -- the library compiled with -DM3_TRACE, in which the
 prefill kernel records clock64 at the phase boundaries of the first chunks of
-its first CTAs -- runs one m3_scan_fwd call on a workload after warm-up calls,
-and prints, per warp group, the median cycles each phase takes and the chunk
-period, plus the tensor-pipe rate inside two of the chunk's MMA batches
-measured in place: the chunk-state GEMM H += B'^T X^ (issue by thread 0 right
-after the group barrier, completion seen by a consumer thread spinning on its
-commit barrier) and the intra-chunk output GEMM Y = SL X (likewise).  A
-batch's rate is its executed FLOPs over its issue-to-completion cycles,
-against the SM's share of the measured dense bf16 peak at the traced clock.
+each CTA, and the start and end clocks and the SM of every CTA -- runs one
+m3_scan_fwd call on a workload after warm-up calls, and prints the spread of
+CTA durations by how many CTAs their SM ran, and, for the CTAs that share
+their SM with another (those set the call's time), the median cycles each
+phase of each warp group takes and the chunk period, plus the tensor-pipe rate
+inside two of the chunk's MMA batches measured in place: the chunk-state GEMM
+H += B''^T X (issue by thread 0 right after the group barrier, completion seen
+by a consumer thread spinning on its commit barrier) and the intra-chunk
+output GEMM Y = SL X (likewise).  A batch's rate is its executed FLOPs over
+its issue-to-completion cycles, against the SM's share of the measured dense
+bf16 peak at the traced clock.
 
     python -m state_space_sequence_04_b300.trace [--workload NAME] [--json PATH]
 """
@@ -30,7 +33,7 @@ import torch  # noqa: E402
 
 from state_space_sequence_04_b300 import binding, build, synth  # noqa: E402
 
-CTAS, CHUNKS, SLOTS = 4, 64, 32          # kTraceCtas, kTraceChunks, kTraceSlots of the kernel
+CTAS, CHUNKS, SLOTS = 512, 32, 32        # kTraceCtas, kTraceChunks, kTraceSlots of the kernel
 CLK_CTAS, CLK_SLOTS = 4096, 6            # kClkCtas, kClkSlots: per CTA (t0 ns, clk0, t1 ns, clk1, SM id, -)
 SMS = 148
 KEYS = ("x", "B", "C", "dt", "A", "lam", "omega")
@@ -78,7 +81,8 @@ def run(wname: str):
     tr = list(buf)
     clk = tr[CTAS * CHUNKS * SLOTS:]
     cta = [clk[k * CLK_SLOTS:(k + 1) * CLK_SLOTS] for k in range(CLK_CTAS)]
-    ran = [c for c in cta if c[2] > c[0] > 0]
+    ran_idx = [k for k, c in enumerate(cta) if c[2] > c[0] > 0]
+    ran = [cta[k] for k in ran_idx]
     # cycles per ns from the CTAs' (globaltimer, clock64) pairs
     ghz = statistics.median((c[3] - c[1]) / (c[2] - c[0]) for c in ran[:CTAS])
     # CTA durations of the last launch of the call, by how many of its CTAs shared the SM
@@ -94,6 +98,10 @@ def run(wname: str):
                                  "duration_us_min_med_max": [min(d), statistics.median(d), max(d)],
                                  "end_us_max": max(e)}
     pair_gap = [abs((v[0][2] - v[0][0]) - (v[1][2] - v[1][0])) / 1e3 for v in per_sm.values() if len(v) == 2]
+    # the phases are taken from CTAs that share their SM with another: those set the call's time
+    load = {k: len(per_sm[cta[k][4]]) for k in ran_idx}
+    most = max(load.values())
+    traced = [k for k in ran_idx if k < CTAS and load[k] == most]
 
     def at(cta, i, slot):
         return tr[(cta * CHUNKS + i) * SLOTS + slot]
@@ -104,13 +112,14 @@ def run(wname: str):
     out = {"workload": wname, "launches_per_call": launches, "sm_ghz_traced": ghz, "consumer": {}, "rotate": {},
            "ctas": {"count": len(ran), "span_us": (max(c[2] for c in ran) - t0) / 1e3, "by_sm_load": spread,
                     "pair_duration_gap_us_median": statistics.median(pair_gap) if pair_gap else None}}
-    nchunk = []
-    for cta in range(CTAS):
+    out["ctas"]["phases_from"] = f"{len(traced)} CTAs on SMs running {most} CTAs, first {CHUNKS} chunks each"
+    nchunk = {}
+    for c in traced:
         k = 0
-        while k < CHUNKS and at(cta, k, 0) != 0 and at(cta, k, 9) != 0:
+        while k < CHUNKS and at(c, k, 0) != 0 and at(c, k, 9) != 0:
             k += 1
-        nchunk.append(k)
-    use = [(cta, i) for cta in range(CTAS) for i in range(1, nchunk[cta] - 1)]
+        nchunk[c] = k
+    use = [(c, i) for c in traced for i in range(1, nchunk[c] - 1)]
     if not use:
         raise SystemExit("no traced chunks")
     for j in range(1, len(CONSUMER)):
