@@ -113,6 +113,8 @@ def run(wname: str):
            "ctas": {"count": len(ran), "span_us": (max(c[2] for c in ran) - t0) / 1e3, "by_sm_load": spread,
                     "pair_duration_gap_us_median": statistics.median(pair_gap) if pair_gap else None}}
     out["ctas"]["phases_from"] = f"{len(traced)} CTAs on SMs running {most} CTAs, first {CHUNKS} chunks each"
+    # every CTA of the launch: (start us, duration us, SM), by block index
+    out["ctas"]["per_cta"] = [[(cta[k][0] - t0) / 1e3, (cta[k][2] - cta[k][0]) / 1e3, cta[k][4]] for k in ran_idx]
     nchunk = {}
     for c in traced:
         k = 0
