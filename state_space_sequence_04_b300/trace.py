@@ -53,7 +53,11 @@ def peak_bf16_tflops():
         return 1800.0, "fallback"
 
 
-def run(wname: str):
+PREP_KEYS = ("x", "B", "C", "dt_raw", "A", "u", "omega")
+ENTRIES = ("plain", "prep", "prep_bc", "prep_bc_gate")
+
+
+def run(wname: str, entry: str = "plain"):
     lib_path = build.build(trace=True)
     binding.LIB_PATH = lib_path
     lib = binding.load()
@@ -61,20 +65,37 @@ def run(wname: str):
     lib.m3_trace_read.restype = ctypes.c_int
     n = CTAS * CHUNKS * SLOTS + CLK_CTAS * CLK_SLOTS
     w = synth.WORKLOADS[wname]
-    d = synth.make_inputs(w, seed=0, device="cuda")
-    args = [d[k] for k in KEYS]
+    if entry == "plain":
+        d = synth.make_inputs(w, seed=0, device="cuda")
+        args = [d[k] for k in KEYS]
+    else:   # m3_scan_fwd_prep: pre-activations, optionally the B / C normalisation and the gate
+        d = synth.make_prep_inputs(w, seed=0, device="cuda")
+        args = [d[k] for k in PREP_KEYS]
+        bc = None if entry == "prep" else {k: (v.to("cuda") if hasattr(v, "shape") else v)
+                                           for k, v in synth.make_bc_params(w.heads, w.rank, w.dstate).items()}
+        z = synth.make_gate(tuple(d["x"].shape), io=w.io, seed=0, device="cuda") if entry == "prep_bc_gate" else None
+        params = binding.prep_params(d["dt_bias"], bc, z)
     path, launches = binding.m3_scan_fwd_plan(w.batch, w.seqlen, w.heads, w.headdim, w.dstate, w.rank, w.chunk,
                                               binding.io_code(d["x"].dtype))
     if path != 1:
         raise SystemExit(f"{wname} does not take the tensor-core path")
     y = torch.empty_like(d["x"])
     fin = torch.empty((w.batch, w.heads, w.dstate, w.headdim), dtype=torch.float32, device="cuda")
-    ws = binding.alloc_workspace(d["x"].shape, w.dstate, w.rank, w.chunk, d["x"].dtype, "cuda")
+    if entry == "plain":
+        ws = binding.alloc_workspace(d["x"].shape, w.dstate, w.rank, w.chunk, d["x"].dtype, "cuda")
+
+        def call():
+            binding._check(binding.m3_scan_fwd(*args, w.rank, w.chunk, y, fin, ws), "m3_scan_fwd")
+    else:
+        ws = binding.alloc_workspace_prep(d["x"].shape, w.dstate, w.rank, w.chunk, d["x"].dtype, "cuda")
+
+        def call():
+            binding._check(binding.m3_scan_fwd_prep(*args, w.rank, w.chunk, y, fin, ws, params), "m3_scan_fwd_prep")
     for _ in range(3):
-        binding._check(binding.m3_scan_fwd(*args, w.rank, w.chunk, y, fin, ws), "m3_scan_fwd")
+        call()
     torch.cuda.synchronize()
     binding._check(lib.m3_trace_read(None, n), "m3_trace_read")
-    binding._check(binding.m3_scan_fwd(*args, w.rank, w.chunk, y, fin, ws), "m3_scan_fwd")
+    call()
     torch.cuda.synchronize()
     buf = (ctypes.c_longlong * n)()
     binding._check(lib.m3_trace_read(ctypes.addressof(buf), n), "m3_trace_read")
@@ -109,7 +130,7 @@ def run(wname: str):
     # the last launch of the call (the full pass) is the one traced last: its values overwrite the state pass's
     QR, P, N = 64, w.headdim, w.dstate   # every chunk runs as 64-row sub-chunks (64 / R tokens)
     MM = 64
-    out = {"workload": wname, "launches_per_call": launches, "sm_ghz_traced": ghz, "consumer": {}, "rotate": {},
+    out = {"workload": wname, "entry": entry, "launches_per_call": launches, "sm_ghz_traced": ghz, "consumer": {}, "rotate": {},
            "ctas": {"count": len(ran), "span_us": (max(c[2] for c in ran) - t0) / 1e3, "by_sm_load": spread,
                     "pair_duration_gap_us_median": statistics.median(pair_gap) if pair_gap else None}}
     out["ctas"]["phases_from"] = f"{len(traced)} CTAs on SMs running {most} CTAs, first {CHUNKS} chunks each"
@@ -162,9 +183,11 @@ def run(wname: str):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default=synth.SISO_1P5B.name, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--entry", default="plain", choices=ENTRIES,
+                    help="m3_scan_fwd, or m3_scan_fwd_prep alone / with the B/C normalisation / and the gate")
     ap.add_argument("--json", default=None)
     a = ap.parse_args()
-    out = run(a.workload)
+    out = run(a.workload, a.entry)
     print(json.dumps(out, indent=1))
     if a.json:
         with open(a.json, "w") as f:
