@@ -102,9 +102,11 @@ M3_API int m3_scan_fwd_plan(int64_t batch, int64_t seqlen, int64_t nheads, int64
  *            multiple of 16.  The result does not depend on it beyond rounding.
  *            The tensor-core path runs every chunk as sub-chunks of 64 / R
  *            tokens (64-row score tiles), the MIMO chunk-length reduction of
- *            section 3.3 taken to one tile shape.  With fewer (batch, head) sequences than
- *            the GPU has CTA slots it also cuts each sequence into segments
- *            (a state pass, the segment scan of m3_state_passing, a full pass).
+ *            section 3.3 taken to one tile shape.  With at most 148 (batch, head)
+ *            sequences (half the 296 CTA slots of a B300) it also cuts every
+ *            sequence at the same places into at most 296 / sequences segments
+ *            (a state pass, the segment scan of m3_state_passing, a full pass:
+ *            3 launches).
  *   y        out [batch, T, H, R, P], io dtype
  *   final_state  out (nullable) [batch, H, N, P] fp32: h_{T-1}, the state a
  *            decode step continues from (its delayed-write cache is
