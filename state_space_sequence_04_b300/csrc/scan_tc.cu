@@ -213,7 +213,6 @@ struct Ctl {
     uint64_t rot_done[2];    // rotate group finished the stage (count 128)
     uint64_t coef_ready[2];  // coefficient block of the stage written (count 128)
     uint64_t coef_free[2];   // consumer done reading the stage's coefficient block (count 128)
-    uint64_t bS;             // scores S of a chunk complete (one commit per chunk, in chunk order)
     uint64_t bH;             // chunk state onto the carry H complete (one per chunk)
     uint64_t bY;             // output Y (and the inter readout Yi issued before it) complete (one per chunk)
     uint64_t never;          // completed by nothing: the failure-path test mode waits on it
@@ -443,7 +442,6 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
             ctl->cb_issued[s] = ctl->cb_waited[s] = 0;
             ctl->x_issued[s] = ctl->x_waited[s] = 0;
         }
-        mbar_init(&ctl->bS, 1);
         mbar_init(&ctl->bH, 1);
         mbar_init(&ctl->bY, 1);
         mbar_init(&ctl->never, 1);
@@ -553,7 +551,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
         group_bar(1);
         const bool odd = tid & 1;
         float ld_sum = 0.f;   // state pass: summed log-decay (thread 0)
-        // S = C~ B''^T of the chunk in stage s, committed to bS (thread 0, which issues every MMA)
+        // S = C~ B''^T of the chunk in stage s (thread 0, which issues every MMA).  No commit of its own:
+        // the chunk-state commit that follows it on the same thread completes only after it
         auto issue_scores = [&](int s) {
             const uint64_t dC = smem_desc(smem_u32(tile_c(s)), 16, 1024, kSwizzle128B);
             const uint64_t dB = smem_desc(smem_u32(tile_b(s)), 16, 1024, kSwizzle128B);
@@ -563,7 +562,6 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                 const uint32_t ko = ((kk >> 2) * QR * 128 + (kk & 3) * 32) >> 4;
                 mma_bf16_ss(tmem + K::T_S, dC + ko, dB + ko, id_s, kk > 0);
             }
-            mma_commit(&ctl->bS);
         };
         // the scores of local chunk s_next are the next ones to issue (thread 0): each chunk's go
         // out as soon as its rotation is done and the previous chunk's mask has read the S columns
@@ -608,9 +606,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                     issue_scores(s);
                     s_next = i + 1;
                 }
-                // the chunk's X (read by the chunk state here and by the output later)
-                if (wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_c, fail_r)) ctl->x_waited[s] += 1;
-                tc_fence_after();
+                // the chunk's X (read by the chunk state here and by the output later) has landed:
+                // the rotate group waited for it before arriving on rot_done
                 // descriptors of the operand bases; a byte offset o moves the start address field by o >> 4
                 const uint64_t dBt = smem_desc(smem_u32(tile_b(s)), QR * 128, 1024, kSwizzle128B);
                 const uint64_t dX = smem_desc(smem_u32(tile_x(s)), 16, 1024, kSwizzle128B);
@@ -633,7 +630,6 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                 }
                 M3_TRACE_C(i, 2);
             }
-            if (FULL) (void)wait_bounded(&ctl->bS, i & 1, fail_c, fail_r);
             (void)wait_bounded(&ctl->bH, i & 1, fail_c, fail_r);
             M3_TRACE_BY(32, i, 12);
             M3_TRACE_C(i, 3);
@@ -1141,6 +1137,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
             M3_TRACE_R(i, 5);
             M3_TRACE_R(i, 6);
             M3_TRACE_R(i, 7);
+            // the chunk's X as well, so that rot_done tells the consumer's MMAs that it has landed
+            if (rt == 0 && !*fail_r && wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_r, fail_c)) ctl->x_waited[s] += 1;
             mbar_arrive(&ctl->rot_done[s]);
             group_bar(2);   // sW is reused by the next chunk
             M3_TRACE_R(i, 8);
