@@ -507,45 +507,75 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
         if (FULL && seg > 0)
             hin = seg < args.S - 1 ? args.h_in + ((int64_t)bh * (args.S - 1) + seg) * NS * P
                                    : args.h_in_last + (int64_t)bh * NS * P;
-        {
-            // H enters batch 1 already decayed by the first chunk: exp(cum_end) H_in
-            float e0 = 0.f;
+        // the carry entering the segment: H_in, or zero (its bf16 copy and the first chunk's decay come
+        // from a state step, below)
+        if (tid < NS || hin == nullptr) {
+#pragma unroll
+            for (int cc = 0; cc < P; cc += 32) {
+                float v[32];
+                if (hin != nullptr && tid < NS) {
+#pragma unroll
+                    for (int i4 = 0; i4 < 32; i4 += 4) {
+                        const float4 q = *reinterpret_cast<const float4*>(hin + (int64_t)tid * P + cc + i4);
+                        v[i4] = q.x; v[i4 + 1] = q.y; v[i4 + 2] = q.z; v[i4 + 3] = q.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int i4 = 0; i4 < 32; ++i4) v[i4] = 0.f;
+                }
+                tmem_st32(tlane + K::T_H + cc, v);
+            }
+            tmem_st_wait();
+        }
+        // ---- the state step: Hb <- bf16(H) (read by the next inter readout Yi), H <- e H with e the decay
+        //      of the chunk about to run (thread = state row n; warp-uniform, the TMEM loads are
+        //      warp-collective).  The carry lives in the segment's rotating frame (B and C are rotated by
+        //      the phase since the segment start), where the transition is the scalar decay alone
+        //      (Propositions 3-4).
+        auto state_step = [&](float e) {
+            if (tid < NS) {
+                const float2 e2 = make_float2(e, e);
+#pragma unroll
+                for (int cc = 0; cc < P; cc += 32) {
+                    float hv[32];
+                    tmem_ld32_sync(tlane + K::T_H + cc, hv);
+                    if (FULL) {
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            const uint4 pk = make_uint4(pack_bf16(hv[q8 * 8 + 0], hv[q8 * 8 + 1]),
+                                                        pack_bf16(hv[q8 * 8 + 2], hv[q8 * 8 + 3]),
+                                                        pack_bf16(hv[q8 * 8 + 4], hv[q8 * 8 + 5]),
+                                                        pack_bf16(hv[q8 * 8 + 6], hv[q8 * 8 + 7]));
+                            *reinterpret_cast<uint4*>(hb + sw128_offset(tid, (cc + q8 * 8) * 2)) = pk;
+                        }
+                    }
+#pragma unroll
+                    for (int i2 = 0; i2 < 32; i2 += 2) {
+                        const float2 sc = __fmul2_rn(e2, make_float2(hv[i2], hv[i2 + 1]));
+                        hv[i2] = sc.x;
+                        hv[i2 + 1] = sc.y;
+                    }
+                    tmem_st32(tlane + K::T_H + cc, hv);
+                }
+                tmem_st_wait();
+                if (FULL) fence_proxy_async_smem();
+            }
+        };
+        // Where it runs.  With R >= 2, at the top of each chunk once rot_done is in (which implies the
+        // chunk's coefficient block), so the consumer -- the critical path of these configurations --
+        // waits one barrier less per chunk.  With R = 1, at the end of the previous chunk (after waiting
+        // for the next chunk's coefficients), where it overlaps the rotate group's longer 64-token
+        // rotation.  Measured both ways: SISO 61.0 / 57.6 Mtok/s, MIMO 30.5 / 31.7, long context
+        // 13.4 / 13.7 (end / top).
+        constexpr bool STEP_AT_TOP = R >= 2;
+        if (!STEP_AT_TOP) {   // chunk 0's step: Hb_{-1} = bf16(H_in), H = e^{cum_end} H_in
+            float e0 = 1.f;
             if (hin != nullptr) {
                 (void)wait_bounded(&ctl->coef_ready[0], 0, fail_c, fail_r);
                 e0 = coef(0)[K::CO_EEND];
             }
-            if (tid < NS || hin == nullptr) {
-#pragma unroll
-                for (int cc = 0; cc < P; cc += 32) {
-                    float v[32];
-                    if (hin != nullptr && tid < NS) {
-#pragma unroll
-                        for (int i4 = 0; i4 < 32; i4 += 4) {
-                            const float4 q = *reinterpret_cast<const float4*>(hin + (int64_t)tid * P + cc + i4);
-                            v[i4] = q.x; v[i4 + 1] = q.y; v[i4 + 2] = q.z; v[i4 + 3] = q.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int i4 = 0; i4 < 32; ++i4) v[i4] = 0.f;
-                    }
-                    if (FULL && tid < NS) {
-#pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8)
-                            *reinterpret_cast<uint4*>(hb + sw128_offset(tid, (cc + q8 * 8) * 2)) =
-                                make_uint4(pack_bf16(v[q8 * 8 + 0], v[q8 * 8 + 1]), pack_bf16(v[q8 * 8 + 2], v[q8 * 8 + 3]),
-                                           pack_bf16(v[q8 * 8 + 4], v[q8 * 8 + 5]), pack_bf16(v[q8 * 8 + 6], v[q8 * 8 + 7]));
-                    }
-#pragma unroll
-                    for (int i4 = 0; i4 < 32; ++i4) v[i4] *= e0;
-                    tmem_st32(tlane + K::T_H + cc, v);
-                }
-                tmem_st_wait();
-            }
-            if (FULL && hin == nullptr) {
-                uint4* hb4 = reinterpret_cast<uint4*>(hb);
-                for (int i = tid; i < NS * 128 / 16; i += 128) hb4[i] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
+            tc_fence_after();
+            state_step(e0);
         }
         tc_fence_before();
         group_bar(1);
@@ -582,6 +612,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
             if constexpr (HOOK) {
                 if (FULL && i == ext.fail_chunk) (void)wait_bounded(&ctl->never, 0, fail_c, fail_r, 50000ull);
             }
+            M3_TRACE_C(i, 8);
+            if constexpr (STEP_AT_TOP) {   // into this chunk: its decay; H+= and Yi of the last are complete
+                tc_fence_after();
+                state_step(co[K::CO_EEND]);
+            }
+            M3_TRACE_C(i, 9);
             tc_fence_before();
             group_bar(1);
             if (*fail_c) break;
@@ -781,54 +817,28 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                 if (tid == 0) ld_sum += co[K::CO_CEND];
             }
 
-            // ---- state: Hb <- bf16(H), H <- e_{c+1} H   (thread = state row n).  The carry lives in
-            //      the segment's rotating frame (B and C are rotated by the phase since the segment
-            //      start), where the transition is the scalar decay alone (Propositions 3-4); Yi has
-            //      read Hb_{c-1}
-            float e_next = 1.f;
-            if (i + 1 < nl) {
-                const int s1 = (i + 1) & 1;
-                (void)wait_bounded(&ctl->coef_ready[s1], ((i + 1) >> 1) & 1, fail_c, fail_r);
-                e_next = coef(s1)[K::CO_EEND];
-            }
-            M3_TRACE_C(i, 8);
-            tc_fence_after();
-            if (tid < NS) {
-                const float2 e2 = make_float2(e_next, e_next);
-#pragma unroll
-                for (int cc = 0; cc < P; cc += 32) {
-                    float hv[32];
-                    tmem_ld32_sync(tlane + K::T_H + cc, hv);
-                    if (FULL) {
-#pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) {
-                            const uint4 pk = make_uint4(pack_bf16(hv[q8 * 8 + 0], hv[q8 * 8 + 1]),
-                                                        pack_bf16(hv[q8 * 8 + 2], hv[q8 * 8 + 3]),
-                                                        pack_bf16(hv[q8 * 8 + 4], hv[q8 * 8 + 5]),
-                                                        pack_bf16(hv[q8 * 8 + 6], hv[q8 * 8 + 7]));
-                            *reinterpret_cast<uint4*>(hb + sw128_offset(tid, (cc + q8 * 8) * 2)) = pk;
-                        }
-                    }
-#pragma unroll
-                    for (int i2 = 0; i2 < 32; i2 += 2) {
-                        const float2 sc = __fmul2_rn(e2, make_float2(hv[i2], hv[i2 + 1]));
-                        hv[i2] = sc.x;
-                        hv[i2 + 1] = sc.y;
-                    }
-                    tmem_st32(tlane + K::T_H + cc, hv);
+            if constexpr (!STEP_AT_TOP) {   // into the next chunk: its decay (none after the last)
+                float e_next = 1.f;
+                if (i + 1 < nl) {
+                    const int s1 = (i + 1) & 1;
+                    (void)wait_bounded(&ctl->coef_ready[s1], ((i + 1) >> 1) & 1, fail_c, fail_r);
+                    e_next = coef(s1)[K::CO_EEND];
                 }
-                tmem_st_wait();
-                if (FULL) fence_proxy_async_smem();
+                M3_TRACE_C(i, 14);
+                tc_fence_after();
+                state_step(e_next);
             }
             // every read of this stage's coefficient block is done (the output took exp(cum_t)
             // in a register): the rotate group may fill it for chunk i+2
             mbar_arrive(&ctl->coef_free[s]);
-            tc_fence_before();
-            group_bar(1);
-            M3_TRACE_C(i, 9);
-            if (*fail_c) break;
+            if constexpr (!STEP_AT_TOP) {
+                tc_fence_before();
+                group_bar(1);
+                M3_TRACE_C(i, 15);
+                if (*fail_c) break;
+            }
         }
-        // the carry after the segment's last chunk (e_next = 1), rotated from the segment's frame
+        // the carry after the segment's last chunk (no decay after it), rotated from the segment's frame
         // to the physical frame by the segment's phase Theta (the last chunk's phase, mod 2 pi)
         const float* co_last = coef((nl - 1) & 1);
         float* dst = nullptr;

@@ -38,9 +38,11 @@ CLK_CTAS, CLK_SLOTS = 4096, 6            # kClkCtas, kClkSlots: per CTA (t0 ns, 
 SMS = 148
 KEYS = ("x", "B", "C", "dt", "A", "lam", "omega")
 # slot names: consumer thread 0 (0-9, in the time order below), observers (11, 12), rotate thread 128 (16-24)
-CONSUMER = [(0, "top"), (1, "stage ready (rot_done + barrier)"), (2, "H+= and Yi issued"), (3, "S and H+= waited"),
-            (4, "mask + barrier"), (5, "Y issued (+ next S)"), (6, "Y waited"), (7, "output stored"),
-            (8, "next coefficients"), (9, "state step + barrier")]
+# (the state step runs at the top of a chunk with R >= 2 (slots 8 -> 9), at the end with R = 1 (14 -> 15))
+CONSUMER = [(0, "top"), (8, "stage ready (rot_done)"), (9, "state step, R >= 2"), (1, "barrier"),
+            (2, "H+= and Yi issued"), (3, "S and H+= waited"), (4, "mask + barrier"), (5, "Y issued (+ next S)"),
+            (6, "Y waited"), (7, "output stored"), (14, "next coefficients, R = 1"),
+            (15, "state step + barrier, R = 1")]
 ROTATE = ["top", "dt/lambda boxes", "coefficients + angle partial sums", "C/B landed", "rotation (C~, B'')",
           "barrier + next boxes issued", "-", "-", "barrier"]
 
