@@ -143,7 +143,7 @@ struct Cfg {
     static constexpr int SMEM = OFF_BAR + 192 + 1024;             // barriers / flags, alignment slack
     // two CTAs per SM when both fit (228 KB per SM, 1 KB reserved per CTA)
     static constexpr int MIN_BLOCKS = 2 * (SMEM + 1024) <= 233472 ? 2 : 1;
-    static constexpr int TX_BOX = 2 * BOX_BYTES, TX_X = X_BYTES;
+    static constexpr int TX_BOX = 2 * BOX_BYTES;
 
     // TMEM columns (the state pass holds the carry alone)
     static constexpr int T_S = 0;
@@ -203,12 +203,12 @@ __device__ __forceinline__ uint32_t word_at(const uint4* a, int i) {
     return (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
 }
 
-// Shared control block (after the barriers).  Three TMA groups per stage, each
+// Shared control block (after the barriers).  Two TMA groups per stage, each
 // issued as soon as its previous contents are dead: the dt / lambda boxes
-// (once the rotate group has read them), C and B (after batch 1), X (after
-// batch 2).
+// (once the rotate group has read them), and C, B and X together (once the
+// chunk's output MMAs are complete).
 struct Ctl {
-    uint64_t fbox[2], fcb[2], fx[2];   // TMA groups landed
+    uint64_t fbox[2], fcbx[2];   // TMA groups landed: the dt / lambda boxes; C, B and X
     uint64_t bc_done[2];     // rotate group rotated the stage's C and B (count 128)
     uint64_t rot_done[2];    // rotate group finished the stage (count 128)
     uint64_t coef_ready[2];  // coefficient block of the stage written (count 128)
@@ -221,7 +221,7 @@ struct Ctl {
     int fail_c, fail_r;      // per-group failure flags
     // copies issued and waited for, modulo 2^16 (only their difference, at most 2, and
     // their parity matter: they drive the bounded drain on failure)
-    uint16_t box_issued[2], box_waited[2], cb_issued[2], cb_waited[2], x_issued[2], x_waited[2];
+    uint16_t box_issued[2], box_waited[2], cbx_issued[2], cbx_waited[2];
 };
 static_assert(sizeof(Ctl) <= 192, "control block must fit its reserved space");
 
@@ -432,15 +432,13 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(&ctl->fbox[s], 1);
-            mbar_init(&ctl->fcb[s], 1);
-            mbar_init(&ctl->fx[s], 1);
+            mbar_init(&ctl->fcbx[s], 1);
             mbar_init(&ctl->bc_done[s], 128);
             mbar_init(&ctl->rot_done[s], 128);
             mbar_init(&ctl->coef_ready[s], 128);
             mbar_init(&ctl->coef_free[s], 128);
             ctl->box_issued[s] = ctl->box_waited[s] = 0;
-            ctl->cb_issued[s] = ctl->cb_waited[s] = 0;
-            ctl->x_issued[s] = ctl->x_waited[s] = 0;
+            ctl->cbx_issued[s] = ctl->cbx_waited[s] = 0;
         }
         mbar_init(&ctl->bH, 1);
         mbar_init(&ctl->bY, 1);
@@ -457,7 +455,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
     }
     __syncthreads();
 
-    // the three TMA groups of local chunk i into stage s (single issuing thread each)
+    // the two TMA groups of local chunk i into stage s (single issuing thread each)
     auto load_box = [&](int i, int s) {
         const int c0 = (c_begin + i) * Q;
         mbar_arrive_expect_tx(&ctl->fbox[s], K::TX_BOX);
@@ -465,20 +463,18 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
         tma_load_3d(box_lam(s), &tm_lam, &ctl->fbox[s], h & ~3, c0, b);
         ctl->box_issued[s] += 1;
     };
-    auto load_cb = [&](int i, int s) {
+    // C, B and X on one barrier: the rotate group waits for them once, and its rot_done then tells the
+    // consumer's MMAs that X has landed as well
+    auto load_cbx = [&](int i, int s) {
         const int c0 = (c_begin + i) * Q;
-        mbar_arrive_expect_tx(&ctl->fcb[s], TX_CB);
+        mbar_arrive_expect_tx(&ctl->fcbx[s], TX_CB + K::X_BYTES);
 #pragma unroll
         for (int p = 0; p < K::NPAN; ++p) {
-            if (FULL) tma_load_5d(tile_c(s) + p * QR * 128, &tm_C, &ctl->fcb[s], 64 * p, 0, h, c0, b);
-            tma_load_5d(tile_b(s) + p * QR * 128, &tm_B, &ctl->fcb[s], 64 * p, 0, h, c0, b);
+            if (FULL) tma_load_5d(tile_c(s) + p * QR * 128, &tm_C, &ctl->fcbx[s], 64 * p, 0, h, c0, b);
+            tma_load_5d(tile_b(s) + p * QR * 128, &tm_B, &ctl->fcbx[s], 64 * p, 0, h, c0, b);
         }
-        ctl->cb_issued[s] += 1;
-    };
-    auto load_x = [&](int i, int s) {
-        mbar_arrive_expect_tx(&ctl->fx[s], K::TX_X);
-        tma_load_5d(tile_x(s), &tm_x, &ctl->fx[s], 0, 0, h, (c_begin + i) * Q, b);
-        ctl->x_issued[s] += 1;
+        tma_load_5d(tile_x(s), &tm_x, &ctl->fcbx[s], 0, 0, h, c0, b);
+        ctl->cbx_issued[s] += 1;
     };
 
     if (warp == 0) {
@@ -488,8 +484,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
     if (tid == 0) {
         for (int i = 0; i < 2 && i < nl; ++i) {
             load_box(i, i);
-            load_cb(i, i);
-            load_x(i, i);
+            load_cbx(i, i);
         }
     }
     tc_fence_before();
@@ -643,7 +638,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                     s_next = i + 1;
                 }
                 // the chunk's X (read by the chunk state here and by the output later) has landed:
-                // the rotate group waited for it before arriving on rot_done
+                // the rotate group waited for it (with C and B) before arriving on rot_done
                 // descriptors of the operand bases; a byte offset o moves the start address field by o >> 4
                 const uint64_t dBt = smem_desc(smem_u32(tile_b(s)), QR * 128, 1024, kSwizzle128B);
                 const uint64_t dX = smem_desc(smem_u32(tile_x(s)), 16, 1024, kSwizzle128B);
@@ -752,8 +747,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                 M3_TRACE_C(i, 6);
                 tc_fence_after();
                 if (tid == 0 && i + 2 < nl && !*fail_c) {
-                    load_cb(i + 2, s);
-                    load_x(i + 2, s);
+                    load_cbx(i + 2, s);
                 }
                 if constexpr (K::M64) {
                     const int row = warp * 16 + (lane & 15), half = lane >> 4, t = row / R, r = row % R;
@@ -811,8 +805,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
             } else {
                 // B'' and X are consumed: the next loads may come in
                 if (tid == 0 && i + 2 < nl && !*fail_c) {
-                    load_cb(i + 2, s);
-                    load_x(i + 2, s);
+                    load_cbx(i + 2, s);
                 }
                 if (tid == 0) ld_sum += co[K::CO_CEND];
             }
@@ -1022,9 +1015,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
             //      this group at most one chunk ahead of the consumer: every barrier the
             //      consumer waits on is then at most one phase ahead.
             M3_TRACE_R(i, 2);
-            const bool got_cb = wait_bounded(&ctl->fcb[s], (i >> 1) & 1, fail_r, fail_c);
+            const bool got_cb = wait_bounded(&ctl->fcbx[s], (i >> 1) & 1, fail_r, fail_c);
             M3_TRACE_R(i, 3);
-            if (rt == 0 && got_cb) ctl->cb_waited[s] += 1;
+            if (rt == 0 && got_cb) ctl->cbx_waited[s] += 1;
             // the consumer may use this chunk's coefficients (exp(cum_end), f) now
             mbar_arrive(&ctl->coef_ready[s]);
             {
@@ -1147,8 +1140,6 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
             M3_TRACE_R(i, 5);
             M3_TRACE_R(i, 6);
             M3_TRACE_R(i, 7);
-            // the chunk's X as well, so that rot_done tells the consumer's MMAs that it has landed
-            if (rt == 0 && !*fail_r && wait_bounded(&ctl->fx[s], (i >> 1) & 1, fail_r, fail_c)) ctl->x_waited[s] += 1;
             mbar_arrive(&ctl->rot_done[s]);
             group_bar(2);   // sW is reused by the next chunk
             M3_TRACE_R(i, 8);
@@ -1169,8 +1160,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
         };
         for (int s = 0; s < 2; ++s) {
             drain(&ctl->fbox[s], ctl->box_waited[s], ctl->box_issued[s]);
-            drain(&ctl->fcb[s], ctl->cb_waited[s], ctl->cb_issued[s]);
-            drain(&ctl->fx[s], ctl->x_waited[s], ctl->x_issued[s]);
+            drain(&ctl->fcbx[s], ctl->cbx_waited[s], ctl->cbx_issued[s]);
         }
         // thread 0 issued every MMA: a commit arrives once all of them are complete
         mma_commit(&ctl->drain);
