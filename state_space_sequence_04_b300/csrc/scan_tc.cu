@@ -822,14 +822,10 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                 state_step(e_next);
             }
             // every read of this stage's coefficient block is done (the output took exp(cum_t)
-            // in a register): the rotate group may fill it for chunk i+2
+            // in a register): the rotate group may fill it for chunk i+2.  (The next chunk's barrier,
+            // after its rot_done wait, orders the state step's writes before its MMAs.)
             mbar_arrive(&ctl->coef_free[s]);
-            if constexpr (!STEP_AT_TOP) {
-                tc_fence_before();
-                group_bar(1);
-                M3_TRACE_C(i, 15);
-                if (*fail_c) break;
-            }
+            M3_TRACE_C(i, 15);
         }
         // the carry after the segment's last chunk (no decay after it), rotated from the segment's frame
         // to the physical frame by the segment's phase Theta (the last chunk's phase, mod 2 pi)

@@ -42,7 +42,7 @@ KEYS = ("x", "B", "C", "dt", "A", "lam", "omega")
 CONSUMER = [(0, "top"), (8, "stage ready (rot_done)"), (9, "state step, R >= 2"), (1, "barrier"),
             (2, "H+= and Yi issued"), (3, "S and H+= waited"), (4, "mask + barrier"), (5, "Y issued (+ next S)"),
             (6, "Y waited"), (7, "output stored"), (14, "next coefficients, R = 1"),
-            (15, "state step + barrier, R = 1")]
+            (15, "state step, R = 1")]
 ROTATE = ["top", "dt/lambda boxes", "coefficients + angle partial sums", "C/B landed", "rotation (C~, B'')",
           "barrier + next boxes issued", "-", "-", "barrier"]
 
