@@ -906,10 +906,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
         for (int i = 0; i < nl; ++i) {
             const int c = c_begin + i, s = i & 1;
             M3_TRACE_R(i, 0);
+            // every thread waits for the boxes itself; a failure is acted on at the next group barrier
             const bool got_box = wait_bounded(&ctl->fbox[s], (i >> 1) & 1, fail_r, fail_c);
-            group_bar(2);
             if (rt == 0 && got_box) ctl->box_waited[s] += 1;
-            if (*fail_r) break;
             float a_t = a;
             if constexpr (PREP) {
                 // Delta and lambda of this head's Q+1 staged tokens, in place (0 past the end)
@@ -948,6 +947,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
             // the consumer is done with chunk i-2's coefficients in this stage
             if (i >= 2) (void)wait_bounded(&ctl->coef_free[s], ((i - 2) >> 1) & 1, fail_r, fail_c);
             group_bar(2);   // every box value is read (the boxes may now hold partial sums)
+            if (*fail_r) break;   // set only inside this group's waits, all before the barrier
             M3_TRACE_R(i, 10);
             float off = 0.f, cend = 0.f;
             for (int k = 0; k < 4; ++k) {
@@ -1129,17 +1129,17 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                 load_omega(c + 1);
                 if (PREP) a_nx = load_a(c + 1);
             }
-            group_bar(2);   // partial sums read: the boxes may take chunk i+2
-            phi0 = *reinterpret_cast<const float4*>(&co[K::CO_THETA + 4 * jg]);
-            if (rt == 0 && i + 2 < nl && !*fail_r) load_box(i + 2, s);
-
+            if constexpr (K::PART_IN_BOX) group_bar(2);   // partial sums read: the box may take chunk i+2
             M3_TRACE_R(i, 5);
             M3_TRACE_R(i, 6);
             M3_TRACE_R(i, 7);
             mbar_arrive(&ctl->rot_done[s]);
-            group_bar(2);   // sW is reused by the next chunk
+            group_bar(2);   // sW is reused by the next chunk; the chunk-end phase Theta is written
             M3_TRACE_R(i, 8);
             if (*fail_r) break;
+            phi0 = *reinterpret_cast<const float4*>(&co[K::CO_THETA + 4 * jg]);
+            // the boxes' values and (without PART_IN_BOX) nothing else of the stage's boxes is still read
+            if (rt == 0 && i + 2 < nl) load_box(i + 2, s);
         }
     }
 
