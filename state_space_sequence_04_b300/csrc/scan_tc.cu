@@ -575,6 +575,9 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
         tc_fence_before();
         group_bar(1);
         const bool odd = tid & 1;
+        // the next C, B and X loads go out from warp 3: warp 0 issues every MMA and is the last to
+        // reach the output
+        constexpr int kCbxThread = 96;
         float ld_sum = 0.f;   // state pass: summed log-decay (thread 0)
         // S = C~ B''^T of the chunk in stage s (thread 0, which issues every MMA).  No commit of its own:
         // the chunk-state commit that follows it on the same thread completes only after it
@@ -746,7 +749,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                 M3_TRACE_BY(32, i, 11);
                 M3_TRACE_C(i, 6);
                 tc_fence_after();
-                if (tid == 0 && i + 2 < nl && !*fail_c) {
+                if (tid == kCbxThread && i + 2 < nl && !*fail_c) {
                     load_cbx(i + 2, s);
                 }
                 if constexpr (K::M64) {
@@ -804,7 +807,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                 M3_TRACE_C(i, 7);
             } else {
                 // B'' and X are consumed: the next loads may come in
-                if (tid == 0 && i + 2 < nl && !*fail_c) {
+                if (tid == kCbxThread && i + 2 < nl && !*fail_c) {
                     load_cbx(i + 2, s);
                 }
                 if (tid == 0) ld_sum += co[K::CO_CEND];
