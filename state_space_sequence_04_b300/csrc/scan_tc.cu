@@ -135,7 +135,10 @@ struct Cfg {
     static constexpr int CO_BYTES = align_up((5 * Q + NS / 2 + 2) * 4, 16);
 
     static constexpr int OFF_HB = 2 * STG_TILE;
-    static constexpr int OFF_BOX = OFF_HB + (FULL ? NS * 128 : 0);   // [stage][dt | lambda]
+    // the full pass's output tile y (QR rows x P, bf16, 128-byte swizzle), written by the consumer
+    // threads and stored by one TMA store
+    static constexpr int OFF_OUT = OFF_HB + (FULL ? NS * 128 : 0);
+    static constexpr int OFF_BOX = OFF_OUT + (FULL ? QR * 128 : 0);   // [stage][dt | lambda]
     static constexpr int OFF_PART = OFF_BOX + 4 * BOX_STRIDE;     // only when not in the boxes
     static constexpr int OFF_CO = OFF_PART + (PART_IN_BOX ? 0 : align_up(PART_BYTES, 16));
     static constexpr int OFF_RPRIV = OFF_CO + 2 * CO_BYTES;       // w[Q], warp sums[4]
@@ -349,31 +352,69 @@ __device__ __forceinline__ void load8(const float* p, float fill, float (&o)[8])
 // block's last token (the first factor <= 1, the second, b_s, <= 2^100); the
 // diagonal block uses 2^(cum2_t - (cum2_s + g_s)) directly (cg = cum2 + g) and
 // rho_t 2^-g_t on the diagonal; blocks above are zero.
+// With R >= 2 a block holds 16 / R tokens, each on R columns: their factors come in
+// as 16-byte loads, one exponential per token, and the diagonal block selects
+// instead of branching per column (the lanes of a warp hold different rows t).
+// Measured with R = 1 the per-column form below is faster (SISO 64.8 against
+// 62.9 Mtok/s); with R = 4 the per-token form (long-context MIMO 15.3 against 15.1).
 template <int R>
 __device__ __forceinline__ void mask_block(float* v, int cb, int t, float ct, float rt, const float* cum2,
                                            const float* bneg, const float* cg) {
-    const int s_lo = cb / R, s_hi = (cb + 15) / R;
-    if (s_lo > t) {
+    if constexpr (R == 1) {
+        const int s_lo = cb, s_hi = cb + 15;
+        if (s_lo > t) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
-    } else if (s_hi < t) {
-        const float a = ex2_approx(ct - cum2[s_hi]);
-        const float2 a2 = make_float2(a, a);
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        } else if (s_hi < t) {
+            const float a = ex2_approx(ct - cum2[s_hi]);
+            const float2 a2 = make_float2(a, a);
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-            const float2 bb = make_float2(bneg[(cb + i) / R], bneg[(cb + i + 1) / R]);
-            const float2 r2 = __fmul2_rn(make_float2(v[i], v[i + 1]), __fmul2_rn(a2, bb));
-            v[i] = r2.x;
-            v[i + 1] = r2.y;
+            for (int i = 0; i < 16; i += 2) {
+                const float2 bb = make_float2(bneg[cb + i], bneg[cb + i + 1]);
+                const float2 r2 = __fmul2_rn(make_float2(v[i], v[i + 1]), __fmul2_rn(a2, bb));
+                v[i] = r2.x;
+                v[i + 1] = r2.y;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int sidx = cb + i;
+                float m = 0.f;
+                if (sidx < t) m = ex2_approx(ct - cg[sidx]);
+                else if (sidx == t) m = rt;
+                v[i] *= m;
+            }
         }
     } else {
+        constexpr int NSB = 16 / R;   // tokens of the block
+        static_assert(16 % R == 0 && NSB % 4 == 0, "a block holds a multiple of 4 tokens");
+        const int s0 = cb / R, s_hi = s0 + NSB - 1;   // cb is a multiple of 16: s0 of NSB (16-byte aligned)
+        if (s0 > t) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int sidx = (cb + i) / R;
-            float m = 0.f;
-            if (sidx < t) m = ex2_approx(ct - cg[sidx]);
-            else if (sidx == t) m = rt;
-            v[i] *= m;
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        } else if (s_hi < t) {
+            const float a = ex2_approx(ct - cum2[s_hi]);
+#pragma unroll
+            for (int j = 0; j < NSB; j += 4) {
+                const float4 q = *reinterpret_cast<const float4*>(bneg + s0 + j);
+                const float b[4] = {a * q.x, a * q.y, a * q.z, a * q.w};
+#pragma unroll
+                for (int k = 0; k < 4 * R; ++k) v[j * R + k] *= b[k / R];
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < NSB; j += 4) {
+                const float4 q = *reinterpret_cast<const float4*>(cg + s0 + j);
+                const float e[4] = {ct - q.x, ct - q.y, ct - q.z, ct - q.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int sj = s0 + j + k;
+                    const float x = ex2_approx(e[k]);   // +inf above the diagonal is selected away
+                    const float m = sj < t ? x : (sj == t ? rt : 0.f);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) v[(j + k) * R + r] *= m;
+                }
+            }
         }
     }
 }
@@ -394,7 +435,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                                                          const __grid_constant__ CUtensorMap tm_B,
                                                          const __grid_constant__ CUtensorMap tm_C,
                                                          const __grid_constant__ CUtensorMap tm_dt,
-                                                         const __grid_constant__ CUtensorMap tm_lam, TcArgs args,
+                                                         const __grid_constant__ CUtensorMap tm_lam,
+                                                         const __grid_constant__ CUtensorMap tm_y, TcArgs args,
                                                          const ExtArgs<PM> ext) {
     using K = Cfg<NS, R, Q, FULL>;
     constexpr bool HOOK = PM == kTestHook;
@@ -428,6 +470,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
     auto box_lam = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_BOX + (2 * s + 1) * K::BOX_STRIDE); };
     auto coef = [&](int s) { return reinterpret_cast<float*>(sm + K::OFF_CO + s * K::CO_BYTES); };
     uint8_t* hb = sm + K::OFF_HB;
+    uint8_t* out_tile = sm + K::OFF_OUT;
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -450,6 +493,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
         prefetch_tensormap(&tm_x);
         prefetch_tensormap(&tm_B);
         if (FULL) prefetch_tensormap(&tm_C);
+        if (FULL) prefetch_tensormap(&tm_y);
         prefetch_tensormap(&tm_dt);
         prefetch_tensormap(&tm_lam);
     }
@@ -575,9 +619,15 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
         tc_fence_before();
         group_bar(1);
         const bool odd = tid & 1;
-        // the next C, B and X loads go out from warp 3: warp 0 issues every MMA and is the last to
-        // reach the output
+        // the next C, B and X loads and the output stores go out from warp 3: warp 0 issues every MMA
+        // and is the last to reach the output
         constexpr int kCbxThread = 96;
+        // y of local chunk j from the output tile (every consumer thread wrote and fenced its rows
+        // before the barrier this follows)
+        auto store_y = [&](int j) {
+            tma_store_5d(&tm_y, out_tile, 0, 0, h, (c_begin + j) * Q, b);
+            bulk_commit_group();
+        };
         float ld_sum = 0.f;   // state pass: summed log-decay (thread 0)
         // S = C~ B''^T of the chunk in stage s (thread 0, which issues every MMA).  No commit of its own:
         // the chunk-state commit that follows it on the same thread completes only after it
@@ -619,6 +669,7 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
             tc_fence_before();
             group_bar(1);
             if (*fail_c) break;
+            if (FULL && tid == kCbxThread && i > 0) store_y(i - 1);
             M3_TRACE_C(i, 1);
             // output gate: this thread's z values of the chunk, loaded now so that their latency
             // hides behind the MMAs and the mask (zero past the end of the sequence)
@@ -719,6 +770,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                     }
                     fence_proxy_async_smem();
                 }
+                // the previous chunk's output store has read the output tile: it may be rewritten
+                if (tid == kCbxThread && i > 0) bulk_wait_read_all();
                 tc_fence_before();
                 group_bar(1);
                 M3_TRACE_C(i, 4);
@@ -752,10 +805,10 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                 if (tid == kCbxThread && i + 2 < nl && !*fail_c) {
                     load_cbx(i + 2, s);
                 }
+                // into the output tile (row (t, r) = t R + r, as x's tile; rows past the sequence's end
+                // are not stored)
                 if constexpr (K::M64) {
-                    const int row = warp * 16 + (lane & 15), half = lane >> 4, t = row / R, r = row % R;
-                    const int tok = c * Q + t;
-                    __nv_bfloat16* yrow = args.y + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P + 32 * half;
+                    const int row = warp * 16 + (lane & 15), half = lane >> 4;
                     const float2 e2 = make_float2(ecum_t, ecum_t);
                     float yv[32], iv[32];
                     tmem_ld16x2x2_sync(tlane + K::T_Y, tlane + K::T_YI, yv, iv);
@@ -770,16 +823,13 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                         }
                         pk[q] = pack_bf16(o.x, o.y);
                     }
-                    if (tok < T) {
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            *reinterpret_cast<uint4*>(yrow + 8 * q4) =
-                                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-                    }
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        *reinterpret_cast<uint4*>(out_tile + sw128_offset(row, (32 * half + 8 * q4) * 2)) =
+                            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                    fence_proxy_async_smem();
                 } else if (warp * 32 < QR) {
-                    const int row = tid, t = row / R, r = row % R;
-                    const int tok = c * Q + t;
-                    __nv_bfloat16* yrow = args.y + ((((int64_t)b * T + tok) * args.H + h) * R + r) * P;
+                    const int row = tid;
                     const float2 e2 = make_float2(ecum_t, ecum_t);
 #pragma unroll
                     for (int cc = 0; cc < P; cc += 32) {
@@ -796,13 +846,12 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                             }
                             pk[q] = pack_bf16(o.x, o.y);
                         }
-                        if (tok < T) {
 #pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4)
-                                *reinterpret_cast<uint4*>(yrow + cc + 8 * q4) =
-                                    make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-                        }
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            *reinterpret_cast<uint4*>(out_tile + sw128_offset(row, (cc + 8 * q4) * 2)) =
+                                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
                     }
+                    fence_proxy_async_smem();
                 }
                 M3_TRACE_C(i, 7);
             } else {
@@ -829,6 +878,13 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
             // after its rot_done wait, orders the state step's writes before its MMAs.)
             mbar_arrive(&ctl->coef_free[s]);
             M3_TRACE_C(i, 15);
+        }
+        if constexpr (FULL) {   // the last chunk's outputs (the loop ends, or breaks, uniformly)
+            group_bar(1);
+            if (tid == kCbxThread) {
+                if (!*fail_c && nl > 0) store_y(nl - 1);
+                bulk_wait_all();   // the output tile stays until the stores have read it
+            }
         }
         // the carry after the segment's last chunk (no decay after it), rotated from the segment's frame
         // to the physical frame by the segment's phase Theta (the last chunk's phase, mod 2 pi)
@@ -1305,6 +1361,15 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
     const cuuint64_t P = d.headdim;
     Maps mf;
     if (!make_maps<R>(mf, d, Q, x, B, C, dt, lambda)) return cudaErrorInvalidValue;
+    CUtensorMap my;   // y as x: tiles of Q tokens x R ranks x 64 channels, 128-byte swizzle
+    {
+        const cuuint64_t Bt = d.batch, T = d.seqlen, H = d.nheads;
+        cuuint64_t dims[5] = {P, (cuuint64_t)R, H, T, Bt};
+        cuuint64_t str[4] = {P * 2, R * P * 2, H * R * P * 2, T * H * R * P * 2};
+        cuuint32_t box[5] = {64, (cuuint32_t)R, 1, (cuuint32_t)Q, 1};
+        if (!make_map(&my, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, y, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
     const SegPlan pl = seg_plan<NS, R, Q>(d);
     const SegWs ws = seg_ws<NS, R, Q>(d);
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
@@ -1348,7 +1413,8 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
         auto k1 = scan_tc_kernel<NS, R, QS, false, PM>;
         e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, KS::SMEM);
         if (e != cudaSuccess) return e;
-        k1<<<(unsigned)(seqs * a1.nseg), KS::kThreads, KS::SMEM, stream>>>(ms.x, ms.B, ms.C, ms.dt, ms.lam, a1, ext);
+        k1<<<(unsigned)(seqs * a1.nseg), KS::kThreads, KS::SMEM, stream>>>(ms.x, ms.B, ms.C, ms.dt, ms.lam, ms.x, a1,
+                                                                           ext);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // segment carries -> the state entering each segment (in place), and into the last one
         e = launch_state_passing(segU, segLD, segTH, nullptr, last, 1, seqs, pl.S - 1, NS, (int64_t)P, stream);
@@ -1360,7 +1426,7 @@ cudaError_t launch_cfg(const ScanDims& d, const void* x, const void* B, const vo
     auto kern = scan_tc_kernel<NS, R, Q, true, PM>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(seqs * pl.S), K::kThreads, K::SMEM, stream>>>(mf.x, mf.B, mf.C, mf.dt, mf.lam, args, ext);
+    kern<<<(unsigned)(seqs * pl.S), K::kThreads, K::SMEM, stream>>>(mf.x, mf.B, mf.C, mf.dt, mf.lam, my, args, ext);
     return cudaGetLastError();
 }
 
