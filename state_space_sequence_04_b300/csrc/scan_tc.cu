@@ -351,12 +351,13 @@ __device__ __forceinline__ void load8(const float* p, float fill, float (&o)[8])
 // factorised factor 2^(cum2_t - cum2_e) 2^(cum2_e - cum2_s - g_s), e = the
 // block's last token (the first factor <= 1, the second, b_s, <= 2^100); the
 // diagonal block uses 2^(cum2_t - (cum2_s + g_s)) directly (cg = cum2 + g) and
-// rho_t 2^-g_t on the diagonal; blocks above are zero.
-// With R >= 2 a block holds 16 / R tokens, each on R columns: their factors come in
-// as 16-byte loads, one exponential per token, and the diagonal block selects
-// instead of branching per column (the lanes of a warp hold different rows t).
-// Measured with R = 1 the per-column form below is faster (SISO 64.8 against
-// 62.9 Mtok/s); with R = 4 the per-token form (long-context MIMO 15.3 against 15.1).
+// rho_t 2^-g_t on the diagonal; blocks above are zero.  The per-token factors
+// come in as 16-byte loads.  With R >= 2 a block holds 16 / R tokens, each on R
+// columns: one exponential per token, and the diagonal block selects instead of
+// branching per column (the lanes of a warp hold different rows t).  With R = 1
+// the diagonal block's exponentials stay predicated per column: measured, the
+// select form is slower there (SISO 62.9 against 64.8 Mtok/s) and faster with
+// R = 4 (long-context MIMO 15.3 against 15.1).
 template <int R>
 __device__ __forceinline__ void mask_block(float* v, int cb, int t, float ct, float rt, const float* cum2,
                                            const float* bneg, const float* cg) {
@@ -369,20 +370,28 @@ __device__ __forceinline__ void mask_block(float* v, int cb, int t, float ct, fl
             const float a = ex2_approx(ct - cum2[s_hi]);
             const float2 a2 = make_float2(a, a);
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-                const float2 bb = make_float2(bneg[cb + i], bneg[cb + i + 1]);
-                const float2 r2 = __fmul2_rn(make_float2(v[i], v[i + 1]), __fmul2_rn(a2, bb));
-                v[i] = r2.x;
-                v[i + 1] = r2.y;
+            for (int i = 0; i < 16; i += 4) {
+                const float4 q = *reinterpret_cast<const float4*>(bneg + cb + i);
+                const float2 r0 = __fmul2_rn(make_float2(v[i], v[i + 1]), __fmul2_rn(a2, make_float2(q.x, q.y)));
+                const float2 r1 = __fmul2_rn(make_float2(v[i + 2], v[i + 3]), __fmul2_rn(a2, make_float2(q.z, q.w)));
+                v[i] = r0.x;
+                v[i + 1] = r0.y;
+                v[i + 2] = r1.x;
+                v[i + 3] = r1.y;
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int sidx = cb + i;
-                float m = 0.f;
-                if (sidx < t) m = ex2_approx(ct - cg[sidx]);
-                else if (sidx == t) m = rt;
-                v[i] *= m;
+            for (int i = 0; i < 16; i += 4) {
+                const float4 q = *reinterpret_cast<const float4*>(cg + cb + i);
+                const float g4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int sidx = cb + i + k;
+                    float m = 0.f;
+                    if (sidx < t) m = ex2_approx(ct - g4[k]);
+                    else if (sidx == t) m = rt;
+                    v[i + k] *= m;
+                }
             }
         }
     } else {
