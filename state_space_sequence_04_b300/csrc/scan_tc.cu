@@ -555,59 +555,74 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
         if (FULL && seg > 0)
             hin = seg < args.S - 1 ? args.h_in + ((int64_t)bh * (args.S - 1) + seg) * NS * P
                                    : args.h_in_last + (int64_t)bh * NS * P;
+        // Carry rows and columns of a thread.  The chunk-state MMA runs at M = NS: with NS = 128 thread =
+        // row n, all P columns (lane n); with NS = 64 row n sits in lane 32 (n / 16) + n % 16 (lanes 0-15
+        // of each warp's quadrant) and two threads share it, 32 columns each.  Every consumer thread
+        // takes part either way.
+        constexpr bool H64 = NS == 64;
+        static_assert(NS == 64 || NS == 128, "carry layouts for NS = 64 and 128");
+        const int hrow = H64 ? warp * 16 + (lane & 15) : tid;
+        const int hc0 = H64 ? 32 * (lane >> 4) : 0;
+        constexpr int HCOLS = H64 ? 32 : P;
+        auto h_ld = [&](int cc, float (&v)[32]) {
+            if constexpr (H64) tmem_ld16x2_sync(tlane + K::T_H, v);
+            else tmem_ld32_sync(tlane + K::T_H + cc, v);
+        };
+        auto h_st = [&](int cc, const float (&v)[32]) {
+            if constexpr (H64) tmem_st16x2(tlane + K::T_H, v);
+            else tmem_st32(tlane + K::T_H + cc, v);
+        };
         // the carry entering the segment: H_in, or zero (its bf16 copy and the first chunk's decay come
         // from a state step, below)
-        if (tid < NS || hin == nullptr) {
+        {
 #pragma unroll
-            for (int cc = 0; cc < P; cc += 32) {
+            for (int cc = 0; cc < HCOLS; cc += 32) {
                 float v[32];
-                if (hin != nullptr && tid < NS) {
+                if (hin != nullptr) {
 #pragma unroll
                     for (int i4 = 0; i4 < 32; i4 += 4) {
-                        const float4 q = *reinterpret_cast<const float4*>(hin + (int64_t)tid * P + cc + i4);
+                        const float4 q = *reinterpret_cast<const float4*>(hin + (int64_t)hrow * P + hc0 + cc + i4);
                         v[i4] = q.x; v[i4 + 1] = q.y; v[i4 + 2] = q.z; v[i4 + 3] = q.w;
                     }
                 } else {
 #pragma unroll
                     for (int i4 = 0; i4 < 32; ++i4) v[i4] = 0.f;
                 }
-                tmem_st32(tlane + K::T_H + cc, v);
+                h_st(cc, v);
             }
             tmem_st_wait();
         }
         // ---- the state step: Hb <- bf16(H) (read by the next inter readout Yi), H <- e H with e the decay
-        //      of the chunk about to run (thread = state row n; warp-uniform, the TMEM loads are
-        //      warp-collective).  The carry lives in the segment's rotating frame (B and C are rotated by
-        //      the phase since the segment start), where the transition is the scalar decay alone
-        //      (Propositions 3-4).
+        //      of the chunk about to run (the carry rows and columns of each thread, above; the TMEM
+        //      loads are warp-collective).  The carry lives in the segment's rotating frame (B and C are
+        //      rotated by the phase since the segment start), where the transition is the scalar decay
+        //      alone (Propositions 3-4).
         auto state_step = [&](float e) {
-            if (tid < NS) {
-                const float2 e2 = make_float2(e, e);
+            const float2 e2 = make_float2(e, e);
 #pragma unroll
-                for (int cc = 0; cc < P; cc += 32) {
-                    float hv[32];
-                    tmem_ld32_sync(tlane + K::T_H + cc, hv);
-                    if (FULL) {
+            for (int cc = 0; cc < HCOLS; cc += 32) {
+                float hv[32];
+                h_ld(cc, hv);
+                if (FULL) {
 #pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) {
-                            const uint4 pk = make_uint4(pack_bf16(hv[q8 * 8 + 0], hv[q8 * 8 + 1]),
-                                                        pack_bf16(hv[q8 * 8 + 2], hv[q8 * 8 + 3]),
-                                                        pack_bf16(hv[q8 * 8 + 4], hv[q8 * 8 + 5]),
-                                                        pack_bf16(hv[q8 * 8 + 6], hv[q8 * 8 + 7]));
-                            *reinterpret_cast<uint4*>(hb + sw128_offset(tid, (cc + q8 * 8) * 2)) = pk;
-                        }
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        const uint4 pk = make_uint4(pack_bf16(hv[q8 * 8 + 0], hv[q8 * 8 + 1]),
+                                                    pack_bf16(hv[q8 * 8 + 2], hv[q8 * 8 + 3]),
+                                                    pack_bf16(hv[q8 * 8 + 4], hv[q8 * 8 + 5]),
+                                                    pack_bf16(hv[q8 * 8 + 6], hv[q8 * 8 + 7]));
+                        *reinterpret_cast<uint4*>(hb + sw128_offset(hrow, (hc0 + cc + q8 * 8) * 2)) = pk;
                     }
-#pragma unroll
-                    for (int i2 = 0; i2 < 32; i2 += 2) {
-                        const float2 sc = __fmul2_rn(e2, make_float2(hv[i2], hv[i2 + 1]));
-                        hv[i2] = sc.x;
-                        hv[i2 + 1] = sc.y;
-                    }
-                    tmem_st32(tlane + K::T_H + cc, hv);
                 }
-                tmem_st_wait();
-                if (FULL) fence_proxy_async_smem();
+#pragma unroll
+                for (int i2 = 0; i2 < 32; i2 += 2) {
+                    const float2 sc = __fmul2_rn(e2, make_float2(hv[i2], hv[i2 + 1]));
+                    hv[i2] = sc.x;
+                    hv[i2 + 1] = sc.y;
+                }
+                h_st(cc, hv);
             }
+            tmem_st_wait();
+            if (FULL) fence_proxy_async_smem();
         };
         // Where it runs.  With R >= 2, at the top of each chunk once rot_done is in (which implies the
         // chunk's coefficient block), so the consumer -- the critical path of these configurations --
@@ -627,7 +642,6 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
         }
         tc_fence_before();
         group_bar(1);
-        const bool odd = tid & 1;
         // the next C, B and X loads and the output stores go out from warp 3: warp 0 issues every MMA
         // and is the last to reach the output
         constexpr int kCbxThread = 96;
@@ -705,9 +719,8 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                 // descriptors of the operand bases; a byte offset o moves the start address field by o >> 4
                 const uint64_t dBt = smem_desc(smem_u32(tile_b(s)), QR * 128, 1024, kSwizzle128B);
                 const uint64_t dX = smem_desc(smem_u32(tile_x(s)), 16, 1024, kSwizzle128B);
-                constexpr uint32_t id_u = idesc_bf16_f32(128, P, true, true);
-                // A is MN-major over n (NS rows; panels QR*128 bytes apart); with NS = 64 the
-                // second panel reads the next QR*128 bytes and its results are unused
+                constexpr uint32_t id_u = idesc_bf16_f32(NS, P, true, true);
+                // A is MN-major over n (M = NS rows; panels QR*128 bytes apart)
 #pragma unroll
                 for (int kk = 0; kk < QR / 16; ++kk)
                     mma_bf16_ss(tmem + K::T_H, dBt + kk * (2048 >> 4), dX + kk * (2048 >> 4), id_u, 1);
@@ -909,18 +922,19 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                 if (tid < NP2) args.seg_th[((int64_t)bh * (args.S - 1) + seg) * NP2 + tid] = co_last[K::CO_THETA + tid];
             }
         }
-        if (!*fail_c && !*fail_r && dst != nullptr && tid < NS) {
+        if (!*fail_c && !*fail_r && dst != nullptr) {
             tc_fence_after();
             float sn, cs;
-            sincosf(co_last[K::CO_THETA + (tid >> 1)], &sn, &cs);
-            // even row 2j: cos*v_2j - sin*v_2j+1 ; odd row 2j+1: sin*v_2j + cos*v_2j+1
+            sincosf(co_last[K::CO_THETA + (hrow >> 1)], &sn, &cs);
+            // even row 2j: cos*v_2j - sin*v_2j+1 ; odd row 2j+1: sin*v_2j + cos*v_2j+1 (row 2j+1 is in the
+            // next lane, the same columns, with either carry layout)
             const float2 c2 = make_float2(cs, cs);
-            const float2 s2 = odd ? make_float2(sn, sn) : make_float2(-sn, -sn);
-            float* fs = dst + (int64_t)tid * P;
+            const float2 s2 = (hrow & 1) ? make_float2(sn, sn) : make_float2(-sn, -sn);
+            float* fs = dst + (int64_t)hrow * P + hc0;
 #pragma unroll
-            for (int cc = 0; cc < P; cc += 32) {
+            for (int cc = 0; cc < HCOLS; cc += 32) {
                 float v[32];
-                tmem_ld32_sync(tlane + K::T_H + cc, v);
+                h_ld(cc, v);
 #pragma unroll
                 for (int i2 = 0; i2 < 32; i2 += 2) {
                     const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[i2], 1),
