@@ -33,9 +33,10 @@
 // after the last chunk it is the final state h_{T-1}.
 //
 // Warp roles (256 threads): warps 0-3 "consumer" (mask, state, output; thread
-// 0 issues every MMA and the C/B and X loads), warps 4-7 "rotate" (coefficients,
-// angles, rotation, the dt/lambda loads), which run one chunk ahead of the
-// consumer on the other shared-memory stage.
+// 0 issues every MMA, thread 96 the C, B and X loads and the TMA store of each
+// chunk's output tile), warps 4-7 "rotate" (coefficients, angles, rotation, the
+// dt/lambda loads), which run one chunk ahead of the consumer on the other
+// shared-memory stage.
 // Every wait is bounded: on timeout the kernel records M3_ERR_TIMEOUT in the
 // status word, drains its copies and MMAs and exits.
 //
@@ -53,9 +54,9 @@
 // of those accumulators sits in TMEM lane 32 (r / 16) + r % 16, and every
 // consumer thread takes half a row (16-lane loads, two column halves), so all
 // four consumer warps share the mask and the output.  With QR = 128 they run
-// with M = 128 (row r in lane r).  The chunk-state MMA always has M = 128
-// (state rows n); with N = 64 its rows 64..127 read the next QR*128 bytes of
-// shared memory (X, inside this CTA's allocation) and are never read.
+// with M = 128 (row r in lane r).  The chunk-state MMA has M = N (state rows
+// n): with N = 64 the carry takes the M = 64 layout too, its rows spread over
+// the four consumer warps' lane quadrants.
 #include <cuda.h>
 
 #include "m3_common.cuh"
@@ -113,8 +114,7 @@ struct Cfg {
     static constexpr int BC_BYTES = NPAN * QR * 128;
     static constexpr int SL_BYTES = QR * QR * 2;
     static_assert(!FULL || SL_BYTES <= BC_BYTES, "the masked scores are written over the chunk's B tile");
-    // one stage: C | B | X, or B | X in the state pass (B is followed by X either way: with NS = 64
-    // the carry MMA's second 64-row half reads X's bytes and its results go unused)
+    // one stage: C | B | X, or B | X in the state pass
     static constexpr int STG_B = FULL ? BC_BYTES : 0, STG_X = STG_B + BC_BYTES;
     static constexpr int STG_TILE = STG_X + X_BYTES;
     static constexpr int BOX_BYTES = 16 * (Q + 1);                // dt / lambda box {4 heads, Q+1 tokens}

@@ -169,11 +169,11 @@ def run(wname: str, entry: str = "plain"):
     # chunks whose scores went out early: thread 0 issued only H+= (and Yi) after the barrier
     hplus = [at(c, i, 12) - at(c, i, 1) for c, i in use if at(c, i - 1, 10) == 1 and at(c, i, 12)]
     yb = [at(c, i, 11) - at(c, i, 4) for c, i in use if at(c, i, 11)]
-    f_h = 2.0 * 128 * P * QR                            # executed: M = 128 state rows, N = P, K = QR
+    f_h = 2.0 * N * P * QR                              # executed: M = N state rows, N = P, K = QR
     f_y = 2.0 * MM * P * QR                             # executed: M = MM rows, N = P, K = QR
     out["gemm_phase"] = {
         "peak_bf16_tflops": pk, "peak_source": src, "sm_flop_per_cycle": per_cycle,
-        "chunk_state": {"shape_MxNxK": [128, P, QR], "cycles": statistics.median(hplus) if hplus else None,
+        "chunk_state": {"shape_MxNxK": [N, P, QR], "cycles": statistics.median(hplus) if hplus else None,
                         "frac_of_sm_peak": f_h / statistics.median(hplus) / per_cycle if hplus else None},
         "output_SLX": {"shape_MxNxK": [MM, P, QR], "cycles": statistics.median(yb) if yb else None,
                        "frac_of_sm_peak": f_y / statistics.median(yb) / per_cycle if yb else None},
