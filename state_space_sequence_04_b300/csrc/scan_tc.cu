@@ -597,29 +597,33 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
         //      loads are warp-collective).  The carry lives in the segment's rotating frame (B and C are
         //      rotated by the phase since the segment start), where the transition is the scalar decay
         //      alone (Propositions 3-4).
-        auto state_step = [&](float e) {
+        auto hb_write = [&](int cc, const float (&hv)[32]) {   // Hb <- bf16(H), 32 columns
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+                const uint4 pk = make_uint4(pack_bf16(hv[q8 * 8 + 0], hv[q8 * 8 + 1]),
+                                            pack_bf16(hv[q8 * 8 + 2], hv[q8 * 8 + 3]),
+                                            pack_bf16(hv[q8 * 8 + 4], hv[q8 * 8 + 5]),
+                                            pack_bf16(hv[q8 * 8 + 6], hv[q8 * 8 + 7]));
+                *reinterpret_cast<uint4*>(hb + sw128_offset(hrow, (hc0 + cc + q8 * 8) * 2)) = pk;
+            }
+        };
+        auto h_scale_st = [&](int cc, float (&hv)[32], float e) {   // H <- e H, 32 columns
             const float2 e2 = make_float2(e, e);
+#pragma unroll
+            for (int i2 = 0; i2 < 32; i2 += 2) {
+                const float2 sc = __fmul2_rn(e2, make_float2(hv[i2], hv[i2 + 1]));
+                hv[i2] = sc.x;
+                hv[i2 + 1] = sc.y;
+            }
+            h_st(cc, hv);
+        };
+        auto state_step = [&](float e) {
 #pragma unroll
             for (int cc = 0; cc < HCOLS; cc += 32) {
                 float hv[32];
                 h_ld(cc, hv);
-                if (FULL) {
-#pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        const uint4 pk = make_uint4(pack_bf16(hv[q8 * 8 + 0], hv[q8 * 8 + 1]),
-                                                    pack_bf16(hv[q8 * 8 + 2], hv[q8 * 8 + 3]),
-                                                    pack_bf16(hv[q8 * 8 + 4], hv[q8 * 8 + 5]),
-                                                    pack_bf16(hv[q8 * 8 + 6], hv[q8 * 8 + 7]));
-                        *reinterpret_cast<uint4*>(hb + sw128_offset(hrow, (hc0 + cc + q8 * 8) * 2)) = pk;
-                    }
-                }
-#pragma unroll
-                for (int i2 = 0; i2 < 32; i2 += 2) {
-                    const float2 sc = __fmul2_rn(e2, make_float2(hv[i2], hv[i2 + 1]));
-                    hv[i2] = sc.x;
-                    hv[i2 + 1] = sc.y;
-                }
-                h_st(cc, hv);
+                if (FULL) hb_write(cc, hv);
+                h_scale_st(cc, hv, e);
             }
             tmem_st_wait();
             if (FULL) fence_proxy_async_smem();
@@ -885,6 +889,15 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
             }
 
             if constexpr (!STEP_AT_TOP) {   // into the next chunk: its decay (none after the last)
+                // Hb = bf16(H) needs no decay: it goes out before the wait for the next chunk's
+                // coefficients, and the last 32 columns stay in registers for the scaling
+                tc_fence_after();
+                float hv[32];
+#pragma unroll
+                for (int cc = 0; cc < HCOLS; cc += 32) {
+                    h_ld(cc, hv);
+                    if (FULL) hb_write(cc, hv);
+                }
                 float e_next = 1.f;
                 if (i + 1 < nl) {
                     const int s1 = (i + 1) & 1;
@@ -892,8 +905,15 @@ __global__ void __launch_bounds__(256, (Cfg<NS, R, Q, FULL>::MIN_BLOCKS)) scan_t
                     e_next = coef(s1)[K::CO_EEND];
                 }
                 M3_TRACE_C(i, 14);
-                tc_fence_after();
-                state_step(e_next);
+                h_scale_st(HCOLS - 32, hv, e_next);
+#pragma unroll
+                for (int cc = 0; cc < HCOLS - 32; cc += 32) {
+                    float hv2[32];
+                    h_ld(cc, hv2);
+                    h_scale_st(cc, hv2, e_next);
+                }
+                tmem_st_wait();
+                if (FULL) fence_proxy_async_smem();
             }
             // every read of this stage's coefficient block is done (the output took exp(cum_t)
             // in a register): the rotate group may fill it for chunk i+2.  (The next chunk's barrier,
