@@ -41,8 +41,8 @@ KEYS = ("x", "B", "C", "dt", "A", "lam", "omega")
 # (the state step runs at the top of a chunk with R >= 2 (slots 8 -> 9), at the end with R = 1 (14 -> 15))
 CONSUMER = [(0, "top"), (8, "stage ready (rot_done)"), (9, "state step, R >= 2"), (1, "barrier"),
             (2, "H+= and Yi issued"), (3, "S and H+= waited"), (4, "mask + barrier"), (5, "Y issued (+ next S)"),
-            (6, "Y waited"), (7, "output stored"), (14, "next coefficients, R = 1"),
-            (15, "state step, R = 1")]
+            (6, "Y waited"), (7, "output stored"), (14, "R = 1: Hb written, next coefficients waited"),
+            (15, "R = 1: H scaled")]
 ROTATE = ["top", "dt/lambda boxes", "coefficients + angle partial sums", "C/B landed", "rotation (C~, B'')",
           "barrier + next boxes issued", "-", "-", "barrier"]
 
