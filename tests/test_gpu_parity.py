@@ -123,6 +123,7 @@ TC_CASES = [
     (1, 4, 257, 64, 64, 2, 128),      # R = 2, N = 64: sub-chunks of 32 tokens
     (1, 4, 9001, 64, 128, 4, 64),     # segments of 8 sub-chunks (4 state-pass chunks), ragged end
     (1, 4, 5000, 64, 64, 2, 64),      # R = 2: segments of 4 sub-chunks (2 state-pass chunks)
+    (1, 4, 9000, 64, 64, 1, 64),      # N = 64, R = 1: segments of 2 chunks, ragged end
 ]
 
 
